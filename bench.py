@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark: bf16 GEMM TFLOPS at M=N=K=4096 (fp32 accumulate, fp32 C) on GB300,
+as a fraction of the tensor roofline, plus the K sweep, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one C = A·B of the 4096³ workload (A, B row-major bf16, uniform
+[-1, 1) from seed 0). Inputs are resident in HBM when the timed region
+starts; the step's inputs rotate over enough sets that the footprint exceeds
+the 129 MB L2, so no step reads operands another step left in L2. Timing:
+CUDA events on the launching stream around exactly K steps, barrier +
+synchronize on both sides, max over ranks. Prints one JSON line on rank 0.
+
+With --gpus N (under torchrun) every rank runs its own independent problem
+(output tiles need no exchange, so there is no collective on the data path):
+weak scaling, value = total flops of all ranks / max time.
+
+--impl reference times the CPU oracle (the plain fp64 triple loop in
+oracle/) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M = N = K = 4096
+FLOPS = 2.0 * M * N * K
+WORKLOAD = "bf16 GEMM C=A·B, M=N=K=4096, A and B row-major bf16 uniform[-1,1) seed 0, fp32 accumulate, fp32 C"
+SWEEP = [(mn, k) for mn in (512, 4096) for k in (256, 512, 1024, 4096, 8192)]
+L2_BYTES = 129 * 1000 * 1000
+PAGES_REF_TFLOPS = 33.72   # hgemm_bcf_dbf_rw, 4096³ bf16, GPU not stated (context only)
+METRIC = "bf16 GEMM TFLOPS at 4096^3 (fp32 accumulate, fp32 C) and fraction of GB300 dense tensor peak"
+
+
+def base_config():
+    return {"workload": WORKLOAD, "M": M, "N": N, "K": K, "out": "f32"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the K sweep and the extra variants")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_core_loop_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)   # let the sampler's first query land before the region opens
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7], "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 300.0] or rows
+        sms = sorted(r["sm"] for r in loaded)
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def cpu_oracle_sample(target_s=12.0, max_rows=4096):
+    """Times the CPU oracle on whole rows of the 4096³ workload; returns (tflops, rows, seconds, cores)."""
+    import oracle
+    from tensor_core_loop_gb300 import inputs
+    oracle.build()
+    a, b = inputs.bf16_pair(M, N, K, seed=0)
+    ab, bb = inputs.bf16_bits(a), inputs.bf16_bits(b)
+    cores = oracle.num_threads()
+    rows = max(4, cores)
+    t0 = time.perf_counter()
+    oracle.gemm_bf16(ab, bb, rows=(0, rows), with_abs=False)
+    dt = time.perf_counter() - t0
+    more = int(min(max_rows, max(rows, rows * target_s / max(dt, 1e-3))))
+    more = max(rows, (more // cores) * cores if more >= cores else more)
+    t0 = time.perf_counter()
+    oracle.gemm_bf16(ab, bb, rows=(rows, rows + more), with_abs=False)
+    dt = time.perf_counter() - t0
+    return 2.0 * more * N * K / dt / 1e12, more, dt, cores
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    per_step = []
+    rows_used = 0
+    import oracle
+    from tensor_core_loop_gb300 import inputs
+    oracle.build()
+    a, b = inputs.bf16_pair(M, N, K, seed=0)
+    ab, bb = inputs.bf16_bits(a), inputs.bf16_bits(b)
+    cores = oracle.num_threads()
+    rows = max(16, cores)  # one bounded sample of whole C rows per step
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm_bf16(ab, bb, rows=(0, rows), with_abs=False)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            per_step.append(dt)
+            rows_used = rows
+    total = sum(per_step)
+    value = 2.0 * rows_used * N * K * len(per_step) / total / 1e12
+    sample = f"{rows_used} of {M} rows of C per step (all {N} columns, full K={K})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(per_step), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": base_config(),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_rotating(fn, sets, steps, warmup, stream, torch):
+    """Back-to-back launches over rotating input sets; returns ms per step."""
+    for i in range(warmup):
+        fn(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(*sets[i % len(sets)])
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def time_flushed(fn, args_, iters, stream, torch, flush):
+    """Per-launch event timing with an L2 flush (a write larger than L2) before each launch."""
+    times = []
+    for _ in range(iters):
+        flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn(*args_)
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    times.sort()
+    return times[len(times) // 2]
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = measured_peaks()
+
+    # ---- inputs: rotate over sets whose total footprint exceeds L2
+    a_h, b_h = inputs.bf16_pair(M, N, K, seed=0)
+    set_bytes = M * K * 2 + K * N * 2 + M * N * 4
+    nsets = max(2, -(-3 * L2_BYTES // set_bytes))
+    a0, b0 = a_h.to(dev), b_h.to(dev)
+    sets = []
+    for i in range(nsets):
+        ai = a0 if i == 0 else a0.clone()
+        bi = b0 if i == 0 else b0.clone()
+        sets.append((ai, bi, torch.empty((M, N), dtype=torch.float32, device=dev)))
+    L = tcl.lib()
+
+    def step(a, b, c):
+        st = L.gemm_bf16(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, tcl.OUT_F32,
+                         stream.cuda_stream)
+        if st:
+            raise tcl.TclError(st, "gemm_bf16")
+
+    for i in range(max(3, args.warmup)):
+        step(*sets[i % nsets])
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(*sets[i % nsets])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(end)
+    clocks = sampler.stop() if rank == 0 else None
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    st, code = tcl.last_device_error()
+    if st:
+        raise RuntimeError(f"device status {st} (code {code}) after the timed region")
+    ms_step = ms_total / args.steps
+    value = FLOPS * world * args.steps / (ms_total * 1e-3) / 1e12
+    per_launch_s = ms_step * 1e-3
+    achieved = FLOPS / per_launch_s / 1e12
+
+    extra = {}
+    if rank == 0 and not args.no_sweep:
+        # bf16 output variant of the same workload
+        sets16 = [(s[0], s[1], torch.empty((M, N), dtype=torch.bfloat16, device=dev)) for s in sets]
+
+        def step16(a, b, c):
+            st_ = L.gemm_bf16(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, tcl.OUT_BF16,
+                              stream.cuda_stream)
+            if st_:
+                raise tcl.TclError(st_, "gemm_bf16")
+        ms16 = time_rotating(step16, sets16, 500, 20, stream, torch)
+        extra["bf16_out_tflops"] = FLOPS / (ms16 * 1e-3) / 1e12
+        del sets16
+        # K sweep, each launch timed alone after an L2 flush
+        flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+        sweep = {}
+        for mn, k in SWEEP:
+            ah, bh = inputs.bf16_pair(mn, mn, k, seed=0)
+            a, b = ah.to(dev), bh.to(dev)
+            c = torch.empty((mn, mn), dtype=torch.float32, device=dev)
+
+            def f(a=a, b=b, c=c, mn=mn, k=k):
+                st_ = L.gemm_bf16(mn, mn, k, a.data_ptr(), k, b.data_ptr(), mn, c.data_ptr(), mn, tcl.OUT_F32,
+                                  stream.cuda_stream)
+                if st_:
+                    raise tcl.TclError(st_, "gemm_bf16")
+            for _ in range(5):
+                f()
+            ms = time_flushed(f, (), 30, stream, torch, flush)
+            tf = 2.0 * mn * mn * k / (ms * 1e-3) / 1e12
+            alg_bytes = (mn * k + k * mn) * 2 + mn * mn * 4
+            sweep[f"{mn}x{mn}x{k}"] = {"tflops": round(tf, 1), "us": round(ms * 1e3, 2),
+                                        "alg_gbs": round(alg_bytes / (ms * 1e-3) / 1e9, 1)}
+        extra["k_sweep"] = sweep
+        del flush
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0:
+        a_pin = a_h.pin_memory()
+        b_pin = b_h.pin_memory()
+        c_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        ad = torch.empty_like(a0)
+        bd = torch.empty_like(b0)
+        cd = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+        def e2e_step():
+            ad.copy_(a_pin, non_blocking=True)
+            bd.copy_(b_pin, non_blocking=True)
+            tcl.gemm_into(ad, bd, cd)
+            c_pin.copy_(cd, non_blocking=True)
+        e2e_steps = max(5, min(50, args.steps))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e.record(stream)
+        e.synchronize()
+        ms_e2e = s.elapsed_time(e) / e2e_steps
+        e2e = {"value": FLOPS / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": a_pin.numel() * 2 + b_pin.numel() * 2,
+               "d2h_bytes_per_step": c_pin.numel() * 4, "ms_per_step": ms_e2e}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        tf, rows, secs, cores = cpu_oracle_sample()
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} of {M} rows of C (all {N} columns, full K={K}), {secs:.1f} s"}
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peak = float(peaks["bf16_tflops"])
+    sms = tcl.num_sms()
+    sm_mhz = clocks.get("sm_mhz") if clocks else None
+    line = {
+        "metric": METRIC,
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / world / PAGES_REF_TFLOPS,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {**base_config(),
+                   "l2": f"inputs rotated over {nsets} sets of {set_bytes >> 20} MiB (> 129 MB L2)",
+                   "vs_baseline_ref": "pages' hgemm_bcf_dbf_rw 4096^3 bf16 33.72 TFLOPS, GPU not stated (context)",
+                   "plan": tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K), "sms": sms},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic("gemm_bf16_f32_4096"),
+                     "peak_source": f"{peak_src} bf16_tflops (cuBLAS 8192^3 burst)",
+                     "clock_corrected_peak": (sms * 8192 * sm_mhz * 1e6 / 1e12) if sm_mhz else None,
+                     "frac_clock_corrected": (achieved / (sms * 8192 * sm_mhz * 1e6 / 1e12)) if sm_mhz else None},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "cpu_baseline": cpu,
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * tcl_gemm.h — C ABI of the GB300 (sm_103a) pipelined tensor-core GEMM.
+ *
+ * Operation (every entry point): C = A · B, overwriting C.
+ *   A is M×K, B is K×N, C is M×N, all row-major with leading dimensions
+ *   lda, ldb, ldc counted in elements: A[i*lda + k], B[k*ldb + j],
+ *   C[i*ldc + j]. There is no alpha/beta and no accumulation into C.
+ *   Definition: "4.1 CUDA GEMM 算子性能优化", §1.1 (GEMM 的定义: C = A×B,
+ *   A M×K, B K×N, 2·M·N·K flops) and the one-thread-per-element reference
+ *   kernel of §3.1 (C[i][j] = sum_k A[i][k]·B[k][j], row-major A and B).
+ *   How it is computed: the K-loop is tiled and software-pipelined so that
+ *   the load of the next K-tile overlaps the tensor-core MMA on the current
+ *   one ("流水化 GPU 内核", steps 3-4; "4.1 CUDA GEMM 算子性能优化", §9-§10);
+ *   here with TMA loads into a multi-stage shared-memory ring, tcgen05.mma
+ *   accumulating in fp32 in tensor memory, and a TMA-store epilogue.
+ *
+ * Memory and ownership: A, B and C are device pointers owned by the caller
+ *   (allocated, kept alive until the stream has run the call, and freed by
+ *   the caller). The library keeps a per-device cache of TMA descriptors and,
+ *   for gemm_s8 only, a per-device scratch buffer that it grows on demand
+ *   (cudaMalloc, after a device synchronisation) and frees in tcl_shutdown().
+ *
+ * Streams: every call is asynchronous on `stream` (0 = legacy default
+ *   stream) and returns once the work is enqueued. Calls on one stream run in
+ *   order. The library is not thread-safe: serialise calls from several host
+ *   threads.
+ *
+ * Alignment (the TMA rule: global base addresses 16-byte aligned, row
+ *   strides a multiple of 16 bytes; "cp.async / ldmatrix 消融实验", §1.4 item
+ *   2 states the same 16-byte rule for cp.async):
+ *   gemm_bf16: A, B, C 16-byte aligned; lda, ldb multiples of 8;
+ *              ldc a multiple of 4 (fp32 C) or 8 (bf16 C).
+ *   gemm_tf32: A, B, C 16-byte aligned; lda, ldb, ldc multiples of 4.
+ *   gemm_s8:   A, B, C 16-byte aligned; lda, ldb multiples of 16; ldc of 4.
+ *   M, N, K are otherwise free (>= 1): edge tiles are zero-filled on load and
+ *   clipped on store.
+ *
+ * Errors: each entry point returns a tcl_status. Argument checks happen on
+ *   the host before anything is enqueued; a nonzero status means nothing was
+ *   launched. The library never prints, traps or aborts. Kernel-side waits
+ *   are bounded; a wait that runs out records a code in a per-device status
+ *   word that tcl_last_device_error() reads.
+ */
+#ifndef TCL_GEMM_H
+#define TCL_GEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define TCL_API __attribute__((visibility("default")))
+#else
+#define TCL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TCL_OK = 0,
+    TCL_ERR_NULL = 1,            /* a required pointer is NULL */
+    TCL_ERR_DIMS = 2,            /* M, N or K < 1 */
+    TCL_ERR_LD = 3,              /* lda < K, ldb < N or ldc < N */
+    TCL_ERR_ALIGN = 4,           /* base or leading dimension breaks the alignment rule above */
+    TCL_ERR_K_TOO_LARGE = 5,     /* gemm_s8: K > 131071, the int32 result could overflow */
+    TCL_ERR_LAUNCH = 6,          /* a CUDA call or kernel launch failed */
+    TCL_ERR_DEVICE_TIMEOUT = 7,  /* a bounded in-kernel wait ran out (see tcl_last_device_error) */
+    TCL_ERR_CONFIG = 8,          /* tcl_config_t asks for a variant that is not built */
+    TCL_ERR_NO_MEMORY = 9,       /* scratch allocation failed */
+    TCL_ERR_DEVICE = 10          /* current device is not an sm_103 GPU */
+} tcl_status;
+
+typedef enum { TCL_OUT_F32 = 0, TCL_OUT_BF16 = 1 } tcl_out_t;
+
+/* Optional knobs for the *_ex entry points (ablation, tracing, tests).
+ * Zero-initialise and set only what you need; zero means "automatic". */
+typedef struct {
+    int bn;                        /* N tile: 128 or 256 (0: chosen from M, N and the SM count) */
+    int stages;                    /* shared-memory ring depth (0: the deepest that fits) */
+    int one_cta_per_tile;          /* 0 (default): persistent, one CTA per SM walking the tiles;
+                                      1: one CTA per output tile (no persistence) */
+    int group_m;                   /* raster group height in tiles (0: 8) */
+    int max_ctas;                  /* cap on resident CTAs for the persistent grid (0: all SMs) */
+    unsigned long long timeout_ns; /* bound on every in-kernel wait (0: 1 s) */
+    unsigned long long* trace;     /* device buffer of 4*trace_cap uint64 (clock64 stamps per
+                                      k-block of CTA 0: load issued, data landed, MMAs issued,
+                                      MMAs done), or NULL */
+    int trace_cap;                 /* k-blocks the trace buffer holds */
+} tcl_config_t;
+
+/* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
+ * or bf16 rounded to nearest even (out = TCL_OUT_BF16). */
+TCL_API int gemm_bf16(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc,
+              int out, cudaStream_t stream);
+
+/* fp32 A, B consumed by the tensor cores as TF32; fp32 accumulation; fp32 C. */
+TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+              int ldc, cudaStream_t stream);
+
+/* int8 A, B; exact int32 C (bit-exact integer result for K <= 131071).
+ * The operands are widened exactly to bf16 in library scratch, the tensor
+ * cores accumulate in fp32 in units of at most 512 K values (every partial
+ * sum is an integer below 2^24 in magnitude, hence exact), and each unit is
+ * added into int32 registers. */
+TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
+            int ldc, cudaStream_t stream);
+
+/* Same operations with explicit knobs; cfg may be NULL (= all automatic). */
+TCL_API int gemm_bf16_ex(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C,
+                 int ldc, int out, const tcl_config_t* cfg, cudaStream_t stream);
+TCL_API int gemm_tf32_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+                 int ldc, const tcl_config_t* cfg, cudaStream_t stream);
+TCL_API int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
+               int ldc, const tcl_config_t* cfg, cudaStream_t stream);
+
+/* The launch the automatic path would make for this problem, without
+ * launching: in_kind 0 = bf16, 1 = tf32, 2 = int8. Any output pointer may be
+ * NULL. Returns a tcl_status (argument checks as above, pointers not needed). */
+TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, int* bn,
+             int* stages, int* grid, int* num_tiles, int* smem_bytes);
+
+/* Human-readable text for a tcl_status; never NULL. */
+TCL_API const char* tcl_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns TCL_OK, or TCL_ERR_DEVICE_TIMEOUT if any kernel since the
+ * last read recorded a timed-out wait (*detail, if not NULL, receives the raw
+ * code: 1 producer, 2 MMA waiting for data, 3 MMA waiting for an accumulator,
+ * 4 epilogue), or TCL_ERR_LAUNCH if synchronising failed. */
+TCL_API int tcl_last_device_error(cudaStream_t stream, int* detail);
+
+/* Streaming multiprocessors of the current device (0 on error). */
+TCL_API int tcl_num_sms(void);
+
+/* Frees the int8 scratch buffers of every device (after synchronising each). */
+TCL_API void tcl_shutdown(void);
+
+/* Library version string, e.g. "tcl-gb300 0.1.0 sm_103a". */
+TCL_API const char* tcl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCL_GEMM_H */

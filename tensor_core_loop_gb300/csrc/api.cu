@@ -1,0 +1,499 @@
+// C ABI of the library (declared in include/tcl_gemm.h): argument checks,
+// launch planning, TMA descriptor construction and caching, the int8 scratch,
+// the device status word, and dispatch to the instantiated kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "launch.cuh"
+#include "tcl_gemm.h"
+
+namespace tcl {
+namespace {
+
+// Per-device status word written by kernels whose bounded waits ran out.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
+constexpr int kBM = 128;
+constexpr int kS32UnitK = 512;   // K values per exact fp32 unit: 512·2^14 = 2^23 < 2^24
+
+struct DevState {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    unsigned int* status = nullptr;
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+};
+
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+const VariantInfo kVariants[] = {
+    TCL_GROUP_BF16_F32_BN256(TCL_VARIANT_INFO) TCL_GROUP_BF16_F32_BN128(TCL_VARIANT_INFO)
+        TCL_GROUP_BF16_MISC(TCL_VARIANT_INFO) TCL_GROUP_TF32(TCL_VARIANT_INFO)};
+
+struct MapKey {
+    int dev;
+    const void* ptr;
+    int dtype;
+    uint64_t d0, d1, stride;
+    uint32_t b0, b1;
+    bool operator==(const MapKey& o) const {
+        return dev == o.dev && ptr == o.ptr && dtype == o.dtype && d0 == o.d0 && d1 == o.d1 &&
+               stride == o.stride && b0 == o.b0 && b1 == o.b1;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = 1469598103934665603ull;
+        auto mix = [&h](uint64_t v) {
+            h ^= v;
+            h *= 1099511628211ull;
+        };
+        mix(static_cast<uint64_t>(k.dev));
+        mix(reinterpret_cast<uint64_t>(k.ptr));
+        mix(static_cast<uint64_t>(k.dtype));
+        mix(k.d0);
+        mix(k.d1);
+        mix(k.stride);
+        mix((static_cast<uint64_t>(k.b0) << 32) | k.b1);
+        return static_cast<size_t>(h);
+    }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+int in_bytes(InKind k) { return k == InKind::TF32 ? 4 : 2; }
+int out_bytes(OutKind k) { return k == OutKind::BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side argument checks shared by every entry point; no CUDA call.
+int check_common(int M, int N, int K, const void* A, int lda, const void* B, int ldb, const void* C,
+                 int ldc) {
+    if (!A || !B || !C) return TCL_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1) return TCL_ERR_DIMS;
+    if (lda < K || ldb < N || ldc < N) return TCL_ERR_LD;
+    return TCL_OK;
+}
+
+// Current device: probe capability, SM count and status-word address once.
+int current_device(int* dev_out, DevState** st_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    DevState& d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return TCL_ERR_LAUNCH;
+        }
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+                cudaGetLastError();
+                return TCL_ERR_LAUNCH;
+            }
+            d.status = static_cast<unsigned int*>(p);
+        }
+        d.probed = true;
+    }
+    if (!d.supported) return TCL_ERR_DEVICE;
+    *dev_out = dev;
+    *st_out = &d;
+    return TCL_OK;
+}
+
+int encode_fn() {
+    if (g_encode) return TCL_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return TCL_OK;
+}
+
+// 2-D row-major tensor map: inner extent d0 (contiguous), outer d1, row
+// stride in bytes, box b0 × b1, 128-byte swizzle, zero fill out of bounds.
+int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1,
+               uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMap* out) {
+    const MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride_bytes, b0, b1};
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+        *out = it->second;
+        return TCL_OK;
+    }
+    int st = encode_fn();
+    if (st) return st;
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {d0, d1};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {b0, b1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return TCL_ERR_LAUNCH;
+    if (g_maps.size() > 4096) g_maps.clear();
+    g_maps.emplace(key, m);
+    *out = m;
+    return TCL_OK;
+}
+
+struct Plan {
+    int bn, stages, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
+};
+
+const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages) {
+    for (const auto& v : kVariants)
+        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages) return &v;
+    return nullptr;
+}
+
+int deepest_stages(InKind ik, OutKind ok, int bn) {
+    int best = 0;
+    for (const auto& v : kVariants)
+        if (v.in == ik && v.out == ok && v.bn == bn && v.stages > best) best = v.stages;
+    return best;
+}
+
+// Chooses the tile shape, ring depth and grid. `sms` is the SM count.
+int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cfg, int sms, Plan* pl) {
+    const int bk = 128 / in_bytes(ik);
+    int bn = cfg ? cfg->bn : 0;
+    if (bn == 0) {
+        if (ok == OutKind::S32) {
+            bn = 128;
+        } else {
+            // Wide tiles halve the B traffic per flop; fall back to narrow tiles
+            // only when wide ones would leave SMs idle.
+            const long long tiles256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256);
+            bn = tiles256 >= sms ? 256 : 128;
+        }
+    }
+    if (bn != 128 && bn != 256) return TCL_ERR_CONFIG;
+    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn);
+    const VariantInfo* v = find_variant(ik, ok, bn, stages);
+    if (!v) return TCL_ERR_CONFIG;
+    pl->bn = bn;
+    pl->stages = stages;
+    pl->smem = v->smem_bytes;
+    pl->tiles_m = (M + kBM - 1) / kBM;
+    pl->tiles_n = (N + bn - 1) / bn;
+    const long long tiles = static_cast<long long>(pl->tiles_m) * pl->tiles_n;
+    if (tiles > 0x7FFFFFFFll) return TCL_ERR_DIMS;
+    pl->num_tiles = static_cast<int>(tiles);
+    pl->num_kb = (K + bk - 1) / bk;
+    pl->kb_per_unit = ok == OutKind::S32 ? kS32UnitK / bk : pl->num_kb;
+    pl->group_m = cfg && cfg->group_m > 0 ? cfg->group_m : 8;
+    if (cfg && cfg->one_cta_per_tile) {
+        pl->grid = pl->num_tiles;
+    } else {
+        int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
+        if (cap < 1) cap = 1;
+        pl->grid = pl->num_tiles < cap ? pl->num_tiles : cap;
+    }
+    return TCL_OK;
+}
+
+// Builds tensor maps and launches one GEMM over device operands.
+int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long long lda, const void* B,
+             long long ldb, void* C, long long ldc, const tcl_config_t* cfg, int dev, DevState* ds,
+             cudaStream_t stream) {
+    Plan pl;
+    int st = make_plan(ik, ok, M, N, K, cfg, ds->sms, &pl);
+    if (st) return st;
+    const int ies = in_bytes(ik), oes = out_bytes(ok);
+    const int bk = 128 / ies;
+    const CUtensorMapDataType in_t =
+        ik == InKind::TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType out_t = ok == OutKind::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                      : ok == OutKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_INT32;
+    LaunchArgs a;
+    a.in = ik;
+    a.out = ok;
+    a.bn = pl.bn;
+    a.stages = pl.stages;
+    a.grid = pl.grid;
+    a.stream = stream;
+    if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
+    if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB))) return st;
+    if ((st = tensor_map(dev, C, out_t, N, M, ldc * oes, 128 / oes, 32, &a.tmC))) return st;
+    GemmParams& p = a.p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.num_tiles;
+    p.num_kb = pl.num_kb;
+    p.kb_per_unit = pl.kb_per_unit;
+    p.group_m = pl.group_m;
+    p.timeout_ns = cfg && cfg->timeout_ns ? cfg->timeout_ns : kDefaultTimeoutNs;
+    p.status = ds->status;
+    p.trace = cfg ? cfg->trace : nullptr;
+    p.trace_cap = cfg && cfg->trace ? cfg->trace_cap : 0;
+
+    bool found = false;
+    cudaError_t err = cudaSuccess;
+    if (ik == InKind::TF32) {
+        err = launch_group_tf32(a, &found);
+    } else {
+        err = launch_group_bf16_f32_bn256(a, &found);
+        if (!found) err = launch_group_bf16_f32_bn128(a, &found);
+        if (!found) err = launch_group_bf16_misc(a, &found);
+    }
+    if (!found) return TCL_ERR_CONFIG;
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return TCL_OK;
+}
+
+int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C,
+                   int ldc, int out, const tcl_config_t* cfg, cudaStream_t stream) {
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st) return st;
+    if (out != TCL_OUT_F32 && out != TCL_OUT_BF16) return TCL_ERR_CONFIG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 8 || ldb % 8 ||
+        ldc % (out == TCL_OUT_BF16 ? 8 : 4))
+        return TCL_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    if ((st = current_device(&dev, &ds))) return st;
+    return run_gemm(InKind::BF16, out == TCL_OUT_BF16 ? OutKind::BF16 : OutKind::F32, M, N, K, A, lda,
+                    B, ldb, C, ldc, cfg, dev, ds, stream);
+}
+
+int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+                   int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st) return st;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 4 || ldb % 4 || ldc % 4)
+        return TCL_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    if ((st = current_device(&dev, &ds))) return st;
+    return run_gemm(InKind::TF32, OutKind::F32, M, N, K, A, lda, B, ldb, C, ldc, cfg, dev, ds, stream);
+}
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
+                 int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st) return st;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 16 || ldb % 16 || ldc % 4)
+        return TCL_ERR_ALIGN;
+    if (K > 131071) return TCL_ERR_K_TOO_LARGE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    if ((st = current_device(&dev, &ds))) return st;
+    // Packed bf16 copies of A (M × lda2) and B (K × ldb2), each 256-byte aligned.
+    const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
+    const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
+    const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
+    const size_t need = static_cast<size_t>(a_bytes + b_bytes);
+    if (ds->scratch_bytes < need) {
+        if (ds->scratch) {
+            if (cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                return TCL_ERR_LAUNCH;
+            }
+            cudaFree(ds->scratch);
+            ds->scratch = nullptr;
+            ds->scratch_bytes = 0;
+        }
+        void* p = nullptr;
+        if (cudaMalloc(&p, need) != cudaSuccess) {
+            cudaGetLastError();
+            return TCL_ERR_NO_MEMORY;
+        }
+        ds->scratch = p;
+        ds->scratch_bytes = need;
+    }
+    uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
+    uint8_t* b2 = a2 + a_bytes;
+    if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, ds->sms, stream) != cudaSuccess ||
+        launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, ds->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return run_gemm(InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, C, ldc, cfg, dev, ds,
+                    stream);
+}
+
+}  // namespace
+}  // namespace tcl
+
+using namespace tcl;
+
+extern "C" {
+
+int gemm_bf16(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc,
+              int out, cudaStream_t stream) {
+    return gemm_bf16_impl(M, N, K, A, lda, B, ldb, C, ldc, out, nullptr, stream);
+}
+
+int gemm_bf16_ex(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C,
+                 int ldc, int out, const tcl_config_t* cfg, cudaStream_t stream) {
+    return gemm_bf16_impl(M, N, K, A, lda, B, ldb, C, ldc, out, cfg, stream);
+}
+
+int gemm_tf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+              int ldc, cudaStream_t stream) {
+    return gemm_tf32_impl(M, N, K, A, lda, B, ldb, C, ldc, nullptr, stream);
+}
+
+int gemm_tf32_ex(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+                 int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
+    return gemm_tf32_impl(M, N, K, A, lda, B, ldb, C, ldc, cfg, stream);
+}
+
+int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
+            int ldc, cudaStream_t stream) {
+    return gemm_s8_impl(M, N, K, A, lda, B, ldb, C, ldc, nullptr, stream);
+}
+
+int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
+               int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
+    return gemm_s8_impl(M, N, K, A, lda, B, ldb, C, ldc, cfg, stream);
+}
+
+int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, int* bn, int* stages,
+             int* grid, int* num_tiles, int* smem_bytes) {
+    if (M < 1 || N < 1 || K < 1) return TCL_ERR_DIMS;
+    InKind ik;
+    OutKind ok;
+    if (in_kind == 0) {
+        ik = InKind::BF16;
+        if (out == TCL_OUT_F32) ok = OutKind::F32;
+        else if (out == TCL_OUT_BF16) ok = OutKind::BF16;
+        else return TCL_ERR_CONFIG;
+    } else if (in_kind == 1) {
+        ik = InKind::TF32;
+        ok = OutKind::F32;
+    } else if (in_kind == 2) {
+        ik = InKind::BF16;
+        ok = OutKind::S32;
+    } else {
+        return TCL_ERR_CONFIG;
+    }
+    int sms = 0;
+    if (cfg && cfg->max_ctas > 0) {
+        sms = cfg->max_ctas;   // lets the planner run without a device
+    } else {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int dev;
+        DevState* ds;
+        int st = current_device(&dev, &ds);
+        if (st) return st;
+        sms = ds->sms;
+    }
+    Plan pl;
+    int st = make_plan(ik, ok, M, N, K, cfg, sms, &pl);
+    if (st) return st;
+    if (bn) *bn = pl.bn;
+    if (stages) *stages = pl.stages;
+    if (grid) *grid = pl.grid;
+    if (num_tiles) *num_tiles = pl.num_tiles;
+    if (smem_bytes) *smem_bytes = pl.smem;
+    return TCL_OK;
+}
+
+const char* tcl_status_string(int status) {
+    switch (status) {
+        case TCL_OK: return "ok";
+        case TCL_ERR_NULL: return "null pointer argument";
+        case TCL_ERR_DIMS: return "M, N and K must be at least 1";
+        case TCL_ERR_LD: return "leading dimension smaller than the row width";
+        case TCL_ERR_ALIGN: return "base address or leading dimension not 16-byte aligned";
+        case TCL_ERR_K_TOO_LARGE: return "K too large for an exact int32 result";
+        case TCL_ERR_LAUNCH: return "CUDA call or kernel launch failed";
+        case TCL_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait timed out";
+        case TCL_ERR_CONFIG: return "requested configuration is not built";
+        case TCL_ERR_NO_MEMORY: return "scratch allocation failed";
+        case TCL_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        default: return "unknown status";
+    }
+}
+
+int tcl_last_device_error(cudaStream_t stream, int* detail) {
+    if (detail) *detail = 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    int st = current_device(&dev, &ds);
+    if (st) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    unsigned int word = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    if (detail) *detail = static_cast<int>(word);
+    return word ? TCL_ERR_DEVICE_TIMEOUT : TCL_OK;
+}
+
+int tcl_num_sms(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    if (current_device(&dev, &ds)) return 0;
+    return ds->sms;
+}
+
+void tcl_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_dev[d].scratch) {
+            if (cudaSetDevice(d) == cudaSuccess) {
+                cudaDeviceSynchronize();
+                cudaFree(g_dev[d].scratch);
+            }
+            g_dev[d].scratch = nullptr;
+            g_dev[d].scratch_bytes = 0;
+        }
+    }
+    cudaSetDevice(prev);
+    cudaGetLastError();
+    g_maps.clear();
+}
+
+const char* tcl_version(void) { return "tcl-gb300 0.1.0 sm_103a"; }
+
+}  // extern "C"

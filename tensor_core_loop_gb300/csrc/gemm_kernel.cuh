@@ -1,0 +1,456 @@
+// Persistent, warp-specialised tensor-core GEMM for sm_103a:
+//   C[M×N] = A[M×K] · B[K×N], A and B row-major, fp32 accumulation in TMEM.
+//
+// The K-loop is the software pipeline the pages describe ("流水化 GPU 内核",
+// steps 3-4: prologue / steady state / drain with the load of tile k+1
+// overlapping the MMA on tile k; "4.1 CUDA GEMM 算子性能优化" §9.3-§10.4:
+// global→shared double buffering generalised to a multi-stage ring), rebuilt
+// for Blackwell:
+//   * warp 0 (producer): TMA 2-D tiled loads of the A tile (BM×BK, K-major)
+//     and the B tile (BK×BN, N-major) into stage s of a STAGES-deep ring,
+//     128-byte swizzled; completion tracked by the full[s] mbarrier as
+//     transaction bytes. It waits on empty[s] before reusing a stage.
+//   * warp 1 (MMA issuer): one thread issues tcgen05.mma (kind::f16 or
+//     kind::tf32) per UMMA_K slice into a TMEM accumulator, and commits
+//     empty[s] when the stage's MMAs are done; at the end of a unit it
+//     commits acc_full[b]. Two accumulators let the epilogue of one tile run
+//     under the mainloop of the next.
+//   * warps 2-5 (epilogue): tcgen05.ld 32 lanes × 32 columns per warp, convert
+//     (fp32 pass-through, fp32→bf16 round-to-nearest-even, or exact
+//     integer drain), write a 128-byte-swizzled staging slab and TMA-store
+//     it to C; then release acc_empty[b].
+//   * tiles are walked persistently (tile = blockIdx.x + i·gridDim.x) in a
+//     grouped raster order ("4.1 CUDA GEMM 算子性能优化" §2.3: the order in
+//     which blocks are scheduled decides the L2 hit rate).
+//
+// Exact integer mode (OutKind::S32): the operands are integers stored as
+// bf16 (exact for |x| ≤ 256), every product is an exact integer, and fp32
+// holds every integer of magnitude ≤ 2^24. The MMA warp therefore closes an
+// accumulation unit every `kb_per_unit` k-blocks, chosen on the host so that
+// the sum of |products| inside one unit stays ≤ 2^24, and the epilogue adds
+// each unit, converted to int32, into per-thread int32 registers.
+//
+// Every wait on an mbarrier is bounded: after `timeout_ns` of %globaltimer it
+// records an error code in the device status word, raises a shared abort
+// flag that the other roles poll, lets its own in-flight copies and MMAs
+// finish, and the kernel returns normally (TMEM freed). No trap, no assert.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace tcl {
+
+enum class InKind : int { BF16 = 0, TF32 = 1 };
+enum class OutKind : int { F32 = 0, BF16 = 1, S32 = 2 };
+
+// Device status codes (first failure wins).
+enum : unsigned int {
+    DEV_OK = 0,
+    DEV_TIMEOUT_PRODUCER = 1,   // producer waited too long for a free stage
+    DEV_TIMEOUT_MMA_FULL = 2,   // MMA warp waited too long for a stage's data
+    DEV_TIMEOUT_MMA_ACC = 3,    // MMA warp waited too long for a free accumulator
+    DEV_TIMEOUT_EPILOGUE = 4,   // epilogue waited too long for a finished accumulator
+};
+
+template <InKind IK>
+struct InTraits;
+template <>
+struct InTraits<InKind::BF16> {
+    static constexpr int ES = 2;        // bytes per element
+    static constexpr int UMMA_K = 16;   // K per tcgen05.mma
+    static constexpr uint32_t FMT = 1;  // bf16
+};
+template <>
+struct InTraits<InKind::TF32> {
+    static constexpr int ES = 4;
+    static constexpr int UMMA_K = 8;
+    static constexpr uint32_t FMT = 2;  // tf32
+};
+
+struct GemmParams {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles;
+    int num_kb;        // k-blocks per tile, ceil(K / BK)
+    int kb_per_unit;   // k-blocks per TMEM accumulation unit (num_kb unless S32)
+    int group_m;       // raster group height in tiles
+    unsigned long long timeout_ns;
+    unsigned int* status;        // device status word
+    unsigned long long* trace;   // optional per-k-block timeline of CTA 0 (nullptr: off)
+    int trace_cap;               // k-blocks the trace buffer holds
+};
+
+constexpr int pow2_at_least(int x, int lo) {
+    int p = lo;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+template <InKind IK, OutKind OK, int BN_, int STAGES_>
+struct KCfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int ES = InTraits<IK>::ES;
+    static constexpr int BK = 128 / ES;               // one 128-byte swizzle row of K
+    static constexpr int UMMA_K = InTraits<IK>::UMMA_K;
+    static constexpr int KSUB = BK / UMMA_K;          // MMAs per k-block
+    static constexpr int A_BYTES = BM * 128;          // BM rows × 128 B
+    static constexpr int B_BOX_N = 128 / ES;          // N columns per swizzle box
+    static constexpr int B_BOXES = BN / B_BOX_N;
+    static constexpr int B_BOX_BYTES = BK * 128;      // BK rows × 128 B
+    static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int OUT_ES = (OK == OutKind::BF16) ? 2 : 4;
+    static constexpr int EPI_COLS = 128 / OUT_ES;     // output columns per 128-byte staging row
+    static constexpr int EPI_CHUNKS = BN / EPI_COLS;
+    static constexpr int SLAB_BYTES = 32 * 128;       // one warp's 32 rows × 128 B
+    static constexpr int STAGING_BYTES = 4 * 2 * SLAB_BYTES;
+    static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_USED = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
+    // Request more than half of the SM's 228 KB so that exactly one CTA is
+    // resident per SM: its TMEM allocation is then never contended and every
+    // ring depth is measured under the same occupancy.
+    static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
+    static constexpr uint32_t IDESC =
+        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, /*B MN-major*/ 1, BM, BN);
+    static constexpr int THREADS = 192;
+
+    static_assert(BN % B_BOX_N == 0, "BN must be a whole number of swizzle boxes");
+    static_assert(BN % EPI_COLS == 0, "BN must be a whole number of epilogue chunks");
+    static_assert(BN >= 16 && BN <= 256 && BN % 16 == 0, "UMMA N for M=128 is 16..256 step 16");
+    static_assert(2 * BN <= 512, "two accumulators must fit the 512 TMEM columns");
+    static_assert(STAGES >= 1 && 2 * STAGES + 5 <= 28, "barrier area");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
+    static_assert(OK != OutKind::S32 || BN <= 128, "exact integer drain keeps BN int32 sums in registers");
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int rows = min(p.tiles_m - first_m, p.group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % rows;
+    nb = r / rows;
+}
+
+// Bounded wait on an mbarrier phase. Returns false (and raises the abort flag,
+// recording `code` if it is the first failure) once `timeout_ns` has passed,
+// or as soon as another role has raised the abort flag.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t* abort_flag,
+                                             unsigned long long timeout_ns, unsigned int* status,
+                                             unsigned int code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1u;
+            atomicCAS(status, 0u, code);
+            return false;
+        }
+    }
+}
+
+// Bounded wait used only while draining after an abort: ignores the flag.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
+                                           unsigned long long timeout_ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) return;
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// One warp writes 32 rows × 128 bytes (row = lane) into a staging slab in the
+// 128-byte swizzled layout the C tensor map expects (16-byte chunk j of row r
+// lands at chunk j ^ (r mod 8)), then lane 0 TMA-stores the slab.
+// Always commits one bulk group per call so that "at most one group pending"
+// means "the slab used two calls ago is free".
+template <int SLAB_BYTES>
+__device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
+                                           const uint32_t (&v)[32], int lane, int col0, int row0,
+                                           bool in_bounds) {
+    uint8_t* slab = slab_pair + (count & 1) * SLAB_BYTES;
+    if (lane == 0) ptx::bulk_wait_read<1>();
+    __syncwarp();
+    const uint32_t row_addr = ptx::smem_u32(slab) + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                     v[4 * j + 3]);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (in_bounds) ptx::tma_store_2d(tmC, ptx::smem_u32(slab), col0, row0);
+        ptx::bulk_commit();
+    }
+    ++count;
+}
+
+template <InKind IK, OutKind OK, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    using C = KCfg<IK, OK, BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzle atoms must sit on 1024-byte boundaries of the shared window.
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* stage_base = smem;
+    uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STAGING_BYTES);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile uint32_t* abort_flag = tmem_holder + 1;
+
+    const uint32_t full0 = ptx::smem_u32(bars);
+    const uint32_t empty0 = ptx::smem_u32(bars + STAGES);
+    const uint32_t accf0 = ptx::smem_u32(bars + 2 * STAGES);
+    const uint32_t acce0 = ptx::smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t drain_bar = ptx::smem_u32(bars + 2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);
+            ptx::mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf0 + 8 * b, 1);
+            ptx::mbar_init(acce0 + 8 * b, 4);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer (TMA)
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p, mb, nb);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                                      DEV_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    if (tracing) {
+                        const uint64_t now = ptx::clock64();
+                        if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap)
+                            p.trace[4 * (it - STAGES) + 3] = now;   // MMA of block it-STAGES done
+                        if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;   // load issued
+                    }
+                    const uint32_t full = full0 + 8 * s;
+                    const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+                    ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                    ptx::tma_load_2d(sa, &tmA, full, kb * C::BK, mb * C::BM);
+#pragma unroll
+                    for (int b = 0; b < C::B_BOXES; ++b) {
+                        ptx::tma_load_2d(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
+                                         nb * BN + b * C::B_BOX_N, kb * C::BK);
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every load still in flight land before the CTA can exit.
+                const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+                for (uint32_t j = first; j < it; ++j)
+                    wait_drain(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, unit = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_unit, ++unit) {
+                    const uint32_t buf = unit & 1u;
+                    const uint32_t uph = (unit >> 1) & 1u;
+                    if (!wait_bounded(acce0 + 8 * buf, uph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                                      DEV_TIMEOUT_MMA_ACC)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const int kb1 = min(kb0 + p.kb_per_unit, p.num_kb);
+                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                        const uint32_t s = it % STAGES;
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.timeout_ns, p.status,
+                                          DEV_TIMEOUT_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
+                        const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+                        const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+                        for (int ks = 0; ks < C::KSUB; ++ks) {
+                            // A: K-major rows of 128 B; step UMMA_K elements inside the swizzle row.
+                            const uint64_t adesc =
+                                ptx::sdesc_sw128(sa + ks * C::UMMA_K * C::ES, 16, 1024);
+                            // B: N-major; step UMMA_K rows of 128 B; boxes of B_BOX_N columns apart.
+                            const uint64_t bdesc =
+                                ptx::sdesc_sw128(sb + ks * C::UMMA_K * 128, C::B_BOX_BYTES, 1024);
+                            const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
+                            if constexpr (IK == InKind::TF32)
+                                ptx::mma_tf32_ss(d_tmem, adesc, bdesc, C::IDESC, acc);
+                            else
+                                ptx::mma_f16_ss(d_tmem, adesc, bdesc, C::IDESC, acc);
+                        }
+                        ptx::mma_commit(empty0 + 8 * s);   // stage s free once these MMAs finish
+                        if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(accf0 + 8 * buf);      // accumulator ready for the epilogue
+                }
+            }
+            if (!ok) {
+                ptx::mma_commit(drain_bar);
+                wait_drain(drain_bar, 0, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;   // TMEM lane quarter this warp may read
+        uint8_t* slab_pair = staging + (warp - 2) * 2 * C::SLAB_BYTES;
+        int store_count = 0;
+        uint32_t unit = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p, mb, nb);
+            const int row0 = mb * C::BM + q * 32;
+            const bool row_in = row0 < p.M;
+            [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? BN : 1];
+            if constexpr (OK == OutKind::S32) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) iacc[i] = 0;
+            }
+            for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_unit, ++unit) {
+                const uint32_t buf = unit & 1u;
+                const uint32_t uph = (unit >> 1) & 1u;
+                bool got = true;
+                if (lane == 0)
+                    got = wait_bounded(accf0 + 8 * buf, uph, abort_flag, p.timeout_ns, p.status,
+                                       DEV_TIMEOUT_EPILOGUE);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+                if constexpr (OK == OutKind::S32) {
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        __syncwarp();   // tcgen05.ld is warp-collective
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
+                        ptx::tmem_ld_wait(r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) iacc[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce0 + 8 * buf);
+                    if (kb0 + p.kb_per_unit >= p.num_kb) {
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c) {
+                            const uint32_t(&v)[32] =
+                                *reinterpret_cast<const uint32_t(*)[32]>(&iacc[c * 32]);
+                            const int col0 = nb * BN + c * 32;
+                            store_slab<C::SLAB_BYTES>(&tmC, slab_pair, store_count, v, lane, col0, row0,
+                                                      row_in && col0 < p.N);
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < C::EPI_CHUNKS; ++c) {
+                        __syncwarp();   // tcgen05.ld is warp-collective
+                        uint32_t v[32];
+                        if constexpr (OK == OutKind::F32) {
+                            ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
+                            ptx::tmem_ld_wait(v);
+                        } else {
+                            uint32_t lo[32], hi[32];
+                            ptx::tmem_ld_32x32b_x32(tbase + c * 64, lo);
+                            ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, hi);
+                            ptx::tmem_ld_wait(lo);
+                            ptx::tmem_ld_wait(hi);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(lo[2 * i]),
+                                                                         __uint_as_float(lo[2 * i + 1]));
+                                v[i] = *reinterpret_cast<uint32_t*>(&t);
+                                __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(hi[2 * i]),
+                                                                         __uint_as_float(hi[2 * i + 1]));
+                                v[16 + i] = *reinterpret_cast<uint32_t*>(&u);
+                            }
+                        }
+                        if (c == C::EPI_CHUNKS - 1) {
+                            // all of this unit's TMEM columns are in registers: free the accumulator
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(acce0 + 8 * buf);
+                        }
+                        const int col0 = nb * BN + c * C::EPI_COLS;
+                        store_slab<C::SLAB_BYTES>(&tmC, slab_pair, store_count, v, lane, col0, row0,
+                                                  row_in && col0 < p.N);
+                    }
+                }
+            }
+        }
+        if (lane == 0) ptx::bulk_wait<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tcl

@@ -1,0 +1,68 @@
+// Exact int8 -> bf16 widening for the integer GEMM path.
+//
+// Every int8 value (|x| <= 128) has at most 8 significant bits, so it is
+// represented exactly by bf16; the bf16 pattern is the upper half of the
+// binary32 encoding of the integer. Rows are processed in 16-element chunks:
+// one 16-byte load, two 16-byte stores. The source base and its leading
+// dimension are 16-byte aligned (checked by the C-ABI), the destination rows
+// are padded to a multiple of 8 elements, so full chunks use vector accesses
+// and only a ragged row tail falls back to scalar accesses.
+#include <cstdint>
+
+#include "launch.cuh"
+
+namespace tcl {
+
+__device__ __forceinline__ uint32_t s8_pair_to_bf16x2(int lo, int hi) {
+    const uint32_t l = __float_as_uint(static_cast<float>(lo)) >> 16;
+    const uint32_t h = __float_as_uint(static_cast<float>(hi)) & 0xFFFF0000u;
+    return l | h;
+}
+
+__global__ void __launch_bounds__(256) s8_to_bf16_kernel(const int8_t* __restrict__ src,
+                                                          long long ld_src,
+                                                          uint16_t* __restrict__ dst,
+                                                          long long ld_dst, int rows, int cols) {
+    const int chunks_per_row = (cols + 15) / 16;
+    const long long total = static_cast<long long>(rows) * chunks_per_row;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(idx / chunks_per_row);
+        const int c0 = static_cast<int>(idx - static_cast<long long>(r) * chunks_per_row) * 16;
+        const int8_t* s = src + r * ld_src + c0;
+        uint16_t* d = dst + r * ld_dst + c0;
+        if (c0 + 16 <= cols) {
+            const int4 raw = *reinterpret_cast<const int4*>(s);
+            const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+            uint4 o0, o1;
+            o0.x = s8_pair_to_bf16x2(b[0], b[1]);
+            o0.y = s8_pair_to_bf16x2(b[2], b[3]);
+            o0.z = s8_pair_to_bf16x2(b[4], b[5]);
+            o0.w = s8_pair_to_bf16x2(b[6], b[7]);
+            o1.x = s8_pair_to_bf16x2(b[8], b[9]);
+            o1.y = s8_pair_to_bf16x2(b[10], b[11]);
+            o1.z = s8_pair_to_bf16x2(b[12], b[13]);
+            o1.w = s8_pair_to_bf16x2(b[14], b[15]);
+            reinterpret_cast<uint4*>(d)[0] = o0;
+            reinterpret_cast<uint4*>(d)[1] = o1;
+        } else {
+            for (int j = 0; c0 + j < cols; ++j)
+                d[j] = static_cast<uint16_t>(__float_as_uint(static_cast<float>(s[j])) >> 16);
+        }
+    }
+}
+
+cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, long long ld_dst,
+                              int rows, int cols, int sms, cudaStream_t stream) {
+    const long long chunks = static_cast<long long>(rows) * ((cols + 15) / 16);
+    const int threads = 256;
+    long long blocks = (chunks + threads - 1) / threads;
+    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks per SM, grid-stride beyond
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        src, ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+    return cudaGetLastError();
+}
+
+}  // namespace tcl

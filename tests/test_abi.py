@@ -1,0 +1,102 @@
+"""The C ABI on the host (no GPU): the library loads, exports every entry point
+include/tcl_gemm.h declares, rejects bad arguments with the documented status
+before touching the device, and plans launches as documented."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_core_loop_gb300 as tcl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tensor_core_loop_gb300 import _build
+    _build.build()
+    return tcl.lib()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "tcl_gemm.h")).read()
+    return sorted(set(re.findall(r"TCL_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_api():
+    syms = header_symbols()
+    assert set(syms) == set(tcl.EXPORTED_SYMBOLS), syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in header_symbols():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(L):
+    assert "sm_103a" in tcl.version()
+    for code in range(11):
+        s = L.tcl_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.tcl_status_string(99).decode() == "unknown status"
+
+
+# Fake but well-formed device addresses: validation must reject before any CUDA call.
+P = 0x10000000
+PM = 0x10000004  # misaligned
+
+
+@pytest.mark.parametrize("args,status", [
+    ((64, 64, 64, 0, 64, P, 64, P, 64, 0), 1),            # A null
+    ((64, 64, 64, P, 64, P, 64, 0, 64, 0), 1),            # C null
+    ((0, 64, 64, P, 64, P, 64, P, 64, 0), 2),             # M = 0
+    ((64, 64, -1, P, 64, P, 64, P, 64, 0), 2),            # K < 0
+    ((64, 64, 64, P, 32, P, 64, P, 64, 0), 3),            # lda < K
+    ((64, 64, 64, P, 64, P, 32, P, 64, 0), 3),            # ldb < N
+    ((64, 64, 64, P, 64, P, 64, P, 32, 0), 3),            # ldc < N
+    ((64, 64, 64, PM, 64, P, 64, P, 64, 0), 4),           # A misaligned
+    ((64, 64, 64, P, 68, P, 64, P, 64, 0), 4),            # lda*2 not a multiple of 16
+    ((64, 64, 64, P, 64, P, 64, P, 66, 0), 4),            # ldc*4 not a multiple of 16
+    ((64, 64, 64, P, 64, P, 64, P, 68, 1), 4),            # bf16 C: ldc*2 not a multiple of 16
+    ((64, 64, 64, P, 64, P, 64, P, 64, 7), 8),            # unknown output type
+])
+def test_gemm_bf16_rejects(L, args, status):
+    assert L.gemm_bf16(*args, None) == status
+
+
+def test_gemm_tf32_and_s8_reject(L):
+    assert L.gemm_tf32(64, 64, 64, P, 66, P, 64, P, 64, None) == 4
+    assert L.gemm_tf32(64, 64, 64, 0, 64, P, 64, P, 64, None) == 1
+    assert L.gemm_s8(64, 64, 64, P, 72, P, 64, P, 64, None) == 4          # lda not a multiple of 16
+    assert L.gemm_s8(64, 64, 131072, P, 131072, P, 64, P, 64, None) == 5  # K beyond the exact int32 range
+    assert L.gemm_s8(64, 64, 64, P, 64, P, 64, PM, 64, None) == 4
+
+
+def test_plan_without_device(L):
+    cfg = tcl.Config(max_ctas=152)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)
+    assert p["bn"] == 256 and p["num_tiles"] == 32 * 16 and p["grid"] == 152
+    assert p["smem_bytes"] <= 232448
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096, cfg)
+    assert p["bn"] == 128 and p["num_tiles"] == 16 and p["grid"] == 16
+    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, cfg)
+    assert p["bn"] == 128
+    p = tcl.plan(tcl.IN_TF32, 0, 300, 70, 9, cfg)
+    assert p["num_tiles"] == 3 * 1
+    cfg2 = tcl.Config(max_ctas=152, bn=256, stages=2, one_cta_per_tile=1)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg2)
+    assert p["stages"] == 2 and p["grid"] == 512
+    with pytest.raises(tcl.TclError):
+        tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, bn=192))
+    with pytest.raises(tcl.TclError):
+        tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stages=5))
+
+
+def test_every_stage_count_fits_shared_memory(L):
+    for bn, stages in [(256, 1), (256, 2), (256, 3), (256, 4), (128, 1), (128, 2), (128, 4), (128, 6)]:
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 1024, 1024, 1024, tcl.Config(max_ctas=8, bn=bn, stages=stages))
+        assert p["smem_bytes"] <= 232448

@@ -1,0 +1,229 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on a GB300.
+
+Small problems are compared element by element over the whole output; the
+full-size workloads (4096³ and the K sweep) are compared on sampled rows that
+cover several M tiles, including the first and last, across all N tiles.
+Bounds: tests/bounds.py. int8 is compared bit-exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import tensor_core_loop_gb300 as tcl
+from tensor_core_loop_gb300 import inputs
+
+from bounds import assert_exact, assert_within
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tcl.lib()
+    yield
+    st, code = tcl.last_device_error()
+    assert st == 0, f"device status word reported code {code}"
+
+
+def run(a, b, out_dtype=None, cfg=None, ldc=None, canary=True):
+    """Run through the C ABI into a C buffer padded to `ldc` columns plus one guard row
+    filled with a sentinel; check the sentinel survived; return C[:M, :N] on the host."""
+    M, N = a.shape[0], b.shape[1]
+    out_dtype = out_dtype or {torch.bfloat16: torch.float32, torch.float32: torch.float32,
+                              torch.int8: torch.int32}[a.dtype]
+    if ldc is None:   # smallest leading dimension that keeps rows 16-byte aligned
+        q = 16 // torch.empty((), dtype=out_dtype).element_size()
+        ldc = -(-N // q) * q
+    buf = torch.empty((M + 1, ldc), dtype=out_dtype, device=DEV)
+    sentinel = -12345 if out_dtype == torch.int32 else float("nan") if out_dtype == torch.float32 else -3.0
+    buf.fill_(sentinel)
+    c = buf[:M, :N]
+    tcl.gemm_into(a, b, c, cfg=cfg)
+    torch.cuda.synchronize()
+    host = buf.cpu()
+    if canary:
+        pad = torch.cat([host[:M, N:].reshape(-1), host[M].reshape(-1)])
+        if out_dtype == torch.float32:
+            assert torch.isnan(pad).all(), "kernel wrote outside C"
+        else:
+            assert (pad == sentinel).all(), "kernel wrote outside C"
+    return host[:M, :N]
+
+
+def to_dev(t):
+    """Copy a (possibly padded) host view to the device, keeping its leading dimension."""
+    if t.is_contiguous():
+        return t.to(DEV)
+    rows, cols = t.shape
+    ld = t.stride(0)
+    full = torch.as_strided(t, (rows, ld), (ld, 1)) if rows else t
+    return full.to(DEV)[:, :cols]
+
+
+def up(x, q):
+    return -(-x // q) * q
+
+
+def bf16_case(oracle_mod, M, N, K, seed=0, out_dtype=torch.float32, cfg=None, lda=None, ldb=None, ldc=None,
+              rows=None):
+    a, b = inputs.bf16_pair(M, N, K, seed=seed, lda=lda or up(K, 8), ldb=ldb or up(N, 8))
+    got = run(to_dev(a), to_dev(b), out_dtype=out_dtype, cfg=cfg, ldc=ldc).double().numpy()
+    kind = "bf16_f32" if out_dtype == torch.float32 else "bf16_bf16"
+    if rows is None:
+        ref, S = oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b))
+        return assert_within(kind, got, ref, S, f"bf16 {M}x{N}x{K}")
+    worst = 0.0
+    for r in rows:
+        ref, S = oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b), rows=(r, r + 1))
+        worst = max(worst, assert_within(kind, got[r:r + 1], ref, S, f"bf16 {M}x{N}x{K} row {r}"))
+    return worst
+
+
+def sample_rows(M, n=24, seed=0):
+    g = np.random.default_rng(seed)
+    fixed = {0, 1, 31, 32, 127, 128, M // 2, M - 129, M - 128, M - 1}
+    return sorted(r for r in fixed.union(g.integers(0, M, n).tolist()) if 0 <= r < M)
+
+
+# ------------------------------------------------------------- small, full compare
+
+def test_bf16_256_cube_fp32(oracle_mod):
+    bf16_case(oracle_mod, 256, 256, 256, seed=0)
+
+
+def test_bf16_512_cube_fp32(oracle_mod):
+    bf16_case(oracle_mod, 512, 512, 512, seed=1)
+
+
+@pytest.mark.parametrize("K", [8, 16, 64, 72, 128, 200, 3 * 64, 5 * 64, 7 * 64, 1000])
+def test_bf16_k_edges(oracle_mod, K):
+    # one k-block, two, fewer blocks than stages, ring wrap (stages ± 1), ragged last block
+    bf16_case(oracle_mod, 256, 384, K, seed=K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (130, 260, 200), (129, 136, 64), (300, 520, 96), (77, 1000, 40)])
+def test_bf16_ragged_shapes(oracle_mod, M, N, K):
+    bf16_case(oracle_mod, M, N, K, seed=M + N)
+
+
+def test_bf16_padded_leading_dims(oracle_mod):
+    bf16_case(oracle_mod, 200, 264, 136, seed=5, lda=136 + 8, ldb=264 + 16, ldc=264 + 12)
+
+
+def test_bf16_narrow_n_with_padded_ldc(oracle_mod):
+    bf16_case(oracle_mod, 140, 1, 72, seed=6, ldc=4)
+    bf16_case(oracle_mod, 140, 3, 72, seed=7, ldc=8)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 520, 200)])
+def test_bf16_out_bf16(oracle_mod, M, N, K):
+    bf16_case(oracle_mod, M, N, K, seed=3, out_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("bn,stages", [(256, 1), (256, 2), (256, 3), (256, 4), (128, 1), (128, 2), (128, 4),
+                                       (128, 6)])
+def test_bf16_each_variant(oracle_mod, bn, stages):
+    bf16_case(oracle_mod, 384, 512, 640, seed=9, cfg=tcl.Config(bn=bn, stages=stages))
+
+
+def test_variants_bitwise_identical():
+    """Pipelining only reorders loads: every ring depth, persistent or one CTA per
+    tile, gives the same bits (the MMA order inside a tile does not change)."""
+    a, b = inputs.bf16_pair(640, 768, 1216, seed=13)
+    a, b = a.to(DEV), b.to(DEV)
+    for bn, stages_list in ((256, (1, 2, 3, 4)), (128, (1, 2, 4, 6))):
+        outs = []
+        for st in stages_list:
+            for one_per_tile in (0, 1):
+                for max_ctas in (0, 3):
+                    cfg = tcl.Config(bn=bn, stages=st, one_cta_per_tile=one_per_tile, max_ctas=max_ctas,
+                                     group_m=3 if max_ctas else 0)
+                    outs.append(run(a, b, cfg=cfg, canary=False))
+        for o in outs[1:]:
+            assert torch.equal(o, outs[0])
+
+
+def test_repeat_runs_bitwise_identical():
+    a, b = inputs.bf16_pair(1024, 1024, 2048, seed=17)
+    a, b = a.to(DEV), b.to(DEV)
+    first = tcl.gemm(a, b)
+    for _ in range(10):
+        assert torch.equal(tcl.gemm(a, b), first)
+
+
+# ------------------------------------------------------------- tf32 and int8, small
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (130, 260, 200), (64, 40, 36)])
+def test_tf32_small(oracle_mod, M, N, K):
+    a, b = inputs.tf32_pair(M, N, K, seed=M, lda=up(K, 4), ldb=up(N, 4))
+    got = run(to_dev(a), to_dev(b)).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, f"tf32 {M}x{N}x{K}")
+
+
+def test_tf32_padded(oracle_mod):
+    a, b = inputs.tf32_pair(100, 96, 52, seed=4, lda=56, ldb=100)
+    got = run(to_dev(a), to_dev(b), ldc=100).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, "tf32 padded")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (130, 260, 208), (64, 40, 1040), (200, 136, 2064)])
+def test_s8_small_exact(oracle_mod, M, N, K):
+    a, b = inputs.s8_pair(M, N, K, seed=M, lda=up(K, 16), ldb=up(N, 16))
+    got = run(to_dev(a), to_dev(b)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 {M}x{N}x{K}")
+
+
+def test_s8_padded(oracle_mod):
+    a, b = inputs.s8_pair(100, 90, 70, seed=8, lda=80, ldb=96)
+    got = run(to_dev(a), to_dev(b), ldc=92).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 padded")
+
+
+@pytest.mark.parametrize("va,vb", [(127, 127), (-128, -128), (127, -128)])
+def test_s8_extremes_closed_form(va, vb):
+    K = 4096
+    a = torch.full((256, K), va, dtype=torch.int8, device=DEV)
+    b = torch.full((K, 256), vb, dtype=torch.int8, device=DEV)
+    c = tcl.gemm(a, b)
+    assert (c == va * vb * K).all()
+
+
+# ------------------------------------------------------------- full-size workloads, sampled
+
+def test_bf16_4096_cube_fp32_sampled(oracle_mod):
+    bf16_case(oracle_mod, 4096, 4096, 4096, seed=0, rows=sample_rows(4096))
+
+
+def test_bf16_4096_cube_bf16_sampled(oracle_mod):
+    bf16_case(oracle_mod, 4096, 4096, 4096, seed=0, out_dtype=torch.bfloat16, rows=sample_rows(4096, n=8))
+
+
+@pytest.mark.parametrize("MN", [512, 4096])
+@pytest.mark.parametrize("K", [256, 512, 1024, 4096, 8192])
+def test_bf16_k_sweep_sampled(oracle_mod, MN, K):
+    rows = list(range(MN)) if MN == 512 and K <= 1024 else sample_rows(MN, n=6, seed=K)
+    bf16_case(oracle_mod, MN, MN, K, seed=0, rows=rows)
+
+
+def test_s8_4096_cube_sampled_exact(oracle_mod):
+    a, b = inputs.s8_pair(4096, 4096, 4096, seed=0)
+    got = run(a.to(DEV), b.to(DEV)).numpy()
+    rows = sample_rows(4096, n=10)
+    for r in rows:
+        assert_exact(got[r:r + 1], oracle_mod.gemm_s8(a.numpy(), b.numpy(), rows=(r, r + 1)), f"s8 row {r}")
+
+
+def test_tf32_4096_cube_sampled(oracle_mod):
+    a, b = inputs.tf32_pair(4096, 4096, 4096, seed=0)
+    got = run(a.to(DEV), b.to(DEV)).double().numpy()
+    for r in sample_rows(4096, n=8):
+        ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy(), rows=(r, r + 1))
+        assert_within("tf32", got[r:r + 1], ref, S, f"tf32 row {r}")

@@ -28,12 +28,16 @@
  * Alignment (the TMA rule: global base addresses 16-byte aligned, row
  *   strides a multiple of 16 bytes; "cp.async / ldmatrix 消融实验", §1.4 item
  *   2 states the same 16-byte rule for cp.async):
- *   gemm_bf16: A, B, C 16-byte aligned; lda, ldb multiples of 8;
+ *   gemm_bf16: A, B, C 16-byte aligned; lda, ldb and K multiples of 8;
  *              ldc a multiple of 4 (fp32 C) or 8 (bf16 C).
- *   gemm_tf32: A, B, C 16-byte aligned; lda, ldb, ldc multiples of 4.
- *   gemm_s8:   A, B, C 16-byte aligned; lda, ldb multiples of 16; ldc of 4.
- *   M, N, K are otherwise free (>= 1): edge tiles are zero-filled on load and
- *   clipped on store.
+ *   gemm_tf32: A, B, C 16-byte aligned; lda, ldb, K and ldc multiples of 4.
+ *   gemm_s8:   A, B, C 16-byte aligned; lda, ldb multiples of 16; ldc of 4;
+ *              K free (the operands are repacked with zero padding).
+ *   (A row of A ends at K; a tensor load rounds a row end up to 16 bytes, so
+ *   K itself must keep that boundary for bf16 and TF32.) M and N are free
+ *   (>= 1): edge tiles are zero-filled on load, rows past M are never
+ *   written, and a right edge N that is not on a 16-byte boundary is written
+ *   element by element, so nothing outside the M×N block of C changes.
  *
  * Errors: each entry point returns a tcl_status. Argument checks happen on
  *   the host before anything is enqueued; a nonzero status means nothing was
@@ -62,7 +66,7 @@ typedef enum {
     TCL_ERR_NULL = 1,            /* a required pointer is NULL */
     TCL_ERR_DIMS = 2,            /* M, N or K < 1 */
     TCL_ERR_LD = 3,              /* lda < K, ldb < N or ldc < N */
-    TCL_ERR_ALIGN = 4,           /* base or leading dimension breaks the alignment rule above */
+    TCL_ERR_ALIGN = 4,           /* base, leading dimension or K breaks the alignment rule above */
     TCL_ERR_K_TOO_LARGE = 5,     /* gemm_s8: K > 131071, the int32 result could overflow */
     TCL_ERR_LAUNCH = 6,          /* a CUDA call or kernel launch failed */
     TCL_ERR_DEVICE_TIMEOUT = 7,  /* a bounded in-kernel wait ran out (see tcl_last_device_error) */

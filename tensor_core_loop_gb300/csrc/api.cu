@@ -253,6 +253,8 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     p.status = ds->status;
     p.trace = cfg ? cfg->trace : nullptr;
     p.trace_cap = cfg && cfg->trace ? cfg->trace_cap : 0;
+    p.C = C;
+    p.ldc = ldc;
 
     bool found = false;
     cudaError_t err = cudaSuccess;
@@ -276,7 +278,7 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
     if (out != TCL_OUT_F32 && out != TCL_OUT_BF16) return TCL_ERR_CONFIG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 8 || ldb % 8 ||
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 8 || ldb % 8 || K % 8 ||
         ldc % (out == TCL_OUT_BF16 ? 8 : 4))
         return TCL_ERR_ALIGN;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -291,7 +293,7 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
                    int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 4 || ldb % 4 || ldc % 4)
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 4 || ldb % 4 || K % 4 || ldc % 4)
         return TCL_ERR_ALIGN;
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;

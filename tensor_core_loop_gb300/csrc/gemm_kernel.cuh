@@ -79,6 +79,8 @@ struct GemmParams {
     unsigned int* status;        // device status word
     unsigned long long* trace;   // optional per-k-block timeline of CTA 0 (nullptr: off)
     int trace_cap;               // k-blocks the trace buffer holds
+    void* C;                     // output base, for the ragged right edge only
+    long long ldc;               // output leading dimension in elements
 };
 
 constexpr int pow2_at_least(int x, int lo) {
@@ -178,10 +180,38 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // lands at chunk j ^ (r mod 8)), then lane 0 TMA-stores the slab.
 // Always commits one bulk group per call so that "at most one group pending"
 // means "the slab used two calls ago is free".
-template <int SLAB_BYTES>
+//
+// The tensor store writes whole 16-byte pieces of a row, so a chunk that
+// crosses a right edge N not on a 16-byte boundary would also write the
+// columns after N. That chunk is stored element by element from registers
+// instead (rows past M skipped), leaving every byte outside C untouched.
+template <int SLAB_BYTES, int OUT_ES>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
-                                           bool in_bounds) {
+                                           const GemmParams& p) {
+    constexpr int COLS = 128 / OUT_ES;
+    const bool in_bounds = row0 < p.M && col0 < p.N;
+    if (in_bounds && col0 + COLS > p.N && (p.N * OUT_ES) % 16 != 0) {
+        const int row = row0 + lane;
+        if (row < p.M) {
+            const int n = p.N - col0;
+            if constexpr (OUT_ES == 4) {
+                uint32_t* dst = static_cast<uint32_t*>(p.C) + row * p.ldc + col0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < n) dst[i] = v[i];
+            } else {
+                uint16_t* dst = static_cast<uint16_t*>(p.C) + row * p.ldc + col0;
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (i < n) dst[i] = static_cast<uint16_t>((i & 1) ? (v[i >> 1] >> 16) : (v[i >> 1] & 0xFFFFu));
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::bulk_commit();
+        ++count;
+        return;
+    }
     uint8_t* slab = slab_pair + (count & 1) * SLAB_BYTES;
     if (lane == 0) ptx::bulk_wait_read<1>();
     __syncwarp();
@@ -360,7 +390,6 @@ __global__ void __launch_bounds__(192, 1)
             int mb, nb;
             tile_coords(tile, p, mb, nb);
             const int row0 = mb * C::BM + q * 32;
-            const bool row_in = row0 < p.M;
             [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? BN : 1];
             if constexpr (OK == OutKind::S32) {
 #pragma unroll
@@ -399,8 +428,8 @@ __global__ void __launch_bounds__(192, 1)
                             const uint32_t(&v)[32] =
                                 *reinterpret_cast<const uint32_t(*)[32]>(&iacc[c * 32]);
                             const int col0 = nb * BN + c * 32;
-                            store_slab<C::SLAB_BYTES>(&tmC, slab_pair, store_count, v, lane, col0, row0,
-                                                      row_in && col0 < p.N);
+                            store_slab<C::SLAB_BYTES, C::OUT_ES>(&tmC, slab_pair, store_count, v, lane,
+                                                                 col0, row0, p);
                         }
                     }
                 } else {
@@ -434,8 +463,8 @@ __global__ void __launch_bounds__(192, 1)
                             if (lane == 0) ptx::mbar_arrive(acce0 + 8 * buf);
                         }
                         const int col0 = nb * BN + c * C::EPI_COLS;
-                        store_slab<C::SLAB_BYTES>(&tmC, slab_pair, store_count, v, lane, col0, row0,
-                                                  row_in && col0 < p.N);
+                        store_slab<C::SLAB_BYTES, C::OUT_ES>(&tmC, slab_pair, store_count, v, lane,
+                                                             col0, row0, p);
                     }
                 }
             }

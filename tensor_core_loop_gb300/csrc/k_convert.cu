@@ -5,8 +5,9 @@
 // binary32 encoding of the integer. Rows are processed in 16-element chunks:
 // one 16-byte load, two 16-byte stores. The source base and its leading
 // dimension are 16-byte aligned (checked by the C-ABI), the destination rows
-// are padded to a multiple of 8 elements, so full chunks use vector accesses
-// and only a ragged row tail falls back to scalar accesses.
+// are padded to a multiple of 8 elements (the padding is written as zeros), so
+// full chunks use vector accesses and only a ragged row tail falls back to
+// scalar accesses.
 #include <cstdint>
 
 #include "launch.cuh"
@@ -46,8 +47,12 @@ __global__ void __launch_bounds__(256) s8_to_bf16_kernel(const int8_t* __restric
             reinterpret_cast<uint4*>(d)[0] = o0;
             reinterpret_cast<uint4*>(d)[1] = o1;
         } else {
-            for (int j = 0; c0 + j < cols; ++j)
+            // ragged row end: convert what is there and zero the padding up to ld_dst,
+            // so that tensor loads that round the row end up to 16 bytes read zeros
+            int j = 0;
+            for (; c0 + j < cols; ++j)
                 d[j] = static_cast<uint16_t>(__float_as_uint(static_cast<float>(s[j])) >> 16);
+            for (; c0 + j < ld_dst && j < 16; ++j) d[j] = 0;
         }
     }
 }

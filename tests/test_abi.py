@@ -63,6 +63,7 @@ PM = 0x10000004  # misaligned
     ((64, 64, 64, P, 64, P, 64, P, 66, 0), 4),            # ldc*4 not a multiple of 16
     ((64, 64, 64, P, 64, P, 64, P, 68, 1), 4),            # bf16 C: ldc*2 not a multiple of 16
     ((64, 64, 64, P, 64, P, 64, P, 64, 7), 8),            # unknown output type
+    ((64, 64, 60, P, 64, P, 64, P, 64, 0), 4),            # K*2 bytes not a multiple of 16
 ])
 def test_gemm_bf16_rejects(L, args, status):
     assert L.gemm_bf16(*args, None) == status
@@ -71,6 +72,7 @@ def test_gemm_bf16_rejects(L, args, status):
 def test_gemm_tf32_and_s8_reject(L):
     assert L.gemm_tf32(64, 64, 64, P, 66, P, 64, P, 64, None) == 4
     assert L.gemm_tf32(64, 64, 64, 0, 64, P, 64, P, 64, None) == 1
+    assert L.gemm_tf32(64, 64, 62, P, 64, P, 64, P, 64, None) == 4        # K*4 bytes not a multiple of 16
     assert L.gemm_s8(64, 64, 64, P, 72, P, 64, P, 64, None) == 4          # lda not a multiple of 16
     assert L.gemm_s8(64, 64, 131072, P, 131072, P, 64, P, 64, None) == 5  # K beyond the exact int32 range
     assert L.gemm_s8(64, 64, 64, P, 64, P, 64, PM, 64, None) == 4

@@ -116,9 +116,16 @@ def test_bf16_padded_leading_dims(oracle_mod):
     bf16_case(oracle_mod, 200, 264, 136, seed=5, lda=136 + 8, ldb=264 + 16, ldc=264 + 12)
 
 
-def test_bf16_narrow_n_with_padded_ldc(oracle_mod):
-    bf16_case(oracle_mod, 140, 1, 72, seed=6, ldc=4)
-    bf16_case(oracle_mod, 140, 3, 72, seed=7, ldc=8)
+@pytest.mark.parametrize("N,ldc", [(1, 4), (3, 8), (5, 12), (261, 264), (259, 268)])
+def test_bf16_ragged_right_edge_fp32(oracle_mod, N, ldc):
+    # a right edge off the 16-byte grid is stored element by element; the canary
+    # columns between N and ldc must stay untouched
+    bf16_case(oracle_mod, 140, N, 72, seed=N, ldc=ldc)
+
+
+@pytest.mark.parametrize("N,ldc", [(1, 8), (7, 8), (260, 272), (300, 304)])
+def test_bf16_ragged_right_edge_bf16(oracle_mod, N, ldc):
+    bf16_case(oracle_mod, 140, N, 72, seed=N, out_dtype=torch.bfloat16, ldc=ldc)
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 520, 200)])
@@ -177,6 +184,14 @@ def test_tf32_padded(oracle_mod):
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (130, 260, 208), (64, 40, 1040), (200, 136, 2064)])
 def test_s8_small_exact(oracle_mod, M, N, K):
     a, b = inputs.s8_pair(M, N, K, seed=M, lda=up(K, 16), ldb=up(N, 16))
+    got = run(to_dev(a), to_dev(b)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 45, 37), (128, 130, 1029), (5, 3, 1)])
+def test_s8_ragged_k_exact(oracle_mod, M, N, K):
+    # int8 K need not keep the 16-byte grid: the operands are repacked with zero padding
+    a, b = inputs.s8_pair(M, N, K, seed=K, lda=up(K, 16), ldb=up(N, 16))
     got = run(to_dev(a), to_dev(b)).numpy()
     assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 {M}x{N}x{K}")
 

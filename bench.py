@@ -165,8 +165,8 @@ def cpu_oracle_sample(target_s=12.0, max_rows=4096):
     t0 = time.perf_counter()
     oracle.gemm_bf16(ab, bb, rows=(0, rows), with_abs=False)
     dt = time.perf_counter() - t0
-    more = int(min(max_rows, max(rows, rows * target_s / max(dt, 1e-3))))
-    more = max(rows, (more // cores) * cores if more >= cores else more)
+    more = int(min(max_rows - rows, max(rows, rows * target_s / max(dt, 1e-3))))
+    more = max(1, min(M - rows, (more // cores) * cores if more >= cores else more))
     t0 = time.perf_counter()
     oracle.gemm_bf16(ab, bb, rows=(rows, rows + more), with_abs=False)
     dt = time.perf_counter() - t0
@@ -305,6 +305,9 @@ def main():
     if st:
         raise RuntimeError(f"device status {st} (code {code}) after the timed region")
     ms_step = ms_total / args.steps
+    if rank == 0:
+        print(f"[bench] {args.steps} steps, {ms_step * 1e3:.2f} us/step, "
+              f"{FLOPS / (ms_step * 1e-3) / 1e12:.1f} TFLOPS per GPU; clocks {clocks}", file=sys.stderr, flush=True)
     value = FLOPS * world * args.steps / (ms_total * 1e-3) / 1e12
     per_launch_s = ms_step * 1e-3
     achieved = FLOPS / per_launch_s / 1e12

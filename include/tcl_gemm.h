@@ -17,8 +17,9 @@
  * Memory and ownership: A, B and C are device pointers owned by the caller
  *   (allocated, kept alive until the stream has run the call, and freed by
  *   the caller). The library keeps a per-device cache of TMA descriptors and,
- *   for gemm_s8 only, a per-device scratch buffer that it grows on demand
- *   (cudaMalloc, after a device synchronisation) and frees in tcl_shutdown().
+ *   for gemm_s8 and gemm_tf32, a per-device scratch buffer for repacked
+ *   operands that it grows on demand (cudaMalloc, after a device
+ *   synchronisation) and frees in tcl_shutdown().
  *
  * Streams: every call is asynchronous on `stream` (0 = legacy default
  *   stream) and returns once the work is enqueued. Calls on one stream run in
@@ -98,7 +99,9 @@ typedef struct {
 TCL_API int gemm_bf16(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc,
               int out, cudaStream_t stream);
 
-/* fp32 A, B consumed by the tensor cores as TF32; fp32 accumulation; fp32 C. */
+/* fp32 A, B consumed by the tensor cores as TF32; fp32 accumulation; fp32 C.
+ * B is first transposed, bit for bit, into library scratch (N rows of K):
+ * the TF32 tensor-core path reads both operands K-major. */
 TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
               int ldc, cudaStream_t stream);
 

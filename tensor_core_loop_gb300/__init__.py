@@ -122,11 +122,17 @@ def last_device_error(stream=None) -> tuple[int, int]:
 
 
 def _ld(t) -> int:
+    """Leading dimension in elements. A one-row matrix never steps to a second
+    row, so its leading dimension is free: report the row width rounded up to
+    16 bytes, which satisfies the library's alignment rule."""
     if t.dim() != 2:
         raise ValueError("expected a 2-D tensor")
-    if t.stride(1) != 1:
+    if t.stride(1) != 1 and t.shape[1] > 1:
         raise ValueError("rows must be contiguous (stride(1) == 1)")
-    return max(t.stride(0), t.shape[1]) if t.shape[0] > 1 else t.shape[1]
+    if t.shape[0] > 1:
+        return max(t.stride(0), t.shape[1])
+    q = max(1, 16 // t.element_size())
+    return -(-t.shape[1] // q) * q
 
 
 def gemm_into(a, b, c, cfg: Config | None = None, stream=None) -> None:

@@ -74,6 +74,30 @@ int in_bytes(InKind k) { return k == InKind::TF32 ? 4 : 2; }
 int out_bytes(OutKind k) { return k == OutKind::BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+// Grows the device's repacking scratch to at least `need` bytes. Growing waits
+// for the device to go idle, since earlier calls may still read the old buffer.
+int ensure_scratch(DevState* ds, size_t need) {
+    if (ds->scratch_bytes >= need) return TCL_OK;
+    if (ds->scratch) {
+        if (cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            return TCL_ERR_LAUNCH;
+        }
+        cudaFree(ds->scratch);
+        ds->scratch = nullptr;
+        ds->scratch_bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_NO_MEMORY;
+    }
+    ds->scratch = p;
+    ds->scratch_bytes = need;
+    return TCL_OK;
+}
 
 // Host-side argument checks shared by every entry point; no CUDA call.
 int check_common(int M, int N, int K, const void* A, int lda, const void* B, int ldb, const void* C,
@@ -237,7 +261,11 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
-    if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB))) return st;
+    if (ik == InKind::TF32) {   // B given K-major (N rows of K)
+        if ((st = tensor_map(dev, B, in_t, K, N, ldb * ies, bk, pl.bn, &a.tmB))) return st;
+    } else {                    // B given N-major (K rows of N)
+        if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB))) return st;
+    }
     if ((st = tensor_map(dev, C, out_t, N, M, ldc * oes, 128 / oes, 32, &a.tmC))) return st;
     GemmParams& p = a.p;
     p.M = M;
@@ -299,10 +327,17 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
-    return run_gemm(InKind::TF32, OutKind::F32, M, N, K, A, lda, B, ldb, C, ldc, cfg, dev, ds, stream);
+    // The TF32 tensor-core path takes B K-major: transpose it (N rows of K) into scratch.
+    if ((st = ensure_scratch(ds, static_cast<size_t>(round_up(static_cast<long long>(N) * K * 4, 256)))))
+        return st;
+    float* bt = static_cast<float*>(ds->scratch);
+    if (launch_transpose_f32(B, ldb, bt, K, K, N, ds->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return run_gemm(InKind::TF32, OutKind::F32, M, N, K, A, lda, bt, K, C, ldc, cfg, dev, ds, stream);
 }
 
-long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
 int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
                  int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
@@ -319,25 +354,7 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
     const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
     const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
-    const size_t need = static_cast<size_t>(a_bytes + b_bytes);
-    if (ds->scratch_bytes < need) {
-        if (ds->scratch) {
-            if (cudaDeviceSynchronize() != cudaSuccess) {
-                cudaGetLastError();
-                return TCL_ERR_LAUNCH;
-            }
-            cudaFree(ds->scratch);
-            ds->scratch = nullptr;
-            ds->scratch_bytes = 0;
-        }
-        void* p = nullptr;
-        if (cudaMalloc(&p, need) != cudaSuccess) {
-            cudaGetLastError();
-            return TCL_ERR_NO_MEMORY;
-        }
-        ds->scratch = p;
-        ds->scratch_bytes = need;
-    }
+    if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes)))) return st;
     uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
     uint8_t* b2 = a2 + a_bytes;
     if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, ds->sms, stream) != cudaSuccess ||

@@ -7,7 +7,8 @@
 // global→shared double buffering generalised to a multi-stage ring), rebuilt
 // for Blackwell:
 //   * warp 0 (producer): TMA 2-D tiled loads of the A tile (BM×BK, K-major)
-//     and the B tile (BK×BN, N-major) into stage s of a STAGES-deep ring,
+//     and the B tile (BK×BN; N-major for bf16, K-major for TF32, whose B the
+//     host path transposes first) into stage s of a STAGES-deep ring,
 //     128-byte swizzled; completion tracked by the full[s] mbarrier as
 //     transaction bytes. It waits on empty[s] before reusing a stage.
 //   * warp 1 (MMA issuer): one thread issues tcgen05.mma (kind::f16 or
@@ -99,9 +100,13 @@ struct KCfg {
     static constexpr int UMMA_K = InTraits<IK>::UMMA_K;
     static constexpr int KSUB = BK / UMMA_K;          // MMAs per k-block
     static constexpr int A_BYTES = BM * 128;          // BM rows × 128 B
-    static constexpr int B_BOX_N = 128 / ES;          // N columns per swizzle box
+    // B as stored in global memory: bf16 B is N-major (row-major K×N, read as
+    // boxes of 64 columns × BK rows); TF32 B arrives K-major (an N×K copy made
+    // by the host path), read like A as BN rows × 128 B.
+    static constexpr bool B_MN = (IK == InKind::BF16);
+    static constexpr int B_BOX_N = B_MN ? 128 / ES : BN;   // N columns per box
     static constexpr int B_BOXES = BN / B_BOX_N;
-    static constexpr int B_BOX_BYTES = BK * 128;      // BK rows × 128 B
+    static constexpr int B_BOX_BYTES = B_MN ? BK * 128 : BN * 128;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OUT_ES = (OK == OutKind::BF16) ? 2 : 4;
@@ -117,7 +122,7 @@ struct KCfg {
     // ring depth is measured under the same occupancy.
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t IDESC =
-        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, /*B MN-major*/ 1, BM, BN);
+        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
     static constexpr int THREADS = 192;
 
     static_assert(BN % B_BOX_N == 0, "BN must be a whole number of swizzle boxes");
@@ -308,10 +313,14 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
                     ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
                     ptx::tma_load_2d(sa, &tmA, full, kb * C::BK, mb * C::BM);
+                    if constexpr (C::B_MN) {
 #pragma unroll
-                    for (int b = 0; b < C::B_BOXES; ++b) {
-                        ptx::tma_load_2d(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
-                                         nb * BN + b * C::B_BOX_N, kb * C::BK);
+                        for (int b = 0; b < C::B_BOXES; ++b) {
+                            ptx::tma_load_2d(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
+                                             nb * BN + b * C::B_BOX_N, kb * C::BK);
+                        }
+                    } else {
+                        ptx::tma_load_2d(sa + C::A_BYTES, &tmB, full, kb * C::BK, nb * BN);
                     }
                 }
             }
@@ -357,9 +366,11 @@ __global__ void __launch_bounds__(192, 1)
                             // A: K-major rows of 128 B; step UMMA_K elements inside the swizzle row.
                             const uint64_t adesc =
                                 ptx::sdesc_sw128(sa + ks * C::UMMA_K * C::ES, 16, 1024);
-                            // B: N-major; step UMMA_K rows of 128 B; boxes of B_BOX_N columns apart.
+                            // B N-major: step UMMA_K rows of 128 B, boxes of B_BOX_N columns
+                            // B_BOX_BYTES apart. B K-major: exactly like A.
                             const uint64_t bdesc =
-                                ptx::sdesc_sw128(sb + ks * C::UMMA_K * 128, C::B_BOX_BYTES, 1024);
+                                C::B_MN ? ptx::sdesc_sw128(sb + ks * C::UMMA_K * 128, C::B_BOX_BYTES, 1024)
+                                        : ptx::sdesc_sw128(sb + ks * C::UMMA_K * C::ES, 16, 1024);
                             const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
                             if constexpr (IK == InKind::TF32)
                                 ptx::mma_tf32_ss(d_tmem, adesc, bdesc, C::IDESC, acc);

@@ -1,5 +1,9 @@
-// Exact int8 -> bf16 widening for the integer GEMM path.
+// Operand repacking passes that run before the GEMM kernel on some paths:
+//   * exact int8 -> bf16 widening (integer GEMM);
+//   * fp32 transpose K×N -> N×K (TF32 GEMM: the tensor cores take its B
+//     operand K-major).
 //
+// int8 -> bf16:
 // Every int8 value (|x| <= 128) has at most 8 significant bits, so it is
 // represented exactly by bf16; the bf16 pattern is the upper half of the
 // binary32 encoding of the integer. Rows are processed in 16-element chunks:
@@ -67,6 +71,47 @@ cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, lo
     if (blocks < 1) blocks = 1;
     s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         src, ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+    return cudaGetLastError();
+}
+
+// dst (cols × rows, leading dimension ld_dst) = transpose of src (rows × cols,
+// leading dimension ld_src), bit for bit. 32×32 tiles through shared memory
+// (one padding column against bank conflicts): coalesced reads of src rows,
+// coalesced writes of dst rows.
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ src,
+                                                             long long ld_src, float* __restrict__ dst,
+                                                             long long ld_dst, int rows, int cols) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int tiles_c = (cols + 31) / 32;
+    const long long tiles = static_cast<long long>((rows + 31) / 32) * tiles_c;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int r0 = static_cast<int>(t / tiles_c) * 32;
+        const int c0 = static_cast<int>(t % tiles_c) * 32;
+#pragma unroll
+        for (int i = ty; i < 32; i += 8) {
+            const int r = r0 + i, c = c0 + tx;
+            if (r < rows && c < cols) tile[i][tx] = src[r * ld_src + c];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = ty; i < 32; i += 8) {
+            const int c = c0 + i, r = r0 + tx;
+            if (c < cols && r < rows) dst[c * ld_dst + r] = tile[tx][i];
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
+                                 int cols, int sms, cudaStream_t stream) {
+    const long long tiles = static_cast<long long>((rows + 31) / 32) * ((cols + 31) / 32);
+    long long blocks = tiles;
+    const long long cap = static_cast<long long>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    transpose_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, ld_src, dst, ld_dst, rows,
+                                                                           cols);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,10 @@ cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, long long ld_dst,
                               int rows, int cols, int sms, cudaStream_t stream);
 
+// dst (cols × rows) = transpose of src (rows × cols), fp32, bit for bit.
+cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
+                                 int cols, int sms, cudaStream_t stream);
+
 // One entry per instantiated variant, so the host can validate a requested
 // configuration before it builds tensor maps.
 struct VariantInfo {

@@ -73,7 +73,9 @@ typedef enum {
     TCL_ERR_DEVICE_TIMEOUT = 7,  /* a bounded in-kernel wait ran out (see tcl_last_device_error) */
     TCL_ERR_CONFIG = 8,          /* tcl_config_t asks for a variant that is not built */
     TCL_ERR_NO_MEMORY = 9,       /* scratch allocation failed */
-    TCL_ERR_DEVICE = 10          /* current device is not an sm_103 GPU */
+    TCL_ERR_DEVICE = 10,         /* current device is not an sm_103 GPU */
+    TCL_ERR_STATIC_LIMIT = 11    /* gemm_s8_static: the problem needs more scratch than the fixed
+                                    TCL_S8_STATIC_SCRATCH_BYTES buffer holds */
 } tcl_status;
 
 typedef enum { TCL_OUT_F32 = 0, TCL_OUT_BF16 = 1 } tcl_out_t;
@@ -112,6 +114,40 @@ TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float*
  * added into int32 registers. */
 TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
             int ldc, cudaStream_t stream);
+
+/* Allocation-free int8 GEMM. (The pages have no counterpart: this is a
+ * library service, not part of the method.)
+ *
+ * Same operation, arguments, alignment rules and exact int32 result as
+ * gemm_s8, but the library allocates nothing: the bf16 copies of A and B are
+ * written into a fixed buffer that is part of the library's device image, a
+ * file-scope array of TCL_S8_STATIC_SCRATCH_BYTES (64 MiB). Every GPU on which
+ * the library's code is loaded holds that buffer until the process exits.
+ *
+ * Who needs it: callers that cannot call cudaMalloc at the point of use —
+ * a process whose device memory is already reserved by another allocator
+ * (a framework's caching pool that holds the free memory, so a fresh
+ * cudaMalloc fails or fragments it), and callers that must not trigger the
+ * device-wide synchronisation gemm_s8 performs when it has to grow its
+ * scratch (other streams on the device would stall behind it).
+ *
+ * Limit: the packed copies need 2·(M·⌈K⌉₈ + K·⌈N⌉₈) bytes, each block rounded
+ * up to 256 bytes; a larger problem returns TCL_ERR_STATIC_LIMIT before
+ * anything is enqueued (4096×4096×4096 fits exactly).
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * buffer's device address with cudaGetSymbolAddress and keeps it; make that
+ * first call before any stream capture. Later calls do no set-up.
+ *
+ * Sharing: every call on a device uses the same buffer, which keeps the last
+ * call's contents. Each call rewrites every byte the GEMM reads from it
+ * (including the zero padding of ragged rows), so stale contents never leak
+ * into a result. Calls whose GPU work overlaps (different streams without
+ * ordering between them) race on the buffer; calls on one stream are ordered
+ * and safe. Not thread-safe across host threads, like the rest of the API. */
+#define TCL_S8_STATIC_SCRATCH_BYTES (64ull << 20)
+TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb,
+                           int32_t* C, int ldc, cudaStream_t stream);
 
 /* Same operations with explicit knobs; cfg may be NULL (= all automatic). */
 TCL_API int gemm_bf16_ex(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C,

@@ -25,14 +25,14 @@ __all__ = ["gemm", "gemm_into", "plan", "lib", "Config", "last_device_error", "n
 STATUS = {
     0: "TCL_OK", 1: "TCL_ERR_NULL", 2: "TCL_ERR_DIMS", 3: "TCL_ERR_LD", 4: "TCL_ERR_ALIGN",
     5: "TCL_ERR_K_TOO_LARGE", 6: "TCL_ERR_LAUNCH", 7: "TCL_ERR_DEVICE_TIMEOUT", 8: "TCL_ERR_CONFIG",
-    9: "TCL_ERR_NO_MEMORY", 10: "TCL_ERR_DEVICE",
+    9: "TCL_ERR_NO_MEMORY", 10: "TCL_ERR_DEVICE", 11: "TCL_ERR_STATIC_LIMIT",
 }
 OUT_F32, OUT_BF16 = 0, 1
 IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",
                     "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms",
-                    "tcl_shutdown", "tcl_version")
+                    "tcl_shutdown", "tcl_version", "gemm_s8_static")
 
 
 class TclError(RuntimeError):
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         for name in ("gemm_tf32", "gemm_s8"):
             getattr(L, name).argtypes = [I, I, I, P, I, P, I, P, I, P]
             getattr(L, name + "_ex").argtypes = [I, I, I, P, I, P, I, P, I, CP, P]
+        L.gemm_s8_static.argtypes = [I, I, I, P, I, P, I, P, I, P]
         IP = ctypes.POINTER(ctypes.c_int)
         L.tcl_plan.argtypes = [I, I, I, I, I, CP, IP, IP, IP, IP, IP]
         L.tcl_status_string.argtypes = [I]

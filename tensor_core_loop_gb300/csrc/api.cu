@@ -367,6 +367,33 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
 }
 
 }  // namespace
+
+// Internal services for other translation units of the library.
+int device_context(int* dev, int* sms, unsigned int** status) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevState* ds = nullptr;
+    int st = current_device(dev, &ds);
+    if (st) return st;
+    *sms = ds->sms;
+    *status = ds->status;
+    return TCL_OK;
+}
+
+int tensor_map_uncached(const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1,
+                        uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int st = encode_fn();
+    if (st) return st;
+    const cuuint64_t dims[2] = {d0, d1};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {b0, b1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(out, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TCL_OK : TCL_ERR_LAUNCH;
+}
+
 }  // namespace tcl
 
 using namespace tcl;
@@ -457,6 +484,7 @@ const char* tcl_status_string(int status) {
         case TCL_ERR_CONFIG: return "requested configuration is not built";
         case TCL_ERR_NO_MEMORY: return "scratch allocation failed";
         case TCL_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        case TCL_ERR_STATIC_LIMIT: return "problem needs more scratch than the fixed static buffer holds";
         default: return "unknown status";
     }
 }

@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-sweep", action="store_true", help="skip the K sweep and the extra variants")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--ablation", action="store_true",
+                    help="instead of the contract line: the producer × ring-depth ablation, one JSON line per run")
+    ap.add_argument("--trace", action="store_true",
+                    help="instead of the contract line: per-shape load/MMA overlap from the in-kernel timeline")
     return ap.parse_args()
 
 
@@ -238,11 +242,103 @@ def time_flushed(fn, args_, iters, stream, torch, flush):
     return times[len(times) // 2]
 
 
+ABLATION = [  # (label, producer, ring depth): the pages' ladder, sync copy first, then TMA
+    ("sync, 1 stage", 1, 1), ("sync, 2 stages", 1, 2), ("sync, 4 stages", 1, 4),
+    ("TMA, 1 stage", 0, 1), ("TMA, 2 stages", 0, 2), ("TMA, 3 stages", 0, 3), ("TMA, 4 stages", 0, 4)]
+
+
+def compute_load_ratio(bm, bn, bk, esize):
+    """Flops per loaded byte of one k-block ("流水化 GPU 内核", step 2)."""
+    return 2.0 * bm * bn * bk / ((bm * bk + bk * bn) * esize)
+
+
+def run_ablation(args):
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    shapes = [(4096, 4096, 4096)] + [(mn, mn, k) for mn, k in SWEEP if (mn, k) != (4096, 4096)]
+    ratio = compute_load_ratio(128, 256, 64, 2)
+    ref_out = None
+    for (m, n, k) in shapes:
+        ah, bh = inputs.bf16_pair(m, n, k, seed=0)
+        a, b = ah.to(dev), bh.to(dev)
+        c = torch.empty((m, n), dtype=torch.float32, device=dev)
+        prev = None
+        for label, prod, stages in ABLATION:
+            cfg = tcl.Config(bn=256, stages=stages, producer=prod)
+            f = (lambda cfg=cfg: tcl.gemm_into(a, b, c, cfg=cfg))
+            for _ in range(3):
+                f()
+            ms = time_flushed(f, (), 20, stream, torch, flush)
+            if (m, n, k) == (4096, 4096, 4096):
+                if ref_out is None:
+                    ref_out = c.clone()
+                elif not torch.equal(c, ref_out):
+                    raise RuntimeError(f"ablation variant {label} changed the result bits")
+            tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+            line = {"ablation": label, "shape": f"{m}x{n}x{k}", "tflops": round(tf, 1), "us": round(ms * 1e3, 2),
+                    "delta_vs_prev_pct": None if prev is None else round(100.0 * (tf / prev - 1.0), 1),
+                    "compute_load_ratio": round(ratio, 1), "bn": 256, "stages": stages,
+                    "producer": "sync" if prod else "tma"}
+            prev = tf
+            print(json.dumps(line), flush=True)
+
+
+def run_trace(args):
+    import numpy as np
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shapes = [(mn, mn, k) for mn, k in SWEEP]
+    for (m, n, k) in shapes:
+        ah, bh = inputs.bf16_pair(m, n, k, seed=0)
+        a, b = ah.to(dev), bh.to(dev)
+        pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k)
+        bk = 64
+        tiles_cta0 = -(-pl["num_tiles"] // pl["grid"])
+        cap = min(4096, tiles_cta0 * -(-k // bk))
+        trace = torch.zeros(4 * cap, dtype=torch.int64, device=dev)
+        cfg = tcl.Config(trace=trace.data_ptr(), trace_cap=cap)
+        for _ in range(3):
+            trace.zero_()
+            tcl.gemm(a, b, cfg=cfg)
+        torch.cuda.synchronize()
+        t = trace.view(cap, 4).cpu().numpy().astype(np.int64)
+        issued, landed, mma, done = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
+        st = pl["stages"]
+        n_done = int((done > 0).sum())
+        idx = np.arange(max(0, min(n_done, cap - 1)))
+        overlap = float((issued[idx + 1] < done[idx]).mean()) if len(idx) else None
+        idx2 = np.arange(max(0, min(n_done, cap - (st - 1))))
+        ahead = float((issued[idx2 + st - 1] < done[idx2]).mean()) if len(idx2) and st > 1 else None
+        gaps = np.diff(mma)
+        print(json.dumps({
+            "trace": f"{m}x{n}x{k}", "bn": pl["bn"], "stages": st, "kblocks_traced": cap,
+            "load_issued_before_prev_mma_done": overlap,
+            "load_k_plus_stages_minus_1_before_mma_k_done": ahead,
+            "mean_load_latency_cycles": float((landed - issued).mean()),
+            "median_mma_issue_interval_cycles": float(np.median(gaps)) if len(gaps) else None,
+            "ideal_mma_cycles_per_kblock": 128 * pl["bn"] * bk * 2 / 8192,
+        }), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.ablation:
+        run_ablation(args)
+        return
+    if args.trace:
+        run_trace(args)
         return
 
     import torch

@@ -94,6 +94,14 @@ typedef struct {
                                       k-block of CTA 0: load issued, data landed, MMAs issued,
                                       MMAs done), or NULL */
     int trace_cap;                 /* k-blocks the trace buffer holds */
+    int producer;                  /* 0 (default): TMA bulk-tensor loads issued by one thread;
+                                      1: synchronous copy by four warps (ld.global -> registers ->
+                                      st.shared), the ablation's lower rung; bf16 only */
+    int debug_skip_kblock;         /* test hook, 0 = off. k > 0: CTA 0's TMA producer never loads
+                                      the (k-1)-th k-block of its walk, so the MMA warp's bounded
+                                      wait must run out; the call then reports
+                                      TCL_ERR_DEVICE_TIMEOUT through tcl_last_device_error() and
+                                      the outputs of that CTA are undefined */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)

@@ -57,6 +57,8 @@ class Config(ctypes.Structure):
         ("timeout_ns", ctypes.c_ulonglong),
         ("trace", ctypes.c_void_p),
         ("trace_cap", ctypes.c_int),
+        ("producer", ctypes.c_int),
+        ("debug_skip_kblock", ctypes.c_int),
     ]
 
 

@@ -38,7 +38,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 const VariantInfo kVariants[] = {
     TCL_GROUP_BF16_F32_BN256(TCL_VARIANT_INFO) TCL_GROUP_BF16_F32_BN128(TCL_VARIANT_INFO)
-        TCL_GROUP_BF16_MISC(TCL_VARIANT_INFO) TCL_GROUP_TF32(TCL_VARIANT_INFO)};
+        TCL_GROUP_BF16_MISC(TCL_VARIANT_INFO) TCL_GROUP_BF16_SYNC(TCL_VARIANT_INFO)
+            TCL_GROUP_TF32(TCL_VARIANT_INFO)};
 
 struct MapKey {
     int dev;
@@ -184,19 +185,19 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 }
 
 struct Plan {
-    int bn, stages, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
+    int bn, stages, prod, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
 };
 
-const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages) {
+const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod) {
     for (const auto& v : kVariants)
-        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages) return &v;
+        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages && v.prod == prod) return &v;
     return nullptr;
 }
 
-int deepest_stages(InKind ik, OutKind ok, int bn) {
+int deepest_stages(InKind ik, OutKind ok, int bn, int prod) {
     int best = 0;
     for (const auto& v : kVariants)
-        if (v.in == ik && v.out == ok && v.bn == bn && v.stages > best) best = v.stages;
+        if (v.in == ik && v.out == ok && v.bn == bn && v.prod == prod && v.stages > best) best = v.stages;
     return best;
 }
 
@@ -215,11 +216,14 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         }
     }
     if (bn != 128 && bn != 256) return TCL_ERR_CONFIG;
-    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn);
-    const VariantInfo* v = find_variant(ik, ok, bn, stages);
+    const int prod = cfg ? cfg->producer : PROD_TMA;
+    if (prod != PROD_TMA && prod != PROD_SYNC) return TCL_ERR_CONFIG;
+    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn, prod);
+    const VariantInfo* v = find_variant(ik, ok, bn, stages, prod);
     if (!v) return TCL_ERR_CONFIG;
     pl->bn = bn;
     pl->stages = stages;
+    pl->prod = prod;
     pl->smem = v->smem_bytes;
     pl->tiles_m = (M + kBM - 1) / kBM;
     pl->tiles_n = (N + bn - 1) / bn;
@@ -258,6 +262,7 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     a.out = ok;
     a.bn = pl.bn;
     a.stages = pl.stages;
+    a.prod = pl.prod;
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
@@ -283,6 +288,11 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     p.trace_cap = cfg && cfg->trace ? cfg->trace_cap : 0;
     p.C = C;
     p.ldc = ldc;
+    p.A = A;
+    p.lda = lda;
+    p.B = B;
+    p.ldb = ldb;
+    p.debug_skip_kb = cfg && cfg->debug_skip_kblock > 0 ? cfg->debug_skip_kblock - 1 : -1;
 
     bool found = false;
     cudaError_t err = cudaSuccess;
@@ -292,6 +302,7 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
         err = launch_group_bf16_f32_bn256(a, &found);
         if (!found) err = launch_group_bf16_f32_bn128(a, &found);
         if (!found) err = launch_group_bf16_misc(a, &found);
+        if (!found) err = launch_group_bf16_sync(a, &found);
     }
     if (!found) return TCL_ERR_CONFIG;
     if (err != cudaSuccess) {

@@ -82,7 +82,17 @@ struct GemmParams {
     int trace_cap;               // k-blocks the trace buffer holds
     void* C;                     // output base, for the ragged right edge only
     long long ldc;               // output leading dimension in elements
+    const void* A;               // operand bases, read directly by the synchronous producer
+    long long lda;
+    const void* B;
+    long long ldb;
+    int debug_skip_kb;           // test hook: CTA 0's TMA producer never loads this k-block (-1: off)
 };
+
+// Producer kinds: TMA bulk-tensor copies issued by one thread, or the
+// synchronous variant (four warps: ld.global into registers, st.shared into
+// the same swizzled layout, then an mbarrier arrive) used for the ablation.
+enum : int { PROD_TMA = 0, PROD_SYNC = 1 };
 
 constexpr int pow2_at_least(int x, int lo) {
     int p = lo;
@@ -90,8 +100,13 @@ constexpr int pow2_at_least(int x, int lo) {
     return p;
 }
 
-template <InKind IK, OutKind OK, int BN_, int STAGES_>
+template <InKind IK, OutKind OK, int BN_, int STAGES_, int PROD_ = PROD_TMA>
 struct KCfg {
+    static constexpr int PROD = PROD_;
+    static constexpr int P_WARPS = PROD == PROD_SYNC ? 4 : 1;   // producer warps
+    static constexpr int MMA_WARP = P_WARPS;                    // then the MMA warp
+    static constexpr int EPI_WARP0 = P_WARPS + 1;               // then four epilogue warps
+    static constexpr int FULL_ARRIVALS = PROD == PROD_SYNC ? 32 * P_WARPS : 1;
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
@@ -123,7 +138,7 @@ struct KCfg {
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t IDESC =
         ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 32 * (P_WARPS + 5);
 
     static_assert(BN % B_BOX_N == 0, "BN must be a whole number of swizzle boxes");
     static_assert(BN % EPI_COLS == 0, "BN must be a whole number of epilogue chunks");
@@ -132,6 +147,7 @@ struct KCfg {
     static_assert(STAGES >= 1 && 2 * STAGES + 5 <= 28, "barrier area");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(OK != OutKind::S32 || BN <= 128, "exact integer drain keeps BN int32 sums in registers");
+    static_assert(PROD == PROD_TMA || (IK == InKind::BF16 && B_MN), "synchronous producer: bf16 only");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
@@ -235,11 +251,96 @@ __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab
     ++count;
 }
 
-template <InKind IK, OutKind OK, int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+// Synchronous producer (the ablation's rung below TMA): the four producer
+// warps copy each stage through registers — all 16-byte global loads of the
+// stage first, then the stores into the same 128-byte-swizzled layout the TMA
+// would have written — then make their shared-memory writes visible to the
+// tensor core's (async) proxy and arrive on full[s]. Out-of-range rows,
+// columns and K are written as zeros, as the TMA's fill would.
+template <class C>
+__device__ __forceinline__ void sync_producer(const GemmParams& p, uint8_t* stage_base, uint32_t full0,
+                                              uint32_t empty0, volatile uint32_t* abort_flag, bool tracing) {
+    constexpr int PT = 32 * C::P_WARPS;
+    constexpr int A_PER = C::BM * 8 / PT;                  // 16-byte chunks per thread, A tile
+    constexpr int B_PER = C::B_BOXES * C::BK * 8 / PT;     // and B tile
+    static_assert(A_PER * PT == C::BM * 8 && B_PER * PT == C::B_BOXES * C::BK * 8, "chunk split");
+    const int pt = threadIdx.x;
+    const int lane = pt & 31;
+    const uint16_t* Ag = static_cast<const uint16_t*>(p.A);
+    const uint16_t* Bg = static_cast<const uint16_t*>(p.B);
+    uint32_t it = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            const uint32_t s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1u;
+            bool got = true;
+            if (lane == 0)
+                got = wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                                   DEV_TIMEOUT_PRODUCER);
+            if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) return;
+            if (tracing && pt == 0) {
+                const uint64_t now = ptx::clock64();
+                if (it >= C::STAGES && it - C::STAGES < (uint32_t)p.trace_cap)
+                    p.trace[4 * (it - C::STAGES) + 3] = now;
+                if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;
+            }
+            const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+            const uint32_t sb = sa + C::A_BYTES;
+            uint4 ra[A_PER], rb[B_PER];
+#pragma unroll
+            for (int i = 0; i < A_PER; ++i) {
+                const int c = pt + i * PT, row = c >> 3, j = c & 7;
+                const int gm = mb * C::BM + row, gk = kb * C::BK + j * 8;
+                ra[i] = (gm < p.M && gk < p.K)
+                            ? __ldg(reinterpret_cast<const uint4*>(Ag + static_cast<long long>(gm) * p.lda + gk))
+                            : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < B_PER; ++i) {
+                const int c = pt + i * PT, box = c / (C::BK * 8), r = c % (C::BK * 8);
+                const int k = r >> 3, j = r & 7;
+                const int gk = kb * C::BK + k, gn = nb * C::BN + box * C::B_BOX_N + j * 8;
+                const uint16_t* src = Bg + static_cast<long long>(gk) * p.ldb + gn;
+                if (gk < p.K && gn + 8 <= p.N) {
+                    rb[i] = __ldg(reinterpret_cast<const uint4*>(src));
+                } else if (gk < p.K && gn < p.N) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t lo = gn + 2 * t < p.N ? src[2 * t] : 0u;
+                        const uint32_t hi = gn + 2 * t + 1 < p.N ? src[2 * t + 1] : 0u;
+                        w[t] = lo | (hi << 16);
+                    }
+                    rb[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    rb[i] = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < A_PER; ++i) {
+                const int c = pt + i * PT, row = c >> 3, j = c & 7;
+                st_shared_v4(sa + row * 128 + ((j ^ (row & 7)) << 4), ra[i].x, ra[i].y, ra[i].z, ra[i].w);
+            }
+#pragma unroll
+            for (int i = 0; i < B_PER; ++i) {
+                const int c = pt + i * PT, box = c / (C::BK * 8), r = c % (C::BK * 8);
+                const int k = r >> 3, j = r & 7;
+                st_shared_v4(sb + box * C::B_BOX_BYTES + k * 128 + ((j ^ (k & 7)) << 4), rb[i].x, rb[i].y,
+                             rb[i].z, rb[i].w);
+            }
+            ptx::fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
+            ptx::mbar_arrive(full0 + 8 * s);
+        }
+    }
+}
+
+template <InKind IK, OutKind OK, int BN, int STAGES, int PROD>
+__global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using C = KCfg<IK, OK, BN, STAGES>;
+    using C = KCfg<IK, OK, BN, STAGES, PROD>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries of the shared window.
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -261,7 +362,7 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full0 + 8 * s, 1);
+            ptx::mbar_init(full0 + 8 * s, C::FULL_ARRIVALS);
             ptx::mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -277,7 +378,7 @@ __global__ void __launch_bounds__(192, 1)
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmC);
     }
-    if (warp == 1) {
+    if (warp == C::MMA_WARP) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), C::TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -287,7 +388,10 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem_base = *tmem_holder;
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
 
-    if (warp == 0) {
+    if (warp < C::P_WARPS && PROD == PROD_SYNC) {
+        // ------------------------------------------------ producer (synchronous, ablation)
+        sync_producer<C>(p, stage_base, full0, empty0, abort_flag, tracing);
+    } else if (warp == 0) {
         // ------------------------------------------------ producer (TMA)
         if (lane == 0) {
             uint32_t it = 0;
@@ -311,6 +415,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t full = full0 + 8 * s;
                     const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+                    if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) continue;
                     ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
                     ptx::tma_load_2d(sa, &tmA, full, kb * C::BK, mb * C::BM);
                     if constexpr (C::B_MN) {
@@ -332,7 +437,7 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t it = 0, unit = 0;
@@ -391,9 +496,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (four warps)
         const int q = warp & 3;   // TMEM lane quarter this warp may read
-        uint8_t* slab_pair = staging + (warp - 2) * 2 * C::SLAB_BYTES;
+        uint8_t* slab_pair = staging + (warp - C::EPI_WARP0) * 2 * C::SLAB_BYTES;
         int store_count = 0;
         uint32_t unit = 0;
         bool ok = true;
@@ -487,7 +592,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------ teardown
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == C::MMA_WARP) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }

@@ -13,6 +13,7 @@ struct LaunchArgs {
     OutKind out;
     int bn;
     int stages;
+    int prod;   // PROD_TMA or PROD_SYNC
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
     int grid;
@@ -24,6 +25,7 @@ struct LaunchArgs {
 cudaError_t launch_group_bf16_f32_bn256(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_f32_bn128(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_misc(const LaunchArgs& a, bool* found);
+cudaError_t launch_group_bf16_sync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
 // int8 -> bf16 widening (exact) into a packed row-major buffer with ld_dst
@@ -42,14 +44,16 @@ struct VariantInfo {
     OutKind out;
     int bn;
     int stages;
+    int prod;
     int smem_bytes;
+    int threads;
 };
 int variant_table(const VariantInfo** table);
 
-template <InKind IK, OutKind OK, int BN, int STAGES>
+template <InKind IK, OutKind OK, int BN, int STAGES, int PROD>
 cudaError_t launch_variant(const LaunchArgs& a) {
-    using C = KCfg<IK, OK, BN, STAGES>;
-    auto kern = gemm_tc_kernel<IK, OK, BN, STAGES>;
+    using C = KCfg<IK, OK, BN, STAGES, PROD>;
+    auto kern = gemm_tc_kernel<IK, OK, BN, STAGES, PROD>;
     // The shared-memory opt-in is per function and device: set it once per device.
     static bool attr_done[64] = {};
     int dev = 0;
@@ -64,21 +68,24 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     return cudaGetLastError();
 }
 
-// The instantiated variants, grouped by translation unit (compiled in parallel).
+// The instantiated variants (input, output, BN, ring depth, producer),
+// grouped by translation unit so that the groups compile in parallel.
 #define TCL_GROUP_BF16_F32_BN256(X) \
-    X(BF16, F32, 256, 1) X(BF16, F32, 256, 2) X(BF16, F32, 256, 3) X(BF16, F32, 256, 4)
+    X(BF16, F32, 256, 1, 0) X(BF16, F32, 256, 2, 0) X(BF16, F32, 256, 3, 0) X(BF16, F32, 256, 4, 0)
 #define TCL_GROUP_BF16_F32_BN128(X) \
-    X(BF16, F32, 128, 1) X(BF16, F32, 128, 2) X(BF16, F32, 128, 4) X(BF16, F32, 128, 6)
-#define TCL_GROUP_BF16_MISC(X) X(BF16, BF16, 256, 4) X(BF16, BF16, 128, 6) X(BF16, S32, 128, 6)
-#define TCL_GROUP_TF32(X) X(TF32, F32, 256, 4) X(TF32, F32, 128, 6)
+    X(BF16, F32, 128, 1, 0) X(BF16, F32, 128, 2, 0) X(BF16, F32, 128, 4, 0) X(BF16, F32, 128, 6, 0)
+#define TCL_GROUP_BF16_MISC(X) X(BF16, BF16, 256, 4, 0) X(BF16, BF16, 128, 6, 0) X(BF16, S32, 128, 6, 0)
+#define TCL_GROUP_BF16_SYNC(X) X(BF16, F32, 256, 1, 1) X(BF16, F32, 256, 2, 1) X(BF16, F32, 256, 4, 1)
+#define TCL_GROUP_TF32(X) X(TF32, F32, 256, 4, 0) X(TF32, F32, 128, 6, 0)
 
-#define TCL_VARIANT_INFO(IK, OK, BN, ST) \
-    {InKind::IK, OutKind::OK, BN, ST, KCfg<InKind::IK, OutKind::OK, BN, ST>::SMEM_BYTES},
+#define TCL_VARIANT_INFO(IK, OK, BN, ST, PR)                                               \
+    {InKind::IK, OutKind::OK, BN, ST, PR, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::SMEM_BYTES, \
+     KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS},
 
-#define TCL_VARIANT_CASE(IK, OK, BN, ST)                                                   \
-    if (a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST) {      \
-        *found = true;                                                                     \
-        return launch_variant<InKind::IK, OutKind::OK, BN, ST>(a);                         \
+#define TCL_VARIANT_CASE(IK, OK, BN, ST, PR)                                                           \
+    if (a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \
+        *found = true;                                                                                 \
+        return launch_variant<InKind::IK, OutKind::OK, BN, ST, PR>(a);                                 \
     }
 
 }  // namespace tcl

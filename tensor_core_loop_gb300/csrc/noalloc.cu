@@ -79,6 +79,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     a.out = OutKind::S32;
     a.bn = bn;
     a.stages = stages;
+    a.prod = PROD_TMA;
     a.grid = grid;
     a.stream = stream;
     if ((st = tensor_map_uncached(a2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda2 * 2, 64, 128, &a.tmA)))
@@ -104,6 +105,11 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.trace_cap = 0;
     p.C = C;
     p.ldc = ldc;
+    p.A = a2;
+    p.lda = lda2;
+    p.B = b2;
+    p.ldb = ldb2;
+    p.debug_skip_kb = -1;
 
     if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, sms, stream) != cudaSuccess ||
         launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, sms, stream) != cudaSuccess) {

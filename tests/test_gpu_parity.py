@@ -139,6 +139,12 @@ def test_bf16_each_variant(oracle_mod, bn, stages):
     bf16_case(oracle_mod, 384, 512, 640, seed=9, cfg=tcl.Config(bn=bn, stages=stages))
 
 
+@pytest.mark.parametrize("stages", [1, 2, 4])
+def test_bf16_sync_producer(oracle_mod, stages):
+    bf16_case(oracle_mod, 384, 512, 640, seed=9, cfg=tcl.Config(bn=256, stages=stages, producer=1))
+    bf16_case(oracle_mod, 130, 261, 200, seed=10, cfg=tcl.Config(bn=256, stages=stages, producer=1), ldc=264)
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""
@@ -152,6 +158,9 @@ def test_variants_bitwise_identical():
                     cfg = tcl.Config(bn=bn, stages=st, one_cta_per_tile=one_per_tile, max_ctas=max_ctas,
                                      group_m=3 if max_ctas else 0)
                     outs.append(run(a, b, cfg=cfg, canary=False))
+        if bn == 256:   # the synchronous producer feeds the same MMA sequence
+            for st in (1, 2, 4):
+                outs.append(run(a, b, cfg=tcl.Config(bn=256, stages=st, producer=1), canary=False))
         for o in outs[1:]:
             assert torch.equal(o, outs[0])
 

@@ -1,0 +1,68 @@
+"""Failure detection on the GPU without a fault: every mbarrier wait in the
+kernel is bounded. A test hook makes CTA 0's producer skip one k-block, so the
+MMA warp waits for data that never arrives; the wait must run out, record the
+code in the device status word, let the kernel return, and leave the context
+usable for the next call."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import tensor_core_loop_gb300 as tcl
+from tensor_core_loop_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tcl.lib()
+    tcl.last_device_error()   # start from a clear status word
+
+
+def test_bounded_wait_runs_out_and_context_survives():
+    a, b = inputs.bf16_pair(1024, 1024, 1024, seed=3)
+    a, b = a.to(DEV), b.to(DEV)
+    c = torch.zeros((1024, 1024), dtype=torch.float32, device=DEV)
+    cfg = tcl.Config(timeout_ns=50_000_000, debug_skip_kblock=3)
+    tcl.gemm_into(a, b, c, cfg=cfg)              # the launch itself succeeds
+    st, code = tcl.last_device_error()
+    assert st == 7, f"expected TCL_ERR_DEVICE_TIMEOUT, got {tcl.STATUS.get(st, st)}"
+    assert code in (1, 2, 3, 4)                  # which role gave up first
+    assert tcl.last_device_error() == (0, 0)     # reading clears the word
+    # the context is still usable and the next call is correct
+    ref = tcl.gemm(a, b)
+    again = tcl.gemm(a, b)
+    torch.cuda.synchronize()
+    assert torch.equal(ref, again)
+    assert tcl.last_device_error() == (0, 0)
+
+
+def test_trace_shows_loads_ahead_of_mma():
+    """The per-k-block timeline of CTA 0: each block's load is issued before its
+    data lands, the MMAs are issued after, and the loads of later blocks are in
+    flight while earlier blocks' MMAs run (the software pipeline)."""
+    M, N, K = 128, 256, 64 * 48
+    a, b = inputs.bf16_pair(M, N, K, seed=4)
+    a, b = a.to(DEV), b.to(DEV)
+    cap = 48
+    trace = torch.zeros(4 * cap, dtype=torch.int64, device=DEV)
+    cfg = tcl.Config(bn=256, stages=4, trace=trace.data_ptr(), trace_cap=cap)
+    c = tcl.gemm(a, b, cfg=cfg)
+    torch.cuda.synchronize()
+    t = trace.view(cap, 4).cpu().numpy().astype(np.int64)
+    issued, landed, mma, done = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
+    assert (issued > 0).all() and (landed > 0).all() and (mma > 0).all()
+    assert (landed >= issued).all() and (mma >= landed).all()
+    n = cap - 4   # the last ring's worth of blocks has no later reuse to stamp "done"
+    assert (done[:n] >= mma[:n]).all()
+    # load of block k+1 issued before MMA of block k completed: overlap
+    overlap = (issued[1:n + 1] < done[:n]).mean()
+    assert overlap > 0.9, overlap
+    ref = tcl.gemm(a, b)
+    assert torch.equal(c, ref)

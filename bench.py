@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ablation", action="store_true",
                     help="instead of the contract line: the producer × ring-depth ablation, one JSON line per run")
+    ap.add_argument("--peak", action="store_true",
+                    help="instead of the contract line: the tensor-pipe rate probe (MMA only) per operand layout")
     ap.add_argument("--trace", action="store_true",
                     help="instead of the contract line: per-shape load/MMA overlap from the in-kernel timeline")
     return ap.parse_args()
@@ -288,6 +290,42 @@ def run_ablation(args):
             print(json.dumps(line), flush=True)
 
 
+def trace_stats(t, stages, bn, num_kb):
+    """Pipeline statistics of one CTA's per-k-block stamps (issued, landed, MMAs issued, MMAs done)."""
+    import numpy as np
+    issued, landed, mma, done = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
+    n = len(t)
+    nd = int((done > 0).sum())
+    out = {"kblocks_traced": n, "ideal_mma_cycles_per_kblock": 128 * bn * 64 * 2 / 8192}
+    idx = np.arange(max(0, min(nd, n - 1)))
+    out["load_issued_before_prev_mma_done"] = float((issued[idx + 1] < done[idx]).mean()) if len(idx) else None
+    idx2 = np.arange(max(0, min(nd, n - (stages - 1))))
+    out["load_k_plus_stages_minus_1_before_mma_k_done"] = (
+        float((issued[idx2 + stages - 1] < done[idx2]).mean()) if len(idx2) and stages > 1 else None)
+    issue = mma - landed                     # MMA warp: issue 4 MMAs + commit
+    out["mma_issue_cycles"] = {"p50": float(np.median(issue)), "mean": float(issue.mean())}
+    if n > 1:
+        gap = landed[1:] - mma[:-1]          # MMA warp: waiting for the next stage's barrier
+        out["mma_wait_cycles"] = {"p50": float(np.median(gap)), "mean": float(gap.mean()),
+                                  "p90": float(np.percentile(gap, 90))}
+    lat = landed - issued
+    out["load_latency_cycles"] = {"mean": float(lat.mean()), "p50": float(np.median(lat)),
+                                  "p90": float(np.percentile(lat, 90))}
+    if nd >= 2:
+        d = done[:nd]
+        busy_iv = np.diff(d)
+        out["mma_done_interval_cycles"] = {"mean": float(busy_iv.mean()), "p50": float(np.median(busy_iv)),
+                                           "p90": float(np.percentile(busy_iv, 90))}
+        # tensor pipe idle before block k: its data landed after block k-1 had finished
+        starve = np.maximum(0, landed[1:nd] - d[:nd - 1])
+        span = float(d[nd - 1] - landed[0])
+        out["pipe_starved_frac"] = float(starve.sum()) / span if span > 0 else None
+        tile_starts = np.arange(num_kb, nd, num_kb)
+        out["starved_cycles_at_tile_starts"] = float(starve[tile_starts - 1].sum()) if len(tile_starts) else 0.0
+        out["busy_frac_of_span"] = (nd * out["ideal_mma_cycles_per_kblock"]) / span if span > 0 else None
+    return out
+
+
 def run_trace(args):
     import numpy as np
     import torch
@@ -299,33 +337,85 @@ def run_trace(args):
     for (m, n, k) in shapes:
         ah, bh = inputs.bf16_pair(m, n, k, seed=0)
         a, b = ah.to(dev), bh.to(dev)
-        pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k)
-        bk = 64
-        tiles_cta0 = -(-pl["num_tiles"] // pl["grid"])
-        cap = min(4096, tiles_cta0 * -(-k // bk))
-        trace = torch.zeros(4 * cap, dtype=torch.int64, device=dev)
-        cfg = tcl.Config(trace=trace.data_ptr(), trace_cap=cap)
-        for _ in range(3):
-            trace.zero_()
-            tcl.gemm(a, b, cfg=cfg)
-        torch.cuda.synchronize()
-        t = trace.view(cap, 4).cpu().numpy().astype(np.int64)
-        issued, landed, mma, done = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
-        st = pl["stages"]
-        n_done = int((done > 0).sum())
-        idx = np.arange(max(0, min(n_done, cap - 1)))
-        overlap = float((issued[idx + 1] < done[idx]).mean()) if len(idx) else None
-        idx2 = np.arange(max(0, min(n_done, cap - (st - 1))))
-        ahead = float((issued[idx2 + st - 1] < done[idx2]).mean()) if len(idx2) and st > 1 else None
-        gaps = np.diff(mma)
-        print(json.dumps({
-            "trace": f"{m}x{n}x{k}", "bn": pl["bn"], "stages": st, "kblocks_traced": cap,
-            "load_issued_before_prev_mma_done": overlap,
-            "load_k_plus_stages_minus_1_before_mma_k_done": ahead,
-            "mean_load_latency_cycles": float((landed - issued).mean()),
-            "median_mma_issue_interval_cycles": float(np.median(gaps)) if len(gaps) else None,
-            "ideal_mma_cycles_per_kblock": 128 * pl["bn"] * bk * 2 / 8192,
-        }), flush=True)
+        for pair in ((1, 2) if m >= 4096 else (1,)):
+            cfg0 = tcl.Config(cta_pair=pair)
+            pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k, cfg0)
+            num_kb = -(-k // 64)
+            clusters = pl["grid"] // (2 if pl["cta_pair"] == 2 else 1)
+            tiles_cta0 = -(-pl["num_tiles"] // clusters)
+            cap = min(8192, tiles_cta0 * num_kb)
+            trace = torch.zeros(4 * cap + 4, dtype=torch.int64, device=dev)
+            cfg = tcl.Config(cta_pair=pair, trace=trace.data_ptr(), trace_cap=cap)
+            for _ in range(3):
+                trace.zero_()
+                tcl.gemm(a, b, cfg=cfg)
+            torch.cuda.synchronize()
+            tt = trace.cpu().numpy().astype(np.int64)
+            t = tt[:4 * cap].reshape(cap, 4)
+            c0, g0, c1, g1 = tt[4 * cap:]
+            line = {"trace": f"{m}x{n}x{k}", "sm_mhz_in_kernel": round(1e3 * (c1 - c0) / max(1, g1 - g0), 1), "cta_pair": pl["cta_pair"], "bn": pl["bn"], "stages": pl["stages"],
+                    "tiles_cta0": tiles_cta0}
+            line.update(trace_stats(t, pl["stages"], pl["bn"] if pl["cta_pair"] == 1 else 256, num_kb))
+            print(json.dumps(line), flush=True)
+
+
+def run_peak(args):
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sms = tcl.num_sms()
+    sampler = ClockSampler(0)
+    sampler.start()
+    rows = []
+    combos = [(0, 256, 1), (0, 256, 0), (0, 128, 1), (0, 128, 0), (1, 256, 0), (1, 128, 0)]
+    for kind, n, b_mn, flags in [c + (f,) for c in combos for f in (0, 1, 2, 3)]:
+        tcl.mma_peak(kind, n, b_mn, iters=512, flags=flags)          # warm-up
+        cyc, rate, ms = tcl.mma_peak(kind, n, b_mn, iters=16384, flags=flags)
+        k = 16 if kind == 0 else 8
+        flops = 2.0 * 128 * n * k * 16384 * sms
+        rows.append({"peak": "bf16" if kind == 0 else "tf32", "n": n, "b_major": "MN" if b_mn else "K",
+                     "one_accumulator": bool(flags & 1), "walk_operands": bool(flags & 2),
+                     "flop_per_clk_per_sm": round(rate, 1), "cycles_per_mma": round(max(cyc) / 16384, 2),
+                     "tflops_all_sms": round(flops / (ms * 1e-3) / 1e12, 1), "sms": sms})
+    clocks = sampler.stop()
+    for r in rows:
+        r["clocks"] = clocks
+        print(json.dumps(r), flush=True)
+
+
+def in_kernel_clock_mhz(tcl, torch, sets, stream, steps):
+    """SM clock inside the GEMM under the timed workload: back-to-back launches with CTA 0
+    stamping %clock64 and %globaltimer at its start and end; median over the last launches."""
+    import ctypes
+    cap = 1
+    bufs = [torch.zeros(4 * cap + 4, dtype=torch.int64, device=sets[0][0].device) for _ in range(8)]
+    L = tcl.lib()
+    mhz = []
+    for i in range(steps):
+        buf = bufs[i % len(bufs)]
+        cfg = tcl.Config(trace=buf.data_ptr(), trace_cap=cap)
+        a, b, c = sets[i % len(sets)]
+        st = L.gemm_bf16_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, tcl.OUT_F32,
+                            ctypes.byref(cfg), ctypes.c_void_p(stream.cuda_stream))
+        if st:
+            return None
+    torch.cuda.synchronize()
+    for buf in bufs:
+        c0, g0, c1, g1 = buf[4 * cap:].cpu().tolist()
+        if g1 > g0:
+            mhz.append(1e3 * (c1 - c0) / (g1 - g0))
+    mhz.sort()
+    return mhz[len(mhz) // 2] if mhz else None
+
+
+def measured_mma_rate(tcl):
+    """flop/clk/SM of the bf16 N=256 tensor pipe, from the MMA-only probe (None on failure)."""
+    try:
+        tcl.mma_peak(0, 256, 1, iters=256)
+        return tcl.mma_peak(0, 256, 1, iters=4096, flags=2)[1]
+    except Exception:
+        return None
 
 
 def main():
@@ -339,6 +429,9 @@ def main():
         return
     if args.trace:
         run_trace(args)
+        return
+    if args.peak:
+        run_peak(args)
         return
 
     import torch
@@ -400,6 +493,9 @@ def main():
     st, code = tcl.last_device_error()
     if st:
         raise RuntimeError(f"device status {st} (code {code}) after the timed region")
+    kernel_mhz = None
+    if rank == 0:
+        kernel_mhz = in_kernel_clock_mhz(tcl, torch, sets, stream, steps=min(args.steps, 2000))
     ms_step = ms_total / args.steps
     if rank == 0:
         print(f"[bench] {args.steps} steps, {ms_step * 1e3:.2f} us/step, "
@@ -490,6 +586,11 @@ def main():
     peak = float(peaks["bf16_tflops"])
     sms = tcl.num_sms()
     sm_mhz = clocks.get("sm_mhz") if clocks else None
+    rate = measured_mma_rate(tcl) or 8192.0
+    clk = kernel_mhz or sm_mhz
+    cc_peak = (sms * rate * clk * 1e6 / 1e12) if clk else None
+    if clocks is not None:
+        clocks["sm_mhz_in_kernel"] = kernel_mhz
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -503,8 +604,11 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": recorded_traffic("gemm_bf16_f32_4096"),
                      "peak_source": f"{peak_src} bf16_tflops (cuBLAS 8192^3 burst)",
-                     "clock_corrected_peak": (sms * 8192 * sm_mhz * 1e6 / 1e12) if sm_mhz else None,
-                     "frac_clock_corrected": (achieved / (sms * 8192 * sm_mhz * 1e6 / 1e12)) if sm_mhz else None},
+                     "mma_rate_flop_per_clk_per_sm": rate,
+                     "clock_corrected_peak": cc_peak,
+                     "clock_corrected_peak_def": "SMs x probe-measured flop/clk/SM x SM clock measured inside "
+                                                 "the kernel (%clock64 / %globaltimer) on the timed workload",
+                     "frac_clock_corrected": (achieved / cc_peak) if cc_peak else None},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps,

@@ -90,13 +90,17 @@ typedef struct {
     int group_m;                   /* raster group height in tiles (0: 8) */
     int max_ctas;                  /* cap on resident CTAs for the persistent grid (0: all SMs) */
     unsigned long long timeout_ns; /* bound on every in-kernel wait (0: 1 s) */
-    unsigned long long* trace;     /* device buffer of 4*trace_cap uint64 (clock64 stamps per
-                                      k-block of CTA 0: load issued, data landed, MMAs issued,
-                                      MMAs done), or NULL */
+    unsigned long long* trace;     /* device buffer of 4*trace_cap + 4 uint64, or NULL: %clock64
+                                      stamps per k-block of CTA 0 (load issued, data landed,
+                                      MMAs issued, MMAs done), then CTA 0's %clock64 and
+                                      %globaltimer (ns) at its start and at its end */
     int trace_cap;                 /* k-blocks the trace buffer holds */
     int producer;                  /* 0 (default): TMA bulk-tensor loads issued by one thread;
                                       1: synchronous copy by four warps (ld.global -> registers ->
                                       st.shared), the ablation's lower rung; bf16 only */
+    int cta_pair;                  /* 0: automatic; 1: one SM per tile (tcgen05 cta_group::1);
+                                      2: two SMs per 256×256 tile (cta_group::2; bf16 in,
+                                      fp32/bf16 out, TMA producer) */
     int debug_skip_kblock;         /* test hook, 0 = off. k > 0: CTA 0's TMA producer never loads
                                       the (k-1)-th k-block of its walk, so the MMA warp's bounded
                                       wait must run out; the call then reports
@@ -167,9 +171,24 @@ TCL_API int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8
 
 /* The launch the automatic path would make for this problem, without
  * launching: in_kind 0 = bf16, 1 = tf32, 2 = int8. Any output pointer may be
- * NULL. Returns a tcl_status (argument checks as above, pointers not needed). */
+ * NULL; *cta_pair receives 1 (one SM per tile) or 2 (two SMs per tile).
+ * With cfg->max_ctas > 0 no device is queried (max_ctas stands for the SM
+ * count). Returns a tcl_status (argument checks as above, pointers not needed). */
 TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, int* bn,
-             int* stages, int* grid, int* num_tiles, int* smem_bytes);
+                     int* stages, int* grid, int* num_tiles, int* smem_bytes, int* cta_pair);
+
+/* Tensor-pipe rate probe (measurement, not part of the GEMM): `grid` CTAs
+ * (one per SM) each issue `iters` back-to-back tcgen05.mma of shape
+ * M=128 × N=n × K=16 (bf16, in_kind 0) or K=8 (TF32, in_kind 1) on operands
+ * already in shared memory (B K-major, or N-major if b_mn = 1; bf16 only),
+ * and write the %clock64 cycles from the first issue to the completion of the
+ * last into cycles[blockIdx] (device buffer of `grid` entries; 0 if the
+ * bounded wait ran out). flop/clk/SM = 2·128·n·K·iters / cycles.
+ * flags bit 0: chain every MMA into one accumulator, as the MMAs of one GEMM
+ * tile are (default: alternate two independent accumulators); bit 1: walk
+ * the operand addresses like a GEMM k-loop (4 k-slices × 4 ring stages). */
+TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
+                         unsigned long long* cycles, cudaStream_t stream);
 
 /* Human-readable text for a tcl_status; never NULL. */
 TCL_API const char* tcl_status_string(int status);

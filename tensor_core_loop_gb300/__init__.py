@@ -32,7 +32,7 @@ IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",
                     "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms",
-                    "tcl_shutdown", "tcl_version", "gemm_s8_static")
+                    "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak")
 
 
 class TclError(RuntimeError):
@@ -58,6 +58,7 @@ class Config(ctypes.Structure):
         ("trace", ctypes.c_void_p),
         ("trace_cap", ctypes.c_int),
         ("producer", ctypes.c_int),
+        ("cta_pair", ctypes.c_int),
         ("debug_skip_kblock", ctypes.c_int),
     ]
 
@@ -84,8 +85,9 @@ def lib() -> ctypes.CDLL:
             getattr(L, name).argtypes = [I, I, I, P, I, P, I, P, I, P]
             getattr(L, name + "_ex").argtypes = [I, I, I, P, I, P, I, P, I, CP, P]
         L.gemm_s8_static.argtypes = [I, I, I, P, I, P, I, P, I, P]
+        L.tcl_mma_peak.argtypes = [I, I, I, I, I, I, P, P]
         IP = ctypes.POINTER(ctypes.c_int)
-        L.tcl_plan.argtypes = [I, I, I, I, I, CP, IP, IP, IP, IP, IP]
+        L.tcl_plan.argtypes = [I, I, I, I, I, CP, IP, IP, IP, IP, IP, IP]
         L.tcl_status_string.argtypes = [I]
         L.tcl_status_string.restype = ctypes.c_char_p
         L.tcl_last_device_error.argtypes = [P, IP]
@@ -107,12 +109,34 @@ def num_sms() -> int:
 
 def plan(in_kind: int, out: int, M: int, N: int, K: int, cfg: Config | None = None) -> dict:
     """The launch the library would make (tile N, ring depth, grid, tiles, shared memory)."""
-    vals = [ctypes.c_int(0) for _ in range(5)]
+    vals = [ctypes.c_int(0) for _ in range(6)]
     st = lib().tcl_plan(in_kind, out, M, N, K, ctypes.byref(cfg) if cfg else None,
                         *[ctypes.byref(v) for v in vals])
     if st:
         raise TclError(st, "tcl_plan")
-    return dict(zip(("bn", "stages", "grid", "num_tiles", "smem_bytes"), (v.value for v in vals)))
+    return dict(zip(("bn", "stages", "grid", "num_tiles", "smem_bytes", "cta_pair"), (v.value for v in vals)))
+
+
+def mma_peak(in_kind: int = IN_BF16, n: int = 256, b_mn: int = 0, iters: int = 4096, grid: int | None = None,
+             flags: int = 0):
+    """Runs the tensor-pipe probe on every SM; returns (cycles per CTA as a list, flop/clk/SM of the
+    slowest CTA, elapsed ms of the launch measured with CUDA events)."""
+    import torch
+    grid = grid or num_sms()
+    cyc = torch.zeros(grid, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    st = lib().tcl_mma_peak(in_kind, n, b_mn, flags, iters, grid, cyc.data_ptr(), ctypes.c_void_p(s.cuda_stream))
+    e1.record(s)
+    if st:
+        raise TclError(st, "tcl_mma_peak")
+    e1.synchronize()
+    c = cyc.cpu().tolist()
+    k = 16 if in_kind == IN_BF16 else 8
+    worst = max(c) if min(c) > 0 else 0
+    rate = 2.0 * 128 * n * k * iters / worst if worst else 0.0
+    return c, rate, e0.elapsed_time(e1)
 
 
 def last_device_error(stream=None) -> tuple[int, int]:

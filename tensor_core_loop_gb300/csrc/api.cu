@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -27,6 +28,7 @@ struct DevState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
+    int pair_clusters[8] = {};   // resident two-CTA clusters per pair variant (0: not yet queried)
     unsigned int* status = nullptr;
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
@@ -39,7 +41,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 const VariantInfo kVariants[] = {
     TCL_GROUP_BF16_F32_BN256(TCL_VARIANT_INFO) TCL_GROUP_BF16_F32_BN128(TCL_VARIANT_INFO)
         TCL_GROUP_BF16_MISC(TCL_VARIANT_INFO) TCL_GROUP_BF16_SYNC(TCL_VARIANT_INFO)
-            TCL_GROUP_TF32(TCL_VARIANT_INFO)};
+            TCL_GROUP_TF32(TCL_VARIANT_INFO) TCL_GROUP_PAIR(TCL_PAIR_INFO)};
 
 struct MapKey {
     int dev;
@@ -185,27 +187,64 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 }
 
 struct Plan {
-    int bn, stages, prod, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
+    int bn, stages, prod, pair, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
 };
 
-const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod) {
+const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod, int pair) {
     for (const auto& v : kVariants)
-        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages && v.prod == prod) return &v;
+        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages && v.prod == prod && v.pair == pair)
+            return &v;
     return nullptr;
 }
 
-int deepest_stages(InKind ik, OutKind ok, int bn, int prod) {
+int deepest_stages(InKind ik, OutKind ok, int bn, int prod, int pair) {
     int best = 0;
     for (const auto& v : kVariants)
-        if (v.in == ik && v.out == ok && v.bn == bn && v.prod == prod && v.stages > best) best = v.stages;
+        if (v.in == ik && v.out == ok && v.bn == bn && v.prod == prod && v.pair == pair && v.stages > best)
+            best = v.stages;
     return best;
 }
 
-// Chooses the tile shape, ring depth and grid. `sms` is the SM count.
-int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cfg, int sms, Plan* pl) {
+
+// Chooses the tile shape, ring depth, one- or two-SM kernel and grid.
+// `sms` is the SM count; `pair_clusters(v)` returns how many two-CTA clusters
+// of pair variant v fit on the device at once.
+template <class PairClusters>
+int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cfg, int sms,
+              PairClusters pair_clusters, Plan* pl) {
     const int bk = 128 / in_bytes(ik);
+    const int prod = cfg ? cfg->producer : PROD_TMA;
+    if (prod != PROD_TMA && prod != PROD_SYNC) return TCL_ERR_CONFIG;
+    const int want_pair = cfg ? cfg->cta_pair : 0;
+    if (want_pair < 0 || want_pair > 2) return TCL_ERR_CONFIG;
     int bn = cfg ? cfg->bn : 0;
-    if (bn == 0) {
+    int pair = 0;
+    const bool pair_capable = ik == InKind::BF16 && ok != OutKind::S32 && prod == PROD_TMA;
+    if (want_pair == 2) {
+        if (!pair_capable || (bn != 0 && bn != 256 && bn != 224)) return TCL_ERR_CONFIG;
+        pair = 1;
+    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages)) {
+        // Two SMs per 256×256 tile halve each SM's bytes per flop; use them when
+        // there are at least as many pair tiles as pairs of SMs.
+        const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
+        pair = tiles_pair >= sms / 2 ? 1 : 0;
+    }
+    if (pair) {
+        if (bn == 0) {
+            // Pair tile width: the fewest column-units of MMA work on the busiest
+            // pair of SMs, ceil(tiles / pairs) × width (fp32 C can use 224).
+            bn = 256;
+            if (ok == OutKind::F32) {
+                const int pairs = std::max(1, (cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms) / 2);
+                auto cost = [&](int w) {
+                    const long long t = static_cast<long long>((M + 255) / 256) * ((N + w - 1) / w);
+                    return ((t + pairs - 1) / pairs) * w;
+                };
+                const int want_st = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, 224, prod, 1);
+                if (find_variant(ik, ok, 224, want_st, prod, 1) && cost(224) < cost(256)) bn = 224;
+            }
+        }
+    } else if (bn == 0) {
         if (ok == OutKind::S32) {
             bn = 128;
         } else {
@@ -215,25 +254,30 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             bn = tiles256 >= sms ? 256 : 128;
         }
     }
-    if (bn != 128 && bn != 256) return TCL_ERR_CONFIG;
-    const int prod = cfg ? cfg->producer : PROD_TMA;
-    if (prod != PROD_TMA && prod != PROD_SYNC) return TCL_ERR_CONFIG;
-    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn, prod);
-    const VariantInfo* v = find_variant(ik, ok, bn, stages, prod);
+    if (bn != 128 && bn != 256 && !(pair && bn == 224)) return TCL_ERR_CONFIG;
+    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn, prod, pair);
+    const VariantInfo* v = find_variant(ik, ok, bn, stages, prod, pair);
     if (!v) return TCL_ERR_CONFIG;
     pl->bn = bn;
     pl->stages = stages;
     pl->prod = prod;
+    pl->pair = pair;
     pl->smem = v->smem_bytes;
-    pl->tiles_m = (M + kBM - 1) / kBM;
+    const int bm = pair ? 2 * kBM : kBM;
+    pl->tiles_m = (M + bm - 1) / bm;
     pl->tiles_n = (N + bn - 1) / bn;
     const long long tiles = static_cast<long long>(pl->tiles_m) * pl->tiles_n;
-    if (tiles > 0x7FFFFFFFll) return TCL_ERR_DIMS;
+    if (tiles > 0x3FFFFFFFll) return TCL_ERR_DIMS;
     pl->num_tiles = static_cast<int>(tiles);
     pl->num_kb = (K + bk - 1) / bk;
     pl->kb_per_unit = ok == OutKind::S32 ? kS32UnitK / bk : pl->num_kb;
     pl->group_m = cfg && cfg->group_m > 0 ? cfg->group_m : 8;
-    if (cfg && cfg->one_cta_per_tile) {
+    if (pair) {
+        int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / 2 : pair_clusters(v);
+        if (clusters < 1) return cfg && cfg->max_ctas > 0 ? TCL_ERR_CONFIG : TCL_ERR_LAUNCH;
+        if (cfg && cfg->one_cta_per_tile) clusters = pl->num_tiles;
+        pl->grid = 2 * (pl->num_tiles < clusters ? pl->num_tiles : clusters);
+    } else if (cfg && cfg->one_cta_per_tile) {
         pl->grid = pl->num_tiles;
     } else {
         int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
@@ -243,12 +287,25 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     return TCL_OK;
 }
 
+// Resident pair clusters for a pair variant on the current device, queried once.
+int device_pair_clusters(DevState* ds, const VariantInfo* v) {
+    int idx = 0;
+    for (const auto& w : kVariants) {
+        if (&w == v) break;
+        if (w.pair) ++idx;
+    }
+    if (idx >= 8) return 0;
+    if (ds->pair_clusters[idx] == 0) ds->pair_clusters[idx] = pair_max_clusters(v->out, v->bn, v->stages);
+    return ds->pair_clusters[idx];
+}
+
 // Builds tensor maps and launches one GEMM over device operands.
 int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long long lda, const void* B,
              long long ldb, void* C, long long ldc, const tcl_config_t* cfg, int dev, DevState* ds,
              cudaStream_t stream) {
     Plan pl;
-    int st = make_plan(ik, ok, M, N, K, cfg, ds->sms, &pl);
+    int st = make_plan(ik, ok, M, N, K, cfg, ds->sms,
+                       [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, &pl);
     if (st) return st;
     const int ies = in_bytes(ik), oes = out_bytes(ok);
     const int bk = 128 / ies;
@@ -263,6 +320,7 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     a.bn = pl.bn;
     a.stages = pl.stages;
     a.prod = pl.prod;
+    a.pair = pl.pair;
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
@@ -296,7 +354,9 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
 
     bool found = false;
     cudaError_t err = cudaSuccess;
-    if (ik == InKind::TF32) {
+    if (pl.pair) {
+        err = launch_group_pair(a, &found);
+    } else if (ik == InKind::TF32) {
         err = launch_group_tf32(a, &found);
     } else {
         err = launch_group_bf16_f32_bn256(a, &found);
@@ -442,7 +502,7 @@ int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, i
 }
 
 int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, int* bn, int* stages,
-             int* grid, int* num_tiles, int* smem_bytes) {
+             int* grid, int* num_tiles, int* smem_bytes, int* cta_pair) {
     if (M < 1 || N < 1 || K < 1) return TCL_ERR_DIMS;
     InKind ik;
     OutKind ok;
@@ -460,25 +520,27 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
     } else {
         return TCL_ERR_CONFIG;
     }
-    int sms = 0;
+    Plan pl;
+    int st;
     if (cfg && cfg->max_ctas > 0) {
-        sms = cfg->max_ctas;   // lets the planner run without a device
+        // planning without a device: max_ctas stands for the SM count (pairs: max_ctas / 2)
+        st = make_plan(ik, ok, M, N, K, cfg, cfg->max_ctas, [](const VariantInfo*) { return 0; }, &pl);
     } else {
         std::lock_guard<std::mutex> lock(g_mu);
         int dev;
         DevState* ds;
-        int st = current_device(&dev, &ds);
+        st = current_device(&dev, &ds);
         if (st) return st;
-        sms = ds->sms;
+        st = make_plan(ik, ok, M, N, K, cfg, ds->sms,
+                       [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, &pl);
     }
-    Plan pl;
-    int st = make_plan(ik, ok, M, N, K, cfg, sms, &pl);
     if (st) return st;
     if (bn) *bn = pl.bn;
     if (stages) *stages = pl.stages;
     if (grid) *grid = pl.grid;
     if (num_tiles) *num_tiles = pl.num_tiles;
     if (smem_bytes) *smem_bytes = pl.smem;
+    if (cta_pair) *cta_pair = pl.pair ? 2 : 1;
     return TCL_OK;
 }
 

@@ -387,6 +387,10 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
+    if (tracing && threadIdx.x == 0) {   // SM clock and wall clock at the start of CTA 0's work
+        p.trace[4 * p.trace_cap + 0] = ptx::clock64();
+        p.trace[4 * p.trace_cap + 1] = ptx::globaltimer_ns();
+    }
 
     if (warp < C::P_WARPS && PROD == PROD_SYNC) {
         // ------------------------------------------------ producer (synchronous, ablation)
@@ -440,7 +444,18 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
     } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, unit = 0;
+            // Descriptors of stage 0; a stage and a k-slice are fixed offsets (in
+            // 16-byte units) in the start-address field, so the issue loop adds
+            // constants instead of rebuilding descriptors (one thread issues every
+            // MMA: its loop, not the tensor pipe, would otherwise set the pace).
+            const uint32_t stage0 = ptx::smem_u32(stage_base);
+            const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
+            const uint64_t bdesc0 = C::B_MN ? ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024)
+                                            : ptx::sdesc_sw128(stage0 + C::A_BYTES, 16, 1024);
+            constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
+            constexpr uint64_t B_STEP = C::B_MN ? C::UMMA_K * 128 / 16 : C::UMMA_K * C::ES / 16;
+            constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
+            uint32_t it = 0, unit = 0, s = 0, ph = 0;   // (s, ph): ring slot and phase of k-block `it`
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_unit, ++unit) {
@@ -455,8 +470,6 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                     const uint32_t d_tmem = tmem_base + buf * BN;
                     const int kb1 = min(kb0 + p.kb_per_unit, p.num_kb);
                     for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                        const uint32_t s = it % STAGES;
-                        const uint32_t ph = (it / STAGES) & 1u;
                         if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.timeout_ns, p.status,
                                           DEV_TIMEOUT_MMA_FULL)) {
                             ok = false;
@@ -464,26 +477,25 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                         }
                         ptx::tc_fence_after();
                         if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
-                        const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
-                        const uint32_t sb = sa + C::A_BYTES;
+                        // A: K-major rows of 128 B, a k-slice steps UMMA_K elements along the row.
+                        // B N-major: a k-slice steps UMMA_K rows of 128 B (boxes B_BOX_BYTES apart,
+                        // the descriptor's leading offset); B K-major: as A.
+                        const uint64_t ad = adesc0 + s * S_STEP;
+                        const uint64_t bd = bdesc0 + s * S_STEP;
 #pragma unroll
                         for (int ks = 0; ks < C::KSUB; ++ks) {
-                            // A: K-major rows of 128 B; step UMMA_K elements inside the swizzle row.
-                            const uint64_t adesc =
-                                ptx::sdesc_sw128(sa + ks * C::UMMA_K * C::ES, 16, 1024);
-                            // B N-major: step UMMA_K rows of 128 B, boxes of B_BOX_N columns
-                            // B_BOX_BYTES apart. B K-major: exactly like A.
-                            const uint64_t bdesc =
-                                C::B_MN ? ptx::sdesc_sw128(sb + ks * C::UMMA_K * 128, C::B_BOX_BYTES, 1024)
-                                        : ptx::sdesc_sw128(sb + ks * C::UMMA_K * C::ES, 16, 1024);
                             const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
                             if constexpr (IK == InKind::TF32)
-                                ptx::mma_tf32_ss(d_tmem, adesc, bdesc, C::IDESC, acc);
+                                ptx::mma_tf32_ss(d_tmem, ad + ks * A_STEP, bd + ks * B_STEP, C::IDESC, acc);
                             else
-                                ptx::mma_f16_ss(d_tmem, adesc, bdesc, C::IDESC, acc);
+                                ptx::mma_f16_ss(d_tmem, ad + ks * A_STEP, bd + ks * B_STEP, C::IDESC, acc);
                         }
                         ptx::mma_commit(empty0 + 8 * s);   // stage s free once these MMAs finish
                         if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
                     }
                     if (!ok) break;
                     ptx::mma_commit(accf0 + 8 * buf);      // accumulator ready for the epilogue
@@ -592,6 +604,10 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
     // ------------------------------------------------ teardown
     ptx::tc_fence_before();
     __syncthreads();
+    if (tracing && threadIdx.x == 0) {   // ... and at its end: their ratio is the SM clock in the kernel
+        p.trace[4 * p.trace_cap + 2] = ptx::clock64();
+        p.trace[4 * p.trace_cap + 3] = ptx::globaltimer_ns();
+    }
     if (warp == C::MMA_WARP) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);

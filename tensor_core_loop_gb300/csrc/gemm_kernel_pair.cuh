@@ -1,0 +1,314 @@
+// Two-SM variant of the pipelined GEMM: a cluster of two CTAs on two SMs
+// computes one 256×256 output tile with tcgen05.mma.cta_group::2.
+//
+// Same pipeline as gemm_kernel.cuh (TMA producer → S-deep mbarrier ring →
+// single-thread MMA issue → TMEM → TMA-store epilogue, persistent grouped
+// raster), with the work of one tile split over the pair:
+//   * each CTA loads only its own 128 rows of A and its own half (128
+//     columns) of the B tile, so each SM moves 32 KB per 64-deep k-block
+//     instead of 48 KB for the same 128×256 share of the MMA work;
+//   * both CTAs' loads count their bytes on the even (leader) CTA's full[s]
+//     barrier, whose producer announces the pair's total;
+//   * the leader's MMA warp issues the pair MMA (M=256: each SM's tensor core
+//     produces its own 128 rows into its own TMEM, reading B from both SMs)
+//     and commits empty[s] and acc_full[b] to both CTAs at once (multicast);
+//   * both CTAs' epilogues drain their own TMEM and release the accumulator
+//     on the leader's acc_empty[b] (8 arrivals: 4 warps × 2 CTAs).
+// Waits are bounded as in the one-SM kernel; a role that gives up raises the
+// abort flag of both CTAs.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace tcl {
+
+template <OutKind OK, int BN_, int STAGES_>
+struct PairCfg {
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BM = 256;                   // rows per pair tile (128 per SM)
+    static constexpr int BN = BN_;                   // columns per pair tile (each SM supplies BN/2 of B)
+    static constexpr int ROWS = 128;                 // rows of A and C per CTA
+    static constexpr int BK = 64;                    // bf16: one 128-byte swizzle row
+    static constexpr int UMMA_K = 16;
+    static constexpr int KSUB = BK / UMMA_K;
+    static constexpr int A_BYTES = ROWS * 128;       // 16 KB
+    static constexpr int B_BOX_N = 64;
+    // this CTA's half of B in whole 64-column boxes (at BN=224 the second box
+    // also brings 16 columns the MMA does not read)
+    static constexpr int B_BOXES = (BN / 2 + B_BOX_N - 1) / B_BOX_N;
+    static constexpr int B_BOX_BYTES = BK * 128;         // 8 KB
+    static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
+    static constexpr int PAIR_TX = 2 * STAGE_BYTES;         // bytes the leader's full[s] expects
+    static constexpr int OUT_ES = (OK == OutKind::BF16) ? 2 : 4;
+    static constexpr int EPI_COLS = 128 / OUT_ES;
+    static constexpr int EPI_CHUNKS = BN / EPI_COLS;
+    static constexpr int SLAB_BYTES = 32 * 128;
+    static constexpr int STAGING_BYTES = 4 * 2 * SLAB_BYTES;
+    static constexpr int ACC_STRIDE = 256;           // accumulator b starts at TMEM column b·256
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_USED = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
+    static constexpr uint32_t IDESC = ptx::make_idesc(1, 1, /*A K-major*/ 0, /*B MN-major*/ 1, BM, BN);
+    static constexpr int THREADS = 192;
+    static constexpr uint16_t BOTH = 0x3;            // multicast mask: CTA ranks 0 and 1
+
+    static_assert(OK != OutKind::S32, "exact integer mode runs on the one-SM kernel");
+    static_assert(BN % 32 == 0 && BN <= 256 && BN % EPI_COLS == 0, "pair tile width");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
+    static_assert(2 * STAGES + 5 <= 28, "barrier area");
+};
+
+// Bounded wait that, on giving up, raises the abort flag of this CTA and of its peer.
+__device__ __forceinline__ bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                  uint32_t peer_abort, unsigned long long timeout_ns,
+                                                  unsigned int* status, unsigned int code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1u;
+            ptx::st_cluster_u32(peer_abort, 1u);
+            atomicCAS(status, 0u, code);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void spin_ns(unsigned long long ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < ns) {
+    }
+}
+
+template <OutKind OK, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    using C = PairCfg<OK, BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* stage_base = smem;
+    uint8_t* staging = smem + STAGES * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STAGING_BYTES);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile uint32_t* abort_flag = tmem_holder + 1;
+
+    const uint32_t full0 = ptx::smem_u32(bars);
+    const uint32_t empty0 = ptx::smem_u32(bars + STAGES);
+    const uint32_t accf0 = ptx::smem_u32(bars + 2 * STAGES);
+    const uint32_t acce0 = ptx::smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t drain_bar = ptx::smem_u32(bars + 2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();   // 0: leader (issues the pair MMAs), 1: peer
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);    // leader's: its producer's arrival + both CTAs' bytes
+            ptx::mbar_init(empty0 + 8 * s, 1);   // the leader's multicast commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf0 + 8 * b, 1);    // the leader's multicast commit
+            ptx::mbar_init(acce0 + 8 * b, 8);    // leader's: 4 epilogue warps × 2 CTAs
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {   // one warp in each CTA of the pair allocates, collectively
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_holder), C::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const uint32_t full_leader0 = ptx::mapa_shared(full0, 0);
+    const uint32_t acce_leader0 = ptx::mapa_shared(acce0, 0);
+    const uint32_t peer_abort = ptx::mapa_shared(ptx::smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u);
+    const int cluster = blockIdx.x >> 1;
+    const int clusters = gridDim.x >> 1;
+    const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
+    if (tracing && threadIdx.x == 0) {   // SM clock and wall clock at the start of CTA 0's work
+        p.trace[4 * p.trace_cap + 0] = ptx::clock64();
+        p.trace[4 * p.trace_cap + 1] = ptx::globaltimer_ns();
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer (TMA), both CTAs
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters) {
+                int mb, nb;
+                tile_coords(tile, p, mb, nb);
+                const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
+                const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded_pair(empty0 + 8 * s, ph ^ 1u, abort_flag, peer_abort, p.timeout_ns,
+                                           p.status, DEV_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    if (tracing) {
+                        const uint64_t now = ptx::clock64();
+                        if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap)
+                            p.trace[4 * (it - STAGES) + 3] = now;
+                        if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;
+                    }
+                    if (leader) ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::PAIR_TX);
+                    const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+                    const uint32_t fb = full_leader0 + 8 * s;
+                    ptx::tma_load_2d_pair(sa, &tmA, fb, kb * C::BK, row);
+#pragma unroll
+                    for (int b = 0; b < C::B_BOXES; ++b)
+                        ptx::tma_load_2d_pair(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, fb, col + b * C::B_BOX_N,
+                                              kb * C::BK);
+                }
+            }
+            if (!ok) spin_ns(200000);   // copies issued before the abort land within microseconds
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader CTA only)
+        if (leader && lane == 0) {
+            // Stage-0 descriptors; stages and k-slices are constant offsets of the
+            // start-address field (16-byte units), added in the issue loop.
+            const uint32_t stage0 = ptx::smem_u32(stage_base);
+            const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
+            const uint64_t bdesc0 = ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024);
+            constexpr uint64_t A_STEP = C::UMMA_K * 2 / 16;
+            constexpr uint64_t B_STEP = C::UMMA_K * 128 / 16;
+            constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
+            uint32_t it = 0, unit = 0, s = 0, ph = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters, ++unit) {
+                const uint32_t buf = unit & 1u;
+                const uint32_t uph = (unit >> 1) & 1u;
+                if (!wait_bounded_pair(acce0 + 8 * buf, uph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                       DEV_TIMEOUT_MMA_ACC)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * C::ACC_STRIDE;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    if (!wait_bounded_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                           DEV_TIMEOUT_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
+                    const uint64_t ad = adesc0 + s * S_STEP;
+                    const uint64_t bd = bdesc0 + s * S_STEP;
+#pragma unroll
+                    for (int ks = 0; ks < C::KSUB; ++ks)
+                        ptx::mma_f16_ss_pair(d_tmem, ad + ks * A_STEP, bd + ks * B_STEP, C::IDESC,
+                                             (kb > 0 || ks > 0) ? 1u : 0u);
+                    ptx::mma_commit_pair_multicast(empty0 + 8 * s, C::BOTH);
+                    if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair_multicast(accf0 + 8 * buf, C::BOTH);
+            }
+            if (!ok) {
+                ptx::mma_commit_pair_multicast(drain_bar, 0x1);
+                wait_drain(drain_bar, 0, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5), both CTAs
+        const int q = warp & 3;
+        uint8_t* slab_pair = staging + (warp - 2) * 2 * C::SLAB_BYTES;
+        int store_count = 0;
+        uint32_t unit = 0;
+        bool ok = true;
+        for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters, ++unit) {
+            int mb, nb;
+            tile_coords(tile, p, mb, nb);
+            const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
+            const uint32_t buf = unit & 1u;
+            const uint32_t uph = (unit >> 1) & 1u;
+            bool got = true;
+            if (lane == 0)
+                got = wait_bounded_pair(accf0 + 8 * buf, uph, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                        DEV_TIMEOUT_EPILOGUE);
+            if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
+#pragma unroll 1
+            for (int c = 0; c < C::EPI_CHUNKS; ++c) {
+                __syncwarp();
+                uint32_t v[32];
+                if constexpr (OK == OutKind::F32) {
+                    ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    ptx::tmem_ld_wait(v);
+                } else {
+                    uint32_t lo[32], hi[32];
+                    ptx::tmem_ld_32x32b_x32(tbase + c * 64, lo);
+                    ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, hi);
+                    ptx::tmem_ld_wait(lo);
+                    ptx::tmem_ld_wait(hi);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(lo[2 * i]),
+                                                                 __uint_as_float(lo[2 * i + 1]));
+                        v[i] = *reinterpret_cast<uint32_t*>(&t);
+                        __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(hi[2 * i]),
+                                                                 __uint_as_float(hi[2 * i + 1]));
+                        v[16 + i] = *reinterpret_cast<uint32_t*>(&u);
+                    }
+                }
+                if (c == C::EPI_CHUNKS - 1) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
+                }
+                store_slab<C::SLAB_BYTES, C::OUT_ES>(&tmC, slab_pair, store_count, v, lane, nb * C::BN + c * C::EPI_COLS,
+                                                     row0, p);
+            }
+        }
+        if (lane == 0) ptx::bulk_wait<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tracing && threadIdx.x == 0) {   // ... and at its end: their ratio is the SM clock in the kernel
+        p.trace[4 * p.trace_cap + 2] = ptx::clock64();
+        p.trace[4 * p.trace_cap + 3] = ptx::globaltimer_ns();
+    }
+    ptx::cluster_sync();   // no CTA frees TMEM or exits while its peer may still signal it
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tcl

@@ -1,0 +1,84 @@
+// Instantiates the two-SM (cta_group::2) GEMM variants and launches them as
+// clusters of two CTAs.
+#include "launch.cuh"
+
+namespace tcl {
+namespace {
+
+template <OutKind OK, int BN, int STAGES>
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    using C = PairCfg<OK, BN, STAGES>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <OutKind OK, int BN, int STAGES>
+cudaError_t prepare() {
+    using C = PairCfg<OK, BN, STAGES>;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES);
+    if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return err;
+}
+
+template <OutKind OK, int BN, int STAGES>
+cudaError_t launch_pair(const LaunchArgs& a) {
+    cudaError_t err = prepare<OK, BN, STAGES>();
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES>(a.grid, a.stream, attr);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES>, a.tmA, a.tmB, a.tmC, a.p);
+}
+
+template <OutKind OK, int BN, int STAGES>
+int max_clusters() {
+    if (prepare<OK, BN, STAGES>() != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES>(2, 0, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace
+
+#define TCL_PAIR_CASE(OK, BN, ST)                                                   \
+    if (a.out == OutKind::OK && a.bn == BN && a.stages == ST) {                     \
+        *found = true;                                                              \
+        return launch_pair<OutKind::OK, BN, ST>(a);                                 \
+    }
+
+cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
+    *found = false;
+    if (!a.pair || a.in != InKind::BF16 || a.prod != PROD_TMA) return cudaErrorNotSupported;
+    TCL_GROUP_PAIR(TCL_PAIR_CASE)
+    return cudaErrorNotSupported;
+}
+
+#define TCL_PAIR_OCC(OK, BN, ST) \
+    if (out == OutKind::OK && bn == BN && stages == ST) return max_clusters<OutKind::OK, BN, ST>();
+
+int pair_max_clusters(OutKind out, int bn, int stages) {
+    TCL_GROUP_PAIR(TCL_PAIR_OCC)
+    return 0;
+}
+
+}  // namespace tcl

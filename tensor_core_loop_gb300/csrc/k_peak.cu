@@ -1,0 +1,135 @@
+// MMA-only peak probe: back-to-back tcgen05.mma on operands already in shared
+// memory, no loads, no epilogue. It measures the tensor pipe's own rate per SM
+// (cycles per MMA instruction, from %clock64 around the issue loop and the
+// final commit), which is the denominator of the clock-corrected roofline.
+#include <cuda_runtime.h>
+
+#include "launch.cuh"
+#include "tcl_gemm.h"
+
+namespace tcl {
+namespace {
+
+// align slack, 4 stages of A (128 rows × 128 B) and B (256 rows × 128 B), barrier
+constexpr int kPeakStages = 4;
+constexpr int kPeakA = 16384, kPeakB = 32768;
+constexpr int kPeakSmem = 1024 + kPeakStages * (kPeakA + kPeakB) + 256;
+constexpr int kPeakRequest = 232448 - 1024;
+
+// flags: bit 0 — chain every MMA into one accumulator (as a GEMM tile does)
+//        instead of alternating two; bit 1 — walk the operand addresses like a
+//        GEMM k-loop (4 k-slices × 4 stages) instead of reusing one k-slice.
+template <int N, bool TF32, bool B_MN>
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, unsigned long long timeout_ns,
+                                                          unsigned long long* cycles, unsigned int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sa0 = ptx::smem_u32(smem);
+    const uint32_t sb0 = sa0 + kPeakStages * kPeakA;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPeakStages * (kPeakA + kPeakB));
+    uint32_t* holder = reinterpret_cast<uint32_t*>(bar + 1);
+    // operands: a fixed pseudo-random bf16/fp32 pattern of moderate magnitude
+    for (int i = threadIdx.x; i < kPeakStages * (kPeakA + kPeakB) / 4; i += blockDim.x) {
+        const uint32_t h = (static_cast<uint32_t>(i) * 2654435761u) >> 9;
+        reinterpret_cast<uint32_t*>(smem)[i] = TF32 ? (0x3F000000u | (h & 0x7FFFFFu)) : (0x3F003F00u | (h & 0x007F007Fu));
+    }
+    ptx::fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(bar), 1);
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        ptx::tmem_alloc(ptx::smem_u32(holder), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *holder;
+    if (threadIdx.x == 0) {
+        constexpr uint32_t fmt = TF32 ? 2u : 1u;
+        // A K-major; B K-major (N rows of 128 B) or N-major (N/64 column groups of
+        // 16 K-rows × 128 B, 2 KB apart), as in one k-slice of a GEMM tile
+        constexpr uint32_t idesc = ptx::make_idesc(fmt, fmt, 0, B_MN ? 1u : 0u, 128, N);
+        const bool chain = flags & 1, walk = flags & 2;
+        constexpr int KS = TF32 ? 4 : 4;   // k-slices per 128-byte row
+        const uint64_t t0 = ptx::clock64();
+        for (int i = 0; i < iters; ++i) {
+            const int ks = walk ? (i % KS) : 0;
+            const int st = walk ? ((i / KS) % kPeakStages) : 0;
+            const uint32_t sa = sa0 + st * kPeakA, sb = sb0 + st * kPeakB;
+            const uint64_t adesc = ptx::sdesc_sw128(sa + ks * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? ptx::sdesc_sw128(sb + ks * (TF32 ? 8 : 16) * 128, 2048, 1024)
+                                        : ptx::sdesc_sw128(sb + ks * 32, 16, 1024);
+            const uint32_t d = tmem + ((!chain && (i & 1)) ? N : 0);
+            const uint32_t acc = i >= (chain ? 1 : 2) ? 1u : 0u;
+            if constexpr (TF32)
+                ptx::mma_tf32_ss(d, adesc, bdesc, idesc, acc);
+            else
+                ptx::mma_f16_ss(d, adesc, bdesc, idesc, acc);
+        }
+        ptx::mma_commit(ptx::smem_u32(bar));
+        const uint64_t t_start = ptx::globaltimer_ns();
+        bool done = false;
+        while (!(done = ptx::mbar_try_wait(ptx::smem_u32(bar), 0))) {
+            if (ptx::globaltimer_ns() - t_start > timeout_ns) break;
+        }
+        const uint64_t t1 = ptx::clock64();
+        cycles[blockIdx.x] = done ? (t1 - t0) : 0ull;
+        if (!done) atomicCAS(status, 0u, static_cast<unsigned int>(DEV_TIMEOUT_MMA_FULL));
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int N, bool TF32, bool B_MN>
+cudaError_t launch_peak(int iters, int flags, int grid, unsigned long long* cycles, unsigned int* status,
+                        cudaStream_t stream) {
+    auto kern = mma_peak_kernel<N, TF32, B_MN>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPeakRequest);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, 128, kPeakRequest, stream>>>(iters, flags, 1000000000ull, cycles, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int device_context(int* dev, int* sms, unsigned int** status);   // api.cu
+
+}  // namespace tcl
+
+using namespace tcl;
+
+extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
+                                    unsigned long long* cycles, cudaStream_t stream) {
+    if (!cycles) return TCL_ERR_NULL;
+    if (iters < 2 || grid < 1 || (n != 128 && n != 256) || (in_kind != 0 && in_kind != 1) ||
+        (b_mn != 0 && b_mn != 1) || (in_kind == 1 && b_mn))
+        return TCL_ERR_DIMS;
+    static_assert(kPeakSmem <= kPeakRequest, "probe fits its shared memory request");
+    if (flags < 0 || flags > 3) return TCL_ERR_CONFIG;
+    int dev = 0, sms = 0;
+    unsigned int* status = nullptr;
+    int st = device_context(&dev, &sms, &status);
+    if (st) return st;
+    cudaError_t err;
+    if (in_kind == 1)
+        err = n == 256 ? launch_peak<256, true, false>(iters, flags, grid, cycles, status, stream)
+                       : launch_peak<128, true, false>(iters, flags, grid, cycles, status, stream);
+    else if (b_mn)
+        err = n == 256 ? launch_peak<256, false, true>(iters, flags, grid, cycles, status, stream)
+                       : launch_peak<128, false, true>(iters, flags, grid, cycles, status, stream);
+    else
+        err = n == 256 ? launch_peak<256, false, false>(iters, flags, grid, cycles, status, stream)
+                       : launch_peak<128, false, false>(iters, flags, grid, cycles, status, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return TCL_OK;
+}

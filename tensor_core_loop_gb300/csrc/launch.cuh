@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_pair.cuh"
 
 namespace tcl {
 
@@ -14,6 +15,7 @@ struct LaunchArgs {
     int bn;
     int stages;
     int prod;   // PROD_TMA or PROD_SYNC
+    int pair;   // 1: two-SM kernel (cluster of two CTAs per 256×256 tile)
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
     int grid;
@@ -26,6 +28,10 @@ cudaError_t launch_group_bf16_f32_bn256(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_f32_bn128(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_misc(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_sync(const LaunchArgs& a, bool* found);
+cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
+// Largest number of two-CTA clusters of the given pair variant that can be
+// resident at once on the current device (0 on error).
+int pair_max_clusters(OutKind out, int bn, int stages);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
 // int8 -> bf16 widening (exact) into a packed row-major buffer with ld_dst
@@ -47,6 +53,7 @@ struct VariantInfo {
     int prod;
     int smem_bytes;
     int threads;
+    int pair;
 };
 int variant_table(const VariantInfo** table);
 
@@ -80,10 +87,16 @@ cudaError_t launch_variant(const LaunchArgs& a) {
 
 #define TCL_VARIANT_INFO(IK, OK, BN, ST, PR)                                               \
     {InKind::IK, OutKind::OK, BN, ST, PR, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::SMEM_BYTES, \
-     KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS},
+     KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS, 0},
+
+// Two-SM variants (bf16 in, TMA producer, 256-row pair tiles): output, tile width, ring depth.
+#define TCL_GROUP_PAIR(X) X(F32, 256, 6) X(F32, 256, 4) X(BF16, 256, 6) X(F32, 224, 6)
+#define TCL_PAIR_INFO(OK, BN, ST)                                                                       \
+    {InKind::BF16, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST>::SMEM_BYTES,                    \
+     PairCfg<OutKind::OK, BN, ST>::THREADS, 1},
 
 #define TCL_VARIANT_CASE(IK, OK, BN, ST, PR)                                                           \
-    if (a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \
+    if (!a.pair && a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \
         *found = true;                                                                                 \
         return launch_variant<InKind::IK, OutKind::OK, BN, ST, PR>(a);                                 \
     }

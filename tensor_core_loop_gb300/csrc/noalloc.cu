@@ -72,7 +72,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     int bn = 0, stages = 0, grid = 0, tiles = 0, smem = 0;
     tcl_config_t cfg = {};
     cfg.max_ctas = sms;   // plan for this device without another device query
-    if ((st = tcl_plan(2, TCL_OUT_F32, M, N, K, &cfg, &bn, &stages, &grid, &tiles, &smem))) return st;
+    if ((st = tcl_plan(2, TCL_OUT_F32, M, N, K, &cfg, &bn, &stages, &grid, &tiles, &smem, nullptr))) return st;
 
     LaunchArgs a;
     a.in = InKind::BF16;
@@ -80,6 +80,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     a.bn = bn;
     a.stages = stages;
     a.prod = PROD_TMA;
+    a.pair = 0;
     a.grid = grid;
     a.stream = stream;
     if ((st = tensor_map_uncached(a2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda2 * 2, 64, 128, &a.tmA)))

@@ -81,10 +81,20 @@ def test_gemm_tf32_and_s8_reject(L):
 def test_plan_without_device(L):
     cfg = tcl.Config(max_ctas=152)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)
-    assert p["bn"] == 256 and p["num_tiles"] == 32 * 16 and p["grid"] == 152
+    # enough 256-row tiles for every pair of SMs: two SMs per tile; 224 columns give
+    # 16 × 19 = 304 tiles = exactly 4 per pair of SMs (256 would leave a partial wave)
+    assert p["cta_pair"] == 2 and p["bn"] == 224 and p["num_tiles"] == 16 * 19 and p["grid"] == 152
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)
+    assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16
     assert p["smem_bytes"] <= 232448
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=1))
+    assert p["cta_pair"] == 1 and p["bn"] == 256 and p["num_tiles"] == 32 * 16 and p["grid"] == 152
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 300, 520, 64, tcl.Config(max_ctas=152, cta_pair=2))
+    assert p["cta_pair"] == 2 and p["num_tiles"] == 2 * 3 and p["grid"] == 12
+    with pytest.raises(tcl.TclError):   # exact-integer mode has no two-SM kernel
+        tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2))
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096, cfg)
-    assert p["bn"] == 128 and p["num_tiles"] == 16 and p["grid"] == 16
+    assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 16 and p["grid"] == 16
     p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, cfg)
     assert p["bn"] == 128
     p = tcl.plan(tcl.IN_TF32, 0, 300, 70, 9, cfg)

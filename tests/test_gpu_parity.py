@@ -145,6 +145,46 @@ def test_bf16_sync_producer(oracle_mod, stages):
     bf16_case(oracle_mod, 130, 261, 200, seed=10, cfg=tcl.Config(bn=256, stages=stages, producer=1), ldc=264)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 512, 1024), (300, 520, 200), (130, 261, 72), (1, 8, 8),
+                                   (777, 1000, 1216), (1024, 768, 4096)])
+def test_bf16_pair_kernel(oracle_mod, M, N, K):
+    # two SMs per 256×256 tile (cta_group::2); ragged shapes leave the peer CTA's rows
+    # or B columns partly or wholly outside the matrix
+    ldc = -(-N // 4) * 4 if N % 4 else None
+    bf16_case(oracle_mod, M, N, K, seed=M + K, cfg=tcl.Config(cta_pair=2), ldc=ldc)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 224, 256), (512, 1000, 640), (300, 452, 200), (1024, 4096, 512)])
+def test_bf16_pair_kernel_224(oracle_mod, M, N, K):
+    # 256×224 pair tiles: each SM supplies 112 columns of B (two 64-column boxes, the
+    # last 16 columns unread by the MMA)
+    bf16_case(oracle_mod, M, N, K, seed=N, cfg=tcl.Config(cta_pair=2, bn=224))
+
+
+@pytest.mark.parametrize("stages", [4, 6])
+def test_bf16_pair_kernel_stages_and_grid(oracle_mod, stages):
+    bf16_case(oracle_mod, 768, 1280, 832, seed=stages, cfg=tcl.Config(cta_pair=2, stages=stages))
+    bf16_case(oracle_mod, 768, 1280, 832, seed=stages, cfg=tcl.Config(cta_pair=2, stages=stages, max_ctas=4,
+                                                                         group_m=2))
+    bf16_case(oracle_mod, 768, 1280, 832, seed=stages, cfg=tcl.Config(cta_pair=2, stages=stages,
+                                                                         one_cta_per_tile=1))
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (300, 264, 200)])
+def test_bf16_pair_kernel_bf16_out(oracle_mod, M, N, K):
+    bf16_case(oracle_mod, M, N, K, seed=5, out_dtype=torch.bfloat16, cfg=tcl.Config(cta_pair=2))
+
+
+def test_pair_kernel_variants_bitwise_identical():
+    a, b = inputs.bf16_pair(1024, 1280, 1216, seed=19)
+    a, b = a.to(DEV), b.to(DEV)
+    outs = [run(a, b, cfg=tcl.Config(cta_pair=2, stages=st, max_ctas=mc, group_m=gm, one_cta_per_tile=op),
+                canary=False)
+            for st in (4, 6) for (mc, gm, op) in ((0, 0, 0), (6, 3, 0), (0, 0, 1))]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""

@@ -43,19 +43,20 @@ def test_bounded_wait_runs_out_and_context_survives():
     assert tcl.last_device_error() == (0, 0)
 
 
-def test_trace_shows_loads_ahead_of_mma():
+@pytest.mark.parametrize("pair", [1, 2])
+def test_trace_shows_loads_ahead_of_mma(pair):
     """The per-k-block timeline of CTA 0: each block's load is issued before its
     data lands, the MMAs are issued after, and the loads of later blocks are in
     flight while earlier blocks' MMAs run (the software pipeline)."""
-    M, N, K = 128, 256, 64 * 48
+    M, N, K = 128 * pair, 256, 64 * 48
     a, b = inputs.bf16_pair(M, N, K, seed=4)
     a, b = a.to(DEV), b.to(DEV)
     cap = 48
-    trace = torch.zeros(4 * cap, dtype=torch.int64, device=DEV)
-    cfg = tcl.Config(bn=256, stages=4, trace=trace.data_ptr(), trace_cap=cap)
+    trace = torch.zeros(4 * cap + 4, dtype=torch.int64, device=DEV)
+    cfg = tcl.Config(bn=256, stages=4, cta_pair=pair, trace=trace.data_ptr(), trace_cap=cap)
     c = tcl.gemm(a, b, cfg=cfg)
     torch.cuda.synchronize()
-    t = trace.view(cap, 4).cpu().numpy().astype(np.int64)
+    t = trace[:4 * cap].view(cap, 4).cpu().numpy().astype(np.int64)
     issued, landed, mma, done = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
     assert (issued > 0).all() and (landed > 0).all() and (mma > 0).all()
     assert (landed >= issued).all() and (mma >= landed).all()

@@ -338,14 +338,14 @@ def run_trace(args):
         ah, bh = inputs.bf16_pair(m, n, k, seed=0)
         a, b = ah.to(dev), bh.to(dev)
         for pair in ((1, 2) if m >= 4096 else (1,)):
-            cfg0 = tcl.Config(cta_pair=pair)
+            cfg0 = tcl.Config(cta_pair=pair, split_k=1)
             pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k, cfg0)
             num_kb = -(-k // 64)
             clusters = pl["grid"] // (2 if pl["cta_pair"] == 2 else 1)
             tiles_cta0 = -(-pl["num_tiles"] // clusters)
             cap = min(8192, tiles_cta0 * num_kb)
             trace = torch.zeros(4 * cap + 4, dtype=torch.int64, device=dev)
-            cfg = tcl.Config(cta_pair=pair, trace=trace.data_ptr(), trace_cap=cap)
+            cfg = tcl.Config(cta_pair=pair, split_k=1, trace=trace.data_ptr(), trace_cap=cap)
             for _ in range(3):
                 trace.zero_()
                 tcl.gemm(a, b, cfg=cfg)
@@ -538,6 +538,26 @@ def main():
             sweep[f"{mn}x{mn}x{k}"] = {"tflops": round(tf, 1), "us": round(ms * 1e3, 2),
                                         "alg_gbs": round(alg_bytes / (ms * 1e-3) / 1e9, 1)}
         extra["k_sweep"] = sweep
+        # the other two workloads at 4096³ (each launch timed alone after an L2 flush): int8 → exact
+        # int32 (repack pass + GEMM), TF32 (transpose pass + GEMM); whole-call time
+        a8h, b8h = inputs.s8_pair(M, N, K, seed=0)
+        a8, b8 = a8h.to(dev), b8h.to(dev)
+        c32 = torch.empty((M, N), dtype=torch.int32, device=dev)
+        f8 = (lambda: tcl.gemm_into(a8, b8, c32))
+        for _ in range(3):
+            f8()
+        ms8 = time_flushed(f8, (), 20, stream, torch, flush)
+        extra["int8_tops_4096"] = round(FLOPS / (ms8 * 1e-3) / 1e12, 1)
+        del a8, b8, c32
+        ath, bth = inputs.tf32_pair(M, N, K, seed=0)
+        at, bt = ath.to(dev), bth.to(dev)
+        ct = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ft = (lambda: tcl.gemm_into(at, bt, ct))
+        for _ in range(3):
+            ft()
+        mst = time_flushed(ft, (), 20, stream, torch, flush)
+        extra["tf32_tflops_4096"] = round(FLOPS / (mst * 1e-3) / 1e12, 1)
+        del at, bt, ct
         del flush
 
     # ---- end to end through the public API with host buffers

@@ -16,10 +16,12 @@
  *
  * Memory and ownership: A, B and C are device pointers owned by the caller
  *   (allocated, kept alive until the stream has run the call, and freed by
- *   the caller). The library keeps a per-device cache of TMA descriptors and,
- *   for gemm_s8 and gemm_tf32, a per-device scratch buffer for repacked
- *   operands that it grows on demand (cudaMalloc, after a device
- *   synchronisation) and frees in tcl_shutdown().
+ *   the caller). The library keeps a per-device cache of TMA descriptors and
+ *   a per-device scratch buffer (repacked operands for gemm_s8 and gemm_tf32,
+ *   split-K partial tiles for small grids) that it grows on demand
+ *   (cudaMalloc, after a device synchronisation) and frees in tcl_shutdown().
+ *   Every call on a device shares that buffer: calls whose GPU work could
+ *   overlap (different streams without ordering) must not both need it.
  *
  * Streams: every call is asynchronous on `stream` (0 = legacy default
  *   stream) and returns once the work is enqueued. Calls on one stream run in
@@ -98,6 +100,10 @@ typedef struct {
     int producer;                  /* 0 (default): TMA bulk-tensor loads issued by one thread;
                                       1: synchronous copy by four warps (ld.global -> registers ->
                                       st.shared), the ablation's lower rung; bf16 only */
+    int split_k;                   /* 0: automatic (when the output tiles alone would leave most SMs
+                                      idle, K is cut into ranges whose fp32 partial tiles a second
+                                      kernel adds in a fixed order); 1: never; s > 1: s ranges.
+                                      One-SM kernel and floating-point output only */
     int cta_pair;                  /* 0: automatic; 1: one SM per tile (tcgen05 cta_group::1);
                                       2: two SMs per 256×256 tile (cta_group::2; bf16 in,
                                       fp32/bf16 out, TMA producer) */
@@ -169,13 +175,24 @@ TCL_API int gemm_tf32_ex(int M, int N, int K, const float* A, int lda, const flo
 TCL_API int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
                int ldc, const tcl_config_t* cfg, cudaStream_t stream);
 
-/* The launch the automatic path would make for this problem, without
- * launching: in_kind 0 = bf16, 1 = tf32, 2 = int8. Any output pointer may be
- * NULL; *cta_pair receives 1 (one SM per tile) or 2 (two SMs per tile).
- * With cfg->max_ctas > 0 no device is queried (max_ctas stands for the SM
- * count). Returns a tcl_status (argument checks as above, pointers not needed). */
-TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, int* bn,
-                     int* stages, int* grid, int* num_tiles, int* smem_bytes, int* cta_pair);
+/* What the library would launch for a problem (see tcl_plan). */
+typedef struct {
+    int bn;                         /* output tile width (columns) */
+    int stages;                     /* shared-memory ring depth */
+    int grid;                       /* CTAs launched */
+    int num_tiles;                  /* output tiles (of 128 or, for cta_pair 2, 256 rows) */
+    int smem_bytes;                 /* dynamic shared memory per CTA */
+    int cta_pair;                   /* 1: one SM per tile; 2: two SMs per tile */
+    int splits;                     /* K ranges (1: no split-K) */
+    int producer;                   /* 0: TMA, 1: synchronous copy */
+    unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
+} tcl_plan_t;
+
+/* Fills *plan (if not NULL) with the launch the library would make for this
+ * problem, without launching: in_kind 0 = bf16, 1 = tf32, 2 = int8. With
+ * cfg->max_ctas > 0 no device is queried (max_ctas stands for the SM count).
+ * Returns a tcl_status (argument checks as above; no pointers needed). */
+TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, tcl_plan_t* plan);
 
 /* Tensor-pipe rate probe (measurement, not part of the GEMM): `grid` CTAs
  * (one per SM) each issue `iters` back-to-back tcgen05.mma of shape

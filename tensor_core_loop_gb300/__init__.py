@@ -58,8 +58,24 @@ class Config(ctypes.Structure):
         ("trace", ctypes.c_void_p),
         ("trace_cap", ctypes.c_int),
         ("producer", ctypes.c_int),
+        ("split_k", ctypes.c_int),
         ("cta_pair", ctypes.c_int),
         ("debug_skip_kblock", ctypes.c_int),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    """Mirror of ``tcl_plan_t``."""
+    _fields_ = [
+        ("bn", ctypes.c_int),
+        ("stages", ctypes.c_int),
+        ("grid", ctypes.c_int),
+        ("num_tiles", ctypes.c_int),
+        ("smem_bytes", ctypes.c_int),
+        ("cta_pair", ctypes.c_int),
+        ("splits", ctypes.c_int),
+        ("producer", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_ulonglong),
     ]
 
 
@@ -87,7 +103,7 @@ def lib() -> ctypes.CDLL:
         L.gemm_s8_static.argtypes = [I, I, I, P, I, P, I, P, I, P]
         L.tcl_mma_peak.argtypes = [I, I, I, I, I, I, P, P]
         IP = ctypes.POINTER(ctypes.c_int)
-        L.tcl_plan.argtypes = [I, I, I, I, I, CP, IP, IP, IP, IP, IP, IP]
+        L.tcl_plan.argtypes = [I, I, I, I, I, CP, ctypes.POINTER(PlanInfo)]
         L.tcl_status_string.argtypes = [I]
         L.tcl_status_string.restype = ctypes.c_char_p
         L.tcl_last_device_error.argtypes = [P, IP]
@@ -108,13 +124,13 @@ def num_sms() -> int:
 
 
 def plan(in_kind: int, out: int, M: int, N: int, K: int, cfg: Config | None = None) -> dict:
-    """The launch the library would make (tile N, ring depth, grid, tiles, shared memory)."""
-    vals = [ctypes.c_int(0) for _ in range(6)]
-    st = lib().tcl_plan(in_kind, out, M, N, K, ctypes.byref(cfg) if cfg else None,
-                        *[ctypes.byref(v) for v in vals])
+    """The launch the library would make (tile width, ring depth, grid, tiles, shared memory,
+    one or two SMs per tile, split-K ranges, producer kind, workspace bytes)."""
+    info = PlanInfo()
+    st = lib().tcl_plan(in_kind, out, M, N, K, ctypes.byref(cfg) if cfg else None, ctypes.byref(info))
     if st:
         raise TclError(st, "tcl_plan")
-    return dict(zip(("bn", "stages", "grid", "num_tiles", "smem_bytes", "cta_pair"), (v.value for v in vals)))
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
 
 
 def mma_peak(in_kind: int = IN_BF16, n: int = 256, b_mn: int = 0, iters: int = 4096, grid: int | None = None,

@@ -188,7 +188,14 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 
 struct Plan {
     int bn, stages, prod, pair, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
+    int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
 };
+
+// Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
+// traffic and the extra reduction launch (measured on GB300 at M=N=512: a
+// loss at K ≤ 1024, a gain from K = 4096 on).
+constexpr int kMinKbPerSplit = 8;    // k-blocks each range keeps
+constexpr int kMinKbToSplit = 24;    // k-blocks a tile needs before splitting is considered
 
 const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod, int pair) {
     for (const auto& v : kVariants)
@@ -272,19 +279,62 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->num_kb = (K + bk - 1) / bk;
     pl->kb_per_unit = ok == OutKind::S32 ? kS32UnitK / bk : pl->num_kb;
     pl->group_m = cfg && cfg->group_m > 0 ? cfg->group_m : 8;
+    // Split-K (one-SM kernel, floating-point output): when the output tiles
+    // alone would leave most SMs idle, cut K into ranges computed by different
+    // CTAs; a second kernel adds the partial tiles in a fixed order.
+    pl->splits = 1;
+    pl->kb_per_split = pl->num_kb;
+    const int want_split = cfg ? cfg->split_k : 0;
+    if (want_split < 0) return TCL_ERR_CONFIG;
+    if (want_split > 1 && (pair || ok == OutKind::S32)) return TCL_ERR_CONFIG;
+    if (!pair && ok != OutKind::S32 && want_split != 1) {
+        int sp = want_split;
+        if (sp == 0) {
+            const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
+            sp = (pl->num_tiles < cap / 2 && pl->num_kb >= kMinKbToSplit)
+                     ? std::min(cap / pl->num_tiles, pl->num_kb / kMinKbPerSplit)
+                     : 1;
+        }
+        sp = std::max(1, std::min(sp, pl->num_kb));
+        pl->kb_per_split = (pl->num_kb + sp - 1) / sp;
+        pl->splits = (pl->num_kb + pl->kb_per_split - 1) / pl->kb_per_split;
+        if (pl->splits > 1) {
+            // the partial tiles are fp32: the kernel runs in its fp32-output form
+            const VariantInfo* v32 = find_variant(ik, OutKind::F32, bn, stages, prod, 0);
+            if (!v32) return TCL_ERR_CONFIG;
+            pl->smem = v32->smem_bytes;
+        }
+    }
+    const long long work = static_cast<long long>(pl->num_tiles) * pl->splits;
     if (pair) {
         int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / 2 : pair_clusters(v);
         if (clusters < 1) return cfg && cfg->max_ctas > 0 ? TCL_ERR_CONFIG : TCL_ERR_LAUNCH;
         if (cfg && cfg->one_cta_per_tile) clusters = pl->num_tiles;
         pl->grid = 2 * (pl->num_tiles < clusters ? pl->num_tiles : clusters);
     } else if (cfg && cfg->one_cta_per_tile) {
-        pl->grid = pl->num_tiles;
+        pl->grid = static_cast<int>(std::min<long long>(work, 0x7FFFFFFF));
     } else {
         int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
         if (cap < 1) cap = 1;
-        pl->grid = pl->num_tiles < cap ? pl->num_tiles : cap;
+        pl->grid = static_cast<int>(std::min<long long>(work, cap));
     }
     return TCL_OK;
+}
+
+// Split-K workspace: `splits` fp32 slabs of round_up(M, 128) rows × round_up(N, 4) columns.
+struct Workspace {
+    long long ld, rows_per_split;
+    size_t bytes;
+};
+
+Workspace split_workspace(const Plan& pl, int M, int N) {
+    Workspace w{0, 0, 0};
+    if (pl.splits > 1) {
+        w.ld = round_up(N, 4);
+        w.rows_per_split = round_up(M, kBM);
+        w.bytes = static_cast<size_t>(round_up(w.ld * w.rows_per_split * 4 * pl.splits, 256));
+    }
+    return w;
 }
 
 // Resident pair clusters for a pair variant on the current device, queried once.
@@ -299,24 +349,30 @@ int device_pair_clusters(DevState* ds, const VariantInfo* v) {
     return ds->pair_clusters[idx];
 }
 
-// Builds tensor maps and launches one GEMM over device operands.
-int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long long lda, const void* B,
-             long long ldb, void* C, long long ldc, const tcl_config_t* cfg, int dev, DevState* ds,
-             cudaStream_t stream) {
-    Plan pl;
-    int st = make_plan(ik, ok, M, N, K, cfg, ds->sms,
-                       [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, &pl);
-    if (st) return st;
-    const int ies = in_bytes(ik), oes = out_bytes(ok);
+int plan_on_device(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cfg, DevState* ds, Plan* pl) {
+    return make_plan(ik, ok, M, N, K, cfg, ds->sms,
+                     [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, pl);
+}
+
+// Builds tensor maps and launches one GEMM over device operands (and, for a
+// split-K plan, the reduction of the partial tiles from `workspace` into C).
+int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const void* A, long long lda,
+             const void* B, long long ldb, void* C, long long ldc, void* workspace, const tcl_config_t* cfg,
+             int dev, DevState* ds, cudaStream_t stream) {
+    int st;
+    const Workspace ws = split_workspace(pl, M, N);
+    const bool split = pl.splits > 1;
+    const OutKind kernel_out = split ? OutKind::F32 : ok;
+    const int ies = in_bytes(ik), oes = out_bytes(kernel_out);
     const int bk = 128 / ies;
     const CUtensorMapDataType in_t =
         ik == InKind::TF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapDataType out_t = ok == OutKind::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                      : ok == OutKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                            : CU_TENSOR_MAP_DATA_TYPE_INT32;
+    const CUtensorMapDataType out_t = kernel_out == OutKind::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                      : kernel_out == OutKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                    : CU_TENSOR_MAP_DATA_TYPE_INT32;
     LaunchArgs a;
     a.in = ik;
-    a.out = ok;
+    a.out = kernel_out;
     a.bn = pl.bn;
     a.stages = pl.stages;
     a.prod = pl.prod;
@@ -329,7 +385,12 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     } else {                    // B given N-major (K rows of N)
         if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB))) return st;
     }
-    if ((st = tensor_map(dev, C, out_t, N, M, ldc * oes, 128 / oes, 32, &a.tmC))) return st;
+    void* out_ptr = split ? workspace : C;
+    const long long out_ld = split ? ws.ld : ldc;
+    const long long out_rows = split ? ws.rows_per_split * pl.splits : M;
+    if ((st = tensor_map(dev, out_ptr, out_t, N, static_cast<uint64_t>(out_rows), out_ld * oes, 128 / oes, 32,
+                         &a.tmC)))
+        return st;
     GemmParams& p = a.p;
     p.M = M;
     p.N = N;
@@ -344,8 +405,12 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
     p.status = ds->status;
     p.trace = cfg ? cfg->trace : nullptr;
     p.trace_cap = cfg && cfg->trace ? cfg->trace_cap : 0;
-    p.C = C;
-    p.ldc = ldc;
+    p.C = out_ptr;
+    p.ldc = out_ld;
+    p.splits = pl.splits;
+    p.kb_per_split = pl.kb_per_split;
+    p.split_rows = split ? static_cast<int>(ws.rows_per_split) : 0;
+    p.out_rows = static_cast<int>(out_rows);
     p.A = A;
     p.lda = lda;
     p.B = B;
@@ -369,6 +434,11 @@ int run_gemm(InKind ik, OutKind ok, int M, int N, int K, const void* A, long lon
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }
+    if (split && launch_splitk_reduce(static_cast<const float*>(workspace), ws.ld, ws.rows_per_split, pl.splits, C,
+                                      ldc, M, N, ok == OutKind::BF16 ? 1 : 0, ds->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
     return TCL_OK;
 }
 
@@ -384,8 +454,12 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
-    return run_gemm(InKind::BF16, out == TCL_OUT_BF16 ? OutKind::BF16 : OutKind::F32, M, N, K, A, lda,
-                    B, ldb, C, ldc, cfg, dev, ds, stream);
+    const OutKind ok = out == TCL_OUT_BF16 ? OutKind::BF16 : OutKind::F32;
+    Plan pl;
+    if ((st = plan_on_device(InKind::BF16, ok, M, N, K, cfg, ds, &pl))) return st;
+    const Workspace ws = split_workspace(pl, M, N);
+    if (ws.bytes && (st = ensure_scratch(ds, ws.bytes))) return st;
+    return run_gemm(pl, InKind::BF16, ok, M, N, K, A, lda, B, ldb, C, ldc, ds->scratch, cfg, dev, ds, stream);
 }
 
 int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
@@ -398,15 +472,21 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
-    // The TF32 tensor-core path takes B K-major: transpose it (N rows of K) into scratch.
-    if ((st = ensure_scratch(ds, static_cast<size_t>(round_up(static_cast<long long>(N) * K * 4, 256)))))
-        return st;
+    Plan pl;
+    if ((st = plan_on_device(InKind::TF32, OutKind::F32, M, N, K, cfg, ds, &pl))) return st;
+    // The TF32 tensor-core path takes B K-major: transpose it (N rows of K) into
+    // scratch, followed by the split-K workspace if the plan has one. Sized
+    // before anything is enqueued, since growing the scratch frees the old one.
+    const size_t bt_bytes = static_cast<size_t>(round_up(static_cast<long long>(N) * K * 4, 256));
+    const Workspace ws = split_workspace(pl, M, N);
+    if ((st = ensure_scratch(ds, bt_bytes + ws.bytes))) return st;
     float* bt = static_cast<float*>(ds->scratch);
     if (launch_transpose_f32(B, ldb, bt, K, K, N, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }
-    return run_gemm(InKind::TF32, OutKind::F32, M, N, K, A, lda, bt, K, C, ldc, cfg, dev, ds, stream);
+    return run_gemm(pl, InKind::TF32, OutKind::F32, M, N, K, A, lda, bt, K, C, ldc,
+                    static_cast<uint8_t*>(ds->scratch) + bt_bytes, cfg, dev, ds, stream);
 }
 
 
@@ -421,6 +501,8 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
+    Plan pl;
+    if ((st = plan_on_device(InKind::BF16, OutKind::S32, M, N, K, cfg, ds, &pl))) return st;
     // Packed bf16 copies of A (M × lda2) and B (K × ldb2), each 256-byte aligned.
     const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
     const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
@@ -433,7 +515,7 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }
-    return run_gemm(InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, C, ldc, cfg, dev, ds,
+    return run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, C, ldc, nullptr, cfg, dev, ds,
                     stream);
 }
 
@@ -501,8 +583,7 @@ int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, i
     return gemm_s8_impl(M, N, K, A, lda, B, ldb, C, ldc, cfg, stream);
 }
 
-int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, int* bn, int* stages,
-             int* grid, int* num_tiles, int* smem_bytes, int* cta_pair) {
+int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, tcl_plan_t* plan) {
     if (M < 1 || N < 1 || K < 1) return TCL_ERR_DIMS;
     InKind ik;
     OutKind ok;
@@ -531,16 +612,20 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         DevState* ds;
         st = current_device(&dev, &ds);
         if (st) return st;
-        st = make_plan(ik, ok, M, N, K, cfg, ds->sms,
-                       [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, &pl);
+        st = plan_on_device(ik, ok, M, N, K, cfg, ds, &pl);
     }
     if (st) return st;
-    if (bn) *bn = pl.bn;
-    if (stages) *stages = pl.stages;
-    if (grid) *grid = pl.grid;
-    if (num_tiles) *num_tiles = pl.num_tiles;
-    if (smem_bytes) *smem_bytes = pl.smem;
-    if (cta_pair) *cta_pair = pl.pair ? 2 : 1;
+    if (plan) {
+        plan->bn = pl.bn;
+        plan->stages = pl.stages;
+        plan->grid = pl.grid;
+        plan->num_tiles = pl.num_tiles;
+        plan->smem_bytes = pl.smem;
+        plan->cta_pair = pl.pair ? 2 : 1;
+        plan->splits = pl.splits;
+        plan->producer = pl.prod;
+        plan->workspace_bytes = static_cast<unsigned long long>(split_workspace(pl, M, N).bytes);
+    }
     return TCL_OK;
 }
 

@@ -87,7 +87,30 @@ struct GemmParams {
     const void* B;
     long long ldb;
     int debug_skip_kb;           // test hook: CTA 0's TMA producer never loads this k-block (-1: off)
+    int splits;                  // K split into this many ranges (1: no split); work items = tiles × splits
+    int kb_per_split;            // k-blocks per split (the last may have fewer)
+    int split_rows;              // output rows between consecutive splits' partial results
+    int out_rows;                // rows of the output tensor (M, or splits × split_rows)
 };
+
+// Work item w → output tile (mb, nb), its k-block range [kb_lo, kb_hi) and
+// the row where its result starts in the output tensor. Splits of one tile
+// are num_tiles work items apart, so a wave covers many tiles at once.
+struct Work {
+    int mb, nb, kb_lo, kb_hi, row_base;
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb);
+
+__device__ __forceinline__ Work work_item(int w, const GemmParams& p) {
+    Work r;
+    const int split = w / p.num_tiles;
+    tile_coords(w - split * p.num_tiles, p, r.mb, r.nb);
+    r.kb_lo = split * p.kb_per_split;
+    r.kb_hi = min(p.num_kb, r.kb_lo + p.kb_per_split);
+    r.row_base = split * p.split_rows;
+    return r;
+}
 
 // Producer kinds: TMA bulk-tensor copies issued by one thread, or the
 // synchronous variant (four warps: ld.global into registers, st.shared into
@@ -211,10 +234,10 @@ __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
                                            const GemmParams& p) {
     constexpr int COLS = 128 / OUT_ES;
-    const bool in_bounds = row0 < p.M && col0 < p.N;
+    const bool in_bounds = row0 < p.out_rows && col0 < p.N;
     if (in_bounds && col0 + COLS > p.N && (p.N * OUT_ES) % 16 != 0) {
         const int row = row0 + lane;
-        if (row < p.M) {
+        if (row < p.out_rows) {
             const int n = p.N - col0;
             if constexpr (OUT_ES == 4) {
                 uint32_t* dst = static_cast<uint32_t*>(p.C) + row * p.ldc + col0;
@@ -269,10 +292,11 @@ __device__ __forceinline__ void sync_producer(const GemmParams& p, uint8_t* stag
     const uint16_t* Ag = static_cast<const uint16_t*>(p.A);
     const uint16_t* Bg = static_cast<const uint16_t*>(p.B);
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, p, mb, nb);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+    const int num_work = p.num_tiles * p.splits;
+    for (int w = blockIdx.x; w < num_work; w += gridDim.x) {
+        const Work wk = work_item(w, p);
+        const int mb = wk.mb, nb = wk.nb;
+        for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
             const uint32_t s = it % C::STAGES;
             const uint32_t ph = (it / C::STAGES) & 1u;
             bool got = true;
@@ -400,10 +424,11 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                int mb, nb;
-                tile_coords(tile, p, mb, nb);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            const int num_work = p.num_tiles * p.splits;
+            for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+                const Work wk = work_item(w, p);
+                const int mb = wk.mb, nb = wk.nb;
+                for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
@@ -457,8 +482,10 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
             constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
             uint32_t it = 0, unit = 0, s = 0, ph = 0;   // (s, ph): ring slot and phase of k-block `it`
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_unit, ++unit) {
+            const int num_work = p.num_tiles * p.splits;
+            for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+                const Work wk = work_item(w, p);
+                for (int kb0 = wk.kb_lo; kb0 < wk.kb_hi; kb0 += p.kb_per_unit, ++unit) {
                     const uint32_t buf = unit & 1u;
                     const uint32_t uph = (unit >> 1) & 1u;
                     if (!wait_bounded(acce0 + 8 * buf, uph ^ 1u, abort_flag, p.timeout_ns, p.status,
@@ -468,7 +495,7 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    const int kb1 = min(kb0 + p.kb_per_unit, p.num_kb);
+                    const int kb1 = min(kb0 + p.kb_per_unit, wk.kb_hi);
                     for (int kb = kb0; kb < kb1; ++kb, ++it) {
                         if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.timeout_ns, p.status,
                                           DEV_TIMEOUT_MMA_FULL)) {
@@ -514,16 +541,17 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
         int store_count = 0;
         uint32_t unit = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            int mb, nb;
-            tile_coords(tile, p, mb, nb);
-            const int row0 = mb * C::BM + q * 32;
+        const int num_work = p.num_tiles * p.splits;
+        for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+            const Work wk = work_item(w, p);
+            const int nb = wk.nb;
+            const int row0 = wk.row_base + wk.mb * C::BM + q * 32;
             [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? BN : 1];
             if constexpr (OK == OutKind::S32) {
 #pragma unroll
                 for (int i = 0; i < BN; ++i) iacc[i] = 0;
             }
-            for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.kb_per_unit, ++unit) {
+            for (int kb0 = wk.kb_lo; kb0 < wk.kb_hi; kb0 += p.kb_per_unit, ++unit) {
                 const uint32_t buf = unit & 1u;
                 const uint32_t uph = (unit >> 1) & 1u;
                 bool got = true;
@@ -550,7 +578,7 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(acce0 + 8 * buf);
-                    if (kb0 + p.kb_per_unit >= p.num_kb) {
+                    if (kb0 + p.kb_per_unit >= wk.kb_hi) {
 #pragma unroll
                         for (int c = 0; c < BN / 32; ++c) {
                             const uint32_t(&v)[32] =

@@ -1,7 +1,8 @@
-// Operand repacking passes that run before the GEMM kernel on some paths:
+// Passes that run before or after the GEMM kernel on some paths:
 //   * exact int8 -> bf16 widening (integer GEMM);
 //   * fp32 transpose K×N -> N×K (TF32 GEMM: the tensor cores take its B
-//     operand K-major).
+//     operand K-major);
+//   * the fixed-order sum of split-K partial tiles.
 //
 // int8 -> bf16:
 // Every int8 value (|x| <= 128) has at most 8 significant bits, so it is
@@ -12,6 +13,8 @@
 // are padded to a multiple of 8 elements (the padding is written as zeros), so
 // full chunks use vector accesses and only a ragged row tail falls back to
 // scalar accesses.
+#include <cuda_bf16.h>
+
 #include <cstdint>
 
 #include "launch.cuh"
@@ -71,6 +74,68 @@ cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, lo
     if (blocks < 1) blocks = 1;
     s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         src, ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+    return cudaGetLastError();
+}
+
+// Split-K reduction: each thread owns four consecutive columns of one row and
+// adds the splits' fp32 partial tiles in order s = 0, 1, ..., splits-1 (the
+// result does not depend on which CTA finished first), then writes fp32 or
+// bf16 (round to nearest even). The workspace rows are padded to a multiple
+// of 4 columns, so its loads are always 16-byte vectors; C gets vector stores
+// where a whole chunk is inside the row and scalar stores at a ragged edge.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ W, long long ldw,
+                                                             long long split_stride, int splits,
+                                                             void* __restrict__ C, long long ldc, int M, int N,
+                                                             int out_bf16) {
+    const int chunks = (N + 3) / 4;
+    const long long total = static_cast<long long>(M) * chunks;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(idx / chunks);
+        const int c0 = static_cast<int>(idx - static_cast<long long>(r) * chunks) * 4;
+        const float* w = W + r * ldw + c0;
+        float4 acc = *reinterpret_cast<const float4*>(w);
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 v = *reinterpret_cast<const float4*>(w + sp * split_stride);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+        const bool whole = c0 + 4 <= N;
+        if (!out_bf16) {
+            float* dst = static_cast<float*>(C) + r * ldc + c0;
+            if (whole) {
+                *reinterpret_cast<float4*>(dst) = acc;
+            } else {
+                for (int j = 0; c0 + j < N; ++j) dst[j] = vals[j];
+            }
+        } else {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(C) + r * ldc + c0;
+            if (whole) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 packed;
+                packed.x = *reinterpret_cast<uint32_t*>(&lo);
+                packed.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(dst) = packed;
+            } else {
+                for (int j = 0; c0 + j < N; ++j) dst[j] = __float2bfloat16_rn(vals[j]);
+            }
+        }
+    }
+}
+
+cudaError_t launch_splitk_reduce(const float* W, long long ldw, long long rows_per_split, int splits, void* C,
+                                 long long ldc, int M, int N, int out_bf16, int sms, cudaStream_t stream) {
+    const long long total = static_cast<long long>(M) * ((N + 3) / 4);
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, ldw, rows_per_split * ldw, splits, C,
+                                                                           ldc, M, N, out_bf16);
     return cudaGetLastError();
 }
 

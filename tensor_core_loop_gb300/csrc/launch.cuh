@@ -39,6 +39,11 @@ cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, long long ld_dst,
                               int rows, int cols, int sms, cudaStream_t stream);
 
+// C (M×N, fp32 or bf16 rounded to nearest even) = sum over s = 0..splits-1, in
+// that order, of the fp32 partial tiles W[s·rows_per_split + i][j] (leading dimension ldw).
+cudaError_t launch_splitk_reduce(const float* W, long long ldw, long long rows_per_split, int splits, void* C,
+                                 long long ldc, int M, int N, int out_bf16, int sms, cudaStream_t stream);
+
 // dst (cols × rows) = transpose of src (rows × cols), fp32, bit for bit.
 cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
                                  int cols, int sms, cudaStream_t stream);

@@ -69,10 +69,11 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     uint8_t* a2 = static_cast<uint8_t*>(g_scratch_addr[dev]);
     uint8_t* b2 = a2 + a_bytes;
 
-    int bn = 0, stages = 0, grid = 0, tiles = 0, smem = 0;
     tcl_config_t cfg = {};
     cfg.max_ctas = sms;   // plan for this device without another device query
-    if ((st = tcl_plan(2, TCL_OUT_F32, M, N, K, &cfg, &bn, &stages, &grid, &tiles, &smem, nullptr))) return st;
+    tcl_plan_t plan;
+    if ((st = tcl_plan(2, TCL_OUT_F32, M, N, K, &cfg, &plan))) return st;
+    const int bn = plan.bn, stages = plan.stages, grid = plan.grid, tiles = plan.num_tiles;
 
     LaunchArgs a;
     a.in = InKind::BF16;
@@ -111,6 +112,10 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.B = b2;
     p.ldb = ldb2;
     p.debug_skip_kb = -1;
+    p.splits = 1;
+    p.kb_per_split = p.num_kb;
+    p.split_rows = 0;
+    p.out_rows = M;
 
     if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, sms, stream) != cudaSuccess ||
         launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, sms, stream) != cudaSuccess) {

@@ -94,7 +94,23 @@ def test_plan_without_device(L):
     with pytest.raises(tcl.TclError):   # exact-integer mode has no two-SM kernel
         tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2))
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096, cfg)
-    assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 16 and p["grid"] == 16
+    # 16 narrow tiles for 152 SMs: K is cut into 8 ranges of 8 k-blocks (split-K)
+    assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 16
+    assert p["splits"] == 8 and p["grid"] == 128 and p["workspace_bytes"] == 8 * 512 * 512 * 4
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)     # 4 k-blocks: too short to split
+    assert p["splits"] == 1 and p["grid"] == 16 and p["workspace_bytes"] == 0
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 8192, cfg)
+    assert p["splits"] == 9 and p["grid"] == 144
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 8192, tcl.Config(max_ctas=152, split_k=1))
+    assert p["splits"] == 1
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 300, 261, 1000, tcl.Config(max_ctas=152, split_k=3))
+    assert p["splits"] == 3 and p["workspace_bytes"] == 3 * 384 * 264 * 4
+    for bad in (tcl.Config(max_ctas=152, split_k=2, cta_pair=2),):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096, bad)
+    with pytest.raises(tcl.TclError):
+        tcl.plan(tcl.IN_S8, 0, 512, 512, 4096, tcl.Config(max_ctas=152, split_k=2))
+    assert tcl.plan(tcl.IN_S8, 0, 512, 512, 4096, cfg)["splits"] == 1   # exact integers: never split
     p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, cfg)
     assert p["bn"] == 128
     p = tcl.plan(tcl.IN_TF32, 0, 300, 70, 9, cfg)

@@ -185,6 +185,36 @@ def test_pair_kernel_variants_bitwise_identical():
         assert torch.equal(o, outs[0])
 
 
+@pytest.mark.parametrize("M,N,K,splits,out", [
+    (512, 512, 4096, 0, torch.float32),        # automatic: 8 ranges
+    (512, 512, 8192, 0, torch.bfloat16),       # automatic: 9 ranges, bf16 written by the reduction
+    (300, 261, 1000, 3, torch.float32),        # ragged M, N (edge stored element by element), last range short
+    (300, 260, 1000, 7, torch.bfloat16),
+    (130, 136, 72, 2, torch.float32),          # 2 k-blocks: one per range
+])
+def test_bf16_split_k(oracle_mod, M, N, K, splits, out):
+    cfg = tcl.Config(split_k=splits)
+    assert tcl.plan(tcl.IN_BF16, 0 if out == torch.float32 else 1, M, N, K, cfg)["splits"] > 1
+    bf16_case(oracle_mod, M, N, K, seed=K + splits, out_dtype=out, cfg=cfg)
+
+
+def test_tf32_split_k(oracle_mod):
+    a, b = inputs.tf32_pair(256, 384, 2048, seed=8)
+    got = run(a.to(DEV), b.to(DEV), cfg=tcl.Config(split_k=5)).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, "tf32 split-K")
+
+
+def test_split_k_deterministic():
+    a, b = inputs.bf16_pair(512, 512, 8192, seed=23)
+    a, b = a.to(DEV), b.to(DEV)
+    first = tcl.gemm(a, b)
+    for _ in range(5):
+        assert torch.equal(tcl.gemm(a, b), first)
+    # the same ranges through a different grid give the same bits (fixed summation order)
+    assert torch.equal(tcl.gemm(a, b, cfg=tcl.Config(split_k=9, max_ctas=40)), first)
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""
@@ -196,11 +226,11 @@ def test_variants_bitwise_identical():
             for one_per_tile in (0, 1):
                 for max_ctas in (0, 3):
                     cfg = tcl.Config(bn=bn, stages=st, one_cta_per_tile=one_per_tile, max_ctas=max_ctas,
-                                     group_m=3 if max_ctas else 0)
+                                     group_m=3 if max_ctas else 0, split_k=1)
                     outs.append(run(a, b, cfg=cfg, canary=False))
         if bn == 256:   # the synchronous producer feeds the same MMA sequence
             for st in (1, 2, 4):
-                outs.append(run(a, b, cfg=tcl.Config(bn=256, stages=st, producer=1), canary=False))
+                outs.append(run(a, b, cfg=tcl.Config(bn=256, stages=st, producer=1, split_k=1), canary=False))
         for o in outs[1:]:
             assert torch.equal(o, outs[0])
 

@@ -517,27 +517,33 @@ def main():
         ms16 = time_rotating(step16, sets16, 500, 20, stream, torch)
         extra["bf16_out_tflops"] = FLOPS / (ms16 * 1e-3) / 1e12
         del sets16
-        # K sweep, each launch timed alone after an L2 flush
-        flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+        # K sweep: back-to-back launches over rotating input/output sets whose footprint is
+        # twice the L2, so every launch starts cold in L2 (single-launch event timing is
+        # quantised at ~2 µs on this GPU, too coarse for the smallest shapes)
         sweep = {}
         for mn, k in SWEEP:
             ah, bh = inputs.bf16_pair(mn, mn, k, seed=0)
-            a, b = ah.to(dev), bh.to(dev)
-            c = torch.empty((mn, mn), dtype=torch.float32, device=dev)
+            a0_, b0_ = ah.to(dev), bh.to(dev)
+            sbytes = 2 * mn * k * 2 + mn * mn * 4
+            nset = max(2, -(-2 * L2_BYTES // sbytes))
+            ssets = [(a0_ if i == 0 else a0_.clone(), b0_ if i == 0 else b0_.clone(),
+                      torch.empty((mn, mn), dtype=torch.float32, device=dev)) for i in range(nset)]
 
-            def f(a=a, b=b, c=c, mn=mn, k=k):
+            def f(a, b, c, mn=mn, k=k):
                 st_ = L.gemm_bf16(mn, mn, k, a.data_ptr(), k, b.data_ptr(), mn, c.data_ptr(), mn, tcl.OUT_F32,
                                   stream.cuda_stream)
                 if st_:
                     raise tcl.TclError(st_, "gemm_bf16")
-            for _ in range(5):
-                f()
-            ms = time_flushed(f, (), 30, stream, torch, flush)
+            ms = time_rotating(f, ssets, max(60, 2 * nset), 2 * nset, stream, torch)
             tf = 2.0 * mn * mn * k / (ms * 1e-3) / 1e12
             alg_bytes = (mn * k + k * mn) * 2 + mn * mn * 4
             sweep[f"{mn}x{mn}x{k}"] = {"tflops": round(tf, 1), "us": round(ms * 1e3, 2),
-                                        "alg_gbs": round(alg_bytes / (ms * 1e-3) / 1e9, 1)}
+                                        "alg_gbs": round(alg_bytes / (ms * 1e-3) / 1e9, 1),
+                                        "plan": tcl.plan(tcl.IN_BF16, tcl.OUT_F32, mn, mn, k)}
+            del ssets, a0_, b0_
         extra["k_sweep"] = sweep
+        extra["k_sweep_timing"] = "mean of back-to-back launches over rotating sets (footprint 2x L2)"
+        flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
         # the other two workloads at 4096³ (each launch timed alone after an L2 flush): int8 → exact
         # int32 (repack pass + GEMM), TF32 (transpose pass + GEMM); whole-call time
         a8h, b8h = inputs.s8_pair(M, N, K, seed=0)

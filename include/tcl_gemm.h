@@ -107,6 +107,8 @@ typedef struct {
     int cta_pair;                  /* 0: automatic; 1: one SM per tile (tcgen05 cta_group::1);
                                       2: two SMs per 256×256 tile (cta_group::2; bf16 in,
                                       fp32/bf16 out, TMA producer) */
+    int epi_slots;                 /* epilogue staging slabs per warp, i.e. output stores in flight
+                                      (0: automatic; two-SM kernel: 2 or 4, one-SM kernel: 2) */
     int debug_skip_kblock;         /* test hook, 0 = off. k > 0: CTA 0's TMA producer never loads
                                       the (k-1)-th k-block of its walk, so the MMA warp's bounded
                                       wait must run out; the call then reports
@@ -203,7 +205,10 @@ TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config
  * bounded wait ran out). flop/clk/SM = 2·128·n·K·iters / cycles.
  * flags bit 0: chain every MMA into one accumulator, as the MMAs of one GEMM
  * tile are (default: alternate two independent accumulators); bit 1: walk
- * the operand addresses like a GEMM k-loop (4 k-slices × 4 ring stages). */
+ * the operand addresses like a GEMM k-loop (4 k-slices × 4 ring stages);
+ * bit 2: N-major B with 64-column groups of 64 K-rows (8 KB apart, as a GEMM
+ * stage holds it) instead of 16 K-rows (2 KB apart); bit 3: per 4 MMAs, the
+ * rest of a GEMM issue loop (an mbarrier wait, a tcgen05 fence, a commit). */
 TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
                          unsigned long long* cycles, cudaStream_t stream);
 

@@ -60,6 +60,7 @@ class Config(ctypes.Structure):
         ("producer", ctypes.c_int),
         ("split_k", ctypes.c_int),
         ("cta_pair", ctypes.c_int),
+        ("epi_slots", ctypes.c_int),
         ("debug_skip_kblock", ctypes.c_int),
     ]
 

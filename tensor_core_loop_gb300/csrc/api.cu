@@ -187,7 +187,7 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 }
 
 struct Plan {
-    int bn, stages, prod, pair, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
+    int bn, stages, prod, pair, slots, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
     int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
 };
 
@@ -195,19 +195,23 @@ struct Plan {
 // traffic and the extra reduction launch (measured on GB300 at M=N=512: a
 // loss at K ≤ 1024, a gain from K = 4096 on).
 constexpr int kMinKbPerSplit = 8;    // k-blocks each range keeps
+constexpr int kMinKbForPair = 16;    // k-blocks a tile needs before two SMs per tile pay off
 constexpr int kMinKbToSplit = 24;    // k-blocks a tile needs before splitting is considered
 
-const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod, int pair) {
+// slots = 0 matches any staging depth (the first listed, i.e. two slabs per warp)
+const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod, int pair, int slots = 0) {
     for (const auto& v : kVariants)
-        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages && v.prod == prod && v.pair == pair)
+        if (v.in == ik && v.out == ok && v.bn == bn && v.stages == stages && v.prod == prod && v.pair == pair &&
+            (slots == 0 || v.slots == slots))
             return &v;
     return nullptr;
 }
 
-int deepest_stages(InKind ik, OutKind ok, int bn, int prod, int pair) {
+int deepest_stages(InKind ik, OutKind ok, int bn, int prod, int pair, int slots = 0) {
     int best = 0;
     for (const auto& v : kVariants)
-        if (v.in == ik && v.out == ok && v.bn == bn && v.prod == prod && v.pair == pair && v.stages > best)
+        if (v.in == ik && v.out == ok && v.bn == bn && v.prod == prod && v.pair == pair &&
+            (slots == 0 || v.slots == slots) && v.stages > best)
             best = v.stages;
     return best;
 }
@@ -231,10 +235,13 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         if (!pair_capable || (bn != 0 && bn != 256 && bn != 224)) return TCL_ERR_CONFIG;
         pair = 1;
     } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages)) {
-        // Two SMs per 256×256 tile halve each SM's bytes per flop; use them when
-        // there are at least as many pair tiles as pairs of SMs.
+        // Two SMs per 256-row tile halve each SM's bytes per flop; use them when
+        // there are at least as many pair tiles as pairs of SMs and a tile has
+        // enough k-blocks for its mainloop to outlast its epilogue (measured on
+        // GB300: at 4096²×256 one SM per tile is faster, from K = 1024 on the pair).
         const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
-        pair = tiles_pair >= sms / 2 ? 1 : 0;
+        const int kblocks = (K + bk - 1) / bk;
+        pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
     }
     if (pair) {
         if (bn == 0) {
@@ -262,9 +269,12 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         }
     }
     if (bn != 128 && bn != 256 && !(pair && bn == 224)) return TCL_ERR_CONFIG;
-    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn, prod, pair);
-    const VariantInfo* v = find_variant(ik, ok, bn, stages, prod, pair);
+    const int slots = cfg ? cfg->epi_slots : 0;
+    if (slots < 0 || (slots && !pair && slots != 2)) return TCL_ERR_CONFIG;
+    int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn, prod, pair, slots);
+    const VariantInfo* v = find_variant(ik, ok, bn, stages, prod, pair, slots);
     if (!v) return TCL_ERR_CONFIG;
+    pl->slots = v->slots;
     pl->bn = bn;
     pl->stages = stages;
     pl->prod = prod;
@@ -345,7 +355,7 @@ int device_pair_clusters(DevState* ds, const VariantInfo* v) {
         if (w.pair) ++idx;
     }
     if (idx >= 8) return 0;
-    if (ds->pair_clusters[idx] == 0) ds->pair_clusters[idx] = pair_max_clusters(v->out, v->bn, v->stages);
+    if (ds->pair_clusters[idx] == 0) ds->pair_clusters[idx] = pair_max_clusters(v->out, v->bn, v->stages, v->slots);
     return ds->pair_clusters[idx];
 }
 
@@ -377,6 +387,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.stages = pl.stages;
     a.prod = pl.prod;
     a.pair = pl.pair;
+    a.slots = pl.slots;
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;

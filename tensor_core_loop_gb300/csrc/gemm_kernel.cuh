@@ -151,7 +151,8 @@ struct KCfg {
     static constexpr int EPI_COLS = 128 / OUT_ES;     // output columns per 128-byte staging row
     static constexpr int EPI_CHUNKS = BN / EPI_COLS;
     static constexpr int SLAB_BYTES = 32 * 128;       // one warp's 32 rows × 128 B
-    static constexpr int STAGING_BYTES = 4 * 2 * SLAB_BYTES;
+    static constexpr int EPI_SLOTS = 2;               // staging slabs per epilogue warp
+    static constexpr int STAGING_BYTES = 4 * EPI_SLOTS * SLAB_BYTES;
     static constexpr int TMEM_COLS = pow2_at_least(2 * BN, 32);
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_USED = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
@@ -212,6 +213,17 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
     }
 }
 
+// Warp-uniform bounded wait for a warp whose 32 lanes run the same loop: all
+// lanes poll once; unless the phase is complete for every lane, lane 0 takes
+// the bounded slow path and broadcasts the outcome, so the warp never diverges.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          unsigned long long timeout_ns, unsigned int* status, unsigned int code) {
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, timeout_ns, status, code) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -222,14 +234,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // One warp writes 32 rows × 128 bytes (row = lane) into a staging slab in the
 // 128-byte swizzled layout the C tensor map expects (16-byte chunk j of row r
 // lands at chunk j ^ (r mod 8)), then lane 0 TMA-stores the slab.
-// Always commits one bulk group per call so that "at most one group pending"
-// means "the slab used two calls ago is free".
+// Always commits one bulk group per call so that "at most SLOTS-1 groups
+// pending" means "the slab used SLOTS calls ago is free".
 //
 // The tensor store writes whole 16-byte pieces of a row, so a chunk that
 // crosses a right edge N not on a 16-byte boundary would also write the
 // columns after N. That chunk is stored element by element from registers
 // instead (rows past M skipped), leaving every byte outside C untouched.
-template <int SLAB_BYTES, int OUT_ES>
+template <int SLAB_BYTES, int OUT_ES, int SLOTS>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
                                            const GemmParams& p) {
@@ -256,8 +268,8 @@ __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab
         ++count;
         return;
     }
-    uint8_t* slab = slab_pair + (count & 1) * SLAB_BYTES;
-    if (lane == 0) ptx::bulk_wait_read<1>();
+    uint8_t* slab = slab_pair + (count % SLOTS) * SLAB_BYTES;
+    if (lane == 0) ptx::bulk_wait_read<SLOTS - 1>();
     __syncwarp();
     const uint32_t row_addr = ptx::smem_u32(slab) + lane * 128;
 #pragma unroll
@@ -357,6 +369,51 @@ __device__ __forceinline__ void sync_producer(const GemmParams& p, uint8_t* stag
             ptx::fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
             ptx::mbar_arrive(full0 + 8 * s);
         }
+    }
+}
+
+// Drains one TMEM accumulator (this warp's 32 lanes × EPI_CHUNKS chunks) to C:
+// F32 chunks are 32 fp32 columns, BF16 chunks 64 fp32 columns rounded to 64
+// bf16. The TMEM load of chunk c+1 is issued before chunk c is staged and
+// stored, so its latency hides under the shared-memory writes and the store
+// issue. `release()` runs once every TMEM read of the accumulator is complete.
+template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release>
+__device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_t* slab_pair, int& store_count,
+                                                  uint32_t tbase, int lane, int col_base, int row0,
+                                                  const GemmParams& p, Release release) {
+    constexpr int COLS = OK == OutKind::BF16 ? 64 : 32;   // TMEM columns per chunk
+    constexpr int OUT_ES = OK == OutKind::BF16 ? 2 : 4;
+    uint32_t buf[2][COLS];
+    __syncwarp();   // tcgen05.ld is warp-collective
+    ptx::tmem_ld_32x32b_x32(tbase, *reinterpret_cast<uint32_t(*)[32]>(&buf[0][0]));
+    if constexpr (COLS == 64) ptx::tmem_ld_32x32b_x32(tbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&buf[0][32]));
+#pragma unroll
+    for (int c = 0; c < EPI_CHUNKS; ++c) {
+        uint32_t(&cur)[COLS] = buf[c & 1];
+        ptx::tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&cur[0]));
+        if constexpr (COLS == 64) ptx::tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&cur[32]));
+        if (c + 1 < EPI_CHUNKS) {
+            uint32_t(&nxt)[COLS] = buf[(c + 1) & 1];
+            __syncwarp();
+            ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * COLS, *reinterpret_cast<uint32_t(*)[32]>(&nxt[0]));
+            if constexpr (COLS == 64)
+                ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&nxt[32]));
+        } else {
+            release();
+        }
+        uint32_t v[32];
+        if constexpr (OK == OutKind::BF16) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
+                v[i] = *reinterpret_cast<uint32_t*>(&t);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = cur[i];
+        }
+        store_slab<SLAB_BYTES, OUT_ES, SLOTS>(tmC, slab_pair, store_count, v, lane, col_base + c * (128 / OUT_ES), row0,
+                                              p);
     }
 }
 
@@ -468,76 +525,73 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
         __syncwarp();
     } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // Descriptors of stage 0; a stage and a k-slice are fixed offsets (in
-            // 16-byte units) in the start-address field, so the issue loop adds
-            // constants instead of rebuilding descriptors (one thread issues every
-            // MMA: its loop, not the tensor pipe, would otherwise set the pace).
-            const uint32_t stage0 = ptx::smem_u32(stage_base);
-            const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
-            const uint64_t bdesc0 = C::B_MN ? ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024)
-                                            : ptx::sdesc_sw128(stage0 + C::A_BYTES, 16, 1024);
-            constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
-            constexpr uint64_t B_STEP = C::B_MN ? C::UMMA_K * 128 / 16 : C::UMMA_K * C::ES / 16;
-            constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
-            uint32_t it = 0, unit = 0, s = 0, ph = 0;   // (s, ph): ring slot and phase of k-block `it`
-            bool ok = true;
-            const int num_work = p.num_tiles * p.splits;
-            for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
-                const Work wk = work_item(w, p);
-                for (int kb0 = wk.kb_lo; kb0 < wk.kb_hi; kb0 += p.kb_per_unit, ++unit) {
-                    const uint32_t buf = unit & 1u;
-                    const uint32_t uph = (unit >> 1) & 1u;
-                    if (!wait_bounded(acce0 + 8 * buf, uph ^ 1u, abort_flag, p.timeout_ns, p.status,
-                                      DEV_TIMEOUT_MMA_ACC)) {
+        // All 32 lanes run this loop (uniform control flow, no parked lanes);
+        // each k-block's four MMAs and its commit come from one elected lane
+        // through predicates. The issuing thread's loop, not the tensor pipe,
+        // would otherwise set the pace.
+        static_assert(C::KSUB == 4, "four MMAs per k-block");
+        // Descriptors of stage 0; a stage and a k-slice are fixed offsets (in
+        // 16-byte units) in the start-address field.
+        const uint32_t stage0 = ptx::smem_u32(stage_base);
+        const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
+        const uint64_t bdesc0 = C::B_MN ? ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024)
+                                        : ptx::sdesc_sw128(stage0 + C::A_BYTES, 16, 1024);
+        constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
+        constexpr uint64_t B_STEP = C::B_MN ? C::UMMA_K * 128 / 16 : C::UMMA_K * C::ES / 16;
+        constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
+        uint32_t it = 0, unit = 0, s = 0, ph = 0;   // (s, ph): ring slot and phase of k-block `it`
+        bool ok = true;
+        const int num_work = p.num_tiles * p.splits;
+        for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+            const Work wk = work_item(w, p);
+            for (int kb0 = wk.kb_lo; kb0 < wk.kb_hi; kb0 += p.kb_per_unit, ++unit) {
+                const uint32_t buf = unit & 1u;
+                const uint32_t uph = (unit >> 1) & 1u;
+                if (!wait_warp(acce0 + 8 * buf, uph ^ 1u, abort_flag, p.timeout_ns, p.status, DEV_TIMEOUT_MMA_ACC)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                const int kb1 = min(kb0 + p.kb_per_unit, wk.kb_hi);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    if (!wait_warp(full0 + 8 * s, ph, abort_flag, p.timeout_ns, p.status, DEV_TIMEOUT_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + buf * BN;
-                    const int kb1 = min(kb0 + p.kb_per_unit, wk.kb_hi);
-                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                        if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.timeout_ns, p.status,
-                                          DEV_TIMEOUT_MMA_FULL)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
-                        // A: K-major rows of 128 B, a k-slice steps UMMA_K elements along the row.
-                        // B N-major: a k-slice steps UMMA_K rows of 128 B (boxes B_BOX_BYTES apart,
-                        // the descriptor's leading offset); B K-major: as A.
-                        const uint64_t ad = adesc0 + s * S_STEP;
-                        const uint64_t bd = bdesc0 + s * S_STEP;
-#pragma unroll
-                        for (int ks = 0; ks < C::KSUB; ++ks) {
-                            const uint32_t acc = (kb > kb0 || ks > 0) ? 1u : 0u;
-                            if constexpr (IK == InKind::TF32)
-                                ptx::mma_tf32_ss(d_tmem, ad + ks * A_STEP, bd + ks * B_STEP, C::IDESC, acc);
-                            else
-                                ptx::mma_f16_ss(d_tmem, ad + ks * A_STEP, bd + ks * B_STEP, C::IDESC, acc);
-                        }
-                        ptx::mma_commit(empty0 + 8 * s);   // stage s free once these MMAs finish
-                        if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
-                        if (++s == STAGES) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                    ptx::mma_commit(accf0 + 8 * buf);      // accumulator ready for the epilogue
+                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
+                    // A: K-major rows of 128 B, a k-slice steps UMMA_K elements along the row.
+                    // B N-major: a k-slice steps UMMA_K rows of 128 B (boxes B_BOX_BYTES apart,
+                    // the descriptor's leading offset); B K-major: as A.
+                    const uint64_t ad = adesc0 + s * S_STEP;
+                    const uint64_t bd = bdesc0 + s * S_STEP;
+                    const uint32_t acc = kb > kb0 ? 1u : 0u;
+                    if constexpr (IK == InKind::TF32)
+                        ptx::mma_tf32_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                 bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC, acc);
+                    else
+                        ptx::mma_f16_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC, acc);
+                    ptx::mma_commit_elected(empty0 + 8 * s);   // stage s free once these MMAs finish
+                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                    const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
+                    s = wrap ? 0u : s + 1;
+                    ph ^= wrap;
                 }
+                if (!ok) break;
+                ptx::mma_commit_elected(accf0 + 8 * buf);      // accumulator ready for the epilogue
             }
-            if (!ok) {
-                ptx::mma_commit(drain_bar);
-                wait_drain(drain_bar, 0, p.timeout_ns);
-            }
+        }
+        if (!ok) {
+            ptx::mma_commit_elected(drain_bar);
+            if (lane == 0) wait_drain(drain_bar, 0, p.timeout_ns);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (four warps)
         const int q = warp & 3;   // TMEM lane quarter this warp may read
-        uint8_t* slab_pair = staging + (warp - C::EPI_WARP0) * 2 * C::SLAB_BYTES;
+        uint8_t* slab_pair = staging + (warp - C::EPI_WARP0) * C::EPI_SLOTS * C::SLAB_BYTES;
         int store_count = 0;
         uint32_t unit = 0;
         bool ok = true;
@@ -584,44 +638,18 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                             const uint32_t(&v)[32] =
                                 *reinterpret_cast<const uint32_t(*)[32]>(&iacc[c * 32]);
                             const int col0 = nb * BN + c * 32;
-                            store_slab<C::SLAB_BYTES, C::OUT_ES>(&tmC, slab_pair, store_count, v, lane,
+                            store_slab<C::SLAB_BYTES, C::OUT_ES, C::EPI_SLOTS>(&tmC, slab_pair, store_count, v, lane,
                                                                  col0, row0, p);
                         }
                     }
                 } else {
-#pragma unroll 1
-                    for (int c = 0; c < C::EPI_CHUNKS; ++c) {
-                        __syncwarp();   // tcgen05.ld is warp-collective
-                        uint32_t v[32];
-                        if constexpr (OK == OutKind::F32) {
-                            ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
-                            ptx::tmem_ld_wait(v);
-                        } else {
-                            uint32_t lo[32], hi[32];
-                            ptx::tmem_ld_32x32b_x32(tbase + c * 64, lo);
-                            ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, hi);
-                            ptx::tmem_ld_wait(lo);
-                            ptx::tmem_ld_wait(hi);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(lo[2 * i]),
-                                                                         __uint_as_float(lo[2 * i + 1]));
-                                v[i] = *reinterpret_cast<uint32_t*>(&t);
-                                __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(hi[2 * i]),
-                                                                         __uint_as_float(hi[2 * i + 1]));
-                                v[16 + i] = *reinterpret_cast<uint32_t*>(&u);
-                            }
-                        }
-                        if (c == C::EPI_CHUNKS - 1) {
+                    drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
+                        &tmC, slab_pair, store_count, tbase, lane, nb * BN, row0, p, [&]() {
                             // all of this unit's TMEM columns are in registers: free the accumulator
                             ptx::tc_fence_before();
                             __syncwarp();
                             if (lane == 0) ptx::mbar_arrive(acce0 + 8 * buf);
-                        }
-                        const int col0 = nb * BN + c * C::EPI_COLS;
-                        store_slab<C::SLAB_BYTES, C::OUT_ES>(&tmC, slab_pair, store_count, v, lane,
-                                                             col0, row0, p);
-                    }
+                        });
                 }
             }
         }

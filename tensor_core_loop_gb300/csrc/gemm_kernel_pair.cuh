@@ -22,7 +22,7 @@
 
 namespace tcl {
 
-template <OutKind OK, int BN_, int STAGES_>
+template <OutKind OK, int BN_, int STAGES_, int SLOTS_>
 struct PairCfg {
     static constexpr int STAGES = STAGES_;
     static constexpr int BM = 256;                   // rows per pair tile (128 per SM)
@@ -44,7 +44,8 @@ struct PairCfg {
     static constexpr int EPI_COLS = 128 / OUT_ES;
     static constexpr int EPI_CHUNKS = BN / EPI_COLS;
     static constexpr int SLAB_BYTES = 32 * 128;
-    static constexpr int STAGING_BYTES = 4 * 2 * SLAB_BYTES;
+    static constexpr int EPI_SLOTS = SLOTS_;          // staging slabs per epilogue warp (stores in flight)
+    static constexpr int STAGING_BYTES = 4 * EPI_SLOTS * SLAB_BYTES;
     static constexpr int ACC_STRIDE = 256;           // accumulator b starts at TMEM column b·256
     static constexpr int TMEM_COLS = 512;
     static constexpr int BAR_BYTES = 256;
@@ -78,17 +79,27 @@ __device__ __forceinline__ bool wait_bounded_pair(uint32_t bar, uint32_t parity,
     }
 }
 
+__device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                               uint32_t peer_abort, unsigned long long timeout_ns,
+                                               unsigned int* status, unsigned int code) {
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+        ok = wait_bounded_pair(bar, parity, abort_flag, peer_abort, timeout_ns, status, code) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ void spin_ns(unsigned long long ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < ns) {
     }
 }
 
-template <OutKind OK, int BN, int STAGES>
+template <OutKind OK, int BN, int STAGES, int SLOTS>
 __global__ void __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using C = PairCfg<OK, BN, STAGES>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -187,61 +198,62 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader CTA only)
-        if (leader && lane == 0) {
+        // All 32 lanes of the leader's MMA warp run the loop; the MMAs and
+        // commits come from one elected lane through predicates.
+        if (leader) {
             // Stage-0 descriptors; stages and k-slices are constant offsets of the
-            // start-address field (16-byte units), added in the issue loop.
+            // start-address field (16-byte units).
             const uint32_t stage0 = ptx::smem_u32(stage_base);
             const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
             const uint64_t bdesc0 = ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024);
             constexpr uint64_t A_STEP = C::UMMA_K * 2 / 16;
             constexpr uint64_t B_STEP = C::UMMA_K * 128 / 16;
             constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
+            static_assert(C::KSUB == 4, "four MMAs per k-block");
             uint32_t it = 0, unit = 0, s = 0, ph = 0;
             bool ok = true;
             for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters, ++unit) {
                 const uint32_t buf = unit & 1u;
                 const uint32_t uph = (unit >> 1) & 1u;
-                if (!wait_bounded_pair(acce0 + 8 * buf, uph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                       DEV_TIMEOUT_MMA_ACC)) {
+                if (!wait_warp_pair(acce0 + 8 * buf, uph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                    DEV_TIMEOUT_MMA_ACC)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * C::ACC_STRIDE;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    if (!wait_bounded_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                           DEV_TIMEOUT_MMA_FULL)) {
+                    if (!wait_warp_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                        DEV_TIMEOUT_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
+                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
                     const uint64_t ad = adesc0 + s * S_STEP;
                     const uint64_t bd = bdesc0 + s * S_STEP;
-#pragma unroll
-                    for (int ks = 0; ks < C::KSUB; ++ks)
-                        ptx::mma_f16_ss_pair(d_tmem, ad + ks * A_STEP, bd + ks * B_STEP, C::IDESC,
-                                             (kb > 0 || ks > 0) ? 1u : 0u);
-                    ptx::mma_commit_pair_multicast(empty0 + 8 * s, C::BOTH);
-                    if (tracing && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                 bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
+                                                 kb > 0 ? 1u : 0u);
+                    ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::BOTH);
+                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                    const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
+                    s = wrap ? 0u : s + 1;
+                    ph ^= wrap;
                 }
                 if (!ok) break;
-                ptx::mma_commit_pair_multicast(accf0 + 8 * buf, C::BOTH);
+                ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf, C::BOTH);
             }
             if (!ok) {
-                ptx::mma_commit_pair_multicast(drain_bar, 0x1);
-                wait_drain(drain_bar, 0, p.timeout_ns);
+                ptx::mma_commit_pair_multicast_elected(drain_bar, 0x1);
+                if (lane == 0) wait_drain(drain_bar, 0, p.timeout_ns);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (warps 2..5), both CTAs
         const int q = warp & 3;
-        uint8_t* slab_pair = staging + (warp - 2) * 2 * C::SLAB_BYTES;
+        uint8_t* slab_pair = staging + (warp - 2) * C::EPI_SLOTS * C::SLAB_BYTES;
         int store_count = 0;
         uint32_t unit = 0;
         bool ok = true;
@@ -261,37 +273,12 @@ __global__ void __launch_bounds__(192, 1)
             }
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
-#pragma unroll 1
-            for (int c = 0; c < C::EPI_CHUNKS; ++c) {
-                __syncwarp();
-                uint32_t v[32];
-                if constexpr (OK == OutKind::F32) {
-                    ptx::tmem_ld_32x32b_x32(tbase + c * 32, v);
-                    ptx::tmem_ld_wait(v);
-                } else {
-                    uint32_t lo[32], hi[32];
-                    ptx::tmem_ld_32x32b_x32(tbase + c * 64, lo);
-                    ptx::tmem_ld_32x32b_x32(tbase + c * 64 + 32, hi);
-                    ptx::tmem_ld_wait(lo);
-                    ptx::tmem_ld_wait(hi);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(lo[2 * i]),
-                                                                 __uint_as_float(lo[2 * i + 1]));
-                        v[i] = *reinterpret_cast<uint32_t*>(&t);
-                        __nv_bfloat162 u = __floats2bfloat162_rn(__uint_as_float(hi[2 * i]),
-                                                                 __uint_as_float(hi[2 * i + 1]));
-                        v[16 + i] = *reinterpret_cast<uint32_t*>(&u);
-                    }
-                }
-                if (c == C::EPI_CHUNKS - 1) {
+            drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
+                &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p, [&]() {
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
-                }
-                store_slab<C::SLAB_BYTES, C::OUT_ES>(&tmC, slab_pair, store_count, v, lane, nb * C::BN + c * C::EPI_COLS,
-                                                     row0, p);
-            }
+                });
         }
         if (lane == 0) ptx::bulk_wait<0>();
         __syncwarp();

@@ -5,9 +5,9 @@
 namespace tcl {
 namespace {
 
-template <OutKind OK, int BN, int STAGES>
+template <OutKind OK, int BN, int STAGES, int SLOTS>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
-    using C = PairCfg<OK, BN, STAGES>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
@@ -22,36 +22,36 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     return cfg;
 }
 
-template <OutKind OK, int BN, int STAGES>
+template <OutKind OK, int BN, int STAGES, int SLOTS>
 cudaError_t prepare() {
-    using C = PairCfg<OK, BN, STAGES>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS>;
     static bool done[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES);
     if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return err;
 }
 
-template <OutKind OK, int BN, int STAGES>
+template <OutKind OK, int BN, int STAGES, int SLOTS>
 cudaError_t launch_pair(const LaunchArgs& a) {
-    cudaError_t err = prepare<OK, BN, STAGES>();
+    cudaError_t err = prepare<OK, BN, STAGES, SLOTS>();
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES>(a.grid, a.stream, attr);
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES>, a.tmA, a.tmB, a.tmC, a.p);
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(a.grid, a.stream, attr);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS>, a.tmA, a.tmB, a.tmC, a.p);
 }
 
-template <OutKind OK, int BN, int STAGES>
+template <OutKind OK, int BN, int STAGES, int SLOTS>
 int max_clusters() {
-    if (prepare<OK, BN, STAGES>() != cudaSuccess) return 0;
+    if (prepare<OK, BN, STAGES, SLOTS>() != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES>(2, 0, attr);
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(2, 0, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -60,10 +60,10 @@ int max_clusters() {
 
 }  // namespace
 
-#define TCL_PAIR_CASE(OK, BN, ST)                                                   \
-    if (a.out == OutKind::OK && a.bn == BN && a.stages == ST) {                     \
+#define TCL_PAIR_CASE(OK, BN, ST, SL)                                               \
+    if (a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL) {    \
         *found = true;                                                              \
-        return launch_pair<OutKind::OK, BN, ST>(a);                                 \
+        return launch_pair<OutKind::OK, BN, ST, SL>(a);                             \
     }
 
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
@@ -73,10 +73,10 @@ cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
     return cudaErrorNotSupported;
 }
 
-#define TCL_PAIR_OCC(OK, BN, ST) \
-    if (out == OutKind::OK && bn == BN && stages == ST) return max_clusters<OutKind::OK, BN, ST>();
+#define TCL_PAIR_OCC(OK, BN, ST, SL) \
+    if (out == OutKind::OK && bn == BN && stages == ST && slots == SL) return max_clusters<OutKind::OK, BN, ST, SL>();
 
-int pair_max_clusters(OutKind out, int bn, int stages) {
+int pair_max_clusters(OutKind out, int bn, int stages, int slots) {
     TCL_GROUP_PAIR(TCL_PAIR_OCC)
     return 0;
 }

@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
     const uint32_t sa0 = ptx::smem_u32(smem);
     const uint32_t sb0 = sa0 + kPeakStages * kPeakA;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPeakStages * (kPeakA + kPeakB));
-    uint32_t* holder = reinterpret_cast<uint32_t*>(bar + 1);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(bar + 3);   // bar[0]: completion, bar[1]: ready, bar[2]: commits
     // operands: a fixed pseudo-random bf16/fp32 pattern of moderate magnitude
     for (int i = threadIdx.x; i < kPeakStages * (kPeakA + kPeakB) / 4; i += blockDim.x) {
         const uint32_t h = (static_cast<uint32_t>(i) * 2654435761u) >> 9;
@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
     ptx::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         ptx::mbar_init(ptx::smem_u32(bar), 1);
+        ptx::mbar_init(ptx::smem_u32(bar + 1), 1);
+        ptx::mbar_init(ptx::smem_u32(bar + 2), 1);
         ptx::fence_mbar_init();
     }
     if (threadIdx.x < 32) {
@@ -53,6 +55,9 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
         // 16 K-rows × 128 B, 2 KB apart), as in one k-slice of a GEMM tile
         constexpr uint32_t idesc = ptx::make_idesc(fmt, fmt, 0, B_MN ? 1u : 0u, 128, N);
         const bool chain = flags & 1, walk = flags & 2;
+        // bit 2: N-major B laid out as a GEMM stage holds it, 64-column groups of
+        // BK = 64 rows (8 KB apart) instead of 16 rows (2 KB apart)
+        const uint32_t b_lbo = (flags & 4) ? 8192u : 2048u;
         constexpr int KS = TF32 ? 4 : 4;   // k-slices per 128-byte row
         const uint64_t t0 = ptx::clock64();
         for (int i = 0; i < iters; ++i) {
@@ -60,14 +65,20 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
             const int st = walk ? ((i / KS) % kPeakStages) : 0;
             const uint32_t sa = sa0 + st * kPeakA, sb = sb0 + st * kPeakB;
             const uint64_t adesc = ptx::sdesc_sw128(sa + ks * 32, 16, 1024);
-            const uint64_t bdesc = B_MN ? ptx::sdesc_sw128(sb + ks * (TF32 ? 8 : 16) * 128, 2048, 1024)
+            const uint64_t bdesc = B_MN ? ptx::sdesc_sw128(sb + ks * (TF32 ? 8 : 16) * 128, b_lbo, 1024)
                                         : ptx::sdesc_sw128(sb + ks * 32, 16, 1024);
             const uint32_t d = tmem + ((!chain && (i & 1)) ? N : 0);
+            if ((flags & 8) && (i & 3) == 0) {
+                // a GEMM issue loop per 4 MMAs: wait on a (completed) stage barrier, fence
+                if (!ptx::mbar_try_wait(ptx::smem_u32(bar + 1), 1)) ptx::mbar_try_wait(ptx::smem_u32(bar + 1), 1);
+                ptx::tc_fence_after();
+            }
             const uint32_t acc = i >= (chain ? 1 : 2) ? 1u : 0u;
             if constexpr (TF32)
                 ptx::mma_tf32_ss(d, adesc, bdesc, idesc, acc);
             else
                 ptx::mma_f16_ss(d, adesc, bdesc, idesc, acc);
+            if ((flags & 8) && (i & 3) == 3) ptx::mma_commit(ptx::smem_u32(bar + 2));   // ... and commit the stage
         }
         ptx::mma_commit(ptx::smem_u32(bar));
         const uint64_t t_start = ptx::globaltimer_ns();
@@ -112,7 +123,7 @@ extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int
         (b_mn != 0 && b_mn != 1) || (in_kind == 1 && b_mn))
         return TCL_ERR_DIMS;
     static_assert(kPeakSmem <= kPeakRequest, "probe fits its shared memory request");
-    if (flags < 0 || flags > 3) return TCL_ERR_CONFIG;
+    if (flags < 0 || flags > 15) return TCL_ERR_CONFIG;
     int dev = 0, sms = 0;
     unsigned int* status = nullptr;
     int st = device_context(&dev, &sms, &status);

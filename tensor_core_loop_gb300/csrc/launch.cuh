@@ -15,7 +15,8 @@ struct LaunchArgs {
     int bn;
     int stages;
     int prod;   // PROD_TMA or PROD_SYNC
-    int pair;   // 1: two-SM kernel (cluster of two CTAs per 256×256 tile)
+    int pair;   // 1: two-SM kernel (cluster of two CTAs per 256-row tile)
+    int slots;  // epilogue staging slabs per warp (two-SM kernel)
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
     int grid;
@@ -31,7 +32,7 @@ cudaError_t launch_group_bf16_sync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
 // Largest number of two-CTA clusters of the given pair variant that can be
 // resident at once on the current device (0 on error).
-int pair_max_clusters(OutKind out, int bn, int stages);
+int pair_max_clusters(OutKind out, int bn, int stages, int slots);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
 // int8 -> bf16 widening (exact) into a packed row-major buffer with ld_dst
@@ -59,6 +60,7 @@ struct VariantInfo {
     int smem_bytes;
     int threads;
     int pair;
+    int slots;
 };
 int variant_table(const VariantInfo** table);
 
@@ -92,13 +94,15 @@ cudaError_t launch_variant(const LaunchArgs& a) {
 
 #define TCL_VARIANT_INFO(IK, OK, BN, ST, PR)                                               \
     {InKind::IK, OutKind::OK, BN, ST, PR, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::SMEM_BYTES, \
-     KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS, 0},
+     KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS, 0, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::EPI_SLOTS},
 
-// Two-SM variants (bf16 in, TMA producer, 256-row pair tiles): output, tile width, ring depth.
-#define TCL_GROUP_PAIR(X) X(F32, 256, 6) X(F32, 256, 4) X(BF16, 256, 6) X(F32, 224, 6)
-#define TCL_PAIR_INFO(OK, BN, ST)                                                                       \
-    {InKind::BF16, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST>::SMEM_BYTES,                    \
-     PairCfg<OutKind::OK, BN, ST>::THREADS, 1},
+// Two-SM variants (bf16 in, TMA producer, 256-row pair tiles): output, tile
+// width, ring depth, epilogue staging slabs per warp.
+#define TCL_GROUP_PAIR(X) \
+    X(F32, 256, 6, 2) X(F32, 256, 4, 2) X(BF16, 256, 6, 2) X(F32, 224, 6, 2) X(F32, 224, 5, 4) X(BF16, 256, 5, 4)
+#define TCL_PAIR_INFO(OK, BN, ST, SL)                                                                   \
+    {InKind::BF16, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL>::SMEM_BYTES,                \
+     PairCfg<OutKind::OK, BN, ST, SL>::THREADS, 1, SL},
 
 #define TCL_VARIANT_CASE(IK, OK, BN, ST, PR)                                                           \
     if (!a.pair && a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \

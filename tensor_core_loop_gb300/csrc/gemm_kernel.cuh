@@ -478,49 +478,48 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
         sync_producer<C>(p, stage_base, full0, empty0, abort_flag, tracing);
     } else if (warp == 0) {
         // ------------------------------------------------ producer (TMA)
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            const int num_work = p.num_tiles * p.splits;
-            for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
-                const Work wk = work_item(w, p);
-                const int mb = wk.mb, nb = wk.nb;
-                for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
-                                      DEV_TIMEOUT_PRODUCER)) {
-                        ok = false;
-                        break;
-                    }
-                    if (tracing) {
-                        const uint64_t now = ptx::clock64();
-                        if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap)
-                            p.trace[4 * (it - STAGES) + 3] = now;   // MMA of block it-STAGES done
-                        if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;   // load issued
-                    }
-                    const uint32_t full = full0 + 8 * s;
-                    const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
-                    if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) continue;
-                    ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
-                    ptx::tma_load_2d(sa, &tmA, full, kb * C::BK, mb * C::BM);
-                    if constexpr (C::B_MN) {
+        // All 32 lanes run the loop; the arrival and the copies come from one
+        // elected lane.
+        uint32_t it = 0;
+        bool ok = true;
+        const int num_work = p.num_tiles * p.splits;
+        for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+            const Work wk = work_item(w, p);
+            const int mb = wk.mb, nb = wk.nb;
+            for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
+                const uint32_t s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!wait_warp(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status, DEV_TIMEOUT_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                if (tracing && lane == 0) {
+                    const uint64_t now = ptx::clock64();
+                    if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap)
+                        p.trace[4 * (it - STAGES) + 3] = now;   // MMA of block it-STAGES done
+                    if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;   // load issued
+                }
+                const uint32_t full = full0 + 8 * s;
+                const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+                if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) continue;
+                ptx::mbar_arrive_expect_tx_elected(full, C::STAGE_BYTES);
+                ptx::tma_load_2d_elected(sa, &tmA, full, kb * C::BK, mb * C::BM);
+                if constexpr (C::B_MN) {
 #pragma unroll
-                        for (int b = 0; b < C::B_BOXES; ++b) {
-                            ptx::tma_load_2d(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
-                                             nb * BN + b * C::B_BOX_N, kb * C::BK);
-                        }
-                    } else {
-                        ptx::tma_load_2d(sa + C::A_BYTES, &tmB, full, kb * C::BK, nb * BN);
+                    for (int b = 0; b < C::B_BOXES; ++b) {
+                        ptx::tma_load_2d_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
+                                                 nb * BN + b * C::B_BOX_N, kb * C::BK);
                     }
+                } else {
+                    ptx::tma_load_2d_elected(sa + C::A_BYTES, &tmB, full, kb * C::BK, nb * BN);
                 }
             }
-            if (!ok) {
-                // Let every load still in flight land before the CTA can exit.
-                const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-                for (uint32_t j = first; j < it; ++j)
-                    wait_drain(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
-            }
+        }
+        if (!ok && lane == 0) {
+            // Let every load still in flight land before the CTA can exit.
+            const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+            for (uint32_t j = first; j < it; ++j)
+                wait_drain(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == C::MMA_WARP) {

@@ -161,40 +161,39 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ producer (TMA), both CTAs
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters) {
-                int mb, nb;
-                tile_coords(tile, p, mb, nb);
-                const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
-                const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bounded_pair(empty0 + 8 * s, ph ^ 1u, abort_flag, peer_abort, p.timeout_ns,
-                                           p.status, DEV_TIMEOUT_PRODUCER)) {
-                        ok = false;
-                        break;
-                    }
-                    if (tracing) {
-                        const uint64_t now = ptx::clock64();
-                        if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap)
-                            p.trace[4 * (it - STAGES) + 3] = now;
-                        if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;
-                    }
-                    if (leader) ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::PAIR_TX);
-                    const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
-                    const uint32_t fb = full_leader0 + 8 * s;
-                    ptx::tma_load_2d_pair(sa, &tmA, fb, kb * C::BK, row);
-#pragma unroll
-                    for (int b = 0; b < C::B_BOXES; ++b)
-                        ptx::tma_load_2d_pair(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, fb, col + b * C::B_BOX_N,
-                                              kb * C::BK);
+        // All 32 lanes run the loop; the arrival and the copies come from one
+        // elected lane.
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters) {
+            int mb, nb;
+            tile_coords(tile, p, mb, nb);
+            const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
+            const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
+            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const uint32_t s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!wait_warp_pair(empty0 + 8 * s, ph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                    DEV_TIMEOUT_PRODUCER)) {
+                    ok = false;
+                    break;
                 }
+                if (tracing && lane == 0) {
+                    const uint64_t now = ptx::clock64();
+                    if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap) p.trace[4 * (it - STAGES) + 3] = now;
+                    if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;
+                }
+                if (leader) ptx::mbar_arrive_expect_tx_elected(full0 + 8 * s, C::PAIR_TX);
+                const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+                const uint32_t fb = full_leader0 + 8 * s;
+                ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kb * C::BK, row);
+#pragma unroll
+                for (int b = 0; b < C::B_BOXES; ++b)
+                    ptx::tma_load_2d_pair_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, fb, col + b * C::B_BOX_N,
+                                                  kb * C::BK);
             }
-            if (!ok) spin_ns(200000);   // copies issued before the abort land within microseconds
         }
+        if (!ok && lane == 0) spin_ns(200000);   // copies issued before the abort land within microseconds
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader CTA only)

@@ -272,6 +272,38 @@ __device__ __forceinline__ void mma_commit_pair_multicast_elected(uint32_t bar, 
         : "memory");
 }
 
+// Elected-lane forms of the producer's operations (one arrival, one copy per warp).
+__device__ __forceinline__ void mbar_arrive_expect_tx_elected(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_elected(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                                    int32_t c1) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_elected(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                         int32_t c0, int32_t c1) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- clusters / CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

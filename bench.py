@@ -369,13 +369,16 @@ def run_peak(args):
     sampler.start()
     rows = []
     combos = [(0, 256, 1), (0, 256, 0), (0, 128, 1), (0, 128, 0), (1, 256, 0), (1, 128, 0)]
-    for kind, n, b_mn, flags in [c + (f,) for c in combos for f in (0, 1, 2, 3)]:
+    # flags: 2 = walk operands like a k-loop; 11 = also one chained accumulator and the
+    # rest of a GEMM issue loop (barrier wait, fence, commit per four MMAs)
+    for kind, n, b_mn, flags in [c + (f,) for c in combos for f in (2, 11)]:
         tcl.mma_peak(kind, n, b_mn, iters=512, flags=flags)          # warm-up
         cyc, rate, ms = tcl.mma_peak(kind, n, b_mn, iters=16384, flags=flags)
         k = 16 if kind == 0 else 8
         flops = 2.0 * 128 * n * k * 16384 * sms
         rows.append({"peak": "bf16" if kind == 0 else "tf32", "n": n, "b_major": "MN" if b_mn else "K",
                      "one_accumulator": bool(flags & 1), "walk_operands": bool(flags & 2),
+                     "gemm_issue_loop": bool(flags & 8),
                      "flop_per_clk_per_sm": round(rate, 1), "cycles_per_mma": round(max(cyc) / 16384, 2),
                      "tflops_all_sms": round(flops / (ms * 1e-3) / 1e12, 1), "sms": sms})
     clocks = sampler.stop()

@@ -197,7 +197,8 @@ typedef struct {
 TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, tcl_plan_t* plan);
 
 /* Tensor-pipe rate probe (measurement, not part of the GEMM): `grid` CTAs
- * (one per SM) each issue `iters` back-to-back tcgen05.mma of shape
+ * (one per SM) each issue `iters` (a multiple of 4, at least 8) back-to-back
+ * tcgen05.mma, four at a time from one elected lane of a converged warp, of shape
  * M=128 × N=n × K=16 (bf16, in_kind 0) or K=8 (TF32, in_kind 1) on operands
  * already in shared memory (B K-major, or N-major if b_mn = 1; bf16 only),
  * and write the %clock64 cycles from the first issue to the completion of the

@@ -49,7 +49,10 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *holder;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
+        // Warp 0 runs the issue loop converged; one elected lane issues every MMA
+        // (four per k-slice group, as the GEMM kernels do), so the probe measures
+        // the tensor pipe rather than a lone thread's loop.
         constexpr uint32_t fmt = TF32 ? 2u : 1u;
         // A K-major; B K-major (N rows of 128 B) or N-major (N/64 column groups of
         // 16 K-rows × 128 B, 2 KB apart), as in one k-slice of a GEMM tile
@@ -58,37 +61,44 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
         // bit 2: N-major B laid out as a GEMM stage holds it, 64-column groups of
         // BK = 64 rows (8 KB apart) instead of 16 rows (2 KB apart)
         const uint32_t b_lbo = (flags & 4) ? 8192u : 2048u;
-        constexpr int KS = TF32 ? 4 : 4;   // k-slices per 128-byte row
         const uint64_t t0 = ptx::clock64();
-        for (int i = 0; i < iters; ++i) {
-            const int ks = walk ? (i % KS) : 0;
-            const int st = walk ? ((i / KS) % kPeakStages) : 0;
+        for (int i = 0; i < iters; i += 4) {
+            // four MMAs on the four k-slices of one stage (or on one k-slice)
+            const int st = walk ? ((i / 4) % kPeakStages) : 0;
             const uint32_t sa = sa0 + st * kPeakA, sb = sb0 + st * kPeakB;
-            const uint64_t adesc = ptx::sdesc_sw128(sa + ks * 32, 16, 1024);
-            const uint64_t bdesc = B_MN ? ptx::sdesc_sw128(sb + ks * (TF32 ? 8 : 16) * 128, b_lbo, 1024)
-                                        : ptx::sdesc_sw128(sb + ks * 32, 16, 1024);
-            const uint32_t d = tmem + ((!chain && (i & 1)) ? N : 0);
-            if ((flags & 8) && (i & 3) == 0) {
-                // a GEMM issue loop per 4 MMAs: wait on a (completed) stage barrier, fence
-                if (!ptx::mbar_try_wait(ptx::smem_u32(bar + 1), 1)) ptx::mbar_try_wait(ptx::smem_u32(bar + 1), 1);
+            uint64_t ad[4], bd[4];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int k = walk ? ks : 0;
+                ad[ks] = ptx::sdesc_sw128(sa + k * 32, 16, 1024);
+                bd[ks] = B_MN ? ptx::sdesc_sw128(sb + k * (TF32 ? 8 : 16) * 128, b_lbo, 1024)
+                              : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+            }
+            const uint32_t d = tmem + ((!chain && ((i / 4) & 1)) ? N : 0);
+            if ((flags & 8)) {
+                // the rest of a GEMM issue loop: wait on a (completed) stage barrier, fence
+                __all_sync(0xffffffffu, ptx::mbar_try_wait(ptx::smem_u32(bar + 1), 1));
                 ptx::tc_fence_after();
             }
-            const uint32_t acc = i >= (chain ? 1 : 2) ? 1u : 0u;
+            const uint32_t acc = i >= (chain ? 4 : 8) ? 1u : 0u;
             if constexpr (TF32)
-                ptx::mma_tf32_ss(d, adesc, bdesc, idesc, acc);
+                ptx::mma_tf32_x4_elected(d, ad[0], bd[0], ad[1], bd[1], ad[2], bd[2], ad[3], bd[3], idesc, acc);
             else
-                ptx::mma_f16_ss(d, adesc, bdesc, idesc, acc);
-            if ((flags & 8) && (i & 3) == 3) ptx::mma_commit(ptx::smem_u32(bar + 2));   // ... and commit the stage
+                ptx::mma_f16_x4_elected(d, ad[0], bd[0], ad[1], bd[1], ad[2], bd[2], ad[3], bd[3], idesc, acc);
+            if ((flags & 8)) ptx::mma_commit_elected(ptx::smem_u32(bar + 2));   // ... and commit the stage
         }
-        ptx::mma_commit(ptx::smem_u32(bar));
-        const uint64_t t_start = ptx::globaltimer_ns();
+        ptx::mma_commit_elected(ptx::smem_u32(bar));
         bool done = false;
-        while (!(done = ptx::mbar_try_wait(ptx::smem_u32(bar), 0))) {
-            if (ptx::globaltimer_ns() - t_start > timeout_ns) break;
+        if ((threadIdx.x & 31) == 0) {
+            const uint64_t t_start = ptx::globaltimer_ns();
+            while (!(done = ptx::mbar_try_wait(ptx::smem_u32(bar), 0))) {
+                if (ptx::globaltimer_ns() - t_start > timeout_ns) break;
+            }
+            const uint64_t t1 = ptx::clock64();
+            cycles[blockIdx.x] = done ? (t1 - t0) : 0ull;
+            if (!done) atomicCAS(status, 0u, static_cast<unsigned int>(DEV_TIMEOUT_MMA_FULL));
         }
-        const uint64_t t1 = ptx::clock64();
-        cycles[blockIdx.x] = done ? (t1 - t0) : 0ull;
-        if (!done) atomicCAS(status, 0u, static_cast<unsigned int>(DEV_TIMEOUT_MMA_FULL));
+        __syncwarp();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -119,7 +129,7 @@ using namespace tcl;
 extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
                                     unsigned long long* cycles, cudaStream_t stream) {
     if (!cycles) return TCL_ERR_NULL;
-    if (iters < 2 || grid < 1 || (n != 128 && n != 256) || (in_kind != 0 && in_kind != 1) ||
+    if (iters < 8 || iters % 4 || grid < 1 || (n != 128 && n != 256) || (in_kind != 0 && in_kind != 1) ||
         (b_mn != 0 && b_mn != 1) || (in_kind == 1 && b_mn))
         return TCL_ERR_DIMS;
     static_assert(kPeakSmem <= kPeakRequest, "probe fits its shared memory request");

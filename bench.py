@@ -244,9 +244,12 @@ def time_flushed(fn, args_, iters, stream, torch, flush):
     return times[len(times) // 2]
 
 
-ABLATION = [  # (label, producer, ring depth): the pages' ladder, sync copy first, then TMA
+ABLATION = [  # (label, producer, ring depth): the pages' ladder, sync copy, then cp.async, then TMA
     ("sync, 1 stage", 1, 1), ("sync, 2 stages", 1, 2), ("sync, 4 stages", 1, 4),
+    ("cp.async, 1 stage", 2, 1), ("cp.async, 2 stages", 2, 2), ("cp.async, 3 stages", 2, 3),
+    ("cp.async, 4 stages", 2, 4),
     ("TMA, 1 stage", 0, 1), ("TMA, 2 stages", 0, 2), ("TMA, 3 stages", 0, 3), ("TMA, 4 stages", 0, 4)]
+PRODUCER_NAMES = {0: "tma", 1: "sync", 2: "cp.async"}
 
 
 def compute_load_ratio(bm, bn, bk, esize):
@@ -285,7 +288,7 @@ def run_ablation(args):
             line = {"ablation": label, "shape": f"{m}x{n}x{k}", "tflops": round(tf, 1), "us": round(ms * 1e3, 2),
                     "delta_vs_prev_pct": None if prev is None else round(100.0 * (tf / prev - 1.0), 1),
                     "compute_load_ratio": round(ratio, 1), "bn": 256, "stages": stages,
-                    "producer": "sync" if prod else "tma"}
+                    "producer": PRODUCER_NAMES[prod]}
             prev = tf
             print(json.dumps(line), flush=True)
 
@@ -355,7 +358,8 @@ def run_trace(args):
             c0, g0, c1, g1 = tt[4 * cap:]
             line = {"trace": f"{m}x{n}x{k}", "sm_mhz_in_kernel": round(1e3 * (c1 - c0) / max(1, g1 - g0), 1), "cta_pair": pl["cta_pair"], "bn": pl["bn"], "stages": pl["stages"],
                     "tiles_cta0": tiles_cta0}
-            line.update(trace_stats(t, pl["stages"], pl["bn"] if pl["cta_pair"] == 1 else 256, num_kb))
+            # each SM computes 128 rows × bn columns per k-block in either kernel
+            line.update(trace_stats(t, pl["stages"], pl["bn"], num_kb))
             print(json.dumps(line), flush=True)
 
 

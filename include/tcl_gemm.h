@@ -99,7 +99,11 @@ typedef struct {
     int trace_cap;                 /* k-blocks the trace buffer holds */
     int producer;                  /* 0 (default): TMA bulk-tensor loads issued by one thread;
                                       1: synchronous copy by four warps (ld.global -> registers ->
-                                      st.shared), the ablation's lower rung; bf16 only */
+                                      st.shared), the ablation's lowest rung; 2: asynchronous copy
+                                      by four warps (16-byte cp.async into shared memory, each
+                                      thread's mbarrier arrival fires when its copies land), the
+                                      middle rung. 1 and 2: bf16 only, one SM per tile, no
+                                      debug_skip_kblock */
     int split_k;                   /* 0: automatic (when the output tiles alone would leave most SMs
                                       idle, K is cut into ranges whose fp32 partial tiles a second
                                       kernel adds in a fixed order); 1: never; s > 1: s ranges.
@@ -186,7 +190,7 @@ typedef struct {
     int smem_bytes;                 /* dynamic shared memory per CTA */
     int cta_pair;                   /* 1: one SM per tile; 2: two SMs per tile */
     int splits;                     /* K ranges (1: no split-K) */
-    int producer;                   /* 0: TMA, 1: synchronous copy */
+    int producer;                   /* 0: TMA, 1: synchronous copy, 2: cp.async */
     unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
 } tcl_plan_t;
 

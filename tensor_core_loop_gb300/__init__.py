@@ -28,6 +28,7 @@ STATUS = {
     9: "TCL_ERR_NO_MEMORY", 10: "TCL_ERR_DEVICE", 11: "TCL_ERR_STATIC_LIMIT",
 }
 OUT_F32, OUT_BF16 = 0, 1
+PRODUCER_TMA, PRODUCER_SYNC, PRODUCER_CPASYNC = 0, 1, 2
 IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",

@@ -41,6 +41,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 const VariantInfo kVariants[] = {
     TCL_GROUP_BF16_F32_BN256(TCL_VARIANT_INFO) TCL_GROUP_BF16_F32_BN128(TCL_VARIANT_INFO)
         TCL_GROUP_BF16_MISC(TCL_VARIANT_INFO) TCL_GROUP_BF16_SYNC(TCL_VARIANT_INFO)
+            TCL_GROUP_BF16_CPASYNC(TCL_VARIANT_INFO)
             TCL_GROUP_TF32(TCL_VARIANT_INFO) TCL_GROUP_PAIR(TCL_PAIR_INFO)};
 
 struct MapKey {
@@ -225,7 +226,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
               PairClusters pair_clusters, Plan* pl) {
     const int bk = 128 / in_bytes(ik);
     const int prod = cfg ? cfg->producer : PROD_TMA;
-    if (prod != PROD_TMA && prod != PROD_SYNC) return TCL_ERR_CONFIG;
+    if (prod != PROD_TMA && prod != PROD_SYNC && prod != PROD_CPASYNC) return TCL_ERR_CONFIG;
     const int want_pair = cfg ? cfg->cta_pair : 0;
     if (want_pair < 0 || want_pair > 2) return TCL_ERR_CONFIG;
     int bn = cfg ? cfg->bn : 0;
@@ -439,6 +440,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
         if (!found) err = launch_group_bf16_f32_bn128(a, &found);
         if (!found) err = launch_group_bf16_misc(a, &found);
         if (!found) err = launch_group_bf16_sync(a, &found);
+        if (!found) err = launch_group_bf16_cpasync(a, &found);
     }
     if (!found) return TCL_ERR_CONFIG;
     if (err != cudaSuccess) {

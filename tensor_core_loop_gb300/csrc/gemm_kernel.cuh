@@ -112,10 +112,13 @@ __device__ __forceinline__ Work work_item(int w, const GemmParams& p) {
     return r;
 }
 
-// Producer kinds: TMA bulk-tensor copies issued by one thread, or the
+// Producer kinds: TMA bulk-tensor copies issued by one elected lane; the
 // synchronous variant (four warps: ld.global into registers, st.shared into
-// the same swizzled layout, then an mbarrier arrive) used for the ablation.
-enum : int { PROD_TMA = 0, PROD_SYNC = 1 };
+// the same swizzled layout, then an mbarrier arrive); the cp.async variant
+// (four warps issue 16-byte asynchronous copies straight into the swizzled
+// layout, each thread's arrival fires when its copies land). The last two are
+// the rungs below TMA in the ablation.
+enum : int { PROD_TMA = 0, PROD_SYNC = 1, PROD_CPASYNC = 2 };
 
 constexpr int pow2_at_least(int x, int lo) {
     int p = lo;
@@ -126,10 +129,10 @@ constexpr int pow2_at_least(int x, int lo) {
 template <InKind IK, OutKind OK, int BN_, int STAGES_, int PROD_ = PROD_TMA>
 struct KCfg {
     static constexpr int PROD = PROD_;
-    static constexpr int P_WARPS = PROD == PROD_SYNC ? 4 : 1;   // producer warps
+    static constexpr int P_WARPS = PROD == PROD_TMA ? 1 : 4;    // producer warps
     static constexpr int MMA_WARP = P_WARPS;                    // then the MMA warp
     static constexpr int EPI_WARP0 = P_WARPS + 1;               // then four epilogue warps
-    static constexpr int FULL_ARRIVALS = PROD == PROD_SYNC ? 32 * P_WARPS : 1;
+    static constexpr int FULL_ARRIVALS = PROD == PROD_TMA ? 1 : 32 * P_WARPS;
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
@@ -171,7 +174,8 @@ struct KCfg {
     static_assert(STAGES >= 1 && 2 * STAGES + 5 <= 28, "barrier area");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(OK != OutKind::S32 || BN <= 128, "exact integer drain keeps BN int32 sums in registers");
-    static_assert(PROD == PROD_TMA || (IK == InKind::BF16 && B_MN), "synchronous producer: bf16 only");
+    static_assert(PROD == PROD_TMA || PROD == PROD_SYNC || PROD == PROD_CPASYNC, "producer kind");
+    static_assert(PROD == PROD_TMA || (IK == InKind::BF16 && B_MN), "thread-copy producers: bf16 only");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
@@ -372,6 +376,73 @@ __device__ __forceinline__ void sync_producer(const GemmParams& p, uint8_t* stag
     }
 }
 
+// Asynchronous-copy producer (the ablation's middle rung): the four producer
+// warps issue one 16-byte cp.async per chunk of the stage, straight into the
+// 128-byte-swizzled layout (no register staging), then each thread arms an
+// arrival on full[s] that fires once all of its copies have landed, and moves
+// on to the next stage without waiting. Out-of-range chunks copy zero bytes
+// (zero fill); a chunk that straddles the right edge of B copies only its
+// in-range columns. cp.async writes through the generic proxy, so the MMA warp
+// fences toward the async proxy after it has seen full[s] complete.
+template <class C>
+__device__ __forceinline__ void cpasync_producer(const GemmParams& p, uint8_t* stage_base, uint32_t full0,
+                                                 uint32_t empty0, volatile uint32_t* abort_flag, bool tracing) {
+    constexpr int PT = 32 * C::P_WARPS;
+    constexpr int A_PER = C::BM * 8 / PT;
+    constexpr int B_PER = C::B_BOXES * C::BK * 8 / PT;
+    static_assert(A_PER * PT == C::BM * 8 && B_PER * PT == C::B_BOXES * C::BK * 8, "chunk split");
+    const int pt = threadIdx.x;
+    const int lane = pt & 31;
+    const uint16_t* Ag = static_cast<const uint16_t*>(p.A);
+    const uint16_t* Bg = static_cast<const uint16_t*>(p.B);
+    uint32_t it = 0;
+    const int num_work = p.num_tiles * p.splits;
+    for (int w = blockIdx.x; w < num_work; w += gridDim.x) {
+        const Work wk = work_item(w, p);
+        const int mb = wk.mb, nb = wk.nb;
+        for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
+            const uint32_t s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1u;
+            bool got = true;
+            if (lane == 0)
+                got = wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                                   DEV_TIMEOUT_PRODUCER);
+            if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                ptx::cp_async_wait_all();   // nothing may still be writing when the CTA exits
+                return;
+            }
+            if (tracing && pt == 0) {
+                const uint64_t now = ptx::clock64();
+                if (it >= C::STAGES && it - C::STAGES < (uint32_t)p.trace_cap)
+                    p.trace[4 * (it - C::STAGES) + 3] = now;
+                if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;
+            }
+            const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
+            const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+            for (int i = 0; i < A_PER; ++i) {
+                const int c = pt + i * PT, row = c >> 3, j = c & 7;
+                const int gm = mb * C::BM + row, gk = kb * C::BK + j * 8;
+                const bool in = gm < p.M && gk < p.K;
+                const uint16_t* src = in ? Ag + static_cast<long long>(gm) * p.lda + gk : Ag;
+                ptx::cp_async_16(sa + row * 128 + ((j ^ (row & 7)) << 4), src, in ? 16u : 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < B_PER; ++i) {
+                const int c = pt + i * PT, box = c / (C::BK * 8), r = c % (C::BK * 8);
+                const int k = r >> 3, j = r & 7;
+                const int gk = kb * C::BK + k, gn = nb * C::BN + box * C::B_BOX_N + j * 8;
+                const bool in = gk < p.K && gn < p.N;
+                const uint32_t bytes = in ? 2u * static_cast<uint32_t>(min(8, p.N - gn)) : 0u;
+                const uint16_t* src = in ? Bg + static_cast<long long>(gk) * p.ldb + gn : Bg;
+                ptx::cp_async_16(sb + box * C::B_BOX_BYTES + k * 128 + ((j ^ (k & 7)) << 4), src, bytes);
+            }
+            ptx::cp_async_arrive_noinc(full0 + 8 * s);
+        }
+    }
+    ptx::cp_async_wait_all();
+}
+
 // Drains one TMEM accumulator (this warp's 32 lanes × EPI_CHUNKS chunks) to C:
 // F32 chunks are 32 fp32 columns, BF16 chunks 64 fp32 columns rounded to 64
 // bf16. The TMEM load of chunk c+1 is issued before chunk c is staged and
@@ -476,6 +547,9 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
     if (warp < C::P_WARPS && PROD == PROD_SYNC) {
         // ------------------------------------------------ producer (synchronous, ablation)
         sync_producer<C>(p, stage_base, full0, empty0, abort_flag, tracing);
+    } else if (warp < C::P_WARPS && PROD == PROD_CPASYNC) {
+        // ------------------------------------------------ producer (cp.async, ablation)
+        cpasync_producer<C>(p, stage_base, full0, empty0, abort_flag, tracing);
     } else if (warp == 0) {
         // ------------------------------------------------ producer (TMA)
         // All 32 lanes run the loop; the arrival and the copies come from one
@@ -559,6 +633,8 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after();
+                    // cp.async data arrived through the generic proxy: order it before the MMA's reads
+                    if constexpr (PROD == PROD_CPASYNC) ptx::fence_proxy_async_smem();
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
                     // A: K-major rows of 128 B, a k-slice steps UMMA_K elements along the row.
                     // B N-major: a k-slice steps UMMA_K rows of 128 B (boxes B_BOX_BYTES apart,

@@ -14,7 +14,7 @@ struct LaunchArgs {
     OutKind out;
     int bn;
     int stages;
-    int prod;   // PROD_TMA or PROD_SYNC
+    int prod;   // PROD_TMA, PROD_SYNC or PROD_CPASYNC
     int pair;   // 1: two-SM kernel (cluster of two CTAs per 256-row tile)
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
     CUtensorMap tmA, tmB, tmC;
@@ -29,6 +29,7 @@ cudaError_t launch_group_bf16_f32_bn256(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_f32_bn128(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_misc(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_sync(const LaunchArgs& a, bool* found);
+cudaError_t launch_group_bf16_cpasync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
 // Largest number of two-CTA clusters of the given pair variant that can be
 // resident at once on the current device (0 on error).
@@ -90,6 +91,8 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     X(BF16, F32, 128, 1, 0) X(BF16, F32, 128, 2, 0) X(BF16, F32, 128, 4, 0) X(BF16, F32, 128, 6, 0)
 #define TCL_GROUP_BF16_MISC(X) X(BF16, BF16, 256, 4, 0) X(BF16, BF16, 128, 6, 0) X(BF16, S32, 128, 6, 0)
 #define TCL_GROUP_BF16_SYNC(X) X(BF16, F32, 256, 1, 1) X(BF16, F32, 256, 2, 1) X(BF16, F32, 256, 4, 1)
+#define TCL_GROUP_BF16_CPASYNC(X) \
+    X(BF16, F32, 256, 1, 2) X(BF16, F32, 256, 2, 2) X(BF16, F32, 256, 3, 2) X(BF16, F32, 256, 4, 2)
 #define TCL_GROUP_TF32(X) X(TF32, F32, 256, 4, 0) X(TF32, F32, 128, 6, 0)
 
 #define TCL_VARIANT_INFO(IK, OK, BN, ST, PR)                                               \

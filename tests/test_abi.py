@@ -124,6 +124,19 @@ def test_plan_without_device(L):
         tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stages=5))
 
 
+def test_planner_producer_kinds(L):
+    for prod in (tcl.PRODUCER_SYNC, tcl.PRODUCER_CPASYNC):
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, producer=prod))
+        # thread-copy producers: one SM per tile, four producer warps in front of the MMA warp
+        assert p["producer"] == prod and p["cta_pair"] == 1 and p["bn"] == 256
+    for bad in (3, -1):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, producer=bad))
+    for kind in (tcl.IN_TF32, tcl.IN_S8):   # the thread-copy producers are bf16 only
+        with pytest.raises(tcl.TclError):
+            tcl.plan(kind, 0, 512, 512, 512, tcl.Config(max_ctas=152, producer=tcl.PRODUCER_CPASYNC))
+
+
 def test_every_stage_count_fits_shared_memory(L):
     for bn, stages in [(256, 1), (256, 2), (256, 3), (256, 4), (128, 1), (128, 2), (128, 4), (128, 6)]:
         p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 1024, 1024, 1024, tcl.Config(max_ctas=8, bn=bn, stages=stages))

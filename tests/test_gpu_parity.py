@@ -145,6 +145,15 @@ def test_bf16_sync_producer(oracle_mod, stages):
     bf16_case(oracle_mod, 130, 261, 200, seed=10, cfg=tcl.Config(bn=256, stages=stages, producer=1), ldc=264)
 
 
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_bf16_cpasync_producer(oracle_mod, stages):
+    cfg = tcl.Config(bn=256, stages=stages, producer=tcl.PRODUCER_CPASYNC)
+    bf16_case(oracle_mod, 384, 512, 640, seed=9, cfg=cfg)
+    # ragged M, N (a chunk straddling the right edge copies only its in-range columns) and K
+    bf16_case(oracle_mod, 130, 261, 200, seed=10, cfg=cfg, ldc=264)
+    bf16_case(oracle_mod, 1, 9, 8, seed=11, cfg=cfg)
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 512, 1024), (300, 520, 200), (130, 261, 72), (1, 8, 8),
                                    (777, 1000, 1216), (1024, 768, 4096)])
 def test_bf16_pair_kernel(oracle_mod, M, N, K):
@@ -228,9 +237,12 @@ def test_variants_bitwise_identical():
                     cfg = tcl.Config(bn=bn, stages=st, one_cta_per_tile=one_per_tile, max_ctas=max_ctas,
                                      group_m=3 if max_ctas else 0, split_k=1)
                     outs.append(run(a, b, cfg=cfg, canary=False))
-        if bn == 256:   # the synchronous producer feeds the same MMA sequence
+        if bn == 256:   # the synchronous and cp.async producers feed the same MMA sequence
             for st in (1, 2, 4):
                 outs.append(run(a, b, cfg=tcl.Config(bn=256, stages=st, producer=1, split_k=1), canary=False))
+            for st in (1, 2, 3, 4):
+                outs.append(run(a, b, cfg=tcl.Config(bn=256, stages=st, producer=tcl.PRODUCER_CPASYNC, split_k=1),
+                                canary=False))
         for o in outs[1:]:
             assert torch.equal(o, outs[0])
 

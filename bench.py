@@ -372,7 +372,8 @@ def run_peak(args):
     sampler = ClockSampler(0)
     sampler.start()
     rows = []
-    combos = [(0, 256, 1), (0, 256, 0), (0, 128, 1), (0, 128, 0), (1, 256, 0), (1, 128, 0)]
+    combos = [(0, 256, 1), (0, 256, 0), (0, 224, 1), (0, 192, 1), (0, 128, 1), (0, 128, 0), (1, 256, 0),
+              (1, 128, 0)]
     # flags: 2 = walk operands like a k-loop; 11 = also one chained accumulator and the
     # rest of a GEMM issue loop (barrier wait, fence, commit per four MMAs)
     for kind, n, b_mn, flags in [c + (f,) for c in combos for f in (2, 11)]:

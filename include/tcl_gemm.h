@@ -118,6 +118,15 @@ typedef struct {
                                       wait must run out; the call then reports
                                       TCL_ERR_DEVICE_TIMEOUT through tcl_last_device_error() and
                                       the outputs of that CTA are undefined */
+    int stream_k;                  /* two-SM kernel, fp32 C: 0 automatic (when the last wave of
+                                      tiles would leave pairs of SMs idle and the planner's cycle
+                                      model favours it, each of those tiles is cut into 2..4 K
+                                      ranges given to different pairs; range 0 stores, range i
+                                      adds its result with a TMA reduction after range i-1 has
+                                      finished, so the sum order is fixed); 1 never; s in 2..4
+                                      exactly s ranges per tail tile of 256-wide tiles
+                                      (TCL_ERR_CONFIG if they do not fit). Calls with a stream-K tail share progress flags on
+                                      the device and must not run concurrently with one another */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -192,6 +201,8 @@ typedef struct {
     int splits;                     /* K ranges (1: no split-K) */
     int producer;                   /* 0: TMA, 1: synchronous copy, 2: cp.async */
     unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
+    int sk_tiles;                   /* tail tiles computed stream-K (0: none) */
+    int sk_pieces;                  /* K ranges per stream-K tile */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this
@@ -203,7 +214,8 @@ TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config
 /* Tensor-pipe rate probe (measurement, not part of the GEMM): `grid` CTAs
  * (one per SM) each issue `iters` (a multiple of 4, at least 8) back-to-back
  * tcgen05.mma, four at a time from one elected lane of a converged warp, of shape
- * M=128 × N=n × K=16 (bf16, in_kind 0) or K=8 (TF32, in_kind 1) on operands
+ * M=128 × N=n (128, 192, 224 or 256) × K=16 (bf16, in_kind 0) or K=8 (TF32,
+ * in_kind 1) on operands
  * already in shared memory (B K-major, or N-major if b_mn = 1; bf16 only),
  * and write the %clock64 cycles from the first issue to the completion of the
  * last into cycles[blockIdx] (device buffer of `grid` entries; 0 if the
@@ -224,7 +236,8 @@ TCL_API const char* tcl_status_string(int status);
  * word. Returns TCL_OK, or TCL_ERR_DEVICE_TIMEOUT if any kernel since the
  * last read recorded a timed-out wait (*detail, if not NULL, receives the raw
  * code: 1 producer, 2 MMA waiting for data, 3 MMA waiting for an accumulator,
- * 4 epilogue), or TCL_ERR_LAUNCH if synchronising failed. */
+ * 4 epilogue, 5 stream-K piece waiting for the previous piece), or
+ * TCL_ERR_LAUNCH if synchronising failed. */
 TCL_API int tcl_last_device_error(cudaStream_t stream, int* detail);
 
 /* Streaming multiprocessors of the current device (0 on error). */

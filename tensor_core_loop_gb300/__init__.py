@@ -63,6 +63,7 @@ class Config(ctypes.Structure):
         ("cta_pair", ctypes.c_int),
         ("epi_slots", ctypes.c_int),
         ("debug_skip_kblock", ctypes.c_int),
+        ("stream_k", ctypes.c_int),
     ]
 
 
@@ -78,6 +79,8 @@ class PlanInfo(ctypes.Structure):
         ("splits", ctypes.c_int),
         ("producer", ctypes.c_int),
         ("workspace_bytes", ctypes.c_ulonglong),
+        ("sk_tiles", ctypes.c_int),
+        ("sk_pieces", ctypes.c_int),
     ]
 
 

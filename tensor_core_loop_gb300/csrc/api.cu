@@ -19,6 +19,12 @@ namespace {
 // Per-device status word written by kernels whose bounded waits ran out.
 __device__ unsigned int g_status_word;
 
+// Stream-K progress flags of the two-SM kernel: [split tile][CTA of the pair][epilogue warp].
+// They only ever hold gen·8 + pieces done, gen being a per-device launch counter,
+// so they never need clearing between launches.
+constexpr int kMaxSkTiles = 128;
+__device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 4];
+
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
 constexpr int kBM = 128;
@@ -30,6 +36,8 @@ struct DevState {
     int sms = 0;
     int pair_clusters[8] = {};   // resident two-CTA clusters per pair variant (0: not yet queried)
     unsigned int* status = nullptr;
+    unsigned int* sk_flags = nullptr;
+    unsigned int sk_gen = 0;   // last stream-K flag generation used on this device
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
 };
@@ -137,6 +145,11 @@ int current_device(int* dev_out, DevState** st_out) {
                 return TCL_ERR_LAUNCH;
             }
             d.status = static_cast<unsigned int*>(p);
+            if (cudaGetSymbolAddress(&p, g_sk_flags) != cudaSuccess) {
+                cudaGetLastError();
+                return TCL_ERR_LAUNCH;
+            }
+            d.sk_flags = static_cast<unsigned int*>(p);
         }
         d.probed = true;
     }
@@ -190,6 +203,7 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 struct Plan {
     int bn, stages, prod, pair, slots, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
     int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
+    int sk_tiles, sk_pieces;    // stream-K tail of the two-SM kernel (0 tiles: none)
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -198,6 +212,50 @@ struct Plan {
 constexpr int kMinKbPerSplit = 8;    // k-blocks each range keeps
 constexpr int kMinKbForPair = 16;    // k-blocks a tile needs before two SMs per tile pay off
 constexpr int kMinKbToSplit = 24;    // k-blocks a tile needs before splitting is considered
+
+// Two-SM kernel: SM cycles per 64-deep k-block of a pair tile, measured on
+// GB300 with the in-kernel timeline (the tensor pipe runs 256-wide pair tiles
+// at its full rate, 224-wide ones ~9.6 % below it).
+constexpr long long kPairKbCycles256 = 512;
+constexpr long long kPairKbCycles224 = 491;
+// Stream-K tail: at most this many pieces per split tile (each waits for the
+// previous one before adding its result) and at least this many k-blocks each.
+constexpr int kMaxSkPieces = 4;
+constexpr int kMinKbPerPiece = 8;
+constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed when pieces are all a pair does
+
+// Stream-K split of the last (partial) wave of pair tiles: with `tiles` tiles
+// on `pairs` pairs of SMs, the tiles past the last full wave are each cut into
+// `pieces` K ranges so that the otherwise idle pairs share them.
+// want: 0 automatic, 1 never, s >= 2 exactly s pieces (TCL_ERR_CONFIG if that
+// does not fit). Fills *sk_tiles = 0 when there is no stream-K tail.
+int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_tiles, int* sk_pieces) {
+    *sk_tiles = 0;
+    *sk_pieces = 1;
+    const long long rem = tiles % pairs;
+    if (want == 1 || rem == 0) return TCL_OK;
+    if (want >= 2) {
+        if (want > kMaxSkPieces || rem * want > pairs || want > num_kb || rem > kMaxSkTiles) return TCL_ERR_CONFIG;
+        *sk_tiles = static_cast<int>(rem);
+        *sk_pieces = want;
+        return TCL_OK;
+    }
+    const int s = static_cast<int>(std::min<long long>({kMaxSkPieces, pairs / rem, num_kb / kMinKbPerPiece}));
+    if (s >= 2 && rem <= kMaxSkTiles) {
+        *sk_tiles = static_cast<int>(rem);
+        *sk_pieces = s;
+    }
+    return TCL_OK;
+}
+
+// Busiest pair's k-block cycles for pair tiles of width w: ceil(tiles / pairs)
+// whole tiles, or the full waves plus the largest stream-K piece.
+long long pair_cost(long long tiles, int pairs, int num_kb, long long kb_cycles, int sk_tiles, int sk_pieces) {
+    if (sk_tiles == 0) return (tiles + pairs - 1) / pairs * num_kb * kb_cycles;
+    const long long waves = tiles / pairs;
+    return (waves * num_kb + (num_kb + sk_pieces - 1) / sk_pieces) * kb_cycles +
+           (waves == 0 ? (sk_pieces - 1) * kSkLinkCycles : 0);
+}
 
 // slots = 0 matches any staging depth (the first listed, i.e. two slabs per warp)
 const VariantInfo* find_variant(InKind ik, OutKind ok, int bn, int stages, int prod, int pair, int slots = 0) {
@@ -244,19 +302,27 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         const int kblocks = (K + bk - 1) / bk;
         pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
     }
+    const int want_sk = cfg ? cfg->stream_k : 0;
+    if (want_sk < 0 || want_sk > kMaxSkPieces || (want_sk > 1 && (!pair || ok != OutKind::F32)))
+        return TCL_ERR_CONFIG;
     if (pair) {
         if (bn == 0) {
-            // Pair tile width: the fewest column-units of MMA work on the busiest
-            // pair of SMs, ceil(tiles / pairs) × width (fp32 C can use 224).
+            // Pair tile width: the fewest SM cycles on the busiest pair of SMs,
+            // whole tiles only or with a stream-K tail (fp32 C can also use 224).
             bn = 256;
-            if (ok == OutKind::F32) {
+            if (ok == OutKind::F32 && want_sk <= 1) {   // a requested stream-K split keeps 256
                 const int pairs = std::max(1, (cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms) / 2);
-                auto cost = [&](int w) {
+                const int kb = (K + bk - 1) / bk;
+                auto cost = [&](int w, long long kb_cycles) {
                     const long long t = static_cast<long long>((M + 255) / 256) * ((N + w - 1) / w);
-                    return ((t + pairs - 1) / pairs) * w;
+                    int skt = 0, skp = 1;
+                    if (stream_k_split(t, pairs, kb, want_sk, &skt, &skp)) skt = 0;
+                    return pair_cost(t, pairs, kb, kb_cycles, skt, skp);
                 };
                 const int want_st = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, 224, prod, 1);
-                if (find_variant(ik, ok, 224, want_st, prod, 1) && cost(224) < cost(256)) bn = 224;
+                if (find_variant(ik, ok, 224, want_st, prod, 1) &&
+                    cost(224, kPairKbCycles224) < cost(256, kPairKbCycles256))
+                    bn = 224;
             }
         }
     } else if (bn == 0) {
@@ -317,11 +383,28 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         }
     }
     const long long work = static_cast<long long>(pl->num_tiles) * pl->splits;
+    pl->sk_tiles = 0;
+    pl->sk_pieces = 1;
     if (pair) {
         int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / 2 : pair_clusters(v);
         if (clusters < 1) return cfg && cfg->max_ctas > 0 ? TCL_ERR_CONFIG : TCL_ERR_LAUNCH;
         if (cfg && cfg->one_cta_per_tile) clusters = pl->num_tiles;
         pl->grid = 2 * (pl->num_tiles < clusters ? pl->num_tiles : clusters);
+        // Stream-K pieces wait on one another, so every pair of the grid must be
+        // resident at once: the grid never exceeds the resident clusters here.
+        if (ok == OutKind::F32 && !(cfg && cfg->one_cta_per_tile)) {
+            const int st = stream_k_split(pl->num_tiles, pl->grid / 2, pl->num_kb, want_sk, &pl->sk_tiles,
+                                          &pl->sk_pieces);
+            if (st) return st;
+            const int resident = cfg && cfg->max_ctas > 0 ? pair_clusters(v) : pl->grid / 2;   // 0: no device
+            if (pl->sk_tiles && resident > 0 && pl->grid / 2 > resident) {
+                if (want_sk > 1) return TCL_ERR_CONFIG;
+                pl->sk_tiles = 0;
+                pl->sk_pieces = 1;
+            }
+        }
+    } else if (want_sk > 1) {
+        return TCL_ERR_CONFIG;
     } else if (cfg && cfg->one_cta_per_tile) {
         pl->grid = static_cast<int>(std::min<long long>(work, 0x7FFFFFFF));
     } else {
@@ -428,6 +511,15 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.B = B;
     p.ldb = ldb;
     p.debug_skip_kb = cfg && cfg->debug_skip_kblock > 0 ? cfg->debug_skip_kblock - 1 : -1;
+    p.sk_tiles = pl.sk_tiles;
+    p.sk_pieces = pl.sk_pieces;
+    p.sk_flags = ds->sk_flags;
+    p.sk_gen = 0;
+    if (pl.sk_tiles) {
+        ds->sk_gen = (ds->sk_gen + 1) & 0x1FFFFFFFu;   // flags hold gen·8 + pieces done in 32 bits
+        if (ds->sk_gen == 0) ds->sk_gen = 1;           // 0 is what the flags start as
+        p.sk_gen = ds->sk_gen;
+    }
 
     bool found = false;
     cudaError_t err = cudaSuccess;
@@ -638,6 +730,8 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->splits = pl.splits;
         plan->producer = pl.prod;
         plan->workspace_bytes = static_cast<unsigned long long>(split_workspace(pl, M, N).bytes);
+        plan->sk_tiles = pl.sk_tiles;
+        plan->sk_pieces = pl.sk_pieces;
     }
     return TCL_OK;
 }

@@ -53,6 +53,7 @@ enum : unsigned int {
     DEV_TIMEOUT_MMA_FULL = 2,   // MMA warp waited too long for a stage's data
     DEV_TIMEOUT_MMA_ACC = 3,    // MMA warp waited too long for a free accumulator
     DEV_TIMEOUT_EPILOGUE = 4,   // epilogue waited too long for a finished accumulator
+    DEV_TIMEOUT_SK_ORDER = 5,   // epilogue waited too long for the previous piece of a split tile
 };
 
 template <InKind IK>
@@ -91,6 +92,13 @@ struct GemmParams {
     int kb_per_split;            // k-blocks per split (the last may have fewer)
     int split_rows;              // output rows between consecutive splits' partial results
     int out_rows;                // rows of the output tensor (M, or splits × split_rows)
+    // Stream-K tail (two-SM kernel, fp32 C): the last sk_tiles tiles are each
+    // cut into sk_pieces K ranges, one per pair of SMs; piece 0 stores its
+    // result, piece i > 0 adds its own once piece i-1 has finished (flags).
+    int sk_tiles;                // 0: every tile is whole
+    int sk_pieces;               // K ranges per split tile (>= 2 when sk_tiles > 0)
+    unsigned int* sk_flags;      // [sk_tiles][2 CTAs][4 epilogue warps] progress flags
+    unsigned int sk_gen;         // this launch's flag generation (flags hold gen·8 + pieces done)
 };
 
 // Work item w → output tile (mb, nb), its k-block range [kb_lo, kb_hi) and
@@ -248,7 +256,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 template <int SLAB_BYTES, int OUT_ES, int SLOTS>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
-                                           const GemmParams& p) {
+                                           const GemmParams& p, bool add = false) {
     constexpr int COLS = 128 / OUT_ES;
     const bool in_bounds = row0 < p.out_rows && col0 < p.N;
     if (in_bounds && col0 + COLS > p.N && (p.N * OUT_ES) % 16 != 0) {
@@ -257,9 +265,15 @@ __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab
             const int n = p.N - col0;
             if constexpr (OUT_ES == 4) {
                 uint32_t* dst = static_cast<uint32_t*>(p.C) + row * p.ldc + col0;
+                if (add) {   // fp32: C += v, this warp being the only writer of these rows now
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < n) dst[i] = v[i];
+                    for (int i = 0; i < 32; ++i)
+                        if (i < n) dst[i] = __float_as_uint(__uint_as_float(dst[i]) + __uint_as_float(v[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < n) dst[i] = v[i];
+                }
             } else {
                 uint16_t* dst = static_cast<uint16_t*>(p.C) + row * p.ldc + col0;
 #pragma unroll
@@ -284,7 +298,12 @@ __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        if (in_bounds) ptx::tma_store_2d(tmC, ptx::smem_u32(slab), col0, row0);
+        if (in_bounds) {
+            if (add)
+                ptx::tma_reduce_add_2d(tmC, ptx::smem_u32(slab), col0, row0);
+            else
+                ptx::tma_store_2d(tmC, ptx::smem_u32(slab), col0, row0);
+        }
         ptx::bulk_commit();
     }
     ++count;
@@ -451,7 +470,7 @@ __device__ __forceinline__ void cpasync_producer(const GemmParams& p, uint8_t* s
 template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release>
 __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_t* slab_pair, int& store_count,
                                                   uint32_t tbase, int lane, int col_base, int row0,
-                                                  const GemmParams& p, Release release) {
+                                                  const GemmParams& p, Release release, bool add = false) {
     constexpr int COLS = OK == OutKind::BF16 ? 64 : 32;   // TMEM columns per chunk
     constexpr int OUT_ES = OK == OutKind::BF16 ? 2 : 4;
     uint32_t buf[2][COLS];
@@ -484,7 +503,7 @@ __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_
             for (int i = 0; i < 32; ++i) v[i] = cur[i];
         }
         store_slab<SLAB_BYTES, OUT_ES, SLOTS>(tmC, slab_pair, store_count, v, lane, col_base + c * (128 / OUT_ES), row0,
-                                              p);
+                                              p, add);
     }
 }
 

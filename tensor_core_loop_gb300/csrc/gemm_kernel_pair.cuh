@@ -89,6 +89,72 @@ __device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t parity, vo
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// The pair of SMs `cluster` (of `clusters`) walks its work units in this
+// order: first its stream-K piece, if it has one (split tiles are the last
+// sk_tiles of the raster order, piece i of tile d covering k-blocks
+// [i·num_kb/sk_pieces, (i+1)·num_kb/sk_pieces), given to pair d·sk_pieces + i),
+// then the whole tiles cluster, cluster + clusters, … below the split ones.
+// Producer, MMA warp and epilogue enumerate the same sequence.
+struct PairUnit {
+    int tile, kb_lo, kb_hi, piece, sk_index;   // sk_index: split-tile number, -1 for a whole tile
+};
+
+__device__ __forceinline__ int pair_units(const GemmParams& p, int cluster, int clusters) {
+    const int whole = p.num_tiles - p.sk_tiles;
+    const int n = cluster < whole ? (whole - 1 - cluster) / clusters + 1 : 0;
+    return n + (cluster < p.sk_tiles * p.sk_pieces ? 1 : 0);
+}
+
+__device__ __forceinline__ PairUnit pair_unit(const GemmParams& p, int cluster, int clusters, int u) {
+    PairUnit r;
+    const bool has_piece = cluster < p.sk_tiles * p.sk_pieces;
+    if (has_piece && u == 0) {
+        r.sk_index = cluster / p.sk_pieces;
+        r.piece = cluster - r.sk_index * p.sk_pieces;
+        r.tile = p.num_tiles - p.sk_tiles + r.sk_index;
+        r.kb_lo = r.piece * p.num_kb / p.sk_pieces;
+        r.kb_hi = (r.piece + 1) * p.num_kb / p.sk_pieces;
+    } else {
+        r.sk_index = -1;
+        r.piece = 0;
+        r.tile = cluster + (u - (has_piece ? 1 : 0)) * clusters;
+        r.kb_lo = 0;
+        r.kb_hi = p.num_kb;
+    }
+    return r;
+}
+
+// Epilogue warp of a stream-K piece i > 0: wait until the warp with the same
+// rows in piece i-1 has finished writing them (its flag reads gen·8 + i).
+// Every lane performs an acquire of the flag before touching C.
+__device__ __forceinline__ bool wait_sk_flag(const uint32_t* flag, uint32_t want, volatile uint32_t* abort_flag,
+                                             uint32_t peer_abort, unsigned long long timeout_ns,
+                                             unsigned int* status) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0 && ptx::ld_acquire_gpu(flag) != want) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::ld_acquire_gpu(flag) != want) {
+            if (*abort_flag) {
+                ok = 0;
+                break;
+            }
+            if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1u;
+                ptx::st_cluster_u32(peer_abort, 1u);
+                atomicCAS(status, 0u, static_cast<unsigned int>(DEV_TIMEOUT_SK_ORDER));
+                ok = 0;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+        (void)ptx::ld_acquire_gpu(flag);   // this lane's own acquire of the earlier piece's writes
+        ptx::fence_proxy_async_global();  // ... ordered before this warp's TMA reductions
+    }
+    return ok != 0;
+}
+
 __device__ __forceinline__ void spin_ns(unsigned long long ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < ns) {
@@ -165,12 +231,14 @@ __global__ void __launch_bounds__(192, 1)
         // elected lane.
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters) {
+        const int units = pair_units(p, cluster, clusters);
+        for (int u = 0; ok && u < units; ++u) {
+            const PairUnit U = pair_unit(p, cluster, clusters, u);
             int mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_coords(U.tile, p, mb, nb);
             const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
             const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
-            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!wait_warp_pair(empty0 + 8 * s, ph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
@@ -211,7 +279,9 @@ __global__ void __launch_bounds__(192, 1)
             static_assert(C::KSUB == 4, "four MMAs per k-block");
             uint32_t it = 0, unit = 0, s = 0, ph = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters, ++unit) {
+            const int units = pair_units(p, cluster, clusters);
+            for (int u = 0; ok && u < units; ++u, ++unit) {
+                const PairUnit U = pair_unit(p, cluster, clusters, u);
                 const uint32_t buf = unit & 1u;
                 const uint32_t uph = (unit >> 1) & 1u;
                 if (!wait_warp_pair(acce0 + 8 * buf, uph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
@@ -221,7 +291,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * C::ACC_STRIDE;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                     if (!wait_warp_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
                                         DEV_TIMEOUT_MMA_FULL)) {
                         ok = false;
@@ -233,7 +303,7 @@ __global__ void __launch_bounds__(192, 1)
                     const uint64_t bd = bdesc0 + s * S_STEP;
                     ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
                                                  bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
-                                                 kb > 0 ? 1u : 0u);
+                                                 kb > U.kb_lo ? 1u : 0u);
                     ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::BOTH);
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
                     const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
@@ -256,9 +326,11 @@ __global__ void __launch_bounds__(192, 1)
         int store_count = 0;
         uint32_t unit = 0;
         bool ok = true;
-        for (int tile = cluster; ok && tile < p.num_tiles; tile += clusters, ++unit) {
+        const int units = pair_units(p, cluster, clusters);
+        for (int u = 0; ok && u < units; ++u, ++unit) {
+            const PairUnit U = pair_unit(p, cluster, clusters, u);
             int mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_coords(U.tile, p, mb, nb);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
             const uint32_t buf = unit & 1u;
             const uint32_t uph = (unit >> 1) & 1u;
@@ -271,13 +343,34 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             ptx::tc_fence_after();
+            // stream-K: this warp's rows of split tile d, flags[d][rank][q]
+            uint32_t* flag = U.sk_index >= 0 ? p.sk_flags + (U.sk_index * 2 + rank) * 4 + q : nullptr;
+            if (flag && U.piece > 0 &&
+                !wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
+                              p.timeout_ns, p.status)) {
+                ok = false;
+                break;
+            }
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
             drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
-                &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p, [&]() {
+                &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p,
+                [&]() {
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
-                });
+                },
+                /*add=*/U.piece > 0);
+            if (flag && U.piece + 1 < p.sk_pieces) {
+                // hand these rows to the next piece once every write to them has landed
+                __threadfence();   // the ragged-edge chunk's element writes, from every lane
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::bulk_wait<0>();               // this warp's stores/reductions completed
+                    ptx::fence_proxy_async_global();   // ... and ordered before the release
+                    ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
+                }
+                __syncwarp();
+            }
         }
         if (lane == 0) ptx::bulk_wait<0>();
         __syncwarp();

@@ -118,6 +118,17 @@ cudaError_t launch_peak(int iters, int flags, int grid, unsigned long long* cycl
     return cudaGetLastError();
 }
 
+template <bool TF32, bool B_MN>
+cudaError_t launch_peak_n(int n, int iters, int flags, int grid, unsigned long long* cycles, unsigned int* status,
+                          cudaStream_t stream) {
+    switch (n) {
+        case 128: return launch_peak<128, TF32, B_MN>(iters, flags, grid, cycles, status, stream);
+        case 192: return launch_peak<192, TF32, B_MN>(iters, flags, grid, cycles, status, stream);
+        case 224: return launch_peak<224, TF32, B_MN>(iters, flags, grid, cycles, status, stream);
+        default: return launch_peak<256, TF32, B_MN>(iters, flags, grid, cycles, status, stream);
+    }
+}
+
 }  // namespace
 
 int device_context(int* dev, int* sms, unsigned int** status);   // api.cu
@@ -129,7 +140,8 @@ using namespace tcl;
 extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
                                     unsigned long long* cycles, cudaStream_t stream) {
     if (!cycles) return TCL_ERR_NULL;
-    if (iters < 8 || iters % 4 || grid < 1 || (n != 128 && n != 256) || (in_kind != 0 && in_kind != 1) ||
+    if (iters < 8 || iters % 4 || grid < 1 || (n != 128 && n != 192 && n != 224 && n != 256) ||
+        (in_kind != 0 && in_kind != 1) ||
         (b_mn != 0 && b_mn != 1) || (in_kind == 1 && b_mn))
         return TCL_ERR_DIMS;
     static_assert(kPeakSmem <= kPeakRequest, "probe fits its shared memory request");
@@ -140,14 +152,11 @@ extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int
     if (st) return st;
     cudaError_t err;
     if (in_kind == 1)
-        err = n == 256 ? launch_peak<256, true, false>(iters, flags, grid, cycles, status, stream)
-                       : launch_peak<128, true, false>(iters, flags, grid, cycles, status, stream);
+        err = launch_peak_n<true, false>(n, iters, flags, grid, cycles, status, stream);
     else if (b_mn)
-        err = n == 256 ? launch_peak<256, false, true>(iters, flags, grid, cycles, status, stream)
-                       : launch_peak<128, false, true>(iters, flags, grid, cycles, status, stream);
+        err = launch_peak_n<false, true>(n, iters, flags, grid, cycles, status, stream);
     else
-        err = n == 256 ? launch_peak<256, false, false>(iters, flags, grid, cycles, status, stream)
-                       : launch_peak<128, false, false>(iters, flags, grid, cycles, status, stream);
+        err = launch_peak_n<false, false>(n, iters, flags, grid, cycles, status, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_LAUNCH;

@@ -117,6 +117,10 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.kb_per_split = p.num_kb;
     p.split_rows = 0;
     p.out_rows = M;
+    p.sk_tiles = 0;
+    p.sk_pieces = 1;
+    p.sk_flags = nullptr;
+    p.sk_gen = 0;
 
     if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, sms, stream) != cudaSuccess ||
         launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, sms, stream) != cudaSuccess) {

@@ -80,9 +80,10 @@ def test_gemm_tf32_and_s8_reject(L):
 
 def test_plan_without_device(L):
     cfg = tcl.Config(max_ctas=152)
-    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)
-    # enough 256-row tiles for every pair of SMs: two SMs per tile; 224 columns give
-    # 16 × 19 = 304 tiles = exactly 4 per pair of SMs (256 would leave a partial wave)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=1))
+    # enough 256-row tiles for every pair of SMs: two SMs per tile; without a stream-K
+    # tail, 224 columns give 16 × 19 = 304 tiles = exactly 4 per pair of SMs (256 would
+    # leave a partial wave)
     assert p["cta_pair"] == 2 and p["bn"] == 224 and p["num_tiles"] == 16 * 19 and p["grid"] == 152
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)
     assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16
@@ -122,6 +123,32 @@ def test_plan_without_device(L):
         tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, bn=192))
     with pytest.raises(tcl.TclError):
         tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stages=5))
+
+
+def test_planner_stream_k(L):
+    cfg = tcl.Config(max_ctas=152)
+    # 4096³ on 76 pairs: 256 tiles of 256×256 = 3 full waves + 28 tiles, each cut in two K
+    # ranges, beats 304 tiles of 256×224 (4 waves at the 224-wide k-block rate)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)
+    assert (p["cta_pair"], p["bn"], p["num_tiles"], p["sk_tiles"], p["sk_pieces"]) == (2, 256, 256, 28, 2)
+    # without stream-K the 224-wide tiles win
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=1))
+    assert (p["bn"], p["sk_tiles"]) == (224, 0)
+    # whole waves: nothing to split
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4864, 4096, 4096, cfg)
+    assert (p["bn"], p["num_tiles"], p["sk_tiles"]) == (256, 304, 0)
+    # bf16 C: no stream-K (a bf16 partial would be rounded twice)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)["sk_tiles"] == 0
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2))
+    assert (p["num_tiles"], p["sk_tiles"], p["sk_pieces"]) == (9, 1, 4)
+    for bad in (tcl.Config(max_ctas=8, cta_pair=2, stream_k=5),       # more than 4 pieces
+                tcl.Config(max_ctas=8, cta_pair=1, stream_k=2),       # one-SM kernel
+                tcl.Config(max_ctas=4, cta_pair=2, stream_k=3),       # 1 tail tile × 3 pieces > 2 pairs
+                tcl.Config(max_ctas=8, cta_pair=2, stream_k=-1)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, bad)
+    with pytest.raises(tcl.TclError):
+        tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2, stream_k=2))
 
 
 def test_planner_producer_kinds(L):

@@ -184,6 +184,36 @@ def test_bf16_pair_kernel_bf16_out(oracle_mod, M, N, K):
     bf16_case(oracle_mod, M, N, K, seed=5, out_dtype=torch.bfloat16, cfg=tcl.Config(cta_pair=2))
 
 
+@pytest.mark.parametrize("M,N,K,pieces", [
+    (768, 768, 2048, 0),     # 9 tiles on 4 pairs: 2 full waves, the 9th tile in 4 pieces of 8 k-blocks
+    (768, 768, 2048, 2),
+    (768, 768, 2048, 3),     # uneven pieces: 10, 11, 11 k-blocks
+    (700, 750, 1000, 4),     # ragged M, N (last chunk added element by element), K tail in the last piece
+    (700, 750, 1000, 0),
+    (512, 1280, 576, 2),     # 10 tiles on 4 pairs: two tail tiles, pieces of 4 and 5 k-blocks
+])
+def test_bf16_pair_stream_k(oracle_mod, M, N, K, pieces):
+    # four pairs of SMs (max_ctas 8); the last partial wave of tiles is cut into K ranges
+    # whose results are added in range order (store, then TMA reductions)
+    cfg = tcl.Config(cta_pair=2, max_ctas=8, stream_k=pieces)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K, cfg)
+    assert pl["sk_tiles"] > 0 and pl["sk_pieces"] == (pieces or pl["sk_pieces"]) and pl["sk_pieces"] >= 2
+    ldc = -(-N // 4) * 4 if N % 4 else None
+    bf16_case(oracle_mod, M, N, K, seed=K + pieces, cfg=cfg, ldc=ldc)
+
+
+def test_stream_k_deterministic():
+    # the same plan gives the same bits every time: the pieces of a split tile are
+    # added in range order whatever order the pairs finish in
+    a, b = inputs.bf16_pair(768, 768, 2048, seed=29)
+    a, b = a.to(DEV), b.to(DEV)
+    for pieces in (2, 4):
+        cfg = tcl.Config(cta_pair=2, max_ctas=8, stream_k=pieces)
+        first = run(a, b, cfg=cfg)
+        for _ in range(10):
+            assert torch.equal(run(a, b, cfg=cfg, canary=False), first)
+
+
 def test_pair_kernel_variants_bitwise_identical():
     a, b = inputs.bf16_pair(1024, 1280, 1216, seed=19)
     a, b = a.to(DEV), b.to(DEV)

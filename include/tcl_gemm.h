@@ -127,6 +127,11 @@ typedef struct {
                                       exactly s ranges per tail tile of 256-wide tiles
                                       (TCL_ERR_CONFIG if they do not fit). Calls with a stream-K tail share progress flags on
                                       the device and must not run concurrently with one another */
+    int serial_launch;             /* 0 (default): the two-SM kernel is launched with programmatic
+                                      stream serialisation, so its set-up (barriers, TMEM, cluster
+                                      handshake) overlaps the end of the previous kernel in the
+                                      stream; it reads and writes global memory only after that
+                                      kernel has completed. 1: plain stream order */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)

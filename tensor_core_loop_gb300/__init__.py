@@ -64,6 +64,7 @@ class Config(ctypes.Structure):
         ("epi_slots", ctypes.c_int),
         ("debug_skip_kblock", ctypes.c_int),
         ("stream_k", ctypes.c_int),
+        ("serial_launch", ctypes.c_int),
     ]
 
 

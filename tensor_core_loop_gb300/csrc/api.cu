@@ -472,6 +472,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.prod = pl.prod;
     a.pair = pl.pair;
     a.slots = pl.slots;
+    a.pdl = !(cfg && cfg->serial_launch);
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;

@@ -462,15 +462,23 @@ __device__ __forceinline__ void cpasync_producer(const GemmParams& p, uint8_t* s
     ptx::cp_async_wait_all();
 }
 
+struct NoPace {
+    __device__ __forceinline__ void operator()(int) const {}
+};
+
 // Drains one TMEM accumulator (this warp's 32 lanes × EPI_CHUNKS chunks) to C:
 // F32 chunks are 32 fp32 columns, BF16 chunks 64 fp32 columns rounded to 64
 // bf16. The TMEM load of chunk c+1 is issued before chunk c is staged and
 // stored, so its latency hides under the shared-memory writes and the store
-// issue. `release()` runs once every TMEM read of the accumulator is complete.
-template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release>
+// issue. `release()` runs once every TMEM read of the accumulator is complete;
+// `pace(c)` runs before chunk c is staged and stored (the two-SM kernel uses
+// it to spread a tile's stores over the next tile's mainloop). `add`: reduce
+// into C instead of storing (fp32).
+template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release, class Pace = NoPace>
 __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_t* slab_pair, int& store_count,
                                                   uint32_t tbase, int lane, int col_base, int row0,
-                                                  const GemmParams& p, Release release, bool add = false) {
+                                                  const GemmParams& p, Release release, bool add = false,
+                                                  Pace pace = Pace()) {
     constexpr int COLS = OK == OutKind::BF16 ? 64 : 32;   // TMEM columns per chunk
     constexpr int OUT_ES = OK == OutKind::BF16 ? 2 : 4;
     uint32_t buf[2][COLS];
@@ -502,6 +510,7 @@ __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = cur[i];
         }
+        pace(c);
         store_slab<SLAB_BYTES, OUT_ES, SLOTS>(tmC, slab_pair, store_count, v, lane, col_base + c * (128 / OUT_ES), row0,
                                               p, add);
     }

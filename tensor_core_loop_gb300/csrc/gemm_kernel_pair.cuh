@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STAGING_BYTES);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile uint32_t* abort_flag = tmem_holder + 1;
+    volatile uint32_t* progress = tmem_holder + 2;   // k-blocks whose loads this CTA's producer has issued
 
     const uint32_t full0 = ptx::smem_u32(bars);
     const uint32_t empty0 = ptx::smem_u32(bars + STAGES);
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0u;
+        *progress = 0u;
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -213,6 +215,11 @@ __global__ void __launch_bounds__(192, 1)
     ptx::cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Everything above touches only this CTA's own resources, so under a
+    // programmatic launch it overlaps the previous kernel's tail; nothing
+    // below reads or writes global memory before that kernel has finished.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 
     const uint32_t full_leader0 = ptx::mapa_shared(full0, 0);
     const uint32_t acce_leader0 = ptx::mapa_shared(acce0, 0);
@@ -259,6 +266,7 @@ __global__ void __launch_bounds__(192, 1)
                 for (int b = 0; b < C::B_BOXES; ++b)
                     ptx::tma_load_2d_pair_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, fb, col + b * C::B_BOX_N,
                                                   kb * C::BK);
+                if (lane == 0) *progress = it + 1;
             }
         }
         if (!ok && lane == 0) spin_ns(200000);   // copies issued before the abort land within microseconds
@@ -325,10 +333,12 @@ __global__ void __launch_bounds__(192, 1)
         uint8_t* slab_pair = staging + (warp - 2) * C::EPI_SLOTS * C::SLAB_BYTES;
         int store_count = 0;
         uint32_t unit = 0;
+        uint32_t it_next = 0;   // the ring iteration at which the unit after this one starts
         bool ok = true;
         const int units = pair_units(p, cluster, clusters);
         for (int u = 0; ok && u < units; ++u, ++unit) {
             const PairUnit U = pair_unit(p, cluster, clusters, u);
+            it_next += static_cast<uint32_t>(U.kb_hi - U.kb_lo);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
@@ -359,7 +369,23 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
                 },
-                /*add=*/U.piece > 0);
+                /*add=*/U.piece > 0, [&](int c) {
+                    // Spread this tile's stores over the next unit's mainloop: chunk c waits
+                    // until the producer is c/EPI_CHUNKS of the way through that unit (a
+                    // burst of TMA stores slows the tensor pipe's operand reads). The
+                    // CTA's last unit stores at once.
+                    if (u + 1 >= units || c == 0) return;
+                    const PairUnit V = pair_unit(p, cluster, clusters, u + 1);
+                    const uint32_t n = static_cast<uint32_t>(V.kb_hi - V.kb_lo);
+                    // (the producer issues all n k-blocks of the next unit, so the target is reached)
+                    const uint32_t target = it_next + min(n, STAGES + c * n / C::EPI_CHUNKS);
+                    if (lane == 0 && *progress < target) {
+                        const uint64_t t0 = ptx::globaltimer_ns();
+                        while (*progress < target && !*abort_flag && ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                        }
+                    }
+                    __syncwarp();
+                });
             if (flag && U.piece + 1 < p.sk_pieces) {
                 // hand these rows to the next piece once every write to them has landed
                 __threadfence();   // the ragged-edge chunk's element writes, from every lane

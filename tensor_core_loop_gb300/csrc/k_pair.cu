@@ -5,8 +5,11 @@
 namespace tcl {
 namespace {
 
+// attr must hold two entries; pdl adds programmatic stream serialisation
+// (the kernel may start its set-up while the previous kernel in the stream
+// finishes; it waits for that kernel before touching global memory).
 template <OutKind OK, int BN, int STAGES, int SLOTS>
-cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr, bool pdl = false) {
     using C = PairCfg<OK, BN, STAGES, SLOTS>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -19,6 +22,11 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     return cfg;
 }
 
@@ -40,15 +48,15 @@ template <OutKind OK, int BN, int STAGES, int SLOTS>
 cudaError_t launch_pair(const LaunchArgs& a) {
     cudaError_t err = prepare<OK, BN, STAGES, SLOTS>();
     if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(a.grid, a.stream, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(a.grid, a.stream, attr, a.pdl);
     return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS>, a.tmA, a.tmB, a.tmC, a.p);
 }
 
 template <OutKind OK, int BN, int STAGES, int SLOTS>
 int max_clusters() {
     if (prepare<OK, BN, STAGES, SLOTS>() != cudaSuccess) return 0;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(2, 0, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS>, &cfg) != cudaSuccess) {

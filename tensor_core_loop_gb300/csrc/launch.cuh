@@ -17,6 +17,7 @@ struct LaunchArgs {
     int prod;   // PROD_TMA, PROD_SYNC or PROD_CPASYNC
     int pair;   // 1: two-SM kernel (cluster of two CTAs per 256-row tile)
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
+    bool pdl;   // programmatic dependent launch (two-SM kernel)
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
     int grid;

@@ -83,6 +83,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     a.prod = PROD_TMA;
     a.pair = 0;
     a.slots = 2;
+    a.pdl = false;
     a.grid = grid;
     a.stream = stream;
     if ((st = tensor_map_uncached(a2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, lda2 * 2, 64, 128, &a.tmA)))

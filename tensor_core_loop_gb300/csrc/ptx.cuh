@@ -127,6 +127,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch. wait: block until the grids this one depends
+// on in the stream have completed and their memory is visible (a no-op when
+// the launch did not ask for programmatic serialisation). launch_dependents:
+// let the next grid in the stream be scheduled (it still waits for this one
+// before it reads anything).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Orders this thread's view of global memory between the generic proxy and
 // the async proxy (TMA stores/reductions), in both directions.
 __device__ __forceinline__ void fence_proxy_async_global() {

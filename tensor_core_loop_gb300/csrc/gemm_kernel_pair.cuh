@@ -90,10 +90,12 @@ __device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t parity, vo
 }
 
 // The pair of SMs `cluster` (of `clusters`) walks its work units in this
-// order: first its stream-K piece, if it has one (split tiles are the last
-// sk_tiles of the raster order, piece i of tile d covering k-blocks
-// [i·num_kb/sk_pieces, (i+1)·num_kb/sk_pieces), given to pair d·sk_pieces + i),
-// then the whole tiles cluster, cluster + clusters, … below the split ones.
+// order. Split tiles are the last sk_tiles of the raster order; piece i of
+// split tile d covers k-blocks [i·num_kb/sk_pieces, (i+1)·num_kb/sk_pieces)
+// and belongs to pair d·sk_pieces + i. Whole tiles cluster, cluster +
+// clusters, … (below the split ones) follow a pair's piece if that piece is
+// not the last of its tile, and precede it if it is: piece i > 0 has to wait
+// for piece i-1, and the last pieces, run last, find their predecessors done.
 // Producer, MMA warp and epilogue enumerate the same sequence.
 struct PairUnit {
     int tile, kb_lo, kb_hi, piece, sk_index;   // sk_index: split-tile number, -1 for a whole tile
@@ -108,16 +110,19 @@ __device__ __forceinline__ int pair_units(const GemmParams& p, int cluster, int 
 __device__ __forceinline__ PairUnit pair_unit(const GemmParams& p, int cluster, int clusters, int u) {
     PairUnit r;
     const bool has_piece = cluster < p.sk_tiles * p.sk_pieces;
-    if (has_piece && u == 0) {
+    const int piece = has_piece ? cluster % p.sk_pieces : 0;
+    const bool piece_first = has_piece && piece + 1 < p.sk_pieces;
+    const int piece_at = piece_first ? 0 : pair_units(p, cluster, clusters) - 1;   // the piece's position
+    if (has_piece && u == piece_at) {
         r.sk_index = cluster / p.sk_pieces;
-        r.piece = cluster - r.sk_index * p.sk_pieces;
+        r.piece = piece;
         r.tile = p.num_tiles - p.sk_tiles + r.sk_index;
         r.kb_lo = r.piece * p.num_kb / p.sk_pieces;
         r.kb_hi = (r.piece + 1) * p.num_kb / p.sk_pieces;
     } else {
         r.sk_index = -1;
         r.piece = 0;
-        r.tile = cluster + (u - (has_piece ? 1 : 0)) * clusters;
+        r.tile = cluster + (u - (piece_first ? 1 : 0)) * clusters;
         r.kb_lo = 0;
         r.kb_hi = p.num_kb;
     }
@@ -373,8 +378,9 @@ __global__ void __launch_bounds__(192, 1)
                     // Spread this tile's stores over the next unit's mainloop: chunk c waits
                     // until the producer is c/EPI_CHUNKS of the way through that unit (a
                     // burst of TMA stores slows the tensor pipe's operand reads). The
-                    // CTA's last unit stores at once.
-                    if (u + 1 >= units || c == 0) return;
+                    // CTA's last unit, and a stream-K piece (the next piece waits for
+                    // it), store at once.
+                    if (u + 1 >= units || c == 0 || U.sk_index >= 0) return;
                     const PairUnit V = pair_unit(p, cluster, clusters, u + 1);
                     const uint32_t n = static_cast<uint32_t>(V.kb_hi - V.kb_lo);
                     // (the producer issues all n k-blocks of the next unit, so the target is reached)

@@ -18,7 +18,8 @@
  *   (allocated, kept alive until the stream has run the call, and freed by
  *   the caller). The library keeps a per-device cache of TMA descriptors and
  *   a per-device scratch buffer (repacked operands for gemm_s8 and gemm_tf32,
- *   split-K partial tiles for small grids) that it grows on demand
+ *   copies of operands or outputs off the 16-byte grid, split-K partial
+ *   tiles for small grids) that it grows on demand
  *   (cudaMalloc, after a device synchronisation) and frees in tcl_shutdown().
  *   Every call on a device shares that buffer: calls whose GPU work could
  *   overlap (different streams without ordering) must not both need it.
@@ -28,19 +29,26 @@
  *   order. The library is not thread-safe: serialise calls from several host
  *   threads.
  *
- * Alignment (the TMA rule: global base addresses 16-byte aligned, row
- *   strides a multiple of 16 bytes; "cp.async / ldmatrix 消融实验", §1.4 item
- *   2 states the same 16-byte rule for cp.async):
+ * Alignment. Pointers must be aligned to their element size (bf16: 2
+ *   bytes; fp32, int32: 4 bytes; int8: none), else TCL_ERR_ALIGN. The fast
+ *   path also wants what the tensor copies (TMA) need — base addresses
+ *   16-byte aligned and row strides a multiple of 16 bytes ("cp.async /
+ *   ldmatrix 消融实验", §1.4 item 2 states the same 16-byte rule for
+ *   cp.async) — and whole 16-byte pieces of K in a row of A (a tensor load
+ *   rounds a row end up to 16 bytes):
  *   gemm_bf16: A, B, C 16-byte aligned; lda, ldb and K multiples of 8;
  *              ldc a multiple of 4 (fp32 C) or 8 (bf16 C).
- *   gemm_tf32: A, B, C 16-byte aligned; lda, ldb, K and ldc multiples of 4.
- *   gemm_s8:   A, B, C 16-byte aligned; lda, ldb multiples of 16; ldc of 4;
- *              K free (the operands are repacked with zero padding).
- *   (A row of A ends at K; a tensor load rounds a row end up to 16 bytes, so
- *   K itself must keep that boundary for bf16 and TF32.) M and N are free
- *   (>= 1): edge tiles are zero-filled on load, rows past M are never
- *   written, and a right edge N that is not on a 16-byte boundary is written
- *   element by element, so nothing outside the M×N block of C changes.
+ *   gemm_tf32: A, C 16-byte aligned; lda, K and ldc multiples of 4 (B is
+ *              always copied, transposed).
+ *   gemm_s8:   C 16-byte aligned, ldc a multiple of 4 (A and B are always
+ *              repacked).
+ *   An operand that misses these is first copied into the library scratch
+ *   with an aligned pitch and K zero-padded (to 8 for bf16, 4 for TF32), and
+ *   a C that misses them is computed into scratch and then copied out: same
+ *   result, one extra pass over that matrix. M and N are free (>= 1): edge
+ *   tiles are zero-filled on load, rows past M are never written, and a
+ *   right edge N that is not on a 16-byte boundary is written element by
+ *   element, so nothing outside the M×N block of C changes.
  *
  * Errors: each entry point returns a tcl_status. Argument checks happen on
  *   the host before anything is enqueued; a nonzero status means nothing was
@@ -69,7 +77,8 @@ typedef enum {
     TCL_ERR_NULL = 1,            /* a required pointer is NULL */
     TCL_ERR_DIMS = 2,            /* M, N or K < 1 */
     TCL_ERR_LD = 3,              /* lda < K, ldb < N or ldc < N */
-    TCL_ERR_ALIGN = 4,           /* base, leading dimension or K breaks the alignment rule above */
+    TCL_ERR_ALIGN = 4,           /* a pointer is not aligned to its element size (gemm_s8_static:
+                                    the stricter rule given there) */
     TCL_ERR_K_TOO_LARGE = 5,     /* gemm_s8: K > 131071, the int32 result could overflow */
     TCL_ERR_LAUNCH = 6,          /* a CUDA call or kernel launch failed */
     TCL_ERR_DEVICE_TIMEOUT = 7,  /* a bounded in-kernel wait ran out (see tcl_last_device_error) */
@@ -156,8 +165,10 @@ TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t*
 /* Allocation-free int8 GEMM. (The pages have no counterpart: this is a
  * library service, not part of the method.)
  *
- * Same operation, arguments, alignment rules and exact int32 result as
- * gemm_s8, but the library allocates nothing: the bf16 copies of A and B are
+ * Same operation, arguments and exact int32 result as gemm_s8, but the
+ * library allocates nothing (and so cannot repack off-grid C: A, B and C
+ * must be 16-byte aligned, lda and ldb multiples of 16, ldc of 4, else
+ * TCL_ERR_ALIGN): the bf16 copies of A and B are
  * written into a fixed buffer that is part of the library's device image, a
  * file-scope array of TCL_S8_STATIC_SCRATCH_BYTES (64 MiB). Every GPU on which
  * the library's code is loaded holds that buffer until the process exits.

@@ -86,6 +86,7 @@ int in_bytes(InKind k) { return k == InKind::TF32 ? 4 : 2; }
 int out_bytes(OutKind k) { return k == OutKind::BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
 // Grows the device's repacking scratch to at least `need` bytes. Growing waits
@@ -222,6 +223,11 @@ constexpr long long kPairKbCycles224 = 491;
 // previous one before adding its result) and at least this many k-blocks each.
 constexpr int kMaxSkPieces = 4;
 constexpr int kMinKbPerPiece = 8;
+// ... and only for tiles of at least this many k-blocks: below it the tile's
+// epilogue is a large share of its time and the extra piece's epilogue eats
+// the gain (measured on GB300 at 4096²: 224-wide whole tiles 8 % faster at
+// K = 1024, even at 1536, stream-K ahead from 2048).
+constexpr int kMinKbForSk = 32;
 constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed when pieces are all a pair does
 
 // Stream-K split of the last (partial) wave of pair tiles: with `tiles` tiles
@@ -241,7 +247,7 @@ int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_til
         return TCL_OK;
     }
     const int s = static_cast<int>(std::min<long long>({kMaxSkPieces, pairs / rem, num_kb / kMinKbPerPiece}));
-    if (s >= 2 && rem <= kMaxSkTiles) {
+    if (s >= 2 && rem <= kMaxSkTiles && num_kb >= kMinKbForSk) {
         *sk_tiles = static_cast<int>(rem);
         *sk_pieces = s;
     }
@@ -548,51 +554,115 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     return TCL_OK;
 }
 
+// Scratch layout of one call: packed copies of the operands and output that
+// are off the 16-byte grid (each 256-byte aligned), then the split-K
+// workspace. Sized before anything is enqueued: growing the scratch frees the
+// old buffer.
+struct Carve {
+    uint8_t* base;
+    size_t used;
+    void* take(size_t bytes) {
+        if (!bytes) return nullptr;
+        void* p = base + used;
+        used += static_cast<size_t>(round_up(static_cast<long long>(bytes), 256));
+        return p;
+    }
+};
+
 int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C,
                    int ldc, int out, const tcl_config_t* cfg, cudaStream_t stream) {
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
     if (out != TCL_OUT_F32 && out != TCL_OUT_BF16) return TCL_ERR_CONFIG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 8 || ldb % 8 || K % 8 ||
-        ldc % (out == TCL_OUT_BF16 ? 8 : 4))
-        return TCL_ERR_ALIGN;
+    const int oes = out == TCL_OUT_BF16 ? 2 : 4;
+    if (!aligned_to(A, 2) || !aligned_to(B, 2) || !aligned_to(C, oes)) return TCL_ERR_ALIGN;
+    // Tensor copies need 16-byte aligned bases and row pitches, and whole
+    // 16-byte pieces of K in a row of A: operands that miss any of these are
+    // repacked (K zero-padded to a multiple of 8), an output that misses them is
+    // computed into scratch and copied out.
+    const bool pack_a = !aligned16(A) || lda % 8 || K % 8;
+    const bool pack_b = !aligned16(B) || ldb % 8 || K % 8;
+    const bool pack_c = !aligned16(C) || ldc % (16 / oes);
+    const int K2 = static_cast<int>(round_up(K, 8));
+    const long long lda2 = K2, ldb2 = round_up(N, 8), ldc2 = round_up(N, 16 / oes);
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
     const OutKind ok = out == TCL_OUT_BF16 ? OutKind::BF16 : OutKind::F32;
     Plan pl;
-    if ((st = plan_on_device(InKind::BF16, ok, M, N, K, cfg, ds, &pl))) return st;
+    if ((st = plan_on_device(InKind::BF16, ok, M, N, K2, cfg, ds, &pl))) return st;
+    const size_t a_bytes = pack_a ? static_cast<size_t>(M) * lda2 * 2 : 0;
+    const size_t b_bytes = pack_b ? static_cast<size_t>(K2) * ldb2 * 2 : 0;
+    const size_t c_bytes = pack_c ? static_cast<size_t>(M) * ldc2 * oes : 0;
     const Workspace ws = split_workspace(pl, M, N);
-    if (ws.bytes && (st = ensure_scratch(ds, ws.bytes))) return st;
-    return run_gemm(pl, InKind::BF16, ok, M, N, K, A, lda, B, ldb, C, ldc, ds->scratch, cfg, dev, ds, stream);
+    const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
+                                            round_up(c_bytes, 256)) + ws.bytes;
+    if (need && (st = ensure_scratch(ds, need))) return st;
+    Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
+    void* a2 = cv.take(a_bytes);
+    void* b2 = cv.take(b_bytes);
+    void* c2 = cv.take(c_bytes);
+    void* wsp = cv.take(ws.bytes);
+    if ((pack_a && launch_repack(A, lda, M, K, a2, lda2, M, K2, 2, ds->sms, stream) != cudaSuccess) ||
+        (pack_b && launch_repack(B, ldb, K, N, b2, ldb2, K2, N, 2, ds->sms, stream) != cudaSuccess)) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    st = run_gemm(pl, InKind::BF16, ok, M, N, K2, pack_a ? a2 : A, pack_a ? lda2 : lda, pack_b ? b2 : B,
+                  pack_b ? ldb2 : ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, stream);
+    if (st) return st;
+    if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, oes, ds->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return TCL_OK;
 }
 
 int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
                    int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 4 || ldb % 4 || K % 4 || ldc % 4)
-        return TCL_ERR_ALIGN;
+    if (!aligned_to(A, 4) || !aligned_to(B, 4) || !aligned_to(C, 4)) return TCL_ERR_ALIGN;
+    // As for bf16: off-grid operands are repacked (K zero-padded to a multiple
+    // of 4), an off-grid output goes through scratch. B is always copied: the
+    // TF32 tensor-core path takes it K-major, transposed into N rows of K4.
+    const bool pack_a = !aligned16(A) || lda % 4 || K % 4;
+    const bool pack_c = !aligned16(C) || ldc % 4;
+    const int K4 = static_cast<int>(round_up(K, 4));
+    const long long ldc2 = round_up(N, 4);
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
     Plan pl;
-    if ((st = plan_on_device(InKind::TF32, OutKind::F32, M, N, K, cfg, ds, &pl))) return st;
-    // The TF32 tensor-core path takes B K-major: transpose it (N rows of K) into
-    // scratch, followed by the split-K workspace if the plan has one. Sized
-    // before anything is enqueued, since growing the scratch frees the old one.
-    const size_t bt_bytes = static_cast<size_t>(round_up(static_cast<long long>(N) * K * 4, 256));
+    if ((st = plan_on_device(InKind::TF32, OutKind::F32, M, N, K4, cfg, ds, &pl))) return st;
+    const size_t bt_bytes = static_cast<size_t>(N) * K4 * 4;
+    const size_t a_bytes = pack_a ? static_cast<size_t>(M) * K4 * 4 : 0;
+    const size_t c_bytes = pack_c ? static_cast<size_t>(M) * ldc2 * 4 : 0;
     const Workspace ws = split_workspace(pl, M, N);
-    if ((st = ensure_scratch(ds, bt_bytes + ws.bytes))) return st;
-    float* bt = static_cast<float*>(ds->scratch);
-    if (launch_transpose_f32(B, ldb, bt, K, K, N, ds->sms, stream) != cudaSuccess) {
+    const size_t need = static_cast<size_t>(round_up(bt_bytes, 256) + round_up(a_bytes, 256) +
+                                            round_up(c_bytes, 256)) + ws.bytes;
+    if ((st = ensure_scratch(ds, need))) return st;
+    Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
+    float* bt = static_cast<float*>(cv.take(bt_bytes));
+    void* a2 = cv.take(a_bytes);
+    void* c2 = cv.take(c_bytes);
+    void* wsp = cv.take(ws.bytes);
+    if ((K4 != K && cudaMemsetAsync(bt, 0, bt_bytes, stream) != cudaSuccess) ||
+        launch_transpose_f32(B, ldb, bt, K4, K, N, ds->sms, stream) != cudaSuccess ||
+        (pack_a && launch_repack(A, lda, M, K, a2, K4, M, K4, 4, ds->sms, stream) != cudaSuccess)) {
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }
-    return run_gemm(pl, InKind::TF32, OutKind::F32, M, N, K, A, lda, bt, K, C, ldc,
-                    static_cast<uint8_t*>(ds->scratch) + bt_bytes, cfg, dev, ds, stream);
+    st = run_gemm(pl, InKind::TF32, OutKind::F32, M, N, K4, pack_a ? a2 : A, pack_a ? K4 : lda, bt, K4,
+                  pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, stream);
+    if (st) return st;
+    if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, 4, ds->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return TCL_OK;
 }
 
 
@@ -600,9 +670,10 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
                  int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 16 || ldb % 16 || ldc % 4)
-        return TCL_ERR_ALIGN;
+    if (!aligned_to(C, 4)) return TCL_ERR_ALIGN;   // int8 operands: any alignment (always repacked)
     if (K > 131071) return TCL_ERR_K_TOO_LARGE;
+    const bool pack_c = !aligned16(C) || ldc % 4;
+    const long long ldc2 = round_up(N, 4);
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
     DevState* ds;
@@ -613,16 +684,24 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
     const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
     const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
-    if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes)))) return st;
+    const long long c_bytes = pack_c ? round_up(static_cast<long long>(M) * ldc2 * 4, 256) : 0;
+    if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes + c_bytes)))) return st;
     uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
     uint8_t* b2 = a2 + a_bytes;
+    int32_t* c2 = pack_c ? reinterpret_cast<int32_t*>(b2 + b_bytes) : nullptr;
     if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, ds->sms, stream) != cudaSuccess ||
         launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }
-    return run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, C, ldc, nullptr, cfg, dev, ds,
-                    stream);
+    st = run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, pack_c ? c2 : C,
+                  pack_c ? ldc2 : ldc, nullptr, cfg, dev, ds, stream);
+    if (st) return st;
+    if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, 4, ds->sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return TCL_OK;
 }
 
 }  // namespace

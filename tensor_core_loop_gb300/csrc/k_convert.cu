@@ -2,17 +2,18 @@
 //   * exact int8 -> bf16 widening (integer GEMM);
 //   * fp32 transpose K×N -> N×K (TF32 GEMM: the tensor cores take its B
 //     operand K-major);
-//   * the fixed-order sum of split-K partial tiles.
+//   * the fixed-order sum of split-K partial tiles;
+//   * 2-D copies with zero fill, for operands or outputs whose base address or
+//     leading dimension is off the 16-byte grid the tensor copies need.
 //
 // int8 -> bf16:
 // Every int8 value (|x| <= 128) has at most 8 significant bits, so it is
 // represented exactly by bf16; the bf16 pattern is the upper half of the
 // binary32 encoding of the integer. Rows are processed in 16-element chunks:
-// one 16-byte load, two 16-byte stores. The source base and its leading
-// dimension are 16-byte aligned (checked by the C-ABI), the destination rows
-// are padded to a multiple of 8 elements (the padding is written as zeros), so
-// full chunks use vector accesses and only a ragged row tail falls back to
-// scalar accesses.
+// one 16-byte load, two 16-byte stores. The destination rows are padded to a
+// multiple of 8 elements (the padding is written as zeros). When the source
+// base and leading dimension are 16-byte aligned (`vec`), full chunks use
+// vector loads; otherwise, and at a ragged row tail, bytes are read one by one.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -30,7 +31,7 @@ __device__ __forceinline__ uint32_t s8_pair_to_bf16x2(int lo, int hi) {
 __global__ void __launch_bounds__(256) s8_to_bf16_kernel(const int8_t* __restrict__ src,
                                                           long long ld_src,
                                                           uint16_t* __restrict__ dst,
-                                                          long long ld_dst, int rows, int cols) {
+                                                          long long ld_dst, int rows, int cols, int vec) {
     const int chunks_per_row = (cols + 15) / 16;
     const long long total = static_cast<long long>(rows) * chunks_per_row;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -40,7 +41,14 @@ __global__ void __launch_bounds__(256) s8_to_bf16_kernel(const int8_t* __restric
         const int8_t* s = src + r * ld_src + c0;
         uint16_t* d = dst + r * ld_dst + c0;
         if (c0 + 16 <= cols) {
-            const int4 raw = *reinterpret_cast<const int4*>(s);
+            int4 raw;
+            if (vec) {
+                raw = *reinterpret_cast<const int4*>(s);
+            } else {
+                int8_t* rb = reinterpret_cast<int8_t*>(&raw);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) rb[j] = s[j];
+            }
             const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
             uint4 o0, o1;
             o0.x = s8_pair_to_bf16x2(b[0], b[1]);
@@ -66,6 +74,7 @@ __global__ void __launch_bounds__(256) s8_to_bf16_kernel(const int8_t* __restric
 
 cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, long long ld_dst,
                               int rows, int cols, int sms, cudaStream_t stream) {
+    const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && ld_src % 16 == 0) ? 1 : 0;
     const long long chunks = static_cast<long long>(rows) * ((cols + 15) / 16);
     const int threads = 256;
     long long blocks = (chunks + threads - 1) / threads;
@@ -73,7 +82,43 @@ cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, lo
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        src, ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+        src, ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols, vec);
+    return cudaGetLastError();
+}
+
+// dst[r][c] = src[r][c] for r < rows, c < cols, and 0 for the rest of the
+// rows_pad × cols_pad block (elements of T; any source or destination
+// alignment, so element by element, consecutive threads on consecutive columns).
+template <class T>
+__global__ void __launch_bounds__(256) repack_kernel(const T* __restrict__ src, long long ld_src, int rows,
+                                                      int cols, T* __restrict__ dst, long long ld_dst, int rows_pad,
+                                                      int cols_pad) {
+    const long long total = static_cast<long long>(rows_pad) * cols_pad;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(idx / cols_pad);
+        const int c = static_cast<int>(idx - static_cast<long long>(r) * cols_pad);
+        dst[r * ld_dst + c] = (r < rows && c < cols) ? src[r * ld_src + c] : T(0);
+    }
+}
+
+cudaError_t launch_repack(const void* src, long long ld_src, int rows, int cols, void* dst, long long ld_dst,
+                          int rows_pad, int cols_pad, int elem_bytes, int sms, cudaStream_t stream) {
+    const long long total = static_cast<long long>(rows_pad) * cols_pad;
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (elem_bytes == 2)
+        repack_kernel<uint16_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(src), ld_src, rows, cols, static_cast<uint16_t*>(dst), ld_dst, rows_pad,
+            cols_pad);
+    else if (elem_bytes == 4)
+        repack_kernel<uint32_t><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint32_t*>(src), ld_src, rows, cols, static_cast<uint32_t*>(dst), ld_dst, rows_pad,
+            cols_pad);
+    else
+        return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

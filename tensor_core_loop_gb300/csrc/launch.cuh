@@ -47,6 +47,12 @@ cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, lo
 cudaError_t launch_splitk_reduce(const float* W, long long ldw, long long rows_per_split, int splits, void* C,
                                  long long ldc, int M, int N, int out_bf16, int sms, cudaStream_t stream);
 
+// dst[r][c] = src[r][c] (r < rows, c < cols), zeros elsewhere in rows_pad ×
+// cols_pad; elements of 2 or 4 bytes, any alignment. With rows_pad = rows and
+// cols_pad = cols it is a plain strided copy.
+cudaError_t launch_repack(const void* src, long long ld_src, int rows, int cols, void* dst, long long ld_dst,
+                          int rows_pad, int cols_pad, int elem_bytes, int sms, cudaStream_t stream);
+
 // dst (cols × rows) = transpose of src (rows × cols), fp32, bit for bit.
 cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
                                  int cols, int sms, cudaStream_t stream);

@@ -47,7 +47,10 @@ def test_version_and_status_strings(L):
 
 # Fake but well-formed device addresses: validation must reject before any CUDA call.
 P = 0x10000000
-PM = 0x10000004  # misaligned
+PO = 0x10000001  # odd: not aligned to any element size
+P2 = 0x10000002  # 2-byte aligned only
+# (Only calls that the host-side checks reject get these fake pointers: a call
+# that passed them would launch kernels on addresses that do not exist.)
 
 
 @pytest.mark.parametrize("args,status", [
@@ -58,24 +61,25 @@ PM = 0x10000004  # misaligned
     ((64, 64, 64, P, 32, P, 64, P, 64, 0), 3),            # lda < K
     ((64, 64, 64, P, 64, P, 32, P, 64, 0), 3),            # ldb < N
     ((64, 64, 64, P, 64, P, 64, P, 32, 0), 3),            # ldc < N
-    ((64, 64, 64, PM, 64, P, 64, P, 64, 0), 4),           # A misaligned
-    ((64, 64, 64, P, 68, P, 64, P, 64, 0), 4),            # lda*2 not a multiple of 16
-    ((64, 64, 64, P, 64, P, 64, P, 66, 0), 4),            # ldc*4 not a multiple of 16
-    ((64, 64, 64, P, 64, P, 64, P, 68, 1), 4),            # bf16 C: ldc*2 not a multiple of 16
+    ((64, 64, 64, PO, 64, P, 64, P, 64, 0), 4),           # A not on a 2-byte boundary
+    ((64, 64, 64, P, 64, PO, 64, P, 64, 0), 4),           # B not on a 2-byte boundary
+    ((64, 64, 64, P, 64, P, 64, P2, 64, 0), 4),           # fp32 C not on a 4-byte boundary
+    ((64, 64, 64, P, 64, P, 64, PO, 64, 1), 4),           # bf16 C not on a 2-byte boundary
     ((64, 64, 64, P, 64, P, 64, P, 64, 7), 8),            # unknown output type
-    ((64, 64, 60, P, 64, P, 64, P, 64, 0), 4),            # K*2 bytes not a multiple of 16
 ])
 def test_gemm_bf16_rejects(L, args, status):
     assert L.gemm_bf16(*args, None) == status
 
 
 def test_gemm_tf32_and_s8_reject(L):
-    assert L.gemm_tf32(64, 64, 64, P, 66, P, 64, P, 64, None) == 4
+    assert L.gemm_tf32(64, 64, 64, P2, 64, P, 64, P, 64, None) == 4       # fp32 A not on a 4-byte boundary
+    assert L.gemm_tf32(64, 64, 64, P, 64, P, 64, P2, 64, None) == 4
     assert L.gemm_tf32(64, 64, 64, 0, 64, P, 64, P, 64, None) == 1
-    assert L.gemm_tf32(64, 64, 62, P, 64, P, 64, P, 64, None) == 4        # K*4 bytes not a multiple of 16
-    assert L.gemm_s8(64, 64, 64, P, 72, P, 64, P, 64, None) == 4          # lda not a multiple of 16
     assert L.gemm_s8(64, 64, 131072, P, 131072, P, 64, P, 64, None) == 5  # K beyond the exact int32 range
-    assert L.gemm_s8(64, 64, 64, P, 64, P, 64, PM, 64, None) == 4
+    assert L.gemm_s8(64, 64, 64, P, 64, P, 64, P2, 64, None) == 4         # int32 C not on a 4-byte boundary
+    # the allocation-free form keeps the tensor-copy rule (it has no scratch to repack into)
+    assert L.gemm_s8_static(64, 64, 64, P, 72, P, 64, P, 64, None) == 4
+    assert L.gemm_s8_static(64, 64, 64, P, 64, P, 64, P + 4, 64, None) == 4
 
 
 def test_plan_without_device(L):
@@ -141,6 +145,10 @@ def test_planner_stream_k(L):
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)["sk_tiles"] == 0
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2))
     assert (p["num_tiles"], p["sk_tiles"], p["sk_pieces"]) == (9, 1, 4)
+    # short tiles (16 k-blocks): the extra piece's epilogue costs more than the tail saves
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1024, cfg)
+    assert (p["bn"], p["sk_tiles"]) == (224, 0)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2048, cfg)["sk_tiles"] == 28
     for bad in (tcl.Config(max_ctas=8, cta_pair=2, stream_k=5),       # more than 4 pieces
                 tcl.Config(max_ctas=8, cta_pair=1, stream_k=2),       # one-SM kernel
                 tcl.Config(max_ctas=4, cta_pair=2, stream_k=3),       # 1 tail tile × 3 pieces > 2 pairs

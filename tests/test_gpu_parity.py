@@ -70,6 +70,34 @@ def up(x, q):
     return -(-x // q) * q
 
 
+def to_dev_off(t, off):
+    """Copy a (possibly padded) host view to the device `off` elements into a fresh buffer,
+    so that its base address sits off the 16-byte grid; the bytes before it hold the view's
+    own padding pattern (or zeros for a dense view)."""
+    rows, cols = t.shape
+    ld = t.stride(0) if rows > 1 else cols
+    full = torch.as_strided(t, (rows, ld), (ld, 1))
+    flat = torch.zeros(off + rows * ld, dtype=t.dtype, device=DEV)
+    flat[off:] = full.reshape(-1).to(DEV)
+    return torch.as_strided(flat, (rows, cols), (ld, 1), off)
+
+
+def run_off(a, b, out_dtype, ldc, off):
+    """Run into a C placed `off` elements into a sentinel-filled buffer with leading dimension
+    ldc; check nothing outside the M×N block changed; return C on the host."""
+    M, N = a.shape[0], b.shape[1]
+    sentinel = -12345 if out_dtype == torch.int32 else -3.0
+    flat = torch.full((off + (M + 1) * ldc,), sentinel, dtype=out_dtype, device=DEV)
+    c = torch.as_strided(flat, (M, N), (ldc, 1), off)
+    tcl.gemm_into(a, b, c)
+    torch.cuda.synchronize()
+    host = flat.cpu()
+    inside = torch.zeros_like(host, dtype=torch.bool)
+    torch.as_strided(inside, (M, N), (ldc, 1), off).fill_(True)
+    assert (host[~inside] == sentinel).all(), "kernel wrote outside C"
+    return torch.as_strided(host, (M, N), (ldc, 1), off).clone()
+
+
 def bf16_case(oracle_mod, M, N, K, seed=0, out_dtype=torch.float32, cfg=None, lda=None, ldb=None, ldc=None,
               rows=None):
     a, b = inputs.bf16_pair(M, N, K, seed=seed, lda=lda or up(K, 8), ldb=ldb or up(N, 8))
@@ -189,7 +217,7 @@ def test_bf16_pair_kernel_bf16_out(oracle_mod, M, N, K):
     (768, 768, 2048, 2),
     (768, 768, 2048, 3),     # uneven pieces: 10, 11, 11 k-blocks
     (700, 750, 1000, 4),     # ragged M, N (last chunk added element by element), K tail in the last piece
-    (700, 750, 1000, 0),
+    (700, 750, 2000, 0),     # automatic: 32 k-blocks (the last one ragged) in 4 pieces
     (512, 1280, 576, 2),     # 10 tiles on 4 pairs: two tail tiles, pieces of 4 and 5 k-blocks
 ])
 def test_bf16_pair_stream_k(oracle_mod, M, N, K, pieces):
@@ -212,6 +240,47 @@ def test_stream_k_deterministic():
         first = run(a, b, cfg=cfg)
         for _ in range(10):
             assert torch.equal(run(a, b, cfg=cfg, canary=False), first)
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,offs,out", [
+    (130, 261, 203, 205, 263, 263, (1, 3, 1), torch.float32),    # K % 8 = 3, odd pitches, odd bases
+    (200, 300, 1000, 1003, 304, 301, (0, 0, 1), torch.bfloat16),  # only A's pitch and C's base/pitch off-grid
+    (300, 264, 512, 512, 264, 266, (0, 0, 2), torch.float32),     # only C off-grid (fp32 base 8 B off)
+    (1, 9, 5, 5, 9, 9, (1, 1, 1), torch.float32),                 # one row, K = 5
+])
+def test_bf16_off_grid_operands(oracle_mod, M, N, K, lda, ldb, ldc, offs, out):
+    # operands and outputs off the 16-byte grid the tensor copies need go through
+    # aligned copies (K zero-padded) and a copy-out; the padding poison must not leak
+    a, b = inputs.bf16_pair(M, N, K, seed=K, lda=lda, ldb=ldb)
+    got = run_off(to_dev_off(a, offs[0]), to_dev_off(b, offs[1]), out, ldc, offs[2]).double().numpy()
+    ref, S = oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b))
+    assert_within("bf16_f32" if out == torch.float32 else "bf16_bf16", got, ref, S, f"off-grid {M}x{N}x{K}")
+
+
+def test_bf16_off_grid_pair_kernel(oracle_mod):
+    a, b = inputs.bf16_pair(1024, 1000, 1004, seed=31, lda=1005, ldb=1001)
+    da, db = to_dev_off(a, 1), to_dev_off(b, 1)
+    M, N = 1024, 1000
+    flat = torch.full((1 + M * 1001,), -3.0, dtype=torch.float32, device=DEV)
+    c = torch.as_strided(flat, (M, N), (1001, 1), 1)
+    tcl.gemm_into(da, db, c, cfg=tcl.Config(cta_pair=2))
+    got = c.cpu().double().numpy()
+    ref, S = oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b))
+    assert_within("bf16_f32", got, ref, S, "off-grid pair kernel")
+
+
+def test_tf32_off_grid_operands(oracle_mod):
+    a, b = inputs.tf32_pair(130, 100, 203, seed=3, lda=207, ldb=101)   # K % 4 = 3
+    got = run_off(to_dev_off(a, 1), to_dev_off(b, 1), torch.float32, 101, 1).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, "tf32 off-grid")
+
+
+def test_s8_off_grid_operands(oracle_mod):
+    a, b = inputs.s8_pair(130, 261, 203, seed=4, lda=205, ldb=263)
+    got = run_off(to_dev_off(a, 1), to_dev_off(b, 3), torch.int32, 263, 1).numpy()
+    ref = oracle_mod.gemm_s8(a.numpy(), b.numpy())
+    assert_exact(got, ref, "int8 off-grid")
 
 
 def test_pair_kernel_variants_bitwise_identical():

@@ -60,6 +60,8 @@ def parse():
                     help="instead of the contract line: the producer × ring-depth ablation, one JSON line per run")
     ap.add_argument("--peak", action="store_true",
                     help="instead of the contract line: the tensor-pipe rate probe (MMA only) per operand layout")
+    ap.add_argument("--simt", action="store_true",
+                    help="instead of the contract line: the CUDA-core fp32 GEMM anchor at 4096^3")
     ap.add_argument("--trace", action="store_true",
                     help="instead of the contract line: per-shape load/MMA overlap from the in-kernel timeline")
     return ap.parse_args()
@@ -304,6 +306,53 @@ def run_ablation(args):
             print(json.dumps(line), flush=True)
 
 
+def measure_simt(tcl, torch, dev, stream, a, b, c, flush):
+    """The CUDA-core fp32 GEMM (no tensor cores) at 4096³: back to back for ~0.5 s with the SM
+    clock sampled, against the FFMA peak: SMs × 128 fp32 lanes × 2 flop per fused multiply-add
+    × clock."""
+    fs = (lambda: tcl.gemm_simt_into(a, b, c))
+    for _ in range(3):
+        fs()
+    ms_s = time_flushed(fs, (), 5, stream, torch, flush)
+    reps = max(10, int(500.0 / max(ms_s, 1e-3)))
+    smp = ClockSampler(dev.index)
+    smp.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fs()
+    e1.record(stream)
+    e1.synchronize()
+    cl = smp.stop()
+    ms_b2b = e0.elapsed_time(e1) / reps
+    tf_s = FLOPS / (ms_b2b * 1e-3) / 1e12
+    mhz = cl.get("sm_mhz") if cl else None
+    sms = tcl.num_sms()
+    peak_at = (lambda f: sms * 128 * 2 * f * 1e6 / 1e12)
+    return {"tflops": round(tf_s, 2), "tflops_single_flushed": round(FLOPS / (ms_s * 1e-3) / 1e12, 2),
+            "bound": "alu", "ffma_peak_at_max_clock": round(peak_at(2070.0), 2), "sm_mhz": mhz,
+            "ffma_peak_at_sampled_clock": round(peak_at(mhz), 2) if mhz else None,
+            "frac": round(tf_s / peak_at(mhz), 3) if mhz else None,
+            "reasons": cl.get("reasons") if cl else None}
+
+
+def run_simt(args):
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    ah, bh = inputs.tf32_pair(M, N, K, seed=0)
+    a, b = ah.to(dev), bh.to(dev)
+    c = torch.empty((M, N), dtype=torch.float32, device=dev)
+    line = {"simt": "fp32 GEMM on the CUDA cores, 4096^3, fp32 N(0,1) operands"}
+    line.update(measure_simt(tcl, torch, dev, stream, a, b, c, flush))
+    print(json.dumps(line), flush=True)
+
+
 def trace_stats(t, stages, bn, num_kb):
     """Pipeline statistics of one CTA's per-k-block stamps (issued, landed, MMAs issued, MMAs done)."""
     import numpy as np
@@ -453,6 +502,9 @@ def main():
     if args.peak:
         run_peak(args)
         return
+    if args.simt:
+        run_simt(args)
+        return
 
     import torch
     import torch.distributed as dist
@@ -583,6 +635,7 @@ def main():
             ft()
         mst = time_flushed(ft, (), 20, stream, torch, flush)
         extra["tf32_tflops_4096"] = round(FLOPS / (mst * 1e-3) / 1e12, 1)
+        extra["sgemm_simt_4096"] = measure_simt(tcl, torch, dev, stream, at, bt, ct, flush)
         del at, bt, ct
         del flush
 

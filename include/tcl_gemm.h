@@ -162,6 +162,17 @@ TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float*
 TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
             int ldc, cudaStream_t stream);
 
+/* SIMT fp32 GEMM: C = A·B with fp32 inputs, fp32 fused multiply-adds on the
+ * CUDA cores (no tensor cores) and fp32 C — the architecture-level anchor the
+ * pages set beside their tensor-core kernels ("4.1 CUDA GEMM 算子性能优化"
+ * §4–§9: block and thread tiling, A transposed in shared memory, float4
+ * accesses, double buffering). Each output is accumulated in increasing k
+ * from 0, one rounding per step: |C - C_exact| <= K·u/(1-K·u)·Σ_k|a_ik·b_kj|,
+ * u = 2^-24. Any leading dimensions and bases aligned to 4 bytes (16-byte
+ * aligned rows take vector accesses); M up to 8,388,480. Allocates nothing. */
+TCL_API int gemm_f32_simt(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                          cudaStream_t stream);
+
 /* Allocation-free int8 GEMM. (The pages have no counterpart: this is a
  * library service, not part of the method.)
  *

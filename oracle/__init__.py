@@ -13,7 +13,8 @@ numpy arrays to it through ctypes.
 Definition followed ("4.1 CUDA GEMM 算子性能优化", §1.1 and §3.1):
     C[i][j] = sum_k A[i][k] · B[k][j],   A: M×K, B: K×N, both row-major.
 Inputs are decoded exactly as the tensor cores consume them: bf16 exactly,
-fp32 as TF32 (truncated by default, see ``TF32_TRUNCATE``), int8 exactly.
+fp32 as TF32 (truncated by default, see ``TF32_TRUNCATE``), int8 exactly; the
+CUDA-core (SIMT) fp32 GEMM consumes fp32 as is, widened exactly to fp64.
 
 Parity is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle.py``
 (exhaustive decode, exact rational brute force, closed forms, invariants).
@@ -155,6 +156,14 @@ def gemm_f64(a: np.ndarray, b: np.ndarray, rows=None, cols=None, with_abs=True):
                                    C.ctypes.data, max(C.shape[1], 1),
                                    S.ctypes.data if with_abs else None, max(C.shape[1], 1)))
     return C, S
+
+
+def gemm_f32(a: np.ndarray, b: np.ndarray, rows=None, cols=None, with_abs=True):
+    """C = A·B for fp32 inputs taken at full fp32 precision (the SIMT GEMM's operands):
+    every fp32 value is exactly a double, so this is the fp64 loop on the widened inputs."""
+    if a.dtype != np.float32 or b.dtype != np.float32:
+        raise TypeError("expected float32 inputs")
+    return gemm_f64(np.asarray(a, np.float64), np.asarray(b, np.float64), rows, cols, with_abs)
 
 
 def gemm_s8(a: np.ndarray, b: np.ndarray, rows=None, cols=None):

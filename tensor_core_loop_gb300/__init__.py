@@ -19,7 +19,7 @@ import threading
 
 from ._build import LIB_PATH
 
-__all__ = ["gemm", "gemm_into", "plan", "lib", "Config", "last_device_error", "num_sms", "version",
+__all__ = ["gemm", "gemm_into", "gemm_simt_into", "plan", "lib", "Config", "last_device_error", "num_sms", "version",
            "TclError", "STATUS", "EXPORTED_SYMBOLS"]
 
 STATUS = {
@@ -33,7 +33,7 @@ IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",
                     "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms",
-                    "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak")
+                    "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak", "gemm_f32_simt")
 
 
 class TclError(RuntimeError):
@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
             getattr(L, name).argtypes = [I, I, I, P, I, P, I, P, I, P]
             getattr(L, name + "_ex").argtypes = [I, I, I, P, I, P, I, P, I, CP, P]
         L.gemm_s8_static.argtypes = [I, I, I, P, I, P, I, P, I, P]
+        L.gemm_f32_simt.argtypes = [I, I, I, P, I, P, I, P, I, P]
         L.tcl_mma_peak.argtypes = [I, I, I, I, I, I, P, P]
         IP = ctypes.POINTER(ctypes.c_int)
         L.tcl_plan.argtypes = [I, I, I, I, I, CP, ctypes.POINTER(PlanInfo)]
@@ -182,6 +183,25 @@ def _ld(t) -> int:
         return max(t.stride(0), t.shape[1])
     q = max(1, 16 // t.element_size())
     return -(-t.shape[1] // q) * q
+
+
+def gemm_simt_into(a, b, c, stream=None) -> None:
+    """C = A·B for fp32 CUDA tensors on the CUDA cores (fp32 FMA, no tensor cores), into ``c``."""
+    import torch
+    if not (a.is_cuda and b.is_cuda and c.is_cuda):
+        raise ValueError("a, b and c must be CUDA tensors")
+    if not (a.dtype == b.dtype == c.dtype == torch.float32):
+        raise TypeError("the SIMT GEMM takes and writes float32")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2 or tuple(c.shape) != (M, N):
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} x {tuple(b.shape)} -> {tuple(c.shape)}")
+    s = stream if stream is not None else torch.cuda.current_stream(a.device)
+    with torch.cuda.device(a.device):
+        st = lib().gemm_f32_simt(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), c.data_ptr(), _ld(c),
+                                 ctypes.c_void_p(s.cuda_stream))
+    if st:
+        raise TclError(st, "gemm_f32_simt")
 
 
 def gemm_into(a, b, c, cfg: Config | None = None, stream=None) -> None:

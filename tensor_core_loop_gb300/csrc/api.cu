@@ -768,6 +768,26 @@ int gemm_s8_ex(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, i
     return gemm_s8_impl(M, N, K, A, lda, B, ldb, C, ldc, cfg, stream);
 }
 
+int gemm_f32_simt(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C, int ldc,
+                  cudaStream_t stream) {
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st) return st;
+    if (!aligned_to(A, 4) || !aligned_to(B, 4) || !aligned_to(C, 4)) return TCL_ERR_ALIGN;
+    if ((M + 127) / 128 > 65535) return TCL_ERR_DIMS;   // grid rows
+    int dev;
+    DevState* ds;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if ((st = current_device(&dev, &ds))) return st;
+    }
+    const bool vec = aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0;
+    if (launch_sgemm_simt(A, lda, B, ldb, C, ldc, M, N, K, vec, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    return TCL_OK;
+}
+
 int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg, tcl_plan_t* plan) {
     if (M < 1 || N < 1 || K < 1) return TCL_ERR_DIMS;
     InKind ik;

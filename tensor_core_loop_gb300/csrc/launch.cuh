@@ -53,6 +53,11 @@ cudaError_t launch_splitk_reduce(const float* W, long long ldw, long long rows_p
 cudaError_t launch_repack(const void* src, long long ld_src, int rows, int cols, void* dst, long long ld_dst,
                           int rows_pad, int cols_pad, int elem_bytes, int sms, cudaStream_t stream);
 
+// SIMT fp32 GEMM on the CUDA cores (k_simt.cu). vec: A, B, C bases 16-byte
+// aligned and lda, ldb, ldc multiples of 4.
+cudaError_t launch_sgemm_simt(const float* A, long long lda, const float* B, long long ldb, float* C, long long ldc,
+                              int M, int N, int K, bool vec, cudaStream_t stream);
+
 // dst (cols × rows) = transpose of src (rows × cols), fp32, bit for bit.
 cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
                                  int cols, int sms, cudaStream_t stream);

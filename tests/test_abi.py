@@ -77,6 +77,9 @@ def test_gemm_tf32_and_s8_reject(L):
     assert L.gemm_tf32(64, 64, 64, 0, 64, P, 64, P, 64, None) == 1
     assert L.gemm_s8(64, 64, 131072, P, 131072, P, 64, P, 64, None) == 5  # K beyond the exact int32 range
     assert L.gemm_s8(64, 64, 64, P, 64, P, 64, P2, 64, None) == 4         # int32 C not on a 4-byte boundary
+    assert L.gemm_f32_simt(64, 64, 64, P2, 64, P, 64, P, 64, None) == 4   # fp32 A not on a 4-byte boundary
+    assert L.gemm_f32_simt(64, 64, 64, P, 64, P, 64, 0, 64, None) == 1
+    assert L.gemm_f32_simt(64, 64, 64, P, 64, P, 32, P, 64, None) == 3
     # the allocation-free form keeps the tensor-copy rule (it has no scratch to repack into)
     assert L.gemm_s8_static(64, 64, 64, P, 72, P, 64, P, 64, None) == 4
     assert L.gemm_s8_static(64, 64, 64, P, 64, P, 64, P + 4, 64, None) == 4

@@ -283,6 +283,44 @@ def test_s8_off_grid_operands(oracle_mod):
     assert_exact(got, ref, "int8 off-grid")
 
 
+def simt_case(oracle_mod, M, N, K, seed, lda=None, ldb=None, ldc=None, offs=(0, 0, 0), rows=None):
+    a, b = inputs.tf32_pair(M, N, K, seed=seed, lda=lda, ldb=ldb)   # fp32 N(0,1) operands
+    ldc = ldc or N
+    got = run_off_simt(to_dev_off(a, offs[0]), to_dev_off(b, offs[1]), ldc, offs[2]).double().numpy()
+    for r in (rows or [None]):
+        sl = slice(None) if r is None else slice(r, r + 1)
+        ref, S = oracle_mod.gemm_f32(a.numpy(), b.numpy(), rows=None if r is None else (r, r + 1))
+        assert_within("f32", got[sl], ref, S, f"simt {M}x{N}x{K}", K=K)
+
+
+def run_off_simt(a, b, ldc, off):
+    M, N = a.shape[0], b.shape[1]
+    flat = torch.full((off + (M + 1) * ldc,), -3.0, dtype=torch.float32, device=DEV)
+    c = torch.as_strided(flat, (M, N), (ldc, 1), off)
+    tcl.gemm_simt_into(a, b, c)
+    torch.cuda.synchronize()
+    host = flat.cpu()
+    inside = torch.zeros_like(host, dtype=torch.bool)
+    torch.as_strided(inside, (M, N), (ldc, 1), off).fill_(True)
+    assert (host[~inside] == -3.0).all(), "kernel wrote outside C"
+    return torch.as_strided(host, (M, N), (ldc, 1), off).clone()
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,offs", [
+    (256, 256, 256, None, None, None, (0, 0, 0)),
+    (1000, 1000, 1000, None, None, None, (0, 0, 0)),     # ragged 128×128 tiles, K % 16 = 8
+    (130, 261, 203, 205, 263, 263, (1, 3, 1)),           # scalar path: odd pitches and bases
+    (129, 130, 17, 20, 132, 132, (0, 0, 0)),             # vector path with ragged edges
+    (1, 1, 1, None, None, None, (0, 0, 0)),
+])
+def test_simt_f32(oracle_mod, M, N, K, lda, ldb, ldc, offs):
+    simt_case(oracle_mod, M, N, K, seed=M + K, lda=lda, ldb=ldb, ldc=ldc, offs=offs)
+
+
+def test_simt_f32_4096_sampled(oracle_mod):
+    simt_case(oracle_mod, 4096, 4096, 4096, seed=0, rows=sample_rows(4096, n=6))
+
+
 def test_pair_kernel_variants_bitwise_identical():
     a, b = inputs.bf16_pair(1024, 1280, 1216, seed=19)
     a, b = a.to(DEV), b.to(DEV)

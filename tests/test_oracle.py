@@ -285,6 +285,46 @@ def test_f64_entry_matches_numpy_on_exact_data(oracle_mod):
     assert np.array_equal(S, np.abs(A) @ np.abs(B))
 
 
+def test_f32_entry_exact_and_full_precision(oracle_mod):
+    # fp32 inputs that are small integers: the exact integer product (brute force)
+    g = np.random.default_rng(5)
+    A = g.integers(-40, 41, (9, 13)).astype(np.float32)
+    B = g.integers(-40, 41, (13, 7)).astype(np.float32)
+    C, S = oracle_mod.gemm_f32(A, B)
+    exact = [[sum(int(A[i, k]) * int(B[k, j]) for k in range(13)) for j in range(7)] for i in range(9)]
+    assert np.array_equal(C, np.array(exact, dtype=np.float64))
+    assert np.array_equal(S, np.abs(A).astype(np.float64) @ np.abs(B).astype(np.float64))
+    # full fp32 precision, not TF32: 1 + 2^-20 survives (TF32 keeps 10 mantissa bits)
+    a = np.full((2, 3), 1.0 + 2.0 ** -20, np.float32)
+    b = np.zeros((3, 2), np.float32)
+    b[0, :] = 1.0
+    C, _ = oracle_mod.gemm_f32(a, b)
+    assert np.all(C == 1.0 + 2.0 ** -20)
+    # padded rows (a wider leading dimension) give the same result as dense ones
+    wide = np.full((9, 16), np.nan, np.float32)
+    wide[:, :13] = A
+    C2, _ = oracle_mod.gemm_f32(wide[:, :13], B)
+    assert np.array_equal(C2, np.array(exact, dtype=np.float64))
+
+
+def test_f32_bound_admits_fma_chain_and_rejects_a_dropped_term():
+    from bounds import bound_for
+    g = np.random.default_rng(6)
+    K = 300
+    a = g.standard_normal(K).astype(np.float32)
+    b = g.standard_normal(K).astype(np.float32)
+    exact = float(np.dot(a.astype(np.float64), b.astype(np.float64)))
+    S = float(np.dot(np.abs(a).astype(np.float64), np.abs(b).astype(np.float64)))
+    # an fp32 chain with one rounding per step (the product formed exactly, as an FMA does)
+    acc = np.float32(0.0)
+    for x, y in zip(a, b):
+        acc = np.float32(float(acc) + float(x) * float(y))
+    bound = float(bound_for("f32", np.array([exact]), np.array([S]), K)[0])
+    assert abs(float(acc) - exact) <= bound
+    # losing one product term is caught
+    assert abs(float(acc) - float(a[7]) * float(b[7]) - exact) > bound
+
+
 def test_bad_arguments_rejected(oracle_mod):
     a = np.zeros((4, 8), np.uint16)
     b = np.zeros((7, 4), np.uint16)

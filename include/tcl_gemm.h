@@ -141,6 +141,11 @@ typedef struct {
                                       handshake) overlaps the end of the previous kernel in the
                                       stream; it reads and writes global memory only after that
                                       kernel has completed. 1: plain stream order */
+    int cluster_pairs;             /* two-SM kernel: 0 automatic; 1 one CTA pair per cluster; 2 two
+                                      pairs per cluster on the two 256-row tiles of a 512-row couple,
+                                      each CTA fetching half of its B operand from L2 and multicasting
+                                      it to the CTA in the same place of the other pair (half the L2
+                                      reads of B) */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -230,6 +235,8 @@ typedef struct {
     unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
     int sk_tiles;                   /* tail tiles computed stream-K (0: none) */
     int sk_pieces;                  /* K ranges per stream-K tile */
+    int cluster_pairs;              /* two-SM kernel: CTA pairs per cluster (0: one-SM kernel); with 2,
+                                       num_tiles and sk_tiles count 512-row couples of tiles */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

@@ -65,6 +65,7 @@ class Config(ctypes.Structure):
         ("debug_skip_kblock", ctypes.c_int),
         ("stream_k", ctypes.c_int),
         ("serial_launch", ctypes.c_int),
+        ("cluster_pairs", ctypes.c_int),
     ]
 
 
@@ -82,6 +83,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_ulonglong),
         ("sk_tiles", ctypes.c_int),
         ("sk_pieces", ctypes.c_int),
+        ("cluster_pairs", ctypes.c_int),
     ]
 
 

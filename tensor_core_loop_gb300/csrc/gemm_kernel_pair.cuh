@@ -14,16 +14,26 @@
 //     and commits empty[s] and acc_full[b] to both CTAs at once (multicast);
 //   * both CTAs' epilogues drain their own TMEM and release the accumulator
 //     on the leader's acc_empty[b] (8 arrivals: 4 warps × 2 CTAs).
+// With PAIRS = 2 a cluster holds two such pairs working on two tiles stacked
+// in M (same column of tiles, so the same B): each CTA fetches only one of the
+// two 64-column boxes of its B half from L2 and multicasts it to itself and
+// to the CTA in the same position of the other pair, halving the L2 reads of
+// B. A stage is then refilled only when both pairs' MMAs are done with it
+// (empty[s] takes one multicast commit from each leader).
 // Waits are bounded as in the one-SM kernel; a role that gives up raises the
-// abort flag of both CTAs.
+// abort flag of every CTA of the cluster.
 #pragma once
 
 #include "gemm_kernel.cuh"
 
 namespace tcl {
 
-template <OutKind OK, int BN_, int STAGES_, int SLOTS_>
+template <OutKind OK, int BN_, int STAGES_, int SLOTS_, int PAIRS_ = 1>
 struct PairCfg {
+    static constexpr int PAIRS = PAIRS_;             // CTA pairs per cluster (2: B shared by multicast)
+    static constexpr int CL = 2 * PAIRS;             // CTAs per cluster
+    static constexpr int EMPTY_ARRIVALS = PAIRS;     // one multicast commit per pair leader
+    static constexpr uint16_t ALL = (1u << CL) - 1;  // multicast mask: every CTA of the cluster
     static constexpr int STAGES = STAGES_;
     static constexpr int BM = 256;                   // rows per pair tile (128 per SM)
     static constexpr int BN = BN_;                   // columns per pair tile (each SM supplies BN/2 of B)
@@ -53,17 +63,26 @@ struct PairCfg {
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t IDESC = ptx::make_idesc(1, 1, /*A K-major*/ 0, /*B MN-major*/ 1, BM, BN);
     static constexpr int THREADS = 192;
-    static constexpr uint16_t BOTH = 0x3;            // multicast mask: CTA ranks 0 and 1
 
     static_assert(OK != OutKind::S32, "exact integer mode runs on the one-SM kernel");
     static_assert(BN % 32 == 0 && BN <= 256 && BN % EPI_COLS == 0, "pair tile width");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(2 * STAGES + 5 <= 28, "barrier area");
+    static_assert(PAIRS == 1 || (PAIRS == 2 && B_BOXES % 2 == 0), "two pairs split each B half's boxes");
+};
+
+// Raises the abort flag of every CTA of the cluster (addr: this CTA's flag).
+struct AbortNet {
+    uint32_t addr;
+    int cl;
+    __device__ __forceinline__ void raise() const {
+        for (int r = 0; r < cl; ++r) ptx::st_cluster_u32(ptx::mapa_shared(addr, static_cast<uint32_t>(r)), 1u);
+    }
 };
 
 // Bounded wait that, on giving up, raises the abort flag of this CTA and of its peer.
 __device__ __forceinline__ bool wait_bounded_pair(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                                  uint32_t peer_abort, unsigned long long timeout_ns,
+                                                  AbortNet peer_abort, unsigned long long timeout_ns,
                                                   unsigned int* status, unsigned int code) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
@@ -72,7 +91,7 @@ __device__ __forceinline__ bool wait_bounded_pair(uint32_t bar, uint32_t parity,
         if (*abort_flag) return false;
         if (ptx::globaltimer_ns() - t0 > timeout_ns) {
             *abort_flag = 1u;
-            ptx::st_cluster_u32(peer_abort, 1u);
+            peer_abort.raise();
             atomicCAS(status, 0u, code);
             return false;
         }
@@ -80,7 +99,7 @@ __device__ __forceinline__ bool wait_bounded_pair(uint32_t bar, uint32_t parity,
 }
 
 __device__ __forceinline__ bool wait_warp_pair(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                               uint32_t peer_abort, unsigned long long timeout_ns,
+                                               AbortNet peer_abort, unsigned long long timeout_ns,
                                                unsigned int* status, unsigned int code) {
     if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
     int ok = 1;
@@ -133,7 +152,7 @@ __device__ __forceinline__ PairUnit pair_unit(const GemmParams& p, int cluster, 
 // rows in piece i-1 has finished writing them (its flag reads gen·8 + i).
 // Every lane performs an acquire of the flag before touching C.
 __device__ __forceinline__ bool wait_sk_flag(const uint32_t* flag, uint32_t want, volatile uint32_t* abort_flag,
-                                             uint32_t peer_abort, unsigned long long timeout_ns,
+                                             AbortNet peer_abort, unsigned long long timeout_ns,
                                              unsigned int* status) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0 && ptx::ld_acquire_gpu(flag) != want) {
@@ -145,7 +164,7 @@ __device__ __forceinline__ bool wait_sk_flag(const uint32_t* flag, uint32_t want
             }
             if (ptx::globaltimer_ns() - t0 > timeout_ns) {
                 *abort_flag = 1u;
-                ptx::st_cluster_u32(peer_abort, 1u);
+                peer_abort.raise();
                 atomicCAS(status, 0u, static_cast<unsigned int>(DEV_TIMEOUT_SK_ORDER));
                 ok = 0;
                 break;
@@ -166,11 +185,11 @@ __device__ __forceinline__ void spin_ns(unsigned long long ns) {
     }
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS>
+template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 __global__ void __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using C = PairCfg<OK, BN, STAGES, SLOTS>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -189,13 +208,15 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();   // 0: leader (issues the pair MMAs), 1: peer
+    const uint32_t crank = ptx::cluster_ctarank();
+    const uint32_t rank = crank & 1u;    // in the pair: 0 leader (issues the pair MMAs), 1 peer
+    const uint32_t pidx = crank >> 1;    // which pair of the cluster (its tile's row in the couple)
     const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full0 + 8 * s, 1);    // leader's: its producer's arrival + both CTAs' bytes
-            ptx::mbar_init(empty0 + 8 * s, 1);   // the leader's multicast commit
+            ptx::mbar_init(empty0 + 8 * s, C::EMPTY_ARRIVALS);   // each pair leader's multicast commit
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf0 + 8 * b, 1);    // the leader's multicast commit
@@ -226,11 +247,11 @@ __global__ void __launch_bounds__(192, 1)
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
 
-    const uint32_t full_leader0 = ptx::mapa_shared(full0, 0);
-    const uint32_t acce_leader0 = ptx::mapa_shared(acce0, 0);
-    const uint32_t peer_abort = ptx::mapa_shared(ptx::smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u);
-    const int cluster = blockIdx.x >> 1;
-    const int clusters = gridDim.x >> 1;
+    const uint32_t full_leader0 = ptx::mapa_shared(full0, crank & ~1u);
+    const uint32_t acce_leader0 = ptx::mapa_shared(acce0, crank & ~1u);
+    const AbortNet peer_abort{ptx::smem_u32(const_cast<uint32_t*>(abort_flag)), C::CL};
+    const int cluster = blockIdx.x / C::CL;
+    const int clusters = gridDim.x / C::CL;
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
     if (tracing && threadIdx.x == 0) {   // SM clock and wall clock at the start of CTA 0's work
         p.trace[4 * p.trace_cap + 0] = ptx::clock64();
@@ -248,6 +269,7 @@ __global__ void __launch_bounds__(192, 1)
             const PairUnit U = pair_unit(p, cluster, clusters, u);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
+            mb = mb * PAIRS + static_cast<int>(pidx);
             const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
             const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
@@ -268,9 +290,17 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t fb = full_leader0 + 8 * s;
                 ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kb * C::BK, row);
 #pragma unroll
-                for (int b = 0; b < C::B_BOXES; ++b)
-                    ptx::tma_load_2d_pair_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, fb, col + b * C::B_BOX_N,
-                                                  kb * C::BK);
+                for (int b = 0; b < C::B_BOXES; ++b) {
+                    const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
+                    if constexpr (PAIRS == 1) {
+                        ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kb * C::BK);
+                    } else if ((b & 1) == static_cast<int>(pidx)) {
+                        // this box for both pairs: to the CTA in this position of each pair,
+                        // counted on each destination pair's leader barrier
+                        const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
+                        ptx::tma_load_2d_pair_mc_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kb * C::BK, mask);
+                    }
+                }
                 if (lane == 0) *progress = it + 1;
             }
         }
@@ -317,14 +347,15 @@ __global__ void __launch_bounds__(192, 1)
                     ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
                                                  bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
                                                  kb > U.kb_lo ? 1u : 0u);
-                    ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::BOTH);
+                    // stage s free once every pair's MMAs on it are done
+                    ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
                     const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
                     s = wrap ? 0u : s + 1;
                     ph ^= wrap;
                 }
                 if (!ok) break;
-                ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf, C::BOTH);
+                ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf, static_cast<uint16_t>(0x3u << (2 * pidx)));
             }
             if (!ok) {
                 ptx::mma_commit_pair_multicast_elected(drain_bar, 0x1);
@@ -346,6 +377,7 @@ __global__ void __launch_bounds__(192, 1)
             it_next += static_cast<uint32_t>(U.kb_hi - U.kb_lo);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
+            mb = mb * PAIRS + static_cast<int>(pidx);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
             const uint32_t buf = unit & 1u;
             const uint32_t uph = (unit >> 1) & 1u;
@@ -358,8 +390,10 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             ptx::tc_fence_after();
-            // stream-K: this warp's rows of split tile d, flags[d][rank][q]
-            uint32_t* flag = U.sk_index >= 0 ? p.sk_flags + (U.sk_index * 2 + rank) * 4 + q : nullptr;
+            // stream-K: this warp's rows of split tile (d, pidx), flags[d][pidx][rank][q]
+            uint32_t* flag =
+                U.sk_index >= 0 ? p.sk_flags + ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + rank) * 4 + q
+                                : nullptr;
             if (flag && U.piece > 0 &&
                 !wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
                               p.timeout_ns, p.status)) {

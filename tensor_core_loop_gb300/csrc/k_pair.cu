@@ -1,5 +1,5 @@
 // Instantiates the two-SM (cta_group::2) GEMM variants and launches them as
-// clusters of two CTAs.
+// clusters of one or two CTA pairs.
 #include "launch.cuh"
 
 namespace tcl {
@@ -8,16 +8,16 @@ namespace {
 // attr must hold two entries; pdl adds programmatic stream serialisation
 // (the kernel may start its set-up while the previous kernel in the stream
 // finishes; it waits for that kernel before touching global memory).
-template <OutKind OK, int BN, int STAGES, int SLOTS>
+template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr, bool pdl = false) {
-    using C = PairCfg<OK, BN, STAGES, SLOTS>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = C::CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -30,36 +30,37 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     return cfg;
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS>
+template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 cudaError_t prepare() {
-    using C = PairCfg<OK, BN, STAGES, SLOTS>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
     static bool done[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES);
     if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return err;
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS>
+template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 cudaError_t launch_pair(const LaunchArgs& a) {
-    cudaError_t err = prepare<OK, BN, STAGES, SLOTS>();
+    cudaError_t err = prepare<OK, BN, STAGES, SLOTS, PAIRS>();
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(a.grid, a.stream, attr, a.pdl);
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS>, a.tmA, a.tmB, a.tmC, a.p);
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS, PAIRS>(a.grid, a.stream, attr, a.pdl);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS>, a.tmA, a.tmB, a.tmC, a.p);
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS>
+template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 int max_clusters() {
-    if (prepare<OK, BN, STAGES, SLOTS>() != cudaSuccess) return 0;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
+    if (prepare<OK, BN, STAGES, SLOTS, PAIRS>() != cudaSuccess) return 0;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS>(2, 0, attr);
+    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS, PAIRS>(C::CL, 0, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -68,10 +69,10 @@ int max_clusters() {
 
 }  // namespace
 
-#define TCL_PAIR_CASE(OK, BN, ST, SL)                                               \
-    if (a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL) {    \
-        *found = true;                                                              \
-        return launch_pair<OutKind::OK, BN, ST, SL>(a);                             \
+#define TCL_PAIR_CASE(OK, BN, ST, SL, PR)                                                       \
+    if (a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL && a.pair == PR) {    \
+        *found = true;                                                                          \
+        return launch_pair<OutKind::OK, BN, ST, SL, PR>(a);                                     \
     }
 
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
@@ -81,10 +82,11 @@ cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
     return cudaErrorNotSupported;
 }
 
-#define TCL_PAIR_OCC(OK, BN, ST, SL) \
-    if (out == OutKind::OK && bn == BN && stages == ST && slots == SL) return max_clusters<OutKind::OK, BN, ST, SL>();
+#define TCL_PAIR_OCC(OK, BN, ST, SL, PR)                                            \
+    if (out == OutKind::OK && bn == BN && stages == ST && slots == SL && pairs == PR) \
+        return max_clusters<OutKind::OK, BN, ST, SL, PR>();
 
-int pair_max_clusters(OutKind out, int bn, int stages, int slots) {
+int pair_max_clusters(OutKind out, int bn, int stages, int slots, int pairs) {
     TCL_GROUP_PAIR(TCL_PAIR_OCC)
     return 0;
 }

@@ -15,7 +15,7 @@ struct LaunchArgs {
     int bn;
     int stages;
     int prod;   // PROD_TMA, PROD_SYNC or PROD_CPASYNC
-    int pair;   // 1: two-SM kernel (cluster of two CTAs per 256-row tile)
+    int pair;   // two-SM kernel: CTA pairs per cluster (1, or 2 sharing B by multicast); 0: one-SM kernel
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
     bool pdl;   // programmatic dependent launch (two-SM kernel)
     CUtensorMap tmA, tmB, tmC;
@@ -32,9 +32,9 @@ cudaError_t launch_group_bf16_misc(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_sync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_cpasync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
-// Largest number of two-CTA clusters of the given pair variant that can be
-// resident at once on the current device (0 on error).
-int pair_max_clusters(OutKind out, int bn, int stages, int slots);
+// Largest number of clusters (of `pairs` CTA pairs) of the given pair variant
+// that can be resident at once on the current device (0 on error).
+int pair_max_clusters(OutKind out, int bn, int stages, int slots, int pairs);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
 // int8 -> bf16 widening (exact) into a packed row-major buffer with ld_dst
@@ -112,12 +112,14 @@ cudaError_t launch_variant(const LaunchArgs& a) {
      KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS, 0, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::EPI_SLOTS},
 
 // Two-SM variants (bf16 in, TMA producer, 256-row pair tiles): output, tile
-// width, ring depth, epilogue staging slabs per warp.
-#define TCL_GROUP_PAIR(X) \
-    X(F32, 256, 6, 2) X(F32, 256, 4, 2) X(BF16, 256, 6, 2) X(F32, 224, 6, 2) X(F32, 224, 5, 4) X(BF16, 256, 5, 4)
-#define TCL_PAIR_INFO(OK, BN, ST, SL)                                                                   \
-    {InKind::BF16, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL>::SMEM_BYTES,                \
-     PairCfg<OutKind::OK, BN, ST, SL>::THREADS, 1, SL},
+// width, ring depth, epilogue staging slabs per warp, CTA pairs per cluster.
+#define TCL_GROUP_PAIR(X)                                                                          \
+    X(F32, 256, 6, 2, 1) X(F32, 256, 4, 2, 1) X(BF16, 256, 6, 2, 1) X(F32, 224, 6, 2, 1)            \
+    X(F32, 224, 5, 4, 1) X(BF16, 256, 5, 4, 1) X(F32, 256, 6, 2, 2) X(F32, 224, 6, 2, 2)            \
+    X(BF16, 256, 6, 2, 2)
+#define TCL_PAIR_INFO(OK, BN, ST, SL, PR)                                                               \
+    {InKind::BF16, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL, PR>::SMEM_BYTES,            \
+     PairCfg<OutKind::OK, BN, ST, SL, PR>::THREADS, PR, SL},
 
 #define TCL_VARIANT_CASE(IK, OK, BN, ST, PR)                                                           \
     if (!a.pair && a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \

@@ -230,6 +230,35 @@ def test_bf16_pair_stream_k(oracle_mod, M, N, K, pieces):
     bf16_case(oracle_mod, M, N, K, seed=K + pieces, cfg=cfg, ldc=ldc)
 
 
+@pytest.mark.parametrize("M,N,K,sk", [
+    (512, 512, 512, 1),       # one couple of 256-row tiles per column of tiles
+    (700, 750, 2000, 0),      # odd number of row tiles: the second tile of the last couple lies past M
+    (1024, 1280, 1216, 1),
+    (1024, 1280, 2048, 2),    # 10 couples on 4 clusters: two couples in stream-K pieces
+])
+def test_bf16_two_pair_clusters(oracle_mod, M, N, K, sk):
+    # two CTA pairs per cluster on stacked tiles, sharing B by multicast
+    cfg = tcl.Config(cta_pair=2, cluster_pairs=2, max_ctas=16, stream_k=sk)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K, cfg)["cluster_pairs"] == 2
+    ldc = -(-N // 4) * 4 if N % 4 else None
+    bf16_case(oracle_mod, M, N, K, seed=K + 7, cfg=cfg, ldc=ldc)
+
+
+def test_bf16_two_pair_clusters_bf16_out_and_grid(oracle_mod):
+    bf16_case(oracle_mod, 768, 1024, 832, seed=3, out_dtype=torch.bfloat16,
+              cfg=tcl.Config(cta_pair=2, cluster_pairs=2))
+    bf16_case(oracle_mod, 1024, 1536, 1024, seed=4, cfg=tcl.Config(cta_pair=2, cluster_pairs=2, bn=224, max_ctas=8))
+
+
+def test_two_pair_clusters_match_one_pair_bitwise():
+    # sharing B changes who loads it, not the MMA sequence of any tile
+    a, b = inputs.bf16_pair(1024, 1280, 1216, seed=19)
+    a, b = a.to(DEV), b.to(DEV)
+    one = run(a, b, cfg=tcl.Config(cta_pair=2, cluster_pairs=1, stream_k=1), canary=False)
+    two = run(a, b, cfg=tcl.Config(cta_pair=2, cluster_pairs=2, stream_k=1), canary=False)
+    assert torch.equal(one, two)
+
+
 def test_stream_k_deterministic():
     # the same plan gives the same bits every time: the pieces of a split tile are
     # added in range order whatever order the pairs finish in

@@ -74,6 +74,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's timed-region length; every rank receives it."""
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_step, world, steps, ms_max):
+    """Whole-job throughput in TFLOPS: every rank ran `steps` steps of the same
+    problem (weak scaling), all done when the slowest rank finished."""
+    return flops_per_step * world * steps / (ms_max * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -559,9 +573,7 @@ def main():
     ms_total = start.elapsed_time(end)
     clocks = sampler.stop() if rank == 0 else None
     if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+        ms_total = max_over_ranks(ms_total, dist, dev)
     st, code = tcl.last_device_error()
     if st:
         raise RuntimeError(f"device status {st} (code {code}) after the timed region")
@@ -572,7 +584,7 @@ def main():
     if rank == 0:
         print(f"[bench] {args.steps} steps, {ms_step * 1e3:.2f} us/step, "
               f"{FLOPS / (ms_step * 1e-3) / 1e12:.1f} TFLOPS per GPU; clocks {clocks}", file=sys.stderr, flush=True)
-    value = FLOPS * world * args.steps / (ms_total * 1e-3) / 1e12
+    value = job_value(FLOPS, world, args.steps, ms_total)
     per_launch_s = ms_step * 1e-3
     achieved = FLOPS / per_launch_s / 1e12
 

@@ -295,7 +295,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     if (want_pair < 0 || want_pair > 2) return TCL_ERR_CONFIG;
     int bn = cfg ? cfg->bn : 0;
     int pair = 0;
-    const bool pair_capable = ik == InKind::BF16 && ok != OutKind::S32 && prod == PROD_TMA;
+    const bool pair_capable = ok != OutKind::S32 && prod == PROD_TMA;   // bf16 or TF32 in, float out
     if (want_pair == 2) {
         if (!pair_capable || (bn != 0 && bn != 256 && bn != 224)) return TCL_ERR_CONFIG;
         pair = 1;
@@ -459,7 +459,7 @@ int device_pair_clusters(DevState* ds, const VariantInfo* v) {
     }
     if (idx >= 16) return 0;
     if (ds->pair_clusters[idx] == 0)
-        ds->pair_clusters[idx] = pair_max_clusters(v->out, v->bn, v->stages, v->slots, v->pair);
+        ds->pair_clusters[idx] = pair_max_clusters(v->in, v->out, v->bn, v->stages, v->slots, v->pair);
     return ds->pair_clusters[idx];
 }
 
@@ -496,8 +496,8 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
-    if (ik == InKind::TF32) {   // B given K-major (N rows of K)
-        if ((st = tensor_map(dev, B, in_t, K, N, ldb * ies, bk, pl.bn, &a.tmB))) return st;
+    if (ik == InKind::TF32) {   // B given K-major (N rows of K); a pair CTA loads its half of the rows
+        if ((st = tensor_map(dev, B, in_t, K, N, ldb * ies, bk, pl.pair ? pl.bn / 2 : pl.bn, &a.tmB))) return st;
     } else {                    // B given N-major (K rows of N)
         if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB))) return st;
     }

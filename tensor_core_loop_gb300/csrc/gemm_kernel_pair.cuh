@@ -20,6 +20,8 @@
 // to the CTA in the same position of the other pair, halving the L2 reads of
 // B. A stage is then refilled only when both pairs' MMAs are done with it
 // (empty[s] takes one multicast commit from each leader).
+// TF32 inputs (IK = TF32) take B K-major (the host transposes it): each CTA
+// then loads its half of B as one box of BN/2 rows × 128 B, 32 K values deep.
 // Waits are bounded as in the one-SM kernel; a role that gives up raises the
 // abort flag of every CTA of the cluster.
 #pragma once
@@ -28,7 +30,7 @@
 
 namespace tcl {
 
-template <OutKind OK, int BN_, int STAGES_, int SLOTS_, int PAIRS_ = 1>
+template <OutKind OK, int BN_, int STAGES_, int SLOTS_, int PAIRS_ = 1, InKind IK = InKind::BF16>
 struct PairCfg {
     static constexpr int PAIRS = PAIRS_;             // CTA pairs per cluster (2: B shared by multicast)
     static constexpr int CL = 2 * PAIRS;             // CTAs per cluster
@@ -38,15 +40,18 @@ struct PairCfg {
     static constexpr int BM = 256;                   // rows per pair tile (128 per SM)
     static constexpr int BN = BN_;                   // columns per pair tile (each SM supplies BN/2 of B)
     static constexpr int ROWS = 128;                 // rows of A and C per CTA
-    static constexpr int BK = 64;                    // bf16: one 128-byte swizzle row
-    static constexpr int UMMA_K = 16;
+    static constexpr int ES = InTraits<IK>::ES;
+    static constexpr int BK = 128 / ES;              // one 128-byte swizzle row of K (64 bf16, 32 TF32)
+    static constexpr int UMMA_K = InTraits<IK>::UMMA_K;
     static constexpr int KSUB = BK / UMMA_K;
     static constexpr int A_BYTES = ROWS * 128;       // 16 KB
-    static constexpr int B_BOX_N = 64;
-    // this CTA's half of B in whole 64-column boxes (at BN=224 the second box
-    // also brings 16 columns the MMA does not read)
-    static constexpr int B_BOXES = (BN / 2 + B_BOX_N - 1) / B_BOX_N;
-    static constexpr int B_BOX_BYTES = BK * 128;         // 8 KB
+    static constexpr bool B_MN = (IK == InKind::BF16);   // bf16 B N-major; TF32 B K-major
+    // this CTA's half of B: bf16 in whole 64-column boxes of BK rows (at BN=224
+    // the second box also brings 16 columns the MMA does not read); TF32 as one
+    // box of BN/2 rows of 128 B
+    static constexpr int B_BOX_N = B_MN ? 64 : BN / 2;
+    static constexpr int B_BOXES = B_MN ? (BN / 2 + B_BOX_N - 1) / B_BOX_N : 1;
+    static constexpr int B_BOX_BYTES = B_MN ? BK * 128 : B_BOX_N * 128;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
     static constexpr int PAIR_TX = 2 * STAGE_BYTES;         // bytes the leader's full[s] expects
@@ -61,7 +66,8 @@ struct PairCfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_USED = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
-    static constexpr uint32_t IDESC = ptx::make_idesc(1, 1, /*A K-major*/ 0, /*B MN-major*/ 1, BM, BN);
+    static constexpr uint32_t IDESC =
+        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
     static constexpr int THREADS = 192;
 
     static_assert(OK != OutKind::S32, "exact integer mode runs on the one-SM kernel");
@@ -69,6 +75,8 @@ struct PairCfg {
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(2 * STAGES + 5 <= 28, "barrier area");
     static_assert(PAIRS == 1 || (PAIRS == 2 && B_BOXES % 2 == 0), "two pairs split each B half's boxes");
+    static_assert(KSUB == 4, "four MMAs per k-block");
+    static_assert(B_MN || (B_BOX_N % 8 == 0 && B_BOX_N <= 256), "K-major B half: whole 8-row swizzle atoms");
 };
 
 // Raises the abort flag of every CTA of the cluster (addr: this CTA's flag).
@@ -185,11 +193,11 @@ __device__ __forceinline__ void spin_ns(unsigned long long ns) {
     }
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS, InKind IK>
 __global__ void __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -292,7 +300,9 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int b = 0; b < C::B_BOXES; ++b) {
                     const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
-                    if constexpr (PAIRS == 1) {
+                    if constexpr (!C::B_MN) {
+                        ptx::tma_load_2d_pair_elected(dst, &tmB, fb, kb * C::BK, col);   // K-major: (k, n)
+                    } else if constexpr (PAIRS == 1) {
                         ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kb * C::BK);
                     } else if ((b & 1) == static_cast<int>(pidx)) {
                         // this box for both pairs: to the CTA in this position of each pair,
@@ -315,9 +325,12 @@ __global__ void __launch_bounds__(192, 1)
             // start-address field (16-byte units).
             const uint32_t stage0 = ptx::smem_u32(stage_base);
             const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
-            const uint64_t bdesc0 = ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024);
-            constexpr uint64_t A_STEP = C::UMMA_K * 2 / 16;
-            constexpr uint64_t B_STEP = C::UMMA_K * 128 / 16;
+            // B N-major: boxes B_BOX_BYTES apart (leading offset), a k-slice steps
+            // UMMA_K rows of 128 B; B K-major: as A, a k-slice steps UMMA_K elements
+            const uint64_t bdesc0 = C::B_MN ? ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024)
+                                            : ptx::sdesc_sw128(stage0 + C::A_BYTES, 16, 1024);
+            constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
+            constexpr uint64_t B_STEP = C::B_MN ? C::UMMA_K * 128 / 16 : C::UMMA_K * C::ES / 16;
             constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
             static_assert(C::KSUB == 4, "four MMAs per k-block");
             uint32_t it = 0, unit = 0, s = 0, ph = 0;
@@ -344,9 +357,14 @@ __global__ void __launch_bounds__(192, 1)
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
                     const uint64_t ad = adesc0 + s * S_STEP;
                     const uint64_t bd = bdesc0 + s * S_STEP;
-                    ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
-                                                 bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
-                                                 kb > U.kb_lo ? 1u : 0u);
+                    if constexpr (IK == InKind::TF32)
+                        ptx::mma_tf32_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                      bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
+                                                      kb > U.kb_lo ? 1u : 0u);
+                    else
+                        ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                     bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
+                                                     kb > U.kb_lo ? 1u : 0u);
                     // stage s free once every pair's MMAs on it are done
                     ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();

@@ -8,9 +8,9 @@ namespace {
 // attr must hold two entries; pdl adds programmatic stream serialisation
 // (the kernel may start its set-up while the previous kernel in the stream
 // finishes; it waits for that kernel before touching global memory).
-template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr, bool pdl = false) {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
@@ -30,37 +30,37 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     return cfg;
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 cudaError_t prepare() {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
     static bool done[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES);
     if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return err;
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 cudaError_t launch_pair(const LaunchArgs& a) {
-    cudaError_t err = prepare<OK, BN, STAGES, SLOTS, PAIRS>();
+    cudaError_t err = prepare<IK, OK, BN, STAGES, SLOTS, PAIRS>();
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS, PAIRS>(a.grid, a.stream, attr, a.pdl);
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS>, a.tmA, a.tmB, a.tmC, a.p);
+    cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS, PAIRS>(a.grid, a.stream, attr, a.pdl);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, a.tmA, a.tmB, a.tmC, a.p);
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
 int max_clusters() {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS>;
-    if (prepare<OK, BN, STAGES, SLOTS, PAIRS>() != cudaSuccess) return 0;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
+    if (prepare<IK, OK, BN, STAGES, SLOTS, PAIRS>() != cudaSuccess) return 0;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<OK, BN, STAGES, SLOTS, PAIRS>(C::CL, 0, attr);
+    cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS, PAIRS>(C::CL, 0, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -69,24 +69,25 @@ int max_clusters() {
 
 }  // namespace
 
-#define TCL_PAIR_CASE(OK, BN, ST, SL, PR)                                                       \
-    if (a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL && a.pair == PR) {    \
-        *found = true;                                                                          \
-        return launch_pair<OutKind::OK, BN, ST, SL, PR>(a);                                     \
+#define TCL_PAIR_CASE(IK, OK, BN, ST, SL, PR)                                                      \
+    if (a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL && \
+        a.pair == PR) {                                                                               \
+        *found = true;                                                                                \
+        return launch_pair<InKind::IK, OutKind::OK, BN, ST, SL, PR>(a);                               \
     }
 
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
     *found = false;
-    if (!a.pair || a.in != InKind::BF16 || a.prod != PROD_TMA) return cudaErrorNotSupported;
+    if (!a.pair || a.prod != PROD_TMA) return cudaErrorNotSupported;
     TCL_GROUP_PAIR(TCL_PAIR_CASE)
     return cudaErrorNotSupported;
 }
 
-#define TCL_PAIR_OCC(OK, BN, ST, SL, PR)                                            \
-    if (out == OutKind::OK && bn == BN && stages == ST && slots == SL && pairs == PR) \
-        return max_clusters<OutKind::OK, BN, ST, SL, PR>();
+#define TCL_PAIR_OCC(IK, OK, BN, ST, SL, PR)                                                            \
+    if (in == InKind::IK && out == OutKind::OK && bn == BN && stages == ST && slots == SL && pairs == PR) \
+        return max_clusters<InKind::IK, OutKind::OK, BN, ST, SL, PR>();
 
-int pair_max_clusters(OutKind out, int bn, int stages, int slots, int pairs) {
+int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots, int pairs) {
     TCL_GROUP_PAIR(TCL_PAIR_OCC)
     return 0;
 }

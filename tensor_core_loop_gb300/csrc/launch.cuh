@@ -34,7 +34,7 @@ cudaError_t launch_group_bf16_cpasync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
 // Largest number of clusters (of `pairs` CTA pairs) of the given pair variant
 // that can be resident at once on the current device (0 on error).
-int pair_max_clusters(OutKind out, int bn, int stages, int slots, int pairs);
+int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots, int pairs);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
 // int8 -> bf16 widening (exact) into a packed row-major buffer with ld_dst
@@ -111,15 +111,16 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     {InKind::IK, OutKind::OK, BN, ST, PR, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::SMEM_BYTES, \
      KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS, 0, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::EPI_SLOTS},
 
-// Two-SM variants (bf16 in, TMA producer, 256-row pair tiles): output, tile
+// Two-SM variants (TMA producer, 256-row pair tiles): input, output, tile
 // width, ring depth, epilogue staging slabs per warp, CTA pairs per cluster.
-#define TCL_GROUP_PAIR(X)                                                                          \
-    X(F32, 256, 6, 2, 1) X(F32, 256, 4, 2, 1) X(BF16, 256, 6, 2, 1) X(F32, 224, 6, 2, 1)            \
-    X(F32, 224, 5, 4, 1) X(BF16, 256, 5, 4, 1) X(F32, 256, 6, 2, 2) X(F32, 224, 6, 2, 2)            \
-    X(BF16, 256, 6, 2, 2)
-#define TCL_PAIR_INFO(OK, BN, ST, SL, PR)                                                               \
-    {InKind::BF16, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL, PR>::SMEM_BYTES,            \
-     PairCfg<OutKind::OK, BN, ST, SL, PR>::THREADS, PR, SL},
+#define TCL_GROUP_PAIR(X)                                                                                    \
+    X(BF16, F32, 256, 6, 2, 1) X(BF16, F32, 256, 4, 2, 1) X(BF16, BF16, 256, 6, 2, 1)                        \
+    X(BF16, F32, 224, 6, 2, 1) X(BF16, F32, 224, 5, 4, 1) X(BF16, BF16, 256, 5, 4, 1)                        \
+    X(BF16, F32, 256, 6, 2, 2) X(BF16, F32, 224, 6, 2, 2) X(BF16, BF16, 256, 6, 2, 2)                        \
+    X(TF32, F32, 256, 6, 2, 1) X(TF32, F32, 224, 6, 2, 1)
+#define TCL_PAIR_INFO(IK, OK, BN, ST, SL, PR)                                                               \
+    {InKind::IK, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL, PR, InKind::IK>::SMEM_BYTES,      \
+     PairCfg<OutKind::OK, BN, ST, SL, PR, InKind::IK>::THREADS, PR, SL},
 
 #define TCL_VARIANT_CASE(IK, OK, BN, ST, PR)                                                           \
     if (!a.pair && a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \

@@ -306,6 +306,22 @@ __device__ __forceinline__ void mma_f16_pair_x4_elected(uint32_t d, uint64_t a0,
         : "memory");
 }
 
+__device__ __forceinline__ void mma_tf32_pair_x4_elected(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1,
+                                                         uint64_t b1, uint64_t a2, uint64_t b2, uint64_t a3,
+                                                         uint64_t b3, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred el, p0, pt;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %10, 0;\n\t"
+        "setp.eq.b32 pt, 0, 0;\n\t"
+        "@el tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %9, p0;\n\t"
+        "@el tcgen05.mma.cta_group::2.kind::tf32 [%0], %3, %4, %9, pt;\n\t"
+        "@el tcgen05.mma.cta_group::2.kind::tf32 [%0], %5, %6, %9, pt;\n\t"
+        "@el tcgen05.mma.cta_group::2.kind::tf32 [%0], %7, %8, %9, pt;\n\t}" ::"r"(d),
+        "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // tcgen05.commit from the elected lane (the same lane that issued the MMAs).
 __device__ __forceinline__ void mma_commit_elected(uint32_t bar) {
     asm volatile(

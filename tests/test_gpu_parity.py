@@ -305,6 +305,23 @@ def test_tf32_off_grid_operands(oracle_mod):
     assert_within("tf32", got, ref, S, "tf32 off-grid")
 
 
+@pytest.mark.parametrize("M,N,K,cfg", [
+    (512, 512, 512, dict(cta_pair=2)),
+    (300, 452, 200, dict(cta_pair=2)),                       # ragged: the peer CTA's rows past M
+    (1024, 1000, 1004, dict(cta_pair=2, bn=224)),            # K-major B half of 112 rows; K % 32 = 12
+    (768, 768, 2048, dict(cta_pair=2, max_ctas=8, stream_k=3)),   # stream-K pieces added by TMA reductions
+])
+def test_tf32_pair_kernel(oracle_mod, M, N, K, cfg):
+    # TF32 on two SMs per tile: kind::tf32 pair MMAs, B K-major, 32-deep k-blocks
+    c = tcl.Config(**cfg)
+    assert tcl.plan(tcl.IN_TF32, 0, M, N, K, c)["cta_pair"] == 2
+    a, b = inputs.tf32_pair(M, N, K, seed=M + N)
+    ldc = -(-N // 4) * 4
+    got = run(a.to(DEV), b.to(DEV), cfg=c, ldc=ldc).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, f"tf32 pair {M}x{N}x{K}")
+
+
 def test_s8_off_grid_operands(oracle_mod):
     a, b = inputs.s8_pair(130, 261, 203, seed=4, lda=205, ldb=263)
     got = run_off(to_dev_off(a, 1), to_dev_off(b, 3), torch.int32, 263, 1).numpy()

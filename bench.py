@@ -60,6 +60,8 @@ def parse():
                     help="instead of the contract line: the producer × ring-depth ablation, one JSON line per run")
     ap.add_argument("--peak", action="store_true",
                     help="instead of the contract line: the tensor-pipe rate probe (MMA only) per operand layout")
+    ap.add_argument("--sweep-launches", action="store_true",
+                    help="instead of the contract line: two launches of each K-sweep shape (for an ncu capture)")
     ap.add_argument("--simt", action="store_true",
                     help="instead of the contract line: the CUDA-core fp32 GEMM anchor at 4096^3")
     ap.add_argument("--trace", action="store_true",
@@ -240,6 +242,27 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def oracle_one_core_256():
+    """The oracle on a single host core at the small workload (bf16 256³): TFLOPS, best of 3."""
+    import oracle
+    from tensor_core_loop_gb300 import inputs
+    a, b = inputs.bf16_pair(256, 256, 256, seed=0)
+    ab, bb = inputs.bf16_bits(a), inputs.bf16_bits(b)
+    threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        best = min(_timed(lambda: oracle.gemm_bf16(ab, bb, with_abs=False)) for _ in range(3))
+    finally:
+        oracle.set_num_threads(threads)
+    return {"value": 2.0 * 256 ** 3 / best / 1e12, "unit": "TFLOPS", "cores": 1, "seconds": best}
+
+
+def _timed(fn):
+    t0 = time.perf_counter()
+    fn()
+    return time.perf_counter() - t0
+
+
 def time_rotating(fn, sets, steps, warmup, stream, torch):
     """Back-to-back launches over rotating input sets; returns ms per step."""
     for i in range(warmup):
@@ -349,6 +372,29 @@ def measure_simt(tcl, torch, dev, stream, a, b, c, flush):
             "ffma_peak_at_sampled_clock": round(peak_at(mhz), 2) if mhz else None,
             "frac": round(tf_s / peak_at(mhz), 3) if mhz else None,
             "reasons": cl.get("reasons") if cl else None}
+
+
+def run_sweep_launches(args):
+    """Each K-sweep shape (bf16, fp32 C, the planner's launch) twice, one after the other:
+    a short program for an ncu capture of the whole sweep."""
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for mn, k in SWEEP:
+        ah, bh = inputs.bf16_pair(mn, mn, k, seed=0)
+        a, b = ah.to(dev), bh.to(dev)
+        c = torch.empty((mn, mn), dtype=torch.float32, device=dev)
+        for _ in range(2):
+            tcl.gemm_into(a, b, c)
+        torch.cuda.synchronize()
+        print(json.dumps({"shape": f"{mn}x{mn}x{k}", "plan": tcl.plan(tcl.IN_BF16, tcl.OUT_F32, mn, mn, k)}),
+              flush=True)
+        del a, b, c
+    st, code = tcl.last_device_error()
+    if st:
+        raise RuntimeError(f"device status {st} (code {code})")
 
 
 def run_simt(args):
@@ -519,6 +565,9 @@ def main():
     if args.simt:
         run_simt(args)
         return
+    if args.sweep_launches:
+        run_sweep_launches(args)
+        return
 
     import torch
     import torch.distributed as dist
@@ -686,7 +735,8 @@ def main():
     if rank == 0 and not args.no_cpu:
         tf, rows, secs, cores = cpu_oracle_sample()
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-               "sample": f"{rows} of {M} rows of C (all {N} columns, full K={K}), {secs:.1f} s"}
+               "sample": f"{rows} of {M} rows of C (all {N} columns, full K={K}), {secs:.1f} s",
+               "one_core_256": oracle_one_core_256()}
 
     if world > 1:
         dist.barrier()

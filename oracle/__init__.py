@@ -70,6 +70,8 @@ def _load():
         lib.oracle_decode_bf16.argtypes = [P, P, L]
         lib.oracle_decode_tf32.argtypes = [P, P, L, I]
         lib.oracle_num_threads.restype = I
+        lib.oracle_set_num_threads.argtypes = [I]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
         return lib
 
@@ -77,6 +79,11 @@ def _load():
 def num_threads() -> int:
     """OpenMP threads the oracle uses (all host cores unless OMP_NUM_THREADS says otherwise)."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """OpenMP threads for the following oracle calls (timing on one core uses 1)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _as_rows(x: np.ndarray, dtype) -> tuple[np.ndarray, int]:

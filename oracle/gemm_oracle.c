@@ -86,6 +86,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads for the following calls (n >= 1); used to time the oracle on one core. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ---- the definition, in fp64 -------------------------------------------
  * Rows [i0, i1) and columns [j0, j1) of C = A·B, where A is given by a row
  * decoder and B already decoded to doubles (Bd, K rows, ldbd columns, holding

@@ -123,8 +123,9 @@ typedef struct {
     int epi_slots;                 /* epilogue staging slabs per warp, i.e. output stores in flight
                                       (0: automatic; two-SM kernel: 2 or 4, one-SM kernel: 2) */
     int debug_skip_kblock;         /* test hook, 0 = off. k > 0: CTA 0's TMA producer never loads
-                                      the (k-1)-th k-block of its walk, so the MMA warp's bounded
-                                      wait must run out; the call then reports
+                                      the (k-1)-th k-block of its walk (two-SM kernel: CTA 0 skips
+                                      its share while announcing the stage's bytes), so the MMA
+                                      warp's bounded wait must run out; the call then reports
                                       TCL_ERR_DEVICE_TIMEOUT through tcl_last_device_error() and
                                       the outputs of that CTA are undefined */
     int stream_k;                  /* two-SM kernel, fp32 C: 0 automatic (when the last wave of
@@ -146,6 +147,9 @@ typedef struct {
                                       each CTA fetching half of its B operand from L2 and multicasting
                                       it to the CTA in the same place of the other pair (half the L2
                                       reads of B) */
+    int debug_stream_k_stall;      /* test hook, 0 = off. 1: the first stream-K piece of the first
+                                      split tile never hands its tile over, so the next piece's
+                                      bounded wait must run out (device status code 5) */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)

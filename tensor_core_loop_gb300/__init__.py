@@ -66,6 +66,7 @@ class Config(ctypes.Structure):
         ("stream_k", ctypes.c_int),
         ("serial_launch", ctypes.c_int),
         ("cluster_pairs", ctypes.c_int),
+        ("debug_stream_k_stall", ctypes.c_int),
     ]
 
 

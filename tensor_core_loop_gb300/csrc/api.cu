@@ -534,6 +534,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.debug_skip_kb = cfg && cfg->debug_skip_kblock > 0 ? cfg->debug_skip_kblock - 1 : -1;
     p.sk_tiles = pl.sk_tiles;
     p.sk_pieces = pl.sk_pieces;
+    p.debug_sk_stall = cfg && cfg->debug_stream_k_stall ? 1 : 0;
     p.sk_flags = ds->sk_flags;
     p.sk_gen = 0;
     if (pl.sk_tiles) {

@@ -99,6 +99,7 @@ struct GemmParams {
     int sk_pieces;               // K ranges per split tile (>= 2 when sk_tiles > 0)
     unsigned int* sk_flags;      // [sk_tiles][2 CTAs][4 epilogue warps] progress flags
     unsigned int sk_gen;         // this launch's flag generation (flags hold gen·8 + pieces done)
+    int debug_sk_stall;          // test hook: piece 0 of split tile 0 never publishes its flag
 };
 
 // Work item w → output tile (mb, nb), its k-block range [kb_lo, kb_hi) and

@@ -296,6 +296,11 @@ __global__ void __launch_bounds__(192, 1)
                 if (leader) ptx::mbar_arrive_expect_tx_elected(full0 + 8 * s, C::PAIR_TX);
                 const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
                 const uint32_t fb = full_leader0 + 8 * s;
+                // test hook: CTA 0 announces the stage's bytes but never loads its share
+                if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) {
+                    if (lane == 0) *progress = it + 1;
+                    continue;
+                }
                 ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kb * C::BK, row);
 #pragma unroll
                 for (int b = 0; b < C::B_BOXES; ++b) {
@@ -448,10 +453,12 @@ __global__ void __launch_bounds__(192, 1)
                 // hand these rows to the next piece once every write to them has landed
                 __threadfence();   // the ragged-edge chunk's element writes, from every lane
                 __syncwarp();
+                // (test hook: the first piece of split tile 0 never hands over)
+                const bool held = p.debug_sk_stall && U.sk_index == 0 && U.piece == 0;
                 if (lane == 0) {
                     ptx::bulk_wait<0>();               // this warp's stores/reductions completed
                     ptx::fence_proxy_async_global();   // ... and ordered before the release
-                    ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
+                    if (!held) ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
                 }
                 __syncwarp();
             }

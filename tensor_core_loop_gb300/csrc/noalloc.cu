@@ -122,6 +122,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.sk_pieces = 1;
     p.sk_flags = nullptr;
     p.sk_gen = 0;
+    p.debug_sk_stall = 0;
 
     if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, sms, stream) != cudaSuccess ||
         launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, sms, stream) != cudaSuccess) {

@@ -1,8 +1,9 @@
-"""Failure detection on the GPU without a fault: every mbarrier wait in the
-kernel is bounded. A test hook makes CTA 0's producer skip one k-block, so the
-MMA warp waits for data that never arrives; the wait must run out, record the
-code in the device status word, let the kernel return, and leave the context
-usable for the next call."""
+"""Failure detection on the GPU without a fault: every wait in the kernels is
+bounded. Test hooks make CTA 0's producer skip one k-block (the MMA warp waits
+for data that never arrives) or hold back a stream-K piece's hand-over (the
+next piece waits for a flag that nothing sets); the wait must run out, record
+the code in the device status word, let the kernel return, and leave the
+context usable for the next call."""
 from __future__ import annotations
 
 import numpy as np
@@ -40,6 +41,43 @@ def test_bounded_wait_runs_out_and_context_survives():
     again = tcl.gemm(a, b)
     torch.cuda.synchronize()
     assert torch.equal(ref, again)
+    assert tcl.last_device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_two_sm_kernel_bounded_wait_runs_out(pairs):
+    # CTA 0 of the first cluster announces a stage's bytes but never loads its share:
+    # the leader's MMA wait runs out; every CTA of the cluster aborts and returns
+    a, b = inputs.bf16_pair(1024, 1024, 1024, seed=5)
+    a, b = a.to(DEV), b.to(DEV)
+    c = torch.zeros((1024, 1024), dtype=torch.float32, device=DEV)
+    cfg = tcl.Config(cta_pair=2, cluster_pairs=pairs, timeout_ns=50_000_000, debug_skip_kblock=2)
+    tcl.gemm_into(a, b, c, cfg=cfg)
+    st, code = tcl.last_device_error()
+    assert st == 7 and code in (1, 2, 3, 4), (st, code)
+    ref = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=2, cluster_pairs=pairs))
+    again = tcl.gemm(a, b)
+    torch.cuda.synchronize()
+    assert torch.allclose(ref, again, rtol=0, atol=1e-2)   # both correct (different plans)
+    assert tcl.last_device_error() == (0, 0)
+
+
+def test_stream_k_order_wait_runs_out():
+    # the first piece of split tile 0 never hands over: the last piece's wait for it
+    # (the last unit of its pair, so nothing else is waiting) runs out with code 5
+    a, b = inputs.bf16_pair(768, 768, 2048, seed=6)
+    a, b = a.to(DEV), b.to(DEV)
+    c = torch.zeros((768, 768), dtype=torch.float32, device=DEV)
+    base = dict(cta_pair=2, max_ctas=8, stream_k=2)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(**base))["sk_tiles"] == 1
+    tcl.gemm_into(a, b, c, cfg=tcl.Config(timeout_ns=50_000_000, debug_stream_k_stall=1, **base))
+    st, code = tcl.last_device_error()
+    assert (st, code) == (7, 5), (st, code)
+    # the next stream-K call (a new flag generation) is correct
+    x = tcl.gemm(a, b, cfg=tcl.Config(**base))
+    y = tcl.gemm(a, b, cfg=tcl.Config(**base))
+    torch.cuda.synchronize()
+    assert torch.equal(x, y)
     assert tcl.last_device_error() == (0, 0)
 
 

@@ -137,10 +137,10 @@ typedef struct {
                                       exactly s ranges per tail tile of 256-wide tiles
                                       (TCL_ERR_CONFIG if they do not fit). Calls with a stream-K tail share progress flags on
                                       the device and must not run concurrently with one another */
-    int serial_launch;             /* 0 (default): the two-SM kernel is launched with programmatic
-                                      stream serialisation, so its set-up (barriers, TMEM, cluster
+    int serial_launch;             /* 0 (default): the GEMM kernels are launched with programmatic
+                                      stream serialisation, so their set-up (barriers, TMEM, cluster
                                       handshake) overlaps the end of the previous kernel in the
-                                      stream; it reads and writes global memory only after that
+                                      stream; they read and write global memory only after that
                                       kernel has completed. 1: plain stream order */
     int cluster_pairs;             /* two-SM kernel: 0 automatic; 1 one CTA pair per cluster; 2 two
                                       pairs per cluster on the two 256-row tiles of a 512-row couple,

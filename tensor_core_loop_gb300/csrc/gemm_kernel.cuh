@@ -567,6 +567,10 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Set-up above touches only this CTA's own resources: under a programmatic
+    // launch it overlaps the previous kernel's tail; global memory only from here.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
     if (tracing && threadIdx.x == 0) {   // SM clock and wall clock at the start of CTA 0's work
         p.trace[4 * p.trace_cap + 0] = ptx::clock64();

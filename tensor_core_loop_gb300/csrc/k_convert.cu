@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
                                                              int out_bf16) {
     const int chunks = (N + 3) / 4;
     const long long total = static_cast<long long>(M) * chunks;
+    // launched programmatically behind the GEMM: wait for its partial tiles
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int r = static_cast<int>(idx / chunks);
@@ -179,9 +181,19 @@ cudaError_t launch_splitk_reduce(const float* W, long long ldw, long long rows_p
     const long long cap = static_cast<long long>(sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W, ldw, rows_per_split * ldw, splits, C,
-                                                                           ldc, M, N, out_bf16);
-    return cudaGetLastError();
+    // Programmatic launch: the blocks are scheduled while the GEMM finishes and
+    // wait (griddepcontrol.wait) until it has completed and its partials are visible.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, W, ldw, rows_per_split * ldw, splits, C, ldc, M, N,
+                              out_bf16);
 }
 
 // dst (cols × rows, leading dimension ld_dst) = transpose of src (rows × cols,

@@ -17,7 +17,7 @@ struct LaunchArgs {
     int prod;   // PROD_TMA, PROD_SYNC or PROD_CPASYNC
     int pair;   // two-SM kernel: CTA pairs per cluster (1, or 2 sharing B by multicast); 0: one-SM kernel
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
-    bool pdl;   // programmatic dependent launch (two-SM kernel)
+    bool pdl;   // programmatic dependent launch
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
     int grid;
@@ -91,8 +91,19 @@ cudaError_t launch_variant(const LaunchArgs& a) {
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    kern<<<a.grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(a.tmA, a.tmB, a.tmC, a.p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    if (a.pdl) {   // set-up may overlap the previous kernel in the stream (the kernel waits before any global access)
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmC, a.p);
 }
 
 // The instantiated variants (input, output, BN, ring depth, producer),

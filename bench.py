@@ -703,18 +703,14 @@ def main():
     # ---- end to end through the public API with host buffers
     e2e = None
     if rank == 0:
+        # the host-buffer call of the C ABI: it uploads A and B, runs the GEMM and
+        # downloads C, pipelined over row chunks, every step inside the timed region
         a_pin = a_h.pin_memory()
         b_pin = b_h.pin_memory()
         c_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        ad = torch.empty_like(a0)
-        bd = torch.empty_like(b0)
-        cd = torch.empty((M, N), dtype=torch.float32, device=dev)
 
         def e2e_step():
-            ad.copy_(a_pin, non_blocking=True)
-            bd.copy_(b_pin, non_blocking=True)
-            tcl.gemm_into(ad, bd, cd)
-            c_pin.copy_(cd, non_blocking=True)
+            tcl.gemm_host_into(a_pin, b_pin, c_pin, stream=stream)
         e2e_steps = max(5, min(50, args.steps))
         for _ in range(3):
             e2e_step()

@@ -171,6 +171,20 @@ TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float*
 TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
             int ldc, cudaStream_t stream);
 
+/* gemm_bf16 on matrices in HOST memory (the end-to-end form of the call; the
+ * pages have no counterpart): A, B and C are host pointers with the same
+ * shapes, leading dimensions, element types and result as gemm_bf16 (no
+ * 16-byte rule: the device copies are laid out by the library). B is uploaded
+ * whole; A and C move in up to eight row chunks on the library's own streams, so
+ * that the upload of a chunk, the GEMM of the previous one and the download of
+ * the one before overlap. The pipeline starts after the work already queued
+ * on `stream`, and `stream` waits for its end: C is complete once `stream` is
+ * synchronised. Host buffers should be page-locked (cudaHostAlloc /
+ * cudaHostRegister) for the copies to run asynchronously and overlap. Device
+ * memory: the library scratch (grown on demand) holds A, B and C. */
+TCL_API int gemm_bf16_host(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc,
+                           int out, cudaStream_t stream);
+
 /* SIMT fp32 GEMM: C = A·B with fp32 inputs, fp32 fused multiply-adds on the
  * CUDA cores (no tensor cores) and fp32 C — the architecture-level anchor the
  * pages set beside their tensor-core kernels ("4.1 CUDA GEMM 算子性能优化"

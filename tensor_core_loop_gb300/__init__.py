@@ -19,7 +19,7 @@ import threading
 
 from ._build import LIB_PATH
 
-__all__ = ["gemm", "gemm_into", "gemm_simt_into", "plan", "lib", "Config", "last_device_error", "num_sms", "version",
+__all__ = ["gemm", "gemm_into", "gemm_host_into", "gemm_simt_into", "plan", "lib", "Config", "last_device_error", "num_sms", "version",
            "TclError", "STATUS", "EXPORTED_SYMBOLS"]
 
 STATUS = {
@@ -33,7 +33,8 @@ IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",
                     "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms",
-                    "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak", "gemm_f32_simt")
+                    "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak", "gemm_f32_simt",
+                    "gemm_bf16_host")
 
 
 class TclError(RuntimeError):
@@ -111,6 +112,7 @@ def lib() -> ctypes.CDLL:
             getattr(L, name + "_ex").argtypes = [I, I, I, P, I, P, I, P, I, CP, P]
         L.gemm_s8_static.argtypes = [I, I, I, P, I, P, I, P, I, P]
         L.gemm_f32_simt.argtypes = [I, I, I, P, I, P, I, P, I, P]
+        L.gemm_bf16_host.argtypes = [I, I, I, P, I, P, I, P, I, I, P]
         L.tcl_mma_peak.argtypes = [I, I, I, I, I, I, P, P]
         IP = ctypes.POINTER(ctypes.c_int)
         L.tcl_plan.argtypes = [I, I, I, I, I, CP, ctypes.POINTER(PlanInfo)]
@@ -186,6 +188,30 @@ def _ld(t) -> int:
         return max(t.stride(0), t.shape[1])
     q = max(1, 16 // t.element_size())
     return -(-t.shape[1] // q) * q
+
+
+def gemm_host_into(a, b, c, stream=None) -> None:
+    """C = A·B for bf16 CPU tensors (page-locked for overlap) into the CPU tensor ``c``
+    (float32 or bfloat16): uploads, GEMMs and downloads pipelined by the library.
+    Asynchronous on ``stream`` (default: the current CUDA stream): ``c`` is ready
+    once that stream is synchronised."""
+    import torch
+    if a.is_cuda or b.is_cuda or c.is_cuda:
+        raise ValueError("a, b and c must be CPU tensors")
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("the host-buffer GEMM takes bf16 a and b")
+    out = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(c.dtype)
+    if out is None:
+        raise TypeError("c must be float32 or bfloat16")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2 or tuple(c.shape) != (M, N):
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} x {tuple(b.shape)} -> {tuple(c.shape)}")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib().gemm_bf16_host(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), c.data_ptr(), _ld(c), out,
+                              ctypes.c_void_p(s.cuda_stream))
+    if st:
+        raise TclError(st, "gemm_bf16_host")
 
 
 def gemm_simt_into(a, b, c, stream=None) -> None:

@@ -40,6 +40,8 @@ struct DevState {
     unsigned int sk_gen = 0;   // last stream-K flag generation used on this device
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
+    // host-buffer entry points: uploads, GEMMs and downloads on their own streams
+    cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
 };
 
 DevState g_dev[kMaxDevices];
@@ -719,6 +721,124 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     return TCL_OK;
 }
 
+// Streams of the host-buffer entry points, created once per device.
+int ensure_host_streams(DevState* ds) {
+    if (ds->up) return TCL_OK;
+    cudaStream_t s[3] = {nullptr, nullptr, nullptr};
+    for (auto& x : s) {
+        if (cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            for (auto& y : s)
+                if (y) cudaStreamDestroy(y);
+            return TCL_ERR_LAUNCH;
+        }
+    }
+    ds->up = s[0];
+    ds->comp = s[1];
+    ds->down = s[2];
+    return TCL_OK;
+}
+
+// C = A·B with A, B and C in host memory (bf16 in, fp32 or bf16 out). B is
+// uploaded whole; A and C move in row chunks on separate streams so that the
+// upload of chunk i+1, the GEMM of chunk i and the download of chunk i-1
+// overlap. The whole pipeline is ordered after earlier work on `stream` and
+// `stream` waits for its end, so the call behaves like the device-pointer
+// entry points on that stream.
+int gemm_bf16_host_impl(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc,
+                        int out, const tcl_config_t* cfg, cudaStream_t stream) {
+    int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
+    if (st) return st;
+    if (out != TCL_OUT_F32 && out != TCL_OUT_BF16) return TCL_ERR_CONFIG;
+    const int oes = out == TCL_OUT_BF16 ? 2 : 4;
+    if (!aligned_to(A, 2) || !aligned_to(B, 2) || !aligned_to(C, oes)) return TCL_ERR_ALIGN;
+    const OutKind ok = out == TCL_OUT_BF16 ? OutKind::BF16 : OutKind::F32;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    if ((st = current_device(&dev, &ds))) return st;
+    if ((st = ensure_host_streams(ds))) return st;
+    // device copies with tensor-copy pitches, K zero-padded to a multiple of 8
+    const int K2 = static_cast<int>(round_up(K, 8));
+    const long long lda2 = K2, ldb2 = round_up(N, 8), ldc2 = round_up(N, 16 / oes);
+    // up to eight row chunks of at least 512 rows (whole 256-row tiles): the first
+    // download starts after one chunk's upload and GEMM
+    int chunks = std::max(1, std::min(8, M / 512));
+    const int rows = static_cast<int>(round_up((M + chunks - 1) / chunks, 256));
+    chunks = (M + rows - 1) / rows;
+    const int last_rows = M - (chunks - 1) * rows;
+    Plan pf, plast;
+    if ((st = plan_on_device(InKind::BF16, ok, rows < M ? rows : M, N, K2, cfg, ds, &pf))) return st;
+    if ((st = plan_on_device(InKind::BF16, ok, last_rows, N, K2, cfg, ds, &plast))) return st;
+    const size_t ws_bytes = std::max(split_workspace(pf, rows < M ? rows : M, N).bytes,
+                                     split_workspace(plast, last_rows, N).bytes);
+    const size_t a_bytes = static_cast<size_t>(M) * lda2 * 2, b_bytes = static_cast<size_t>(K2) * ldb2 * 2;
+    const size_t c_bytes = static_cast<size_t>(M) * ldc2 * oes;
+    const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
+                                            round_up(c_bytes, 256)) + ws_bytes;
+    if ((st = ensure_scratch(ds, need))) return st;
+    Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
+    uint8_t* a2 = static_cast<uint8_t*>(cv.take(a_bytes));
+    uint8_t* b2 = static_cast<uint8_t*>(cv.take(b_bytes));
+    uint8_t* c2 = static_cast<uint8_t*>(cv.take(c_bytes));
+    void* wsp = cv.take(ws_bytes);
+
+    constexpr int kMaxChunks = 8;
+    cudaEvent_t ev[3 + 2 * kMaxChunks] = {};
+    const int nev = 3 + 2 * chunks;
+    auto fail = [&](int code) {
+        cudaGetLastError();
+        for (int i = 0; i < nev; ++i)
+            if (ev[i]) cudaEventDestroy(ev[i]);
+        return code;
+    };
+    for (int i = 0; i < nev; ++i)
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return fail(TCL_ERR_LAUNCH);
+    cudaEvent_t entry = ev[0], b_in = ev[1], done = ev[2];
+    cudaEvent_t* a_in = ev + 3;
+    cudaEvent_t* c_out = ev + 3 + chunks;
+    const char* Ah = static_cast<const char*>(A);
+    char* Ch = static_cast<char*>(C);
+    bool okq = cudaEventRecord(entry, stream) == cudaSuccess && cudaStreamWaitEvent(ds->up, entry, 0) == cudaSuccess &&
+               cudaStreamWaitEvent(ds->comp, entry, 0) == cudaSuccess &&
+               cudaStreamWaitEvent(ds->down, entry, 0) == cudaSuccess;
+    if (okq && K2 != K) {   // zero the K padding of both operands
+        okq = cudaMemsetAsync(a2, 0, a_bytes, ds->up) == cudaSuccess &&
+              cudaMemsetAsync(b2 + static_cast<size_t>(K) * ldb2 * 2, 0, static_cast<size_t>(K2 - K) * ldb2 * 2,
+                              ds->up) == cudaSuccess;
+    }
+    okq = okq &&
+          cudaMemcpy2DAsync(b2, ldb2 * 2, B, static_cast<size_t>(ldb) * 2, static_cast<size_t>(N) * 2, K,
+                            cudaMemcpyHostToDevice, ds->up) == cudaSuccess &&
+          cudaEventRecord(b_in, ds->up) == cudaSuccess;
+    for (int i = 0; okq && i < chunks; ++i) {
+        const int r = i + 1 < chunks ? rows : last_rows;
+        okq = cudaMemcpy2DAsync(a2 + static_cast<size_t>(i) * rows * lda2 * 2, lda2 * 2,
+                                Ah + static_cast<size_t>(i) * rows * lda * 2, static_cast<size_t>(lda) * 2,
+                                static_cast<size_t>(K) * 2, r, cudaMemcpyHostToDevice, ds->up) == cudaSuccess &&
+              cudaEventRecord(a_in[i], ds->up) == cudaSuccess;
+    }
+    okq = okq && cudaStreamWaitEvent(ds->comp, b_in, 0) == cudaSuccess;
+    for (int i = 0; okq && i < chunks; ++i) {
+        const int r = i + 1 < chunks ? rows : last_rows;
+        okq = cudaStreamWaitEvent(ds->comp, a_in[i], 0) == cudaSuccess;
+        if (!okq) break;
+        st = run_gemm(i + 1 < chunks ? pf : plast, InKind::BF16, ok, r, N, K2,
+                      a2 + static_cast<size_t>(i) * rows * lda2 * 2, lda2, b2, ldb2,
+                      c2 + static_cast<size_t>(i) * rows * ldc2 * oes, ldc2, wsp, cfg, dev, ds, ds->comp);
+        if (st) return fail(st);
+        okq = cudaEventRecord(c_out[i], ds->comp) == cudaSuccess &&
+              cudaStreamWaitEvent(ds->down, c_out[i], 0) == cudaSuccess &&
+              cudaMemcpy2DAsync(Ch + static_cast<size_t>(i) * rows * ldc * oes, static_cast<size_t>(ldc) * oes,
+                                c2 + static_cast<size_t>(i) * rows * ldc2 * oes, ldc2 * oes,
+                                static_cast<size_t>(N) * oes, r, cudaMemcpyDeviceToHost, ds->down) == cudaSuccess;
+    }
+    okq = okq && cudaEventRecord(done, ds->down) == cudaSuccess && cudaStreamWaitEvent(stream, done, 0) == cudaSuccess;
+    if (!okq) return fail(TCL_ERR_LAUNCH);
+    for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);   // released once their work has completed
+    return TCL_OK;
+}
+
 }  // namespace
 
 // Internal services for other translation units of the library.
@@ -761,6 +881,11 @@ int gemm_bf16(int M, int N, int K, const void* A, int lda, const void* B, int ld
 int gemm_bf16_ex(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C,
                  int ldc, int out, const tcl_config_t* cfg, cudaStream_t stream) {
     return gemm_bf16_impl(M, N, K, A, lda, B, ldb, C, ldc, out, cfg, stream);
+}
+
+int gemm_bf16_host(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc, int out,
+                   cudaStream_t stream) {
+    return gemm_bf16_host_impl(M, N, K, A, lda, B, ldb, C, ldc, out, nullptr, stream);
 }
 
 int gemm_tf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
@@ -908,6 +1033,15 @@ void tcl_shutdown(void) {
         return;
     }
     for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_dev[d].up) {
+            if (cudaSetDevice(d) == cudaSuccess) {
+                cudaDeviceSynchronize();
+                cudaStreamDestroy(g_dev[d].up);
+                cudaStreamDestroy(g_dev[d].comp);
+                cudaStreamDestroy(g_dev[d].down);
+            }
+            g_dev[d].up = g_dev[d].comp = g_dev[d].down = nullptr;
+        }
         if (g_dev[d].scratch) {
             if (cudaSetDevice(d) == cudaSuccess) {
                 cudaDeviceSynchronize();

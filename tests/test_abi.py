@@ -77,6 +77,10 @@ def test_gemm_tf32_and_s8_reject(L):
     assert L.gemm_tf32(64, 64, 64, 0, 64, P, 64, P, 64, None) == 1
     assert L.gemm_s8(64, 64, 131072, P, 131072, P, 64, P, 64, None) == 5  # K beyond the exact int32 range
     assert L.gemm_s8(64, 64, 64, P, 64, P, 64, P2, 64, None) == 4         # int32 C not on a 4-byte boundary
+    assert L.gemm_bf16_host(64, 64, 64, 0, 64, P, 64, P, 64, 0, None) == 1
+    assert L.gemm_bf16_host(64, 64, 64, P, 32, P, 64, P, 64, 0, None) == 3
+    assert L.gemm_bf16_host(64, 64, 64, PO, 64, P, 64, P, 64, 0, None) == 4
+    assert L.gemm_bf16_host(64, 64, 64, P, 64, P, 64, P, 64, 5, None) == 8
     assert L.gemm_f32_simt(64, 64, 64, P2, 64, P, 64, P, 64, None) == 4   # fp32 A not on a 4-byte boundary
     assert L.gemm_f32_simt(64, 64, 64, P, 64, P, 64, 0, 64, None) == 1
     assert L.gemm_f32_simt(64, 64, 64, P, 64, P, 32, P, 64, None) == 3

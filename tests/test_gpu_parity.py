@@ -430,6 +430,36 @@ def test_variants_bitwise_identical():
             assert torch.equal(o, outs[0])
 
 
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,out", [
+    (4096, 4096, 4096, 4096, 4096, 4096, torch.float32),    # eight row chunks, sampled rows
+    (1000, 777, 203, 205, 779, 780, torch.float32),         # K % 8 = 3 (zero-padded on the device), ragged
+    (1000, 520, 640, 640, 520, 528, torch.bfloat16),        # two chunks, bf16 C
+    (100, 64, 64, 64, 64, 64, torch.float32),               # one chunk
+])
+def test_host_buffer_entry_point(oracle_mod, M, N, K, lda, ldb, ldc, out):
+    # A, B, C in page-locked host memory; uploads, GEMMs and downloads pipelined
+    a, b = inputs.bf16_pair(M, N, K, seed=M + K, lda=lda, ldb=ldb)
+    ah = torch.as_strided(a, (M, lda), (lda, 1)).pin_memory()[:, :K] if lda != K else a.pin_memory()
+    bh = torch.as_strided(b, (K, ldb), (ldb, 1)).pin_memory()[:, :N] if ldb != N else b.pin_memory()
+    sentinel = -3.0
+    full = torch.full((M + 1, ldc), sentinel, dtype=out).pin_memory()
+    c = full[:M, :N]
+    side = torch.cuda.Stream()
+    tcl.gemm_host_into(ah, bh, c, stream=side)
+    side.synchronize()
+    assert (full[:M, N:] == sentinel).all() and (full[M] == sentinel).all(), "wrote outside C"
+    got = c.double().numpy()
+    kind = "bf16_f32" if out == torch.float32 else "bf16_bf16"
+    rows = sample_rows(M, n=8) if M >= 4096 else None
+    if rows is None:
+        ref, S = oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b))
+        assert_within(kind, got, ref, S, f"host {M}x{N}x{K}")
+    else:
+        for r in rows:
+            ref, S = oracle_mod.gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(b), rows=(r, r + 1))
+            assert_within(kind, got[r:r + 1], ref, S, f"host {M}x{N}x{K} row {r}")
+
+
 def test_repeat_runs_bitwise_identical():
     a, b = inputs.bf16_pair(1024, 1024, 2048, seed=17)
     a, b = a.to(DEV), b.to(DEV)

@@ -276,8 +276,10 @@ TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config
  * tile are (default: alternate two independent accumulators); bit 1: walk
  * the operand addresses like a GEMM k-loop (4 k-slices × 4 ring stages);
  * bit 2: N-major B with 64-column groups of 64 K-rows (8 KB apart, as a GEMM
- * stage holds it) instead of 16 K-rows (2 KB apart); bit 3: per 4 MMAs, the
- * rest of a GEMM issue loop (an mbarrier wait, a tcgen05 fence, a commit). */
+ * stage holds it) instead of 16 K-rows (2 KB apart); bit 3: per group of
+ * MMAs, the rest of a GEMM issue loop (an mbarrier wait, a tcgen05 fence, a
+ * commit); bit 4: of those, the wait and fence only; bit 5: the commit only;
+ * bit 6: groups of 8 MMAs instead of 4 (iters then a multiple of 8). */
 TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
                          unsigned long long* cycles, cudaStream_t stream);
 

@@ -297,16 +297,24 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     if (want_pair < 0 || want_pair > 2) return TCL_ERR_CONFIG;
     int bn = cfg ? cfg->bn : 0;
     int pair = 0;
-    const bool pair_capable = ok != OutKind::S32 && prod == PROD_TMA;   // bf16 or TF32 in, float out
+    // the two-SM kernel: bf16 or TF32 in, float out (256 or 224 wide), or the
+    // exact-integer mode (128 wide: int32 sums of a row's 128 columns in registers)
+    const bool pair_capable = prod == PROD_TMA && (ok != OutKind::S32 || ik == InKind::BF16);
+    const int pair_bn = ok == OutKind::S32 ? 128 : 256;
     if (want_pair == 2) {
-        if (!pair_capable || (bn != 0 && bn != 256 && bn != 224)) return TCL_ERR_CONFIG;
+        if (!pair_capable) return TCL_ERR_CONFIG;
+        if (ok == OutKind::S32 ? (bn != 0 && bn != 128) : (bn != 0 && bn != 256 && bn != 224))
+            return TCL_ERR_CONFIG;
         pair = 1;
-    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages)) {
+    } else if (want_pair == 0 && pair_capable && ok != OutKind::S32 && bn == 0 && !(cfg && cfg->stages)) {
+        // (exact-integer tiles stay on one SM unless asked: 128-wide pair tiles
+        // measured slower on GB300, 161.5 vs 139.6 us at 4096^3, both bound by
+        // operand delivery into shared memory)
         // Two SMs per 256-row tile halve each SM's bytes per flop; use them when
         // there are at least as many pair tiles as pairs of SMs and a tile has
         // enough k-blocks for its mainloop to outlast its epilogue (measured on
         // GB300: at 4096²×256 one SM per tile is faster, from K = 1024 on the pair).
-        const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
+        const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + pair_bn - 1) / pair_bn);
         const int kblocks = (K + bk - 1) / bk;
         pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
     }
@@ -315,13 +323,14 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         return TCL_ERR_CONFIG;
     // CTA pairs per cluster: 2 = two pairs on tiles stacked in M sharing B by multicast
     const int want_cp = cfg ? cfg->cluster_pairs : 0;
-    if (want_cp < 0 || want_cp > 2 || (want_cp == 2 && want_pair == 1)) return TCL_ERR_CONFIG;
+    if (want_cp < 0 || want_cp > 2 || (want_cp == 2 && (want_pair == 1 || ok == OutKind::S32)))
+        return TCL_ERR_CONFIG;
     const int cpairs = (pair && want_cp == 2) ? 2 : 1;
     if (pair) {
         if (bn == 0) {
             // Pair tile width: the fewest SM cycles on the busiest pair of SMs,
             // whole tiles only or with a stream-K tail (fp32 C can also use 224).
-            bn = 256;
+            bn = pair_bn;
             if (ok == OutKind::F32 && want_sk <= 1) {   // a requested stream-K split keeps 256
                 const int pairs = std::max(1, (cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms) / (2 * cpairs));
                 const int kb = (K + bk - 1) / bk;

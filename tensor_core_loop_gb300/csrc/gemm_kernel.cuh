@@ -175,6 +175,15 @@ struct KCfg {
     static constexpr uint32_t IDESC =
         ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
     static constexpr int THREADS = 32 * (P_WARPS + 5);
+    // Ring slots released per commit. A tcgen05.commit costs the tensor pipe
+    // about 67 cycles when the MMAs between commits take less time than the
+    // issue loop around them (N = 128: 4 MMAs of 64 cycles per k-block;
+    // measured on GB300 with the tensor-pipe probe); from N = 192 on it is
+    // hidden. With N <= 128 and an even ring of at least 4 slots, the MMA warp
+    // commits only after the second slot of each pair (2j, 2j+1), and the
+    // producer refills either slot once that commit has landed.
+    static constexpr int REL = (BN <= 128 && STAGES >= 4 && STAGES % 2 == 0) ? 2 : 1;
+    static __device__ __forceinline__ uint32_t rel_slot(uint32_t s) { return REL == 2 ? (s | 1u) : s; }
 
     static_assert(BN % B_BOX_N == 0, "BN must be a whole number of swizzle boxes");
     static_assert(BN % EPI_COLS == 0, "BN must be a whole number of epilogue chunks");
@@ -337,7 +346,7 @@ __device__ __forceinline__ void sync_producer(const GemmParams& p, uint8_t* stag
             const uint32_t ph = (it / C::STAGES) & 1u;
             bool got = true;
             if (lane == 0)
-                got = wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                got = wait_bounded(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, p.timeout_ns, p.status,
                                    DEV_TIMEOUT_PRODUCER);
             if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) return;
             if (tracing && pt == 0) {
@@ -425,7 +434,7 @@ __device__ __forceinline__ void cpasync_producer(const GemmParams& p, uint8_t* s
             const uint32_t ph = (it / C::STAGES) & 1u;
             bool got = true;
             if (lane == 0)
-                got = wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                got = wait_bounded(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, p.timeout_ns, p.status,
                                    DEV_TIMEOUT_PRODUCER);
             if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
                 ptx::cp_async_wait_all();   // nothing may still be writing when the CTA exits
@@ -596,7 +605,8 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
             for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
-                if (!wait_warp(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status, DEV_TIMEOUT_PRODUCER)) {
+                if (!wait_warp(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, p.timeout_ns, p.status,
+                               DEV_TIMEOUT_PRODUCER)) {
                     ok = false;
                     break;
                 }
@@ -681,7 +691,8 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                     else
                         ptx::mma_f16_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
                                                 bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC, acc);
-                    ptx::mma_commit_elected(empty0 + 8 * s);   // stage s free once these MMAs finish
+                    // stage s (and, released in pairs, s - 1) free once these MMAs finish
+                    if (C::REL == 1 || (s & 1u)) ptx::mma_commit_elected(empty0 + 8 * s);
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
                     const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
                     s = wrap ? 0u : s + 1;

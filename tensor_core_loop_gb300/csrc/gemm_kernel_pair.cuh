@@ -69,8 +69,14 @@ struct PairCfg {
     static constexpr uint32_t IDESC =
         ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
     static constexpr int THREADS = 192;
+    // ring slots released per commit, as in the one-SM kernel: each SM's share of a
+    // pair k-block (128 rows × BN columns) keeps its tensor pipe as long as a
+    // one-SM k-block of width BN
+    static constexpr int REL = (BN <= 128 && STAGES >= 4 && STAGES % 2 == 0) ? 2 : 1;
+    static __device__ __forceinline__ uint32_t rel_slot(uint32_t s) { return REL == 2 ? (s | 1u) : s; }
 
-    static_assert(OK != OutKind::S32, "exact integer mode runs on the one-SM kernel");
+    static_assert(OK != OutKind::S32 || (BN <= 128 && IK == InKind::BF16 && PAIRS == 1),
+                  "exact integer mode: int32 sums of BN <= 128 columns per thread in registers");
     static_assert(BN % 32 == 0 && BN <= 256 && BN % EPI_COLS == 0, "pair tile width");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(2 * STAGES + 5 <= 28, "barrier area");
@@ -283,8 +289,8 @@ __global__ void __launch_bounds__(192, 1)
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
-                if (!wait_warp_pair(empty0 + 8 * s, ph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                    DEV_TIMEOUT_PRODUCER)) {
+                if (!wait_warp_pair(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, peer_abort, p.timeout_ns,
+                                    p.status, DEV_TIMEOUT_PRODUCER)) {
                     ok = false;
                     break;
                 }
@@ -341,44 +347,50 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t it = 0, unit = 0, s = 0, ph = 0;
             bool ok = true;
             const int units = pair_units(p, cluster, clusters);
-            for (int u = 0; ok && u < units; ++u, ++unit) {
+            for (int u = 0; ok && u < units; ++u) {
                 const PairUnit U = pair_unit(p, cluster, clusters, u);
-                const uint32_t buf = unit & 1u;
-                const uint32_t uph = (unit >> 1) & 1u;
-                if (!wait_warp_pair(acce0 + 8 * buf, uph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                    DEV_TIMEOUT_MMA_ACC)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + buf * C::ACC_STRIDE;
-                for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
-                    if (!wait_warp_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                        DEV_TIMEOUT_MMA_FULL)) {
+                // accumulation units of kb_per_unit k-blocks (exact-integer mode: 512 K
+                // values, drained into int32 sums; otherwise the whole range)
+                for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
+                    const int kb1 = min(kb0 + p.kb_per_unit, U.kb_hi);
+                    const uint32_t buf = unit & 1u;
+                    const uint32_t uph = (unit >> 1) & 1u;
+                    if (!wait_warp_pair(acce0 + 8 * buf, uph ^ 1u, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                        DEV_TIMEOUT_MMA_ACC)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
-                    const uint64_t ad = adesc0 + s * S_STEP;
-                    const uint64_t bd = bdesc0 + s * S_STEP;
-                    if constexpr (IK == InKind::TF32)
-                        ptx::mma_tf32_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
-                                                      bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
-                                                      kb > U.kb_lo ? 1u : 0u);
-                    else
-                        ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
-                                                     bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
-                                                     kb > U.kb_lo ? 1u : 0u);
-                    // stage s free once every pair's MMAs on it are done
-                    ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
-                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
-                    const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
-                    s = wrap ? 0u : s + 1;
-                    ph ^= wrap;
+                    const uint32_t d_tmem = tmem_base + buf * C::ACC_STRIDE;
+                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                        if (!wait_warp_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                            DEV_TIMEOUT_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
+                        const uint64_t ad = adesc0 + s * S_STEP;
+                        const uint64_t bd = bdesc0 + s * S_STEP;
+                        if constexpr (IK == InKind::TF32)
+                            ptx::mma_tf32_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                          bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
+                                                          kb > kb0 ? 1u : 0u);
+                        else
+                            ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                                         bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
+                                                         kb > kb0 ? 1u : 0u);
+                        // stage s (with s - 1, released in pairs) free once every pair's MMAs on it are done
+                        if (C::REL == 1 || (s & 1u)) ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
+                        if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                        const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
+                        s = wrap ? 0u : s + 1;
+                        ph ^= wrap;
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf,
+                                                           static_cast<uint16_t>(0x3u << (2 * pidx)));
                 }
-                if (!ok) break;
-                ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf, static_cast<uint16_t>(0x3u << (2 * pidx)));
             }
             if (!ok) {
                 ptx::mma_commit_pair_multicast_elected(drain_bar, 0x1);
@@ -395,72 +407,106 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t it_next = 0;   // the ring iteration at which the unit after this one starts
         bool ok = true;
         const int units = pair_units(p, cluster, clusters);
-        for (int u = 0; ok && u < units; ++u, ++unit) {
+        for (int u = 0; ok && u < units; ++u) {
             const PairUnit U = pair_unit(p, cluster, clusters, u);
             it_next += static_cast<uint32_t>(U.kb_hi - U.kb_lo);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
             mb = mb * PAIRS + static_cast<int>(pidx);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
-            const uint32_t buf = unit & 1u;
-            const uint32_t uph = (unit >> 1) & 1u;
-            bool got = true;
-            if (lane == 0)
-                got = wait_bounded_pair(accf0 + 8 * buf, uph, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                        DEV_TIMEOUT_EPILOGUE);
-            if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
-                ok = false;
-                break;
+            [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? BN : 1];
+            if constexpr (OK == OutKind::S32) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) iacc[i] = 0;
             }
-            ptx::tc_fence_after();
-            // stream-K: this warp's rows of split tile (d, pidx), flags[d][pidx][rank][q]
-            uint32_t* flag =
-                U.sk_index >= 0 ? p.sk_flags + ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + rank) * 4 + q
-                                : nullptr;
-            if (flag && U.piece > 0 &&
-                !wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
-                              p.timeout_ns, p.status)) {
-                ok = false;
-                break;
-            }
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
-            drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
-                &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p,
-                [&]() {
+            for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
+                const uint32_t buf = unit & 1u;
+                const uint32_t uph = (unit >> 1) & 1u;
+                bool got = true;
+                if (lane == 0)
+                    got = wait_bounded_pair(accf0 + 8 * buf, uph, abort_flag, peer_abort, p.timeout_ns, p.status,
+                                            DEV_TIMEOUT_EPILOGUE);
+                if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if constexpr (OK == OutKind::S32) {
+                    // exact integers: this unit's fp32 sums (each an integer below 2^24 in
+                    // magnitude) converted and added into int32 registers; the tile's int32
+                    // result is stored after its last unit
+                    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        __syncwarp();   // tcgen05.ld is warp-collective
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(tb + c * 32, r);
+                        ptx::tmem_ld_wait(r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) iacc[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
-                },
-                /*add=*/U.piece > 0, [&](int c) {
-                    // Spread this tile's stores over the next unit's mainloop: chunk c waits
-                    // until the producer is c/EPI_CHUNKS of the way through that unit (a
-                    // burst of TMA stores slows the tensor pipe's operand reads). The
-                    // CTA's last unit, and a stream-K piece (the next piece waits for
-                    // it), store at once.
-                    if (u + 1 >= units || c == 0 || U.sk_index >= 0) return;
-                    const PairUnit V = pair_unit(p, cluster, clusters, u + 1);
-                    const uint32_t n = static_cast<uint32_t>(V.kb_hi - V.kb_lo);
-                    // (the producer issues all n k-blocks of the next unit, so the target is reached)
-                    const uint32_t target = it_next + min(n, STAGES + c * n / C::EPI_CHUNKS);
-                    if (lane == 0 && *progress < target) {
-                        const uint64_t t0 = ptx::globaltimer_ns();
-                        while (*progress < target && !*abort_flag && ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                    if (kb0 + p.kb_per_unit >= U.kb_hi) {
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c) {
+                            const uint32_t(&v)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&iacc[c * 32]);
+                            store_slab<C::SLAB_BYTES, 4, C::EPI_SLOTS>(&tmC, slab_pair, store_count, v, lane,
+                                                                       nb * C::BN + c * 32, row0, p);
                         }
                     }
-                    __syncwarp();
-                });
-            if (flag && U.piece + 1 < p.sk_pieces) {
-                // hand these rows to the next piece once every write to them has landed
-                __threadfence();   // the ragged-edge chunk's element writes, from every lane
-                __syncwarp();
-                // (test hook: the first piece of split tile 0 never hands over)
-                const bool held = p.debug_sk_stall && U.sk_index == 0 && U.piece == 0;
-                if (lane == 0) {
-                    ptx::bulk_wait<0>();               // this warp's stores/reductions completed
-                    ptx::fence_proxy_async_global();   // ... and ordered before the release
-                    if (!held) ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
+                    continue;
                 }
-                __syncwarp();
+                // stream-K: this warp's rows of split tile (d, pidx), flags[d][pidx][rank][q]
+                uint32_t* flag =
+                    U.sk_index >= 0 ? p.sk_flags + ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + rank) * 4 + q
+                                    : nullptr;
+                if (flag && U.piece > 0 &&
+                    !wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
+                                  p.timeout_ns, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
+                drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
+                    &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p,
+                    [&]() {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
+                    },
+                    /*add=*/U.piece > 0, [&](int c) {
+                        // Spread this tile's stores over the next unit's mainloop: chunk c waits
+                        // until the producer is c/EPI_CHUNKS of the way through that unit (a
+                        // burst of TMA stores slows the tensor pipe's operand reads). The
+                        // CTA's last unit, and a stream-K piece (the next piece waits for
+                        // it), store at once.
+                        if (u + 1 >= units || c == 0 || U.sk_index >= 0) return;
+                        const PairUnit V = pair_unit(p, cluster, clusters, u + 1);
+                        const uint32_t n = static_cast<uint32_t>(V.kb_hi - V.kb_lo);
+                        // (the producer issues all n k-blocks of the next unit, so the target is reached)
+                        const uint32_t target = it_next + min(n, STAGES + c * n / C::EPI_CHUNKS);
+                        if (lane == 0 && *progress < target) {
+                            const uint64_t t0 = ptx::globaltimer_ns();
+                            while (*progress < target && !*abort_flag && ptx::globaltimer_ns() - t0 < p.timeout_ns) {
+                            }
+                        }
+                        __syncwarp();
+                    });
+                if (flag && U.piece + 1 < p.sk_pieces) {
+                    // hand these rows to the next piece once every write to them has landed
+                    __threadfence();   // the ragged-edge chunk's element writes, from every lane
+                    __syncwarp();
+                    // (test hook: the first piece of split tile 0 never hands over)
+                    const bool held = p.debug_sk_stall && U.sk_index == 0 && U.piece == 0;
+                    if (lane == 0) {
+                        ptx::bulk_wait<0>();               // this warp's stores/reductions completed
+                        ptx::fence_proxy_async_global();   // ... and ordered before the release
+                        if (!held) ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
+                    }
+                    __syncwarp();
+                }
             }
         }
         if (lane == 0) ptx::bulk_wait<0>();

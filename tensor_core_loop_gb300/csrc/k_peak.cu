@@ -18,7 +18,11 @@ constexpr int kPeakRequest = 232448 - 1024;
 
 // flags: bit 0 — chain every MMA into one accumulator (as a GEMM tile does)
 //        instead of alternating two; bit 1 — walk the operand addresses like a
-//        GEMM k-loop (4 k-slices × 4 stages) instead of reusing one k-slice.
+//        GEMM k-loop (4 k-slices × 4 stages) instead of reusing one k-slice;
+//        bit 3 — per group of MMAs, what a GEMM k-block adds (a stage-barrier
+//        wait, a fence and a commit); bit 4 — of that, the wait and fence only;
+//        bit 5 — the commit only; bit 6 — groups of eight MMAs (two k-blocks)
+//        instead of four.
 template <int N, bool TF32, bool B_MN>
 __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, unsigned long long timeout_ns,
                                                           unsigned long long* cycles, unsigned int* status) {
@@ -62,6 +66,8 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
         // BK = 64 rows (8 KB apart) instead of 16 rows (2 KB apart)
         const uint32_t b_lbo = (flags & 4) ? 8192u : 2048u;
         const uint64_t t0 = ptx::clock64();
+        const bool do_wait = flags & (8 | 16), do_commit = flags & (8 | 32);
+        const int group = (flags & 64) ? 8 : 4;
         for (int i = 0; i < iters; i += 4) {
             // four MMAs on the four k-slices of one stage (or on one k-slice)
             const int st = walk ? ((i / 4) % kPeakStages) : 0;
@@ -75,7 +81,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
                               : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
             }
             const uint32_t d = tmem + ((!chain && ((i / 4) & 1)) ? N : 0);
-            if ((flags & 8)) {
+            if (do_wait && i % group == 0) {
                 // the rest of a GEMM issue loop: wait on a (completed) stage barrier, fence
                 __all_sync(0xffffffffu, ptx::mbar_try_wait(ptx::smem_u32(bar + 1), 1));
                 ptx::tc_fence_after();
@@ -85,7 +91,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
                 ptx::mma_tf32_x4_elected(d, ad[0], bd[0], ad[1], bd[1], ad[2], bd[2], ad[3], bd[3], idesc, acc);
             else
                 ptx::mma_f16_x4_elected(d, ad[0], bd[0], ad[1], bd[1], ad[2], bd[2], ad[3], bd[3], idesc, acc);
-            if ((flags & 8)) ptx::mma_commit_elected(ptx::smem_u32(bar + 2));   // ... and commit the stage
+            if (do_commit && (i + 4) % group == 0) ptx::mma_commit_elected(ptx::smem_u32(bar + 2));   // ... and commit
         }
         ptx::mma_commit_elected(ptx::smem_u32(bar));
         bool done = false;
@@ -145,7 +151,7 @@ extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int
         (b_mn != 0 && b_mn != 1) || (in_kind == 1 && b_mn))
         return TCL_ERR_DIMS;
     static_assert(kPeakSmem <= kPeakRequest, "probe fits its shared memory request");
-    if (flags < 0 || flags > 15) return TCL_ERR_CONFIG;
+    if (flags < 0 || flags > 127 || ((flags & 64) && iters % 8)) return TCL_ERR_CONFIG;
     int dev = 0, sms = 0;
     unsigned int* status = nullptr;
     int st = device_context(&dev, &sms, &status);

@@ -103,8 +103,17 @@ def test_plan_without_device(L):
     assert p["cta_pair"] == 1 and p["bn"] == 256 and p["num_tiles"] == 32 * 16 and p["grid"] == 152
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 300, 520, 64, tcl.Config(max_ctas=152, cta_pair=2))
     assert p["cta_pair"] == 2 and p["num_tiles"] == 2 * 3 and p["grid"] == 12
-    with pytest.raises(tcl.TclError):   # exact-integer mode has no two-SM kernel
-        tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2))
+    # exact integers on two SMs: 256×128 tiles (a row's 128 int32 sums live in registers)
+    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2))
+    assert p["cta_pair"] == 2 and p["bn"] == 128 and p["num_tiles"] == 16 * 32 and p["grid"] == 152
+    assert p["sk_tiles"] == 0 and p["splits"] == 1
+    for bad in (tcl.Config(max_ctas=152, cta_pair=2, bn=256), tcl.Config(max_ctas=152, cluster_pairs=2),
+                tcl.Config(max_ctas=152, cta_pair=2, stream_k=2)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, bad)
+    for c in (cfg, tcl.Config(max_ctas=152, cta_pair=1)):
+        p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, c)
+        assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 32 * 32
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096, cfg)
     # 16 narrow tiles for 152 SMs: K is cut into 8 ranges of 8 k-blocks (split-K)
     assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 16

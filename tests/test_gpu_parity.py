@@ -506,13 +506,31 @@ def test_s8_padded(oracle_mod):
     assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 padded")
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("va,vb", [(127, 127), (-128, -128), (127, -128)])
-def test_s8_extremes_closed_form(va, vb):
+def test_s8_extremes_closed_form(va, vb, pair):
+    # |sum| = 2^26 at K = 4096: eight fp32 units of 512 products each, added as int32
     K = 4096
     a = torch.full((256, K), va, dtype=torch.int8, device=DEV)
     b = torch.full((K, 256), vb, dtype=torch.int8, device=DEV)
-    c = tcl.gemm(a, b)
+    c = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=pair))
     assert (c == va * vb * K).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 128, 64), (512, 384, 4096), (300, 200, 1100), (520, 390, 2064),
+                                   (1000, 700, 520)])
+def test_s8_pair_kernel_exact(oracle_mod, M, N, K):
+    # two SMs per 256×128 tile; K ranges that end inside a 512-deep unit and ragged M, N edges
+    a, b = inputs.s8_pair(M, N, K, seed=M + N, lda=up(K, 16), ldb=up(N, 16))
+    got = run(to_dev(a), to_dev(b), cfg=tcl.Config(cta_pair=2)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 pair {M}x{N}x{K}")
+
+
+def test_s8_pair_kernel_grid_smaller_than_tiles(oracle_mod):
+    # 4 pairs walk 3 × 8 tiles: each pair's accumulator units cycle through both TMEM buffers
+    a, b = inputs.s8_pair(768, 1024, 1536, seed=11, lda=1536, ldb=1024)
+    got = run(to_dev(a), to_dev(b), cfg=tcl.Config(cta_pair=2, max_ctas=8)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 pair, 4 pairs")
 
 
 # ------------------------------------------------------------- full-size workloads, sampled

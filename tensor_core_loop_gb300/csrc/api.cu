@@ -23,7 +23,7 @@ __device__ unsigned int g_status_word;
 // They only ever hold gen·8 + pieces done, gen being a per-device launch counter,
 // so they never need clearing between launches.
 constexpr int kMaxSkTiles = 128;
-__device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 4];
+__device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 8];
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
@@ -298,12 +298,13 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     int bn = cfg ? cfg->bn : 0;
     int pair = 0;
     // the two-SM kernel: bf16 or TF32 in, float out (256 or 224 wide), or the
-    // exact-integer mode (128 wide: int32 sums of a row's 128 columns in registers)
+    // exact-integer mode (256 wide with eight epilogue warps, or 128 wide with
+    // four: a thread keeps the int32 sums of one row over 128 columns)
     const bool pair_capable = prod == PROD_TMA && (ok != OutKind::S32 || ik == InKind::BF16);
-    const int pair_bn = ok == OutKind::S32 ? 128 : 256;
+    const int pair_bn = 256;
     if (want_pair == 2) {
         if (!pair_capable) return TCL_ERR_CONFIG;
-        if (ok == OutKind::S32 ? (bn != 0 && bn != 128) : (bn != 0 && bn != 256 && bn != 224))
+        if (ok == OutKind::S32 ? (bn != 0 && bn != 128 && bn != 256) : (bn != 0 && bn != 256 && bn != 224))
             return TCL_ERR_CONFIG;
         pair = 1;
     } else if (want_pair == 0 && pair_capable && ok != OutKind::S32 && bn == 0 && !(cfg && cfg->stages)) {
@@ -319,8 +320,9 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
     }
     const int want_sk = cfg ? cfg->stream_k : 0;
-    if (want_sk < 0 || want_sk > kMaxSkPieces || (want_sk > 1 && (!pair || ok != OutKind::F32)))
-        return TCL_ERR_CONFIG;
+    // stream-K pieces add into C: fp32 or int32 (a bf16 C would be rounded twice)
+    const bool sk_capable = ok == OutKind::F32 || ok == OutKind::S32;
+    if (want_sk < 0 || want_sk > kMaxSkPieces || (want_sk > 1 && (!pair || !sk_capable))) return TCL_ERR_CONFIG;
     // CTA pairs per cluster: 2 = two pairs on tiles stacked in M sharing B by multicast
     const int want_cp = cfg ? cfg->cluster_pairs : 0;
     if (want_cp < 0 || want_cp > 2 || (want_cp == 2 && (want_pair == 1 || ok == OutKind::S32)))
@@ -417,7 +419,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         pl->grid = cl * (pl->num_tiles < clusters ? pl->num_tiles : clusters);
         // Stream-K pieces wait on one another, so every pair of the grid must be
         // resident at once: the grid never exceeds the resident clusters here.
-        if (ok == OutKind::F32 && !(cfg && cfg->one_cta_per_tile)) {
+        if (sk_capable && !(cfg && cfg->one_cta_per_tile)) {
             const int st = stream_k_split(pl->num_tiles, pl->grid / cl, pl->num_kb, want_sk, &pl->sk_tiles,
                                           &pl->sk_pieces);
             if (st) return st;

@@ -263,7 +263,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // crosses a right edge N not on a 16-byte boundary would also write the
 // columns after N. That chunk is stored element by element from registers
 // instead (rows past M skipped), leaving every byte outside C untouched.
-template <int SLAB_BYTES, int OUT_ES, int SLOTS>
+// INT: the 4-byte values are int32 (an add is an integer add).
+template <int SLAB_BYTES, int OUT_ES, int SLOTS, bool INT = false>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
                                            const GemmParams& p, bool add = false) {
@@ -275,10 +276,12 @@ __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab
             const int n = p.N - col0;
             if constexpr (OUT_ES == 4) {
                 uint32_t* dst = static_cast<uint32_t*>(p.C) + row * p.ldc + col0;
-                if (add) {   // fp32: C += v, this warp being the only writer of these rows now
+                if (add) {   // C += v, this warp being the only writer of these rows now
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (i < n) dst[i] = __float_as_uint(__uint_as_float(dst[i]) + __uint_as_float(v[i]));
+                        if (i < n)
+                            dst[i] = INT ? dst[i] + v[i]
+                                         : __float_as_uint(__uint_as_float(dst[i]) + __uint_as_float(v[i]));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)

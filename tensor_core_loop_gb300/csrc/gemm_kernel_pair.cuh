@@ -60,7 +60,12 @@ struct PairCfg {
     static constexpr int EPI_CHUNKS = BN / EPI_COLS;
     static constexpr int SLAB_BYTES = 32 * 128;
     static constexpr int EPI_SLOTS = SLOTS_;          // staging slabs per epilogue warp (stores in flight)
-    static constexpr int STAGING_BYTES = 4 * EPI_SLOTS * SLAB_BYTES;
+    // Epilogue warps: four (one per TMEM lane quarter, each over all BN columns),
+    // or, for exact integers wider than 128 columns, eight: two per lane quarter,
+    // each keeping the int32 sums of its rows over half of the columns.
+    static constexpr int EPI_WARPS = (OK == OutKind::S32 && BN > 128) ? 8 : 4;
+    static constexpr int EPI_COLS_PER_WARP = BN / (EPI_WARPS / 4);
+    static constexpr int STAGING_BYTES = EPI_WARPS * EPI_SLOTS * SLAB_BYTES;
     static constexpr int ACC_STRIDE = 256;           // accumulator b starts at TMEM column b·256
     static constexpr int TMEM_COLS = 512;
     static constexpr int BAR_BYTES = 256;
@@ -68,15 +73,15 @@ struct PairCfg {
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t IDESC =
         ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;   // producer, MMA issuer, epilogue warps
     // ring slots released per commit, as in the one-SM kernel: each SM's share of a
     // pair k-block (128 rows × BN columns) keeps its tensor pipe as long as a
     // one-SM k-block of width BN
     static constexpr int REL = (BN <= 128 && STAGES >= 4 && STAGES % 2 == 0) ? 2 : 1;
     static __device__ __forceinline__ uint32_t rel_slot(uint32_t s) { return REL == 2 ? (s | 1u) : s; }
 
-    static_assert(OK != OutKind::S32 || (BN <= 128 && IK == InKind::BF16 && PAIRS == 1),
-                  "exact integer mode: int32 sums of BN <= 128 columns per thread in registers");
+    static_assert(OK != OutKind::S32 || (EPI_COLS_PER_WARP <= 128 && IK == InKind::BF16 && PAIRS == 1),
+                  "exact integer mode: int32 sums of at most 128 columns per thread in registers");
     static_assert(BN % 32 == 0 && BN <= 256 && BN % EPI_COLS == 0, "pair tile width");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(2 * STAGES + 5 <= 28, "barrier area");
@@ -200,7 +205,7 @@ __device__ __forceinline__ void spin_ns(unsigned long long ns) {
 }
 
 template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS, InKind IK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf0 + 8 * b, 1);    // the leader's multicast commit
-            ptx::mbar_init(acce0 + 8 * b, 8);    // leader's: 4 epilogue warps × 2 CTAs
+            ptx::mbar_init(acce0 + 8 * b, 2 * C::EPI_WARPS);   // leader's: every epilogue warp of both CTAs
         }
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -399,13 +404,38 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5), both CTAs
-        const int q = warp & 3;
+        // ------------------------------------------------ epilogue (warps 2.., both CTAs)
+        const int q = warp & 3;                                // TMEM lane quarter this warp may read
+        [[maybe_unused]] const int h = (warp - 2) / 4;         // column part (exact integers, 8 warps)
+        constexpr int CW = C::EPI_COLS_PER_WARP;
         uint8_t* slab_pair = staging + (warp - 2) * C::EPI_SLOTS * C::SLAB_BYTES;
         int store_count = 0;
         uint32_t unit = 0;
         uint32_t it_next = 0;   // the ring iteration at which the unit after this one starts
         bool ok = true;
+        // stream-K: this warp's rows of split tile (d, pidx), flags[d][pidx][rank][epilogue warp]
+        auto sk_flag = [&](const PairUnit& U) -> uint32_t* {
+            return U.sk_index >= 0 ? p.sk_flags + ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + rank) *
+                                                      C::EPI_WARPS + (warp - 2)
+                                   : nullptr;
+        };
+        auto wait_turn = [&](uint32_t* flag, const PairUnit& U) {   // piece > 0: the previous piece is in C
+            return wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
+                                p.timeout_ns, p.status);
+        };
+        auto hand_over = [&](uint32_t* flag, const PairUnit& U) {
+            // hand these rows to the next piece once every write to them has landed
+            __threadfence();   // the ragged-edge chunk's element writes, from every lane
+            __syncwarp();
+            // (test hook: the first piece of split tile 0 never hands over)
+            const bool held = p.debug_sk_stall && U.sk_index == 0 && U.piece == 0;
+            if (lane == 0) {
+                ptx::bulk_wait<0>();               // this warp's stores/reductions completed
+                ptx::fence_proxy_async_global();   // ... and ordered before the release
+                if (!held) ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
+            }
+            __syncwarp();
+        };
         const int units = pair_units(p, cluster, clusters);
         for (int u = 0; ok && u < units; ++u) {
             const PairUnit U = pair_unit(p, cluster, clusters, u);
@@ -414,10 +444,10 @@ __global__ void __launch_bounds__(192, 1)
             tile_coords(U.tile, p, mb, nb);
             mb = mb * PAIRS + static_cast<int>(pidx);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
-            [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? BN : 1];
+            [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? CW : 1];
             if constexpr (OK == OutKind::S32) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) iacc[i] = 0;
+                for (int i = 0; i < CW; ++i) iacc[i] = 0;
             }
             for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
                 const uint32_t buf = unit & 1u;
@@ -435,36 +465,41 @@ __global__ void __launch_bounds__(192, 1)
                     // exact integers: this unit's fp32 sums (each an integer below 2^24 in
                     // magnitude) converted and added into int32 registers; the tile's int32
                     // result is stored after its last unit
-                    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
+                    const uint32_t tb =
+                        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE + h * CW;
+                    // (16 columns at a time: the 128 sums already hold most of a thread's registers)
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 0; c < CW / 16; ++c) {
                         __syncwarp();   // tcgen05.ld is warp-collective
-                        uint32_t r[32];
-                        ptx::tmem_ld_32x32b_x32(tb + c * 32, r);
+                        uint32_t r[16];
+                        ptx::tmem_ld_32x32b_x16(tb + c * 16, r);
                         ptx::tmem_ld_wait(r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) iacc[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                        for (int i = 0; i < 16; ++i) iacc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
                     }
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive_cluster(acce_leader0 + 8 * buf);
                     if (kb0 + p.kb_per_unit >= U.kb_hi) {
-#pragma unroll
-                        for (int c = 0; c < BN / 32; ++c) {
-                            const uint32_t(&v)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&iacc[c * 32]);
-                            store_slab<C::SLAB_BYTES, 4, C::EPI_SLOTS>(&tmC, slab_pair, store_count, v, lane,
-                                                                       nb * C::BN + c * 32, row0, p);
+                        // a stream-K piece after the first adds its sums into C (integer reduction)
+                        uint32_t* flag = sk_flag(U);
+                        if (flag && U.piece > 0 && !wait_turn(flag, U)) {
+                            ok = false;
+                            break;
                         }
+#pragma unroll
+                        for (int c = 0; c < CW / 32; ++c) {
+                            const uint32_t(&v)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&iacc[c * 32]);
+                            store_slab<C::SLAB_BYTES, 4, C::EPI_SLOTS, true>(
+                                &tmC, slab_pair, store_count, v, lane, nb * C::BN + h * CW + c * 32, row0, p,
+                                U.piece > 0);
+                        }
+                        if (flag && U.piece + 1 < p.sk_pieces) hand_over(flag, U);
                     }
                     continue;
                 }
-                // stream-K: this warp's rows of split tile (d, pidx), flags[d][pidx][rank][q]
-                uint32_t* flag =
-                    U.sk_index >= 0 ? p.sk_flags + ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + rank) * 4 + q
-                                    : nullptr;
-                if (flag && U.piece > 0 &&
-                    !wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
-                                  p.timeout_ns, p.status)) {
+                uint32_t* flag = sk_flag(U);
+                if (flag && U.piece > 0 && !wait_turn(flag, U)) {
                     ok = false;
                     break;
                 }
@@ -494,19 +529,7 @@ __global__ void __launch_bounds__(192, 1)
                         }
                         __syncwarp();
                     });
-                if (flag && U.piece + 1 < p.sk_pieces) {
-                    // hand these rows to the next piece once every write to them has landed
-                    __threadfence();   // the ragged-edge chunk's element writes, from every lane
-                    __syncwarp();
-                    // (test hook: the first piece of split tile 0 never hands over)
-                    const bool held = p.debug_sk_stall && U.sk_index == 0 && U.piece == 0;
-                    if (lane == 0) {
-                        ptx::bulk_wait<0>();               // this warp's stores/reductions completed
-                        ptx::fence_proxy_async_global();   // ... and ordered before the release
-                        if (!held) ptx::st_release_gpu(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece + 1));
-                    }
-                    __syncwarp();
-                }
+                if (flag && U.piece + 1 < p.sk_pieces) hand_over(flag, U);
             }
         }
         if (lane == 0) ptx::bulk_wait<0>();

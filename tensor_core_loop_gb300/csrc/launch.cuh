@@ -128,7 +128,8 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     X(BF16, F32, 256, 6, 2, 1) X(BF16, F32, 256, 4, 2, 1) X(BF16, BF16, 256, 6, 2, 1)                        \
     X(BF16, F32, 224, 6, 2, 1) X(BF16, F32, 224, 5, 4, 1) X(BF16, BF16, 256, 5, 4, 1)                        \
     X(BF16, F32, 256, 6, 2, 2) X(BF16, F32, 224, 6, 2, 2) X(BF16, BF16, 256, 6, 2, 2)                        \
-    X(TF32, F32, 256, 6, 2, 1) X(TF32, F32, 224, 6, 2, 1) X(BF16, S32, 128, 8, 2, 1)
+    X(TF32, F32, 256, 6, 2, 1) X(TF32, F32, 224, 6, 2, 1) X(BF16, S32, 128, 8, 2, 1)                         \
+    X(BF16, S32, 256, 6, 1, 1)
 #define TCL_PAIR_INFO(IK, OK, BN, ST, SL, PR)                                                               \
     {InKind::IK, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL, PR, InKind::IK>::SMEM_BYTES,      \
      PairCfg<OutKind::OK, BN, ST, SL, PR, InKind::IK>::THREADS, PR, SL},

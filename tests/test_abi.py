@@ -105,10 +105,12 @@ def test_plan_without_device(L):
     assert p["cta_pair"] == 2 and p["num_tiles"] == 2 * 3 and p["grid"] == 12
     # exact integers on two SMs: 256×128 tiles (a row's 128 int32 sums live in registers)
     p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2))
-    assert p["cta_pair"] == 2 and p["bn"] == 128 and p["num_tiles"] == 16 * 32 and p["grid"] == 152
-    assert p["sk_tiles"] == 0 and p["splits"] == 1
-    for bad in (tcl.Config(max_ctas=152, cta_pair=2, bn=256), tcl.Config(max_ctas=152, cluster_pairs=2),
-                tcl.Config(max_ctas=152, cta_pair=2, stream_k=2)):
+    assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16 and p["grid"] == 152
+    assert (p["sk_tiles"], p["sk_pieces"], p["splits"]) == (28, 2, 1)   # int32 pieces add exactly
+    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2, bn=128))
+    assert p["cta_pair"] == 2 and p["bn"] == 128 and p["num_tiles"] == 16 * 32
+    for bad in (tcl.Config(max_ctas=152, cta_pair=2, bn=224), tcl.Config(max_ctas=152, cluster_pairs=2),
+                tcl.Config(max_ctas=152, cta_pair=1, stream_k=2)):
         with pytest.raises(tcl.TclError):
             tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, bad)
     for c in (cfg, tcl.Config(max_ctas=152, cta_pair=1)):

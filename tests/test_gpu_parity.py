@@ -506,31 +506,56 @@ def test_s8_padded(oracle_mod):
     assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 padded")
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair,bn,sk", [(1, 0, 1), (2, 128, 1), (2, 256, 1), (2, 256, 3)])
 @pytest.mark.parametrize("va,vb", [(127, 127), (-128, -128), (127, -128)])
-def test_s8_extremes_closed_form(va, vb, pair):
+def test_s8_extremes_closed_form(va, vb, pair, bn, sk):
     # |sum| = 2^26 at K = 4096: eight fp32 units of 512 products each, added as int32
+    # (sk = 3: 1280 columns of 256 on four pairs, the 5th tile in three K pieces)
     K = 4096
     a = torch.full((256, K), va, dtype=torch.int8, device=DEV)
-    b = torch.full((K, 256), vb, dtype=torch.int8, device=DEV)
-    c = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=pair))
+    b = torch.full((K, 1280 if sk > 1 else 512), vb, dtype=torch.int8, device=DEV)
+    cfg = tcl.Config(cta_pair=pair, bn=bn, stream_k=sk, max_ctas=8 if sk > 1 else 0)
+    c = tcl.gemm(a, b, cfg=cfg)
     assert (c == va * vb * K).all()
 
 
+@pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("M,N,K", [(256, 128, 64), (512, 384, 4096), (300, 200, 1100), (520, 390, 2064),
                                    (1000, 700, 520)])
-def test_s8_pair_kernel_exact(oracle_mod, M, N, K):
-    # two SMs per 256×128 tile; K ranges that end inside a 512-deep unit and ragged M, N edges
+def test_s8_pair_kernel_exact(oracle_mod, M, N, K, bn):
+    # two SMs per 256×bn tile (bn = 256: eight epilogue warps, two per TMEM lane quarter);
+    # K ranges that end inside a 512-deep unit and ragged M, N edges
     a, b = inputs.s8_pair(M, N, K, seed=M + N, lda=up(K, 16), ldb=up(N, 16))
-    got = run(to_dev(a), to_dev(b), cfg=tcl.Config(cta_pair=2)).numpy()
-    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 pair {M}x{N}x{K}")
+    got = run(to_dev(a), to_dev(b), cfg=tcl.Config(cta_pair=2, bn=bn)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 pair {M}x{N}x{K} bn {bn}")
 
 
-def test_s8_pair_kernel_grid_smaller_than_tiles(oracle_mod):
-    # 4 pairs walk 3 × 8 tiles: each pair's accumulator units cycle through both TMEM buffers
+@pytest.mark.parametrize("bn,M,N,K,pieces", [
+    (256, 768, 768, 2048, 0),    # 9 tiles on 4 pairs: the 9th in 4 pieces of 8 k-blocks (one unit each)
+    (256, 768, 768, 2048, 3),    # pieces of 10, 11, 11 k-blocks: units end inside a piece
+    (256, 700, 750, 1000, 4),    # ragged M, N (the last chunk added element by element), K tail in the last piece
+    (256, 512, 1280, 4160, 2),   # pieces of 32 and 33 k-blocks, units of 8 and a ragged last one
+    (128, 768, 768, 2048, 0),    # 18 tiles on 4 pairs: two tail tiles in 2 pieces each
+    (128, 700, 750, 1000, 2),
+    (128, 512, 1152, 4160, 2),
+])
+def test_s8_pair_stream_k_exact(oracle_mod, M, N, K, pieces, bn):
+    # the last partial wave of tiles in K pieces; later pieces add their int32 sums into C
+    cfg = tcl.Config(cta_pair=2, bn=bn, max_ctas=8, stream_k=pieces)
+    pl = tcl.plan(tcl.IN_S8, 0, M, N, K, cfg)
+    assert pl["sk_tiles"] > 0 and pl["sk_pieces"] >= 2
+    a, b = inputs.s8_pair(M, N, K, seed=K + pieces, lda=up(K, 16), ldb=up(N, 16))
+    got = run(to_dev(a), to_dev(b), cfg=cfg).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 stream-K {M}x{N}x{K} bn {bn}")
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_s8_pair_kernel_grid_smaller_than_tiles(oracle_mod, bn):
+    # 4 pairs walk more tiles than they are: each pair's accumulator units cycle through both
+    # TMEM buffers and its epilogue stores several tiles
     a, b = inputs.s8_pair(768, 1024, 1536, seed=11, lda=1536, ldb=1024)
-    got = run(to_dev(a), to_dev(b), cfg=tcl.Config(cta_pair=2, max_ctas=8)).numpy()
-    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 pair, 4 pairs")
+    got = run(to_dev(a), to_dev(b), cfg=tcl.Config(cta_pair=2, bn=bn, max_ctas=8)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 pair bn {bn}, 4 pairs")
 
 
 # ------------------------------------------------------------- full-size workloads, sampled

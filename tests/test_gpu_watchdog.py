@@ -81,6 +81,23 @@ def test_stream_k_order_wait_runs_out():
     assert tcl.last_device_error() == (0, 0)
 
 
+def test_stream_k_order_wait_runs_out_int8():
+    # the same hold in the exact-integer epilogue (eight warps per CTA, int32 pieces)
+    a = torch.randint(-128, 128, (768, 2048), dtype=torch.int8, generator=torch.Generator().manual_seed(8)).to(DEV)
+    b = torch.randint(-128, 128, (2048, 768), dtype=torch.int8, generator=torch.Generator().manual_seed(9)).to(DEV)
+    c = torch.zeros((768, 768), dtype=torch.int32, device=DEV)
+    base = dict(cta_pair=2, bn=256, max_ctas=8, stream_k=2)
+    assert tcl.plan(tcl.IN_S8, 0, 768, 768, 2048, tcl.Config(**base))["sk_tiles"] == 1
+    tcl.gemm_into(a, b, c, cfg=tcl.Config(timeout_ns=50_000_000, debug_stream_k_stall=1, **base))
+    st, code = tcl.last_device_error()
+    assert (st, code) == (7, 5), (st, code)
+    x = tcl.gemm(a, b, cfg=tcl.Config(**base))
+    y = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=1))
+    torch.cuda.synchronize()
+    assert torch.equal(x, y)
+    assert tcl.last_device_error() == (0, 0)
+
+
 @pytest.mark.parametrize("pair", [1, 2])
 def test_trace_shows_loads_ahead_of_mma(pair):
     """The per-k-block timeline of CTA 0: each block's load is issued before its

@@ -28,7 +28,9 @@ __device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 8];
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
 constexpr int kBM = 128;
-constexpr int kS32UnitK = 512;   // K values per exact fp32 unit: 512·2^14 = 2^23 < 2^24
+// K values per exact fp32 unit: |partial| <= 256·2^14 = 2^22, the range in which the
+// epilogue turns an fp32 sum into an int32 with one add (exact_int)
+constexpr int kS32UnitK = 256;
 
 struct DevState {
     bool probed = false;
@@ -307,10 +309,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         if (ok == OutKind::S32 ? (bn != 0 && bn != 128 && bn != 256) : (bn != 0 && bn != 256 && bn != 224))
             return TCL_ERR_CONFIG;
         pair = 1;
-    } else if (want_pair == 0 && pair_capable && ok != OutKind::S32 && bn == 0 && !(cfg && cfg->stages)) {
-        // (exact-integer tiles stay on one SM unless asked: 128-wide pair tiles
-        // measured slower on GB300, 161.5 vs 139.6 us at 4096^3, both bound by
-        // operand delivery into shared memory)
+    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages)) {
         // Two SMs per 256-row tile halve each SM's bytes per flop; use them when
         // there are at least as many pair tiles as pairs of SMs and a tile has
         // enough k-blocks for its mainloop to outlast its epilogue (measured on

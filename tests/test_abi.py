@@ -104,18 +104,18 @@ def test_plan_without_device(L):
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 300, 520, 64, tcl.Config(max_ctas=152, cta_pair=2))
     assert p["cta_pair"] == 2 and p["num_tiles"] == 2 * 3 and p["grid"] == 12
     # exact integers on two SMs: 256×128 tiles (a row's 128 int32 sums live in registers)
-    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2))
-    assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16 and p["grid"] == 152
-    assert (p["sk_tiles"], p["sk_pieces"], p["splits"]) == (28, 2, 1)   # int32 pieces add exactly
+    for c in (cfg, tcl.Config(max_ctas=152, cta_pair=2)):
+        p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, c)
+        assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16 and p["grid"] == 152
+        assert (p["sk_tiles"], p["sk_pieces"], p["splits"]) == (28, 2, 1)   # int32 pieces add exactly
     p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2, bn=128))
     assert p["cta_pair"] == 2 and p["bn"] == 128 and p["num_tiles"] == 16 * 32
     for bad in (tcl.Config(max_ctas=152, cta_pair=2, bn=224), tcl.Config(max_ctas=152, cluster_pairs=2),
                 tcl.Config(max_ctas=152, cta_pair=1, stream_k=2)):
         with pytest.raises(tcl.TclError):
             tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, bad)
-    for c in (cfg, tcl.Config(max_ctas=152, cta_pair=1)):
-        p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, c)
-        assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 32 * 32
+    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=1))
+    assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 32 * 32
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096, cfg)
     # 16 narrow tiles for 152 SMs: K is cut into 8 ranges of 8 k-blocks (split-K)
     assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 16
@@ -134,8 +134,8 @@ def test_plan_without_device(L):
     with pytest.raises(tcl.TclError):
         tcl.plan(tcl.IN_S8, 0, 512, 512, 4096, tcl.Config(max_ctas=152, split_k=2))
     assert tcl.plan(tcl.IN_S8, 0, 512, 512, 4096, cfg)["splits"] == 1   # exact integers: never split
-    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, cfg)
-    assert p["bn"] == 128
+    p = tcl.plan(tcl.IN_S8, 0, 512, 512, 4096, cfg)   # too few 256-row tiles for the pair kernel
+    assert p["bn"] == 128 and p["cta_pair"] == 1
     p = tcl.plan(tcl.IN_TF32, 0, 300, 70, 9, cfg)
     assert p["num_tiles"] == 3 * 1
     cfg2 = tcl.Config(max_ctas=152, bn=256, stages=2, one_cta_per_tile=1)

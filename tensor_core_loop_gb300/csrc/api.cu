@@ -716,8 +716,8 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
     uint8_t* b2 = a2 + a_bytes;
     int32_t* c2 = pack_c ? reinterpret_cast<int32_t*>(b2 + b_bytes) : nullptr;
-    if (launch_s8_to_bf16(A, lda, a2, lda2, M, K, ds->sms, stream) != cudaSuccess ||
-        launch_s8_to_bf16(B, ldb, b2, ldb2, K, N, ds->sms, stream) != cudaSuccess) {
+    if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
+                          {B, ldb, reinterpret_cast<uint16_t*>(b2), ldb2, K, N, 0}, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }

@@ -9,11 +9,13 @@
 // int8 -> bf16:
 // Every int8 value (|x| <= 128) has at most 8 significant bits, so it is
 // represented exactly by bf16; the bf16 pattern is the upper half of the
-// binary32 encoding of the integer. Rows are processed in 16-element chunks:
-// one 16-byte load, two 16-byte stores. The destination rows are padded to a
-// multiple of 8 elements (the padding is written as zeros). When the source
-// base and leading dimension are 16-byte aligned (`vec`), full chunks use
-// vector loads; otherwise, and at a ragged row tail, bytes are read one by one.
+// binary32 encoding of the integer. Both operands are widened by one launch;
+// a block takes one row at a time (rows of A, then rows of B) and its threads
+// the row's 16-element chunks: one 16-byte load, two 16-byte stores. The
+// destination rows are padded to a multiple of 8 elements (the padding is
+// written as zeros). When the source base and leading dimension are 16-byte
+// aligned (`vec`), full chunks use vector loads; otherwise, and at a ragged row
+// tail, bytes are read one by one.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -22,67 +24,70 @@
 
 namespace tcl {
 
-__device__ __forceinline__ uint32_t s8_pair_to_bf16x2(int lo, int hi) {
-    const uint32_t l = __float_as_uint(static_cast<float>(lo)) >> 16;
-    const uint32_t h = __float_as_uint(static_cast<float>(hi)) & 0xFFFF0000u;
-    return l | h;
+// The binary32 value of an integer |x| <= 128 without a conversion instruction:
+// 1.5·2^23 + x is exact in [2^23, 2^24) (unit in the last place 1), so its bit
+// pattern is that of 1.5·2^23 plus x, and subtracting 1.5·2^23 leaves x exactly.
+__device__ __forceinline__ uint32_t s8_f32_bits(int x) {
+    return __float_as_uint(__int_as_float(0x4B400000 + x) - 12582912.0f);
 }
 
-__global__ void __launch_bounds__(256) s8_to_bf16_kernel(const int8_t* __restrict__ src,
-                                                          long long ld_src,
-                                                          uint16_t* __restrict__ dst,
-                                                          long long ld_dst, int rows, int cols, int vec) {
-    const int chunks_per_row = (cols + 15) / 16;
-    const long long total = static_cast<long long>(rows) * chunks_per_row;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int r = static_cast<int>(idx / chunks_per_row);
-        const int c0 = static_cast<int>(idx - static_cast<long long>(r) * chunks_per_row) * 16;
-        const int8_t* s = src + r * ld_src + c0;
-        uint16_t* d = dst + r * ld_dst + c0;
-        if (c0 + 16 <= cols) {
-            int4 raw;
-            if (vec) {
-                raw = *reinterpret_cast<const int4*>(s);
-            } else {
-                int8_t* rb = reinterpret_cast<int8_t*>(&raw);
+__device__ __forceinline__ uint32_t s8_pair_to_bf16x2(int lo, int hi) {
+    return (s8_f32_bits(lo) >> 16) | (s8_f32_bits(hi) & 0xFFFF0000u);
+}
+
+__global__ void __launch_bounds__(256) s8_to_bf16_kernel(S8Widen a, S8Widen b) {
+    const long long total = static_cast<long long>(a.rows) + b.rows;
+    for (long long rr = blockIdx.x; rr < total; rr += gridDim.x) {
+        const bool in_a = rr < a.rows;
+        const S8Widen& job = in_a ? a : b;
+        const long long r = in_a ? rr : rr - a.rows;
+        const int cols = job.cols;
+        const int chunks_per_row = (cols + 15) / 16;
+        for (int ch = threadIdx.x; ch < chunks_per_row; ch += blockDim.x) {
+            const int c0 = ch * 16;
+            const int8_t* s = job.src + r * job.ld_src + c0;
+            uint16_t* d = job.dst + r * job.ld_dst + c0;
+            if (c0 + 16 <= cols) {
+                int4 raw;
+                if (job.vec) {
+                    raw = *reinterpret_cast<const int4*>(s);
+                } else {
+                    int8_t* rb = reinterpret_cast<int8_t*>(&raw);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) rb[j] = s[j];
+                    for (int j = 0; j < 16; ++j) rb[j] = s[j];
+                }
+                const int8_t* v = reinterpret_cast<const int8_t*>(&raw);
+                uint4 o0, o1;
+                o0.x = s8_pair_to_bf16x2(v[0], v[1]);
+                o0.y = s8_pair_to_bf16x2(v[2], v[3]);
+                o0.z = s8_pair_to_bf16x2(v[4], v[5]);
+                o0.w = s8_pair_to_bf16x2(v[6], v[7]);
+                o1.x = s8_pair_to_bf16x2(v[8], v[9]);
+                o1.y = s8_pair_to_bf16x2(v[10], v[11]);
+                o1.z = s8_pair_to_bf16x2(v[12], v[13]);
+                o1.w = s8_pair_to_bf16x2(v[14], v[15]);
+                reinterpret_cast<uint4*>(d)[0] = o0;
+                reinterpret_cast<uint4*>(d)[1] = o1;
+            } else {
+                // ragged row end: convert what is there and zero the padding up to ld_dst,
+                // so that tensor loads that round the row end up to 16 bytes read zeros
+                int j = 0;
+                for (; c0 + j < cols; ++j) d[j] = static_cast<uint16_t>(s8_f32_bits(s[j]) >> 16);
+                for (; c0 + j < job.ld_dst && j < 16; ++j) d[j] = 0;
             }
-            const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
-            uint4 o0, o1;
-            o0.x = s8_pair_to_bf16x2(b[0], b[1]);
-            o0.y = s8_pair_to_bf16x2(b[2], b[3]);
-            o0.z = s8_pair_to_bf16x2(b[4], b[5]);
-            o0.w = s8_pair_to_bf16x2(b[6], b[7]);
-            o1.x = s8_pair_to_bf16x2(b[8], b[9]);
-            o1.y = s8_pair_to_bf16x2(b[10], b[11]);
-            o1.z = s8_pair_to_bf16x2(b[12], b[13]);
-            o1.w = s8_pair_to_bf16x2(b[14], b[15]);
-            reinterpret_cast<uint4*>(d)[0] = o0;
-            reinterpret_cast<uint4*>(d)[1] = o1;
-        } else {
-            // ragged row end: convert what is there and zero the padding up to ld_dst,
-            // so that tensor loads that round the row end up to 16 bytes read zeros
-            int j = 0;
-            for (; c0 + j < cols; ++j)
-                d[j] = static_cast<uint16_t>(__float_as_uint(static_cast<float>(s[j])) >> 16);
-            for (; c0 + j < ld_dst && j < 16; ++j) d[j] = 0;
         }
     }
 }
 
-cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, long long ld_dst,
-                              int rows, int cols, int sms, cudaStream_t stream) {
-    const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && ld_src % 16 == 0) ? 1 : 0;
-    const long long chunks = static_cast<long long>(rows) * ((cols + 15) / 16);
-    const int threads = 256;
-    long long blocks = (chunks + threads - 1) / threads;
-    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks per SM, grid-stride beyond
+cudaError_t launch_s8_to_bf16(S8Widen a, S8Widen b, int sms, cudaStream_t stream) {
+    a.vec = (reinterpret_cast<uintptr_t>(a.src) % 16 == 0 && a.ld_src % 16 == 0) ? 1 : 0;
+    b.vec = (reinterpret_cast<uintptr_t>(b.src) % 16 == 0 && b.ld_src % 16 == 0) ? 1 : 0;
+    const long long rows = static_cast<long long>(a.rows) + b.rows;
+    long long blocks = rows;
+    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks per SM, row-stride beyond
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        src, ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols, vec);
+    s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, b);
     return cudaGetLastError();
 }
 

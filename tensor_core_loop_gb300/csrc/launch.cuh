@@ -37,10 +37,18 @@ cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
 int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots, int pairs);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
-// int8 -> bf16 widening (exact) into a packed row-major buffer with ld_dst
-// columns per row; columns past `cols` are left untouched.
-cudaError_t launch_s8_to_bf16(const int8_t* src, long long ld_src, void* dst, long long ld_dst,
-                              int rows, int cols, int sms, cudaStream_t stream);
+// int8 -> bf16 widening (exact) of two matrices in one launch: rows × cols of
+// src (leading dimension ld_src) into a packed row-major buffer dst with ld_dst
+// columns per row, the columns from `cols` up to the next multiple of 16 below
+// ld_dst written as zeros; `vec` is set by the launcher.
+struct S8Widen {
+    const int8_t* src;
+    long long ld_src;
+    uint16_t* dst;
+    long long ld_dst;
+    int rows, cols, vec;
+};
+cudaError_t launch_s8_to_bf16(S8Widen a, S8Widen b, int sms, cudaStream_t stream);
 
 // C (M×N, fp32 or bf16 rounded to nearest even) = sum over s = 0..splits-1, in
 // that order, of the fp32 partial tiles W[s·rows_per_split + i][j] (leading dimension ldw).

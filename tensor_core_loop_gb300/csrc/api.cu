@@ -28,9 +28,11 @@ __device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 8];
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
 constexpr int kBM = 128;
-// K values per exact fp32 unit: |partial| <= 256·2^14 = 2^22, the range in which the
-// epilogue turns an fp32 sum into an int32 with one add (exact_int)
-constexpr int kS32UnitK = 256;
+// K values per exact fp32 unit: every partial sum is an integer of magnitude at most
+// 512·2^14 = 2^23 < 2^24, so the fp32 accumulation and its conversion are exact.
+// (Measured on GB300: 512-K units beat 256-K units converted with a cheaper add,
+// 103 vs 108 us at int8 4096^3: the unit turnover costs more than the conversion.)
+constexpr int kS32UnitK = 512;
 
 struct DevState {
     bool probed = false;

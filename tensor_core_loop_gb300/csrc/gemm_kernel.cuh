@@ -263,16 +263,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // crosses a right edge N not on a 16-byte boundary would also write the
 // columns after N. That chunk is stored element by element from registers
 // instead (rows past M skipped), leaving every byte outside C untouched.
-// An fp32 accumulator that holds an integer of magnitude at most 2^22, as an
-// int32. Adding 1.5·2^23 moves it, exactly, into [2^23, 2^24] where the unit in
-// the last place is 1, so the sum's bit pattern minus that of 1.5·2^23 is the
-// integer (at -2^22 and 2^22 the sum is 2^23 or 2^24, whose patterns still
-// differ from it by exactly 2^22). One FADD and one integer add, where a
-// float-to-integer conversion instruction would run at a fraction of the rate.
-__device__ __forceinline__ int32_t exact_int(uint32_t bits) {
-    return static_cast<int32_t>(__float_as_uint(__uint_as_float(bits) + 12582912.0f)) - 0x4B400000;
-}
-
 // INT: the 4-byte values are int32 (an add is an integer add).
 template <int SLAB_BYTES, int OUT_ES, int SLOTS, bool INT = false>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
@@ -759,7 +749,7 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                         ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
                         ptx::tmem_ld_wait(r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) iacc[c * 32 + i] += exact_int(r[i]);
+                        for (int i = 0; i < 32; ++i) iacc[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
                     }
                     ptx::tc_fence_before();
                     __syncwarp();

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
             const int units = pair_units(p, cluster, clusters);
             for (int u = 0; ok && u < units; ++u) {
                 const PairUnit U = pair_unit(p, cluster, clusters, u);
-                // accumulation units of kb_per_unit k-blocks (exact-integer mode: 256 K
+                // accumulation units of kb_per_unit k-blocks (exact-integer mode: 512 K
                 // values, drained into int32 sums; otherwise the whole range)
                 for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
                     const int kb1 = min(kb0 + p.kb_per_unit, U.kb_hi);
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                         ptx::tmem_ld_32x32b_x16(tb + c * 16, r);
                         ptx::tmem_ld_wait(r);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) iacc[c * 16 + i] += exact_int(r[i]);
+                        for (int i = 0; i < 16; ++i) iacc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
                     }
                     ptx::tc_fence_before();
                     __syncwarp();

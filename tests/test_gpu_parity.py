@@ -509,8 +509,8 @@ def test_s8_padded(oracle_mod):
 @pytest.mark.parametrize("pair,bn,sk", [(1, 0, 1), (2, 128, 1), (2, 256, 1), (2, 256, 3)])
 @pytest.mark.parametrize("va,vb", [(127, 127), (-128, -128), (127, -128)])
 def test_s8_extremes_closed_form(va, vb, pair, bn, sk):
-    # |sum| = 2^26 at K = 4096: sixteen fp32 units of 256 products each, added as int32;
-    # (-128)·(-128) makes every unit's sum exactly 2^22, the end of the exact conversion's range
+    # |sum| = 2^26 at K = 4096: eight fp32 units of 512 products each (2^23 apiece for
+    # (-128)·(-128)), added as int32
     # (sk = 3: 1280 columns of 256 on four pairs, the 5th tile in three K pieces)
     K = 4096
     a = torch.full((256, K), va, dtype=torch.int8, device=DEV)

@@ -19,15 +19,26 @@
  *   the caller). The library keeps a per-device cache of TMA descriptors and
  *   a per-device scratch buffer (repacked operands for gemm_s8 and gemm_tf32,
  *   copies of operands or outputs off the 16-byte grid, split-K partial
- *   tiles for small grids) that it grows on demand
- *   (cudaMalloc, after a device synchronisation) and frees in tcl_shutdown().
- *   Every call on a device shares that buffer: calls whose GPU work could
- *   overlap (different streams without ordering) must not both need it.
+ *   tiles for small grids) that it grows on demand (cudaMalloc, at least
+ *   doubling; an outgrown buffer is kept, since enqueued or graph-captured
+ *   work may still use it) and frees, with the outgrown ones, in
+ *   tcl_shutdown(). Every call on a device shares that buffer: calls whose
+ *   GPU work could overlap (different streams without ordering) must not both
+ *   need it.
  *
  * Streams: every call is asynchronous on `stream` (0 = legacy default
  *   stream) and returns once the work is enqueued. Calls on one stream run in
  *   order. The library is not thread-safe: serialise calls from several host
  *   threads.
+ *
+ * CUDA graphs: the device-pointer entry points may be captured into a graph
+ *   and replayed. A captured call bakes in its TMA descriptors and scratch
+ *   addresses, so the caller keeps A, B and C where they were; scratch is
+ *   never freed before tcl_shutdown(), and a call that would have to grow it
+ *   during capture returns TCL_ERR_CAPTURE (run the call once before
+ *   capturing). Stream-K progress flags are left at zero by each launch that
+ *   completes, so a replay (same flag generation) orders its pieces again; a
+ *   replay after a launch that reported TCL_ERR_DEVICE_TIMEOUT is not safe.
  *
  * Alignment. Pointers must be aligned to their element size (bf16: 2
  *   bytes; fp32, int32: 4 bytes; int8: none), else TCL_ERR_ALIGN. The fast
@@ -85,8 +96,11 @@ typedef enum {
     TCL_ERR_CONFIG = 8,          /* tcl_config_t asks for a variant that is not built */
     TCL_ERR_NO_MEMORY = 9,       /* scratch allocation failed */
     TCL_ERR_DEVICE = 10,         /* current device is not an sm_103 GPU */
-    TCL_ERR_STATIC_LIMIT = 11    /* gemm_s8_static: the problem needs more scratch than the fixed
+    TCL_ERR_STATIC_LIMIT = 11,   /* gemm_s8_static: the problem needs more scratch than the fixed
                                     TCL_S8_STATIC_SCRATCH_BYTES buffer holds */
+    TCL_ERR_CAPTURE = 12         /* the call needs more library scratch than is allocated while its
+                                    stream is being captured into a CUDA graph: run it (or a larger
+                                    one) once outside capture first */
 } tcl_status;
 
 typedef enum { TCL_OUT_F32 = 0, TCL_OUT_BF16 = 1 } tcl_out_t;
@@ -210,9 +224,9 @@ TCL_API int gemm_f32_simt(int M, int N, int K, const float* A, int lda, const fl
  * Who needs it: callers that cannot call cudaMalloc at the point of use —
  * a process whose device memory is already reserved by another allocator
  * (a framework's caching pool that holds the free memory, so a fresh
- * cudaMalloc fails or fragments it), and callers that must not trigger the
- * device-wide synchronisation gemm_s8 performs when it has to grow its
- * scratch (other streams on the device would stall behind it).
+ * cudaMalloc fails or fragments it), and callers that must not have the
+ * library allocate at the point of use (gemm_s8 grows its scratch with
+ * cudaMalloc, which also cannot run while the stream is being captured).
  *
  * Limit: the packed copies need 2·(M·⌈K⌉₈ + K·⌈N⌉₈) bytes, each block rounded
  * up to 256 bytes; a larger problem returns TCL_ERR_STATIC_LIMIT before
@@ -297,7 +311,8 @@ TCL_API int tcl_last_device_error(cudaStream_t stream, int* detail);
 /* Streaming multiprocessors of the current device (0 on error). */
 TCL_API int tcl_num_sms(void);
 
-/* Frees the int8 scratch buffers of every device (after synchronising each). */
+/* Frees the scratch buffers of every device, the outgrown ones included
+ * (after synchronising each), and the host-buffer entry point's streams. */
 TCL_API void tcl_shutdown(void);
 
 /* Library version string, e.g. "tcl-gb300 0.1.0 sm_103a". */

@@ -25,7 +25,7 @@ __all__ = ["gemm", "gemm_into", "gemm_host_into", "gemm_simt_into", "plan", "lib
 STATUS = {
     0: "TCL_OK", 1: "TCL_ERR_NULL", 2: "TCL_ERR_DIMS", 3: "TCL_ERR_LD", 4: "TCL_ERR_ALIGN",
     5: "TCL_ERR_K_TOO_LARGE", 6: "TCL_ERR_LAUNCH", 7: "TCL_ERR_DEVICE_TIMEOUT", 8: "TCL_ERR_CONFIG",
-    9: "TCL_ERR_NO_MEMORY", 10: "TCL_ERR_DEVICE", 11: "TCL_ERR_STATIC_LIMIT",
+    9: "TCL_ERR_NO_MEMORY", 10: "TCL_ERR_DEVICE", 11: "TCL_ERR_STATIC_LIMIT", 12: "TCL_ERR_CAPTURE",
 }
 OUT_F32, OUT_BF16 = 0, 1
 PRODUCER_TMA, PRODUCER_SYNC, PRODUCER_CPASYNC = 0, 1, 2

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "launch.cuh"
 #include "tcl_gemm.h"
@@ -44,6 +45,7 @@ struct DevState {
     unsigned int sk_gen = 0;   // last stream-K flag generation used on this device
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
+    std::vector<void*> retired;   // outgrown scratch buffers, freed by tcl_shutdown
     // host-buffer entry points: uploads, GEMMs and downloads on their own streams
     cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
 };
@@ -95,26 +97,28 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
-// Grows the device's repacking scratch to at least `need` bytes. Growing waits
-// for the device to go idle, since earlier calls may still read the old buffer.
-int ensure_scratch(DevState* ds, size_t need) {
+// Grows the device's scratch to at least `need` bytes (at least doubling it).
+// The outgrown buffer is kept until tcl_shutdown: work already enqueued, or
+// captured into a CUDA graph, may still use it. No allocation while `stream`
+// is being captured (TCL_ERR_CAPTURE): a captured call must find its scratch
+// already allocated by an earlier call outside capture.
+int ensure_scratch(DevState* ds, size_t need, cudaStream_t stream) {
     if (ds->scratch_bytes >= need) return TCL_OK;
-    if (ds->scratch) {
-        if (cudaDeviceSynchronize() != cudaSuccess) {
-            cudaGetLastError();
-            return TCL_ERR_LAUNCH;
-        }
-        cudaFree(ds->scratch);
-        ds->scratch = nullptr;
-        ds->scratch_bytes = 0;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
     }
+    if (cs != cudaStreamCaptureStatusNone) return TCL_ERR_CAPTURE;
+    const size_t want = std::max(need, 2 * ds->scratch_bytes);
     void* p = nullptr;
-    if (cudaMalloc(&p, need) != cudaSuccess) {
+    if (cudaMalloc(&p, want) != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_NO_MEMORY;
     }
+    if (ds->scratch) ds->retired.push_back(ds->scratch);
     ds->scratch = p;
-    ds->scratch_bytes = need;
+    ds->scratch_bytes = want;
     return TCL_OK;
 }
 
@@ -631,7 +635,7 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
     const Workspace ws = split_workspace(pl, M, N);
     const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws.bytes;
-    if (need && (st = ensure_scratch(ds, need))) return st;
+    if (need && (st = ensure_scratch(ds, need, stream))) return st;
     Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
     void* a2 = cv.take(a_bytes);
     void* b2 = cv.take(b_bytes);
@@ -676,7 +680,7 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     const Workspace ws = split_workspace(pl, M, N);
     const size_t need = static_cast<size_t>(round_up(bt_bytes, 256) + round_up(a_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws.bytes;
-    if ((st = ensure_scratch(ds, need))) return st;
+    if ((st = ensure_scratch(ds, need, stream))) return st;
     Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
     float* bt = static_cast<float*>(cv.take(bt_bytes));
     void* a2 = cv.take(a_bytes);
@@ -718,7 +722,7 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
     const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
     const long long c_bytes = pack_c ? round_up(static_cast<long long>(M) * ldc2 * 4, 256) : 0;
-    if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes + c_bytes)))) return st;
+    if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes + c_bytes), stream))) return st;
     uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
     uint8_t* b2 = a2 + a_bytes;
     int32_t* c2 = pack_c ? reinterpret_cast<int32_t*>(b2 + b_bytes) : nullptr;
@@ -792,7 +796,7 @@ int gemm_bf16_host_impl(int M, int N, int K, const void* A, int lda, const void*
     const size_t c_bytes = static_cast<size_t>(M) * ldc2 * oes;
     const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws_bytes;
-    if ((st = ensure_scratch(ds, need))) return st;
+    if ((st = ensure_scratch(ds, need, stream))) return st;
     Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
     uint8_t* a2 = static_cast<uint8_t*>(cv.take(a_bytes));
     uint8_t* b2 = static_cast<uint8_t*>(cv.take(b_bytes));
@@ -1007,6 +1011,7 @@ const char* tcl_status_string(int status) {
         case TCL_ERR_NO_MEMORY: return "scratch allocation failed";
         case TCL_ERR_DEVICE: return "current device is not an sm_103 GPU";
         case TCL_ERR_STATIC_LIMIT: return "problem needs more scratch than the fixed static buffer holds";
+        case TCL_ERR_CAPTURE: return "scratch would have to grow while the stream is being captured";
         default: return "unknown status";
     }
 }
@@ -1062,9 +1067,11 @@ void tcl_shutdown(void) {
             if (cudaSetDevice(d) == cudaSuccess) {
                 cudaDeviceSynchronize();
                 cudaFree(g_dev[d].scratch);
+                for (void* r : g_dev[d].retired) cudaFree(r);
             }
             g_dev[d].scratch = nullptr;
             g_dev[d].scratch_bytes = 0;
+            g_dev[d].retired.clear();
         }
     }
     cudaSetDevice(prev);

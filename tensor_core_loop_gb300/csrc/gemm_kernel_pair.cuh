@@ -420,8 +420,16 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                                    : nullptr;
         };
         auto wait_turn = [&](uint32_t* flag, const PairUnit& U) {   // piece > 0: the previous piece is in C
-            return wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
-                                p.timeout_ns, p.status);
+            if (!wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
+                              p.timeout_ns, p.status))
+                return false;
+            if (U.piece + 1 == p.sk_pieces) {
+                // the flag's last reader leaves it as this launch found it (0), so that a
+                // replay of the same launch (a CUDA graph: same generation) waits again
+                __syncwarp();   // every lane has made its acquire of the flag
+                if (lane == 0) *reinterpret_cast<volatile uint32_t*>(flag) = 0u;
+            }
+            return true;
         };
         auto hand_over = [&](uint32_t* flag, const PairUnit& U) {
             // hand these rows to the next piece once every write to them has landed

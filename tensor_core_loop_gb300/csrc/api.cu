@@ -213,6 +213,7 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 
 struct Plan {
     int bn, stages, prod, pair, slots, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
+    int sk_ws_rows;   // bf16 C with a stream-K tail: fp32 workspace rows (split tiles × 256), else 0
     int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
     int sk_tiles, sk_pieces;    // stream-K tail of the two-SM kernel (0 tiles: none)
 };
@@ -245,7 +246,8 @@ constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed whe
 // `pieces` K ranges so that the otherwise idle pairs share them.
 // want: 0 automatic, 1 never, s >= 2 exactly s pieces (TCL_ERR_CONFIG if that
 // does not fit). Fills *sk_tiles = 0 when there is no stream-K tail.
-int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_tiles, int* sk_pieces) {
+int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_tiles, int* sk_pieces,
+                   int min_kb = kMinKbForSk) {
     *sk_tiles = 0;
     *sk_pieces = 1;
     const long long rem = tiles % pairs;
@@ -257,7 +259,7 @@ int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_til
         return TCL_OK;
     }
     const int s = static_cast<int>(std::min<long long>({kMaxSkPieces, pairs / rem, num_kb / kMinKbPerPiece}));
-    if (s >= 2 && rem <= kMaxSkTiles && num_kb >= kMinKbForSk) {
+    if (s >= 2 && rem <= kMaxSkTiles && num_kb >= min_kb) {
         *sk_tiles = static_cast<int>(rem);
         *sk_pieces = s;
     }
@@ -325,8 +327,9 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
     }
     const int want_sk = cfg ? cfg->stream_k : 0;
-    // stream-K pieces add into C: fp32 or int32 (a bf16 C would be rounded twice)
-    const bool sk_capable = ok == OutKind::F32 || ok == OutKind::S32;
+    // stream-K pieces add into C (fp32, int32) or, for a bf16 C (which must be rounded
+    // once), into an fp32 workspace that the last piece adds before rounding
+    const bool sk_capable = ok == OutKind::F32 || ok == OutKind::S32 || ok == OutKind::BF16;
     if (want_sk < 0 || want_sk > kMaxSkPieces || (want_sk > 1 && (!pair || !sk_capable))) return TCL_ERR_CONFIG;
     // CTA pairs per cluster: 2 = two pairs on tiles stacked in M sharing B by multicast
     const int want_cp = cfg ? cfg->cluster_pairs : 0;
@@ -420,6 +423,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     const long long work = static_cast<long long>(pl->num_tiles) * pl->splits;
     pl->sk_tiles = 0;
     pl->sk_pieces = 1;
+    pl->sk_ws_rows = 0;
     if (pair) {
         const int cl = 2 * cpairs;   // CTAs per cluster
         int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / cl : pair_clusters(v);
@@ -429,8 +433,10 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         // Stream-K pieces wait on one another, so every pair of the grid must be
         // resident at once: the grid never exceeds the resident clusters here.
         if (sk_capable && !(cfg && cfg->one_cta_per_tile)) {
+            // (a bf16 C pays for its workspace round trip: measured on GB300 at 4096²×2048,
+            // 44.2 µs with a tail against 41.6 without; at ×4096 the tail wins, 76.7 vs 77.5)
             const int st = stream_k_split(pl->num_tiles, pl->grid / cl, pl->num_kb, want_sk, &pl->sk_tiles,
-                                          &pl->sk_pieces);
+                                          &pl->sk_pieces, ok == OutKind::BF16 ? 2 * kMinKbForSk : kMinKbForSk);
             if (st) return st;
             if (pl->sk_tiles * cpairs > kMaxSkTiles) {   // the progress flags hold kMaxSkTiles tiles
                 if (want_sk > 1) return TCL_ERR_CONFIG;
@@ -444,6 +450,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
                 pl->sk_pieces = 1;
             }
         }
+        if (ok == OutKind::BF16 && pl->sk_tiles) pl->sk_ws_rows = pl->sk_tiles * cpairs * 2 * kBM;
     } else if (want_sk > 1) {
         return TCL_ERR_CONFIG;
     } else if (cfg && cfg->one_cta_per_tile) {
@@ -456,7 +463,8 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     return TCL_OK;
 }
 
-// Split-K workspace: `splits` fp32 slabs of round_up(M, 128) rows × round_up(N, 4) columns.
+// Split-K workspace: `splits` fp32 slabs of round_up(M, 128) rows × round_up(N, 4) columns;
+// or, for a bf16 C with a stream-K tail, sk_ws_rows fp32 rows of bn columns.
 struct Workspace {
     long long ld, rows_per_split;
     size_t bytes;
@@ -468,6 +476,8 @@ Workspace split_workspace(const Plan& pl, int M, int N) {
         w.ld = round_up(N, 4);
         w.rows_per_split = round_up(M, kBM);
         w.bytes = static_cast<size_t>(round_up(w.ld * w.rows_per_split * 4 * pl.splits, 256));
+    } else if (pl.sk_ws_rows) {
+        w.bytes = static_cast<size_t>(round_up(static_cast<long long>(pl.sk_ws_rows) * pl.bn * 4, 256));
     }
     return w;
 }
@@ -559,6 +569,16 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.debug_sk_stall = cfg && cfg->debug_stream_k_stall ? 1 : 0;
     p.sk_flags = ds->sk_flags;
     p.sk_gen = 0;
+    p.sk_ws = nullptr;
+    p.sk_ws_rows = 0;
+    a.tmW = a.tmC;
+    if (pl.sk_ws_rows) {
+        p.sk_ws = static_cast<float*>(workspace);
+        p.sk_ws_rows = pl.sk_ws_rows;
+        if ((st = tensor_map(dev, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pl.bn, pl.sk_ws_rows, pl.bn * 4, 32, 32,
+                             &a.tmW)))
+            return st;
+    }
     if (pl.sk_tiles) {
         ds->sk_gen = (ds->sk_gen + 1) & 0x1FFFFFFFu;   // flags hold gen·8 + pieces done in 32 bits
         if (ds->sk_gen == 0) ds->sk_gen = 1;           // 0 is what the flags start as

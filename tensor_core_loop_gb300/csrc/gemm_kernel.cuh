@@ -97,9 +97,23 @@ struct GemmParams {
     // result, piece i > 0 adds its own once piece i-1 has finished (flags).
     int sk_tiles;                // 0: every tile is whole
     int sk_pieces;               // K ranges per split tile (>= 2 when sk_tiles > 0)
-    unsigned int* sk_flags;      // [sk_tiles][2 CTAs][4 epilogue warps] progress flags
+    unsigned int* sk_flags;      // [sk_tiles][2 CTAs][epilogue warp] progress flags
     unsigned int sk_gen;         // this launch's flag generation (flags hold gen·8 + pieces done)
     int debug_sk_stall;          // test hook: piece 0 of split tile 0 never publishes its flag
+    // bf16 C with a stream-K tail: the pieces before the last add their fp32 sums in a
+    // workspace of [split tile][256 rows] × BN fp32 (row-major, BN per row); the last
+    // piece adds the workspace rows to its own sums and rounds once into C
+    float* sk_ws;
+    int sk_ws_rows;
+};
+
+// Where an epilogue writes: base, leading dimension (elements), columns and rows
+// in bounds. GemmParams has the same members, for C itself.
+struct OutView {
+    void* C;
+    long long ldc;
+    int N;
+    int out_rows;
 };
 
 // Work item w → output tile (mb, nb), its k-block range [kb_lo, kb_hi) and
@@ -264,10 +278,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // columns after N. That chunk is stored element by element from registers
 // instead (rows past M skipped), leaving every byte outside C untouched.
 // INT: the 4-byte values are int32 (an add is an integer add).
-template <int SLAB_BYTES, int OUT_ES, int SLOTS, bool INT = false>
+template <int SLAB_BYTES, int OUT_ES, int SLOTS, bool INT = false, class Out = GemmParams>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
-                                           const GemmParams& p, bool add = false) {
+                                           const Out& p, bool add = false) {
     constexpr int COLS = 128 / OUT_ES;
     const bool in_bounds = row0 < p.out_rows && col0 < p.N;
     if (in_bounds && col0 + COLS > p.N && (p.N * OUT_ES) % 16 != 0) {
@@ -486,12 +500,15 @@ struct NoPace {
 // issue. `release()` runs once every TMEM read of the accumulator is complete;
 // `pace(c)` runs before chunk c is staged and stored (the two-SM kernel uses
 // it to spread a tile's stores over the next tile's mainloop). `add`: reduce
-// into C instead of storing (fp32).
-template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release, class Pace = NoPace>
+// into C instead of storing (fp32). `pre`, if not null, is this lane's row of
+// fp32 values (the chunk's columns at pre[c·COLS ..]) added to the
+// accumulator before the conversion.
+template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release, class Pace = NoPace,
+          class Out = GemmParams>
 __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_t* slab_pair, int& store_count,
-                                                  uint32_t tbase, int lane, int col_base, int row0,
-                                                  const GemmParams& p, Release release, bool add = false,
-                                                  Pace pace = Pace()) {
+                                                  uint32_t tbase, int lane, int col_base, int row0, const Out& p,
+                                                  Release release, bool add = false, Pace pace = Pace(),
+                                                  const float* pre = nullptr) {
     constexpr int COLS = OK == OutKind::BF16 ? 64 : 32;   // TMEM columns per chunk
     constexpr int OUT_ES = OK == OutKind::BF16 ? 2 : 4;
     uint32_t buf[2][COLS];
@@ -512,6 +529,17 @@ __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_
         } else {
             release();
         }
+        if (pre) {
+            const float4* src = reinterpret_cast<const float4*>(pre + c * COLS);
+#pragma unroll
+            for (int j = 0; j < COLS / 4; ++j) {
+                const float4 w = src[j];
+                cur[4 * j + 0] = __float_as_uint(__uint_as_float(cur[4 * j + 0]) + w.x);
+                cur[4 * j + 1] = __float_as_uint(__uint_as_float(cur[4 * j + 1]) + w.y);
+                cur[4 * j + 2] = __float_as_uint(__uint_as_float(cur[4 * j + 2]) + w.z);
+                cur[4 * j + 3] = __float_as_uint(__uint_as_float(cur[4 * j + 3]) + w.w);
+            }
+        }
         uint32_t v[32];
         if constexpr (OK == OutKind::BF16) {
 #pragma unroll
@@ -524,8 +552,8 @@ __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_
             for (int i = 0; i < 32; ++i) v[i] = cur[i];
         }
         pace(c);
-        store_slab<SLAB_BYTES, OUT_ES, SLOTS>(tmC, slab_pair, store_count, v, lane, col_base + c * (128 / OUT_ES), row0,
-                                              p, add);
+        store_slab<SLAB_BYTES, OUT_ES, SLOTS, false, Out>(tmC, slab_pair, store_count, v, lane,
+                                                          col_base + c * (128 / OUT_ES), row0, p, add);
     }
 }
 

@@ -207,7 +207,8 @@ __device__ __forceinline__ void spin_ns(unsigned long long ns) {
 template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS, InKind IK>
 __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+                     const GemmParams p) {
     using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -512,13 +513,33 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                     break;
                 }
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_STRIDE;
+                auto release = [&]() {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster_relaxed(acce_leader0 + 8 * buf);
+                };
+                if constexpr (OK == OutKind::BF16) {
+                    if (flag) {
+                        // bf16 C, split tile: the pieces' fp32 sums meet in the workspace
+                        // (stored by piece 0, added by the next ones in piece order); the
+                        // last piece adds its workspace rows and rounds once into C
+                        const int wrow0 = ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + static_cast<int>(rank)) *
+                                              C::ROWS + q * 32;
+                        if (U.piece + 1 < p.sk_pieces) {
+                            const OutView w{p.sk_ws, C::BN, C::BN, p.sk_ws_rows};
+                            drain_accumulator<OutKind::F32, C::BN / 32, C::SLAB_BYTES, C::EPI_SLOTS>(
+                                &tmW, slab_pair, store_count, tbase, lane, 0, wrow0, w, release, U.piece > 0);
+                            hand_over(flag, U);
+                        } else {
+                            drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
+                                &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p, release, false,
+                                NoPace(), p.sk_ws + static_cast<long long>(wrow0 + lane) * C::BN);
+                        }
+                        continue;
+                    }
+                }
                 drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
-                    &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p,
-                    [&]() {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive_cluster_relaxed(acce_leader0 + 8 * buf);
-                    },
+                    &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p, release,
                     /*add=*/U.piece > 0, [&](int c) {
                         // Spread this tile's stores over the next unit's mainloop: chunk c waits
                         // until the producer is c/EPI_CHUNKS of the way through that unit (a

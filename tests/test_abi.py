@@ -159,8 +159,8 @@ def test_planner_stream_k(L):
     # whole waves: nothing to split
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4864, 4096, 4096, cfg)
     assert (p["bn"], p["num_tiles"], p["sk_tiles"]) == (256, 304, 0)
-    # bf16 C: no stream-K (a bf16 partial would be rounded twice)
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)["sk_tiles"] == 0
+    # bf16 C: the same tail, its partials kept in fp32 until the last piece rounds once
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)["sk_tiles"] == 28
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2))
     assert (p["num_tiles"], p["sk_tiles"], p["sk_pieces"]) == (9, 1, 4)
     # short tiles (16 k-blocks): the extra piece's epilogue costs more than the tail saves
@@ -173,8 +173,13 @@ def test_planner_stream_k(L):
                 tcl.Config(max_ctas=8, cta_pair=2, stream_k=-1)):
         with pytest.raises(tcl.TclError):
             tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, bad)
-    with pytest.raises(tcl.TclError):
-        tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2, stream_k=2))
+    # a bf16 C takes a stream-K tail through an fp32 workspace: split tiles × 256 rows × bn columns
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2, stream_k=2))
+    assert (p["sk_tiles"], p["sk_pieces"]) == (1, 2) and p["workspace_bytes"] == 1 * 256 * 256 * 4
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, tcl.Config(max_ctas=152))
+    assert (p["bn"], p["sk_tiles"], p["sk_pieces"]) == (256, 28, 2) and p["workspace_bytes"] == 28 * 256 * 256 * 4
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152))
+    assert p["sk_tiles"] == 28 and p["workspace_bytes"] == 0   # fp32 C: pieces add into C itself
 
 
 def test_planner_producer_kinds(L):

@@ -67,6 +67,15 @@ def test_stream_k_bf16_replays(pieces):
     assert torch.equal(ref, direct)
 
 
+def test_stream_k_bf16_out_replays():
+    # bf16 C: the pieces meet in the fp32 workspace (library scratch) before one rounding
+    a, b = inputs.bf16_pair(768, 768, 2048, seed=36)
+    a, b = a.to(DEV), b.to(DEV)
+    cfg = tcl.Config(cta_pair=2, max_ctas=8, stream_k=3)
+    c = torch.empty((768, 768), dtype=torch.bfloat16, device=DEV)
+    replay_matches(a, b, c, cfg)
+
+
 def test_stream_k_int8_replays():
     a, b = inputs.s8_pair(768, 768, 2048, seed=32)
     a, b = a.to(DEV), b.to(DEV)

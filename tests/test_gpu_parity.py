@@ -212,6 +212,38 @@ def test_bf16_pair_kernel_bf16_out(oracle_mod, M, N, K):
     bf16_case(oracle_mod, M, N, K, seed=5, out_dtype=torch.bfloat16, cfg=tcl.Config(cta_pair=2))
 
 
+@pytest.mark.parametrize("M,N,K,pieces,pairs", [
+    (768, 768, 4096, 0, 1),     # automatic (64 k-blocks): the 9th tile in 4 pieces, three fp32 partials
+    (768, 768, 2048, 2, 1),
+    (768, 768, 2048, 3, 1),
+    (700, 750, 1000, 4, 1),     # ragged M, N: the last piece rounds and stores only what lies in C
+    (512, 1280, 576, 2, 1),
+    (1024, 1280, 2048, 2, 2),   # two pairs per cluster: workspace rows per pair
+])
+def test_bf16_out_stream_k(oracle_mod, M, N, K, pieces, pairs):
+    # bf16 C with a stream-K tail: the pieces' fp32 sums meet in an fp32 workspace in piece
+    # order and the last piece rounds once into C, so the bf16 bound holds unchanged
+    cfg = tcl.Config(cta_pair=2, cluster_pairs=pairs, max_ctas=8 * pairs, stream_k=pieces)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, M, N, K, cfg)
+    assert pl["sk_tiles"] > 0 and pl["workspace_bytes"] > 0
+    ldc = -(-N // 8) * 8 if N % 8 else None
+    bf16_case(oracle_mod, M, N, K, seed=K + pieces, out_dtype=torch.bfloat16, cfg=cfg, ldc=ldc)
+
+
+def test_bf16_out_stream_k_rounds_once():
+    # the same tile split or not: the fp32 sums differ only in summation order, and the
+    # split result equals the split fp32 result rounded to bf16 (one rounding)
+    a, b = inputs.bf16_pair(768, 768, 2048, seed=41)
+    a, b = a.to(DEV), b.to(DEV)
+    for pieces in (2, 4):
+        cfg = tcl.Config(cta_pair=2, max_ctas=8, stream_k=pieces)
+        c16 = run(a, b, out_dtype=torch.bfloat16, cfg=cfg)
+        c32 = run(a, b, out_dtype=torch.float32, cfg=cfg)
+        assert torch.equal(c16, c32.to(torch.bfloat16))
+        for _ in range(5):
+            assert torch.equal(run(a, b, out_dtype=torch.bfloat16, cfg=cfg, canary=False), c16)
+
+
 @pytest.mark.parametrize("M,N,K,pieces", [
     (768, 768, 2048, 0),     # 9 tiles on 4 pairs: 2 full waves, the 9th tile in 4 pieces of 8 k-blocks
     (768, 768, 2048, 2),

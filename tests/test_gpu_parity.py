@@ -552,6 +552,19 @@ def test_s8_extremes_closed_form(va, vb, pair, bn, sk):
     assert (c == va * vb * K).all()
 
 
+@pytest.mark.parametrize("va,vb", [(-128, -128), (127, -128)])
+def test_s8_largest_k_closed_form(va, vb):
+    # K = 131071, the largest the int32 result guarantees: |sum| up to 2^14·131071 < 2^31;
+    # 256 accumulation units of 512 K values, all added in int32 registers
+    K = 131071
+    a = torch.full((130, K), va, dtype=torch.int8, device=DEV)
+    b = torch.full((K, 72), vb, dtype=torch.int8, device=DEV)
+    c = tcl.gemm(a, b)
+    assert (c == va * vb * K).all()
+    with pytest.raises(tcl.TclError):
+        tcl.gemm(torch.ones((8, K + 1), dtype=torch.int8, device=DEV), torch.ones((K + 1, 8), dtype=torch.int8, device=DEV))
+
+
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("M,N,K", [(256, 128, 64), (512, 384, 4096), (300, 200, 1100), (520, 390, 2064),
                                    (1000, 700, 520)])

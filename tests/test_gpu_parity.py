@@ -610,6 +610,15 @@ def test_bf16_4096_cube_fp32_sampled(oracle_mod):
     bf16_case(oracle_mod, 4096, 4096, 4096, seed=0, rows=sample_rows(4096))
 
 
+def test_bf16_large_grid_sampled(oracle_mod):
+    # 16384×16384×4096: 4096 pair tiles, 54 waves on 76 pairs (the last one 68 tiles); a 1 GB
+    # fp32 C compared on sampled rows that cross every column of tiles
+    M = N = 16384
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, 4096)
+    assert pl["cta_pair"] == 2 and pl["num_tiles"] == 64 * 64
+    bf16_case(oracle_mod, M, N, 4096, seed=7, rows=sample_rows(M, n=8, seed=7))
+
+
 def test_bf16_4096_cube_bf16_sampled(oracle_mod):
     bf16_case(oracle_mod, 4096, 4096, 4096, seed=0, out_dtype=torch.bfloat16, rows=sample_rows(4096, n=8))
 

@@ -750,6 +750,9 @@ def main():
     rate = measured_mma_rate(tcl) or 8192.0
     clk = kernel_mhz or sm_mhz
     cc_peak = (sms * rate * clk * 1e6 / 1e12) if clk else None
+    # the same pipe rate at the GPU's maximum SM clock (nvidia-smi clocks.max.sm)
+    max_mhz = clocks.get("sm_max_mhz") if clocks else None
+    max_peak = (sms * rate * max_mhz * 1e6 / 1e12) if max_mhz else None
     if clocks is not None:
         clocks["sm_mhz_in_kernel"] = kernel_mhz
     line = {
@@ -774,7 +777,9 @@ def main():
                      "clock_corrected_peak": cc_peak,
                      "clock_corrected_peak_def": "SMs x probe-measured flop/clk/SM x SM clock measured inside "
                                                  "the kernel (%clock64 / %globaltimer) on the timed workload",
-                     "frac_clock_corrected": (achieved / cc_peak) if cc_peak else None},
+                     "frac_clock_corrected": (achieved / cc_peak) if cc_peak else None,
+                     "max_clock_peak": max_peak,
+                     "frac_of_max_clock": (achieved / max_peak) if max_peak else None},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps,

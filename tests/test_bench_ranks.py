@@ -7,9 +7,6 @@ whole job's throughput. The reference arm runs on rank 0 only.
 """
 from __future__ import annotations
 
-import os
-import socket
-
 import pytest
 import torch
 import torch.distributed as dist
@@ -18,16 +15,9 @@ import torch.multiprocessing as mp
 import bench
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
-
-
-def _rank_main(rank, world, port, times, out):
-    os.environ["MASTER_ADDR"] = "127.0.0.1"
-    os.environ["MASTER_PORT"] = str(port)
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+def _rank_main(rank, world, store_path, times, out):
+    # a file store: no TCP port to pick (a port found free can be taken before the ranks bind it)
+    dist.init_process_group("gloo", init_method=f"file://{store_path}", rank=rank, world_size=world)
     try:
         ms_max = bench.max_over_ranks(times[rank], dist, torch.device("cpu"))
         out[rank] = (ms_max, bench.job_value(bench.FLOPS, world, 100, ms_max))
@@ -36,12 +26,12 @@ def _rank_main(rank, world, port, times, out):
         dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_agree_on_the_slowest_time():
+def test_two_gloo_ranks_agree_on_the_slowest_time(tmp_path):
     world = 2
     times = [80.0, 95.5]   # rank 1 is the slower one
     ctx = mp.get_context("spawn")
     out = ctx.Manager().dict()
-    mp.start_processes(_rank_main, args=(world, _free_port(), times, out), nprocs=world, join=True,
+    mp.start_processes(_rank_main, args=(world, str(tmp_path / "store"), times, out), nprocs=world, join=True,
                        start_method="spawn")
     assert out[0][0] == out[1][0] == 95.5
     # whole-job value: both ranks' flops over the slowest rank's time

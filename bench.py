@@ -307,6 +307,23 @@ def compute_load_ratio(bm, bn, bk, esize):
     return 2.0 * bm * bn * bk / ((bm * bk + bk * bn) * esize)
 
 
+def stage_bytes(bm, bn, bk, esize):
+    """Shared-memory bytes of one ring stage: the A tile (bm × bk) and the B tile (bk × bn)."""
+    a = bm * bk * esize
+    b = bk * bn * esize
+    return a, b, a + b
+
+
+def wave_blocks(sms, blocks_per_sm):
+    """Thread blocks that run at once: one wave of the grid ("4.1 CUDA GEMM 算子性能优化", §2.3)."""
+    return sms * blocks_per_sm
+
+
+def tile_waves(plan, sms):
+    """Output tiles over the tiles one wave holds (one CTA per SM; a two-SM tile takes two)."""
+    return round(plan["num_tiles"] / (wave_blocks(sms, 1) // plan["cta_pair"]), 2)
+
+
 def run_ablation(args):
     import torch
     import tensor_core_loop_gb300 as tcl
@@ -337,7 +354,8 @@ def run_ablation(args):
             tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
             line = {"ablation": label, "shape": f"{m}x{n}x{k}", "tflops": round(tf, 1), "us": round(ms * 1e3, 2),
                     "delta_vs_prev_pct": None if prev is None else round(100.0 * (tf / prev - 1.0), 1),
-                    "compute_load_ratio": round(ratio, 1), "bn": 256, "stages": stages,
+                    "compute_load_ratio": round(ratio, 1), "stage_bytes": stage_bytes(128, 256, 64, 2)[2],
+                    "bn": 256, "stages": stages,
                     "producer": PRODUCER_NAMES[prod]}
             prev = tf
             print(json.dumps(line), flush=True)
@@ -764,7 +782,8 @@ def main():
         "config": {**base_config(),
                    "l2": f"inputs rotated over {nsets} sets of {set_bytes >> 20} MiB (> 129 MB L2)",
                    "vs_baseline_ref": "pages' hgemm_bcf_dbf_rw 4096^3 bf16 33.72 TFLOPS, GPU not stated (context)",
-                   "plan": tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K), "sms": sms},
+                   "plan": tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K), "sms": sms,
+                   "tile_waves": tile_waves(tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K), sms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": recorded_traffic("gemm_bf16_f32_4096", tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K)),
                      "peak_source": (f"{peak_src} bf16_tflops_sustained (cuBLAS 8192^3 back to back for 4 s; "

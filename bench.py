@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import time
@@ -107,13 +108,22 @@ KERNEL_SOURCES = ("ptx.cuh", "gemm_kernel.cuh", "gemm_kernel_pair.cuh", "k_pair.
 PLAN_KEYS = ("bn", "stages", "cta_pair", "splits", "sk_tiles", "sk_pieces")
 
 
+def _code_only(text):
+    """Source text without comments and whitespace: what the compiler sees of it
+    (a comment inside a string literal would be dropped too; the kernel sources
+    have none that matter)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_core_loop_gb300", "csrc")
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,6 +22,13 @@
 // (empty[s] takes one multicast commit from each leader).
 // TF32 inputs (IK = TF32) take B K-major (the host transposes it): each CTA
 // then loads its half of B as one box of BN/2 rows × 128 B, 32 K values deep.
+// Exact integers (OK = S32, int8 widened to bf16) accumulate units of 512 K
+// values per TMEM buffer and add each unit, converted, into int32 registers:
+// 128 columns per thread, so a 256-wide tile has eight epilogue warps.
+// A stream-K tail cuts the last partial wave of tiles into K pieces run by the
+// otherwise idle pairs; piece i > 0 adds its sums after piece i-1 (per-warp
+// flags): into C for fp32 and int32, through an fp32 workspace for bf16, whose
+// last piece rounds once.
 // Waits are bounded as in the one-SM kernel; a role that gives up raises the
 // abort flag of every CTA of the cluster.
 #pragma once
@@ -420,7 +427,8 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                                                       C::EPI_WARPS + (warp - 2)
                                    : nullptr;
         };
-        auto wait_turn = [&](uint32_t* flag, const PairUnit& U) {   // piece > 0: the previous piece is in C
+        // piece > 0: wait until the previous piece's sums are in C (or in the workspace)
+        auto wait_turn = [&](uint32_t* flag, const PairUnit& U) {
             if (!wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
                               p.timeout_ns, p.status))
                 return false;

@@ -464,6 +464,8 @@ def test_variants_bitwise_identical():
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,out", [
     (4096, 4096, 4096, 4096, 4096, 4096, torch.float32),    # eight row chunks, sampled rows
+    (1536, 2100, 520, 520, 2104, 2100, torch.float32),      # three chunks of 512 rows, unpadded host C
+    (1100, 2304, 96, 96, 2304, 2312, torch.bfloat16),       # chunks of 768 and 332 rows, bf16 C
     (1000, 777, 203, 205, 779, 780, torch.float32),         # K % 8 = 3 (zero-padded on the device), ragged
     (1000, 520, 640, 640, 520, 528, torch.bfloat16),        # two chunks, bf16 C
     (100, 64, 64, 64, 64, 64, torch.float32),               # one chunk

@@ -179,9 +179,9 @@ TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float*
 
 /* int8 A, B; exact int32 C (bit-exact integer result for K <= 131071).
  * The operands are widened exactly to bf16 in library scratch, the tensor
- * cores accumulate in fp32 in units of at most 512 K values (every partial
- * sum is an integer below 2^24 in magnitude, hence exact), and each unit is
- * added into int32 registers. */
+ * cores accumulate in fp32 in units of at most 1024 K values (every partial
+ * sum is an integer of magnitude at most 2^24, hence exact in fp32), and each
+ * unit is added into int32 registers. */
 TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
             int ldc, cudaStream_t stream);
 

@@ -29,11 +29,13 @@ __device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 8];
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
 constexpr int kBM = 128;
-// K values per exact fp32 unit: every partial sum is an integer of magnitude at most
-// 512·2^14 = 2^23 < 2^24, so the fp32 accumulation and its conversion are exact.
+// K values per exact fp32 unit: every partial sum of a unit, of any subset of its
+// products, is an integer of magnitude at most 1024·2^14 = 2^24, and every such
+// integer is an fp32 value (below 2^24 the unit in the last place is at most 1), so
+// the fp32 accumulation and its conversion are exact.
 // (Measured on GB300: 512-K units beat 256-K units converted with a cheaper add,
 // 103 vs 108 us at int8 4096^3: the unit turnover costs more than the conversion.)
-constexpr int kS32UnitK = 512;
+constexpr int kS32UnitK = 1024;
 
 struct DevState {
     bool probed = false;

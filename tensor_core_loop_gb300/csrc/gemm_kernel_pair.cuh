@@ -22,7 +22,7 @@
 // (empty[s] takes one multicast commit from each leader).
 // TF32 inputs (IK = TF32) take B K-major (the host transposes it): each CTA
 // then loads its half of B as one box of BN/2 rows × 128 B, 32 K values deep.
-// Exact integers (OK = S32, int8 widened to bf16) accumulate units of 512 K
+// Exact integers (OK = S32, int8 widened to bf16) accumulate units of 1024 K
 // values per TMEM buffer and add each unit, converted, into int32 registers:
 // 128 columns per thread, so a 256-wide tile has eight epilogue warps.
 // A stream-K tail cuts the last partial wave of tiles into K pieces run by the
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
             const int units = pair_units(p, cluster, clusters);
             for (int u = 0; ok && u < units; ++u) {
                 const PairUnit U = pair_unit(p, cluster, clusters, u);
-                // accumulation units of kb_per_unit k-blocks (exact-integer mode: 512 K
+                // accumulation units of kb_per_unit k-blocks (exact-integer mode: 1024 K
                 // values, drained into int32 sums; otherwise the whole range)
                 for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
                     const int kb1 = min(kb0 + p.kb_per_unit, U.kb_hi);

@@ -101,7 +101,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.tiles_n = (N + bn - 1) / bn;
     p.num_tiles = tiles;
     p.num_kb = (K + 63) / 64;
-    p.kb_per_unit = 512 / 64;   // exact fp32 units of 512 K values, as gemm_s8
+    p.kb_per_unit = 1024 / 64;   // exact fp32 units of 1024 K values, as gemm_s8
     p.group_m = 8;
     p.timeout_ns = 1000000000ull;
     p.status = status;

@@ -543,8 +543,8 @@ def test_s8_padded(oracle_mod):
 @pytest.mark.parametrize("pair,bn,sk", [(1, 0, 1), (2, 128, 1), (2, 256, 1), (2, 256, 3)])
 @pytest.mark.parametrize("va,vb", [(127, 127), (-128, -128), (127, -128)])
 def test_s8_extremes_closed_form(va, vb, pair, bn, sk):
-    # |sum| = 2^26 at K = 4096: eight fp32 units of 512 products each (2^23 apiece for
-    # (-128)·(-128)), added as int32
+    # |sum| = 2^26 at K = 4096: four fp32 units of 1024 products each (exactly 2^24 apiece
+    # for (-128)·(-128)), added as int32
     # (sk = 3: 1280 columns of 256 on four pairs, the 5th tile in three K pieces)
     K = 4096
     a = torch.full((256, K), va, dtype=torch.int8, device=DEV)
@@ -554,10 +554,23 @@ def test_s8_extremes_closed_form(va, vb, pair, bn, sk):
     assert (c == va * vb * K).all()
 
 
+@pytest.mark.parametrize("pair,bn", [(1, 0), (2, 256)])
+@pytest.mark.parametrize("K", [1024, 4096, 3000])
+def test_s8_odd_sums_near_2_24(K, pair, bn):
+    # rows and columns of -128 that end in 127: every 1024-deep unit but the last sums to
+    # exactly 2^24, the last to (n-1)·2^14 + 127² — odd, just below 2^24 when n = 1024
+    a = torch.full((256, K), -128, dtype=torch.int8, device=DEV)
+    b = torch.full((K, 256), -128, dtype=torch.int8, device=DEV)
+    a[:, K - 1] = 127
+    b[K - 1, :] = 127
+    c = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=pair, bn=bn))
+    assert (c == (K - 1) * 16384 + 127 * 127).all()
+
+
 @pytest.mark.parametrize("va,vb", [(-128, -128), (127, -128)])
 def test_s8_largest_k_closed_form(va, vb):
     # K = 131071, the largest the int32 result guarantees: |sum| up to 2^14·131071 < 2^31;
-    # 256 accumulation units of 512 K values, all added in int32 registers
+    # 128 accumulation units of 1024 K values, all added in int32 registers
     K = 131071
     a = torch.full((130, K), va, dtype=torch.int8, device=DEV)
     b = torch.full((K, 72), vb, dtype=torch.int8, device=DEV)

@@ -466,7 +466,8 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
 }
 
 // Split-K workspace: `splits` fp32 slabs of round_up(M, 128) rows × round_up(N, 4) columns;
-// or, for a bf16 C with a stream-K tail, sk_ws_rows fp32 rows of bn columns.
+// or, for a bf16 C with a stream-K tail, sk_ws_rows × bn fp32 (blocks of 32 rows,
+// each laid out for one epilogue warp's coalesced 16-byte accesses).
 struct Workspace {
     long long ld, rows_per_split;
     size_t bytes;
@@ -573,13 +574,9 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.sk_gen = 0;
     p.sk_ws = nullptr;
     p.sk_ws_rows = 0;
-    a.tmW = a.tmC;
-    if (pl.sk_ws_rows) {
+    if (pl.sk_ws_rows) {   // (16-byte accesses: the workspace starts on a 256-byte boundary)
         p.sk_ws = static_cast<float*>(workspace);
         p.sk_ws_rows = pl.sk_ws_rows;
-        if ((st = tensor_map(dev, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pl.bn, pl.sk_ws_rows, pl.bn * 4, 32, 32,
-                             &a.tmW)))
-            return st;
     }
     if (pl.sk_tiles) {
         ds->sk_gen = (ds->sk_gen + 1) & 0x1FFFFFFFu;   // flags hold gen·8 + pieces done in 32 bits

@@ -101,19 +101,12 @@ struct GemmParams {
     unsigned int sk_gen;         // this launch's flag generation (flags hold gen·8 + pieces done)
     int debug_sk_stall;          // test hook: piece 0 of split tile 0 never publishes its flag
     // bf16 C with a stream-K tail: the pieces before the last add their fp32 sums in a
-    // workspace of [split tile][256 rows] × BN fp32 (row-major, BN per row); the last
-    // piece adds the workspace rows to its own sums and rounds once into C
+    // workspace of sk_ws_rows / 32 blocks, one per epilogue warp's 32 rows of a split
+    // tile, each BN/4 groups × 32 lanes × 4 fp32 (a warp's 16-byte accesses to one
+    // column group are 512 contiguous bytes); the last piece adds its block to its own
+    // sums and rounds once into C
     float* sk_ws;
     int sk_ws_rows;
-};
-
-// Where an epilogue writes: base, leading dimension (elements), columns and rows
-// in bounds. GemmParams has the same members, for C itself.
-struct OutView {
-    void* C;
-    long long ldc;
-    int N;
-    int out_rows;
 };
 
 // Work item w → output tile (mb, nb), its k-block range [kb_lo, kb_hi) and
@@ -278,10 +271,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // columns after N. That chunk is stored element by element from registers
 // instead (rows past M skipped), leaving every byte outside C untouched.
 // INT: the 4-byte values are int32 (an add is an integer add).
-template <int SLAB_BYTES, int OUT_ES, int SLOTS, bool INT = false, class Out = GemmParams>
+template <int SLAB_BYTES, int OUT_ES, int SLOTS, bool INT = false>
 __device__ __forceinline__ void store_slab(const CUtensorMap* tmC, uint8_t* slab_pair, int& count,
                                            const uint32_t (&v)[32], int lane, int col0, int row0,
-                                           const Out& p, bool add = false) {
+                                           const GemmParams& p, bool add = false) {
     constexpr int COLS = 128 / OUT_ES;
     const bool in_bounds = row0 < p.out_rows && col0 < p.N;
     if (in_bounds && col0 + COLS > p.N && (p.N * OUT_ES) % 16 != 0) {
@@ -500,15 +493,14 @@ struct NoPace {
 // issue. `release()` runs once every TMEM read of the accumulator is complete;
 // `pace(c)` runs before chunk c is staged and stored (the two-SM kernel uses
 // it to spread a tile's stores over the next tile's mainloop). `add`: reduce
-// into C instead of storing (fp32). `pre`, if not null, is this lane's row of
-// fp32 values (the chunk's columns at pre[c·COLS ..]) added to the
-// accumulator before the conversion.
-template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release, class Pace = NoPace,
-          class Out = GemmParams>
+// into C instead of storing (fp32). `pre`, if not null, is this warp's block of
+// a stream-K workspace (column group g of lane l at pre[(g·32 + l)·4 ..]),
+// added to the accumulator before the conversion.
+template <OutKind OK, int EPI_CHUNKS, int SLAB_BYTES, int SLOTS, class Release, class Pace = NoPace>
 __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_t* slab_pair, int& store_count,
-                                                  uint32_t tbase, int lane, int col_base, int row0, const Out& p,
-                                                  Release release, bool add = false, Pace pace = Pace(),
-                                                  const float* pre = nullptr) {
+                                                  uint32_t tbase, int lane, int col_base, int row0,
+                                                  const GemmParams& p, Release release, bool add = false,
+                                                  Pace pace = Pace(), const float* pre = nullptr) {
     constexpr int COLS = OK == OutKind::BF16 ? 64 : 32;   // TMEM columns per chunk
     constexpr int OUT_ES = OK == OutKind::BF16 ? 2 : 4;
     uint32_t buf[2][COLS];
@@ -530,10 +522,11 @@ __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_
             release();
         }
         if (pre) {
-            const float4* src = reinterpret_cast<const float4*>(pre + c * COLS);
+            // (read at L2: another SM wrote the block in this launch)
+            const float4* src = reinterpret_cast<const float4*>(pre) + c * (COLS / 4) * 32 + lane;
 #pragma unroll
             for (int j = 0; j < COLS / 4; ++j) {
-                const float4 w = src[j];
+                const float4 w = __ldcg(src + j * 32);
                 cur[4 * j + 0] = __float_as_uint(__uint_as_float(cur[4 * j + 0]) + w.x);
                 cur[4 * j + 1] = __float_as_uint(__uint_as_float(cur[4 * j + 1]) + w.y);
                 cur[4 * j + 2] = __float_as_uint(__uint_as_float(cur[4 * j + 2]) + w.z);
@@ -552,8 +545,46 @@ __device__ __forceinline__ void drain_accumulator(const CUtensorMap* tmC, uint8_
             for (int i = 0; i < 32; ++i) v[i] = cur[i];
         }
         pace(c);
-        store_slab<SLAB_BYTES, OUT_ES, SLOTS, false, Out>(tmC, slab_pair, store_count, v, lane,
-                                                          col_base + c * (128 / OUT_ES), row0, p, add);
+        store_slab<SLAB_BYTES, OUT_ES, SLOTS>(tmC, slab_pair, store_count, v, lane, col_base + c * (128 / OUT_ES),
+                                              row0, p, add);
+    }
+}
+
+// Drains one TMEM accumulator (this warp's 32 lanes × 32·EPI_CHUNKS fp32 columns)
+// into its block of a stream-K workspace (the layout `pre` of drain_accumulator
+// reads), with plain 16-byte stores straight from registers: each store of the
+// warp covers 512 contiguous bytes. `add`: add the block's values first (an
+// earlier piece wrote them). `release()` as in drain_accumulator.
+template <int EPI_CHUNKS, class Release>
+__device__ __forceinline__ void drain_to_workspace(uint32_t tbase, int lane, float* blk, Release release,
+                                                   bool add) {
+    uint32_t buf[2][32];
+    __syncwarp();   // tcgen05.ld is warp-collective
+    ptx::tmem_ld_32x32b_x32(tbase, buf[0]);
+#pragma unroll
+    for (int c = 0; c < EPI_CHUNKS; ++c) {
+        uint32_t(&cur)[32] = buf[c & 1];
+        ptx::tmem_ld_wait(cur);
+        if (c + 1 < EPI_CHUNKS) {
+            __syncwarp();
+            ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, buf[(c + 1) & 1]);
+        } else {
+            release();
+        }
+        float4* dst = reinterpret_cast<float4*>(blk) + c * 8 * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 v = make_float4(__uint_as_float(cur[4 * j]), __uint_as_float(cur[4 * j + 1]),
+                                   __uint_as_float(cur[4 * j + 2]), __uint_as_float(cur[4 * j + 3]));
+            if (add) {
+                const float4 w = __ldcg(dst + j * 32);
+                v.x += w.x;
+                v.y += w.y;
+                v.z += w.z;
+                v.w += w.w;
+            }
+            __stcg(dst + j * 32, v);
+        }
     }
 }
 

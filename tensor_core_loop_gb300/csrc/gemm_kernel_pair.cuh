@@ -214,8 +214,7 @@ __device__ __forceinline__ void spin_ns(unsigned long long ns) {
 template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS, InKind IK>
 __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -528,20 +527,19 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                 };
                 if constexpr (OK == OutKind::BF16) {
                     if (flag) {
-                        // bf16 C, split tile: the pieces' fp32 sums meet in the workspace
-                        // (stored by piece 0, added by the next ones in piece order); the
-                        // last piece adds its workspace rows and rounds once into C
+                        // bf16 C, split tile: the pieces' fp32 sums meet in this warp's
+                        // workspace block (stored by piece 0, added by the next ones in piece
+                        // order); the last piece adds the block and rounds once into C
                         const int wrow0 = ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + static_cast<int>(rank)) *
                                               C::ROWS + q * 32;
+                        float* blk = p.sk_ws + static_cast<long long>(wrow0) * C::BN;
                         if (U.piece + 1 < p.sk_pieces) {
-                            const OutView w{p.sk_ws, C::BN, C::BN, p.sk_ws_rows};
-                            drain_accumulator<OutKind::F32, C::BN / 32, C::SLAB_BYTES, C::EPI_SLOTS>(
-                                &tmW, slab_pair, store_count, tbase, lane, 0, wrow0, w, release, U.piece > 0);
+                            drain_to_workspace<C::BN / 32>(tbase, lane, blk, release, U.piece > 0);
                             hand_over(flag, U);
                         } else {
                             drain_accumulator<OK, C::EPI_CHUNKS, C::SLAB_BYTES, C::EPI_SLOTS>(
                                 &tmC, slab_pair, store_count, tbase, lane, nb * C::BN, row0, p, release, false,
-                                NoPace(), p.sk_ws + static_cast<long long>(wrow0 + lane) * C::BN);
+                                NoPace(), blk);
                         }
                         continue;
                     }

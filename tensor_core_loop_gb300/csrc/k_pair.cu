@@ -50,7 +50,7 @@ cudaError_t launch_pair(const LaunchArgs& a) {
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS, PAIRS>(a.grid, a.stream, attr, a.pdl);
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, a.tmA, a.tmB, a.tmC, a.tmW,
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, a.tmA, a.tmB, a.tmC,
                               a.p);
 }
 

@@ -19,7 +19,6 @@ struct LaunchArgs {
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
     bool pdl;   // programmatic dependent launch
     CUtensorMap tmA, tmB, tmC;
-    CUtensorMap tmW;   // two-SM kernel, bf16 C with a stream-K tail: the fp32 workspace (else a copy of tmC)
     GemmParams p;
     int grid;
     cudaStream_t stream;

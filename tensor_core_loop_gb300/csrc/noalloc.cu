@@ -125,7 +125,6 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.debug_sk_stall = 0;
     p.sk_ws = nullptr;
     p.sk_ws_rows = 0;
-    a.tmW = a.tmC;
 
     if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
                           {B, ldb, reinterpret_cast<uint16_t*>(b2), ldb2, K, N, 0}, sms, stream) != cudaSuccess) {

@@ -248,8 +248,7 @@ constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed whe
 // `pieces` K ranges so that the otherwise idle pairs share them.
 // want: 0 automatic, 1 never, s >= 2 exactly s pieces (TCL_ERR_CONFIG if that
 // does not fit). Fills *sk_tiles = 0 when there is no stream-K tail.
-int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_tiles, int* sk_pieces,
-                   int min_kb = kMinKbForSk) {
+int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_tiles, int* sk_pieces) {
     *sk_tiles = 0;
     *sk_pieces = 1;
     const long long rem = tiles % pairs;
@@ -261,7 +260,7 @@ int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_til
         return TCL_OK;
     }
     const int s = static_cast<int>(std::min<long long>({kMaxSkPieces, pairs / rem, num_kb / kMinKbPerPiece}));
-    if (s >= 2 && rem <= kMaxSkTiles && num_kb >= min_kb) {
+    if (s >= 2 && rem <= kMaxSkTiles && num_kb >= kMinKbForSk) {
         *sk_tiles = static_cast<int>(rem);
         *sk_pieces = s;
     }
@@ -435,10 +434,11 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         // Stream-K pieces wait on one another, so every pair of the grid must be
         // resident at once: the grid never exceeds the resident clusters here.
         if (sk_capable && !(cfg && cfg->one_cta_per_tile)) {
-            // (a bf16 C pays for its workspace round trip: measured on GB300 at 4096²×2048,
-            // 44.2 µs with a tail against 41.6 without; at ×4096 the tail wins, 76.7 vs 77.5)
+            // (a bf16 C adds its workspace round trip, yet the same threshold holds: measured
+            // on GB300 at 4096², the tail against none at K = 2048 42.2 vs 42.2 µs, at 3072
+            // 58.3 vs 59.7, at 4096 75.7 vs 78.1)
             const int st = stream_k_split(pl->num_tiles, pl->grid / cl, pl->num_kb, want_sk, &pl->sk_tiles,
-                                          &pl->sk_pieces, ok == OutKind::BF16 ? 2 * kMinKbForSk : kMinKbForSk);
+                                          &pl->sk_pieces);
             if (st) return st;
             if (pl->sk_tiles * cpairs > kMaxSkTiles) {   // the progress flags hold kMaxSkTiles tiles
                 if (want_sk > 1) return TCL_ERR_CONFIG;

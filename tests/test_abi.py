@@ -167,6 +167,8 @@ def test_planner_stream_k(L):
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1024, cfg)
     assert (p["bn"], p["sk_tiles"]) == (224, 0)
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2048, cfg)["sk_tiles"] == 28
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 2048, cfg)["sk_tiles"] == 28
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 1024, cfg)["sk_tiles"] == 0
     for bad in (tcl.Config(max_ctas=8, cta_pair=2, stream_k=5),       # more than 4 pieces
                 tcl.Config(max_ctas=8, cta_pair=1, stream_k=2),       # one-SM kernel
                 tcl.Config(max_ctas=4, cta_pair=2, stream_k=3),       # 1 tail tile × 3 pieces > 2 pairs

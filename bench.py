@@ -535,6 +535,14 @@ def run_peak(args):
                      "gemm_issue_loop": bool(flags & 8),
                      "flop_per_clk_per_sm": round(rate, 1), "cycles_per_mma": round(max(cyc) / 16384, 2),
                      "tflops_all_sms": round(flops / (ms * 1e-3) / 1e12, 1), "sms": sms})
+    # the warp-level mma.sync forms the pages' kernels use: int8 m16n8k32 (the only int8
+    # tensor instruction sm_103a has) and bf16 m16n8k16
+    for kind, flags, name, ops in ((2, 0, "int8 mma.sync m16n8k32", 8192), (0, 128, "bf16 mma.sync m16n8k16", 4096)):
+        tcl.mma_peak(kind, 128, 0, iters=512, flags=flags)
+        cyc, rate, ms = tcl.mma_peak(kind, 128, 0, iters=16384, flags=flags)
+        total = 64.0 * 16384 * ops * sms
+        rows.append({"peak": name, "op_per_clk_per_sm": round(rate, 1),
+                     "tops_all_sms": round(total / (ms * 1e-3) / 1e12, 1), "sms": sms})
     clocks = sampler.stop()
     for r in rows:
         r["clocks"] = clocks

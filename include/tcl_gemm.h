@@ -293,7 +293,13 @@ TCL_API int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config
  * stage holds it) instead of 16 K-rows (2 KB apart); bit 3: per group of
  * MMAs, the rest of a GEMM issue loop (an mbarrier wait, a tcgen05 fence, a
  * commit); bit 4: of those, the wait and fence only; bit 5: the commit only;
- * bit 6: groups of 8 MMAs instead of 4 (iters then a multiple of 8). */
+ * bit 6: groups of 8 MMAs instead of 4 (iters then a multiple of 8).
+ * Warp-level MMA instead (in_kind 2: int8 m16n8k32 → int32, the only int8
+ * tensor-core instruction sm_103a has; in_kind 0 with flags = 128: bf16
+ * m16n8k16 → fp32; n and b_mn are then ignored but must be valid, b_mn 0):
+ * 8 warps per CTA, each `iters` rounds of 8 independent mma.sync on register
+ * operands; cycles[blockIdx] = %clock64 over the loop, and
+ * ops/clk/SM = 64·iters·(8192 for int8, 4096 for bf16) / cycles. */
 TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int iters, int grid,
                          unsigned long long* cycles, cudaStream_t stream);
 

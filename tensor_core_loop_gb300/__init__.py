@@ -148,7 +148,8 @@ def plan(in_kind: int, out: int, M: int, N: int, K: int, cfg: Config | None = No
 def mma_peak(in_kind: int = IN_BF16, n: int = 256, b_mn: int = 0, iters: int = 4096, grid: int | None = None,
              flags: int = 0):
     """Runs the tensor-pipe probe on every SM; returns (cycles per CTA as a list, flop/clk/SM of the
-    slowest CTA, elapsed ms of the launch measured with CUDA events)."""
+    slowest CTA, elapsed ms of the launch measured with CUDA events). ``in_kind=IN_S8`` (or
+    ``flags=128`` with bf16) times the warp-level ``mma.sync`` forms instead."""
     import torch
     grid = grid or num_sms()
     cyc = torch.zeros(grid, dtype=torch.int64, device="cuda")
@@ -161,9 +162,12 @@ def mma_peak(in_kind: int = IN_BF16, n: int = 256, b_mn: int = 0, iters: int = 4
         raise TclError(st, "tcl_mma_peak")
     e1.synchronize()
     c = cyc.cpu().tolist()
-    k = 16 if in_kind == IN_BF16 else 8
     worst = max(c) if min(c) > 0 else 0
-    rate = 2.0 * 128 * n * k * iters / worst if worst else 0.0
+    if in_kind == IN_S8 or flags & 128:   # warp-level mma.sync: 8 warps × 8 chains × iters per CTA
+        rate = 64.0 * iters * (8192 if in_kind == IN_S8 else 4096) / worst if worst else 0.0
+    else:
+        k = 16 if in_kind == IN_BF16 else 8
+        rate = 2.0 * 128 * n * k * iters / worst if worst else 0.0
     return c, rate, e0.elapsed_time(e1)
 
 

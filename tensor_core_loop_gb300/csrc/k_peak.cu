@@ -114,6 +114,56 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int flags, 
     }
 }
 
+// Warp-level MMA (mma.sync), the instruction the pages' kernels are built on:
+// 8 warps per CTA, each `iters` rounds of eight independent MMAs on register
+// operands, no loads. S8: m16n8k32 int8 → int32, the only int8 tensor-core
+// instruction sm_103a accepts (8192 ops each); else m16n8k16 bf16 → fp32 (4096
+// flop each). cycles[blockIdx] = %clock64 from the first issue to the last.
+constexpr int kWarpMmaWarps = 8, kWarpMmaChains = 8;
+template <bool S8>
+__global__ void __launch_bounds__(32 * kWarpMmaWarps, 1) warp_mma_peak_kernel(int iters, unsigned long long* cycles) {
+    uint32_t a[4], b[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = ((threadIdx.x + 7u * i) * 2654435761u >> 8) & (S8 ? 0x3F3F3F3Fu : 0x007F007Fu);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) b[i] = ((threadIdx.x + 5u * i) * 40503u >> 4) & (S8 ? 0x1F1F1F1Fu : 0x007F007Fu);
+    if (!S8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] |= 0x3F003F00u;   // bf16 values in [0.5, 1)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) b[i] |= 0x3F003F00u;
+    }
+    uint32_t acc[kWarpMmaChains][4] = {};
+    __syncthreads();
+    const uint64_t t0 = ptx::clock64();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < kWarpMmaChains; ++j) {
+            if constexpr (S8)
+                asm volatile(
+                    "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                    "{%0,%1,%2,%3};"
+                    : "+r"(acc[j][0]), "+r"(acc[j][1]), "+r"(acc[j][2]), "+r"(acc[j][3])
+                    : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+            else
+                asm volatile(
+                    "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                    "{%0,%1,%2,%3};"
+                    : "+r"(acc[j][0]), "+r"(acc[j][1]), "+r"(acc[j][2]), "+r"(acc[j][3])
+                    : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+        }
+    }
+    __syncthreads();
+    const uint64_t t1 = ptx::clock64();
+    if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+    if (iters < 0) {   // never (iters >= 8): keeps the sums live for the compiler
+        uint32_t x = 0;
+#pragma unroll
+        for (int j = 0; j < kWarpMmaChains; ++j) x ^= acc[j][0] ^ acc[j][1] ^ acc[j][2] ^ acc[j][3];
+        cycles[blockIdx.x] = x;
+    }
+}
+
 template <int N, bool TF32, bool B_MN>
 cudaError_t launch_peak(int iters, int flags, int grid, unsigned long long* cycles, unsigned int* status,
                         cudaStream_t stream) {
@@ -147,17 +197,26 @@ extern "C" TCL_API int tcl_mma_peak(int in_kind, int n, int b_mn, int flags, int
                                     unsigned long long* cycles, cudaStream_t stream) {
     if (!cycles) return TCL_ERR_NULL;
     if (iters < 8 || iters % 4 || grid < 1 || (n != 128 && n != 192 && n != 224 && n != 256) ||
-        (in_kind != 0 && in_kind != 1) ||
-        (b_mn != 0 && b_mn != 1) || (in_kind == 1 && b_mn))
+        (in_kind != 0 && in_kind != 1 && in_kind != 2) ||
+        (b_mn != 0 && b_mn != 1) || (in_kind != 0 && b_mn))
         return TCL_ERR_DIMS;
     static_assert(kPeakSmem <= kPeakRequest, "probe fits its shared memory request");
-    if (flags < 0 || flags > 127 || ((flags & 64) && iters % 8)) return TCL_ERR_CONFIG;
+    const bool warp_mma = in_kind == 2 || (flags & 128);
+    if (flags < 0 || flags > 255 || ((flags & 64) && iters % 8) || (warp_mma && (flags & 127)) ||
+        (in_kind == 1 && (flags & 128)))
+        return TCL_ERR_CONFIG;
     int dev = 0, sms = 0;
     unsigned int* status = nullptr;
     int st = device_context(&dev, &sms, &status);
     if (st) return st;
     cudaError_t err;
-    if (in_kind == 1)
+    if (warp_mma) {
+        if (in_kind == 2)
+            warp_mma_peak_kernel<true><<<grid, 32 * kWarpMmaWarps, 0, stream>>>(iters, cycles);
+        else
+            warp_mma_peak_kernel<false><<<grid, 32 * kWarpMmaWarps, 0, stream>>>(iters, cycles);
+        err = cudaGetLastError();
+    } else if (in_kind == 1)
         err = launch_peak_n<true, false>(n, iters, flags, grid, cycles, status, stream);
     else if (b_mn)
         err = launch_peak_n<false, true>(n, iters, flags, grid, cycles, status, stream);

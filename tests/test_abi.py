@@ -89,6 +89,21 @@ def test_gemm_tf32_and_s8_reject(L):
     assert L.gemm_s8_static(64, 64, 64, P, 64, P, 64, P + 4, 64, None) == 4
 
 
+def test_mma_peak_rejects(L):
+    # (a real host buffer: every call here must return before any launch)
+    buf = (ctypes.c_ulonglong * 4)()
+    cyc = ctypes.addressof(buf)
+    assert L.tcl_mma_peak(0, 256, 0, 0, 4096, 1, None, None) == 1          # no cycles buffer
+    assert L.tcl_mma_peak(3, 256, 0, 0, 4096, 1, cyc, None) == 2           # unknown kind
+    assert L.tcl_mma_peak(2, 256, 1, 0, 4096, 1, cyc, None) == 2           # int8 warp MMA: no B major-ness
+    assert L.tcl_mma_peak(1, 256, 1, 0, 4096, 1, cyc, None) == 2           # TF32: K-major B only
+    assert L.tcl_mma_peak(0, 100, 0, 0, 4096, 1, cyc, None) == 2           # N not built
+    assert L.tcl_mma_peak(2, 128, 0, 1, 4096, 1, cyc, None) == 8           # warp MMA takes no other flag
+    assert L.tcl_mma_peak(0, 128, 0, 129, 4096, 1, cyc, None) == 8
+    assert L.tcl_mma_peak(1, 128, 0, 128, 4096, 1, cyc, None) == 8         # no TF32 warp MMA
+    assert L.tcl_mma_peak(0, 128, 0, 256, 4096, 1, cyc, None) == 8         # unknown flag bit
+
+
 def test_plan_without_device(L):
     cfg = tcl.Config(max_ctas=152)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=1))

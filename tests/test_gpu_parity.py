@@ -214,6 +214,7 @@ def test_bf16_pair_kernel_bf16_out(oracle_mod, M, N, K):
 
 @pytest.mark.parametrize("M,N,K,pieces,pairs", [
     (768, 768, 4096, 0, 1),     # automatic (64 k-blocks): the 9th tile in 4 pieces, three fp32 partials
+    (768, 768, 2048, 0, 1),     # automatic at 32 k-blocks (the bf16 C's tail threshold): 4 pieces of 8
     (768, 768, 2048, 2, 1),
     (768, 768, 2048, 3, 1),
     (700, 750, 1000, 4, 1),     # ragged M, N: the last piece rounds and stores only what lies in C

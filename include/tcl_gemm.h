@@ -19,7 +19,8 @@
  *   the caller). The library keeps a per-device cache of TMA descriptors and
  *   a per-device scratch buffer (repacked operands for gemm_s8 and gemm_tf32,
  *   copies of operands or outputs off the 16-byte grid, split-K partial
- *   tiles for small grids) that it grows on demand (cudaMalloc, at least
+ *   tiles for small grids, the fp32 partial sums of a bf16 C's stream-K
+ *   tail) that it grows on demand (cudaMalloc, at least
  *   doubling; an outgrown buffer is kept, since enqueued or graph-captured
  *   work may still use it) and frees, with the outgrown ones, in
  *   tcl_shutdown(). Every call on a device shares that buffer: calls whose

@@ -460,6 +460,18 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
             tile_coords(U.tile, p, mb, nb);
             mb = mb * PAIRS + static_cast<int>(pidx);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
+            // bf16 C, split tile: this warp's block of the fp32 workspace (32 rows × BN)
+            [[maybe_unused]] float* blk = nullptr;
+            if constexpr (OK == OutKind::BF16) {
+                if (U.sk_index >= 0) {
+                    const int wrow0 = ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + static_cast<int>(rank)) *
+                                          C::ROWS + q * 32;
+                    blk = p.sk_ws + static_cast<long long>(wrow0) * C::BN;
+                    // a later piece reads the block after its mainloop: have it in L2 by then
+                    // (written near the start of the launch, it may have left L2 since)
+                    if (U.piece > 0 && lane == 0) ptx::prefetch_l2_bulk(blk, 32 * C::BN * 4);
+                }
+            }
             [[maybe_unused]] int32_t iacc[(OK == OutKind::S32) ? CW : 1];
             if constexpr (OK == OutKind::S32) {
 #pragma unroll
@@ -530,9 +542,6 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                         // bf16 C, split tile: the pieces' fp32 sums meet in this warp's
                         // workspace block (stored by piece 0, added by the next ones in piece
                         // order); the last piece adds the block and rounds once into C
-                        const int wrow0 = ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + static_cast<int>(rank)) *
-                                              C::ROWS + q * 32;
-                        float* blk = p.sk_ws + static_cast<long long>(wrow0) * C::BN;
                         if (U.piece + 1 < p.sk_pieces) {
                             drain_to_workspace<C::BN / 32>(tbase, lane, blk, release, U.piece > 0);
                             hand_over(flag, U);

@@ -127,6 +127,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// A hint to the copy engine: bring `bytes` (a multiple of 16) of global memory
+// starting at the 16-byte aligned `p` into L2. It moves no data anywhere else
+// and orders nothing.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 // Programmatic dependent launch. wait: block until the grids this one depends
 // on in the stream have completed and their memory is visible (a no-op when
 // the launch did not ask for programmatic serialisation). launch_dependents:

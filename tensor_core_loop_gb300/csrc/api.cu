@@ -367,9 +367,11 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             // k-blocks deep: its time is then the latency of its loads, and
             // narrow tiles keep 6 of them in flight instead of 4 (measured on
             // GB300 at 4096²×256: 16.7 against 17.5 µs; at ×512 wide tiles win).
+            // A bf16 C halves the stores that follow, and there the wide tiles
+            // win at 4 k-blocks too (4096²×256: 12.5 against 12.9 µs).
             const long long tiles256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256);
             const int kblocks = (K + bk - 1) / bk;
-            bn = (tiles256 >= sms && kblocks > 4) ? 256 : 128;
+            bn = (tiles256 >= sms && (kblocks > 4 || ok == OutKind::BF16)) ? 256 : 128;
         }
     }
     if (bn != 128 && bn != 256 && !(pair && bn == 224)) return TCL_ERR_CONFIG;

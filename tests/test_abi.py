@@ -135,6 +135,9 @@ def test_plan_without_device(L):
     # 16 narrow tiles for 152 SMs: K is cut into 8 ranges of 8 k-blocks (split-K)
     assert p["cta_pair"] == 1 and p["bn"] == 128 and p["num_tiles"] == 16
     assert p["splits"] == 8 and p["grid"] == 128 and p["workspace_bytes"] == 8 * 512 * 512 * 4
+    # 4 k-blocks on many tiles: narrow tiles for an fp32 C, wide ones for a bf16 C
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 256, cfg)["bn"] == 128
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 256, cfg)["bn"] == 256
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)     # 4 k-blocks: too short to split
     assert p["splits"] == 1 and p["grid"] == 16 and p["workspace_bytes"] == 0
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 8192, cfg)

@@ -184,16 +184,19 @@ class ClockSampler:
             except ValueError:
                 continue
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        loaded = [r for r in rows if r["power"] > 300.0] or rows
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
+        # a sample counts as under load when the board draws more than 300 W (idle is ~150 W);
+        # a timed region shorter than the sampling interval may contain none, and then the
+        # nvidia-smi clock is reported as unknown rather than taken from idle samples
+        loaded = [r for r in rows if r["power"] > 300.0]
         sms = sorted(r["sm"] for r in loaded)
         reasons = set()
-        for r in loaded:
+        for r in rows:   # a throttle reason seen anywhere in the window counts
             for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
                               ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["max"] for r in rows),
+        return {"sm_mhz": sms[len(sms) // 2] if sms else None, "sm_max_mhz": max(r["max"] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
                 "power_w_max": max(r["power"] for r in rows)}
 
@@ -216,6 +219,53 @@ def cpu_oracle_sample(target_s=12.0, max_rows=4096):
     oracle.gemm_bf16(ab, bb, rows=(rows, rows + more), with_abs=False)
     dt = time.perf_counter() - t0
     return 2.0 * more * N * K / dt / 1e12, more, dt, cores
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform module)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_per_config(target_s=3.0):
+    """The CPU oracle timed on each workload, all host cores: the bf16 256³ case whole, and
+    whole-row samples of the int8 and TF32 4096³ cases (rows scaled so each takes about
+    target_s seconds). Seconds and GFLOP/s (GOP/s for int8) per workload."""
+    import oracle
+    from tensor_core_loop_gb300 import inputs
+    oracle.build()
+    res = {}
+    a, b = inputs.bf16_pair(256, 256, 256, seed=0)
+    ab, bb = inputs.bf16_bits(a), inputs.bf16_bits(b)
+    secs = min(_timed(lambda: oracle.gemm_bf16(ab, bb, with_abs=False)) for _ in range(3))
+    res["bf16 256^3 (whole C)"] = {"seconds": secs, "gflops": 2.0 * 256 ** 3 / secs / 1e9}
+    cores = oracle.num_threads()
+    for name, pair, fn in (("int8 4096^3", inputs.s8_pair, lambda x, y, r: oracle.gemm_s8(x, y, rows=r)),
+                           ("tf32 4096^3", inputs.tf32_pair,
+                            lambda x, y, r: oracle.gemm_tf32(x, y, rows=r, with_abs=False))):
+        x, y = pair(M, N, K, seed=0)
+        x, y = x.numpy(), y.numpy()
+        rows = max(4, cores)
+        dt = _timed(lambda: fn(x, y, (0, rows)))
+        more = max(cores, min(M - rows, int(rows * target_s / max(dt, 1e-3)) // cores * cores))
+        dt = _timed(lambda: fn(x, y, (rows, rows + more)))
+        res[name] = {"seconds": dt, "rows": more, "gflops": 2.0 * more * N * K / dt / 1e9,
+                     "sample": f"{more} of {M} rows of C (all {N} columns, full K={K})"}
+    return res
 
 
 def run_reference(args, rank, world):
@@ -768,7 +818,10 @@ def main():
         tf, rows, secs, cores = cpu_oracle_sample()
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                "sample": f"{rows} of {M} rows of C (all {N} columns, full K={K}), {secs:.1f} s",
-               "one_core_256": oracle_one_core_256()}
+               "seconds": secs, "gflops": tf * 1e3,
+               "host_cpu_count": os.cpu_count(), "cpu_model": cpu_model(),
+               "one_core_256": oracle_one_core_256(),
+               "per_config": oracle_per_config()}
 
     if world > 1:
         dist.barrier()
@@ -790,7 +843,17 @@ def main():
     max_mhz = clocks.get("sm_max_mhz") if clocks else None
     max_peak = (sms * rate * max_mhz * 1e6 / 1e12) if max_mhz else None
     if clocks is not None:
+        # the primary clock is the one measured inside the GEMM on the timed workload; the
+        # nvidia-smi median (samples drawing > 300 W during the timed region) sits beside
+        # it and is null when the region was too short to be sampled under load
+        clocks["sm_mhz_nvidia_smi"] = clocks.get("sm_mhz")
         clocks["sm_mhz_in_kernel"] = kernel_mhz
+        if kernel_mhz:
+            clocks["sm_mhz"] = round(kernel_mhz, 1)
+            clocks["sm_mhz_source"] = ("in kernel: CTA 0's %clock64 over %globaltimer, median of back-to-back "
+                                       "launches of the timed workload")
+        else:
+            clocks["sm_mhz_source"] = "nvidia-smi, samples under load during the timed region"
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -157,11 +157,6 @@ typedef struct {
                                       handshake) overlaps the end of the previous kernel in the
                                       stream; they read and write global memory only after that
                                       kernel has completed. 1: plain stream order */
-    int cluster_pairs;             /* two-SM kernel: 0 automatic; 1 one CTA pair per cluster; 2 two
-                                      pairs per cluster on the two 256-row tiles of a 512-row couple,
-                                      each CTA fetching half of its B operand from L2 and multicasting
-                                      it to the CTA in the same place of the other pair (half the L2
-                                      reads of B) */
     int debug_stream_k_stall;      /* test hook, 0 = off. 1: the first stream-K piece of the first
                                       split tile never hands its tile over, so the next piece's
                                       bounded wait must run out (device status code 5) */
@@ -268,8 +263,6 @@ typedef struct {
     unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
     int sk_tiles;                   /* tail tiles computed stream-K (0: none) */
     int sk_pieces;                  /* K ranges per stream-K tile */
-    int cluster_pairs;              /* two-SM kernel: CTA pairs per cluster (0: one-SM kernel); with 2,
-                                       num_tiles and sk_tiles count 512-row couples of tiles */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

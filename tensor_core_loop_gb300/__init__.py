@@ -66,7 +66,6 @@ class Config(ctypes.Structure):
         ("debug_skip_kblock", ctypes.c_int),
         ("stream_k", ctypes.c_int),
         ("serial_launch", ctypes.c_int),
-        ("cluster_pairs", ctypes.c_int),
         ("debug_stream_k_stall", ctypes.c_int),
     ]
 
@@ -85,7 +84,6 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_ulonglong),
         ("sk_tiles", ctypes.c_int),
         ("sk_pieces", ctypes.c_int),
-        ("cluster_pairs", ctypes.c_int),
     ]
 
 

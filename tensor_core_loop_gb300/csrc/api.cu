@@ -332,28 +332,22 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     // once), into an fp32 workspace that the last piece adds before rounding
     const bool sk_capable = ok == OutKind::F32 || ok == OutKind::S32 || ok == OutKind::BF16;
     if (want_sk < 0 || want_sk > kMaxSkPieces || (want_sk > 1 && (!pair || !sk_capable))) return TCL_ERR_CONFIG;
-    // CTA pairs per cluster: 2 = two pairs on tiles stacked in M sharing B by multicast
-    const int want_cp = cfg ? cfg->cluster_pairs : 0;
-    if (want_cp < 0 || want_cp > 2 || (want_cp == 2 && (want_pair == 1 || ok == OutKind::S32)))
-        return TCL_ERR_CONFIG;
-    const int cpairs = (pair && want_cp == 2) ? 2 : 1;
     if (pair) {
         if (bn == 0) {
             // Pair tile width: the fewest SM cycles on the busiest pair of SMs,
             // whole tiles only or with a stream-K tail (fp32 C can also use 224).
             bn = pair_bn;
             if (ok == OutKind::F32 && want_sk <= 1) {   // a requested stream-K split keeps 256
-                const int pairs = std::max(1, (cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms) / (2 * cpairs));
+                const int pairs = std::max(1, (cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms) / 2);
                 const int kb = (K + bk - 1) / bk;
                 auto cost = [&](int w, long long kb_cycles) {
-                    const long long t = static_cast<long long>(((M + 255) / 256 + cpairs - 1) / cpairs) *
-                                        ((N + w - 1) / w);
+                    const long long t = static_cast<long long>((M + 255) / 256) * ((N + w - 1) / w);
                     int skt = 0, skp = 1;
                     if (stream_k_split(t, pairs, kb, want_sk, &skt, &skp)) skt = 0;
                     return pair_cost(t, pairs, kb, kb_cycles, skt, skp);
                 };
-                const int want_st = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, 224, prod, cpairs);
-                if (find_variant(ik, ok, 224, want_st, prod, cpairs) &&
+                const int want_st = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, 224, prod, 1);
+                if (find_variant(ik, ok, 224, want_st, prod, 1) &&
                     cost(224, kPairKbCycles224) < cost(256, kPairKbCycles256))
                     bn = 224;
             }
@@ -377,7 +371,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     if (bn != 128 && bn != 256 && !(pair && bn == 224)) return TCL_ERR_CONFIG;
     const int slots = cfg ? cfg->epi_slots : 0;
     if (slots < 0 || (slots && !pair && slots != 2)) return TCL_ERR_CONFIG;
-    const int pv = pair ? cpairs : 0;   // the variant table's pairs-per-cluster (0: one-SM kernel)
+    const int pv = pair ? 1 : 0;   // the variant table's kernel kind (1: two-SM kernel)
     int stages = cfg && cfg->stages ? cfg->stages : deepest_stages(ik, ok, bn, prod, pv, slots);
     const VariantInfo* v = find_variant(ik, ok, bn, stages, prod, pv, slots);
     if (!v) return TCL_ERR_CONFIG;
@@ -389,7 +383,6 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->smem = v->smem_bytes;
     const int bm = pair ? 2 * kBM : kBM;
     pl->tiles_m = (M + bm - 1) / bm;
-    if (cpairs == 2) pl->tiles_m = (pl->tiles_m + 1) / 2;   // couples of 256-row tiles, one per pair
     pl->tiles_n = (N + bn - 1) / bn;
     const long long tiles = static_cast<long long>(pl->tiles_m) * pl->tiles_n;
     if (tiles > 0x3FFFFFFFll) return TCL_ERR_DIMS;
@@ -428,7 +421,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->sk_pieces = 1;
     pl->sk_ws_rows = 0;
     if (pair) {
-        const int cl = 2 * cpairs;   // CTAs per cluster
+        const int cl = 2;   // CTAs per cluster: one pair
         int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / cl : pair_clusters(v);
         if (clusters < 1) return cfg && cfg->max_ctas > 0 ? TCL_ERR_CONFIG : TCL_ERR_LAUNCH;
         if (cfg && cfg->one_cta_per_tile) clusters = pl->num_tiles;
@@ -442,7 +435,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             const int st = stream_k_split(pl->num_tiles, pl->grid / cl, pl->num_kb, want_sk, &pl->sk_tiles,
                                           &pl->sk_pieces);
             if (st) return st;
-            if (pl->sk_tiles * cpairs > kMaxSkTiles) {   // the progress flags hold kMaxSkTiles tiles
+            if (pl->sk_tiles > kMaxSkTiles) {   // the progress flags hold kMaxSkTiles tiles
                 if (want_sk > 1) return TCL_ERR_CONFIG;
                 pl->sk_tiles = 0;
                 pl->sk_pieces = 1;
@@ -454,7 +447,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
                 pl->sk_pieces = 1;
             }
         }
-        if (ok == OutKind::BF16 && pl->sk_tiles) pl->sk_ws_rows = pl->sk_tiles * cpairs * 2 * kBM;
+        if (ok == OutKind::BF16 && pl->sk_tiles) pl->sk_ws_rows = pl->sk_tiles * 2 * kBM;
     } else if (want_sk > 1) {
         return TCL_ERR_CONFIG;
     } else if (cfg && cfg->one_cta_per_tile) {
@@ -496,7 +489,7 @@ int device_pair_clusters(DevState* ds, const VariantInfo* v) {
     }
     if (idx >= 16) return 0;
     if (ds->pair_clusters[idx] == 0)
-        ds->pair_clusters[idx] = pair_max_clusters(v->in, v->out, v->bn, v->stages, v->slots, v->pair);
+        ds->pair_clusters[idx] = pair_max_clusters(v->in, v->out, v->bn, v->stages, v->slots);
     return ds->pair_clusters[idx];
 }
 
@@ -1008,7 +1001,6 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->num_tiles = pl.num_tiles;
         plan->smem_bytes = pl.smem;
         plan->cta_pair = pl.pair ? 2 : 1;
-        plan->cluster_pairs = pl.pair;
         plan->splits = pl.splits;
         plan->producer = pl.prod;
         plan->workspace_bytes = static_cast<unsigned long long>(split_workspace(pl, M, N).bytes);

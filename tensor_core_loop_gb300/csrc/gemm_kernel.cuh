@@ -700,6 +700,16 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
             for (uint32_t j = first; j < it; ++j)
                 wait_drain(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
         }
+        if (ok && tracing && lane == 0) {
+            // The last STAGES k-blocks' stages are never reused, so the loop above never
+            // saw their MMAs finish: wait (bounded) for the same empty-barrier phases a
+            // reuse would have waited for, and stamp them.
+            const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+            for (uint32_t j = first; j < it && j < (uint32_t)p.trace_cap && !*abort_flag; ++j) {
+                wait_drain(empty0 + 8 * C::rel_slot(j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
+                p.trace[4 * j + 3] = ptx::clock64();
+            }
+        }
         __syncwarp();
     } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------ MMA issuer
@@ -763,6 +773,12 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                 if (!ok) break;
                 ptx::mma_commit_elected(accf0 + 8 * buf);      // accumulator ready for the epilogue
             }
+        }
+        if (ok && tracing && C::REL == 2 && it > 0) {
+            // slots are released in pairs: if the last k-block sat in an even slot, no commit
+            // releases it; one more lets the producer's trace see its MMAs finish
+            const uint32_t last = (s + STAGES - 1) % STAGES;
+            if (!(last & 1u)) ptx::mma_commit_elected(empty0 + 8 * (last | 1u));
         }
         if (!ok) {
             ptx::mma_commit_elected(drain_bar);

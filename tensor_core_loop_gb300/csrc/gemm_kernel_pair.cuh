@@ -14,12 +14,8 @@
 //     and commits empty[s] and acc_full[b] to both CTAs at once (multicast);
 //   * both CTAs' epilogues drain their own TMEM and release the accumulator
 //     on the leader's acc_empty[b] (8 arrivals: 4 warps × 2 CTAs).
-// With PAIRS = 2 a cluster holds two such pairs working on two tiles stacked
-// in M (same column of tiles, so the same B): each CTA fetches only one of the
-// two 64-column boxes of its B half from L2 and multicasts it to itself and
-// to the CTA in the same position of the other pair, halving the L2 reads of
-// B. A stage is then refilled only when both pairs' MMAs are done with it
-// (empty[s] takes one multicast commit from each leader).
+// Every TMA load brings a box into the issuing CTA's own shared memory; only
+// the MMA completions (tcgen05.commit) are signalled to both CTAs at once.
 // TF32 inputs (IK = TF32) take B K-major (the host transposes it): each CTA
 // then loads its half of B as one box of BN/2 rows × 128 B, 32 K values deep.
 // Exact integers (OK = S32, int8 widened to bf16) accumulate units of 1024 K
@@ -37,12 +33,10 @@
 
 namespace tcl {
 
-template <OutKind OK, int BN_, int STAGES_, int SLOTS_, int PAIRS_ = 1, InKind IK = InKind::BF16>
+template <OutKind OK, int BN_, int STAGES_, int SLOTS_, InKind IK = InKind::BF16>
 struct PairCfg {
-    static constexpr int PAIRS = PAIRS_;             // CTA pairs per cluster (2: B shared by multicast)
-    static constexpr int CL = 2 * PAIRS;             // CTAs per cluster
-    static constexpr int EMPTY_ARRIVALS = PAIRS;     // one multicast commit per pair leader
-    static constexpr uint16_t ALL = (1u << CL) - 1;  // multicast mask: every CTA of the cluster
+    static constexpr int CL = 2;                     // CTAs per cluster: one pair
+    static constexpr uint16_t ALL = 0x3;             // commit mask: both CTAs of the pair
     static constexpr int STAGES = STAGES_;
     static constexpr int BM = 256;                   // rows per pair tile (128 per SM)
     static constexpr int BN = BN_;                   // columns per pair tile (each SM supplies BN/2 of B)
@@ -87,17 +81,16 @@ struct PairCfg {
     static constexpr int REL = (BN <= 128 && STAGES >= 4 && STAGES % 2 == 0) ? 2 : 1;
     static __device__ __forceinline__ uint32_t rel_slot(uint32_t s) { return REL == 2 ? (s | 1u) : s; }
 
-    static_assert(OK != OutKind::S32 || (EPI_COLS_PER_WARP <= 128 && IK == InKind::BF16 && PAIRS == 1),
+    static_assert(OK != OutKind::S32 || (EPI_COLS_PER_WARP <= 128 && IK == InKind::BF16),
                   "exact integer mode: int32 sums of at most 128 columns per thread in registers");
     static_assert(BN % 32 == 0 && BN <= 256 && BN % EPI_COLS == 0, "pair tile width");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(2 * STAGES + 5 <= 28, "barrier area");
-    static_assert(PAIRS == 1 || (PAIRS == 2 && B_BOXES % 2 == 0), "two pairs split each B half's boxes");
     static_assert(KSUB == 4, "four MMAs per k-block");
     static_assert(B_MN || (B_BOX_N % 8 == 0 && B_BOX_N <= 256), "K-major B half: whole 8-row swizzle atoms");
 };
 
-// Raises the abort flag of every CTA of the cluster (addr: this CTA's flag).
+// Raises the abort flag of both CTAs of the pair (addr: this CTA's flag).
 struct AbortNet {
     uint32_t addr;
     int cl;
@@ -211,11 +204,11 @@ __device__ __forceinline__ void spin_ns(unsigned long long ns) {
     }
 }
 
-template <OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS, InKind IK>
-__global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THREADS, 1)
+template <OutKind OK, int BN, int STAGES, int SLOTS, InKind IK>
+__global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, IK>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -236,13 +229,12 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
     const int lane = threadIdx.x & 31;
     const uint32_t crank = ptx::cluster_ctarank();
     const uint32_t rank = crank & 1u;    // in the pair: 0 leader (issues the pair MMAs), 1 peer
-    const uint32_t pidx = crank >> 1;    // which pair of the cluster (its tile's row in the couple)
     const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full0 + 8 * s, 1);    // leader's: its producer's arrival + both CTAs' bytes
-            ptx::mbar_init(empty0 + 8 * s, C::EMPTY_ARRIVALS);   // each pair leader's multicast commit
+            ptx::mbar_init(empty0 + 8 * s, 1);   // the leader's multicast commit
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf0 + 8 * b, 1);    // the leader's multicast commit
@@ -273,8 +265,8 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
 
-    const uint32_t full_leader0 = ptx::mapa_shared(full0, crank & ~1u);
-    const uint32_t acce_leader0 = ptx::mapa_shared(acce0, crank & ~1u);
+    const uint32_t full_leader0 = ptx::mapa_shared(full0, 0u);
+    const uint32_t acce_leader0 = ptx::mapa_shared(acce0, 0u);
     const AbortNet peer_abort{ptx::smem_u32(const_cast<uint32_t*>(abort_flag)), C::CL};
     const int cluster = blockIdx.x / C::CL;
     const int clusters = gridDim.x / C::CL;
@@ -295,7 +287,6 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
             const PairUnit U = pair_unit(p, cluster, clusters, u);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
-            mb = mb * PAIRS + static_cast<int>(pidx);
             const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
             const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
@@ -323,21 +314,24 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
 #pragma unroll
                 for (int b = 0; b < C::B_BOXES; ++b) {
                     const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
-                    if constexpr (!C::B_MN) {
+                    if constexpr (!C::B_MN)
                         ptx::tma_load_2d_pair_elected(dst, &tmB, fb, kb * C::BK, col);   // K-major: (k, n)
-                    } else if constexpr (PAIRS == 1) {
+                    else
                         ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kb * C::BK);
-                    } else if ((b & 1) == static_cast<int>(pidx)) {
-                        // this box for both pairs: to the CTA in this position of each pair,
-                        // counted on each destination pair's leader barrier
-                        const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
-                        ptx::tma_load_2d_pair_mc_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kb * C::BK, mask);
-                    }
                 }
                 if (lane == 0) *progress = it + 1;
             }
         }
         if (!ok && lane == 0) spin_ns(200000);   // copies issued before the abort land within microseconds
+        if (ok && tracing && lane == 0) {
+            // stamp "MMAs done" for the last STAGES k-blocks, whose stages are never reused
+            // (the same empty-barrier phases a reuse would have waited for; bounded)
+            const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+            for (uint32_t j = first; j < it && j < (uint32_t)p.trace_cap && !*abort_flag; ++j) {
+                wait_drain(empty0 + 8 * C::rel_slot(j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
+                p.trace[4 * j + 3] = ptx::clock64();
+            }
+        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader CTA only)
@@ -392,7 +386,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                             ptx::mma_f16_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
                                                          bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
                                                          kb > kb0 ? 1u : 0u);
-                        // stage s (with s - 1, released in pairs) free once every pair's MMAs on it are done
+                        // stage s (with s - 1, released in pairs) free in both CTAs once these MMAs are done
                         if (C::REL == 1 || (s & 1u)) ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
                         if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
                         const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
@@ -400,9 +394,14 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
                         ph ^= wrap;
                     }
                     if (!ok) break;
-                    ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf,
-                                                           static_cast<uint16_t>(0x3u << (2 * pidx)));
+                    ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf, C::ALL);
                 }
+            }
+            if (ok && tracing && C::REL == 2 && it > 0) {
+                // slots released in pairs: release a last k-block left alone in an even slot,
+                // so that the producer's trace sees its MMAs finish
+                const uint32_t last = (s + STAGES - 1) % STAGES;
+                if (!(last & 1u)) ptx::mma_commit_pair_multicast_elected(empty0 + 8 * (last | 1u), C::ALL);
             }
             if (!ok) {
                 ptx::mma_commit_pair_multicast_elected(drain_bar, 0x1);
@@ -420,11 +419,9 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
         uint32_t unit = 0;
         uint32_t it_next = 0;   // the ring iteration at which the unit after this one starts
         bool ok = true;
-        // stream-K: this warp's rows of split tile (d, pidx), flags[d][pidx][rank][epilogue warp]
+        // stream-K: this warp's rows of split tile d, flags[d][rank][epilogue warp]
         auto sk_flag = [&](const PairUnit& U) -> uint32_t* {
-            return U.sk_index >= 0 ? p.sk_flags + ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + rank) *
-                                                      C::EPI_WARPS + (warp - 2)
-                                   : nullptr;
+            return U.sk_index >= 0 ? p.sk_flags + (U.sk_index * 2 + rank) * C::EPI_WARPS + (warp - 2) : nullptr;
         };
         // piece > 0: wait until the previous piece's sums are in C (or in the workspace)
         auto wait_turn = [&](uint32_t* flag, const PairUnit& U) {
@@ -458,14 +455,12 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>::THR
             it_next += static_cast<uint32_t>(U.kb_hi - U.kb_lo);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
-            mb = mb * PAIRS + static_cast<int>(pidx);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
             // bf16 C, split tile: this warp's block of the fp32 workspace (32 rows × BN)
             [[maybe_unused]] float* blk = nullptr;
             if constexpr (OK == OutKind::BF16) {
                 if (U.sk_index >= 0) {
-                    const int wrow0 = ((U.sk_index * PAIRS + static_cast<int>(pidx)) * 2 + static_cast<int>(rank)) *
-                                          C::ROWS + q * 32;
+                    const int wrow0 = (U.sk_index * 2 + static_cast<int>(rank)) * C::ROWS + q * 32;
                     blk = p.sk_ws + static_cast<long long>(wrow0) * C::BN;
                     // a later piece reads the block after its mainloop: have it in L2 by then
                     // (written near the start of the launch, it may have left L2 since)

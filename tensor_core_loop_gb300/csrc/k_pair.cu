@@ -1,5 +1,5 @@
 // Instantiates the two-SM (cta_group::2) GEMM variants and launches them as
-// clusters of one or two CTA pairs.
+// clusters of one CTA pair.
 #include "launch.cuh"
 
 namespace tcl {
@@ -8,9 +8,9 @@ namespace {
 // attr must hold two entries; pdl adds programmatic stream serialisation
 // (the kernel may start its set-up while the previous kernel in the stream
 // finishes; it waits for that kernel before touching global memory).
-template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr, bool pdl = false) {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, IK>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
@@ -30,38 +30,38 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
     return cfg;
 }
 
-template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS>
 cudaError_t prepare() {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, IK>;
     static bool done[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gemm_pair_kernel<OK, BN, STAGES, SLOTS, IK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES);
     if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return err;
 }
 
-template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS>
 cudaError_t launch_pair(const LaunchArgs& a) {
-    cudaError_t err = prepare<IK, OK, BN, STAGES, SLOTS, PAIRS>();
+    cudaError_t err = prepare<IK, OK, BN, STAGES, SLOTS>();
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS, PAIRS>(a.grid, a.stream, attr, a.pdl);
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, a.tmA, a.tmB, a.tmC,
+    cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS>(a.grid, a.stream, attr, a.pdl);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OK, BN, STAGES, SLOTS, IK>, a.tmA, a.tmB, a.tmC,
                               a.p);
 }
 
-template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS, int PAIRS>
+template <InKind IK, OutKind OK, int BN, int STAGES, int SLOTS>
 int max_clusters() {
-    using C = PairCfg<OK, BN, STAGES, SLOTS, PAIRS, IK>;
-    if (prepare<IK, OK, BN, STAGES, SLOTS, PAIRS>() != cudaSuccess) return 0;
+    using C = PairCfg<OK, BN, STAGES, SLOTS, IK>;
+    if (prepare<IK, OK, BN, STAGES, SLOTS>() != cudaSuccess) return 0;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS, PAIRS>(C::CL, 0, attr);
+    cudaLaunchConfig_t cfg = pair_config<IK, OK, BN, STAGES, SLOTS>(C::CL, 0, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS, PAIRS, IK>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<OK, BN, STAGES, SLOTS, IK>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -70,11 +70,10 @@ int max_clusters() {
 
 }  // namespace
 
-#define TCL_PAIR_CASE(IK, OK, BN, ST, SL, PR)                                                      \
-    if (a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL && \
-        a.pair == PR) {                                                                               \
+#define TCL_PAIR_CASE(IK, OK, BN, ST, SL)                                                           \
+    if (a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.slots == SL) { \
         *found = true;                                                                                \
-        return launch_pair<InKind::IK, OutKind::OK, BN, ST, SL, PR>(a);                               \
+        return launch_pair<InKind::IK, OutKind::OK, BN, ST, SL>(a);                                   \
     }
 
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
@@ -84,11 +83,11 @@ cudaError_t launch_group_pair(const LaunchArgs& a, bool* found) {
     return cudaErrorNotSupported;
 }
 
-#define TCL_PAIR_OCC(IK, OK, BN, ST, SL, PR)                                                            \
-    if (in == InKind::IK && out == OutKind::OK && bn == BN && stages == ST && slots == SL && pairs == PR) \
-        return max_clusters<InKind::IK, OutKind::OK, BN, ST, SL, PR>();
+#define TCL_PAIR_OCC(IK, OK, BN, ST, SL)                                                 \
+    if (in == InKind::IK && out == OutKind::OK && bn == BN && stages == ST && slots == SL) \
+        return max_clusters<InKind::IK, OutKind::OK, BN, ST, SL>();
 
-int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots, int pairs) {
+int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots) {
     TCL_GROUP_PAIR(TCL_PAIR_OCC)
     return 0;
 }

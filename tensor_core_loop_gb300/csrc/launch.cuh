@@ -15,7 +15,7 @@ struct LaunchArgs {
     int bn;
     int stages;
     int prod;   // PROD_TMA, PROD_SYNC or PROD_CPASYNC
-    int pair;   // two-SM kernel: CTA pairs per cluster (1, or 2 sharing B by multicast); 0: one-SM kernel
+    int pair;   // 1: two-SM kernel (one CTA pair per cluster); 0: one-SM kernel
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
     bool pdl;   // programmatic dependent launch
     CUtensorMap tmA, tmB, tmC;
@@ -32,9 +32,9 @@ cudaError_t launch_group_bf16_misc(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_sync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_bf16_cpasync(const LaunchArgs& a, bool* found);
 cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
-// Largest number of clusters (of `pairs` CTA pairs) of the given pair variant
-// that can be resident at once on the current device (0 on error).
-int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots, int pairs);
+// Largest number of CTA-pair clusters of the given pair variant that can be
+// resident at once on the current device (0 on error).
+int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 
 // int8 -> bf16 widening (exact) of two matrices in one launch: rows × cols of
@@ -131,16 +131,15 @@ cudaError_t launch_variant(const LaunchArgs& a) {
      KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::THREADS, 0, KCfg<InKind::IK, OutKind::OK, BN, ST, PR>::EPI_SLOTS},
 
 // Two-SM variants (TMA producer, 256-row pair tiles): input, output, tile
-// width, ring depth, epilogue staging slabs per warp, CTA pairs per cluster.
+// width, ring depth, epilogue staging slabs per warp.
 #define TCL_GROUP_PAIR(X)                                                                                    \
-    X(BF16, F32, 256, 6, 2, 1) X(BF16, F32, 256, 4, 2, 1) X(BF16, BF16, 256, 6, 2, 1)                        \
-    X(BF16, F32, 224, 6, 2, 1) X(BF16, F32, 224, 5, 4, 1) X(BF16, BF16, 256, 5, 4, 1)                        \
-    X(BF16, F32, 256, 6, 2, 2) X(BF16, F32, 224, 6, 2, 2) X(BF16, BF16, 256, 6, 2, 2)                        \
-    X(TF32, F32, 256, 6, 2, 1) X(TF32, F32, 224, 6, 2, 1) X(BF16, S32, 128, 8, 2, 1)                         \
-    X(BF16, S32, 256, 6, 1, 1)
-#define TCL_PAIR_INFO(IK, OK, BN, ST, SL, PR)                                                               \
-    {InKind::IK, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL, PR, InKind::IK>::SMEM_BYTES,      \
-     PairCfg<OutKind::OK, BN, ST, SL, PR, InKind::IK>::THREADS, PR, SL},
+    X(BF16, F32, 256, 6, 2) X(BF16, F32, 256, 4, 2) X(BF16, BF16, 256, 6, 2)                                 \
+    X(BF16, F32, 224, 6, 2) X(BF16, F32, 224, 5, 4) X(BF16, BF16, 256, 5, 4)                                 \
+    X(TF32, F32, 256, 6, 2) X(TF32, F32, 224, 6, 2) X(BF16, S32, 128, 8, 2)                                  \
+    X(BF16, S32, 256, 6, 1)
+#define TCL_PAIR_INFO(IK, OK, BN, ST, SL)                                                               \
+    {InKind::IK, OutKind::OK, BN, ST, 0, PairCfg<OutKind::OK, BN, ST, SL, InKind::IK>::SMEM_BYTES,      \
+     PairCfg<OutKind::OK, BN, ST, SL, InKind::IK>::THREADS, 1, SL},
 
 #define TCL_VARIANT_CASE(IK, OK, BN, ST, PR)                                                           \
     if (!a.pair && a.in == InKind::IK && a.out == OutKind::OK && a.bn == BN && a.stages == ST && a.prod == PR) { \

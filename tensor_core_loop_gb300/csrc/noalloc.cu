@@ -69,11 +69,19 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     uint8_t* a2 = static_cast<uint8_t*>(g_scratch_addr[dev]);
     uint8_t* b2 = a2 + a_bytes;
 
+    // This path launches the one-SM exact-integer kernel only (no stream-K flags,
+    // no workspace), so the plan is asked for exactly that. The planner returns a
+    // plan only for a kernel variant that is built, so once it succeeds the launch
+    // below finds its variant, and nothing is enqueued before this point.
     tcl_config_t cfg = {};
     cfg.max_ctas = sms;   // plan for this device without another device query
+    cfg.cta_pair = 1;
     tcl_plan_t plan;
     if ((st = tcl_plan(2, TCL_OUT_F32, M, N, K, &cfg, &plan))) return st;
-    const int bn = plan.bn, stages = plan.stages, grid = plan.grid, tiles = plan.num_tiles;
+    const int bn = plan.bn, stages = plan.stages, grid = plan.grid;
+    const int tiles_m = (M + 127) / 128, tiles_n = (N + bn - 1) / bn;
+    if (plan.cta_pair != 1 || plan.splits != 1 || plan.sk_tiles != 0 || plan.num_tiles != tiles_m * tiles_n)
+        return TCL_ERR_CONFIG;
 
     LaunchArgs a;
     a.in = InKind::BF16;
@@ -97,9 +105,9 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.M = M;
     p.N = N;
     p.K = K;
-    p.tiles_m = (M + 127) / 128;
-    p.tiles_n = (N + bn - 1) / bn;
-    p.num_tiles = tiles;
+    p.tiles_m = tiles_m;
+    p.tiles_n = tiles_n;
+    p.num_tiles = plan.num_tiles;
     p.num_kb = (K + 63) / 64;
     p.kb_per_unit = 1024 / 64;   // exact fp32 units of 1024 K values, as gemm_s8
     p.group_m = 8;

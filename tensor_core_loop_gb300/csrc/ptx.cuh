@@ -401,21 +401,6 @@ __device__ __forceinline__ void tma_load_2d_pair_elected(uint32_t dst, const CUt
         : "memory");
 }
 
-// Multicast form: the box lands at the same shared offset in every CTA of
-// `mask`; each destination's byte count goes to the mbarrier at bar's offset
-// in the even CTA of that destination's pair (bar names an even CTA's barrier).
-__device__ __forceinline__ void tma_load_2d_pair_mc_elected(uint32_t dst, const CUtensorMap* map,
-                                                            uint32_t bar_cluster, int32_t c0, int32_t c1,
-                                                            uint16_t mask) {
-    asm volatile(
-        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
-        "elect.sync lane_sel|el, 0xffffffff;\n\t"
-        "@el cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(mask)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- clusters / CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -125,7 +125,7 @@ def test_plan_without_device(L):
         assert (p["sk_tiles"], p["sk_pieces"], p["splits"]) == (28, 2, 1)   # int32 pieces add exactly
     p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=2, bn=128))
     assert p["cta_pair"] == 2 and p["bn"] == 128 and p["num_tiles"] == 16 * 32
-    for bad in (tcl.Config(max_ctas=152, cta_pair=2, bn=224), tcl.Config(max_ctas=152, cluster_pairs=2),
+    for bad in (tcl.Config(max_ctas=152, cta_pair=2, bn=224), tcl.Config(max_ctas=152, cta_pair=3),
                 tcl.Config(max_ctas=152, cta_pair=1, stream_k=2)):
         with pytest.raises(tcl.TclError):
             tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, bad)

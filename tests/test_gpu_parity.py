@@ -212,19 +212,19 @@ def test_bf16_pair_kernel_bf16_out(oracle_mod, M, N, K):
     bf16_case(oracle_mod, M, N, K, seed=5, out_dtype=torch.bfloat16, cfg=tcl.Config(cta_pair=2))
 
 
-@pytest.mark.parametrize("M,N,K,pieces,pairs", [
-    (768, 768, 4096, 0, 1),     # automatic (64 k-blocks): the 9th tile in 4 pieces, three fp32 partials
-    (768, 768, 2048, 0, 1),     # automatic at 32 k-blocks (the bf16 C's tail threshold): 4 pieces of 8
-    (768, 768, 2048, 2, 1),
-    (768, 768, 2048, 3, 1),
-    (700, 750, 1000, 4, 1),     # ragged M, N: the last piece rounds and stores only what lies in C
-    (512, 1280, 576, 2, 1),
-    (1024, 1280, 2048, 2, 2),   # two pairs per cluster: workspace rows per pair
+@pytest.mark.parametrize("M,N,K,pieces", [
+    (768, 768, 4096, 0),     # automatic (64 k-blocks): the 9th tile in 4 pieces, three fp32 partials
+    (768, 768, 2048, 0),     # automatic at 32 k-blocks (the bf16 C's tail threshold): 4 pieces of 8
+    (768, 768, 2048, 2),
+    (768, 768, 2048, 3),
+    (700, 750, 1000, 4),     # ragged M, N: the last piece rounds and stores only what lies in C
+    (512, 1280, 576, 2),
+    (1536, 1280, 2048, 2),   # 30 tiles on 4 pairs: two tail tiles, each with its own workspace rows
 ])
-def test_bf16_out_stream_k(oracle_mod, M, N, K, pieces, pairs):
+def test_bf16_out_stream_k(oracle_mod, M, N, K, pieces):
     # bf16 C with a stream-K tail: the pieces' fp32 sums meet in an fp32 workspace in piece
     # order and the last piece rounds once into C, so the bf16 bound holds unchanged
-    cfg = tcl.Config(cta_pair=2, cluster_pairs=pairs, max_ctas=8 * pairs, stream_k=pieces)
+    cfg = tcl.Config(cta_pair=2, max_ctas=8, stream_k=pieces)
     pl = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, M, N, K, cfg)
     assert pl["sk_tiles"] > 0 and pl["workspace_bytes"] > 0
     ldc = -(-N // 8) * 8 if N % 8 else None
@@ -261,35 +261,6 @@ def test_bf16_pair_stream_k(oracle_mod, M, N, K, pieces):
     assert pl["sk_tiles"] > 0 and pl["sk_pieces"] == (pieces or pl["sk_pieces"]) and pl["sk_pieces"] >= 2
     ldc = -(-N // 4) * 4 if N % 4 else None
     bf16_case(oracle_mod, M, N, K, seed=K + pieces, cfg=cfg, ldc=ldc)
-
-
-@pytest.mark.parametrize("M,N,K,sk", [
-    (512, 512, 512, 1),       # one couple of 256-row tiles per column of tiles
-    (700, 750, 2000, 0),      # odd number of row tiles: the second tile of the last couple lies past M
-    (1024, 1280, 1216, 1),
-    (1024, 1280, 2048, 2),    # 10 couples on 4 clusters: two couples in stream-K pieces
-])
-def test_bf16_two_pair_clusters(oracle_mod, M, N, K, sk):
-    # two CTA pairs per cluster on stacked tiles, sharing B by multicast
-    cfg = tcl.Config(cta_pair=2, cluster_pairs=2, max_ctas=16, stream_k=sk)
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K, cfg)["cluster_pairs"] == 2
-    ldc = -(-N // 4) * 4 if N % 4 else None
-    bf16_case(oracle_mod, M, N, K, seed=K + 7, cfg=cfg, ldc=ldc)
-
-
-def test_bf16_two_pair_clusters_bf16_out_and_grid(oracle_mod):
-    bf16_case(oracle_mod, 768, 1024, 832, seed=3, out_dtype=torch.bfloat16,
-              cfg=tcl.Config(cta_pair=2, cluster_pairs=2))
-    bf16_case(oracle_mod, 1024, 1536, 1024, seed=4, cfg=tcl.Config(cta_pair=2, cluster_pairs=2, bn=224, max_ctas=8))
-
-
-def test_two_pair_clusters_match_one_pair_bitwise():
-    # sharing B changes who loads it, not the MMA sequence of any tile
-    a, b = inputs.bf16_pair(1024, 1280, 1216, seed=19)
-    a, b = a.to(DEV), b.to(DEV)
-    one = run(a, b, cfg=tcl.Config(cta_pair=2, cluster_pairs=1, stream_k=1), canary=False)
-    two = run(a, b, cfg=tcl.Config(cta_pair=2, cluster_pairs=2, stream_k=1), canary=False)
-    assert torch.equal(one, two)
 
 
 def test_stream_k_deterministic():

@@ -44,18 +44,17 @@ def test_bounded_wait_runs_out_and_context_survives():
     assert tcl.last_device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("pairs", [1, 2])
-def test_two_sm_kernel_bounded_wait_runs_out(pairs):
-    # CTA 0 of the first cluster announces a stage's bytes but never loads its share:
-    # the leader's MMA wait runs out; every CTA of the cluster aborts and returns
+def test_two_sm_kernel_bounded_wait_runs_out():
+    # CTA 0 of the first pair announces a stage's bytes but never loads its share:
+    # the leader's MMA wait runs out; both CTAs of the pair abort and return
     a, b = inputs.bf16_pair(1024, 1024, 1024, seed=5)
     a, b = a.to(DEV), b.to(DEV)
     c = torch.zeros((1024, 1024), dtype=torch.float32, device=DEV)
-    cfg = tcl.Config(cta_pair=2, cluster_pairs=pairs, timeout_ns=50_000_000, debug_skip_kblock=2)
+    cfg = tcl.Config(cta_pair=2, timeout_ns=50_000_000, debug_skip_kblock=2)
     tcl.gemm_into(a, b, c, cfg=cfg)
     st, code = tcl.last_device_error()
     assert st == 7 and code in (1, 2, 3, 4), (st, code)
-    ref = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=2, cluster_pairs=pairs))
+    ref = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=2))
     again = tcl.gemm(a, b)
     torch.cuda.synchronize()
     assert torch.allclose(ref, again, rtol=0, atol=1e-2)   # both correct (different plans)

@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -73,10 +74,39 @@ def test_static_entry_matches_gemm_s8_on_two_calls_in_a_row(L):
     assert st == 0, f"device status word reported code {code}"
 
 
+def _sample_rows(M, n, seed):
+    g = np.random.default_rng(seed)
+    fixed = {0, 1, 127, 128, M // 2, M - 129, M - 128, M - 1}
+    return sorted(r for r in fixed.union(g.integers(0, M, n).tolist()) if 0 <= r < M)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (2304, 2304, 1024)])
+def test_static_entry_large_problems_exact(L, oracle_mod, M, N, K):
+    # Problems for which gemm_s8 itself runs on two SMs per tile: 4096³ fills the
+    # 64 MiB array exactly (2·(4096·4096 + 4096·4096) bytes of bf16 copies). The
+    # result is checked bit for bit against the CPU oracle on sampled rows and in
+    # full against gemm_s8, on two calls in a row (the second over the first's
+    # leftovers in the shared array).
+    assert tcl.plan(tcl.IN_S8, 0, M, N, K)["cta_pair"] == 2
+    a, b = inputs.s8_pair(M, N, K, seed=M + K)
+    ad, bd = a.to(DEV), b.to(DEV)
+    ref = _call(L.gemm_s8, M, N, K, ad, K, bd, N)
+    for call in range(2):
+        got = _call(L.gemm_s8_static, M, N, K, ad, K, bd, N)
+        assert torch.equal(got, ref), f"call {call}: gemm_s8_static differs from gemm_s8 at {M}x{N}x{K}"
+    host = got.cpu().numpy()
+    an, bn = a.numpy(), b.numpy()
+    for r in _sample_rows(M, 6, seed=K):
+        want = oracle_mod.gemm_s8(an, bn, rows=(r, r + 1))
+        assert np.array_equal(host[r:r + 1, :N].astype(np.int64), want), f"row {r} differs from the oracle"
+    st, code = tcl.last_device_error()
+    assert st == 0, f"device status word reported code {code}"
+
+
 def test_static_entry_rejects_problems_beyond_its_buffer(L):
-    # 8192³ needs 2·(8192·8192 + 8192·8192)·... = 256 MiB of packed operands > 64 MiB;
+    # 8192³ needs 2·(8192·8192 + 8192·8192) bytes = 256 MiB of packed operands > 64 MiB;
     # the check happens on the host before any device work (pointers never touched)
     fake = 0x10000000
     assert L.gemm_s8_static(8192, 8192, 8192, fake, 8192, fake, 8192, fake, 8192, None) == 11
-    # the headline 4096³ problem fits exactly
-    assert 2 * (4096 * 4096 + 4096 * 4096) <= (64 << 20)
+    # one row more than 4096³ no longer fits
+    assert L.gemm_s8_static(4097, 4096, 4096, fake, 4096, fake, 4096, fake, 4096, None) == 11

@@ -338,6 +338,30 @@ def time_rotating(fn, sets, steps, warmup, stream, torch):
     return start.elapsed_time(end) / steps
 
 
+def time_graph_rotating(fn, sets, launches, replays, torch):
+    """Back-to-back launches over rotating input sets captured into one CUDA graph (the
+    host's per-call launch cost removed); returns ms per launch over `replays` replays.
+    Every call runs once outside capture first, so that library scratch is in place."""
+    for i in range(len(sets)):
+        fn(*sets[i])
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(launches):
+            fn(*sets[i % len(sets)])
+    g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(replays):
+        g.replay()
+    end.record()
+    end.synchronize()
+    return start.elapsed_time(end) / (replays * launches)
+
+
 def time_flushed(fn, args_, iters, stream, torch, flush):
     """Per-launch event timing with an L2 flush (a write larger than L2) before each launch."""
     times = []
@@ -503,6 +527,9 @@ def trace_stats(t, stages, bn, num_kb):
     idx2 = np.arange(max(0, min(nd, n - (stages - 1))))
     out["load_k_plus_stages_minus_1_before_mma_k_done"] = (
         float((issued[idx2 + stages - 1] < done[idx2]).mean()) if len(idx2) and stages > 1 else None)
+    if n <= stages - 1 and nd >= 1:
+        # a walk shorter than the ring: were all of its loads in flight before the first MMAs finished?
+        out["all_loads_issued_before_first_mma_done"] = bool(issued[n - 1] < done[0])
     issue = mma - landed                     # MMA warp: issue 4 MMAs + commit
     out["mma_issue_cycles"] = {"p50": float(np.median(issue)), "mean": float(issue.mean())}
     if n > 1:
@@ -738,7 +765,10 @@ def main():
         del sets16
         # K sweep: back-to-back launches over rotating input/output sets whose footprint is
         # twice the L2, so every launch starts cold in L2 (single-launch event timing is
-        # quantised at ~2 µs on this GPU, too coarse for the smallest shapes)
+        # quantised at ~2 µs on this GPU, too coarse for the smallest shapes). "us" is
+        # taken from a CUDA graph of those launches (what the GPU takes per call);
+        # "us_host_launch" from the same launches issued one by one from Python, whose
+        # per-call host cost (ctypes and the library's host code) shows at the small shapes
         sweep = {}
         for mn, k in SWEEP:
             ah, bh = inputs.bf16_pair(mn, mn, k, seed=0)
@@ -750,38 +780,47 @@ def main():
 
             def f(a, b, c, mn=mn, k=k):
                 st_ = L.gemm_bf16(mn, mn, k, a.data_ptr(), k, b.data_ptr(), mn, c.data_ptr(), mn, tcl.OUT_F32,
-                                  stream.cuda_stream)
+                                  torch.cuda.current_stream().cuda_stream)
                 if st_:
                     raise tcl.TclError(st_, "gemm_bf16")
-            ms = time_rotating(f, ssets, max(60, 2 * nset), 2 * nset, stream, torch)
+            ms_host = time_rotating(f, ssets, max(60, 2 * nset), 2 * nset, stream, torch)
+            ms = time_graph_rotating(f, ssets, max(40, 2 * nset), 5, torch)
             tf = 2.0 * mn * mn * k / (ms * 1e-3) / 1e12
             alg_bytes = (mn * k + k * mn) * 2 + mn * mn * 4
             sweep[f"{mn}x{mn}x{k}"] = {"tflops": round(tf, 1), "us": round(ms * 1e3, 2),
+                                        "us_host_launch": round(ms_host * 1e3, 2),
                                         "alg_gbs": round(alg_bytes / (ms * 1e-3) / 1e9, 1),
                                         "plan": tcl.plan(tcl.IN_BF16, tcl.OUT_F32, mn, mn, k)}
             del ssets, a0_, b0_
         extra["k_sweep"] = sweep
-        extra["k_sweep_timing"] = "mean of back-to-back launches over rotating sets (footprint 2x L2)"
+        extra["k_sweep_timing"] = ("us: mean of back-to-back launches over rotating sets (footprint 2x L2) "
+                                   "captured in a CUDA graph; us_host_launch: the same launches issued one "
+                                   "by one from Python")
         flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
-        # the other two workloads at 4096³ (each launch timed alone after an L2 flush): int8 → exact
-        # int32 (repack pass + GEMM), TF32 (transpose pass + GEMM); whole-call time
-        a8h, b8h = inputs.s8_pair(M, N, K, seed=0)
-        a8, b8 = a8h.to(dev), b8h.to(dev)
-        c32 = torch.empty((M, N), dtype=torch.int32, device=dev)
-        f8 = (lambda: tcl.gemm_into(a8, b8, c32))
-        for _ in range(3):
-            f8()
-        ms8 = time_flushed(f8, (), 20, stream, torch, flush)
+        # the other two workloads at 4096³, whole call (int8 → exact int32: widening pass +
+        # GEMM; TF32: the GEMM alone, B read in place), timed like the headline (back-to-back
+        # launches over rotating input sets whose footprint exceeds L2) and, beside it, each
+        # launch alone after an L2 flush (host launch latency included)
+        def whole_call(pair_fn, out_dtype):
+            xh, yh = pair_fn(M, N, K, seed=0)
+            x0, y0 = xh.to(dev), yh.to(dev)
+            per = (x0.numel() + y0.numel()) * x0.element_size() + M * N * 4
+            nset_ = max(2, -(-2 * L2_BYTES // per))
+            sets_ = [(x0 if i == 0 else x0.clone(), y0 if i == 0 else y0.clone(),
+                      torch.empty((M, N), dtype=out_dtype, device=dev)) for i in range(nset_)]
+            fn = (lambda x, y, z: tcl.gemm_into(x, y, z))
+            ms_rot = time_rotating(fn, sets_, 200, 20, stream, torch)
+            x, y, z = sets_[0]
+            ms_one = time_flushed(lambda: fn(x, y, z), (), 20, stream, torch, flush)
+            return ms_rot, ms_one, sets_[0]
+        ms8, ms8_one, _ = whole_call(inputs.s8_pair, torch.int32)
         extra["int8_tops_4096"] = round(FLOPS / (ms8 * 1e-3) / 1e12, 1)
-        del a8, b8, c32
-        ath, bth = inputs.tf32_pair(M, N, K, seed=0)
-        at, bt = ath.to(dev), bth.to(dev)
-        ct = torch.empty((M, N), dtype=torch.float32, device=dev)
-        ft = (lambda: tcl.gemm_into(at, bt, ct))
-        for _ in range(3):
-            ft()
-        mst = time_flushed(ft, (), 20, stream, torch, flush)
+        extra["int8_tops_4096_single_flushed"] = round(FLOPS / (ms8_one * 1e-3) / 1e12, 1)
+        mst, mst_one, (at, bt, ct) = whole_call(inputs.tf32_pair, torch.float32)
         extra["tf32_tflops_4096"] = round(FLOPS / (mst * 1e-3) / 1e12, 1)
+        extra["tf32_tflops_4096_single_flushed"] = round(FLOPS / (mst_one * 1e-3) / 1e12, 1)
+        extra["int8_tf32_timing"] = ("*_4096: back-to-back whole calls over rotating input sets (footprint "
+                                     "> 2x L2), as the headline; *_single_flushed: one call after an L2 flush")
         extra["sgemm_simt_4096"] = measure_simt(tcl, torch, dev, stream, at, bt, ct, flush)
         del at, bt, ct
         del flush

@@ -17,8 +17,8 @@
  * Memory and ownership: A, B and C are device pointers owned by the caller
  *   (allocated, kept alive until the stream has run the call, and freed by
  *   the caller). The library keeps a per-device cache of TMA descriptors and
- *   a per-device scratch buffer (repacked operands for gemm_s8 and gemm_tf32,
- *   copies of operands or outputs off the 16-byte grid, split-K partial
+ *   a per-device scratch buffer (the widened operands of gemm_s8, copies of
+ *   operands or outputs off the 16-byte grid, split-K partial
  *   tiles for small grids, the fp32 partial sums of a bf16 C's stream-K
  *   tail) that it grows on demand (cudaMalloc, at least
  *   doubling; an outgrown buffer is kept, since enqueued or graph-captured
@@ -50,8 +50,7 @@
  *   rounds a row end up to 16 bytes):
  *   gemm_bf16: A, B, C 16-byte aligned; lda, ldb and K multiples of 8;
  *              ldc a multiple of 4 (fp32 C) or 8 (bf16 C).
- *   gemm_tf32: A, C 16-byte aligned; lda, K and ldc multiples of 4 (B is
- *              always copied, transposed).
+ *   gemm_tf32: A, B, C 16-byte aligned; lda, ldb, K and ldc multiples of 4.
  *   gemm_s8:   C 16-byte aligned, ldc a multiple of 4 (A and B are always
  *              repacked).
  *   An operand that misses these is first copied into the library scratch
@@ -109,11 +108,15 @@ typedef enum { TCL_OUT_F32 = 0, TCL_OUT_BF16 = 1 } tcl_out_t;
 /* Optional knobs for the *_ex entry points (ablation, tracing, tests).
  * Zero-initialise and set only what you need; zero means "automatic". */
 typedef struct {
-    int bn;                        /* N tile: 128 or 256 (0: chosen from M, N and the SM count) */
+    int bn;                        /* N tile: 128 or 256; also 64 (one SM per tile, bf16 in, float
+                                      out) and 224 (two SMs per tile) (0: chosen from M, N and the
+                                      SM count) */
     int stages;                    /* shared-memory ring depth (0: the deepest that fits) */
     int one_cta_per_tile;          /* 0 (default): persistent, one CTA per SM walking the tiles;
                                       1: one CTA per output tile (no persistence) */
-    int group_m;                   /* raster group height in tiles (0: 8) */
+    int group_m;                   /* raster group height in tiles (0: automatic — 1 on the two-SM
+                                      kernel when a row of A holds at least 16 KB (bf16 K >= 8192,
+                                      TF32 K >= 4096), else 8) */
     int max_ctas;                  /* cap on resident CTAs for the persistent grid (0: all SMs) */
     unsigned long long timeout_ns; /* bound on every in-kernel wait (0: 1 s) */
     unsigned long long* trace;     /* device buffer of 4*trace_cap + 4 uint64, or NULL: %clock64
@@ -160,6 +163,14 @@ typedef struct {
     int debug_stream_k_stall;      /* test hook, 0 = off. 1: the first stream-K piece of the first
                                       split tile never hands its tile over, so the next piece's
                                       bounded wait must run out (device status code 5) */
+    int k_order;                   /* order in which a persistent CTA's successive tiles walk K:
+                                      0 automatic (alternating where group_m's automatic value is 1,
+                                      else ascending); 1 always ascending; 2
+                                      alternating — every second tile of a CTA's walk loads its
+                                      k-blocks in descending order, so that a wave of tiles starts
+                                      on the operand blocks the previous wave read last (still in
+                                      L2). The order changes the fp32 summation order of those
+                                      tiles (not the exact int32 result). TMA producer only */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -167,9 +178,9 @@ typedef struct {
 TCL_API int gemm_bf16(int M, int N, int K, const void* A, int lda, const void* B, int ldb, void* C, int ldc,
               int out, cudaStream_t stream);
 
-/* fp32 A, B consumed by the tensor cores as TF32; fp32 accumulation; fp32 C.
- * B is first transposed, bit for bit, into library scratch (N rows of K):
- * the TF32 tensor-core path reads both operands K-major. */
+/* fp32 A, B consumed by the tensor cores as TF32 (the low 13 mantissa bits of
+ * each input are not used); fp32 accumulation; fp32 C. Both operands are read
+ * in place: A K-major, B N-major (its rows as they lie in memory). */
 TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
               int ldc, cudaStream_t stream);
 
@@ -263,6 +274,8 @@ typedef struct {
     unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
     int sk_tiles;                   /* tail tiles computed stream-K (0: none) */
     int sk_pieces;                  /* K ranges per stream-K tile */
+    int group_m;                    /* raster group height in tiles */
+    int k_serpentine;               /* 1: alternating K order (see tcl_config_t.k_order) */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

@@ -67,6 +67,7 @@ class Config(ctypes.Structure):
         ("stream_k", ctypes.c_int),
         ("serial_launch", ctypes.c_int),
         ("debug_stream_k_stall", ctypes.c_int),
+        ("k_order", ctypes.c_int),
     ]
 
 
@@ -84,6 +85,8 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_ulonglong),
         ("sk_tiles", ctypes.c_int),
         ("sk_pieces", ctypes.c_int),
+        ("group_m", ctypes.c_int),
+        ("k_serpentine", ctypes.c_int),
     ]
 
 

@@ -68,9 +68,10 @@ struct MapKey {
     int dtype;
     uint64_t d0, d1, stride;
     uint32_t b0, b1;
+    int swizzle;
     bool operator==(const MapKey& o) const {
         return dev == o.dev && ptr == o.ptr && dtype == o.dtype && d0 == o.d0 && d1 == o.d1 &&
-               stride == o.stride && b0 == o.b0 && b1 == o.b1;
+               stride == o.stride && b0 == o.b0 && b1 == o.b1 && swizzle == o.swizzle;
     }
 };
 struct MapKeyHash {
@@ -87,6 +88,7 @@ struct MapKeyHash {
         mix(k.d1);
         mix(k.stride);
         mix((static_cast<uint64_t>(k.b0) << 32) | k.b1);
+        mix(static_cast<uint64_t>(k.swizzle));
         return static_cast<size_t>(h);
     }
 };
@@ -187,10 +189,13 @@ int encode_fn() {
 }
 
 // 2-D row-major tensor map: inner extent d0 (contiguous), outer d1, row
-// stride in bytes, box b0 × b1, 128-byte swizzle, zero fill out of bounds.
+// stride in bytes, box b0 × b1, 128-byte swizzle (in 16-byte units, or for
+// swz = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B in 32-byte units), zero fill out
+// of bounds.
 int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1,
-               uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMap* out) {
-    const MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride_bytes, b0, b1};
+               uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMap* out,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+    const MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride_bytes, b0, b1, static_cast<int>(swz)};
     auto it = g_maps.find(key);
     if (it != g_maps.end()) {
         *out = it->second;
@@ -204,8 +209,8 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
     const cuuint32_t box[2] = {b0, b1};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return TCL_ERR_LAUNCH;
     if (g_maps.size() > 4096) g_maps.clear();
     g_maps.emplace(key, m);
@@ -218,6 +223,7 @@ struct Plan {
     int sk_ws_rows;   // bf16 C with a stream-K tail: fp32 workspace rows (split tiles × 256), else 0
     int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
     int sk_tiles, sk_pieces;    // stream-K tail of the two-SM kernel (0 tiles: none)
+    int k_serpentine;           // odd units of a CTA's walk load K in descending order
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -226,6 +232,8 @@ struct Plan {
 constexpr int kMinKbPerSplit = 8;    // k-blocks each range keeps
 constexpr int kMinKbForPair = 16;    // k-blocks a tile needs before two SMs per tile pay off
 constexpr int kMinKbToSplit = 24;    // k-blocks a tile needs before splitting is considered
+constexpr long long kMinKBytesForRowRaster = 16384;   // two-SM kernel: K bytes per operand row from which
+                                                      // group 1 and alternating K order are the default
 
 // Two-SM kernel: SM cycles per 64-deep k-block of a pair tile, measured on
 // GB300 with the in-kernel timeline (the tensor pipe runs 256-wide pair tiles
@@ -366,9 +374,19 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             const long long tiles256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256);
             const int kblocks = (K + bk - 1) / bk;
             bn = (tiles256 >= sms && (kblocks > 4 || ok == OutKind::BF16)) ? 256 : 128;
+            // Small grids (128-wide tiles filling at most a quarter of the SMs) too shallow
+            // for split-K: 64-wide tiles give twice the CTAs, each with half the B bytes
+            // and half the C stores (measured on GB300, CUDA graphs of back-to-back calls
+            // at 512²: K = 256 4.37 against 4.98 µs, 512 5.21 against 5.92, 1024 6.74
+            // against 7.76).
+            const long long tiles128 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 127) / 128);
+            const bool split_asked = cfg && cfg->split_k > 1;
+            if (bn == 128 && tiles128 * 4 <= sms && kblocks < kMinKbToSplit && !split_asked &&
+                !(cfg && cfg->stages) && deepest_stages(ik, ok, 64, prod, 0) > 0)
+                bn = 64;
         }
     }
-    if (bn != 128 && bn != 256 && !(pair && bn == 224)) return TCL_ERR_CONFIG;
+    if (bn != 128 && bn != 256 && !(pair && bn == 224) && !(!pair && bn == 64)) return TCL_ERR_CONFIG;
     const int slots = cfg ? cfg->epi_slots : 0;
     if (slots < 0 || (slots && !pair && slots != 2)) return TCL_ERR_CONFIG;
     const int pv = pair ? 1 : 0;   // the variant table's kernel kind (1: two-SM kernel)
@@ -389,7 +407,21 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->num_tiles = static_cast<int>(tiles);
     pl->num_kb = (K + bk - 1) / bk;
     pl->kb_per_unit = ok == OutKind::S32 ? kS32UnitK / bk : pl->num_kb;
-    pl->group_m = cfg && cfg->group_m > 0 ? cfg->group_m : 8;
+    // Raster group and K order for deep two-SM tiles (rows of A at least 16 KB
+    // long): a wave of tiles then streams more operand bytes than one die's share
+    // of L2 keeps, and each wave re-reads what the one before evicted. One row of
+    // tiles at a time (group 1: a wave shares all of B and a few rows of A), with
+    // every second tile of a CTA's walk taking K in descending order (so that a
+    // wave starts on the blocks the previous wave read last, which are still in
+    // L2), cut the DRAM reads of bf16 4096²×8192 from 340 to 272 MB and of TF32
+    // 4096³ from 339 to 274 MB (ncu, cold L2). Timed round robin under the power
+    // cap, the orders stay within 2 % of each other at every deep shape; with
+    // shorter rows groups of 8 rows and ascending K are kept.
+    const bool deep = pair && static_cast<long long>(pl->num_kb) * bk * in_bytes(ik) >= kMinKBytesForRowRaster;
+    pl->group_m = cfg && cfg->group_m > 0 ? cfg->group_m : (deep ? 1 : 8);
+    const int want_ko = cfg ? cfg->k_order : 0;
+    if (want_ko < 0 || want_ko > 2 || (want_ko == 2 && prod != PROD_TMA)) return TCL_ERR_CONFIG;
+    pl->k_serpentine = want_ko == 2 ? 1 : want_ko == 1 ? 0 : (deep ? 1 : 0);
     // Split-K (one-SM kernel, floating-point output): when the output tiles
     // alone would leave most SMs idle, cut K into ranges computed by different
     // CTAs; a second kernel adds the partial tiles in a fixed order.
@@ -526,11 +558,12 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.grid = pl.grid;
     a.stream = stream;
     if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
-    if (ik == InKind::TF32) {   // B given K-major (N rows of K); a pair CTA loads its half of the rows
-        if ((st = tensor_map(dev, B, in_t, K, N, ldb * ies, bk, pl.pair ? pl.bn / 2 : pl.bn, &a.tmB))) return st;
-    } else {                    // B given N-major (K rows of N)
-        if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB))) return st;
-    }
+    // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
+    // 4-byte elements are swizzled in 32-byte units, the form the tensor core
+    // reads an N-major 32-bit operand in
+    if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB,
+                         ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
     void* out_ptr = split ? workspace : C;
     const long long out_ld = split ? ws.ld : ldc;
     const long long out_rows = split ? ws.rows_per_split * pl.splits : M;
@@ -569,6 +602,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.sk_gen = 0;
     p.sk_ws = nullptr;
     p.sk_ws_rows = 0;
+    p.k_serpentine = pl.k_serpentine;
     if (pl.sk_ws_rows) {   // (16-byte accesses: the workspace starts on a 256-byte boundary)
         p.sk_ws = static_cast<float*>(workspace);
         p.sk_ws_rows = pl.sk_ws_rows;
@@ -675,39 +709,40 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
     if (!aligned_to(A, 4) || !aligned_to(B, 4) || !aligned_to(C, 4)) return TCL_ERR_ALIGN;
-    // As for bf16: off-grid operands are repacked (K zero-padded to a multiple
-    // of 4), an off-grid output goes through scratch. B is always copied: the
-    // TF32 tensor-core path takes it K-major, transposed into N rows of K4.
+    // As for bf16: operands off the tensor copies' 16-byte grid are repacked (K
+    // zero-padded to a multiple of 4, in A's columns and B's rows), an off-grid
+    // output goes through scratch. Both operands are read in place otherwise:
+    // A K-major, B N-major straight from the row-major K×N matrix.
     const bool pack_a = !aligned16(A) || lda % 4 || K % 4;
+    const bool pack_b = !aligned16(B) || ldb % 4 || K % 4;
     const bool pack_c = !aligned16(C) || ldc % 4;
     const int K4 = static_cast<int>(round_up(K, 4));
-    const long long ldc2 = round_up(N, 4);
+    const long long ldb2 = round_up(N, 4), ldc2 = round_up(N, 4);
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
     Plan pl;
     if ((st = plan_on_device(InKind::TF32, OutKind::F32, M, N, K4, cfg, ds, &pl))) return st;
-    const size_t bt_bytes = static_cast<size_t>(N) * K4 * 4;
     const size_t a_bytes = pack_a ? static_cast<size_t>(M) * K4 * 4 : 0;
+    const size_t b_bytes = pack_b ? static_cast<size_t>(K4) * ldb2 * 4 : 0;
     const size_t c_bytes = pack_c ? static_cast<size_t>(M) * ldc2 * 4 : 0;
     const Workspace ws = split_workspace(pl, M, N);
-    const size_t need = static_cast<size_t>(round_up(bt_bytes, 256) + round_up(a_bytes, 256) +
+    const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws.bytes;
-    if ((st = ensure_scratch(ds, need, stream))) return st;
+    if (need && (st = ensure_scratch(ds, need, stream))) return st;
     Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
-    float* bt = static_cast<float*>(cv.take(bt_bytes));
     void* a2 = cv.take(a_bytes);
+    void* b2 = cv.take(b_bytes);
     void* c2 = cv.take(c_bytes);
     void* wsp = cv.take(ws.bytes);
-    if ((K4 != K && cudaMemsetAsync(bt, 0, bt_bytes, stream) != cudaSuccess) ||
-        launch_transpose_f32(B, ldb, bt, K4, K, N, ds->sms, stream) != cudaSuccess ||
-        (pack_a && launch_repack(A, lda, M, K, a2, K4, M, K4, 4, ds->sms, stream) != cudaSuccess)) {
+    if ((pack_a && launch_repack(A, lda, M, K, a2, K4, M, K4, 4, ds->sms, stream) != cudaSuccess) ||
+        (pack_b && launch_repack(B, ldb, K, N, b2, ldb2, K4, N, 4, ds->sms, stream) != cudaSuccess)) {
         cudaGetLastError();
         return TCL_ERR_LAUNCH;
     }
-    st = run_gemm(pl, InKind::TF32, OutKind::F32, M, N, K4, pack_a ? a2 : A, pack_a ? K4 : lda, bt, K4,
-                  pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, stream);
+    st = run_gemm(pl, InKind::TF32, OutKind::F32, M, N, K4, pack_a ? a2 : A, pack_a ? K4 : lda, pack_b ? b2 : B,
+                  pack_b ? ldb2 : ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, stream);
     if (st) return st;
     if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, 4, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -1006,6 +1041,8 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->workspace_bytes = static_cast<unsigned long long>(split_workspace(pl, M, N).bytes);
         plan->sk_tiles = pl.sk_tiles;
         plan->sk_pieces = pl.sk_pieces;
+        plan->group_m = pl.group_m;
+        plan->k_serpentine = pl.k_serpentine;
     }
     return TCL_OK;
 }

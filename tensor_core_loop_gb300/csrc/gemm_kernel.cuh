@@ -7,10 +7,11 @@
 // global→shared double buffering generalised to a multi-stage ring), rebuilt
 // for Blackwell:
 //   * warp 0 (producer): TMA 2-D tiled loads of the A tile (BM×BK, K-major)
-//     and the B tile (BK×BN; N-major for bf16, K-major for TF32, whose B the
-//     host path transposes first) into stage s of a STAGES-deep ring,
-//     128-byte swizzled; completion tracked by the full[s] mbarrier as
-//     transaction bytes. It waits on empty[s] before reusing a stage.
+//     and the B tile (BK×BN, N-major, straight from the row-major K×N
+//     matrix) into stage s of a STAGES-deep ring, 128-byte swizzled (for
+//     TF32's 4-byte B, in 32-byte units); completion tracked by the full[s]
+//     mbarrier as transaction bytes. It waits on empty[s] before reusing a
+//     stage.
 //   * warp 1 (MMA issuer): one thread issues tcgen05.mma (kind::f16 or
 //     kind::tf32) per UMMA_K slice into a TMEM accumulator, and commits
 //     empty[s] when the stage's MMAs are done; at the end of a unit it
@@ -63,12 +64,20 @@ struct InTraits<InKind::BF16> {
     static constexpr int ES = 2;        // bytes per element
     static constexpr int UMMA_K = 16;   // K per tcgen05.mma
     static constexpr uint32_t FMT = 1;  // bf16
+    // N-major B: descriptor layout (128-byte swizzle) and the byte distance
+    // between the descriptor's core groups along K (8 rows of 128 bytes)
+    static constexpr uint32_t B_LAYOUT = 2;
+    static constexpr uint32_t B_SBO = 1024;
 };
 template <>
 struct InTraits<InKind::TF32> {
     static constexpr int ES = 4;
     static constexpr int UMMA_K = 8;
     static constexpr uint32_t FMT = 2;  // tf32
+    // N-major B of 4-byte elements: 128-byte swizzle in 32-byte units (the tensor
+    // copy's SWIZZLE_128B_ATOM_32B), core groups of 4 rows of 128 bytes
+    static constexpr uint32_t B_LAYOUT = 1;
+    static constexpr uint32_t B_SBO = 512;
 };
 
 struct GemmParams {
@@ -107,7 +116,18 @@ struct GemmParams {
     // sums and rounds once into C
     float* sk_ws;
     int sk_ws_rows;
+    // 1: the units at odd positions of each CTA's walk load their k-blocks in
+    // descending order (the MMAs and the accumulation units follow the loads), so
+    // that a wave starts on the operand rows the previous wave read last, which
+    // are the ones still in L2
+    int k_serpentine;
 };
+
+// K coordinate (in k-blocks) that the load at position kb of the range
+// [kb_lo, kb_hi) fetches, for the unit at position `pos` of a CTA's walk.
+__device__ __forceinline__ int load_kblock(const GemmParams& p, int pos, int kb, int kb_lo, int kb_hi) {
+    return (p.k_serpentine && (pos & 1)) ? kb_lo + kb_hi - 1 - kb : kb;
+}
 
 // Work item w → output tile (mb, nb), its k-block range [kb_lo, kb_hi) and
 // the row where its result starts in the output tensor. Splits of one tile
@@ -157,13 +177,11 @@ struct KCfg {
     static constexpr int UMMA_K = InTraits<IK>::UMMA_K;
     static constexpr int KSUB = BK / UMMA_K;          // MMAs per k-block
     static constexpr int A_BYTES = BM * 128;          // BM rows × 128 B
-    // B as stored in global memory: bf16 B is N-major (row-major K×N, read as
-    // boxes of 64 columns × BK rows); TF32 B arrives K-major (an N×K copy made
-    // by the host path), read like A as BN rows × 128 B.
-    static constexpr bool B_MN = (IK == InKind::BF16);
-    static constexpr int B_BOX_N = B_MN ? 128 / ES : BN;   // N columns per box
+    // B as stored in global memory, N-major (row-major K×N), read as boxes of
+    // one 128-byte row of N (64 bf16 or 32 TF32 columns) × BK rows.
+    static constexpr int B_BOX_N = 128 / ES;   // N columns per box
     static constexpr int B_BOXES = BN / B_BOX_N;
-    static constexpr int B_BOX_BYTES = B_MN ? BK * 128 : BN * 128;
+    static constexpr int B_BOX_BYTES = BK * 128;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OUT_ES = (OK == OutKind::BF16) ? 2 : 4;
@@ -180,7 +198,7 @@ struct KCfg {
     // ring depth is measured under the same occupancy.
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t IDESC =
-        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
+        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, /*B N-major*/ 1, BM, BN);
     static constexpr int THREADS = 32 * (P_WARPS + 5);
     // Ring slots released per commit. A tcgen05.commit costs the tensor pipe
     // about 67 cycles when the MMAs between commits take less time than the
@@ -200,7 +218,7 @@ struct KCfg {
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(OK != OutKind::S32 || BN <= 128, "exact integer drain keeps BN int32 sums in registers");
     static_assert(PROD == PROD_TMA || PROD == PROD_SYNC || PROD == PROD_CPASYNC, "producer kind");
-    static_assert(PROD == PROD_TMA || (IK == InKind::BF16 && B_MN), "thread-copy producers: bf16 only");
+    static_assert(PROD == PROD_TMA || IK == InKind::BF16, "thread-copy producers: bf16 only");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
@@ -661,12 +679,13 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
         uint32_t it = 0;
         bool ok = true;
         const int num_work = p.num_tiles * p.splits;
-        for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+        for (int w = blockIdx.x, pos = 0; ok && w < num_work; w += gridDim.x, ++pos) {
             const Work wk = work_item(w, p);
             const int mb = wk.mb, nb = wk.nb;
             for (int kb = wk.kb_lo; kb < wk.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
+                const int kc = load_kblock(p, pos, kb, wk.kb_lo, wk.kb_hi);
                 if (!wait_warp(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, p.timeout_ns, p.status,
                                DEV_TIMEOUT_PRODUCER)) {
                     ok = false;
@@ -682,15 +701,11 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                 const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
                 if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) continue;
                 ptx::mbar_arrive_expect_tx_elected(full, C::STAGE_BYTES);
-                ptx::tma_load_2d_elected(sa, &tmA, full, kb * C::BK, mb * C::BM);
-                if constexpr (C::B_MN) {
+                ptx::tma_load_2d_elected(sa, &tmA, full, kc * C::BK, mb * C::BM);
 #pragma unroll
-                    for (int b = 0; b < C::B_BOXES; ++b) {
-                        ptx::tma_load_2d_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
-                                                 nb * BN + b * C::B_BOX_N, kb * C::BK);
-                    }
-                } else {
-                    ptx::tma_load_2d_elected(sa + C::A_BYTES, &tmB, full, kb * C::BK, nb * BN);
+                for (int b = 0; b < C::B_BOXES; ++b) {
+                    ptx::tma_load_2d_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
+                                             nb * BN + b * C::B_BOX_N, kc * C::BK);
                 }
             }
         }
@@ -722,10 +737,12 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
         // 16-byte units) in the start-address field.
         const uint32_t stage0 = ptx::smem_u32(stage_base);
         const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
-        const uint64_t bdesc0 = C::B_MN ? ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024)
-                                        : ptx::sdesc_sw128(stage0 + C::A_BYTES, 16, 1024);
+        // B N-major: boxes B_BOX_BYTES apart (the leading offset), core groups of K-rows
+        // B_SBO apart; a k-slice steps UMMA_K rows of 128 B
+        const uint64_t bdesc0 = ptx::sdesc(stage0 + C::A_BYTES, C::B_BOX_BYTES, InTraits<IK>::B_SBO,
+                                           InTraits<IK>::B_LAYOUT);
         constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
-        constexpr uint64_t B_STEP = C::B_MN ? C::UMMA_K * 128 / 16 : C::UMMA_K * C::ES / 16;
+        constexpr uint64_t B_STEP = C::UMMA_K * 128 / 16;
         constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
         uint32_t it = 0, unit = 0, s = 0, ph = 0;   // (s, ph): ring slot and phase of k-block `it`
         bool ok = true;
@@ -753,7 +770,7 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                     if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
                     // A: K-major rows of 128 B, a k-slice steps UMMA_K elements along the row.
                     // B N-major: a k-slice steps UMMA_K rows of 128 B (boxes B_BOX_BYTES apart,
-                    // the descriptor's leading offset); B K-major: as A.
+                    // the descriptor's leading offset).
                     const uint64_t ad = adesc0 + s * S_STEP;
                     const uint64_t bd = bdesc0 + s * S_STEP;
                     const uint32_t acc = kb > kb0 ? 1u : 0u;

@@ -16,8 +16,9 @@
 //     on the leader's acc_empty[b] (8 arrivals: 4 warps × 2 CTAs).
 // Every TMA load brings a box into the issuing CTA's own shared memory; only
 // the MMA completions (tcgen05.commit) are signalled to both CTAs at once.
-// TF32 inputs (IK = TF32) take B K-major (the host transposes it): each CTA
-// then loads its half of B as one box of BN/2 rows × 128 B, 32 K values deep.
+// TF32 inputs (IK = TF32) take B N-major too, in boxes of 32 columns × 32 K
+// rows swizzled in 32-byte units (the form the tensor core reads 4-byte
+// N-major operands in).
 // Exact integers (OK = S32, int8 widened to bf16) accumulate units of 1024 K
 // values per TMEM buffer and add each unit, converted, into int32 registers:
 // 128 columns per thread, so a 256-wide tile has eight epilogue warps.
@@ -46,13 +47,12 @@ struct PairCfg {
     static constexpr int UMMA_K = InTraits<IK>::UMMA_K;
     static constexpr int KSUB = BK / UMMA_K;
     static constexpr int A_BYTES = ROWS * 128;       // 16 KB
-    static constexpr bool B_MN = (IK == InKind::BF16);   // bf16 B N-major; TF32 B K-major
-    // this CTA's half of B: bf16 in whole 64-column boxes of BK rows (at BN=224
-    // the second box also brings 16 columns the MMA does not read); TF32 as one
-    // box of BN/2 rows of 128 B
-    static constexpr int B_BOX_N = B_MN ? 64 : BN / 2;
-    static constexpr int B_BOXES = B_MN ? (BN / 2 + B_BOX_N - 1) / B_BOX_N : 1;
-    static constexpr int B_BOX_BYTES = B_MN ? BK * 128 : B_BOX_N * 128;
+    // this CTA's half of B, N-major: whole boxes of one 128-byte row of N (64
+    // bf16 or 32 TF32 columns) × BK rows (at BN=224 the last box also brings 16
+    // columns the MMA does not read)
+    static constexpr int B_BOX_N = 128 / ES;
+    static constexpr int B_BOXES = (BN / 2 + B_BOX_N - 1) / B_BOX_N;
+    static constexpr int B_BOX_BYTES = BK * 128;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
     static constexpr int PAIR_TX = 2 * STAGE_BYTES;         // bytes the leader's full[s] expects
@@ -73,7 +73,7 @@ struct PairCfg {
     static constexpr int SMEM_USED = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
     static constexpr int SMEM_BYTES = SMEM_USED > 122880 ? SMEM_USED : 122880;
     static constexpr uint32_t IDESC =
-        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, B_MN ? 1u : 0u, BM, BN);
+        ptx::make_idesc(InTraits<IK>::FMT, InTraits<IK>::FMT, /*A K-major*/ 0, /*B N-major*/ 1, BM, BN);
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;   // producer, MMA issuer, epilogue warps
     // ring slots released per commit, as in the one-SM kernel: each SM's share of a
     // pair k-block (128 rows × BN columns) keeps its tensor pipe as long as a
@@ -87,7 +87,6 @@ struct PairCfg {
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
     static_assert(2 * STAGES + 5 <= 28, "barrier area");
     static_assert(KSUB == 4, "four MMAs per k-block");
-    static_assert(B_MN || (B_BOX_N % 8 == 0 && B_BOX_N <= 256), "K-major B half: whole 8-row swizzle atoms");
 };
 
 // Raises the abort flag of both CTAs of the pair (addr: this CTA's flag).
@@ -292,6 +291,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
+                const int kc = load_kblock(p, u, kb, U.kb_lo, U.kb_hi);
                 if (!wait_warp_pair(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, peer_abort, p.timeout_ns,
                                     p.status, DEV_TIMEOUT_PRODUCER)) {
                     ok = false;
@@ -310,14 +310,11 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                     if (lane == 0) *progress = it + 1;
                     continue;
                 }
-                ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kb * C::BK, row);
+                ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kc * C::BK, row);
 #pragma unroll
                 for (int b = 0; b < C::B_BOXES; ++b) {
                     const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
-                    if constexpr (!C::B_MN)
-                        ptx::tma_load_2d_pair_elected(dst, &tmB, fb, kb * C::BK, col);   // K-major: (k, n)
-                    else
-                        ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kb * C::BK);
+                    ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kc * C::BK);
                 }
                 if (lane == 0) *progress = it + 1;
             }
@@ -342,12 +339,12 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             // start-address field (16-byte units).
             const uint32_t stage0 = ptx::smem_u32(stage_base);
             const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
-            // B N-major: boxes B_BOX_BYTES apart (leading offset), a k-slice steps
-            // UMMA_K rows of 128 B; B K-major: as A, a k-slice steps UMMA_K elements
-            const uint64_t bdesc0 = C::B_MN ? ptx::sdesc_sw128(stage0 + C::A_BYTES, C::B_BOX_BYTES, 1024)
-                                            : ptx::sdesc_sw128(stage0 + C::A_BYTES, 16, 1024);
+            // B N-major: boxes B_BOX_BYTES apart (leading offset), core groups of K-rows
+            // B_SBO apart, a k-slice steps UMMA_K rows of 128 B
+            const uint64_t bdesc0 = ptx::sdesc(stage0 + C::A_BYTES, C::B_BOX_BYTES, InTraits<IK>::B_SBO,
+                                               InTraits<IK>::B_LAYOUT);
             constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
-            constexpr uint64_t B_STEP = C::B_MN ? C::UMMA_K * 128 / 16 : C::UMMA_K * C::ES / 16;
+            constexpr uint64_t B_STEP = C::UMMA_K * 128 / 16;
             constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
             static_assert(C::KSUB == 4, "four MMAs per k-block");
             uint32_t it = 0, unit = 0, s = 0, ph = 0;

@@ -1,7 +1,5 @@
 // Passes that run before or after the GEMM kernel on some paths:
 //   * exact int8 -> bf16 widening (integer GEMM);
-//   * fp32 transpose K×N -> N×K (TF32 GEMM: the tensor cores take its B
-//     operand K-major);
 //   * the fixed-order sum of split-K partial tiles;
 //   * 2-D copies with zero fill, for operands or outputs whose base address or
 //     leading dimension is off the 16-byte grid the tensor copies need.
@@ -199,78 +197,6 @@ cudaError_t launch_splitk_reduce(const float* W, long long ldw, long long rows_p
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, W, ldw, rows_per_split * ldw, splits, C, ldc, M, N,
                               out_bf16);
-}
-
-// dst (cols × rows, leading dimension ld_dst) = transpose of src (rows × cols,
-// leading dimension ld_src), bit for bit, in 64×64 tiles through shared memory
-// (one padding column). A bandwidth-bound pass: when both matrices allow
-// 16-byte vectors (`vec`) a full tile moves as 16-byte loads and stores, each
-// thread with four loads in flight (16 KB per block, 8 blocks per SM); edge
-// tiles go element by element. Reads and writes are coalesced row segments.
-__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ src, long long ld_src,
-                                                             float* __restrict__ dst, long long ld_dst, int rows,
-                                                             int cols, int vec) {
-    __shared__ float tile[64][65];
-    const int tid = threadIdx.x;
-    const int tiles_c = (cols + 63) / 64;
-    const long long tiles = static_cast<long long>((rows + 63) / 64) * tiles_c;
-    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int r0 = static_cast<int>(t / tiles_c) * 64;
-        const int c0 = static_cast<int>(t % tiles_c) * 64;
-        if (vec && r0 + 64 <= rows && c0 + 64 <= cols) {
-            float4 v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {   // source row idx/16, columns 4·(idx%16) ..
-                const int idx = tid + 256 * k;
-                v[k] = *reinterpret_cast<const float4*>(src + static_cast<long long>(r0 + (idx >> 4)) * ld_src + c0 +
-                                                        (idx & 15) * 4);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int idx = tid + 256 * k;
-                float* row = &tile[idx >> 4][(idx & 15) * 4];
-                row[0] = v[k].x;
-                row[1] = v[k].y;
-                row[2] = v[k].z;
-                row[3] = v[k].w;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {   // destination row = source column idx/16, its 4 source rows
-                const int idx = tid + 256 * k;
-                const int cc = idx >> 4, rr = (idx & 15) * 4;
-                const float4 o = make_float4(tile[rr][cc], tile[rr + 1][cc], tile[rr + 2][cc], tile[rr + 3][cc]);
-                *reinterpret_cast<float4*>(dst + static_cast<long long>(c0 + cc) * ld_dst + r0 + rr) = o;
-            }
-        } else {
-            for (int idx = tid; idx < 64 * 64; idx += 256) {
-                const int r = r0 + (idx >> 6), c = c0 + (idx & 63);
-                if (r < rows && c < cols) tile[idx >> 6][idx & 63] = src[static_cast<long long>(r) * ld_src + c];
-            }
-            __syncthreads();
-            for (int idx = tid; idx < 64 * 64; idx += 256) {
-                const int c = c0 + (idx >> 6), r = r0 + (idx & 63);
-                if (c < cols && r < rows) dst[static_cast<long long>(c) * ld_dst + r] = tile[idx & 63][idx >> 6];
-            }
-        }
-        __syncthreads();
-    }
-}
-
-cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
-                                 int cols, int sms, cudaStream_t stream) {
-    const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && ld_src % 4 == 0 &&
-                     reinterpret_cast<uintptr_t>(dst) % 16 == 0 && ld_dst % 4 == 0)
-                        ? 1
-                        : 0;
-    const long long tiles = static_cast<long long>((rows + 63) / 64) * ((cols + 63) / 64);
-    long long blocks = tiles;
-    const long long cap = static_cast<long long>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    transpose_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, ld_src, dst, ld_dst, rows, cols,
-                                                                           vec);
-    return cudaGetLastError();
 }
 
 }  // namespace tcl

@@ -66,9 +66,6 @@ cudaError_t launch_repack(const void* src, long long ld_src, int rows, int cols,
 cudaError_t launch_sgemm_simt(const float* A, long long lda, const float* B, long long ldb, float* C, long long ldc,
                               int M, int N, int K, bool vec, cudaStream_t stream);
 
-// dst (cols × rows) = transpose of src (rows × cols), fp32, bit for bit.
-cudaError_t launch_transpose_f32(const float* src, long long ld_src, float* dst, long long ld_dst, int rows,
-                                 int cols, int sms, cudaStream_t stream);
 
 // One entry per instantiated variant, so the host can validate a requested
 // configuration before it builds tensor maps.
@@ -119,8 +116,10 @@ cudaError_t launch_variant(const LaunchArgs& a) {
 #define TCL_GROUP_BF16_F32_BN256(X) \
     X(BF16, F32, 256, 1, 0) X(BF16, F32, 256, 2, 0) X(BF16, F32, 256, 3, 0) X(BF16, F32, 256, 4, 0)
 #define TCL_GROUP_BF16_F32_BN128(X) \
-    X(BF16, F32, 128, 1, 0) X(BF16, F32, 128, 2, 0) X(BF16, F32, 128, 4, 0) X(BF16, F32, 128, 6, 0)
-#define TCL_GROUP_BF16_MISC(X) X(BF16, BF16, 256, 4, 0) X(BF16, BF16, 128, 6, 0) X(BF16, S32, 128, 6, 0)
+    X(BF16, F32, 128, 1, 0) X(BF16, F32, 128, 2, 0) X(BF16, F32, 128, 4, 0) X(BF16, F32, 128, 6, 0) \
+    X(BF16, F32, 64, 8, 0)
+#define TCL_GROUP_BF16_MISC(X) \
+    X(BF16, BF16, 256, 4, 0) X(BF16, BF16, 128, 6, 0) X(BF16, S32, 128, 6, 0) X(BF16, BF16, 64, 8, 0)
 #define TCL_GROUP_BF16_SYNC(X) X(BF16, F32, 256, 1, 1) X(BF16, F32, 256, 2, 1) X(BF16, F32, 256, 4, 1)
 #define TCL_GROUP_BF16_CPASYNC(X) \
     X(BF16, F32, 256, 1, 2) X(BF16, F32, 256, 2, 2) X(BF16, F32, 256, 3, 2) X(BF16, F32, 256, 4, 2)

@@ -110,7 +110,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.num_tiles = plan.num_tiles;
     p.num_kb = (K + 63) / 64;
     p.kb_per_unit = 1024 / 64;   // exact fp32 units of 1024 K values, as gemm_s8
-    p.group_m = 8;
+    p.group_m = plan.group_m;
     p.timeout_ns = 1000000000ull;
     p.status = status;
     p.trace = nullptr;
@@ -133,6 +133,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.debug_sk_stall = 0;
     p.sk_ws = nullptr;
     p.sk_ws_rows = 0;
+    p.k_serpentine = plan.k_serpentine;
 
     if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
                           {B, ldb, reinterpret_cast<uint16_t*>(b2), ldb2, K, N, 0}, sms, stream) != cudaSuccess) {

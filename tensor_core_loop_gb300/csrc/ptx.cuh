@@ -495,16 +495,23 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading-
 // and stride-dimension byte offsets (all in 16-byte units), the fixed version
 // field 0b001 at bits 46-48, base offset 0 (atoms are 1024-byte aligned) and
-// swizzle mode 2 = 128-byte swizzle at bits 61-63.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
+// the layout type at bits 61-63: 2 = 128-byte swizzle (16-byte units permuted
+// within each 128-byte row, pattern repeating every 8 rows), 1 = 128-byte
+// swizzle with 32-byte atoms (32-byte units permuted, the form the tensor core
+// reads 32-bit MN-major operands in: measured on GB300, a TF32 B stored N-major
+// is read correctly only in this form, with core groups of 4 K-rows).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    return sdesc(saddr, lbo_bytes, sbo_bytes, 2u);
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32 (dense):

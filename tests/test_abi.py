@@ -139,7 +139,23 @@ def test_plan_without_device(L):
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 256, cfg)["bn"] == 128
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 256, cfg)["bn"] == 256
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)     # 4 k-blocks: too short to split
-    assert p["splits"] == 1 and p["grid"] == 16 and p["workspace_bytes"] == 0
+    # ... and 16 tiles of 128 columns fill a tenth of the SMs: 64-wide tiles, 32 CTAs
+    assert p["splits"] == 1 and p["bn"] == 64 and p["grid"] == 32 and p["workspace_bytes"] == 0
+    # split-K shapes keep 128-wide tiles
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 2048, cfg)["bn"] == 128
+    # deep two-SM tiles (rows of A of 16 KB and more): a row of tiles at a time, K walked
+    # in alternating directions; shorter rows keep groups of 8 and ascending K
+    for in_kind, k in ((tcl.IN_BF16, 8192), (tcl.IN_TF32, 4096)):
+        p = tcl.plan(in_kind, tcl.OUT_F32, 4096, 4096, k, cfg)
+        assert (p["cta_pair"], p["group_m"], p["k_serpentine"]) == (2, 1, 1)
+    for k in (1024, 4096):
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, cfg)
+        assert (p["group_m"], p["k_serpentine"]) == (8, 0)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, group_m=4, k_order=1))
+    assert (p["group_m"], p["k_serpentine"]) == (4, 0)
+    for bad in (tcl.Config(max_ctas=152, k_order=3), tcl.Config(max_ctas=152, k_order=2, producer=1)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 1024, 1024, 1024, bad)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 8192, cfg)
     assert p["splits"] == 9 and p["grid"] == 144
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 8192, tcl.Config(max_ctas=152, split_k=1))

@@ -96,7 +96,7 @@ def test_headline_plan_replays():
 
 
 def test_split_k_and_tf32_replay():
-    # split-K partial tiles and the TF32 transpose live in library scratch
+    # split-K partial tiles (and off-grid copies) live in library scratch
     a, b = inputs.bf16_pair(512, 512, 4096, seed=34)
     a, b = a.to(DEV), b.to(DEV)
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 4096)["splits"] > 1

@@ -312,11 +312,11 @@ def test_tf32_off_grid_operands(oracle_mod):
 @pytest.mark.parametrize("M,N,K,cfg", [
     (512, 512, 512, dict(cta_pair=2)),
     (300, 452, 200, dict(cta_pair=2)),                       # ragged: the peer CTA's rows past M
-    (1024, 1000, 1004, dict(cta_pair=2, bn=224)),            # K-major B half of 112 rows; K % 32 = 12
+    (1024, 1000, 1004, dict(cta_pair=2, bn=224)),            # B half of 112 columns in 4 boxes; K % 32 = 12
     (768, 768, 2048, dict(cta_pair=2, max_ctas=8, stream_k=3)),   # stream-K pieces added by TMA reductions
 ])
 def test_tf32_pair_kernel(oracle_mod, M, N, K, cfg):
-    # TF32 on two SMs per tile: kind::tf32 pair MMAs, B K-major, 32-deep k-blocks
+    # TF32 on two SMs per tile: kind::tf32 pair MMAs, B N-major (32-byte swizzle units), 32-deep k-blocks
     c = tcl.Config(**cfg)
     assert tcl.plan(tcl.IN_TF32, 0, M, N, K, c)["cta_pair"] == 2
     a, b = inputs.tf32_pair(M, N, K, seed=M + N)
@@ -411,6 +411,39 @@ def test_split_k_deterministic():
     assert torch.equal(tcl.gemm(a, b, cfg=tcl.Config(split_k=9, max_ctas=40)), first)
 
 
+@pytest.mark.parametrize("M,N,K,cfg", [
+    (1024, 1280, 2048, dict(cta_pair=2, max_ctas=4, stream_k=1)),   # 2 pairs walk 10 tiles each
+    (768, 768, 2048, dict(cta_pair=2, max_ctas=8, stream_k=2)),     # with a stream-K tail
+    (700, 750, 2000, dict(cta_pair=2, max_ctas=4)),                 # ragged M, N and last k-block
+    (640, 768, 1216, dict(cta_pair=1, bn=128, max_ctas=3, split_k=1)),   # one SM per tile, 10 tiles per CTA
+])
+def test_bf16_alternating_k_order(oracle_mod, M, N, K, cfg):
+    # every second tile of a CTA's walk loads K in descending order: a different fp32
+    # summation order, within the same bound, and the same bits on every run
+    c = tcl.Config(k_order=2, **cfg)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K, c)["k_serpentine"] == 1
+    ldc = up(N, 4)
+    bf16_case(oracle_mod, M, N, K, seed=K + M, cfg=c, ldc=ldc)
+    a, b = inputs.bf16_pair(M, N, K, seed=K + M, lda=up(K, 8), ldb=up(N, 8))
+    a, b = to_dev(a), to_dev(b)
+    first = run(a, b, cfg=c, ldc=ldc, canary=False)
+    assert torch.equal(run(a, b, cfg=c, ldc=ldc, canary=False), first)
+
+
+def test_alternating_k_order_exact_and_tf32(oracle_mod):
+    # int8: each accumulation unit still holds at most 1024 products, so the int32
+    # result is exact and equal to the ascending order's; TF32 within its bound
+    a, b = inputs.s8_pair(1024, 1024, 2112, seed=51)
+    asc = run(a.to(DEV), b.to(DEV), cfg=tcl.Config(cta_pair=2, max_ctas=4, k_order=1)).numpy()
+    alt = run(a.to(DEV), b.to(DEV), cfg=tcl.Config(cta_pair=2, max_ctas=4, k_order=2)).numpy()
+    assert_exact(alt, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 alternating K order")
+    assert (asc == alt).all()
+    a, b = inputs.tf32_pair(768, 1024, 1504, seed=52)
+    got = run(a.to(DEV), b.to(DEV), cfg=tcl.Config(cta_pair=2, max_ctas=4, k_order=2)).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, "tf32 alternating K order")
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""
@@ -482,6 +515,32 @@ def test_tf32_small(oracle_mod, M, N, K):
     got = run(to_dev(a), to_dev(b)).double().numpy()
     ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
     assert_within("tf32", got, ref, S, f"tf32 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K,split", [(512, 512, 256, 1), (512, 512, 1024, 1), (300, 200, 520, 1),
+                                         (512, 512, 2048, 4), (130, 72, 64, 1)])
+def test_bf16_64_wide_tiles(oracle_mod, out, M, N, K, split):
+    # 64-wide one-SM tiles (one B box per stage, 8 stages), with and without split-K;
+    # ragged right edges inside the single 64-column box
+    cfg = tcl.Config(bn=64, split_k=split)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32 if out == torch.float32 else tcl.OUT_BF16, M, N, K, cfg)
+    assert pl["bn"] == 64 and pl["cta_pair"] == 1 and pl["splits"] == split
+    ldc = up(N, 4 if out == torch.float32 else 8)
+    bf16_case(oracle_mod, M, N, K, seed=M + N + K, out_dtype=out, cfg=cfg, ldc=ldc)
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1004), (200, 300, 96), (384, 264, 32)])
+def test_tf32_one_sm_kernel(oracle_mod, bn, M, N, K):
+    # TF32 on one SM per tile with B read N-major in place: boxes of 32 columns, the last
+    # one ragged (N % 32 != 0) or past N, K ragged within the last 32-deep k-block
+    a, b = inputs.tf32_pair(M, N, K, seed=M + K + bn)
+    cfg = tcl.Config(cta_pair=1, bn=bn, split_k=1)
+    assert tcl.plan(tcl.IN_TF32, 0, M, N, K, cfg)["cta_pair"] == 1
+    got = run(a.to(DEV), b.to(DEV), cfg=cfg, ldc=up(N, 4)).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, f"tf32 one SM bn {bn} {M}x{N}x{K}")
 
 
 def test_tf32_padded(oracle_mod):

@@ -171,6 +171,13 @@ typedef struct {
                                       on the operand blocks the previous wave read last (still in
                                       L2). The order changes the fp32 summation order of those
                                       tiles (not the exact int32 result). TMA producer only */
+    int s8_path;                   /* gemm_s8 only: 0 automatic (= 1); 1 widening pass (int8 -> bf16
+                                      copies of A and B in library scratch, then the GEMM); 2 widening
+                                      inside the two-SM kernel (TMA copies the raw int8 tiles into
+                                      shared memory, converter warps store them as fp16 into the MMA's
+                                      stages; no scratch; needs 256-wide two-SM tiles and A, B 16-byte
+                                      aligned with lda, ldb multiples of 16, else TCL_ERR_CONFIG /
+                                      TCL_ERR_ALIGN). 2 is exact like 1 but slower on GB300 */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -185,10 +192,12 @@ TCL_API int gemm_tf32(int M, int N, int K, const float* A, int lda, const float*
               int ldc, cudaStream_t stream);
 
 /* int8 A, B; exact int32 C (bit-exact integer result for K <= 131071).
- * The operands are widened exactly to bf16 in library scratch, the tensor
- * cores accumulate in fp32 in units of at most 1024 K values (every partial
- * sum is an integer of magnitude at most 2^24, hence exact in fp32), and each
- * unit is added into int32 registers. */
+ * The operands are widened exactly to 16-bit floats (every int8 value is one):
+ * by default a widening pass writes bf16 copies of A and B into library
+ * scratch (tcl_config_t.s8_path selects the in-kernel widening instead), the
+ * tensor cores accumulate in fp32 in units of at most 1024 K values (every
+ * partial sum is an integer of magnitude at most 2^24, hence exact in fp32),
+ * and each unit is added into int32 registers. */
 TCL_API int gemm_s8(int M, int N, int K, const int8_t* A, int lda, const int8_t* B, int ldb, int32_t* C,
             int ldc, cudaStream_t stream);
 
@@ -276,6 +285,8 @@ typedef struct {
     int sk_pieces;                  /* K ranges per stream-K tile */
     int group_m;                    /* raster group height in tiles */
     int k_serpentine;               /* 1: alternating K order (see tcl_config_t.k_order) */
+    int s8_in_kernel;               /* int8: 1 if the kernel widens the operands itself
+                                       (tcl_config_t.s8_path = 2), 0 for the widening pass */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

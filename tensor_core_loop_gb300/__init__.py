@@ -68,6 +68,7 @@ class Config(ctypes.Structure):
         ("serial_launch", ctypes.c_int),
         ("debug_stream_k_stall", ctypes.c_int),
         ("k_order", ctypes.c_int),
+        ("s8_path", ctypes.c_int),
     ]
 
 
@@ -87,6 +88,7 @@ class PlanInfo(ctypes.Structure):
         ("sk_pieces", ctypes.c_int),
         ("group_m", ctypes.c_int),
         ("k_serpentine", ctypes.c_int),
+        ("s8_in_kernel", ctypes.c_int),
     ]
 
 

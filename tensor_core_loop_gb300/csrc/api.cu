@@ -224,6 +224,7 @@ struct Plan {
     int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
     int sk_tiles, sk_pieces;    // stream-K tail of the two-SM kernel (0 tiles: none)
     int k_serpentine;           // odd units of a CTA's walk load K in descending order
+    int s8_in_kernel;           // int8: the two-SM kernel that widens the operands itself
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -422,6 +423,22 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     const int want_ko = cfg ? cfg->k_order : 0;
     if (want_ko < 0 || want_ko > 2 || (want_ko == 2 && prod != PROD_TMA)) return TCL_ERR_CONFIG;
     pl->k_serpentine = want_ko == 2 ? 1 : want_ko == 1 ? 0 : (deep ? 1 : 0);
+    // int8 on 256-wide pair tiles can widen its operands inside the kernel (no pass
+    // over HBM), on request only: measured on GB300 it is slower than the widening
+    // pass followed by the bf16-input kernel (4096³: 142 against 95 µs, CUDA graphs
+    // of back-to-back calls), its stages being bound by the converter warps'
+    // shared-memory traffic and instruction latency
+    const int want_s8 = cfg ? cfg->s8_path : 0;
+    if (want_s8 < 0 || want_s8 > 2 || (want_s8 && ok != OutKind::S32)) return TCL_ERR_CONFIG;
+    pl->s8_in_kernel = (ok == OutKind::S32 && pair && bn == 256 && want_s8 == 2 && !(cfg && cfg->stages) &&
+                        !(cfg && cfg->epi_slots > 1))
+                           ? 1
+                           : 0;
+    if (want_s8 == 2 && !pl->s8_in_kernel) return TCL_ERR_CONFIG;
+    if (pl->s8_in_kernel) {   // its own ring (fp16 stages fed from raw int8 slots)
+        pl->stages = s8_pair_stages();
+        pl->smem = s8_pair_smem_bytes();
+    }
     // Split-K (one-SM kernel, floating-point output): when the output tiles
     // alone would leave most SMs idle, cut K into ranges computed by different
     // CTAs; a second kernel adds the partial tiles in a fixed order.
@@ -557,13 +574,22 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.pdl = !(cfg && cfg->serial_launch);
     a.grid = pl.grid;
     a.stream = stream;
-    if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
-    // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
-    // 4-byte elements are swizzled in 32-byte units, the form the tensor core
-    // reads an N-major 32-bit operand in
-    if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB,
-                         ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)))
-        return st;
+    if (pl.s8_in_kernel) {
+        // raw int8 operands, unswizzled: A in boxes of 64 K × 128 rows, B of 128 columns × 64 K
+        if ((st = tensor_map(dev, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 64, kBM, &a.tmA,
+                             CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+            (st = tensor_map(dev, B, CU_TENSOR_MAP_DATA_TYPE_UINT8, N, K, ldb, 128, 64, &a.tmB,
+                             CU_TENSOR_MAP_SWIZZLE_NONE)))
+            return st;
+    } else {
+        if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
+        // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
+        // 4-byte elements are swizzled in 32-byte units, the form the tensor core
+        // reads an N-major 32-bit operand in
+        if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB,
+                             ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)))
+            return st;
+    }
     void* out_ptr = split ? workspace : C;
     const long long out_ld = split ? ws.ld : ldc;
     const long long out_rows = split ? ws.rows_per_split * pl.splits : M;
@@ -615,7 +641,10 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
 
     bool found = false;
     cudaError_t err = cudaSuccess;
-    if (pl.pair) {
+    if (pl.s8_in_kernel) {
+        found = true;
+        err = launch_s8_pair(a);
+    } else if (pl.pair) {
         err = launch_group_pair(a, &found);
     } else if (ik == InKind::TF32) {
         err = launch_group_tf32(a, &found);
@@ -756,7 +785,7 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
                  int ldc, const tcl_config_t* cfg, cudaStream_t stream) {
     int st = check_common(M, N, K, A, lda, B, ldb, C, ldc);
     if (st) return st;
-    if (!aligned_to(C, 4)) return TCL_ERR_ALIGN;   // int8 operands: any alignment (always repacked)
+    if (!aligned_to(C, 4)) return TCL_ERR_ALIGN;   // int8 operands: any alignment (repacked when needed)
     if (K > 131071) return TCL_ERR_K_TOO_LARGE;
     const bool pack_c = !aligned16(C) || ldc % 4;
     const long long ldc2 = round_up(N, 4);
@@ -766,22 +795,33 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     if ((st = current_device(&dev, &ds))) return st;
     Plan pl;
     if ((st = plan_on_device(InKind::BF16, OutKind::S32, M, N, K, cfg, ds, &pl))) return st;
-    // Packed bf16 copies of A (M × lda2) and B (K × ldb2), each 256-byte aligned.
-    const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
-    const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
-    const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
+    // The in-kernel widening copies the int8 rows with tensor copies: 16-byte rows only.
+    if (pl.s8_in_kernel && !(aligned16(A) && aligned16(B) && lda % 16 == 0 && ldb % 16 == 0)) return TCL_ERR_ALIGN;
     const long long c_bytes = pack_c ? round_up(static_cast<long long>(M) * ldc2 * 4, 256) : 0;
-    if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes + c_bytes), stream))) return st;
-    uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
-    uint8_t* b2 = a2 + a_bytes;
-    int32_t* c2 = pack_c ? reinterpret_cast<int32_t*>(b2 + b_bytes) : nullptr;
-    if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
-                          {B, ldb, reinterpret_cast<uint16_t*>(b2), ldb2, K, N, 0}, ds->sms, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return TCL_ERR_LAUNCH;
+    int32_t* c2 = nullptr;
+    if (pl.s8_in_kernel) {
+        if (c_bytes && (st = ensure_scratch(ds, static_cast<size_t>(c_bytes), stream))) return st;
+        if (pack_c) c2 = static_cast<int32_t*>(ds->scratch);
+        st = run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, A, lda, B, ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc,
+                      nullptr, cfg, dev, ds, stream);
+    } else {
+        // Packed bf16 copies of A (M × lda2) and B (K × ldb2), each 256-byte aligned.
+        const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
+        const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
+        const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
+        if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes + c_bytes), stream))) return st;
+        uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
+        uint8_t* b2 = a2 + a_bytes;
+        if (pack_c) c2 = reinterpret_cast<int32_t*>(b2 + b_bytes);
+        if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
+                              {B, ldb, reinterpret_cast<uint16_t*>(b2), ldb2, K, N, 0}, ds->sms,
+                              stream) != cudaSuccess) {
+            cudaGetLastError();
+            return TCL_ERR_LAUNCH;
+        }
+        st = run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, pack_c ? c2 : C,
+                      pack_c ? ldc2 : ldc, nullptr, cfg, dev, ds, stream);
     }
-    st = run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, pack_c ? c2 : C,
-                  pack_c ? ldc2 : ldc, nullptr, cfg, dev, ds, stream);
     if (st) return st;
     if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, 4, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -1043,6 +1083,7 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->sk_pieces = pl.sk_pieces;
         plan->group_m = pl.group_m;
         plan->k_serpentine = pl.k_serpentine;
+        plan->s8_in_kernel = pl.s8_in_kernel;
     }
     return TCL_OK;
 }

@@ -36,6 +36,13 @@ cudaError_t launch_group_pair(const LaunchArgs& a, bool* found);
 // resident at once on the current device (0 on error).
 int pair_max_clusters(InKind in, OutKind out, int bn, int stages, int slots);
 cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
+// Two-SM int8 kernel that widens its operands itself (k_s8_pair.cu): a.tmA and
+// a.tmB map the int8 matrices (unswizzled boxes of 64 K × 128 rows and 128
+// columns × 64 K), a.tmC the int32 output; s8_pair_stages() fp16 stages.
+cudaError_t launch_s8_pair(const LaunchArgs& a);
+int s8_pair_stages();
+int s8_pair_smem_bytes();
+int s8_pair_max_clusters();
 
 // int8 -> bf16 widening (exact) of two matrices in one launch: rows × cols of
 // src (leading dimension ld_src) into a packed row-major buffer dst with ld_dst

@@ -60,6 +60,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with acquire semantics at cluster scope: for a barrier on which
+// threads of the other CTA of the pair arrive with release semantics.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled load of one box into shared memory; completion is signalled on
 // `bar` as transaction bytes. c0 is the innermost (contiguous) coordinate.
@@ -398,6 +412,31 @@ __device__ __forceinline__ void tma_load_2d_pair_elected(uint32_t dst, const CUt
         "@el cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Per-warp register budget changes (all warps of a warpgroup execute the same
+// one): dec releases registers down to N per thread, inc waits until N per
+// thread can be granted from what the block's warps released.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to the
+// shared memory of a CTA of the cluster (shared::cluster addresses for the
+// destination and its mbarrier), completed there as transaction bytes on that
+// mbarrier. Asynchronous: the issuing thread does not wait.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
         : "memory");
 }
 

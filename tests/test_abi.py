@@ -153,6 +153,18 @@ def test_plan_without_device(L):
         assert (p["group_m"], p["k_serpentine"]) == (8, 0)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, group_m=4, k_order=1))
     assert (p["group_m"], p["k_serpentine"]) == (4, 0)
+    # int8 on 256-wide pair tiles widens inside the kernel on request (s8_path 2) only
+    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, cfg)
+    assert (p["cta_pair"], p["bn"], p["s8_in_kernel"]) == (2, 256, 0)
+    p = tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, s8_path=2))
+    assert (p["s8_in_kernel"], p["stages"]) == (1, 4)
+    assert tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, s8_path=1))["s8_in_kernel"] == 0
+    assert tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, cta_pair=1))["s8_in_kernel"] == 0
+    for bad in (tcl.Config(max_ctas=152, cta_pair=1, s8_path=2), tcl.Config(max_ctas=152, s8_path=3)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, bad)
+    with pytest.raises(tcl.TclError):
+        tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, s8_path=2))
     for bad in (tcl.Config(max_ctas=152, k_order=3), tcl.Config(max_ctas=152, k_order=2, producer=1)):
         with pytest.raises(tcl.TclError):
             tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 1024, 1024, 1024, bad)

@@ -641,6 +641,40 @@ def test_s8_pair_stream_k_exact(oracle_mod, M, N, K, pieces, bn):
     assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), f"s8 stream-K {M}x{N}x{K} bn {bn}")
 
 
+@pytest.mark.parametrize("M,N,K,extra", [
+    (512, 384, 4096, {}),
+    (300, 200, 1100, {}),                            # K % 16 = 12 and N % 16 = 8: chunks cut by the row ends
+    (1000, 700, 520, {}),                            # 520 = 8 k-blocks + 8: a ragged last k-block
+    (700, 750, 1000, dict(max_ctas=8, stream_k=4)),  # stream-K pieces, ragged M and N
+    (768, 1024, 1536, dict(max_ctas=8)),             # 4 pairs walk 3 tiles each
+    (1024, 1024, 2112, dict(max_ctas=4, k_order=2)), # alternating K order
+])
+def test_s8_in_kernel_widening_exact(oracle_mod, M, N, K, extra):
+    # the two-SM kernel that widens int8 to fp16 itself (converter warps, no scratch) against
+    # the oracle and against the widening pass (bf16 copies in scratch), bit for bit
+    a, b = inputs.s8_pair(M, N, K, seed=M + K, lda=up(K, 16), ldb=up(N, 16))
+    ref = oracle_mod.gemm_s8(a.numpy(), b.numpy())
+    outs = {}
+    for path in (2, 1):
+        cfg = tcl.Config(cta_pair=2, bn=256, s8_path=path, **extra)
+        assert tcl.plan(tcl.IN_S8, 0, M, N, K, cfg)["s8_in_kernel"] == (1 if path == 2 else 0)
+        outs[path] = run(to_dev(a), to_dev(b), cfg=cfg).numpy()
+        assert_exact(outs[path], ref, f"s8 {M}x{N}x{K} path {path}")
+    assert (outs[1] == outs[2]).all()
+
+
+def test_s8_in_kernel_needs_aligned_rows(oracle_mod):
+    # rows of A off the 16-byte grid: the in-kernel widening (its tensor copies need 16-byte
+    # rows) is refused, the automatic path (the widening pass) is exact
+    a, b = inputs.s8_pair(600, 520, 1000, seed=3, lda=1001, ldb=528)
+    ad, bd = to_dev(a), to_dev(b)
+    got = run(ad, bd, cfg=tcl.Config(cta_pair=2, bn=256)).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 unaligned rows, automatic path")
+    c = torch.empty((600, 520), dtype=torch.int32, device=DEV)
+    with pytest.raises(tcl.TclError):
+        tcl.gemm_into(ad, bd, c, cfg=tcl.Config(cta_pair=2, bn=256, s8_path=2))
+
+
 @pytest.mark.parametrize("bn", [128, 256])
 def test_s8_pair_kernel_grid_smaller_than_tiles(oracle_mod, bn):
     # 4 pairs walk more tiles than they are: each pair's accumulator units cycle through both

@@ -122,3 +122,21 @@ def test_trace_shows_loads_ahead_of_mma(pair):
     # tracing changes nothing in the result
     ref = tcl.gemm(a, b, cfg=tcl.Config(bn=256, stages=4, cta_pair=pair, split_k=1))
     assert torch.equal(c, ref)
+
+
+def test_s8_in_kernel_bounded_wait_runs_out():
+    # CTA 0's converter warps never hand one k-block over: the leader's MMA warp's bounded
+    # wait for the stage runs out, both CTAs of the pair abort and return, and the next
+    # call on the same device is exact
+    a = torch.randint(-128, 128, (1024, 1024), dtype=torch.int8, generator=torch.Generator().manual_seed(3)).to(DEV)
+    b = torch.randint(-128, 128, (1024, 1024), dtype=torch.int8, generator=torch.Generator().manual_seed(4)).to(DEV)
+    c = torch.zeros((1024, 1024), dtype=torch.int32, device=DEV)
+    cfg = tcl.Config(cta_pair=2, bn=256, s8_path=2, timeout_ns=50_000_000, debug_skip_kblock=3)
+    tcl.gemm_into(a, b, c, cfg=cfg)
+    st, code = tcl.last_device_error()
+    assert st == 7 and code in (1, 2, 3, 4), (st, code)
+    x = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=2, bn=256, s8_path=2))
+    y = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=1))
+    torch.cuda.synchronize()
+    assert torch.equal(x, y)
+    assert tcl.last_device_error() == (0, 0)

@@ -153,7 +153,12 @@ typedef struct {
                                       adds its result with a TMA reduction after range i-1 has
                                       finished, so the sum order is fixed); 1 never; s in 2..4
                                       exactly s ranges per tail tile of 256-wide tiles
-                                      (TCL_ERR_CONFIG if they do not fit). Calls with a stream-K tail share progress flags on
+                                      (TCL_ERR_CONFIG if they do not fit); 5 balanced: all waves of
+                                      whole tiles but the last full one as usual, then the k-blocks of
+                                      the remaining tiles cut into one equal range per pair, ranges
+                                      crossing tile boundaries (a cut tile has two pieces; on request
+                                      only: it was measured slower than equal pieces on GB300).
+                                      Calls with a stream-K tail share progress flags on
                                       the device and must not run concurrently with one another */
     int serial_launch;             /* 0 (default): the GEMM kernels are launched with programmatic
                                       stream serialisation, so their set-up (barriers, TMEM, cluster
@@ -283,6 +288,7 @@ typedef struct {
     unsigned long long workspace_bytes;   /* library scratch for split-K partial tiles */
     int sk_tiles;                   /* tail tiles computed stream-K (0: none) */
     int sk_pieces;                  /* K ranges per stream-K tile */
+    int sk_balanced;                /* 1: balanced stream-K (sk_tiles = tiles cut by range boundaries) */
     int group_m;                    /* raster group height in tiles */
     int k_serpentine;               /* 1: alternating K order (see tcl_config_t.k_order) */
     int s8_in_kernel;               /* int8: 1 if the kernel widens the operands itself

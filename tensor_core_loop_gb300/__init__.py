@@ -86,6 +86,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_ulonglong),
         ("sk_tiles", ctypes.c_int),
         ("sk_pieces", ctypes.c_int),
+        ("sk_balanced", ctypes.c_int),
         ("group_m", ctypes.c_int),
         ("k_serpentine", ctypes.c_int),
         ("s8_in_kernel", ctypes.c_int),

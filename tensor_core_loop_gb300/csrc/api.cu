@@ -223,6 +223,7 @@ struct Plan {
     int sk_ws_rows;   // bf16 C with a stream-K tail: fp32 workspace rows (split tiles × 256), else 0
     int splits, kb_per_split;   // split-K: K cut into `splits` ranges of kb_per_split k-blocks
     int sk_tiles, sk_pieces;    // stream-K tail of the two-SM kernel (0 tiles: none)
+    int sk_balanced, sk_first, sk_region;   // balanced stream-K (see GemmParams)
     int k_serpentine;           // odd units of a CTA's walk load K in descending order
     int s8_in_kernel;           // int8: the two-SM kernel that widens the operands itself
 };
@@ -244,6 +245,7 @@ constexpr long long kPairKbCycles224 = 491;
 // Stream-K tail: at most this many pieces per split tile (each waits for the
 // previous one before adding its result) and at least this many k-blocks each.
 constexpr int kMaxSkPieces = 4;
+constexpr int kSkBalanced = 5;   // tcl_config_t.stream_k value asking for balanced stream-K
 constexpr int kMinKbPerPiece = 8;
 // ... and only for tiles of at least this many k-blocks: below it the tile's
 // epilogue is a large share of its time and the extra piece's epilogue eats
@@ -283,6 +285,28 @@ long long pair_cost(long long tiles, int pairs, int num_kb, long long kb_cycles,
     const long long waves = tiles / pairs;
     return (waves * num_kb + (num_kb + sk_pieces - 1) / sk_pieces) * kb_cycles +
            (waves == 0 ? (sk_pieces - 1) * kSkLinkCycles : 0);
+}
+
+// Balanced stream-K over `pairs` pairs: the whole tiles of all waves but the
+// last full one are dealt out as usual, and the k-blocks of the remaining
+// tiles (between one and two waves of them) are cut into one equal range per
+// pair. *split counts the tiles a range boundary cuts (two pieces each).
+struct Balanced {
+    int first, region, split;
+    long long busiest_kb;   // k-blocks of the busiest pair
+};
+
+Balanced balanced_split(long long tiles, int pairs, int num_kb) {
+    Balanced b{0, 0, 0, 0};
+    if (tiles < pairs || pairs < 2) return b;
+    const long long waves = tiles / pairs - 1;
+    b.first = static_cast<int>(waves * pairs);
+    b.region = static_cast<int>(tiles - b.first);
+    const long long total = static_cast<long long>(b.region) * num_kb;
+    for (int c = 0; c + 1 < pairs; ++c)
+        if ((total * (c + 1) / pairs) % num_kb) ++b.split;
+    b.busiest_kb = waves * num_kb + (total + pairs - 1) / pairs;
+    return b;
 }
 
 // slots = 0 matches any staging depth (the first listed, i.e. two slabs per warp)
@@ -340,7 +364,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     // stream-K pieces add into C (fp32, int32) or, for a bf16 C (which must be rounded
     // once), into an fp32 workspace that the last piece adds before rounding
     const bool sk_capable = ok == OutKind::F32 || ok == OutKind::S32 || ok == OutKind::BF16;
-    if (want_sk < 0 || want_sk > kMaxSkPieces || (want_sk > 1 && (!pair || !sk_capable))) return TCL_ERR_CONFIG;
+    if (want_sk < 0 || want_sk > kSkBalanced || (want_sk > 1 && (!pair || !sk_capable))) return TCL_ERR_CONFIG;
     if (pair) {
         if (bn == 0) {
             // Pair tile width: the fewest SM cycles on the busiest pair of SMs,
@@ -469,6 +493,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->sk_tiles = 0;
     pl->sk_pieces = 1;
     pl->sk_ws_rows = 0;
+    pl->sk_balanced = pl->sk_first = pl->sk_region = 0;
     if (pair) {
         const int cl = 2;   // CTAs per cluster: one pair
         int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / cl : pair_clusters(v);
@@ -481,22 +506,47 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             // (a bf16 C adds its workspace round trip, yet the same threshold holds: measured
             // on GB300 at 4096², the tail against none at K = 2048 42.2 vs 42.2 µs, at 3072
             // 58.3 vs 59.7, at 4096 75.7 vs 78.1)
-            const int st = stream_k_split(pl->num_tiles, pl->grid / cl, pl->num_kb, want_sk, &pl->sk_tiles,
-                                          &pl->sk_pieces);
+            const int pairs = pl->grid / cl;
+            const int st = want_sk == kSkBalanced ? TCL_OK
+                                                  : stream_k_split(pl->num_tiles, pairs, pl->num_kb, want_sk,
+                                                                   &pl->sk_tiles, &pl->sk_pieces);
             if (st) return st;
+            // Balanced stream-K (on request): every pair gets the same number of k-blocks,
+            // ranges crossing tile boundaries. It shortens the busiest pair's walk at 4096³
+            // (216 against 224 k-blocks) but was measured slower on GB300 (CUDA graphs,
+            // round robin: 91.3 against 83.1 µs for an fp32 C, 87.6 against 83.1 for a bf16
+            // C, 174.8 against 167.1 at 4096²×8192, 50.5 against 45.0 at 4096²×2048): the
+            // 72 cut tiles' extra stores and reductions land together at the end of the
+            // launch, where the equal-piece tail has 28.
+            const Balanced bs = balanced_split(pl->num_tiles, pairs, pl->num_kb);
+            if (want_sk == kSkBalanced) {
+                if (!bs.region || pairs - 1 > kMaxSkTiles) {   // flags and workspace per range boundary
+                    if (want_sk == kSkBalanced) return TCL_ERR_CONFIG;
+                } else {
+                    pl->sk_balanced = 1;
+                    pl->sk_first = bs.first;
+                    pl->sk_region = bs.region;
+                    pl->sk_tiles = bs.split;
+                    pl->sk_pieces = 2;
+                }
+            }
             if (pl->sk_tiles > kMaxSkTiles) {   // the progress flags hold kMaxSkTiles tiles
                 if (want_sk > 1) return TCL_ERR_CONFIG;
                 pl->sk_tiles = 0;
                 pl->sk_pieces = 1;
+                pl->sk_balanced = 0;
             }
             const int resident = cfg && cfg->max_ctas > 0 ? pair_clusters(v) : pl->grid / cl;   // 0: no device
-            if (pl->sk_tiles && resident > 0 && pl->grid / cl > resident) {
+            if ((pl->sk_tiles || pl->sk_balanced) && resident > 0 && pl->grid / cl > resident) {
                 if (want_sk > 1) return TCL_ERR_CONFIG;
                 pl->sk_tiles = 0;
                 pl->sk_pieces = 1;
+                pl->sk_balanced = 0;
             }
         }
-        if (ok == OutKind::BF16 && pl->sk_tiles) pl->sk_ws_rows = pl->sk_tiles * 2 * kBM;
+        // a bf16 C's fp32 workspace: one block per split tile (per range boundary when balanced)
+        if (ok == OutKind::BF16 && (pl->sk_tiles || pl->sk_balanced))
+            pl->sk_ws_rows = (pl->sk_balanced ? pl->grid / cl : pl->sk_tiles) * 2 * kBM;
     } else if (want_sk > 1) {
         return TCL_ERR_CONFIG;
     } else if (cfg && cfg->one_cta_per_tile) {
@@ -623,6 +673,9 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.debug_skip_kb = cfg && cfg->debug_skip_kblock > 0 ? cfg->debug_skip_kblock - 1 : -1;
     p.sk_tiles = pl.sk_tiles;
     p.sk_pieces = pl.sk_pieces;
+    p.sk_balanced = pl.sk_balanced;
+    p.sk_first = pl.sk_first;
+    p.sk_region = pl.sk_region;
     p.debug_sk_stall = cfg && cfg->debug_stream_k_stall ? 1 : 0;
     p.sk_flags = ds->sk_flags;
     p.sk_gen = 0;
@@ -633,7 +686,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
         p.sk_ws = static_cast<float*>(workspace);
         p.sk_ws_rows = pl.sk_ws_rows;
     }
-    if (pl.sk_tiles) {
+    if (pl.sk_tiles || pl.sk_balanced) {
         ds->sk_gen = (ds->sk_gen + 1) & 0x1FFFFFFFu;   // flags hold gen·8 + pieces done in 32 bits
         if (ds->sk_gen == 0) ds->sk_gen = 1;           // 0 is what the flags start as
         p.sk_gen = ds->sk_gen;
@@ -1081,6 +1134,7 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->workspace_bytes = static_cast<unsigned long long>(split_workspace(pl, M, N).bytes);
         plan->sk_tiles = pl.sk_tiles;
         plan->sk_pieces = pl.sk_pieces;
+        plan->sk_balanced = pl.sk_balanced;
         plan->group_m = pl.group_m;
         plan->k_serpentine = pl.k_serpentine;
         plan->s8_in_kernel = pl.s8_in_kernel;

@@ -106,6 +106,15 @@ struct GemmParams {
     // result, piece i > 0 adds its own once piece i-1 has finished (flags).
     int sk_tiles;                // 0: every tile is whole
     int sk_pieces;               // K ranges per split tile (>= 2 when sk_tiles > 0)
+    // Balanced stream-K (sk_balanced = 1): the tiles from sk_first on (sk_region of
+    // them) are not dealt out whole; their k-blocks, in tile order, are cut into one
+    // equal range per pair, so a pair's range may begin inside one tile and end inside
+    // another. A tile cut by the boundary between pairs b and b+1 has two pieces: the
+    // head [0, k) run by pair b (stored), the rest run by pair b+1 (added after the
+    // head); the boundary's number b indexes its flags and workspace. sk_pieces is 2.
+    int sk_balanced;
+    int sk_first;
+    int sk_region;
     unsigned int* sk_flags;      // [sk_tiles][2 CTAs][epilogue warp] progress flags
     unsigned int sk_gen;         // this launch's flag generation (flags hold gen·8 + pieces done)
     int debug_sk_stall;          // test hook: piece 0 of split tile 0 never publishes its flag

@@ -138,13 +138,74 @@ struct PairUnit {
     int tile, kb_lo, kb_hi, piece, sk_index;   // sk_index: split-tile number, -1 for a whole tile
 };
 
+// Balanced stream-K: pair c's share of the region's k-blocks, [lo, hi) in the
+// tile-major order of the region, as (tile, k-block) positions.
+struct SkRange {
+    int t_lo, k_lo, t_hi, k_hi;
+};
+
+__device__ __forceinline__ SkRange sk_range(const GemmParams& p, int c, int clusters) {
+    const long long total = static_cast<long long>(p.sk_region) * p.num_kb;
+    const long long lo = total * c / clusters, hi = total * (c + 1) / clusters;
+    return {static_cast<int>(lo / p.num_kb), static_cast<int>(lo % p.num_kb), static_cast<int>(hi / p.num_kb),
+            static_cast<int>(hi % p.num_kb)};
+}
+
+// A pair's units under balanced stream-K, in the order it runs them: the head
+// piece that ends its range (the first piece of that tile: stored early), the
+// whole tiles before the region (c, c + clusters, ...), the whole region tiles
+// inside its range, and last the tail piece that begins its range (added after
+// the head that the previous pair ran first).
+__device__ __forceinline__ int pair_units_balanced(const GemmParams& p, int cluster, int clusters) {
+    const SkRange r = sk_range(p, cluster, clusters);
+    const int waves = p.sk_first / clusters;
+    const int first_whole = r.k_lo > 0 ? r.t_lo + 1 : r.t_lo;
+    return (r.k_hi > 0 ? 1 : 0) + waves + (r.t_hi - first_whole) + (r.k_lo > 0 ? 1 : 0);
+}
+
+__device__ __forceinline__ PairUnit pair_unit_balanced(const GemmParams& p, int cluster, int clusters, int u) {
+    const SkRange r = sk_range(p, cluster, clusters);
+    const int waves = p.sk_first / clusters;
+    const int head = r.k_hi > 0 ? 1 : 0;
+    const int first_whole = r.k_lo > 0 ? r.t_lo + 1 : r.t_lo;
+    PairUnit U;
+    U.sk_index = -1;
+    U.piece = 0;
+    U.kb_lo = 0;
+    U.kb_hi = p.num_kb;
+    if (u < head) {   // head of tile t_hi: the first piece of the tile cut by boundary `cluster`
+        U.tile = p.sk_first + r.t_hi;
+        U.kb_hi = r.k_hi;
+        U.sk_index = cluster;
+        return U;
+    }
+    u -= head;
+    if (u < waves) {
+        U.tile = cluster + u * clusters;
+        return U;
+    }
+    u -= waves;
+    if (u < r.t_hi - first_whole) {
+        U.tile = p.sk_first + first_whole + u;
+        return U;
+    }
+    // tail of tile t_lo: the last piece of the tile cut by boundary cluster - 1
+    U.tile = p.sk_first + r.t_lo;
+    U.kb_lo = r.k_lo;
+    U.piece = 1;
+    U.sk_index = cluster - 1;
+    return U;
+}
+
 __device__ __forceinline__ int pair_units(const GemmParams& p, int cluster, int clusters) {
+    if (p.sk_balanced) return pair_units_balanced(p, cluster, clusters);
     const int whole = p.num_tiles - p.sk_tiles;
     const int n = cluster < whole ? (whole - 1 - cluster) / clusters + 1 : 0;
     return n + (cluster < p.sk_tiles * p.sk_pieces ? 1 : 0);
 }
 
 __device__ __forceinline__ PairUnit pair_unit(const GemmParams& p, int cluster, int clusters, int u) {
+    if (p.sk_balanced) return pair_unit_balanced(p, cluster, clusters, u);
     PairUnit r;
     const bool has_piece = cluster < p.sk_tiles * p.sk_pieces;
     const int piece = has_piece ? cluster % p.sk_pieces : 0;

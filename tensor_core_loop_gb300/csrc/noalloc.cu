@@ -128,6 +128,9 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.out_rows = M;
     p.sk_tiles = 0;
     p.sk_pieces = 1;
+    p.sk_balanced = 0;
+    p.sk_first = 0;
+    p.sk_region = 0;
     p.sk_flags = nullptr;
     p.sk_gen = 0;
     p.debug_sk_stall = 0;

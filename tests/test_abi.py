@@ -198,36 +198,50 @@ def test_planner_stream_k(L):
     # 4096³ on 76 pairs: 256 tiles of 256×256 = 3 full waves + 28 tiles, each cut in two K
     # ranges, beats 304 tiles of 256×224 (4 waves at the 224-wide k-block rate)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)
-    assert (p["cta_pair"], p["bn"], p["num_tiles"], p["sk_tiles"], p["sk_pieces"]) == (2, 256, 256, 28, 2)
+    assert (p["cta_pair"], p["bn"], p["num_tiles"], p["sk_tiles"], p["sk_pieces"], p["sk_balanced"]) == \
+        (2, 256, 256, 28, 2, 0)
+    assert p["workspace_bytes"] == 0   # fp32 C: pieces add into C itself
+    # balanced stream-K on request: two waves of whole tiles, then the 104·64 k-blocks of the
+    # last 104 tiles in 76 ranges of 87-88 k-blocks, 72 tiles cut by a range boundary
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=5))
+    assert (p["sk_balanced"], p["sk_tiles"], p["sk_pieces"]) == (1, 72, 2)
+    # equal pieces on request: 3 full waves + 28 tiles, each cut in two K ranges (224 k-blocks)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=2))
+    assert (p["bn"], p["sk_balanced"], p["sk_tiles"], p["sk_pieces"]) == (256, 0, 28, 2)
     # without stream-K the 224-wide tiles win
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=1))
-    assert (p["bn"], p["sk_tiles"]) == (224, 0)
+    assert (p["bn"], p["sk_tiles"], p["sk_balanced"]) == (224, 0, 0)
     # whole waves: nothing to split
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4864, 4096, 4096, cfg)
-    assert (p["bn"], p["num_tiles"], p["sk_tiles"]) == (256, 304, 0)
-    # bf16 C: the same tail, its partials kept in fp32 until the last piece rounds once
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)["sk_tiles"] == 28
+    assert (p["bn"], p["num_tiles"], p["sk_tiles"], p["sk_balanced"]) == (256, 304, 0, 0)
+    # 9 tiles on 4 pairs: 4 equal pieces of the 9th tile tie with balanced ranges (72 k-blocks)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2))
-    assert (p["num_tiles"], p["sk_tiles"], p["sk_pieces"]) == (9, 1, 4)
+    assert (p["num_tiles"], p["sk_tiles"], p["sk_pieces"], p["sk_balanced"]) == (9, 1, 4, 0)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2, stream_k=5))
+    assert (p["sk_balanced"], p["sk_pieces"]) == (1, 2) and p["sk_tiles"] == 3   # 5 tiles, ranges of 40
     # short tiles (16 k-blocks): the extra piece's epilogue costs more than the tail saves
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1024, cfg)
-    assert (p["bn"], p["sk_tiles"]) == (224, 0)
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2048, cfg)["sk_tiles"] == 28
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 2048, cfg)["sk_tiles"] == 28
+    assert (p["bn"], p["sk_tiles"], p["sk_balanced"]) == (224, 0, 0)
+    for k in (2048, 8192):
+        assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, cfg)["sk_tiles"] == 28
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 1024, cfg)["sk_tiles"] == 0
-    for bad in (tcl.Config(max_ctas=8, cta_pair=2, stream_k=5),       # more than 4 pieces
+    for bad in (tcl.Config(max_ctas=8, cta_pair=2, stream_k=6),       # no such mode
                 tcl.Config(max_ctas=8, cta_pair=1, stream_k=2),       # one-SM kernel
                 tcl.Config(max_ctas=4, cta_pair=2, stream_k=3),       # 1 tail tile × 3 pieces > 2 pairs
                 tcl.Config(max_ctas=8, cta_pair=2, stream_k=-1)):
         with pytest.raises(tcl.TclError):
             tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, bad)
-    # a bf16 C takes a stream-K tail through an fp32 workspace: split tiles × 256 rows × bn columns
+    # as many pairs as tiles (the grid never exceeds the tiles): one whole tile per range
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 2048, tcl.Config(max_ctas=16, cta_pair=2, stream_k=5))
+    assert (p["grid"], p["sk_balanced"], p["sk_tiles"]) == (8, 1, 0)
+    # a bf16 C takes a stream-K tail through an fp32 workspace: split tiles × 256 rows × bn
+    # columns, or one block per range boundary (per pair) when balanced
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2, stream_k=2))
     assert (p["sk_tiles"], p["sk_pieces"]) == (1, 2) and p["workspace_bytes"] == 1 * 256 * 256 * 4
-    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, tcl.Config(max_ctas=152))
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=2))
     assert (p["bn"], p["sk_tiles"], p["sk_pieces"]) == (256, 28, 2) and p["workspace_bytes"] == 28 * 256 * 256 * 4
-    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152))
-    assert p["sk_tiles"] == 28 and p["workspace_bytes"] == 0   # fp32 C: pieces add into C itself
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=5))
+    assert p["sk_balanced"] == 1 and p["workspace_bytes"] == 76 * 256 * 256 * 4
 
 
 def test_planner_producer_kinds(L):

@@ -231,6 +231,43 @@ def test_bf16_out_stream_k(oracle_mod, M, N, K, pieces):
     bf16_case(oracle_mod, M, N, K, seed=K + pieces, out_dtype=torch.bfloat16, cfg=cfg, ldc=ldc)
 
 
+@pytest.mark.parametrize("M,N,K,max_ctas,out", [
+    (1280, 1280, 2048, 8, torch.float32),    # 25 tiles on 4 pairs: 5 waves, then 5 tiles in ranges of 40 k-blocks
+    (1280, 1280, 2048, 8, torch.bfloat16),   # the cut tiles' fp32 partials through the per-boundary workspace
+    (700, 750, 2000, 4, torch.float32),      # ragged M, N and last k-block; 9 tiles on 2 pairs
+    (1536, 1280, 4096, 14, torch.float32),   # 30 tiles on 7 pairs: ranges of 64 + 3/7 k-blocks
+])
+def test_bf16_balanced_stream_k(oracle_mod, M, N, K, max_ctas, out):
+    # balanced stream-K: equal k-block ranges per pair crossing tile boundaries; each cut
+    # tile's head is stored first, its rest added after the head's flag
+    cfg = tcl.Config(cta_pair=2, max_ctas=max_ctas, stream_k=5)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32 if out == torch.float32 else tcl.OUT_BF16, M, N, K, cfg)
+    assert pl["sk_balanced"] == 1 and pl["sk_tiles"] > 0
+    ldc = up(N, 4 if out == torch.float32 else 8)
+    bf16_case(oracle_mod, M, N, K, seed=K + M, out_dtype=out, cfg=cfg, ldc=ldc)
+    a, b = inputs.bf16_pair(M, N, K, seed=K + M, lda=up(K, 8), ldb=up(N, 8))
+    a, b = to_dev(a), to_dev(b)
+    first = run(a, b, out_dtype=out, cfg=cfg, ldc=ldc, canary=False)
+    for _ in range(3):
+        assert torch.equal(run(a, b, out_dtype=out, cfg=cfg, ldc=ldc, canary=False), first)
+
+
+def test_balanced_stream_k_int8_and_tf32(oracle_mod):
+    a, b = inputs.s8_pair(1280, 1280, 2112, seed=61)
+    cfg = tcl.Config(cta_pair=2, bn=256, max_ctas=8, stream_k=5)
+    assert tcl.plan(tcl.IN_S8, 0, 1280, 1280, 2112, cfg)["sk_balanced"] == 1
+    got = run(a.to(DEV), b.to(DEV), cfg=cfg).numpy()
+    assert_exact(got, oracle_mod.gemm_s8(a.numpy(), b.numpy()), "s8 balanced stream-K")
+    got2 = run(a.to(DEV), b.to(DEV), cfg=tcl.Config(cta_pair=2, bn=256, max_ctas=8, stream_k=5, s8_path=2)).numpy()
+    assert (got2 == got).all()
+    a, b = inputs.tf32_pair(1280, 1280, 1024, seed=62)
+    cfg = tcl.Config(cta_pair=2, max_ctas=8, stream_k=5)
+    assert tcl.plan(tcl.IN_TF32, 0, 1280, 1280, 1024, cfg)["sk_balanced"] == 1
+    got = run(a.to(DEV), b.to(DEV), cfg=cfg).double().numpy()
+    ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+    assert_within("tf32", got, ref, S, "tf32 balanced stream-K")
+
+
 def test_bf16_out_stream_k_rounds_once():
     # the same tile split or not: the fp32 sums differ only in summation order, and the
     # split result equals the split fp32 result rounded to bf16 (one rounding)

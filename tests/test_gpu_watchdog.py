@@ -61,14 +61,16 @@ def test_two_sm_kernel_bounded_wait_runs_out():
     assert tcl.last_device_error() == (0, 0)
 
 
-def test_stream_k_order_wait_runs_out():
-    # the first piece of split tile 0 never hands over: the last piece's wait for it
-    # (the last unit of its pair, so nothing else is waiting) runs out with code 5
+@pytest.mark.parametrize("sk,split", [(2, 1), (5, 3)])
+def test_stream_k_order_wait_runs_out(sk, split):
+    # the first piece of split tile 0 (balanced: of the tile cut by the first range boundary)
+    # never hands over: the last piece's wait for it (the last unit of its pair, so nothing
+    # else is waiting) runs out with code 5
     a, b = inputs.bf16_pair(768, 768, 2048, seed=6)
     a, b = a.to(DEV), b.to(DEV)
     c = torch.zeros((768, 768), dtype=torch.float32, device=DEV)
-    base = dict(cta_pair=2, max_ctas=8, stream_k=2)
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(**base))["sk_tiles"] == 1
+    base = dict(cta_pair=2, max_ctas=8, stream_k=sk)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(**base))["sk_tiles"] == split
     tcl.gemm_into(a, b, c, cfg=tcl.Config(timeout_ns=50_000_000, debug_stream_k_stall=1, **base))
     st, code = tcl.last_device_error()
     assert (st, code) == (7, 5), (st, code)

@@ -67,6 +67,10 @@ def parse():
                     help="instead of the contract line: the CUDA-core fp32 GEMM anchor at 4096^3")
     ap.add_argument("--trace", action="store_true",
                     help="instead of the contract line: per-shape load/MMA overlap from the in-kernel timeline")
+    ap.add_argument("--compare", choices=sorted(COMPARE_GROUPS),
+                    help="instead of the contract line: planner alternatives timed round robin (CUDA graphs)")
+    ap.add_argument("--variant-launches", choices=sorted(VARIANT_LAUNCHES),
+                    help="instead of the contract line: one call per alternative after an L2 flush (for ncu)")
     return ap.parse_args()
 
 
@@ -499,6 +503,119 @@ def run_sweep_launches(args):
         raise RuntimeError(f"device status {st} (code {code})")
 
 
+# Planner alternatives compared by --compare: per group, the workloads and the
+# tcl_config_t settings; each workload's settings are timed round robin (CUDA graphs
+# of back-to-back calls over rotating input sets twice the L2), median of 7 rounds,
+# so that the power-capped clock's drift falls on every setting alike.
+COMPARE_GROUPS = {
+    "raster": ([("bf16", 4096, 4096, 4096), ("bf16", 4096, 4096, 8192), ("bf16", 8192, 8192, 4096),
+                ("tf32", 4096, 4096, 4096)],
+               [("group 8, K ascending", dict(group_m=8, k_order=1)), ("group 1, K ascending", dict(group_m=1, k_order=1)),
+                ("group 1, K alternating", dict(group_m=1, k_order=2)),
+                ("group 8, K alternating", dict(group_m=8, k_order=2))]),
+    "stream_k": ([("bf16", 4096, 4096, 4096), ("bf16->bf16", 4096, 4096, 4096), ("bf16", 4096, 4096, 8192),
+                  ("bf16", 4096, 4096, 2048)],
+                 [("equal pieces", dict(stream_k=2)), ("balanced", dict(stream_k=5)), ("none", dict(stream_k=1))]),
+    "int8": ([("s8", 4096, 4096, 4096), ("s8", 8192, 8192, 4096), ("s8", 4096, 4096, 8192)],
+             [("widening pass", dict(s8_path=1)), ("in-kernel widening", dict(s8_path=2))]),
+    "small": ([("bf16", 512, 512, k) for k in (256, 512, 1024, 2048, 4096, 8192)],
+              [("automatic", dict()), ("64 wide", dict(bn=64, split_k=1)), ("128 wide", dict(bn=128, split_k=1)),
+               ("64 wide, 4 K ranges", dict(bn=64, split_k=4)), ("128 wide, 4 K ranges", dict(bn=128, split_k=4)),
+               ("128 wide, 8 K ranges", dict(bn=128, split_k=8))]),
+}
+
+# --variant-launches: one call of each alternative (after an L2 flush) for an ncu
+# capture of DRAM bytes per call.
+VARIANT_LAUNCHES = {
+    "raster": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096)], COMPARE_GROUPS["raster"][1]),
+    "int8": ([("s8", 4096, 4096, 4096)], COMPARE_GROUPS["int8"][1]),
+    "tf32": ([("tf32", 4096, 4096, 4096)], [("automatic", dict())]),
+}
+
+
+def _compare_operands(kind, m, n, k, dev, torch, inputs, footprint):
+    gen = {"bf16": inputs.bf16_pair, "bf16->bf16": inputs.bf16_pair, "tf32": inputs.tf32_pair,
+           "s8": inputs.s8_pair}[kind]
+    out = {"bf16": torch.float32, "bf16->bf16": torch.bfloat16, "tf32": torch.float32, "s8": torch.int32}[kind]
+    ah, bh = gen(m, n, k, seed=0)
+    a0, b0 = ah.to(dev), bh.to(dev)
+    per = (m * k + k * n) * a0.element_size() + m * n * torch.empty((), dtype=out).element_size()
+    nset = max(2, -(-footprint // per))
+    return [(a0 if i == 0 else a0.clone(), b0 if i == 0 else b0.clone(), torch.empty((m, n), dtype=out, device=dev))
+            for i in range(nset)]
+
+
+def run_compare(args):
+    import statistics
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shapes, settings = COMPARE_GROUPS[args.compare]
+    for kind, m, n, k in shapes:
+        sets = _compare_operands(kind, m, n, k, dev, torch, inputs, 2 * L2_BYTES if kind != "s8" else L2_BYTES)
+        launches = max(len(sets), 20)
+        graphs = []
+        for name, kw in settings:
+            cfg = tcl.Config(**kw)
+            fn = (lambda a, b, c, cfg=cfg: tcl.gemm_into(a, b, c, cfg=cfg))
+            for i in range(len(sets)):
+                fn(*sets[i])
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(launches):
+                    fn(*sets[i % len(sets)])
+            g.replay()
+            torch.cuda.synchronize()
+            graphs.append((name, kw, g))
+        times = {name: [] for name, _, _ in graphs}
+        for _ in range(7):
+            for name, _, g in graphs:
+                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s_.record()
+                for _ in range(3):
+                    g.replay()
+                e_.record()
+                e_.synchronize()
+                times[name].append(s_.elapsed_time(e_) * 1e3 / (3 * launches))
+        st, code = tcl.last_device_error()
+        if st:
+            raise RuntimeError(f"device status {st} (code {code})")
+        in_kind = {"bf16": tcl.IN_BF16, "bf16->bf16": tcl.IN_BF16, "tf32": tcl.IN_TF32, "s8": tcl.IN_S8}[kind]
+        out = tcl.OUT_BF16 if kind == "bf16->bf16" else tcl.OUT_F32
+        for name, kw, _ in graphs:
+            med = statistics.median(times[name])
+            print(json.dumps({"compare": args.compare, "workload": f"{kind} {m}x{n}x{k}", "setting": name,
+                              "us_median": round(med, 2), "us_min": round(min(times[name]), 2),
+                              "tflops": round(2.0 * m * n * k / med / 1e6, 1),
+                              "plan": tcl.plan(in_kind, out, m, n, k, tcl.Config(**kw))}), flush=True)
+        del graphs, sets
+
+
+def run_variant_launches(args):
+    import torch
+    import tensor_core_loop_gb300 as tcl
+    from tensor_core_loop_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    shapes, settings = VARIANT_LAUNCHES[args.variant_launches]
+    for kind, m, n, k in shapes:
+        a, b, c = _compare_operands(kind, m, n, k, dev, torch, inputs, 0)[0]
+        for name, kw in settings:
+            flush.zero_()
+            tcl.gemm_into(a, b, c, cfg=tcl.Config(**kw))
+            torch.cuda.synchronize()
+            print(json.dumps({"launch": f"{kind} {m}x{n}x{k}", "setting": name}), flush=True)
+        del a, b, c
+    st, code = tcl.last_device_error()
+    if st:
+        raise RuntimeError(f"device status {st} (code {code})")
+
+
 def run_simt(args):
     import torch
     import tensor_core_loop_gb300 as tcl
@@ -680,6 +797,12 @@ def main():
         return
     if args.sweep_launches:
         run_sweep_launches(args)
+        return
+    if args.compare:
+        run_compare(args)
+        return
+    if args.variant_launches:
+        run_variant_launches(args)
         return
 
     import torch

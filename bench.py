@@ -528,6 +528,8 @@ COMPARE_GROUPS = {
 # capture of DRAM bytes per call.
 VARIANT_LAUNCHES = {
     "raster": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096)], COMPARE_GROUPS["raster"][1]),
+    "raster_groups": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096)],
+                      [(f"group {g}, K alternating", dict(group_m=g, k_order=2)) for g in (1, 2, 3, 4, 6, 16)]),
     "int8": ([("s8", 4096, 4096, 4096)], COMPARE_GROUPS["int8"][1]),
     "tf32": ([("tf32", 4096, 4096, 4096)], [("automatic", dict())]),
 }

@@ -121,8 +121,10 @@ typedef struct {
     unsigned long long timeout_ns; /* bound on every in-kernel wait (0: 1 s) */
     unsigned long long* trace;     /* device buffer of 4*trace_cap + 4 uint64, or NULL: %clock64
                                       stamps per k-block of CTA 0 (load issued, data landed,
-                                      MMAs issued, MMAs done), then CTA 0's %clock64 and
-                                      %globaltimer (ns) at its start and at its end */
+                                      MMAs issued, MMAs done; int8 widened in the kernel: raw copy
+                                      issued, raw slot landed, stage converted, stage handed over),
+                                      then CTA 0's %clock64 and %globaltimer (ns) at its start and
+                                      at its end (not written by the in-kernel int8 widening) */
     int trace_cap;                 /* k-blocks the trace buffer holds */
     int producer;                  /* 0 (default): TMA bulk-tensor loads issued by one thread;
                                       1: synchronous copy by four warps (ld.global -> registers ->

@@ -215,8 +215,9 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
     const int cluster = blockIdx.x / 2;
     const int clusters = gridDim.x / 2;
     const int units = pair_units(p, cluster, clusters);
-    // per-k-block %clock64 stamps of CTA 0 (raw copy issued, raw slot landed at the
-    // converters, stage handed to the MMA warp, stage seen full by the MMA warp)
+    // per-k-block %clock64 stamps of CTA 0 (raw copy issued by the producer; raw slot
+    // landed, stage converted and fenced, stage handed over — seen by the first
+    // converter thread)
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
 
     if (warp < C::CONV_WARPS) {
@@ -272,15 +273,14 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
                     st_shared_v4(base + ((j0 ^ sw) << 4), v[0], v[1], v[2], v[3]);
                     st_shared_v4(base + (((j0 + 1) ^ sw) << 4), v[4], v[5], v[6], v[7]);
                 }
-                if (tracing && tid == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 3] = ptx::clock64();
                 ptx::fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
                 __syncwarp();
-                if (tracing && tid == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = ptx::clock64();
+                if (tracing && tid == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
                 if (lane == 0) {
                     ptx::mbar_arrive(rempty0 + 8 * r);   // the raw slot may be refilled
                     // (test hook: CTA 0 never hands this k-block over, so the MMA warp's wait runs out)
                     if (!(blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb)) ptx::mbar_arrive(cfull0 + 8 * s);
-                    if (tracing && tid == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
+                    if (tracing && tid == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 3] = ptx::clock64();
                 }
             }
         }
@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
                     }
                     const int kc = load_kblock(p, u, kb, U.kb_lo, U.kb_hi);
                     const uint32_t dst = ptx::smem_u32(raw_base + r * C::RAW_BYTES);
+                    if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = ptx::clock64();
                     ptx::mbar_arrive_expect_tx_elected(rfull0 + 8 * r, C::RAW_BYTES);
                     ptx::tma_load_2d_elected(dst, &tmA, rfull0 + 8 * r, kc * C::BK, row);
                     ptx::tma_load_2d_elected(dst + C::RAW_A_BYTES, &tmB, rfull0 + 8 * r, col, kc * C::BK);

@@ -33,7 +33,14 @@ __device__ __forceinline__ uint32_t s8_pair_to_bf16x2(int lo, int hi) {
     return (s8_f32_bits(lo) >> 16) | (s8_f32_bits(hi) & 0xFFFF0000u);
 }
 
+// One block per row of A, then of B (the grid covers every row: on GB300 this
+// ran ~4 µs faster at 8192 rows of 4096 than eight resident blocks per SM
+// striding over the rows).
 __global__ void __launch_bounds__(256) s8_to_bf16_kernel(S8Widen a, S8Widen b) {
+    // the GEMM that reads these copies is launched programmatically behind this
+    // pass: let it be scheduled now; it waits for this grid to complete (and its
+    // writes to be visible) before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long total = static_cast<long long>(a.rows) + b.rows;
     for (long long rr = blockIdx.x; rr < total; rr += gridDim.x) {
         const bool in_a = rr < a.rows;
@@ -82,9 +89,10 @@ cudaError_t launch_s8_to_bf16(S8Widen a, S8Widen b, int sms, cudaStream_t stream
     b.vec = (reinterpret_cast<uintptr_t>(b.src) % 16 == 0 && b.ld_src % 16 == 0) ? 1 : 0;
     const long long rows = static_cast<long long>(a.rows) + b.rows;
     long long blocks = rows;
-    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks per SM, row-stride beyond
+    const long long cap = 1LL << 30;   // rows beyond the grid: row-stride
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    (void)sms;
     s8_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, b);
     return cudaGetLastError();
 }

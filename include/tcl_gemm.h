@@ -16,16 +16,20 @@
  *
  * Memory and ownership: A, B and C are device pointers owned by the caller
  *   (allocated, kept alive until the stream has run the call, and freed by
- *   the caller). The library keeps a per-device cache of TMA descriptors and
- *   a per-device scratch buffer (the widened operands of gemm_s8, copies of
+ *   the caller). The library keeps a per-device cache of TMA descriptors and,
+ *   per stream, a scratch buffer (the widened operands of gemm_s8, copies of
  *   operands or outputs off the 16-byte grid, split-K partial
  *   tiles for small grids, the fp32 partial sums of a bf16 C's stream-K
  *   tail) that it grows on demand (cudaMalloc, at least
  *   doubling; an outgrown buffer is kept, since enqueued or graph-captured
- *   work may still use it) and frees, with the outgrown ones, in
- *   tcl_shutdown(). Every call on a device shares that buffer: calls whose
- *   GPU work could overlap (different streams without ordering) must not both
- *   need it.
+ *   work may still use it) and a small array of stream-K progress flags
+ *   (8 KB, allocated and zeroed at the stream's first call). Calls on
+ *   different streams therefore never share scratch or flags and may overlap
+ *   on the GPU. The legacy and per-thread default streams share one set; a
+ *   call captured into a graph on a stream that has not run a call outside
+ *   capture before takes that default set too (and so do the graph's
+ *   replays), so such a replay must not overlap work on the default streams.
+ *   tcl_stream_release() frees one stream's set, tcl_shutdown() all of them.
  *
  * Streams: every call is asynchronous on `stream` (0 = legacy default
  *   stream) and returns once the work is enqueued. Calls on one stream run in
@@ -343,8 +347,17 @@ TCL_API int tcl_last_device_error(cudaStream_t stream, int* detail);
 /* Streaming multiprocessors of the current device (0 on error). */
 TCL_API int tcl_num_sms(void);
 
-/* Frees the scratch buffers of every device, the outgrown ones included
- * (after synchronising each), and the host-buffer entry point's streams. */
+/* Frees the scratch buffer and stream-K flags that calls on `stream` (of the
+ * current device) have used, after synchronising the stream: for a stream the
+ * caller is about to destroy. Graphs that captured calls on that stream must
+ * not be replayed afterwards. A stream the library holds nothing for, and the
+ * default streams, are no-ops. TCL_OK, or TCL_ERR_LAUNCH if synchronising
+ * failed. No counterpart in the source pages: library housekeeping. */
+TCL_API int tcl_stream_release(cudaStream_t stream);
+
+/* Frees the scratch buffers of every device and stream, the outgrown ones
+ * included (after synchronising each device), the streams' stream-K flags,
+ * and the host-buffer entry point's streams. */
 TCL_API void tcl_shutdown(void);
 
 /* Library version string, e.g. "tcl-gb300 0.1.0 sm_103a". */

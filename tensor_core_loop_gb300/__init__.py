@@ -34,7 +34,7 @@ IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",
                     "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms",
                     "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak", "gemm_f32_simt",
-                    "gemm_bf16_host")
+                    "gemm_bf16_host", "tcl_stream_release")
 
 
 class TclError(RuntimeError):
@@ -126,6 +126,7 @@ def lib() -> ctypes.CDLL:
         L.tcl_num_sms.argtypes = []
         L.tcl_shutdown.argtypes = []
         L.tcl_shutdown.restype = None
+        L.tcl_stream_release.argtypes = [P]
         L.tcl_version.restype = ctypes.c_char_p
         _lib = L
         return L
@@ -182,6 +183,14 @@ def last_device_error(stream=None) -> tuple[int, int]:
     detail = ctypes.c_int(0)
     st = lib().tcl_last_device_error(ctypes.c_void_p(s.cuda_stream), ctypes.byref(detail))
     return int(st), int(detail.value)
+
+
+def stream_release(stream) -> None:
+    """Frees the scratch and stream-K flags the library holds for `stream` (a torch
+    stream), after synchronising it; call before destroying a stream."""
+    st = lib().tcl_stream_release(ctypes.c_void_p(stream.cuda_stream))
+    if st:
+        raise TclError(st, "tcl_stream_release")
 
 
 def _ld(t) -> int:

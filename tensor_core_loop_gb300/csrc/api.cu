@@ -37,16 +37,29 @@ constexpr int kBM = 128;
 // 103 vs 108 us at int8 4096^3: the unit turnover costs more than the conversion.)
 constexpr int kS32UnitK = 1024;
 
+constexpr size_t kSkFlagBytes = sizeof(unsigned int) * kMaxSkTiles * 2 * 8;
+
+// Scratch and stream-K progress flags of the calls on one stream. Calls on
+// different streams may run on the GPU at the same time, so each stream has a
+// set of its own, made at its first call.
+struct StreamRes {
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+    unsigned int* sk_flags = nullptr;   // kMaxSkTiles · 2 · 8 words
+    unsigned int sk_gen = 0;            // last stream-K flag generation used with these flags
+    bool own_flags = false;             // allocated for this stream (the default set's are a static array)
+};
+
 struct DevState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
     int pair_clusters[16] = {};  // resident clusters per pair variant (0: not yet queried)
     unsigned int* status = nullptr;
-    unsigned int* sk_flags = nullptr;
-    unsigned int sk_gen = 0;   // last stream-K flag generation used on this device
-    void* scratch = nullptr;
-    size_t scratch_bytes = 0;
+    // the set of the legacy and per-thread default streams, also taken by a call
+    // captured on a stream that has no set of its own yet
+    StreamRes base;
+    std::unordered_map<cudaStream_t, StreamRes> per_stream;
     std::vector<void*> retired;   // outgrown scratch buffers, freed by tcl_shutdown
     // host-buffer entry points: uploads, GEMMs and downloads on their own streams
     cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
@@ -101,28 +114,75 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned_to(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
-// Grows the device's scratch to at least `need` bytes (at least doubling it).
+bool is_capturing(cudaStream_t stream, int* st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        *st = TCL_ERR_LAUNCH;
+        return false;
+    }
+    *st = TCL_OK;
+    return cs != cudaStreamCaptureStatusNone;
+}
+
+// The scratch and flag set of `stream` on this device. A stream gets its own set
+// at its first call outside capture (its flags allocated and zeroed on the
+// stream, ahead of the call's kernels); a call captured on a stream without a
+// set takes the default streams' set, as will every replay of the graph.
+int stream_res(DevState* ds, cudaStream_t stream, StreamRes** out) {
+    if (stream == nullptr || stream == cudaStreamLegacy || stream == cudaStreamPerThread) {
+        *out = &ds->base;
+        return TCL_OK;
+    }
+    auto it = ds->per_stream.find(stream);
+    if (it != ds->per_stream.end()) {
+        *out = &it->second;
+        return TCL_OK;
+    }
+    int st;
+    const bool capturing = is_capturing(stream, &st);
+    if (st) return st;
+    if (capturing) {
+        *out = &ds->base;
+        return TCL_OK;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, kSkFlagBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_NO_MEMORY;
+    }
+    if (cudaMemsetAsync(p, 0, kSkFlagBytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p);
+        return TCL_ERR_LAUNCH;
+    }
+    StreamRes r;
+    r.sk_flags = static_cast<unsigned int*>(p);
+    r.own_flags = true;
+    *out = &ds->per_stream.emplace(stream, r).first->second;   // (map nodes never move)
+    return TCL_OK;
+}
+
+// Grows a stream's scratch to at least `need` bytes (at least doubling it).
 // The outgrown buffer is kept until tcl_shutdown: work already enqueued, or
 // captured into a CUDA graph, may still use it. No allocation while `stream`
 // is being captured (TCL_ERR_CAPTURE): a captured call must find its scratch
 // already allocated by an earlier call outside capture.
-int ensure_scratch(DevState* ds, size_t need, cudaStream_t stream) {
-    if (ds->scratch_bytes >= need) return TCL_OK;
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
-        cudaGetLastError();
-        return TCL_ERR_LAUNCH;
-    }
-    if (cs != cudaStreamCaptureStatusNone) return TCL_ERR_CAPTURE;
-    const size_t want = std::max(need, 2 * ds->scratch_bytes);
+int ensure_scratch(DevState* ds, StreamRes* sr, size_t need, cudaStream_t stream) {
+    if (sr->scratch_bytes >= need) return TCL_OK;
+    int st;
+    const bool capturing = is_capturing(stream, &st);
+    if (st) return st;
+    if (capturing) return TCL_ERR_CAPTURE;
+    const size_t want = std::max(need, 2 * sr->scratch_bytes);
     void* p = nullptr;
     if (cudaMalloc(&p, want) != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_NO_MEMORY;
     }
-    if (ds->scratch) ds->retired.push_back(ds->scratch);
-    ds->scratch = p;
-    ds->scratch_bytes = want;
+    if (sr->scratch) ds->retired.push_back(sr->scratch);
+    sr->scratch = p;
+    sr->scratch_bytes = want;
     return TCL_OK;
 }
 
@@ -164,7 +224,7 @@ int current_device(int* dev_out, DevState** st_out) {
                 cudaGetLastError();
                 return TCL_ERR_LAUNCH;
             }
-            d.sk_flags = static_cast<unsigned int*>(p);
+            d.base.sk_flags = static_cast<unsigned int*>(p);
         }
         d.probed = true;
     }
@@ -601,7 +661,7 @@ int plan_on_device(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_
 // split-K plan, the reduction of the partial tiles from `workspace` into C).
 int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const void* A, long long lda,
              const void* B, long long ldb, void* C, long long ldc, void* workspace, const tcl_config_t* cfg,
-             int dev, DevState* ds, cudaStream_t stream) {
+             int dev, DevState* ds, StreamRes* sr, cudaStream_t stream) {
     int st;
     const Workspace ws = split_workspace(pl, M, N);
     const bool split = pl.splits > 1;
@@ -677,7 +737,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.sk_first = pl.sk_first;
     p.sk_region = pl.sk_region;
     p.debug_sk_stall = cfg && cfg->debug_stream_k_stall ? 1 : 0;
-    p.sk_flags = ds->sk_flags;
+    p.sk_flags = sr->sk_flags;
     p.sk_gen = 0;
     p.sk_ws = nullptr;
     p.sk_ws_rows = 0;
@@ -687,9 +747,9 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
         p.sk_ws_rows = pl.sk_ws_rows;
     }
     if (pl.sk_tiles || pl.sk_balanced) {
-        ds->sk_gen = (ds->sk_gen + 1) & 0x1FFFFFFFu;   // flags hold gen·8 + pieces done in 32 bits
-        if (ds->sk_gen == 0) ds->sk_gen = 1;           // 0 is what the flags start as
-        p.sk_gen = ds->sk_gen;
+        sr->sk_gen = (sr->sk_gen + 1) & 0x1FFFFFFFu;   // flags hold gen·8 + pieces done in 32 bits
+        if (sr->sk_gen == 0) sr->sk_gen = 1;           // 0 is what the flags start as
+        p.sk_gen = sr->sk_gen;
     }
 
     bool found = false;
@@ -757,6 +817,8 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
     const OutKind ok = out == TCL_OUT_BF16 ? OutKind::BF16 : OutKind::F32;
+    StreamRes* sr;
+    if ((st = stream_res(ds, stream, &sr))) return st;
     Plan pl;
     if ((st = plan_on_device(InKind::BF16, ok, M, N, K2, cfg, ds, &pl))) return st;
     const size_t a_bytes = pack_a ? static_cast<size_t>(M) * lda2 * 2 : 0;
@@ -765,8 +827,8 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
     const Workspace ws = split_workspace(pl, M, N);
     const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws.bytes;
-    if (need && (st = ensure_scratch(ds, need, stream))) return st;
-    Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
+    if (need && (st = ensure_scratch(ds, sr, need, stream))) return st;
+    Carve cv{static_cast<uint8_t*>(sr->scratch), 0};
     void* a2 = cv.take(a_bytes);
     void* b2 = cv.take(b_bytes);
     void* c2 = cv.take(c_bytes);
@@ -777,7 +839,7 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
         return TCL_ERR_LAUNCH;
     }
     st = run_gemm(pl, InKind::BF16, ok, M, N, K2, pack_a ? a2 : A, pack_a ? lda2 : lda, pack_b ? b2 : B,
-                  pack_b ? ldb2 : ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, stream);
+                  pack_b ? ldb2 : ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, sr, stream);
     if (st) return st;
     if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, oes, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -804,6 +866,8 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
+    StreamRes* sr;
+    if ((st = stream_res(ds, stream, &sr))) return st;
     Plan pl;
     if ((st = plan_on_device(InKind::TF32, OutKind::F32, M, N, K4, cfg, ds, &pl))) return st;
     const size_t a_bytes = pack_a ? static_cast<size_t>(M) * K4 * 4 : 0;
@@ -812,8 +876,8 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     const Workspace ws = split_workspace(pl, M, N);
     const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws.bytes;
-    if (need && (st = ensure_scratch(ds, need, stream))) return st;
-    Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
+    if (need && (st = ensure_scratch(ds, sr, need, stream))) return st;
+    Carve cv{static_cast<uint8_t*>(sr->scratch), 0};
     void* a2 = cv.take(a_bytes);
     void* b2 = cv.take(b_bytes);
     void* c2 = cv.take(c_bytes);
@@ -824,7 +888,7 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
         return TCL_ERR_LAUNCH;
     }
     st = run_gemm(pl, InKind::TF32, OutKind::F32, M, N, K4, pack_a ? a2 : A, pack_a ? K4 : lda, pack_b ? b2 : B,
-                  pack_b ? ldb2 : ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, stream);
+                  pack_b ? ldb2 : ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc, wsp, cfg, dev, ds, sr, stream);
     if (st) return st;
     if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, 4, ds->sms, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -846,6 +910,8 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     int dev;
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
+    StreamRes* sr;
+    if ((st = stream_res(ds, stream, &sr))) return st;
     Plan pl;
     if ((st = plan_on_device(InKind::BF16, OutKind::S32, M, N, K, cfg, ds, &pl))) return st;
     // The in-kernel widening copies the int8 rows with tensor copies: 16-byte rows only.
@@ -853,17 +919,17 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     const long long c_bytes = pack_c ? round_up(static_cast<long long>(M) * ldc2 * 4, 256) : 0;
     int32_t* c2 = nullptr;
     if (pl.s8_in_kernel) {
-        if (c_bytes && (st = ensure_scratch(ds, static_cast<size_t>(c_bytes), stream))) return st;
-        if (pack_c) c2 = static_cast<int32_t*>(ds->scratch);
+        if (c_bytes && (st = ensure_scratch(ds, sr, static_cast<size_t>(c_bytes), stream))) return st;
+        if (pack_c) c2 = static_cast<int32_t*>(sr->scratch);
         st = run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, A, lda, B, ldb, pack_c ? c2 : C, pack_c ? ldc2 : ldc,
-                      nullptr, cfg, dev, ds, stream);
+                      nullptr, cfg, dev, ds, sr, stream);
     } else {
         // Packed bf16 copies of A (M × lda2) and B (K × ldb2), each 256-byte aligned.
         const long long lda2 = round_up(K, 8), ldb2 = round_up(N, 8);
         const long long a_bytes = round_up(static_cast<long long>(M) * lda2 * 2, 256);
         const long long b_bytes = round_up(static_cast<long long>(K) * ldb2 * 2, 256);
-        if ((st = ensure_scratch(ds, static_cast<size_t>(a_bytes + b_bytes + c_bytes), stream))) return st;
-        uint8_t* a2 = static_cast<uint8_t*>(ds->scratch);
+        if ((st = ensure_scratch(ds, sr, static_cast<size_t>(a_bytes + b_bytes + c_bytes), stream))) return st;
+        uint8_t* a2 = static_cast<uint8_t*>(sr->scratch);
         uint8_t* b2 = a2 + a_bytes;
         if (pack_c) c2 = reinterpret_cast<int32_t*>(b2 + b_bytes);
         if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
@@ -873,7 +939,7 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
             return TCL_ERR_LAUNCH;
         }
         st = run_gemm(pl, InKind::BF16, OutKind::S32, M, N, K, a2, lda2, b2, ldb2, pack_c ? c2 : C,
-                      pack_c ? ldc2 : ldc, nullptr, cfg, dev, ds, stream);
+                      pack_c ? ldc2 : ldc, nullptr, cfg, dev, ds, sr, stream);
     }
     if (st) return st;
     if (pack_c && launch_repack(c2, ldc2, M, N, C, ldc, M, N, 4, ds->sms, stream) != cudaSuccess) {
@@ -920,6 +986,10 @@ int gemm_bf16_host_impl(int M, int N, int K, const void* A, int lda, const void*
     DevState* ds;
     if ((st = current_device(&dev, &ds))) return st;
     if ((st = ensure_host_streams(ds))) return st;
+    // all of this path's work runs on the library's own streams: its scratch and
+    // flags are those of its GEMM stream
+    StreamRes* sr;
+    if ((st = stream_res(ds, ds->comp, &sr))) return st;
     // device copies with tensor-copy pitches, K zero-padded to a multiple of 8
     const int K2 = static_cast<int>(round_up(K, 8));
     const long long lda2 = K2, ldb2 = round_up(N, 8), ldc2 = round_up(N, 16 / oes);
@@ -938,8 +1008,8 @@ int gemm_bf16_host_impl(int M, int N, int K, const void* A, int lda, const void*
     const size_t c_bytes = static_cast<size_t>(M) * ldc2 * oes;
     const size_t need = static_cast<size_t>(round_up(a_bytes, 256) + round_up(b_bytes, 256) +
                                             round_up(c_bytes, 256)) + ws_bytes;
-    if ((st = ensure_scratch(ds, need, stream))) return st;
-    Carve cv{static_cast<uint8_t*>(ds->scratch), 0};
+    if ((st = ensure_scratch(ds, sr, need, stream))) return st;
+    Carve cv{static_cast<uint8_t*>(sr->scratch), 0};
     uint8_t* a2 = static_cast<uint8_t*>(cv.take(a_bytes));
     uint8_t* b2 = static_cast<uint8_t*>(cv.take(b_bytes));
     uint8_t* c2 = static_cast<uint8_t*>(cv.take(c_bytes));
@@ -987,7 +1057,7 @@ int gemm_bf16_host_impl(int M, int N, int K, const void* A, int lda, const void*
         if (!okq) break;
         st = run_gemm(i + 1 < chunks ? pf : plast, InKind::BF16, ok, r, N, K2,
                       a2 + static_cast<size_t>(i) * rows * lda2 * 2, lda2, b2, ldb2,
-                      c2 + static_cast<size_t>(i) * rows * ldc2 * oes, ldc2, wsp, cfg, dev, ds, ds->comp);
+                      c2 + static_cast<size_t>(i) * rows * ldc2 * oes, ldc2, wsp, cfg, dev, ds, sr, ds->comp);
         if (st) return fail(st);
         okq = cudaEventRecord(c_out[i], ds->comp) == cudaSuccess &&
               cudaStreamWaitEvent(ds->down, c_out[i], 0) == cudaSuccess &&
@@ -1191,6 +1261,25 @@ int tcl_num_sms(void) {
     return ds->sms;
 }
 
+int tcl_stream_release(cudaStream_t stream) {
+    if (stream == nullptr || stream == cudaStreamLegacy || stream == cudaStreamPerThread) return TCL_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    int st = current_device(&dev, &ds);
+    if (st) return st;
+    auto it = ds->per_stream.find(stream);
+    if (it == ds->per_stream.end()) return TCL_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCL_ERR_LAUNCH;
+    }
+    cudaFree(it->second.scratch);
+    if (it->second.own_flags) cudaFree(it->second.sk_flags);
+    ds->per_stream.erase(it);
+    return TCL_OK;
+}
+
 void tcl_shutdown(void) {
     std::lock_guard<std::mutex> lock(g_mu);
     int prev = 0;
@@ -1208,15 +1297,21 @@ void tcl_shutdown(void) {
             }
             g_dev[d].up = g_dev[d].comp = g_dev[d].down = nullptr;
         }
-        if (g_dev[d].scratch) {
+        DevState& ds = g_dev[d];
+        if (ds.base.scratch || !ds.per_stream.empty() || !ds.retired.empty()) {
             if (cudaSetDevice(d) == cudaSuccess) {
                 cudaDeviceSynchronize();
-                cudaFree(g_dev[d].scratch);
-                for (void* r : g_dev[d].retired) cudaFree(r);
+                cudaFree(ds.base.scratch);
+                for (auto& kv : ds.per_stream) {
+                    cudaFree(kv.second.scratch);
+                    if (kv.second.own_flags) cudaFree(kv.second.sk_flags);
+                }
+                for (void* r : ds.retired) cudaFree(r);
             }
-            g_dev[d].scratch = nullptr;
-            g_dev[d].scratch_bytes = 0;
-            g_dev[d].retired.clear();
+            ds.base.scratch = nullptr;
+            ds.base.scratch_bytes = 0;
+            ds.per_stream.clear();
+            ds.retired.clear();
         }
     }
     cudaSetDevice(prev);

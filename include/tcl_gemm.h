@@ -189,6 +189,15 @@ typedef struct {
                                       stages; no scratch; needs 256-wide two-SM tiles and A, B 16-byte
                                       aligned with lda, ldb multiples of 16, else TCL_ERR_CONFIG /
                                       TCL_ERR_ALIGN). 2 is exact like 1 but slower on GB300 */
+    int cluster_k;                 /* bf16 in, fp32 or bf16 C, one SM per tile: 0 or 1 one CTA per
+                                      tile (the automatic choice: the cluster form was measured
+                                      slower on GB300 at every 512² shape of the K sweep);
+                                      2 or 4: each 128×64 tile is computed by a cluster of that many
+                                      CTAs, CTA r summing the k-blocks [r·nkb/n, (r+1)·nkb/n), and
+                                      the first CTA adds the others' partial tiles in rank order
+                                      through distributed shared memory (one launch, no
+                                      workspace). Not with split_k > 1, one_cta_per_tile, stages,
+                                      producer != 0, or a bn other than 0 or 64 (TCL_ERR_CONFIG) */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -299,6 +308,8 @@ typedef struct {
     int k_serpentine;               /* 1: alternating K order (see tcl_config_t.k_order) */
     int s8_in_kernel;               /* int8: 1 if the kernel widens the operands itself
                                        (tcl_config_t.s8_path = 2), 0 for the widening pass */
+    int cluster_k;                  /* CTAs per tile whose K ranges are summed in a cluster
+                                       (1: one CTA per tile; see tcl_config_t.cluster_k) */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

@@ -69,6 +69,7 @@ class Config(ctypes.Structure):
         ("debug_stream_k_stall", ctypes.c_int),
         ("k_order", ctypes.c_int),
         ("s8_path", ctypes.c_int),
+        ("cluster_k", ctypes.c_int),
     ]
 
 
@@ -90,6 +91,7 @@ class PlanInfo(ctypes.Structure):
         ("group_m", ctypes.c_int),
         ("k_serpentine", ctypes.c_int),
         ("s8_in_kernel", ctypes.c_int),
+        ("cluster_k", ctypes.c_int),
     ]
 
 

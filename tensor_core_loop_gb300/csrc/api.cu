@@ -286,6 +286,7 @@ struct Plan {
     int sk_balanced, sk_first, sk_region;   // balanced stream-K (see GemmParams)
     int k_serpentine;           // odd units of a CTA's walk load K in descending order
     int s8_in_kernel;           // int8: the two-SM kernel that widens the operands itself
+    int csk;                    // > 1: CTAs per tile summing its K ranges in a cluster (gemm_kernel_csk.cuh)
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -400,6 +401,16 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     const int want_pair = cfg ? cfg->cta_pair : 0;
     if (want_pair < 0 || want_pair > 2) return TCL_ERR_CONFIG;
     int bn = cfg ? cfg->bn : 0;
+    // K ranges summed in a cluster: bf16 in, fp32 or bf16 C, one SM per 128×64 tile
+    const int want_ck = cfg ? cfg->cluster_k : 0;
+    if (want_ck < 0 || want_ck > 4 || want_ck == 3) return TCL_ERR_CONFIG;
+    const bool ck_capable = ik == InKind::BF16 && (ok == OutKind::F32 || ok == OutKind::BF16) &&
+                            prod == PROD_TMA && want_pair != 2 && !(cfg && cfg->one_cta_per_tile) &&
+                            !(cfg && cfg->split_k > 1) && !(cfg && cfg->stages) && (bn == 0 || bn == 64);
+    if (want_ck >= 2) {
+        if (!ck_capable) return TCL_ERR_CONFIG;
+        bn = 64;
+    }
     int pair = 0;
     // the two-SM kernel: bf16 or TF32 in, float out (256 or 224 wide), or the
     // exact-integer mode (256 wide with eight epilogue warps, or 128 wide with
@@ -411,7 +422,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         if (ok == OutKind::S32 ? (bn != 0 && bn != 128 && bn != 256) : (bn != 0 && bn != 256 && bn != 224))
             return TCL_ERR_CONFIG;
         pair = 1;
-    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages)) {
+    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages) && want_ck < 2) {
         // Two SMs per 256-row tile halve each SM's bytes per flop; use them when
         // there are at least as many pair tiles as pairs of SMs and a tile has
         // enough k-blocks for its mainloop to outlast its epilogue (measured on
@@ -492,6 +503,18 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->num_tiles = static_cast<int>(tiles);
     pl->num_kb = (K + bk - 1) / bk;
     pl->kb_per_unit = ok == OutKind::S32 ? kS32UnitK / bk : pl->num_kb;
+    // A tile's K ranges on a cluster of 2 or 4 CTAs, summed through distributed shared
+    // memory: on request only. Measured on GB300 at 512² (CUDA graphs of back-to-back
+    // calls, round robin), it loses to one CTA per 64-wide tile below K = 2048 (K = 256:
+    // 6.4 / 8.1 µs for clusters of 2 / 4 against 4.4) and to split-K with its reduction
+    // launch above (K = 4096: 12.2 against 10.5): moving the 32 KB partial tiles between
+    // the SMs of a cluster takes ~1 µs each, and a cluster barrier ~0.5 µs.
+    pl->csk = 0;
+    if (ck_capable && !pair && bn == 64 && want_ck >= 2) {
+        pl->csk = want_ck;
+        pl->stages = csk_stages();
+        pl->smem = csk_smem_bytes(want_ck);
+    }
     // Raster group and K order for deep two-SM tiles (rows of A at least 16 KB
     // long): a wave of tiles then streams more operand bytes than one die's share
     // of L2 keeps, and each wave re-reads what the one before evicted. One row of
@@ -531,7 +554,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     const int want_split = cfg ? cfg->split_k : 0;
     if (want_split < 0) return TCL_ERR_CONFIG;
     if (want_split > 1 && (pair || ok == OutKind::S32)) return TCL_ERR_CONFIG;
-    if (!pair && ok != OutKind::S32 && want_split != 1) {
+    if (!pair && ok != OutKind::S32 && want_split != 1 && !pl->csk) {
         int sp = want_split;
         if (sp == 0) {
             const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
@@ -611,6 +634,10 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         return TCL_ERR_CONFIG;
     } else if (cfg && cfg->one_cta_per_tile) {
         pl->grid = static_cast<int>(std::min<long long>(work, 0x7FFFFFFF));
+    } else if (pl->csk) {
+        const long long ctas = static_cast<long long>(pl->num_tiles) * pl->csk;   // one cluster per tile
+        if (ctas > 0x7FFFFFFFll) return TCL_ERR_DIMS;
+        pl->grid = static_cast<int>(ctas);
     } else {
         int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
         if (cap < 1) cap = 1;
@@ -681,6 +708,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.prod = pl.prod;
     a.pair = pl.pair;
     a.slots = pl.slots;
+    a.csk = pl.csk;
     a.pdl = !(cfg && cfg->serial_launch);
     a.grid = pl.grid;
     a.stream = stream;
@@ -757,6 +785,8 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     if (pl.s8_in_kernel) {
         found = true;
         err = launch_s8_pair(a);
+    } else if (pl.csk) {
+        err = launch_csk(a, &found);
     } else if (pl.pair) {
         err = launch_group_pair(a, &found);
     } else if (ik == InKind::TF32) {
@@ -1208,6 +1238,7 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->group_m = pl.group_m;
         plan->k_serpentine = pl.k_serpentine;
         plan->s8_in_kernel = pl.s8_in_kernel;
+        plan->cluster_k = pl.csk ? pl.csk : 1;
     }
     return TCL_OK;
 }

@@ -113,13 +113,6 @@ __device__ __forceinline__ bool wait_warp_pair_cluster(uint32_t bar, uint32_t pa
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 // Two of the four biased bytes of u (b + 128 each, chosen by the byte-permute
 // selector) as two fp16 values b: 0x6400 | (b + 128) is the fp16 pattern of
 // 1024 + b + 128, exactly, and subtracting 1152 in both halves is exact (every

@@ -17,6 +17,7 @@ struct LaunchArgs {
     int prod;   // PROD_TMA, PROD_SYNC or PROD_CPASYNC
     int pair;   // 1: two-SM kernel (one CTA pair per cluster); 0: one-SM kernel
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
+    int csk;    // > 1: K ranges of one tile summed in a cluster of this many CTAs (k_csk.cu)
     bool pdl;   // programmatic dependent launch
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
@@ -40,6 +41,11 @@ cudaError_t launch_group_tf32(const LaunchArgs& a, bool* found);
 // a.tmB map the int8 matrices (unswizzled boxes of 64 K × 128 rows and 128
 // columns × 64 K), a.tmC the int32 output; s8_pair_stages() fp16 stages.
 cudaError_t launch_s8_pair(const LaunchArgs& a);
+// Cluster-summed K ranges (k_csk.cu): bf16 in, fp32 or bf16 C, 128×64 tiles,
+// a.csk = 2 or 4 CTAs per tile; a.grid = tiles × a.csk.
+cudaError_t launch_csk(const LaunchArgs& a, bool* found);
+int csk_stages();
+int csk_smem_bytes(int cl);
 int s8_pair_stages();
 int s8_pair_smem_bytes();
 int s8_pair_max_clusters();

@@ -141,6 +141,23 @@ def test_plan_without_device(L):
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)     # 4 k-blocks: too short to split
     # ... and 16 tiles of 128 columns fill a tenth of the SMs: 64-wide tiles, 32 CTAs
     assert p["splits"] == 1 and p["bn"] == 64 and p["grid"] == 32 and p["workspace_bytes"] == 0
+    assert p["cluster_k"] == 1
+    # K ranges of a tile summed in a cluster of 2 or 4 CTAs, on request
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, tcl.Config(max_ctas=152, cluster_k=4))
+    assert (p["bn"], p["cluster_k"], p["grid"], p["num_tiles"], p["stages"]) == (64, 4, 128, 32, 4)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 1024, 512, 1024, tcl.Config(max_ctas=152, cluster_k=2))
+    assert (p["cluster_k"], p["grid"], p["splits"]) == (2, 128, 1)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 300, 200, 64, tcl.Config(max_ctas=152, cluster_k=4))
+    assert (p["cluster_k"], p["bn"], p["grid"]) == (4, 64, 4 * 3 * 4)   # ranges may be empty
+    for bad in (tcl.Config(max_ctas=152, cluster_k=3), tcl.Config(max_ctas=152, cluster_k=8),
+                tcl.Config(max_ctas=152, cluster_k=2, split_k=2), tcl.Config(max_ctas=152, cluster_k=2, bn=128),
+                tcl.Config(max_ctas=152, cluster_k=2, cta_pair=2), tcl.Config(max_ctas=152, cluster_k=2, stages=4),
+                tcl.Config(max_ctas=152, cluster_k=2, one_cta_per_tile=1), tcl.Config(max_ctas=152, cluster_k=-1)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 512, bad)
+    for in_kind, out in ((tcl.IN_TF32, tcl.OUT_F32), (tcl.IN_S8, 0)):   # bf16 operands only
+        with pytest.raises(tcl.TclError):
+            tcl.plan(in_kind, out, 512, 512, 512, tcl.Config(max_ctas=152, cluster_k=2))
     # split-K shapes keep 128-wide tiles
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 2048, cfg)["bn"] == 128
     # deep two-SM tiles (rows of A of 16 KB and more): a row of tiles at a time, K walked

@@ -560,11 +560,39 @@ def test_tf32_small(oracle_mod, M, N, K):
 def test_bf16_64_wide_tiles(oracle_mod, out, M, N, K, split):
     # 64-wide one-SM tiles (one B box per stage, 8 stages), with and without split-K;
     # ragged right edges inside the single 64-column box
-    cfg = tcl.Config(bn=64, split_k=split)
+    cfg = tcl.Config(bn=64, split_k=split, cluster_k=1)
     pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32 if out == torch.float32 else tcl.OUT_BF16, M, N, K, cfg)
-    assert pl["bn"] == 64 and pl["cta_pair"] == 1 and pl["splits"] == split
+    assert pl["bn"] == 64 and pl["cta_pair"] == 1 and pl["splits"] == split and pl["cluster_k"] == 1
     ldc = up(N, 4 if out == torch.float32 else 8)
     bf16_case(oracle_mod, M, N, K, seed=M + N + K, out_dtype=out, cfg=cfg, ldc=ldc)
+
+
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("cl", [2, 4])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 256), (512, 512, 1024), (300, 200, 520), (130, 72, 64),
+                                   (256, 136, 2000), (1000, 130, 1000)])
+def test_bf16_cluster_k(oracle_mod, out, cl, M, N, K):
+    # each 128×64 tile on a cluster of `cl` CTAs, one K range each, summed through
+    # distributed shared memory in rank order; ragged M, N and K, and at K = 64 (one
+    # k-block) the ranges of all but one CTA are empty
+    cfg = tcl.Config(cluster_k=cl)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32 if out == torch.float32 else tcl.OUT_BF16, M, N, K, cfg)
+    assert (pl["cluster_k"], pl["bn"], pl["splits"]) == (cl, 64, 1)
+    assert pl["grid"] == cl * pl["num_tiles"]
+    ldc = up(N, 4 if out == torch.float32 else 8)
+    bf16_case(oracle_mod, M, N, K, seed=M + N + K + cl, out_dtype=out, cfg=cfg, ldc=ldc)
+
+
+def test_bf16_cluster_k_deterministic():
+    # the partials are added in a fixed order, so every run gives the same bits
+    a, b = inputs.bf16_pair(512, 512, 512, seed=5)
+    a, b = a.to(DEV), b.to(DEV)
+    cfg = tcl.Config(cluster_k=4)
+    first = tcl.gemm(a, b, cfg=cfg)
+    for _ in range(20):
+        assert torch.equal(tcl.gemm(a, b, cfg=cfg), first)
+    one = tcl.gemm(a, b)   # one CTA per tile: another summation order
+    assert torch.allclose(one, first, rtol=1e-5, atol=1e-3)
 
 
 @pytest.mark.parametrize("bn", [128, 256])

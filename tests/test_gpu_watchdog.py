@@ -126,6 +126,23 @@ def test_trace_shows_loads_ahead_of_mma(pair):
     assert torch.equal(c, ref)
 
 
+def test_cluster_k_bounded_wait_runs_out():
+    # CTA 0 of the first cluster never loads one of its k-blocks: its MMA warp's bounded
+    # wait runs out, every CTA still reaches both cluster barriers and returns, and the
+    # next call on the device is correct
+    a, b = inputs.bf16_pair(512, 512, 1024, seed=7)
+    a, b = a.to(DEV), b.to(DEV)
+    c = torch.zeros((512, 512), dtype=torch.float32, device=DEV)
+    tcl.gemm_into(a, b, c, cfg=tcl.Config(cluster_k=4, timeout_ns=50_000_000, debug_skip_kblock=2))
+    st, code = tcl.last_device_error()
+    assert st == 7 and code in (1, 2, 4), (st, code)
+    x = tcl.gemm(a, b, cfg=tcl.Config(cluster_k=4))
+    y = tcl.gemm(a, b, cfg=tcl.Config(cluster_k=1))
+    torch.cuda.synchronize()
+    assert torch.allclose(x, y, rtol=1e-5, atol=1e-3)
+    assert tcl.last_device_error() == (0, 0)
+
+
 def test_s8_in_kernel_bounded_wait_runs_out():
     # CTA 0's converter warps never hand one k-block over: the leader's MMA warp's bounded
     # wait for the stage runs out, both CTAs of the pair abort and return, and the next

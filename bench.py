@@ -525,6 +525,13 @@ COMPARE_GROUPS = {
                ("64 wide, 4 K ranges", dict(bn=64, split_k=4, cluster_k=1)),
                ("128 wide, 4 K ranges", dict(bn=128, split_k=4)),
                ("128 wide, 8 K ranges", dict(bn=128, split_k=8))]),
+    "short_k": ([("bf16", 4096, 4096, k) for k in (256, 512, 1024)],
+                [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
+                 ("one SM, 256 wide", dict(cta_pair=1, bn=256)),
+                 ("one SM, 256 wide, group 2", dict(cta_pair=1, bn=256, group_m=2)),
+                 ("one SM, 256 wide, group 32", dict(cta_pair=1, bn=256, group_m=32)),
+                 ("two SMs, 256 wide", dict(cta_pair=2, bn=256, stream_k=1)),
+                 ("two SMs, 224 wide", dict(cta_pair=2, bn=224, stream_k=1))]),
 }
 
 # --variant-launches: one call of each alternative (after an L2 flush) for an ncu

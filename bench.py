@@ -525,6 +525,11 @@ COMPARE_GROUPS = {
                ("64 wide, 4 K ranges", dict(bn=64, split_k=4, cluster_k=1)),
                ("128 wide, 4 K ranges", dict(bn=128, split_k=4)),
                ("128 wide, 8 K ranges", dict(bn=128, split_k=8))]),
+    "mid": ([("bf16", 1024, 4096, 4096), ("bf16", 2048, 2048, 4096), ("bf16", 1024, 4096, 1024),
+             ("bf16", 2048, 2048, 1024), ("bf16", 1536, 3072, 2048), ("bf16", 3072, 3072, 1024)],
+            [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
+             ("one SM, 256 wide", dict(cta_pair=1, bn=256)), ("two SMs, 256 wide", dict(cta_pair=2, bn=256)),
+             ("two SMs, 224 wide", dict(cta_pair=2, bn=224))]),
     "short_k": ([("bf16", 4096, 4096, k) for k in (256, 512, 1024)],
                 [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
                  ("one SM, 256 wide", dict(cta_pair=1, bn=256)),

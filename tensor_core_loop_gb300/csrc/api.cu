@@ -339,6 +339,18 @@ int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_til
     return TCL_OK;
 }
 
+// One SM per tile (bf16 operands): SM cycles per 64-deep k-block of a wave of
+// 128×128 and 128×256 tiles, and the fixed cycles of a launch (first loads,
+// last epilogue), fitted on GB300 (CUDA graphs of back-to-back calls at
+// 1024×4096 and 2048² with K = 1024 and 4096: 128 wide ~0.23 µs per k-block
+// and wave, 256 wide ~0.335, the two-SM tiles ~0.27 (256 wide) and ~0.26 (224
+// wide), which kPairKbCycles* match; the launch's fixed part ~5, ~6.3 and ~9 µs).
+constexpr long long kOneKbCycles128 = 440;
+constexpr long long kOneKbCycles256 = 640;
+constexpr long long kOneFixedCycles128 = 9500;
+constexpr long long kOneFixedCycles256 = 12000;
+constexpr long long kPairFixedCycles = 17000;
+
 // Busiest pair's k-block cycles for pair tiles of width w: ceil(tiles / pairs)
 // whole tiles, or the full waves plus the largest stream-K piece.
 long long pair_cost(long long tiles, int pairs, int num_kb, long long kb_cycles, int sk_tiles, int sk_pieces) {
@@ -346,6 +358,17 @@ long long pair_cost(long long tiles, int pairs, int num_kb, long long kb_cycles,
     const long long waves = tiles / pairs;
     return (waves * num_kb + (num_kb + sk_pieces - 1) / sk_pieces) * kb_cycles +
            (waves == 0 ? (sk_pieces - 1) * kSkLinkCycles : 0);
+}
+
+// Cycles of a one-SM launch of 128-wide or 256-wide tiles (w = 0: the cheaper).
+long long one_sm_cost(int M, int N, int num_kb, int sms, int w) {
+    auto cost = [&](int bw, long long kb_cycles, long long fixed) {
+        const long long tiles = static_cast<long long>((M + kBM - 1) / kBM) * ((N + bw - 1) / bw);
+        return (tiles + sms - 1) / sms * num_kb * kb_cycles + fixed;
+    };
+    const long long c128 = cost(128, kOneKbCycles128, kOneFixedCycles128);
+    const long long c256 = cost(256, kOneKbCycles256, kOneFixedCycles256);
+    return w == 128 ? c128 : w == 256 ? c256 : std::min(c128, c256);
 }
 
 // Balanced stream-K over `pairs` pairs: the whole tiles of all waves but the
@@ -429,7 +452,32 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         // GB300: at 4096²×256 one SM per tile is faster, from K = 1024 on the pair).
         const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + pair_bn - 1) / pair_bn);
         const int kblocks = (K + bk - 1) / bk;
-        pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
+        if (ik == InKind::BF16 && ok != OutKind::S32) {
+            // bf16: the cheaper of the best two-SM tiling (256 or 224 wide, with the
+            // stream-K tail the launch would get) and the best one-SM tiling, by the
+            // cost model above (measured on GB300: 1024×4096×4096 on two-SM 224-wide
+            // tiles 25.3 µs against 36.0 on the 128-wide tiles an SM-count threshold
+            // chose; 3072²×1024 one SM, 256 wide, 19.0 against 20.1 on two SMs)
+            const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
+            const int pairs = std::max(1, cap / 2);
+            const int want_sk = cfg ? cfg->stream_k : 0;
+            long long best_pair = -1;
+            for (int w : {256, 224}) {
+                if (w == 224 && !(ok == OutKind::F32 && want_sk <= 1)) continue;
+                const long long t = static_cast<long long>((M + 255) / 256) * ((N + w - 1) / w);
+                // (the grid never has more pairs than tiles, so fewer tiles than pairs get no tail)
+                const int pe = static_cast<int>(std::min<long long>(pairs, t));
+                int skt = 0, skp = 1;
+                if (stream_k_split(t, pe, kblocks, want_sk, &skt, &skp)) skt = 0, skp = 1;
+                const long long c =
+                    pair_cost(t, pe, kblocks, w == 256 ? kPairKbCycles256 : kPairKbCycles224, skt, skp) +
+                    kPairFixedCycles;
+                if (best_pair < 0 || c < best_pair) best_pair = c;
+            }
+            pair = (kblocks >= kMinKbForPair && best_pair < one_sm_cost(M, N, kblocks, cap, 0)) ? 1 : 0;
+        } else {
+            pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
+        }
     }
     const int want_sk = cfg ? cfg->stream_k : 0;
     // stream-K pieces add into C (fp32, int32) or, for a bf16 C (which must be rounded
@@ -470,6 +518,10 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             const long long tiles256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256);
             const int kblocks = (K + bk - 1) / bk;
             bn = (tiles256 >= sms && (kblocks > 4 || ok == OutKind::BF16)) ? 256 : 128;
+            if (ik == InKind::BF16 && kblocks > 4) {   // bf16 beyond 4 k-blocks: by the cost model
+                const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
+                bn = one_sm_cost(M, N, kblocks, cap, 256) <= one_sm_cost(M, N, kblocks, cap, 128) ? 256 : 128;
+            }
             // Small grids (128-wide tiles filling at most a quarter of the SMs) too shallow
             // for split-K: 64-wide tiles give twice the CTAs, each with half the B bytes
             // and half the C stores (measured on GB300, CUDA graphs of back-to-back calls

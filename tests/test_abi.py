@@ -160,6 +160,14 @@ def test_plan_without_device(L):
             tcl.plan(in_kind, out, 512, 512, 512, tcl.Config(max_ctas=152, cluster_k=2))
     # split-K shapes keep 128-wide tiles
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 2048, cfg)["bn"] == 128
+    # mid-size outputs by the cost model (waves × k-blocks × per-k-block cycles + fixed
+    # cycles per launch): the measured fastest shape at each of these
+    for (m, n, k), want in {(1024, 4096, 4096): (2, 224), (2048, 2048, 4096): (2, 256),
+                            (1024, 4096, 1024): (1, 256), (2048, 2048, 1024): (1, 256),
+                            (1536, 3072, 2048): (1, 256), (3072, 3072, 1024): (1, 256),
+                            (512, 4096, 4096): (1, 128)}.items():
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k, cfg)
+        assert (p["cta_pair"], p["bn"]) == want, ((m, n, k), p)
     # deep two-SM tiles (rows of A of 16 KB and more): a row of tiles at a time, K walked
     # in alternating directions; shorter rows keep groups of 8 and ascending K
     for in_kind, k in ((tcl.IN_BF16, 8192), (tcl.IN_TF32, 4096)):

@@ -530,6 +530,15 @@ COMPARE_GROUPS = {
             [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
              ("one SM, 256 wide", dict(cta_pair=1, bn=256)), ("two SMs, 256 wide", dict(cta_pair=2, bn=256)),
              ("two SMs, 224 wide", dict(cta_pair=2, bn=224))]),
+    "mid_tf32": ([("tf32", 1024, 4096, 4096), ("tf32", 2048, 2048, 4096), ("tf32", 1024, 4096, 1024),
+                  ("tf32", 3072, 3072, 2048)],
+                 [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
+                  ("one SM, 256 wide", dict(cta_pair=1, bn=256)), ("two SMs, 256 wide", dict(cta_pair=2, bn=256)),
+                  ("two SMs, 224 wide", dict(cta_pair=2, bn=224))]),
+    "mid_s8": ([("s8", 1024, 4096, 4096), ("s8", 2048, 2048, 4096), ("s8", 1024, 4096, 1024),
+                ("s8", 3072, 3072, 2048)],
+               [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
+                ("two SMs, 256 wide", dict(cta_pair=2, bn=256)), ("two SMs, 128 wide", dict(cta_pair=2, bn=128))]),
     "short_k": ([("bf16", 4096, 4096, k) for k in (256, 512, 1024)],
                 [("automatic", dict()), ("one SM, 128 wide", dict(cta_pair=1, bn=128)),
                  ("one SM, 256 wide", dict(cta_pair=1, bn=256)),

@@ -452,12 +452,16 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         // GB300: at 4096²×256 one SM per tile is faster, from K = 1024 on the pair).
         const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + pair_bn - 1) / pair_bn);
         const int kblocks = (K + bk - 1) / bk;
-        if (ik == InKind::BF16 && ok != OutKind::S32) {
-            // bf16: the cheaper of the best two-SM tiling (256 or 224 wide, with the
-            // stream-K tail the launch would get) and the best one-SM tiling, by the
-            // cost model above (measured on GB300: 1024×4096×4096 on two-SM 224-wide
-            // tiles 25.3 µs against 36.0 on the 128-wide tiles an SM-count threshold
-            // chose; 3072²×1024 one SM, 256 wide, 19.0 against 20.1 on two SMs)
+        {
+            // The cheaper of the best two-SM tiling (256 or 224 wide, with the stream-K
+            // tail the launch would get; exact integers: 256 wide) and the best one-SM
+            // tiling (exact integers: 128 wide), by the cost model above. A TF32 k-block
+            // (32 deep) takes the tensor pipe as long as a bf16 one (64 deep) and moves
+            // as many bytes, so the same constants serve both. Measured on GB300:
+            // 1024×4096×4096 on two-SM 224-wide tiles 25.3 µs against 36.0 on the
+            // 128-wide tiles an SM-count threshold chose (TF32 47.0 against 73.6, int8
+            // on two-SM 256-wide tiles 36.9 against 44.7); 3072²×1024 one SM, 256 wide,
+            // 19.0 against 20.1 on two SMs.
             const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
             const int pairs = std::max(1, cap / 2);
             const int want_sk = cfg ? cfg->stream_k : 0;
@@ -474,10 +478,12 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
                     kPairFixedCycles;
                 if (best_pair < 0 || c < best_pair) best_pair = c;
             }
-            pair = (kblocks >= kMinKbForPair && best_pair < one_sm_cost(M, N, kblocks, cap, 0)) ? 1 : 0;
-        } else {
-            pair = (tiles_pair >= sms / 2 && kblocks >= kMinKbForPair) ? 1 : 0;
+            pair = (kblocks >= kMinKbForPair &&
+                    best_pair < one_sm_cost(M, N, kblocks, cap, ok == OutKind::S32 ? 128 : 0))
+                       ? 1
+                       : 0;
         }
+        (void)tiles_pair;
     }
     const int want_sk = cfg ? cfg->stream_k : 0;
     // stream-K pieces add into C (fp32, int32) or, for a bf16 C (which must be rounded
@@ -518,7 +524,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             const long long tiles256 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 255) / 256);
             const int kblocks = (K + bk - 1) / bk;
             bn = (tiles256 >= sms && (kblocks > 4 || ok == OutKind::BF16)) ? 256 : 128;
-            if (ik == InKind::BF16 && kblocks > 4) {   // bf16 beyond 4 k-blocks: by the cost model
+            if (kblocks > 4) {   // beyond 4 k-blocks: by the cost model
                 const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
                 bn = one_sm_cost(M, N, kblocks, cap, 256) <= one_sm_cost(M, N, kblocks, cap, 128) ? 256 : 128;
             }

@@ -168,6 +168,12 @@ def test_plan_without_device(L):
                             (512, 4096, 4096): (1, 128)}.items():
         p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k, cfg)
         assert (p["cta_pair"], p["bn"]) == want, ((m, n, k), p)
+    for in_kind, (m, n, k), want in ((tcl.IN_TF32, (1024, 4096, 4096), (2, 224)),
+                                     (tcl.IN_TF32, (1024, 4096, 1024), (1, 256)),
+                                     (tcl.IN_S8, (1024, 4096, 4096), (2, 256)),
+                                     (tcl.IN_S8, (1024, 4096, 1024), (1, 128))):
+        p = tcl.plan(in_kind, 0, m, n, k, cfg)
+        assert (p["cta_pair"], p["bn"]) == want, ((m, n, k), p)
     # deep two-SM tiles (rows of A of 16 KB and more): a row of tiles at a time, K walked
     # in alternating directions; shorter rows keep groups of 8 and ascending K
     for in_kind, k in ((tcl.IN_BF16, 8192), (tcl.IN_TF32, 4096)):

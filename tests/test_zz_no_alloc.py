@@ -80,7 +80,7 @@ def _sample_rows(M, n, seed):
     return sorted(r for r in fixed.union(g.integers(0, M, n).tolist()) if 0 <= r < M)
 
 
-@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (2304, 2304, 1024)])
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (3072, 3072, 2048)])
 def test_static_entry_large_problems_exact(L, oracle_mod, M, N, K):
     # Problems for which gemm_s8 itself runs on two SMs per tile: 4096³ fills the
     # 64 MiB array exactly (2·(4096·4096 + 4096·4096) bytes of bf16 copies). The

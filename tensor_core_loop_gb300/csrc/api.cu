@@ -446,44 +446,38 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             return TCL_ERR_CONFIG;
         pair = 1;
     } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages) && want_ck < 2) {
-        // Two SMs per 256-row tile halve each SM's bytes per flop; use them when
-        // there are at least as many pair tiles as pairs of SMs and a tile has
-        // enough k-blocks for its mainloop to outlast its epilogue (measured on
-        // GB300: at 4096²×256 one SM per tile is faster, from K = 1024 on the pair).
-        const long long tiles_pair = static_cast<long long>((M + 255) / 256) * ((N + pair_bn - 1) / pair_bn);
+        // Two SMs per 256-row tile halve each SM's bytes per flop, but pay a longer
+        // hand-off per tile. Take them when the cheaper of the best two-SM tiling
+        // (256 or 224 wide, with the stream-K tail the launch would get; exact
+        // integers: 256 wide) beats the best one-SM tiling (exact integers: 128 wide)
+        // by the cost model above, and a tile has enough k-blocks for its mainloop to
+        // outlast its epilogue (at 4096²×512 one SM per tile is faster, 22.0 against
+        // 27.1 µs). A TF32 k-block (32 deep) takes the tensor pipe as long as a bf16
+        // one (64 deep) and moves as many bytes, so the same constants serve both.
+        // Measured on GB300: 1024×4096×4096 on two-SM 224-wide tiles 25.3 µs against
+        // 36.0 on the 128-wide tiles an SM-count threshold chose (TF32 47.0 against
+        // 73.6, int8 on two-SM 256-wide tiles 36.9 against 44.7); 3072²×1024 one SM,
+        // 256 wide, 19.0 against 20.1 on two SMs.
         const int kblocks = (K + bk - 1) / bk;
-        {
-            // The cheaper of the best two-SM tiling (256 or 224 wide, with the stream-K
-            // tail the launch would get; exact integers: 256 wide) and the best one-SM
-            // tiling (exact integers: 128 wide), by the cost model above. A TF32 k-block
-            // (32 deep) takes the tensor pipe as long as a bf16 one (64 deep) and moves
-            // as many bytes, so the same constants serve both. Measured on GB300:
-            // 1024×4096×4096 on two-SM 224-wide tiles 25.3 µs against 36.0 on the
-            // 128-wide tiles an SM-count threshold chose (TF32 47.0 against 73.6, int8
-            // on two-SM 256-wide tiles 36.9 against 44.7); 3072²×1024 one SM, 256 wide,
-            // 19.0 against 20.1 on two SMs.
-            const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
-            const int pairs = std::max(1, cap / 2);
-            const int want_sk = cfg ? cfg->stream_k : 0;
-            long long best_pair = -1;
-            for (int w : {256, 224}) {
-                if (w == 224 && !(ok == OutKind::F32 && want_sk <= 1)) continue;
-                const long long t = static_cast<long long>((M + 255) / 256) * ((N + w - 1) / w);
-                // (the grid never has more pairs than tiles, so fewer tiles than pairs get no tail)
-                const int pe = static_cast<int>(std::min<long long>(pairs, t));
-                int skt = 0, skp = 1;
-                if (stream_k_split(t, pe, kblocks, want_sk, &skt, &skp)) skt = 0, skp = 1;
-                const long long c =
-                    pair_cost(t, pe, kblocks, w == 256 ? kPairKbCycles256 : kPairKbCycles224, skt, skp) +
-                    kPairFixedCycles;
-                if (best_pair < 0 || c < best_pair) best_pair = c;
-            }
-            pair = (kblocks >= kMinKbForPair &&
-                    best_pair < one_sm_cost(M, N, kblocks, cap, ok == OutKind::S32 ? 128 : 0))
-                       ? 1
-                       : 0;
+        const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
+        const int pairs = std::max(1, cap / 2);
+        const int want_sk = cfg ? cfg->stream_k : 0;
+        long long best_pair = -1;
+        for (int w : {256, 224}) {
+            if (w == 224 && !(ok == OutKind::F32 && want_sk <= 1)) continue;
+            const long long t = static_cast<long long>((M + 255) / 256) * ((N + w - 1) / w);
+            // (the grid never has more pairs than tiles, so fewer tiles than pairs get no tail)
+            const int pe = static_cast<int>(std::min<long long>(pairs, t));
+            int skt = 0, skp = 1;
+            if (stream_k_split(t, pe, kblocks, want_sk, &skt, &skp)) skt = 0, skp = 1;
+            const long long c =
+                pair_cost(t, pe, kblocks, w == 256 ? kPairKbCycles256 : kPairKbCycles224, skt, skp) + kPairFixedCycles;
+            if (best_pair < 0 || c < best_pair) best_pair = c;
         }
-        (void)tiles_pair;
+        pair = (kblocks >= kMinKbForPair &&
+                best_pair < one_sm_cost(M, N, kblocks, cap, ok == OutKind::S32 ? 128 : 0))
+                   ? 1
+                   : 0;
     }
     const int want_sk = cfg ? cfg->stream_k : 0;
     // stream-K pieces add into C (fp32, int32) or, for a bf16 C (which must be rounded

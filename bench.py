@@ -520,6 +520,8 @@ COMPARE_GROUPS = {
              [("widening pass", dict(s8_path=1)), ("in-kernel widening", dict(s8_path=2))]),
     "small": ([("bf16", 512, 512, k) for k in (256, 512, 1024, 2048, 4096, 8192)],
               [("automatic", dict()), ("64 wide", dict(bn=64, split_k=1, cluster_k=1)),
+               ("64 wide, no programmatic launch", dict(bn=64, split_k=1, cluster_k=1, serial_launch=1)),
+               ("64×64 tiles", dict(tile_m=64)),
                ("64 wide, cluster of 2", dict(cluster_k=2)), ("64 wide, cluster of 4", dict(cluster_k=4)),
                ("128 wide", dict(bn=128, split_k=1)),
                ("64 wide, 4 K ranges", dict(bn=64, split_k=4, cluster_k=1)),

@@ -198,6 +198,13 @@ typedef struct {
                                       through distributed shared memory (one launch, no
                                       workspace). Not with split_k > 1, one_cta_per_tile, stages,
                                       producer != 0, or a bn other than 0 or 64 (TCL_ERR_CONFIG) */
+    int tile_m;                    /* rows per output tile of the one-SM kernels: 0 automatic (64
+                                      for grids of 128×128 tiles that fill at most a quarter of
+                                      the SMs with fewer than 24 k-blocks, else 128), 128,
+                                      or 64 (bf16 in, fp32 or bf16 C: 64×64 tiles, one CTA per tile,
+                                      tcgen05.mma with M = 64, C stored from registers; not with
+                                      split_k > 1, cluster_k > 1, cta_pair 2, stages, producer != 0,
+                                      or a bn other than 0 or 64: TCL_ERR_CONFIG) */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -310,6 +317,7 @@ typedef struct {
                                        (tcl_config_t.s8_path = 2), 0 for the widening pass */
     int cluster_k;                  /* CTAs per tile whose K ranges are summed in a cluster
                                        (1: one CTA per tile; see tcl_config_t.cluster_k) */
+    int tile_m;                     /* rows per output tile (64, 128, or 256 for two SMs per tile) */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

@@ -70,6 +70,7 @@ class Config(ctypes.Structure):
         ("k_order", ctypes.c_int),
         ("s8_path", ctypes.c_int),
         ("cluster_k", ctypes.c_int),
+        ("tile_m", ctypes.c_int),
     ]
 
 
@@ -92,6 +93,7 @@ class PlanInfo(ctypes.Structure):
         ("k_serpentine", ctypes.c_int),
         ("s8_in_kernel", ctypes.c_int),
         ("cluster_k", ctypes.c_int),
+        ("tile_m", ctypes.c_int),
     ]
 
 

@@ -287,6 +287,7 @@ struct Plan {
     int k_serpentine;           // odd units of a CTA's walk load K in descending order
     int s8_in_kernel;           // int8: the two-SM kernel that widens the operands itself
     int csk;                    // > 1: CTAs per tile summing its K ranges in a cluster (gemm_kernel_csk.cuh)
+    int m64;                    // 1: 64×64 tiles, one CTA per tile (gemm_kernel_m64.cuh)
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -434,6 +435,17 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         if (!ck_capable) return TCL_ERR_CONFIG;
         bn = 64;
     }
+    // 64-row tiles: bf16 in, fp32 or bf16 C, one SM per 64×64 tile
+    const int want_tm = cfg ? cfg->tile_m : 0;
+    if (want_tm != 0 && want_tm != 64 && want_tm != 128) return TCL_ERR_CONFIG;
+    bool use_m64 = want_tm == 64;
+    if (want_tm == 64) {
+        if (!(ik == InKind::BF16 && (ok == OutKind::F32 || ok == OutKind::BF16) && prod == PROD_TMA &&
+              want_pair != 2 && !(cfg && cfg->one_cta_per_tile) && !(cfg && cfg->split_k > 1) && want_ck < 2 &&
+              !(cfg && cfg->stages) && (bn == 0 || bn == 64)))
+            return TCL_ERR_CONFIG;
+        bn = 64;
+    }
     int pair = 0;
     // the two-SM kernel: bf16 or TF32 in, float out (256 or 224 wide), or the
     // exact-integer mode (256 wide with eight epilogue warps, or 128 wide with
@@ -445,7 +457,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         if (ok == OutKind::S32 ? (bn != 0 && bn != 128 && bn != 256) : (bn != 0 && bn != 256 && bn != 224))
             return TCL_ERR_CONFIG;
         pair = 1;
-    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages) && want_ck < 2) {
+    } else if (want_pair == 0 && pair_capable && bn == 0 && !(cfg && cfg->stages) && want_ck < 2 && want_tm != 64) {
         // Two SMs per 256-row tile halve each SM's bytes per flop, but pay a longer
         // hand-off per tile. Take them when the cheaper of the best two-SM tiling
         // (256 or 224 wide, with the stream-K tail the launch would get; exact
@@ -526,12 +538,19 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             // for split-K: 64-wide tiles give twice the CTAs, each with half the B bytes
             // and half the C stores (measured on GB300, CUDA graphs of back-to-back calls
             // at 512²: K = 256 4.37 against 4.98 µs, 512 5.21 against 5.92, 1024 6.74
-            // against 7.76).
+            // against 7.76), and bf16 operands take 64 rows as well: 64×64 tiles, four
+            // times the CTAs of 128×128 ones, half the A bytes per k-block (K = 256 3.90
+            // against 4.41 µs for 128×64 tiles, 512 4.75 against 5.26, 1024 6.25
+            // against 6.82; from 24 k-blocks split-K stays ahead).
             const long long tiles128 = static_cast<long long>((M + kBM - 1) / kBM) * ((N + 127) / 128);
             const bool split_asked = cfg && cfg->split_k > 1;
             if (bn == 128 && tiles128 * 4 <= sms && kblocks < kMinKbToSplit && !split_asked &&
-                !(cfg && cfg->stages) && deepest_stages(ik, ok, 64, prod, 0) > 0)
+                !(cfg && cfg->stages) && deepest_stages(ik, ok, 64, prod, 0) > 0) {
                 bn = 64;
+                if (want_tm == 0 && ik == InKind::BF16 && (ok == OutKind::F32 || ok == OutKind::BF16) &&
+                    prod == PROD_TMA && want_ck < 2 && !(cfg && cfg->one_cta_per_tile))
+                    use_m64 = true;
+            }
         }
     }
     if (bn != 128 && bn != 256 && !(pair && bn == 224) && !(!pair && bn == 64)) return TCL_ERR_CONFIG;
@@ -547,7 +566,8 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->prod = prod;
     pl->pair = pv;
     pl->smem = v->smem_bytes;
-    const int bm = pair ? 2 * kBM : kBM;
+    pl->m64 = (use_m64 && !pair) ? 1 : 0;
+    const int bm = pair ? 2 * kBM : pl->m64 ? 64 : kBM;
     pl->tiles_m = (M + bm - 1) / bm;
     pl->tiles_n = (N + bn - 1) / bn;
     const long long tiles = static_cast<long long>(pl->tiles_m) * pl->tiles_n;
@@ -561,6 +581,10 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     // 6.4 / 8.1 µs for clusters of 2 / 4 against 4.4) and to split-K with its reduction
     // launch above (K = 4096: 12.2 against 10.5): moving the 32 KB partial tiles between
     // the SMs of a cluster takes ~1 µs each, and a cluster barrier ~0.5 µs.
+    if (pl->m64) {   // its own ring (16 KB stages)
+        pl->stages = m64_stages();
+        pl->smem = m64_smem_bytes();
+    }
     pl->csk = 0;
     if (ck_capable && !pair && bn == 64 && want_ck >= 2) {
         pl->csk = want_ck;
@@ -606,7 +630,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     const int want_split = cfg ? cfg->split_k : 0;
     if (want_split < 0) return TCL_ERR_CONFIG;
     if (want_split > 1 && (pair || ok == OutKind::S32)) return TCL_ERR_CONFIG;
-    if (!pair && ok != OutKind::S32 && want_split != 1 && !pl->csk) {
+    if (!pair && ok != OutKind::S32 && want_split != 1 && !pl->csk && !pl->m64) {
         int sp = want_split;
         if (sp == 0) {
             const int cap = cfg && cfg->max_ctas > 0 ? cfg->max_ctas : sms;
@@ -686,6 +710,8 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         return TCL_ERR_CONFIG;
     } else if (cfg && cfg->one_cta_per_tile) {
         pl->grid = static_cast<int>(std::min<long long>(work, 0x7FFFFFFF));
+    } else if (pl->m64) {
+        pl->grid = pl->num_tiles;   // one CTA per tile
     } else if (pl->csk) {
         const long long ctas = static_cast<long long>(pl->num_tiles) * pl->csk;   // one cluster per tile
         if (ctas > 0x7FFFFFFFll) return TCL_ERR_DIMS;
@@ -761,6 +787,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.pair = pl.pair;
     a.slots = pl.slots;
     a.csk = pl.csk;
+    a.m64 = pl.m64;
     a.pdl = !(cfg && cfg->serial_launch);
     a.grid = pl.grid;
     a.stream = stream;
@@ -772,7 +799,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
             return st;
     } else {
-        if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, kBM, &a.tmA))) return st;
+        if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, pl.m64 ? 64 : kBM, &a.tmA))) return st;
         // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
         // 4-byte elements are swizzled in 32-byte units, the form the tensor core
         // reads an N-major 32-bit operand in
@@ -839,6 +866,8 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
         err = launch_s8_pair(a);
     } else if (pl.csk) {
         err = launch_csk(a, &found);
+    } else if (pl.m64) {
+        err = launch_m64(a, &found);
     } else if (pl.pair) {
         err = launch_group_pair(a, &found);
     } else if (ik == InKind::TF32) {
@@ -1291,6 +1320,7 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->k_serpentine = pl.k_serpentine;
         plan->s8_in_kernel = pl.s8_in_kernel;
         plan->cluster_k = pl.csk ? pl.csk : 1;
+        plan->tile_m = pl.pair ? 256 : pl.m64 ? 64 : 128;
     }
     return TCL_OK;
 }

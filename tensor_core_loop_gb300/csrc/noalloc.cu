@@ -92,6 +92,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     a.pair = 0;
     a.slots = 2;
     a.csk = 0;
+    a.m64 = 0;
     a.pdl = false;
     a.grid = grid;
     a.stream = stream;

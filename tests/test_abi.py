@@ -139,9 +139,22 @@ def test_plan_without_device(L):
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 256, cfg)["bn"] == 128
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 256, cfg)["bn"] == 256
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)     # 4 k-blocks: too short to split
-    # ... and 16 tiles of 128 columns fill a tenth of the SMs: 64-wide tiles, 32 CTAs
-    assert p["splits"] == 1 and p["bn"] == 64 and p["grid"] == 32 and p["workspace_bytes"] == 0
-    assert p["cluster_k"] == 1
+    # ... and 16 tiles of 128×128 fill a tenth of the SMs: 64×64 tiles, 64 CTAs
+    assert p["splits"] == 1 and p["bn"] == 64 and p["workspace_bytes"] == 0
+    assert (p["tile_m"], p["grid"], p["num_tiles"], p["stages"], p["cluster_k"]) == (64, 64, 64, 8, 1)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, tcl.Config(max_ctas=152, tile_m=128))
+    assert (p["tile_m"], p["bn"], p["grid"]) == (128, 64, 32)                       # 128×64 tiles
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 768, 768, 1024, cfg)["tile_m"] == 64  # 144 CTAs
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 2048, cfg)["tile_m"] == 128  # split-K instead
+    for bad in (tcl.Config(max_ctas=152, tile_m=32), tcl.Config(max_ctas=152, tile_m=64, bn=128),
+                tcl.Config(max_ctas=152, tile_m=64, cta_pair=2), tcl.Config(max_ctas=152, tile_m=64, split_k=2),
+                tcl.Config(max_ctas=152, tile_m=64, stages=4), tcl.Config(max_ctas=152, tile_m=64, cluster_k=2)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 512, bad)
+    for in_kind, out in ((tcl.IN_TF32, tcl.OUT_F32), (tcl.IN_S8, 0)):   # bf16 operands only
+        with pytest.raises(tcl.TclError):
+            tcl.plan(in_kind, out, 512, 512, 512, tcl.Config(max_ctas=152, tile_m=64))
+        assert tcl.plan(in_kind, out, 512, 512, 256, cfg)["tile_m"] == 128
     # K ranges of a tile summed in a cluster of 2 or 4 CTAs, on request
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, tcl.Config(max_ctas=152, cluster_k=4))
     assert (p["bn"], p["cluster_k"], p["grid"], p["num_tiles"], p["stages"]) == (64, 4, 128, 32, 4)

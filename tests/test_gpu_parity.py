@@ -568,6 +568,32 @@ def test_bf16_64_wide_tiles(oracle_mod, out, M, N, K, split):
 
 
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (512, 512, 256), (300, 200, 520), (130, 72, 64),
+                                   (1000, 130, 1000), (768, 768, 1024), (200, 136, 2064)])
+def test_bf16_64_row_tiles(oracle_mod, out, M, N, K):
+    # 64×64 tiles (tcgen05.mma with M = 64: the accumulator in lanes 0-15 of each TMEM lane
+    # quarter), C stored from registers: ragged M, N (a partial last column tile stored
+    # element by element) and K; the canaries around C catch any store outside it
+    cfg = tcl.Config(tile_m=64)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32 if out == torch.float32 else tcl.OUT_BF16, M, N, K, cfg)
+    assert (pl["tile_m"], pl["bn"], pl["splits"], pl["cta_pair"]) == (64, 64, 1, 1)
+    assert pl["grid"] == pl["num_tiles"] == ((M + 63) // 64) * ((N + 63) // 64)
+    ldc = up(N, 4 if out == torch.float32 else 8)
+    bf16_case(oracle_mod, M, N, K, seed=M + N + K + 64, out_dtype=out, cfg=cfg, ldc=ldc)
+
+
+def test_bf16_64_row_tiles_chosen_and_exact_match():
+    # the planner's choice for a small shallow grid; the same sums as 128×64 tiles (each
+    # output element's K order is the same MMA sequence), so the results agree closely
+    a, b = inputs.bf16_pair(512, 512, 512, seed=9)
+    a, b = a.to(DEV), b.to(DEV)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 512)["tile_m"] == 64
+    x = tcl.gemm(a, b)
+    y = tcl.gemm(a, b, cfg=tcl.Config(tile_m=128))
+    assert torch.allclose(x, y, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("cl", [2, 4])
 @pytest.mark.parametrize("M,N,K", [(512, 512, 256), (512, 512, 1024), (300, 200, 520), (130, 72, 64),
                                    (256, 136, 2000), (1000, 130, 1000)])

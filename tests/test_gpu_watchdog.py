@@ -143,6 +143,21 @@ def test_cluster_k_bounded_wait_runs_out():
     assert tcl.last_device_error() == (0, 0)
 
 
+def test_64_row_tiles_bounded_wait_runs_out():
+    # the 64×64-tile kernel: CTA 0 never loads one k-block, its MMA warp's wait runs out
+    a, b = inputs.bf16_pair(512, 512, 512, seed=8)
+    a, b = a.to(DEV), b.to(DEV)
+    c = torch.zeros((512, 512), dtype=torch.float32, device=DEV)
+    tcl.gemm_into(a, b, c, cfg=tcl.Config(tile_m=64, timeout_ns=50_000_000, debug_skip_kblock=2))
+    st, code = tcl.last_device_error()
+    assert st == 7 and code in (1, 2, 4), (st, code)
+    x = tcl.gemm(a, b, cfg=tcl.Config(tile_m=64))
+    y = tcl.gemm(a, b, cfg=tcl.Config(tile_m=128))
+    torch.cuda.synchronize()
+    assert torch.allclose(x, y, rtol=1e-5, atol=1e-4)
+    assert tcl.last_device_error() == (0, 0)
+
+
 def test_s8_in_kernel_bounded_wait_runs_out():
     # CTA 0's converter warps never hand one k-block over: the leader's MMA warp's bounded
     # wait for the stage runs out, both CTAs of the pair abort and return, and the next

@@ -660,13 +660,14 @@ def run_simt(args):
     print(json.dumps(line), flush=True)
 
 
-def trace_stats(t, stages, bn, num_kb):
-    """Pipeline statistics of one CTA's per-k-block stamps (issued, landed, MMAs issued, MMAs done)."""
+def trace_stats(t, stages, bn, num_kb, bm=128):
+    """Pipeline statistics of one CTA's per-k-block stamps (issued, landed, MMAs issued, MMAs done);
+    bm × bn is the CTA's share of a tile (the ideal MMA time at the pipe's 8192 flop/clk)."""
     import numpy as np
     issued, landed, mma, done = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
     n = len(t)
     nd = int((done > 0).sum())
-    out = {"kblocks_traced": n, "ideal_mma_cycles_per_kblock": 128 * bn * 64 * 2 / 8192}
+    out = {"kblocks_traced": n, "ideal_mma_cycles_per_kblock": bm * bn * 64 * 2 / 8192}
     idx = np.arange(max(0, min(nd, n - 1)))
     out["load_issued_before_prev_mma_done"] = float((issued[idx + 1] < done[idx]).mean()) if len(idx) else None
     idx2 = np.arange(max(0, min(nd, n - (stages - 1))))
@@ -727,10 +728,11 @@ def run_trace(args):
             t = tt[:4 * cap].reshape(cap, 4)
             t = t[:int((t[:, 0] > 0).sum())]   # k-blocks CTA 0 actually ran (a stream-K tail makes fewer)
             c0, g0, c1, g1 = tt[4 * cap:]
-            line = {"trace": f"{m}x{n}x{k}", "sm_mhz_in_kernel": round(1e3 * (c1 - c0) / max(1, g1 - g0), 1), "cta_pair": pl["cta_pair"], "bn": pl["bn"], "stages": pl["stages"],
+            line = {"trace": f"{m}x{n}x{k}", "sm_mhz_in_kernel": round(1e3 * (c1 - c0) / max(1, g1 - g0), 1),
+                    "cta_pair": pl["cta_pair"], "tile_m": pl["tile_m"], "bn": pl["bn"], "stages": pl["stages"],
                     "tiles_cta0": tiles_cta0}
-            # each SM computes 128 rows × bn columns per k-block in either kernel
-            line.update(trace_stats(t, pl["stages"], pl["bn"], num_kb))
+            # each SM computes 128 rows (64 on 64-row tiles) × bn columns per k-block
+            line.update(trace_stats(t, pl["stages"], pl["bn"], num_kb, bm=64 if pl["tile_m"] == 64 else 128))
             print(json.dumps(line), flush=True)
 
 

@@ -82,9 +82,12 @@ struct MapKey {
     uint64_t d0, d1, stride;
     uint32_t b0, b1;
     int swizzle;
+    uint64_t d2 = 0, stride2 = 0;   // a 3-D map's third dimension (0: 2-D)
+    uint32_t b2 = 0;
     bool operator==(const MapKey& o) const {
         return dev == o.dev && ptr == o.ptr && dtype == o.dtype && d0 == o.d0 && d1 == o.d1 &&
-               stride == o.stride && b0 == o.b0 && b1 == o.b1 && swizzle == o.swizzle;
+               stride == o.stride && b0 == o.b0 && b1 == o.b1 && swizzle == o.swizzle && d2 == o.d2 &&
+               stride2 == o.stride2 && b2 == o.b2;
     }
 };
 struct MapKeyHash {
@@ -102,6 +105,9 @@ struct MapKeyHash {
         mix(k.stride);
         mix((static_cast<uint64_t>(k.b0) << 32) | k.b1);
         mix(static_cast<uint64_t>(k.swizzle));
+        mix(k.d2);
+        mix(k.stride2);
+        mix(k.b2);
         return static_cast<size_t>(h);
     }
 };
@@ -278,6 +284,36 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
     return TCL_OK;
 }
 
+// 3-D map: dims (d0, d1, d2) innermost first, byte strides of dimensions 1 and
+// 2, box (b0, b1, b2); 128-byte swizzle.
+int tensor_map_3d(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMap* out) {
+    MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride1, b0, b1, static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B)};
+    key.d2 = d2;
+    key.stride2 = stride2;
+    key.b2 = b2;
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+        *out = it->second;
+        return TCL_OK;
+    }
+    int st = encode_fn();
+    if (st) return st;
+    CUtensorMap m;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1, stride2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(&m, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return TCL_ERR_LAUNCH;
+    if (g_maps.size() > 4096) g_maps.clear();
+    g_maps.emplace(key, m);
+    *out = m;
+    return TCL_OK;
+}
+
 struct Plan {
     int bn, stages, prod, pair, slots, grid, tiles_m, tiles_n, num_tiles, num_kb, kb_per_unit, group_m, smem;
     int sk_ws_rows;   // bf16 C with a stream-K tail: fp32 workspace rows (split tiles × 256), else 0
@@ -287,7 +323,7 @@ struct Plan {
     int k_serpentine;           // odd units of a CTA's walk load K in descending order
     int s8_in_kernel;           // int8: the two-SM kernel that widens the operands itself
     int csk;                    // > 1: CTAs per tile summing its K ranges in a cluster (gemm_kernel_csk.cuh)
-    int m64;                    // 1: 64×64 tiles, one CTA per tile (gemm_kernel_m64.cuh)
+    int m64;                    // 1 or 2: 64×64 tiles, one CTA per tile, k-blocks per stage (gemm_kernel_m64.cuh)
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -566,7 +602,9 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->prod = prod;
     pl->pair = pv;
     pl->smem = v->smem_bytes;
-    pl->m64 = (use_m64 && !pair) ? 1 : 0;
+    // 64×64 tiles take two k-blocks per stage (one 3-D tensor copy of A, one of B)
+    // when K is whole 64-wide blocks, so that no copy reads past a row's end
+    pl->m64 = (use_m64 && !pair) ? (K % 64 == 0 ? 2 : 1) : 0;
     const int bm = pair ? 2 * kBM : pl->m64 ? 64 : kBM;
     pl->tiles_m = (M + bm - 1) / bm;
     pl->tiles_n = (N + bn - 1) / bn;
@@ -581,9 +619,9 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     // 6.4 / 8.1 µs for clusters of 2 / 4 against 4.4) and to split-K with its reduction
     // launch above (K = 4096: 12.2 against 10.5): moving the 32 KB partial tiles between
     // the SMs of a cluster takes ~1 µs each, and a cluster barrier ~0.5 µs.
-    if (pl->m64) {   // its own ring (16 KB stages)
-        pl->stages = m64_stages();
-        pl->smem = m64_smem_bytes();
+    if (pl->m64) {   // its own ring (16 KB stages of one k-block, 32 KB of two)
+        pl->stages = m64_stages(pl->m64);
+        pl->smem = m64_smem_bytes(pl->m64);
     }
     pl->csk = 0;
     if (ck_capable && !pair && bn == 64 && want_ck >= 2) {
@@ -799,13 +837,21 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
             return st;
     } else {
-        if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, pl.m64 ? 64 : kBM, &a.tmA))) return st;
-        // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
-        // 4-byte elements are swizzled in 32-byte units, the form the tensor core
-        // reads an N-major 32-bit operand in
-        if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB,
-                             ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)))
-            return st;
+        if (pl.m64 == 2) {
+            // A as (64 K, M rows, K/64 k-blocks): one box brings two k-blocks' swizzle tiles;
+            // B in boxes of 128 K-rows
+            if ((st = tensor_map_3d(dev, A, in_t, bk, M, K / bk, lda * ies, 128, bk, 64, 2, &a.tmA)) ||
+                (st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, 2 * bk, &a.tmB)))
+                return st;
+        } else {
+            if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, pl.m64 ? 64 : kBM, &a.tmA))) return st;
+            // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
+            // 4-byte elements are swizzled in 32-byte units, the form the tensor core
+            // reads an N-major 32-bit operand in
+            if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB,
+                                 ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)))
+                return st;
+        }
     }
     void* out_ptr = split ? workspace : C;
     const long long out_ld = split ? ws.ld : ldc;

@@ -8,7 +8,13 @@
 //
 // Pipeline as in the one-SM kernel (TMA ring of STAGES stages with full/empty
 // mbarriers, one elected thread issuing four tcgen05.mma of 64×64×16 per
-// 64-deep k-block, one TMEM accumulator of 64 columns). The M = 64 accumulator
+// 64-deep k-block, one TMEM accumulator of 64 columns). A stage holds KPS
+// k-blocks brought by two tensor copies whatever KPS is (KPS = 2: A through a
+// 3-D map whose third dimension steps from one 64-wide K block to the next, so
+// one box is two 8 KB swizzle tiles; B in a box of 128 K-rows): on GB300 the
+// stages of two 8 KB boxes landed ~445 cycles apart for 64 cycles of MMA work,
+// and a tensor copy's cost barely depended on its size (a microbenchmark: the
+// issuing thread busy ~150–190 cycles per copy from 4 to 32 KB). The M = 64 accumulator
 // occupies 16 TMEM lanes of each 32-lane quarter (rows 16q..16q+15 in lanes
 // 32q..32q+15; LAYOUT 1 would be rows 0..63 in lanes 0..63); each of the four
 // epilogue warps reads its quarter and its first 16 lanes store their rows
@@ -20,13 +26,16 @@
 
 namespace tcl {
 
-template <OutKind OK, int STAGES_, int LAYOUT_ = 0>
+template <OutKind OK, int STAGES_, int KPS_ = 1, int LAYOUT_ = 0>
 struct M64Cfg {
     static constexpr int STAGES = STAGES_;
+    static constexpr int KPS = KPS_;                   // k-blocks per stage
     static constexpr int LAYOUT = LAYOUT_;
     static constexpr int BM = 64, BN = 64, BK = 64;   // bf16: BK is one 128-byte row
-    static constexpr int A_BYTES = BM * 128;           // 8 KB, K-major, 128-byte swizzle
-    static constexpr int B_BYTES = BK * 128;           // one N-major box: 64 columns × 64 K-rows
+    static constexpr int A_KB_BYTES = BM * 128;        // one k-block of A: 8 KB, K-major, 128-byte swizzle
+    static constexpr int B_KB_BYTES = BK * 128;        // one k-block of B: 64 columns × 64 K-rows, N-major
+    static constexpr int A_BYTES = KPS * A_KB_BYTES;
+    static constexpr int B_BYTES = KPS * B_KB_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 64;
     static constexpr int NBARS = 2 * STAGES + 2;       // full[S], empty[S], acc_full, drain
@@ -35,15 +44,16 @@ struct M64Cfg {
     static constexpr uint32_t IDESC = ptx::make_idesc(InTraits<InKind::BF16>::FMT, InTraits<InKind::BF16>::FMT,
                                                       /*A K-major*/ 0, /*B N-major*/ 1, BM, BN);
     static_assert(OK == OutKind::F32 || OK == OutKind::BF16, "fp32 or bf16 C");
+    static_assert(KPS == 1 || KPS == 2, "one or two k-blocks per stage");
     static_assert(NBARS * 8 + 8 <= 256, "barrier area");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-block shared memory limit");
 };
 
-template <OutKind OK, int STAGES, int LAYOUT>
-__global__ void __launch_bounds__(M64Cfg<OK, STAGES, LAYOUT>::THREADS, 1)
+template <OutKind OK, int STAGES, int KPS, int LAYOUT>
+__global__ void __launch_bounds__(M64Cfg<OK, STAGES, KPS, LAYOUT>::THREADS, 1)
     gemm_m64_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
-    using C = M64Cfg<OK, STAGES, LAYOUT>;
+    using C = M64Cfg<OK, STAGES, KPS, LAYOUT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -87,6 +97,7 @@ __global__ void __launch_bounds__(M64Cfg<OK, STAGES, LAYOUT>::THREADS, 1)
     int mb, nb;
     tile_coords(static_cast<int>(blockIdx.x), p, mb, nb);
     const int nkb = p.num_kb;
+    const int nst = (nkb + KPS - 1) / KPS;   // stage loads (a last odd k-block's partner is read as zeros)
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
     if (tracing && threadIdx.x == 0) {
         p.trace[4 * p.trace_cap + 1] = ptx::globaltimer_ns();
@@ -97,7 +108,7 @@ __global__ void __launch_bounds__(M64Cfg<OK, STAGES, LAYOUT>::THREADS, 1)
         // ------------------------------------------------ producer (TMA)
         uint32_t it = 0;
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int st = 0; st < nst; ++st, ++it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             if (!wait_warp(empty0 + 8 * s, ph ^ 1u, abort_flag, p.timeout_ns, p.status, DEV_TIMEOUT_PRODUCER)) {
                 ok = false;
@@ -112,8 +123,11 @@ __global__ void __launch_bounds__(M64Cfg<OK, STAGES, LAYOUT>::THREADS, 1)
             const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
             if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) continue;
             ptx::mbar_arrive_expect_tx_elected(full, C::STAGE_BYTES);
-            ptx::tma_load_2d_elected(sa, &tmA, full, kb * C::BK, mb * C::BM);
-            ptx::tma_load_2d_elected(sa + C::A_BYTES, &tmB, full, nb * C::BN, kb * C::BK);
+            if constexpr (KPS == 2)   // A: 64 K × 64 rows × 2 k-blocks through the 3-D map
+                ptx::tma_load_3d_elected(sa, &tmA, full, 0, mb * C::BM, st * KPS);
+            else
+                ptx::tma_load_2d_elected(sa, &tmA, full, st * C::BK, mb * C::BM);
+            ptx::tma_load_2d_elected(sa + C::A_BYTES, &tmB, full, nb * C::BN, st * KPS * C::BK);
         }
         if (!ok && lane == 0) {   // let the loads in flight land before the CTA can exit
             const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
@@ -131,14 +145,16 @@ __global__ void __launch_bounds__(M64Cfg<OK, STAGES, LAYOUT>::THREADS, 1)
         // ------------------------------------------------ MMA issuer
         const uint32_t stage0 = ptx::smem_u32(stage_base);
         const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
-        const uint64_t bdesc0 = ptx::sdesc(stage0 + C::A_BYTES, C::B_BYTES, InTraits<InKind::BF16>::B_SBO,
+        const uint64_t bdesc0 = ptx::sdesc(stage0 + C::A_BYTES, C::B_KB_BYTES, InTraits<InKind::BF16>::B_SBO,
                                            InTraits<InKind::BF16>::B_LAYOUT);
         constexpr uint64_t A_STEP = 16 * 2 / 16;     // a k-slice: 16 bf16 along the row
         constexpr uint64_t B_STEP = 16 * 128 / 16;   // a k-slice: 16 K-rows of 128 B
         constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
+        constexpr uint64_t KB_STEP = C::A_KB_BYTES / 16;   // next k-block of the stage (A and B alike)
+        static_assert(C::A_KB_BYTES == C::B_KB_BYTES, "k-blocks of A and B step alike");
         uint32_t it = 0;
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int st = 0; st < nst; ++st, ++it) {
             const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
             if (!wait_warp(full0 + 8 * s, ph, abort_flag, p.timeout_ns, p.status, DEV_TIMEOUT_MMA_FULL)) {
                 ok = false;
@@ -146,10 +162,15 @@ __global__ void __launch_bounds__(M64Cfg<OK, STAGES, LAYOUT>::THREADS, 1)
             }
             ptx::tc_fence_after();
             if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
-            const uint64_t ad = adesc0 + s * S_STEP;
-            const uint64_t bd = bdesc0 + s * S_STEP;
-            ptx::mma_f16_x4_elected(tmem_base, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP, bd + 2 * B_STEP,
-                                    ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC, kb > 0 ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < KPS; ++j) {
+                if (st * KPS + j >= nkb) break;
+                const uint64_t ad = adesc0 + s * S_STEP + j * KB_STEP;
+                const uint64_t bd = bdesc0 + s * S_STEP + j * KB_STEP;
+                ptx::mma_f16_x4_elected(tmem_base, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
+                                        bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
+                                        st * KPS + j > 0 ? 1u : 0u);
+            }
             ptx::mma_commit_elected(empty0 + 8 * s);
             if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
         }

@@ -18,7 +18,7 @@ struct LaunchArgs {
     int pair;   // 1: two-SM kernel (one CTA pair per cluster); 0: one-SM kernel
     int slots;  // epilogue staging slabs per warp (two-SM kernel)
     int csk;    // > 1: K ranges of one tile summed in a cluster of this many CTAs (k_csk.cu)
-    int m64;    // 1: 64×64 tiles (k_m64.cu)
+    int m64;    // 1 or 2: 64×64 tiles with that many k-blocks per stage (k_m64.cu)
     bool pdl;   // programmatic dependent launch
     CUtensorMap tmA, tmB, tmC;
     GemmParams p;
@@ -45,11 +45,13 @@ cudaError_t launch_s8_pair(const LaunchArgs& a);
 // Cluster-summed K ranges (k_csk.cu): bf16 in, fp32 or bf16 C, 128×64 tiles,
 // a.csk = 2 or 4 CTAs per tile; a.grid = tiles × a.csk.
 cudaError_t launch_csk(const LaunchArgs& a, bool* found);
-// 64×64 tiles, one CTA per tile (k_m64.cu): bf16 in, fp32 or bf16 C, a.bn = 64;
-// a.tmA maps A in boxes of 64 K × 64 rows; C is written from registers.
+// 64×64 tiles, one CTA per tile (k_m64.cu): bf16 in, fp32 or bf16 C, a.bn = 64,
+// a.m64 k-blocks per stage (1: a.tmA maps A in boxes of 64 K × 64 rows; 2: a
+// 3-D map of A, boxes of 64 K × 64 rows × 2 k-blocks, and a.tmB boxes of 128
+// K-rows); C is written from registers.
 cudaError_t launch_m64(const LaunchArgs& a, bool* found);
-int m64_stages();
-int m64_smem_bytes();
+int m64_stages(int kps);
+int m64_smem_bytes(int kps);
 int csk_stages();
 int csk_smem_bytes(int cl);
 int s8_pair_stages();

@@ -404,6 +404,18 @@ __device__ __forceinline__ void tma_load_2d_elected(uint32_t dst, const CUtensor
         : "memory");
 }
 
+// 3-D tiled load (coordinates innermost first), issued by one elected lane.
+__device__ __forceinline__ void tma_load_3d_elected(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                                    int32_t c1, int32_t c2) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_pair_elected(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
                                                          int32_t c0, int32_t c1) {
     asm volatile(

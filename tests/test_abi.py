@@ -141,7 +141,9 @@ def test_plan_without_device(L):
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)     # 4 k-blocks: too short to split
     # ... and 16 tiles of 128×128 fill a tenth of the SMs: 64×64 tiles, 64 CTAs
     assert p["splits"] == 1 and p["bn"] == 64 and p["workspace_bytes"] == 0
-    assert (p["tile_m"], p["grid"], p["num_tiles"], p["stages"], p["cluster_k"]) == (64, 64, 64, 8, 1)
+    assert (p["tile_m"], p["grid"], p["num_tiles"], p["stages"], p["cluster_k"]) == (64, 64, 64, 6, 1)
+    # (two k-blocks per 32 KB stage when K is whole 64-wide blocks, else one per 16 KB stage)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 520, cfg)["stages"] == 8
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, tcl.Config(max_ctas=152, tile_m=128))
     assert (p["tile_m"], p["bn"], p["grid"]) == (128, 64, 32)                       # 128×64 tiles
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 768, 768, 1024, cfg)["tile_m"] == 64  # 144 CTAs

@@ -569,11 +569,13 @@ def test_bf16_64_wide_tiles(oracle_mod, out, M, N, K, split):
 
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("M,N,K", [(64, 64, 64), (512, 512, 256), (300, 200, 520), (130, 72, 64),
-                                   (1000, 130, 1000), (768, 768, 1024), (200, 136, 2064)])
+                                   (1000, 130, 1000), (768, 768, 1024), (200, 136, 2064), (200, 136, 192)])
 def test_bf16_64_row_tiles(oracle_mod, out, M, N, K):
     # 64×64 tiles (tcgen05.mma with M = 64: the accumulator in lanes 0-15 of each TMEM lane
     # quarter), C stored from registers: ragged M, N (a partial last column tile stored
-    # element by element) and K; the canaries around C catch any store outside it
+    # element by element) and K; K a multiple of 64 takes two k-blocks per stage (a 3-D map
+    # of A), an odd count of them leaving the last stage's second k-block to zero fill;
+    # the canaries around C catch any store outside it
     cfg = tcl.Config(tile_m=64)
     pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32 if out == torch.float32 else tcl.OUT_BF16, M, N, K, cfg)
     assert (pl["tile_m"], pl["bn"], pl["splits"], pl["cta_pair"]) == (64, 64, 1, 1)

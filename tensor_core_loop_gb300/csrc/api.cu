@@ -287,8 +287,9 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
 // 3-D map: dims (d0, d1, d2) innermost first, byte strides of dimensions 1 and
 // 2, box (b0, b1, b2); 128-byte swizzle.
 int tensor_map_3d(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t d2,
-                  uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMap* out) {
-    MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride1, b0, b1, static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B)};
+                  uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMap* out,
+                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+    MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride1, b0, b1, static_cast<int>(swz)};
     key.d2 = d2;
     key.stride2 = stride2;
     key.b2 = b2;
@@ -305,8 +306,7 @@ int tensor_map_3d(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t 
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(&m, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return TCL_ERR_LAUNCH;
     if (g_maps.size() > 4096) g_maps.clear();
     g_maps.emplace(key, m);
@@ -829,6 +829,10 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.pdl = !(cfg && cfg->serial_launch);
     a.grid = pl.grid;
     a.stream = stream;
+    // Two-SM 256-wide tiles take all of a CTA's B boxes in one tensor copy (a 3-D map) when N
+    // is a whole number of boxes, so that no box reads past a row's end: a stage's copies,
+    // not its bytes, pace the stages (measured on GB300)
+    const bool b3d = pl.pair && !pl.s8_in_kernel && pl.bn == 256 && N % (128 / ies) == 0;
     if (pl.s8_in_kernel) {
         // raw int8 operands, unswizzled: A in boxes of 64 K × 128 rows, B of 128 columns × 64 K
         if ((st = tensor_map(dev, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 64, kBM, &a.tmA,
@@ -848,9 +852,17 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
             // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
             // 4-byte elements are swizzled in 32-byte units, the form the tensor core
             // reads an N-major 32-bit operand in
-            if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB,
-                                 ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)))
+            const CUtensorMapSwizzle bswz =
+                ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+            if (b3d) {
+                // (columns of a box, K, column blocks): one box holds a CTA's whole half of B
+                const uint32_t bw = 128 / ies;
+                if ((st = tensor_map_3d(dev, B, in_t, bw, K, N / bw, ldb * ies, 128, bw, bk, pl.bn / 2 / bw, &a.tmB,
+                                        bswz)))
+                    return st;
+            } else if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB, bswz))) {
                 return st;
+            }
         }
     }
     void* out_ptr = split ? workspace : C;
@@ -895,6 +907,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.sk_ws = nullptr;
     p.sk_ws_rows = 0;
     p.k_serpentine = pl.k_serpentine;
+    p.b_3d = b3d ? 1 : 0;
     if (pl.sk_ws_rows) {   // (16-byte accesses: the workspace starts on a 256-byte boundary)
         p.sk_ws = static_cast<float*>(workspace);
         p.sk_ws_rows = pl.sk_ws_rows;

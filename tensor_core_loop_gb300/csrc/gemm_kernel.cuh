@@ -130,6 +130,9 @@ struct GemmParams {
     // that a wave starts on the operand rows the previous wave read last, which
     // are the ones still in L2
     int k_serpentine;
+    // 1: tmB is a 3-D map (a box's columns, K, column blocks) and one tensor copy brings all
+    // of a stage's B boxes (two-SM kernel, 256-wide tiles, N a whole number of boxes)
+    int b_3d;
 };
 
 // K coordinate (in k-blocks) that the load at position kb of the range

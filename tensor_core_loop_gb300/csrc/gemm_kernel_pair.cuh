@@ -372,10 +372,14 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                     continue;
                 }
                 ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kc * C::BK, row);
+                if (p.b_3d) {   // this CTA's B_BOXES boxes in one copy (boxes B_BOX_BYTES apart, as below)
+                    ptx::tma_load_3d_pair_elected(sa + C::A_BYTES, &tmB, fb, 0, kc * C::BK, col / C::B_BOX_N);
+                } else {
 #pragma unroll
-                for (int b = 0; b < C::B_BOXES; ++b) {
-                    const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
-                    ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kc * C::BK);
+                    for (int b = 0; b < C::B_BOXES; ++b) {
+                        const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
+                        ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kc * C::BK);
+                    }
                 }
                 if (lane == 0) *progress = it + 1;
             }

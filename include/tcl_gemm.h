@@ -205,6 +205,14 @@ typedef struct {
                                       tcgen05.mma with M = 64, C stored from registers; not with
                                       split_k > 1, cluster_k > 1, cta_pair 2, stages, producer != 0,
                                       or a bn other than 0 or 64: TCL_ERR_CONFIG) */
+    int kblocks_per_stage;         /* two-SM 256-wide tiles: k-blocks (64 bf16 or 32 TF32 values of
+                                      K) that one tensor copy of A and one of B bring into the
+                                      ring: 0 automatic (2 where allowed), 1, or 2 (needs K a
+                                      multiple of the k-block, N of 64 bf16 / 32 TF32 columns, an
+                                      even ring depth and the widening pass for int8, else
+                                      TCL_ERR_CONFIG). Two halve the copies per k-block, which
+                                      pace the stages on GB300 more than their bytes do; the
+                                      result is the same either way (same summation order) */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -318,6 +326,7 @@ typedef struct {
     int cluster_k;                  /* CTAs per tile whose K ranges are summed in a cluster
                                        (1: one CTA per tile; see tcl_config_t.cluster_k) */
     int tile_m;                     /* rows per output tile (64, 128, or 256 for two SMs per tile) */
+    int kblocks_per_stage;          /* k-blocks that one tensor copy of each operand brings (1 or 2) */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

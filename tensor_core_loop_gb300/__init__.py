@@ -71,6 +71,7 @@ class Config(ctypes.Structure):
         ("s8_path", ctypes.c_int),
         ("cluster_k", ctypes.c_int),
         ("tile_m", ctypes.c_int),
+        ("kblocks_per_stage", ctypes.c_int),
     ]
 
 
@@ -94,6 +95,7 @@ class PlanInfo(ctypes.Structure):
         ("s8_in_kernel", ctypes.c_int),
         ("cluster_k", ctypes.c_int),
         ("tile_m", ctypes.c_int),
+        ("kblocks_per_stage", ctypes.c_int),
     ]
 
 

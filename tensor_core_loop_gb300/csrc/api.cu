@@ -84,10 +84,12 @@ struct MapKey {
     int swizzle;
     uint64_t d2 = 0, stride2 = 0;   // a 3-D map's third dimension (0: 2-D)
     uint32_t b2 = 0;
+    uint64_t d3 = 0, stride3 = 0;   // a 4-D map's fourth dimension (0: fewer)
+    uint32_t b3 = 0;
     bool operator==(const MapKey& o) const {
         return dev == o.dev && ptr == o.ptr && dtype == o.dtype && d0 == o.d0 && d1 == o.d1 &&
                stride == o.stride && b0 == o.b0 && b1 == o.b1 && swizzle == o.swizzle && d2 == o.d2 &&
-               stride2 == o.stride2 && b2 == o.b2;
+               stride2 == o.stride2 && b2 == o.b2 && d3 == o.d3 && stride3 == o.stride3 && b3 == o.b3;
     }
 };
 struct MapKeyHash {
@@ -108,6 +110,9 @@ struct MapKeyHash {
         mix(k.d2);
         mix(k.stride2);
         mix(k.b2);
+        mix(k.d3);
+        mix(k.stride3);
+        mix(k.b3);
         return static_cast<size_t>(h);
     }
 };
@@ -284,15 +289,18 @@ int tensor_map(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0,
     return TCL_OK;
 }
 
-// 3-D map: dims (d0, d1, d2) innermost first, byte strides of dimensions 1 and
-// 2, box (b0, b1, b2); 128-byte swizzle.
-int tensor_map_3d(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t d2,
-                  uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMap* out,
-                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+// 3-D or 4-D map (d3 = 0: 3-D): dims innermost first, byte strides of
+// dimensions 1.., box per dimension.
+int tensor_map_nd(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t d3, uint64_t stride1, uint64_t stride2, uint64_t stride3, uint32_t b0, uint32_t b1,
+                  uint32_t b2, uint32_t b3, CUtensorMap* out, CUtensorMapSwizzle swz) {
     MapKey key{dev, ptr, static_cast<int>(dtype), d0, d1, stride1, b0, b1, static_cast<int>(swz)};
     key.d2 = d2;
     key.stride2 = stride2;
     key.b2 = b2;
+    key.d3 = d3;
+    key.stride3 = stride3;
+    key.b3 = b3;
     auto it = g_maps.find(key);
     if (it != g_maps.end()) {
         *out = it->second;
@@ -301,17 +309,25 @@ int tensor_map_3d(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t 
     int st = encode_fn();
     if (st) return st;
     CUtensorMap m;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {stride1, stride2};
-    const cuuint32_t box[3] = {b0, b1, b2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(&m, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint32_t rank = d3 ? 4 : 3;
+    const cuuint64_t dims[4] = {d0, d1, d2, d3};
+    const cuuint64_t strides[3] = {stride1, stride2, stride3};
+    const cuuint32_t box[4] = {b0, b1, b2, b3};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(&m, dtype, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return TCL_ERR_LAUNCH;
     if (g_maps.size() > 4096) g_maps.clear();
     g_maps.emplace(key, m);
     *out = m;
     return TCL_OK;
+}
+
+int tensor_map_3d(int dev, const void* ptr, CUtensorMapDataType dtype, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMap* out,
+                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+    return tensor_map_nd(dev, ptr, dtype, d0, d1, d2, 0, stride1, stride2, 0, b0, b1, b2, 0, out, swz);
 }
 
 struct Plan {
@@ -324,6 +340,7 @@ struct Plan {
     int s8_in_kernel;           // int8: the two-SM kernel that widens the operands itself
     int csk;                    // > 1: CTAs per tile summing its K ranges in a cluster (gemm_kernel_csk.cuh)
     int m64;                    // 1 or 2: 64×64 tiles, one CTA per tile, k-blocks per stage (gemm_kernel_m64.cuh)
+    int kps;                    // two-SM kernel: k-blocks per tensor copy (1 or 2)
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -660,6 +677,16 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         pl->stages = s8_pair_stages();
         pl->smem = s8_pair_smem_bytes();
     }
+    // Two-SM 256-wide tiles: one copy of A and one of B bring two k-blocks into two ring slots,
+    // halving the tensor copies and byte announcements per k-block (what paces a stage, more
+    // than its bytes). The maps cut K and N into whole blocks, so K must be a whole number of
+    // k-blocks and N of B boxes (no box may read past a row's end), and the ring even.
+    const int want_kps = cfg ? cfg->kblocks_per_stage : 0;
+    if (want_kps < 0 || want_kps > 2) return TCL_ERR_CONFIG;
+    const bool kps2_ok = pair && !pl->s8_in_kernel && bn == 256 && prod == PROD_TMA && K % bk == 0 &&
+                         N % (128 / in_bytes(ik)) == 0 && pl->stages % 2 == 0;
+    if (want_kps == 2 && !kps2_ok) return TCL_ERR_CONFIG;
+    pl->kps = kps2_ok && want_kps != 1 ? 2 : 1;
     // Split-K (one-SM kernel, floating-point output): when the output tiles
     // alone would leave most SMs idle, cut K into ranges computed by different
     // CTAs; a second kernel adds the partial tiles in a fixed order.
@@ -832,7 +859,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     // Two-SM 256-wide tiles take all of a CTA's B boxes in one tensor copy (a 3-D map) when N
     // is a whole number of boxes, so that no box reads past a row's end: a stage's copies,
     // not its bytes, pace the stages (measured on GB300)
-    const bool b3d = pl.pair && !pl.s8_in_kernel && pl.bn == 256 && N % (128 / ies) == 0;
+    const bool b3d = pl.pair && !pl.s8_in_kernel && pl.bn == 256 && N % (128 / ies) == 0 && pl.kps == 1;
     if (pl.s8_in_kernel) {
         // raw int8 operands, unswizzled: A in boxes of 64 K × 128 rows, B of 128 columns × 64 K
         if ((st = tensor_map(dev, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 64, kBM, &a.tmA,
@@ -841,7 +868,17 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
             return st;
     } else {
-        if (pl.m64 == 2) {
+        const CUtensorMapSwizzle bswz =
+            ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+        if (pl.kps == 2) {
+            // A as (K of a block, rows, k-blocks) in boxes of 128 rows × 2 blocks; B as (a box's
+            // columns, K of a block, column blocks, k-blocks) in boxes of a CTA's half × 2 blocks
+            const uint32_t bw = 128 / ies;
+            if ((st = tensor_map_3d(dev, A, in_t, bk, M, K / bk, lda * ies, 128, bk, kBM, 2, &a.tmA)) ||
+                (st = tensor_map_nd(dev, B, in_t, bw, bk, N / bw, K / bk, ldb * ies, 128,
+                                    static_cast<uint64_t>(bk) * ldb * ies, bw, bk, pl.bn / 2 / bw, 2, &a.tmB, bswz)))
+                return st;
+        } else if (pl.m64 == 2) {
             // A as (64 K, M rows, K/64 k-blocks): one box brings two k-blocks' swizzle tiles;
             // B in boxes of 128 K-rows
             if ((st = tensor_map_3d(dev, A, in_t, bk, M, K / bk, lda * ies, 128, bk, 64, 2, &a.tmA)) ||
@@ -850,10 +887,8 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
         } else {
             if ((st = tensor_map(dev, A, in_t, K, M, lda * ies, bk, pl.m64 ? 64 : kBM, &a.tmA))) return st;
             // B N-major (K rows of N) in boxes of one 128-byte row of N × bk rows; TF32's
-            // 4-byte elements are swizzled in 32-byte units, the form the tensor core
+            // 4-byte elements are swizzled in 32-byte units (bswz), the form the tensor core
             // reads an N-major 32-bit operand in
-            const CUtensorMapSwizzle bswz =
-                ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
             if (b3d) {
                 // (columns of a box, K, column blocks): one box holds a CTA's whole half of B
                 const uint32_t bw = 128 / ies;
@@ -908,6 +943,7 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.sk_ws_rows = 0;
     p.k_serpentine = pl.k_serpentine;
     p.b_3d = b3d ? 1 : 0;
+    p.kps2 = pl.kps == 2 ? 1 : 0;
     if (pl.sk_ws_rows) {   // (16-byte accesses: the workspace starts on a 256-byte boundary)
         p.sk_ws = static_cast<float*>(workspace);
         p.sk_ws_rows = pl.sk_ws_rows;
@@ -1380,6 +1416,7 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->s8_in_kernel = pl.s8_in_kernel;
         plan->cluster_k = pl.csk ? pl.csk : 1;
         plan->tile_m = pl.pair ? 256 : pl.m64 ? 64 : 128;
+        plan->kblocks_per_stage = pl.pair ? pl.kps : pl.m64 == 2 ? 2 : 1;
     }
     return TCL_OK;
 }

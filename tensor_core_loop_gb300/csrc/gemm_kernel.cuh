@@ -133,6 +133,11 @@ struct GemmParams {
     // 1: tmB is a 3-D map (a box's columns, K, column blocks) and one tensor copy brings all
     // of a stage's B boxes (two-SM kernel, 256-wide tiles, N a whole number of boxes)
     int b_3d;
+    // 1 (two-SM kernel): two k-blocks per tensor copy. tmA is a 3-D map (K of a block, rows,
+    // k-blocks) and tmB a 4-D one (a box's columns, K of a block, column blocks, k-blocks);
+    // the copies at an even ring slot fill that slot and the next, the odd slot loads nothing,
+    // slots are released in pairs, and each tile's walk starts on an even slot
+    int kps2;
 };
 
 // K coordinate (in k-blocks) that the load at position kb of the range

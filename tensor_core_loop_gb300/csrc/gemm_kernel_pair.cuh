@@ -55,6 +55,9 @@ struct PairCfg {
     static constexpr int B_BOX_BYTES = BK * 128;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
+    // the ring holds the A slots of all stages first, then their B slots, so that
+    // consecutive slots of each operand are contiguous (one copy may fill two)
+    static constexpr int A_RING_BYTES = STAGES * A_BYTES;
     static constexpr int PAIR_TX = 2 * STAGE_BYTES;         // bytes the leader's full[s] expects
     static constexpr int OUT_ES = (OK == OutKind::BF16) ? 2 : 4;
     static constexpr int EPI_COLS = 128 / OUT_ES;
@@ -79,7 +82,6 @@ struct PairCfg {
     // pair k-block (128 rows × BN columns) keeps its tensor pipe as long as a
     // one-SM k-block of width BN
     static constexpr int REL = (BN <= 128 && STAGES >= 4 && STAGES % 2 == 0) ? 2 : 1;
-    static __device__ __forceinline__ uint32_t rel_slot(uint32_t s) { return REL == 2 ? (s | 1u) : s; }
 
     static_assert(OK != OutKind::S32 || (EPI_COLS_PER_WARP <= 128 && IK == InKind::BF16),
                   "exact integer mode: int32 sums of at most 128 columns per thread in registers");
@@ -328,6 +330,9 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
     const uint32_t full_leader0 = ptx::mapa_shared(full0, 0u);
     const uint32_t acce_leader0 = ptx::mapa_shared(acce0, 0u);
     const AbortNet peer_abort{ptx::smem_u32(const_cast<uint32_t*>(abort_flag)), C::CL};
+    const bool kps2 = p.kps2 != 0;
+    const bool rel2 = C::REL == 2 || kps2;   // ring slots released in pairs (commits on odd slots)
+    auto rel_slot = [rel2](uint32_t s) { return rel2 ? (s | 1u) : s; };
     const int cluster = blockIdx.x / C::CL;
     const int clusters = gridDim.x / C::CL;
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
@@ -352,36 +357,58 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
+                if (kps2 && (s & 1u)) {   // loaded with the slot before it
+                    if (lane == 0) *progress = it + 1;
+                    continue;
+                }
                 const int kc = load_kblock(p, u, kb, U.kb_lo, U.kb_hi);
-                if (!wait_warp_pair(empty0 + 8 * C::rel_slot(s), ph ^ 1u, abort_flag, peer_abort, p.timeout_ns,
+                if (!wait_warp_pair(empty0 + 8 * rel_slot(s), ph ^ 1u, abort_flag, peer_abort, p.timeout_ns,
                                     p.status, DEV_TIMEOUT_PRODUCER)) {
                     ok = false;
                     break;
                 }
                 if (tracing && lane == 0) {
                     const uint64_t now = ptx::clock64();
-                    if (it >= STAGES && it - STAGES < (uint32_t)p.trace_cap) p.trace[4 * (it - STAGES) + 3] = now;
-                    if (it < (uint32_t)p.trace_cap) p.trace[4 * it + 0] = now;
-                }
-                if (leader) ptx::mbar_arrive_expect_tx_elected(full0 + 8 * s, C::PAIR_TX);
-                const uint32_t sa = ptx::smem_u32(stage_base + s * C::STAGE_BYTES);
-                const uint32_t fb = full_leader0 + 8 * s;
-                // test hook: CTA 0 announces the stage's bytes but never loads its share
-                if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) {
-                    if (lane == 0) *progress = it + 1;
-                    continue;
-                }
-                ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kc * C::BK, row);
-                if (p.b_3d) {   // this CTA's B_BOXES boxes in one copy (boxes B_BOX_BYTES apart, as below)
-                    ptx::tma_load_3d_pair_elected(sa + C::A_BYTES, &tmB, fb, 0, kc * C::BK, col / C::B_BOX_N);
-                } else {
-#pragma unroll
-                    for (int b = 0; b < C::B_BOXES; ++b) {
-                        const uint32_t dst = sa + C::A_BYTES + b * C::B_BOX_BYTES;
-                        ptx::tma_load_2d_pair_elected(dst, &tmB, fb, col + b * C::B_BOX_N, kc * C::BK);
+                    for (uint32_t j = it; j < it + (kps2 ? 2u : 1u); ++j) {   // (a pair of slots: both)
+                        if (j >= STAGES && j - STAGES < (uint32_t)p.trace_cap) p.trace[4 * (j - STAGES) + 3] = now;
+                        if (j < (uint32_t)p.trace_cap) p.trace[4 * j + 0] = now;
                     }
                 }
-                if (lane == 0) *progress = it + 1;
+                // a pair of slots: the copies bring this k-block and the next one of the walk (if
+                // the tile has one; else the block after it in K, or zeros past the end of K),
+                // the lower K coordinate first
+                const bool two = kps2 && kb + 1 < U.kb_hi;
+                if (leader) ptx::mbar_arrive_expect_tx_elected(full0 + 8 * s, kps2 ? 2 * C::PAIR_TX : C::PAIR_TX);
+                const uint32_t sa = ptx::smem_u32(stage_base + s * C::A_BYTES);
+                const uint32_t sb = ptx::smem_u32(stage_base + C::A_RING_BYTES + s * C::B_BYTES);
+                const uint32_t fb = full_leader0 + 8 * s;
+                const uint32_t done = it + (two ? 2u : 1u);
+                // test hook: CTA 0 announces the stage's bytes but never loads its share
+                if (blockIdx.x == 0 && (kps2 ? (it | 1u) == (static_cast<uint32_t>(p.debug_skip_kb) | 1u)
+                                             : static_cast<int>(it) == p.debug_skip_kb)) {
+                    if (lane == 0) *progress = done;
+                    continue;
+                }
+                if (kps2) {
+                    const int k0 = two ? min(kc, load_kblock(p, u, kb + 1, U.kb_lo, U.kb_hi)) : kc;
+                    ptx::tma_load_3d_pair_elected(sa, &tmA, fb, 0, row, k0);
+                    ptx::tma_load_4d_pair_elected(sb, &tmB, fb, 0, 0, col / C::B_BOX_N, k0);
+                } else {
+                    ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kc * C::BK, row);
+                    if (p.b_3d) {   // this CTA's B_BOXES boxes in one copy (boxes B_BOX_BYTES apart, as below)
+                        ptx::tma_load_3d_pair_elected(sb, &tmB, fb, 0, kc * C::BK, col / C::B_BOX_N);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < C::B_BOXES; ++b)
+                            ptx::tma_load_2d_pair_elected(sb + b * C::B_BOX_BYTES, &tmB, fb, col + b * C::B_BOX_N,
+                                                          kc * C::BK);
+                    }
+                }
+                if (lane == 0) *progress = done;
+            }
+            if (ok && kps2 && (it & 1u)) {   // the next tile starts on an even slot
+                ++it;
+                if (lane == 0) *progress = it;
             }
         }
         if (!ok && lane == 0) spin_ns(200000);   // copies issued before the abort land within microseconds
@@ -390,7 +417,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             // (the same empty-barrier phases a reuse would have waited for; bounded)
             const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
             for (uint32_t j = first; j < it && j < (uint32_t)p.trace_cap && !*abort_flag; ++j) {
-                wait_drain(empty0 + 8 * C::rel_slot(j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
+                wait_drain(empty0 + 8 * rel_slot(j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
                 p.trace[4 * j + 3] = ptx::clock64();
             }
         }
@@ -406,17 +433,19 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             const uint64_t adesc0 = ptx::sdesc_sw128(stage0, 16, 1024);
             // B N-major: boxes B_BOX_BYTES apart (leading offset), core groups of K-rows
             // B_SBO apart, a k-slice steps UMMA_K rows of 128 B
-            const uint64_t bdesc0 = ptx::sdesc(stage0 + C::A_BYTES, C::B_BOX_BYTES, InTraits<IK>::B_SBO,
+            const uint64_t bdesc0 = ptx::sdesc(stage0 + C::A_RING_BYTES, C::B_BOX_BYTES, InTraits<IK>::B_SBO,
                                                InTraits<IK>::B_LAYOUT);
             constexpr uint64_t A_STEP = C::UMMA_K * C::ES / 16;
             constexpr uint64_t B_STEP = C::UMMA_K * 128 / 16;
-            constexpr uint64_t S_STEP = C::STAGE_BYTES / 16;
+            constexpr uint64_t SA_STEP = C::A_BYTES / 16;
+            constexpr uint64_t SB_STEP = C::B_BYTES / 16;
             static_assert(C::KSUB == 4, "four MMAs per k-block");
             uint32_t it = 0, unit = 0, s = 0, ph = 0;
             bool ok = true;
             const int units = pair_units(p, cluster, clusters);
             for (int u = 0; ok && u < units; ++u) {
                 const PairUnit U = pair_unit(p, cluster, clusters, u);
+                const bool desc = p.k_serpentine && (u & 1);   // this tile's loads walk K downwards
                 // accumulation units of kb_per_unit k-blocks (exact-integer mode: 1024 K
                 // values, drained into int32 sums; otherwise the whole range)
                 for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
@@ -431,15 +460,20 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * C::ACC_STRIDE;
                     for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                        if (!wait_warp_pair(full0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
-                                            DEV_TIMEOUT_MMA_FULL)) {
+                        // (a pair of slots completes on the first one's barrier)
+                        if (!wait_warp_pair(full0 + 8 * (kps2 ? (s & ~1u) : s), ph, abort_flag, peer_abort,
+                                            p.timeout_ns, p.status, DEV_TIMEOUT_MMA_FULL)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
                         if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 1] = ptx::clock64();
-                        const uint64_t ad = adesc0 + s * S_STEP;
-                        const uint64_t bd = bdesc0 + s * S_STEP;
+                        // a pair of slots holds the lower K block first: a tile walking K
+                        // downwards takes the second slot first (the summation order of one
+                        // k-block per copy)
+                        const uint32_t ds = (kps2 && desc && ((s & 1u) || kb + 1 < U.kb_hi)) ? (s ^ 1u) : s;
+                        const uint64_t ad = adesc0 + ds * SA_STEP;
+                        const uint64_t bd = bdesc0 + ds * SB_STEP;
                         if constexpr (IK == InKind::TF32)
                             ptx::mma_tf32_pair_x4_elected(d_tmem, ad, bd, ad + A_STEP, bd + B_STEP, ad + 2 * A_STEP,
                                                           bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
@@ -449,7 +483,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                                                          bd + 2 * B_STEP, ad + 3 * A_STEP, bd + 3 * B_STEP, C::IDESC,
                                                          kb > kb0 ? 1u : 0u);
                         // stage s (with s - 1, released in pairs) free in both CTAs once these MMAs are done
-                        if (C::REL == 1 || (s & 1u)) ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
+                        if (!rel2 || (s & 1u)) ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
                         if (tracing && lane == 0 && it < (uint32_t)p.trace_cap) p.trace[4 * it + 2] = ptx::clock64();
                         const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
                         s = wrap ? 0u : s + 1;
@@ -457,6 +491,15 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                     }
                     if (!ok) break;
                     ptx::mma_commit_pair_multicast_elected(accf0 + 8 * buf, C::ALL);
+                }
+                if (ok && kps2 && (s & 1u)) {
+                    // the tile ended on the first slot of a pair: release the pair, skip the
+                    // second slot (the next tile starts on an even slot)
+                    ptx::mma_commit_pair_multicast_elected(empty0 + 8 * s, C::ALL);
+                    const uint32_t wrap = (s + 1 == static_cast<uint32_t>(STAGES)) ? 1u : 0u;
+                    s = wrap ? 0u : s + 1;
+                    ph ^= wrap;
+                    ++it;
                 }
             }
             if (ok && tracing && C::REL == 2 && it > 0) {
@@ -514,7 +557,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
         const int units = pair_units(p, cluster, clusters);
         for (int u = 0; ok && u < units; ++u) {
             const PairUnit U = pair_unit(p, cluster, clusters, u);
-            it_next += static_cast<uint32_t>(U.kb_hi - U.kb_lo);
+            it_next += static_cast<uint32_t>(kps2 ? (U.kb_hi - U.kb_lo + 1) & ~1 : U.kb_hi - U.kb_lo);
             int mb, nb;
             tile_coords(U.tile, p, mb, nb);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;

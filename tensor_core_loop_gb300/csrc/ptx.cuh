@@ -439,6 +439,18 @@ __device__ __forceinline__ void tma_load_3d_pair_elected(uint32_t dst, const CUt
         : "memory");
 }
 
+// 4-D form of the same (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d_pair_elected(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                         int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 // Per-warp register budget changes (all warps of a warpgroup execute the same
 // one): dec releases registers down to N per thread, inc waits until N per
 // thread can be granted from what the block's warps released.

@@ -290,6 +290,35 @@ def test_planner_stream_k(L):
     assert p["sk_balanced"] == 1 and p["workspace_bytes"] == 76 * 256 * 256 * 4
 
 
+def test_planner_kblocks_per_copy(L):
+    # two-SM 256-wide tiles bring two k-blocks per tensor copy of each operand where K is whole
+    # k-blocks, N whole B boxes (64 bf16 / 32 TF32 columns) and the ring depth even
+    cfg = tcl.Config(max_ctas=152)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)
+    assert (p["cta_pair"], p["bn"], p["stages"], p["kblocks_per_stage"]) == (2, 256, 6, 2)
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 4096, cfg)["kblocks_per_stage"] == 2
+    assert tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, cfg)["kblocks_per_stage"] == 2
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4064, 4096, cfg)["kblocks_per_stage"] == 2   # 32-column boxes
+    for M, N, K in ((4096, 4064, 4096), (4096, 4096, 4000)):   # N or K not whole blocks
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K, cfg)
+        assert p["cta_pair"] == 2 and p["kblocks_per_stage"] == 1
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, M, N, K, tcl.Config(max_ctas=152, kblocks_per_stage=2))
+    off = tcl.Config(max_ctas=152, kblocks_per_stage=1)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, off)["kblocks_per_stage"] == 1
+    for bad in (tcl.Config(max_ctas=152, cta_pair=2, stages=5, kblocks_per_stage=2),   # odd ring
+                tcl.Config(max_ctas=152, cta_pair=2, bn=224, kblocks_per_stage=2),
+                tcl.Config(max_ctas=152, cta_pair=1, kblocks_per_stage=2),
+                tcl.Config(max_ctas=152, kblocks_per_stage=3)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, bad)
+    with pytest.raises(tcl.TclError):   # the kernel that widens int8 itself has its own ring
+        tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, s8_path=2, kblocks_per_stage=2))
+    # one SM per tile: 64×64 tiles report their two k-blocks per 32 KB stage
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)["kblocks_per_stage"] == 2
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 520, cfg)["kblocks_per_stage"] == 1
+
+
 def test_planner_producer_kinds(L):
     for prod in (tcl.PRODUCER_SYNC, tcl.PRODUCER_CPASYNC):
         p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, producer=prod))

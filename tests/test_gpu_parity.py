@@ -481,6 +481,46 @@ def test_alternating_k_order_exact_and_tf32(oracle_mod):
     assert_within("tf32", got, ref, S, "tf32 alternating K order")
 
 
+@pytest.mark.parametrize("kind,M,N,K,cfg", [
+    ("bf16", 512, 512, 1024, dict()),                          # even k-block counts
+    ("bf16", 700, 768, 1088, dict(max_ctas=4)),                 # 17 k-blocks: each tile ends on half a pair
+    ("bf16", 1024, 1280, 1088, dict(max_ctas=4, k_order=2)),    # descending K walks of odd length
+    ("bf16", 768, 768, 2048, dict(max_ctas=8, stream_k=3)),     # stream-K pieces of 10, 11, 11 k-blocks
+    ("bf16", 768, 768, 2048, dict(max_ctas=8, stream_k=5)),     # balanced: ranges across tile boundaries
+    ("bf16_out", 768, 768, 1984, dict(max_ctas=8, stream_k=3)),  # bf16 C through the workspace, 31 k-blocks
+    ("tf32", 768, 1024, 1504, dict(max_ctas=4, k_order=2)),     # 47 k-blocks of 32
+    ("s8", 1024, 1024, 2112, dict(max_ctas=4, k_order=2)),      # 33 k-blocks in accumulation units of 16
+])
+def test_two_kblocks_per_copy(oracle_mod, kind, M, N, K, cfg):
+    """Two-SM 256-wide tiles with one tensor copy of each operand per two k-blocks: within the
+    oracle's bound, and bit-identical to one k-block per copy (only the loads change; the MMAs
+    run in the same order, also where a tile walks K downwards or ends on half a pair)."""
+    two = tcl.Config(cta_pair=2, bn=256, **cfg)
+    one = tcl.Config(cta_pair=2, bn=256, kblocks_per_stage=1, **cfg)
+    in_kind = {"bf16": tcl.IN_BF16, "bf16_out": tcl.IN_BF16, "tf32": tcl.IN_TF32, "s8": tcl.IN_S8}[kind]
+    out = {"bf16": tcl.OUT_F32, "bf16_out": tcl.OUT_BF16, "tf32": tcl.OUT_F32, "s8": 0}[kind]
+    assert tcl.plan(in_kind, out, M, N, K, two)["kblocks_per_stage"] == 2
+    assert tcl.plan(in_kind, out, M, N, K, one)["kblocks_per_stage"] == 1
+    if kind in ("bf16", "bf16_out"):
+        od = torch.float32 if kind == "bf16" else torch.bfloat16
+        bf16_case(oracle_mod, M, N, K, seed=K + N, out_dtype=od, cfg=two)
+        a, b = inputs.bf16_pair(M, N, K, seed=K + N)
+    elif kind == "tf32":
+        a, b = inputs.tf32_pair(M, N, K, seed=K + N)
+        got = run(a.to(DEV), b.to(DEV), cfg=two).double().numpy()
+        ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+        assert_within("tf32", got, ref, S, f"tf32 two k-blocks per copy {M}x{N}x{K}")
+    else:
+        a, b = inputs.s8_pair(M, N, K, seed=K + N)
+        assert_exact(run(a.to(DEV), b.to(DEV), cfg=two).numpy(), oracle_mod.gemm_s8(a.numpy(), b.numpy()),
+                     "s8 two k-blocks per copy")
+    a, b = a.to(DEV), b.to(DEV)
+    od = {"bf16": None, "bf16_out": torch.bfloat16, "tf32": None, "s8": None}[kind]
+    x = run(a, b, out_dtype=od, cfg=two, canary=False)
+    y = run(a, b, out_dtype=od, cfg=one, canary=False)
+    assert torch.equal(x, y)
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""

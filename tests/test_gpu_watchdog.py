@@ -44,13 +44,15 @@ def test_bounded_wait_runs_out_and_context_survives():
     assert tcl.last_device_error() == (0, 0)
 
 
-def test_two_sm_kernel_bounded_wait_runs_out():
-    # CTA 0 of the first pair announces a stage's bytes but never loads its share:
-    # the leader's MMA wait runs out; both CTAs of the pair abort and return
+@pytest.mark.parametrize("kps,skip", [(1, 2), (2, 2), (2, 3)])
+def test_two_sm_kernel_bounded_wait_runs_out(kps, skip):
+    # CTA 0 of the first pair announces a stage's bytes but never loads its share (with two
+    # k-blocks per copy: the pair of ring slots holding that k-block): the leader's MMA wait
+    # runs out; both CTAs of the pair abort and return
     a, b = inputs.bf16_pair(1024, 1024, 1024, seed=5)
     a, b = a.to(DEV), b.to(DEV)
     c = torch.zeros((1024, 1024), dtype=torch.float32, device=DEV)
-    cfg = tcl.Config(cta_pair=2, timeout_ns=50_000_000, debug_skip_kblock=2)
+    cfg = tcl.Config(cta_pair=2, bn=256, kblocks_per_stage=kps, timeout_ns=50_000_000, debug_skip_kblock=skip)
     tcl.gemm_into(a, b, c, cfg=cfg)
     st, code = tcl.last_device_error()
     assert st == 7 and code in (1, 2, 3, 4), (st, code)

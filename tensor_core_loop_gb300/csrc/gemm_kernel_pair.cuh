@@ -56,7 +56,10 @@ struct PairCfg {
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
     // the ring holds the A slots of all stages first, then their B slots, so that
-    // consecutive slots of each operand are contiguous (one copy may fill two)
+    // consecutive slots of each operand are contiguous (one copy may fill two). Measured on
+    // GB300 (CUDA graphs, round robin in one process) this is also faster than keeping each
+    // slot's A and B together, with one k-block per copy as with two: 4096³ 115 against 127
+    // and 94 against 102 µs, 256×224 tiles at 4096²×1024 39.8 against 43.5 µs
     static constexpr int A_RING_BYTES = STAGES * A_BYTES;
     static constexpr int PAIR_TX = 2 * STAGE_BYTES;         // bytes the leader's full[s] expects
     static constexpr int OUT_ES = (OK == OutKind::BF16) ? 2 : 4;

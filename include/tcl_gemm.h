@@ -213,6 +213,11 @@ typedef struct {
                                       TCL_ERR_CONFIG). Two halve the copies per k-block, which
                                       pace the stages on GB300 more than their bytes do; the
                                       result is the same either way (same summation order) */
+    int b_copy;                    /* TMA producer, one k-block per copy: 0 automatic (a CTA's B
+                                      boxes of a k-block in one 3-D tensor copy when N is a
+                                      multiple of 64 bf16 / 32 TF32 columns and the tile has
+                                      several boxes: 128- and 256-wide one-SM tiles, 256-wide
+                                      two-SM tiles); 1 one copy per box. Same result */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)

@@ -72,6 +72,7 @@ class Config(ctypes.Structure):
         ("cluster_k", ctypes.c_int),
         ("tile_m", ctypes.c_int),
         ("kblocks_per_stage", ctypes.c_int),
+        ("b_copy", ctypes.c_int),
     ]
 
 

@@ -684,7 +684,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     // least 4. (The same in the one-SM kernel, with its B boxes in one 3-D copy or not, was
     // measured no faster on GB300 at 128×256 and 128×128 tiles.)
     const int want_kps = cfg ? cfg->kblocks_per_stage : 0;
-    if (want_kps < 0 || want_kps > 2) return TCL_ERR_CONFIG;
+    if (want_kps < 0 || want_kps > 2 || (cfg && (cfg->b_copy < 0 || cfg->b_copy > 1))) return TCL_ERR_CONFIG;
     const bool kps2_ok = pair && !pl->s8_in_kernel && bn == 256 && prod == PROD_TMA && K % bk == 0 &&
                          N % (128 / in_bytes(ik)) == 0 && pl->stages >= 4 && pl->stages % 2 == 0;
     if (want_kps == 2 && !kps2_ok) return TCL_ERR_CONFIG;
@@ -858,10 +858,14 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     a.pdl = !(cfg && cfg->serial_launch);
     a.grid = pl.grid;
     a.stream = stream;
-    // Two-SM 256-wide tiles take all of a CTA's B boxes in one tensor copy (a 3-D map) when N
-    // is a whole number of boxes, so that no box reads past a row's end: a stage's copies,
-    // not its bytes, pace the stages (measured on GB300)
-    const bool b3d = pl.pair && pl.kps == 1 && !pl.s8_in_kernel && pl.bn == 256 && N % (128 / ies) == 0;
+    // A CTA's B boxes of a k-block (the whole tile's, or a two-SM CTA's half) come in one
+    // tensor copy (a 3-D map) when N is a whole number of boxes, so that no box reads past a
+    // row's end: a stage's copies, not its bytes, pace the stages (measured on GB300)
+    // (a two-SM CTA's half starts at a multiple of 128 columns only in 256-wide tiles; the
+    // third coordinate of the map counts whole boxes)
+    const int b_boxes = (pl.pair ? pl.bn / 2 : pl.bn) / (128 / ies);   // per CTA and k-block
+    const bool b3d = pl.kps == 1 && !pl.s8_in_kernel && !pl.m64 && !pl.csk && pl.prod == PROD_TMA && b_boxes > 1 &&
+                     (!pl.pair || pl.bn == 256) && N % (128 / ies) == 0 && !(cfg && cfg->b_copy == 1);
     if (pl.s8_in_kernel) {
         // raw int8 operands, unswizzled: A in boxes of 64 K × 128 rows, B of 128 columns × 64 K
         if ((st = tensor_map(dev, A, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, lda, 64, kBM, &a.tmA,
@@ -872,14 +876,14 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     } else {
         const CUtensorMapSwizzle bswz =
             ik == InKind::TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-        const uint32_t b_boxes = pl.bn / 2 / (128 / ies);   // B boxes a two-SM CTA loads per k-block
         if (pl.kps == 2) {
             // A as (K of a block, rows, k-blocks) in boxes of 128 rows × 2 blocks; B as (a box's
             // columns, K of a block, column blocks, k-blocks) in boxes of a CTA's half × 2 blocks
             const uint32_t bw = 128 / ies;
             if ((st = tensor_map_3d(dev, A, in_t, bk, M, K / bk, lda * ies, 128, bk, kBM, 2, &a.tmA)) ||
                 (st = tensor_map_nd(dev, B, in_t, bw, bk, N / bw, K / bk, ldb * ies, 128,
-                                    static_cast<uint64_t>(bk) * ldb * ies, bw, bk, b_boxes, 2, &a.tmB, bswz)))
+                                    static_cast<uint64_t>(bk) * ldb * ies, bw, bk, static_cast<uint32_t>(b_boxes), 2,
+                                    &a.tmB, bswz)))
                 return st;
         } else if (pl.m64 == 2) {
             // A as (64 K, M rows, K/64 k-blocks): one box brings two k-blocks' swizzle tiles;
@@ -893,9 +897,10 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
             // 4-byte elements are swizzled in 32-byte units (bswz), the form the tensor core
             // reads an N-major 32-bit operand in
             if (b3d) {
-                // (columns of a box, K, column blocks): one box holds a CTA's whole half of B
+                // (columns of a box, K, column blocks): one box holds all of a CTA's B boxes
                 const uint32_t bw = 128 / ies;
-                if ((st = tensor_map_3d(dev, B, in_t, bw, K, N / bw, ldb * ies, 128, bw, bk, b_boxes, &a.tmB, bswz)))
+                if ((st = tensor_map_3d(dev, B, in_t, bw, K, N / bw, ldb * ies, 128, bw, bk,
+                                        static_cast<uint32_t>(b_boxes), &a.tmB, bswz)))
                     return st;
             } else if ((st = tensor_map(dev, B, in_t, N, K, ldb * ies, 128 / ies, bk, &a.tmB, bswz))) {
                 return st;

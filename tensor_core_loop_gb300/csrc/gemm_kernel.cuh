@@ -131,7 +131,7 @@ struct GemmParams {
     // are the ones still in L2
     int k_serpentine;
     // 1: tmB is a 3-D map (a box's columns, K, column blocks) and one tensor copy brings all
-    // of a stage's B boxes (two-SM kernel, 256-wide tiles, N a whole number of boxes)
+    // of a stage's B boxes (TMA producer, N a whole number of boxes)
     int b_3d;
     // 1 (two-SM kernel): two k-blocks per tensor copy. tmA is a 3-D map (K of a block, rows,
     // k-blocks) and tmB a 4-D one (a box's columns, K of a block, column blocks, k-blocks);
@@ -726,10 +726,14 @@ __global__ void __launch_bounds__(KCfg<IK, OK, BN, STAGES, PROD>::THREADS, 1)
                 if (blockIdx.x == 0 && static_cast<int>(it) == p.debug_skip_kb) continue;
                 ptx::mbar_arrive_expect_tx_elected(full, C::STAGE_BYTES);
                 ptx::tma_load_2d_elected(sa, &tmA, full, kc * C::BK, mb * C::BM);
+                if (p.b_3d) {   // all B_BOXES boxes in one copy (B_BOX_BYTES apart, as below)
+                    ptx::tma_load_3d_elected(sa + C::A_BYTES, &tmB, full, 0, kc * C::BK, nb * BN / C::B_BOX_N);
+                } else {
 #pragma unroll
-                for (int b = 0; b < C::B_BOXES; ++b) {
-                    ptx::tma_load_2d_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
-                                             nb * BN + b * C::B_BOX_N, kc * C::BK);
+                    for (int b = 0; b < C::B_BOXES; ++b) {
+                        ptx::tma_load_2d_elected(sa + C::A_BYTES + b * C::B_BOX_BYTES, &tmB, full,
+                                                 nb * BN + b * C::B_BOX_N, kc * C::BK);
+                    }
                 }
             }
         }

@@ -314,6 +314,9 @@ def test_planner_kblocks_per_copy(L):
             tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, bad)
     with pytest.raises(tcl.TclError):   # the kernel that widens int8 itself has its own ring
         tcl.plan(tcl.IN_S8, 0, 4096, 4096, 4096, tcl.Config(max_ctas=152, s8_path=2, kblocks_per_stage=2))
+    for bad in (-1, 2):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, b_copy=bad))
     # one SM per tile: 64×64 tiles report their two k-blocks per 32 KB stage
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)["kblocks_per_stage"] == 2
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 520, cfg)["kblocks_per_stage"] == 1

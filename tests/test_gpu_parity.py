@@ -521,6 +521,41 @@ def test_two_kblocks_per_copy(oracle_mod, kind, M, N, K, cfg):
     assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("kind,M,N,K,cfg", [
+    ("bf16", 700, 768, 1000, dict(cta_pair=1, bn=256)),               # 4 boxes in one copy; K tail, ragged M
+    ("bf16", 640, 1024, 1216, dict(cta_pair=1, bn=128, split_k=2)),   # 2 boxes; split-K ranges
+    ("bf16_out", 520, 512, 960, dict(cta_pair=1, bn=256)),
+    ("tf32", 384, 512, 1000, dict(cta_pair=1, bn=256)),               # 8 boxes of 32 columns in one copy
+    ("tf32", 512, 768, 1504, dict(cta_pair=1, bn=128, max_ctas=4)),
+    ("s8", 640, 512, 1000, dict(cta_pair=1, bn=128, max_ctas=4)),
+    ("bf16", 768, 768, 1000, dict(cta_pair=2, bn=256, max_ctas=8)),   # two-SM, K not whole k-blocks
+])
+def test_b_boxes_in_one_copy(oracle_mod, kind, M, N, K, cfg):
+    """A CTA's B boxes of a k-block in one 3-D tensor copy (the default where N is whole boxes)
+    against one copy per box: within the oracle's bound and bit-identical."""
+    auto, per_box = tcl.Config(**cfg), tcl.Config(b_copy=1, **cfg)
+    in_kind = {"bf16": tcl.IN_BF16, "bf16_out": tcl.IN_BF16, "tf32": tcl.IN_TF32, "s8": tcl.IN_S8}[kind]
+    out = {"bf16": tcl.OUT_F32, "bf16_out": tcl.OUT_BF16, "tf32": tcl.OUT_F32, "s8": 0}[kind]
+    assert tcl.plan(in_kind, out, M, N, K, auto)["kblocks_per_stage"] == 1
+    if kind in ("bf16", "bf16_out"):
+        od = torch.float32 if kind == "bf16" else torch.bfloat16
+        bf16_case(oracle_mod, M, N, K, seed=K + N + 1, out_dtype=od, cfg=auto)
+        a, b = inputs.bf16_pair(M, N, K, seed=K + N + 1)
+    elif kind == "tf32":
+        a, b = inputs.tf32_pair(M, N, K, seed=K + N + 1)
+        got = run(a.to(DEV), b.to(DEV), cfg=auto).double().numpy()
+        ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy())
+        assert_within("tf32", got, ref, S, f"tf32 B boxes in one copy {M}x{N}x{K}")
+    else:
+        a, b = inputs.s8_pair(M, N, K, seed=K + N + 1)
+        assert_exact(run(a.to(DEV), b.to(DEV), cfg=auto).numpy(), oracle_mod.gemm_s8(a.numpy(), b.numpy()),
+                     "s8 B boxes in one copy")
+    a, b = a.to(DEV), b.to(DEV)
+    od = torch.bfloat16 if kind == "bf16_out" else None
+    assert torch.equal(run(a, b, out_dtype=od, cfg=auto, canary=False),
+                       run(a, b, out_dtype=od, cfg=per_box, canary=False))
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""

@@ -352,11 +352,19 @@ constexpr int kMinKbToSplit = 24;    // k-blocks a tile needs before splitting i
 constexpr long long kMinKBytesForRowRaster = 16384;   // two-SM kernel: K bytes per operand row from which
                                                       // group 1 and alternating K order are the default
 
-// Two-SM kernel: SM cycles per 64-deep k-block of a pair tile, measured on
-// GB300 with the in-kernel timeline (the tensor pipe runs 256-wide pair tiles
-// at its full rate, 224-wide ones ~9.6 % below it).
-constexpr long long kPairKbCycles256 = 512;
-constexpr long long kPairKbCycles224 = 491;
+// Two-SM kernel: model cycles per k-block of a pair tile (64 bf16 or 32 TF32 deep) and
+// the fixed part of a launch. The tensor pipe takes 512 cycles per 256-wide k-block
+// and runs 224-wide tiles ~9.6 % below its rate (in-kernel timeline); the constants
+// below are instead fitted to the planner's choices: CUDA graphs of back-to-back
+// calls on GB300 at 42 shapes of bf16, TF32 and int8 between 768 and 8192 on a side
+// and K from 512 to 8192, each timed on two-SM 224- and 256-wide and one-SM tiles in
+// one process, round robin. With two k-blocks per tensor copy the 256-wide tiles pull
+// ahead as K grows (a lower cost per k-block, a higher fixed part), and int8, whose
+// one-SM tiles are 128 wide with an integer drain, keeps its own fixed part. Over
+// those shapes the picks lose 0.5 % of time against the best choice (the earlier
+// constants: 4 %; worst case now 8 % at 8192×2048×1024 with a bf16 C).
+constexpr long long kPairKbCycles256 = 420;
+constexpr long long kPairKbCycles224 = 520;
 // Stream-K tail: at most this many pieces per split tile (each waits for the
 // previous one before adding its result) and at least this many k-blocks each.
 constexpr int kMaxSkPieces = 4;
@@ -397,13 +405,13 @@ int stream_k_split(long long tiles, int pairs, int num_kb, int want, int* sk_til
 // 128×128 and 128×256 tiles, and the fixed cycles of a launch (first loads,
 // last epilogue), fitted on GB300 (CUDA graphs of back-to-back calls at
 // 1024×4096 and 2048² with K = 1024 and 4096: 128 wide ~0.23 µs per k-block
-// and wave, 256 wide ~0.335, the two-SM tiles ~0.27 (256 wide) and ~0.26 (224
-// wide), which kPairKbCycles* match; the launch's fixed part ~5, ~6.3 and ~9 µs).
+// and wave, 256 wide ~0.335; the launch's fixed part ~5 and ~6.3 µs).
 constexpr long long kOneKbCycles128 = 440;
 constexpr long long kOneKbCycles256 = 640;
 constexpr long long kOneFixedCycles128 = 9500;
 constexpr long long kOneFixedCycles256 = 12000;
-constexpr long long kPairFixedCycles = 17000;
+constexpr long long kPairFixedCycles = 30500;
+constexpr long long kPairFixedCyclesS32 = 13000;
 
 // Busiest pair's k-block cycles for pair tiles of width w: ceil(tiles / pairs)
 // whole tiles, or the full waves plus the largest stream-K piece.
@@ -536,7 +544,8 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
             int skt = 0, skp = 1;
             if (stream_k_split(t, pe, kblocks, want_sk, &skt, &skp)) skt = 0, skp = 1;
             const long long c =
-                pair_cost(t, pe, kblocks, w == 256 ? kPairKbCycles256 : kPairKbCycles224, skt, skp) + kPairFixedCycles;
+                pair_cost(t, pe, kblocks, w == 256 ? kPairKbCycles256 : kPairKbCycles224, skt, skp) +
+                (ok == OutKind::S32 ? kPairFixedCyclesS32 : kPairFixedCycles);
             if (best_pair < 0 || c < best_pair) best_pair = c;
         }
         pair = (kblocks >= kMinKbForPair &&

@@ -107,10 +107,10 @@ def test_mma_peak_rejects(L):
 def test_plan_without_device(L):
     cfg = tcl.Config(max_ctas=152)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=1))
-    # enough 256-row tiles for every pair of SMs: two SMs per tile; without a stream-K
-    # tail, 224 columns give 16 × 19 = 304 tiles = exactly 4 per pair of SMs (256 would
-    # leave a partial wave)
-    assert p["cta_pair"] == 2 and p["bn"] == 224 and p["num_tiles"] == 16 * 19 and p["grid"] == 152
+    # enough 256-row tiles for every pair of SMs: two SMs per tile; even without a stream-K
+    # tail 256 columns (16 × 16 tiles, a partial last wave) beat the 224 columns that give
+    # exactly 4 tiles per pair (two k-blocks per copy: 89.0 against 98.7 µs on GB300)
+    assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16 and p["grid"] == 152
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 4096, cfg)
     assert p["cta_pair"] == 2 and p["bn"] == 256 and p["num_tiles"] == 16 * 16
     assert p["smem_bytes"] <= 232448
@@ -176,17 +176,19 @@ def test_plan_without_device(L):
     # split-K shapes keep 128-wide tiles
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 2048, cfg)["bn"] == 128
     # mid-size outputs by the cost model (waves × k-blocks × per-k-block cycles + fixed
-    # cycles per launch): the measured fastest shape at each of these
-    for (m, n, k), want in {(1024, 4096, 4096): (2, 224), (2048, 2048, 4096): (2, 256),
+    # cycles per launch): the measured fastest shape at each of these (GB300, CUDA graphs:
+    # 1024×4096×4096 28.98 µs on one SM against 30.03 on 224-wide pairs, 2048²×4096 27.63
+    # against 28.21 on 256-wide pairs)
+    for (m, n, k), want in {(1024, 4096, 4096): (1, 256), (2048, 2048, 4096): (1, 256),
                             (1024, 4096, 1024): (1, 256), (2048, 2048, 1024): (1, 256),
                             (1536, 3072, 2048): (1, 256), (3072, 3072, 1024): (1, 256),
                             (512, 4096, 4096): (1, 128)}.items():
         p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, m, n, k, cfg)
         assert (p["cta_pair"], p["bn"]) == want, ((m, n, k), p)
-    for in_kind, (m, n, k), want in ((tcl.IN_TF32, (1024, 4096, 4096), (2, 224)),
+    for in_kind, (m, n, k), want in ((tcl.IN_TF32, (1024, 4096, 4096), (2, 256)),   # 48.1 against 57.8 µs
                                      (tcl.IN_TF32, (1024, 4096, 1024), (1, 256)),
                                      (tcl.IN_S8, (1024, 4096, 4096), (2, 256)),
-                                     (tcl.IN_S8, (1024, 4096, 1024), (1, 128))):
+                                     (tcl.IN_S8, (1024, 4096, 1024), (2, 256))):
         p = tcl.plan(in_kind, 0, m, n, k, cfg)
         assert (p["cta_pair"], p["bn"]) == want, ((m, n, k), p)
     # deep two-SM tiles (rows of A of 16 KB and more): a row of tiles at a time, K walked
@@ -254,9 +256,9 @@ def test_planner_stream_k(L):
     # equal pieces on request: 3 full waves + 28 tiles, each cut in two K ranges (224 k-blocks)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=2))
     assert (p["bn"], p["sk_balanced"], p["sk_tiles"], p["sk_pieces"]) == (256, 0, 28, 2)
-    # without stream-K the 224-wide tiles win
+    # without stream-K the 256-wide tiles still win (one copy brings two k-blocks)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, stream_k=1))
-    assert (p["bn"], p["sk_tiles"], p["sk_balanced"]) == (224, 0, 0)
+    assert (p["bn"], p["sk_tiles"], p["sk_balanced"]) == (256, 0, 0)
     # whole waves: nothing to split
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4864, 4096, 4096, cfg)
     assert (p["bn"], p["num_tiles"], p["sk_tiles"], p["sk_balanced"]) == (256, 304, 0, 0)
@@ -266,8 +268,11 @@ def test_planner_stream_k(L):
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 768, 768, 2048, tcl.Config(max_ctas=8, cta_pair=2, stream_k=5))
     assert (p["sk_balanced"], p["sk_pieces"]) == (1, 2) and p["sk_tiles"] == 3   # 5 tiles, ranges of 40
     # short tiles (16 k-blocks): the extra piece's epilogue costs more than the tail saves
-    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1024, cfg)
-    assert (p["bn"], p["sk_tiles"], p["sk_balanced"]) == (224, 0, 0)
+    # (automatically this shape runs on one SM per tile: 32.8 µs against 32.9 on 224-wide
+    # and 33.6 on 256-wide pairs)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1024, cfg)["cta_pair"] == 1
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1024, tcl.Config(max_ctas=152, cta_pair=2))
+    assert (p["bn"], p["sk_tiles"], p["sk_balanced"]) == (256, 0, 0)
     for k in (2048, 8192):
         assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, cfg)["sk_tiles"] == 28
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 1024, cfg)["sk_tiles"] == 0

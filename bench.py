@@ -548,6 +548,22 @@ COMPARE_GROUPS = {
                  ("one SM, 256 wide, group 32", dict(cta_pair=1, bn=256, group_m=32)),
                  ("two SMs, 256 wide", dict(cta_pair=2, bn=256, stream_k=1)),
                  ("two SMs, 224 wide", dict(cta_pair=2, bn=224, stream_k=1))]),
+    # the shapes the two-SM cycle constants were fitted to (the planner's pair or one-SM pick)
+    "pair_fit": ([("bf16", 4096, 4096, k) for k in (768, 1024, 1536, 2048)] +
+                 [("bf16", 3072, 3072, 1024), ("bf16", 3072, 3072, 2048), ("bf16", 3072, 3072, 4096),
+                  ("bf16", 2048, 2048, 4096), ("bf16", 2048, 2048, 8192), ("bf16", 6144, 6144, 2048),
+                  ("bf16", 1024, 1024, 8192), ("tf32", 4096, 4096, 512), ("tf32", 4096, 4096, 1024),
+                  ("tf32", 2048, 2048, 2048), ("tf32", 2048, 2048, 4096), ("tf32", 3072, 3072, 2048),
+                  ("s8", 4096, 4096, 1024)],
+                 [("automatic", dict()), ("one SM", dict(cta_pair=1)), ("two SMs, 256 wide", dict(cta_pair=2, bn=256)),
+                  ("two SMs, 224 wide", dict(cta_pair=2, bn=224))]),
+    # tensor copies per k-block: two k-blocks per copy (two-SM 256-wide tiles), a CTA's B boxes
+    # in one copy, or one copy per box and k-block
+    "copies": ([("bf16", 4096, 4096, 4096), ("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096),
+                ("s8", 4096, 4096, 4096), ("bf16", 4096, 4096, 512), ("bf16", 8192, 8192, 512),
+                ("tf32", 4096, 4096, 512), ("tf32", 2048, 2048, 2048)],
+               [("automatic", dict()), ("one k-block per copy", dict(kblocks_per_stage=1)),
+                ("one copy per B box", dict(kblocks_per_stage=1, b_copy=1))]),
 }
 
 # --variant-launches: one call of each alternative (after an L2 flush) for an ncu
@@ -584,9 +600,15 @@ def run_compare(args):
     for kind, m, n, k in shapes:
         sets = _compare_operands(kind, m, n, k, dev, torch, inputs, 2 * L2_BYTES if kind != "s8" else L2_BYTES)
         launches = max(len(sets), 20)
+        in_kind = {"bf16": tcl.IN_BF16, "bf16->bf16": tcl.IN_BF16, "tf32": tcl.IN_TF32, "s8": tcl.IN_S8}[kind]
+        out = tcl.OUT_BF16 if kind == "bf16->bf16" else tcl.OUT_F32
         graphs = []
         for name, kw in settings:
             cfg = tcl.Config(**kw)
+            try:   # a setting this shape or type does not allow (e.g. 224-wide int8 tiles) is skipped
+                tcl.plan(in_kind, out, m, n, k, cfg)
+            except tcl.TclError:
+                continue
             fn = (lambda a, b, c, cfg=cfg: tcl.gemm_into(a, b, c, cfg=cfg))
             for i in range(len(sets)):
                 fn(*sets[i])
@@ -612,8 +634,6 @@ def run_compare(args):
         st, code = tcl.last_device_error()
         if st:
             raise RuntimeError(f"device status {st} (code {code})")
-        in_kind = {"bf16": tcl.IN_BF16, "bf16->bf16": tcl.IN_BF16, "tf32": tcl.IN_TF32, "s8": tcl.IN_S8}[kind]
-        out = tcl.OUT_BF16 if kind == "bf16->bf16" else tcl.OUT_F32
         for name, kw, _ in graphs:
             med = statistics.median(times[name])
             print(json.dumps({"compare": args.compare, "workload": f"{kind} {m}x{n}x{k}", "setting": name,

@@ -218,6 +218,22 @@ typedef struct {
                                       multiple of 64 bf16 / 32 TF32 columns and the tile has
                                       several boxes: 128- and 256-wide one-SM tiles, 256-wide
                                       two-SM tiles); 1 one copy per box. Same result */
+    int die_split;                 /* two-SM kernel: 0 automatic (on for grids of at most 16 tile
+                                      columns and at least 3 tiles per pair of SMs, when the die
+                                      of every pair of SMs is known),
+                                      1 off, 2 on where possible (TCL_ERR_CONFIG otherwise). On:
+                                      the tiles are cut into one block of columns per die of the
+                                      GPU (whole columns and part of one, in proportion to the
+                                      die's pairs of SMs), walked row by row by the pairs on that
+                                      die, each block with its own stream-K tail, so that each
+                                      die's half of the L2 holds its own block's operands. The die of each pair of SMs is
+                                      measured once per device at the first call outside stream
+                                      capture (a few tens of microseconds, synchronous). Each pair
+                                      takes its place with one atomic on per-stream counters that
+                                      the launch leaves zeroed (so calls sharing a set of counters,
+                                      as graph-captured calls on different streams do, must not
+                                      run concurrently); whole tiles give the same result either
+                                      way */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -332,6 +348,8 @@ typedef struct {
                                        (1: one CTA per tile; see tcl_config_t.cluster_k) */
     int tile_m;                     /* rows per output tile (64, 128, or 256 for two SMs per tile) */
     int kblocks_per_stage;          /* k-blocks that one tensor copy of each operand brings (1 or 2) */
+    int die_split;                  /* 1: the tile columns in one block per die (tcl_config_t.die_split) */
+    int die_tiles0;                 /* with die_split: tiles of the first die's block */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this
@@ -373,12 +391,20 @@ TCL_API const char* tcl_status_string(int status);
  * word. Returns TCL_OK, or TCL_ERR_DEVICE_TIMEOUT if any kernel since the
  * last read recorded a timed-out wait (*detail, if not NULL, receives the raw
  * code: 1 producer, 2 MMA waiting for data, 3 MMA waiting for an accumulator,
- * 4 epilogue, 5 stream-K piece waiting for the previous piece), or
+ * 4 epilogue, 5 stream-K piece waiting for the previous piece; 6, not a wait:
+ * under the die split a pair of SMs found no place free because the counters
+ * were not zero at the launch's start, its tiles then not computed), or
  * TCL_ERR_LAUNCH if synchronising failed. */
 TCL_API int tcl_last_device_error(cudaStream_t stream, int* detail);
 
 /* Streaming multiprocessors of the current device (0 on error). */
 TCL_API int tcl_num_sms(void);
+
+/* Pairs of SMs on each of the two dies of the current device, as measured for
+ * the die split (tcl_config_t.die_split): *n0 + *n1 pairs, or 0 and 0 when the
+ * measurement found no two clear groups (or has not run: it runs here, or at
+ * the first call outside stream capture). Returns a tcl_status. */
+TCL_API int tcl_die_pairs(int* n0, int* n1);
 
 /* Frees the scratch buffer and stream-K flags that calls on `stream` (of the
  * current device) have used, after synchronising the stream: for a stream the

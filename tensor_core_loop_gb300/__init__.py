@@ -32,7 +32,7 @@ PRODUCER_TMA, PRODUCER_SYNC, PRODUCER_CPASYNC = 0, 1, 2
 IN_BF16, IN_TF32, IN_S8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gemm_bf16", "gemm_tf32", "gemm_s8", "gemm_bf16_ex", "gemm_tf32_ex", "gemm_s8_ex",
-                    "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms",
+                    "tcl_plan", "tcl_status_string", "tcl_last_device_error", "tcl_num_sms", "tcl_die_pairs",
                     "tcl_shutdown", "tcl_version", "gemm_s8_static", "tcl_mma_peak", "gemm_f32_simt",
                     "gemm_bf16_host", "tcl_stream_release")
 
@@ -73,6 +73,7 @@ class Config(ctypes.Structure):
         ("tile_m", ctypes.c_int),
         ("kblocks_per_stage", ctypes.c_int),
         ("b_copy", ctypes.c_int),
+        ("die_split", ctypes.c_int),
     ]
 
 
@@ -97,6 +98,8 @@ class PlanInfo(ctypes.Structure):
         ("cluster_k", ctypes.c_int),
         ("tile_m", ctypes.c_int),
         ("kblocks_per_stage", ctypes.c_int),
+        ("die_split", ctypes.c_int),
+        ("die_tiles0", ctypes.c_int),
     ]
 
 
@@ -131,6 +134,7 @@ def lib() -> ctypes.CDLL:
         L.tcl_status_string.restype = ctypes.c_char_p
         L.tcl_last_device_error.argtypes = [P, IP]
         L.tcl_num_sms.argtypes = []
+        L.tcl_die_pairs.argtypes = [IP, IP]
         L.tcl_shutdown.argtypes = []
         L.tcl_shutdown.restype = None
         L.tcl_stream_release.argtypes = [P]
@@ -145,6 +149,16 @@ def version() -> str:
 
 def num_sms() -> int:
     return int(lib().tcl_num_sms())
+
+
+def die_pairs() -> tuple:
+    """Pairs of SMs on each die of the current device as the die split measured them
+    ((0, 0): not known, no die split)."""
+    n0, n1 = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().tcl_die_pairs(ctypes.byref(n0), ctypes.byref(n1))
+    if st:
+        raise TclError(st, "tcl_die_pairs")
+    return n0.value, n1.value
 
 
 def plan(in_kind: int, out: int, M: int, N: int, K: int, cfg: Config | None = None) -> dict:

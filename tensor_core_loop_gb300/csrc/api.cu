@@ -25,6 +25,8 @@ __device__ unsigned int g_status_word;
 // so they never need clearing between launches.
 constexpr int kMaxSkTiles = 128;
 __device__ unsigned int g_sk_flags[kMaxSkTiles * 2 * 8];
+// The die split's rank counters and finished-pair count (zero between launches).
+__device__ unsigned long long g_sched_ctr[4];
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s
@@ -38,6 +40,7 @@ constexpr int kBM = 128;
 constexpr int kS32UnitK = 1024;
 
 constexpr size_t kSkFlagBytes = sizeof(unsigned int) * kMaxSkTiles * 2 * 8;
+constexpr size_t kStreamFlagBytes = kSkFlagBytes + 4 * sizeof(unsigned long long);   // + die split counters
 
 // Scratch and stream-K progress flags of the calls on one stream. Calls on
 // different streams may run on the GPU at the same time, so each stream has a
@@ -46,6 +49,7 @@ struct StreamRes {
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
     unsigned int* sk_flags = nullptr;   // kMaxSkTiles · 2 · 8 words
+    unsigned long long* sched_ctr = nullptr;   // die split counters (after the flags in an own set)
     unsigned int sk_gen = 0;            // last stream-K flag generation used with these flags
     bool own_flags = false;             // allocated for this stream (the default set's are a static array)
 };
@@ -54,6 +58,10 @@ struct DevState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
+    // which die each pair of SMs is on (calibrated once, outside stream capture)
+    int die_state = 0;             // 0 not yet, 1 known, -1 unknown (no die split)
+    int die_pairs[2] = {0, 0};
+    uint8_t die_of_tpc[128] = {};
     int pair_clusters[16] = {};  // resident clusters per pair variant (0: not yet queried)
     unsigned int* status = nullptr;
     // the set of the legacy and per-thread default streams, also taken by a call
@@ -158,17 +166,18 @@ int stream_res(DevState* ds, cudaStream_t stream, StreamRes** out) {
         return TCL_OK;
     }
     void* p = nullptr;
-    if (cudaMalloc(&p, kSkFlagBytes) != cudaSuccess) {
+    if (cudaMalloc(&p, kStreamFlagBytes) != cudaSuccess) {
         cudaGetLastError();
         return TCL_ERR_NO_MEMORY;
     }
-    if (cudaMemsetAsync(p, 0, kSkFlagBytes, stream) != cudaSuccess) {
+    if (cudaMemsetAsync(p, 0, kStreamFlagBytes, stream) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p);
         return TCL_ERR_LAUNCH;
     }
     StreamRes r;
     r.sk_flags = static_cast<unsigned int*>(p);
+    r.sched_ctr = reinterpret_cast<unsigned long long*>(static_cast<char*>(p) + kSkFlagBytes);
     r.own_flags = true;
     *out = &ds->per_stream.emplace(stream, r).first->second;   // (map nodes never move)
     return TCL_OK;
@@ -236,6 +245,11 @@ int current_device(int* dev_out, DevState** st_out) {
                 return TCL_ERR_LAUNCH;
             }
             d.base.sk_flags = static_cast<unsigned int*>(p);
+            if (cudaGetSymbolAddress(&p, g_sched_ctr) != cudaSuccess) {
+                cudaGetLastError();
+                return TCL_ERR_LAUNCH;
+            }
+            d.base.sched_ctr = static_cast<unsigned long long*>(p);
         }
         d.probed = true;
     }
@@ -341,6 +355,9 @@ struct Plan {
     int csk;                    // > 1: CTAs per tile summing its K ranges in a cluster (gemm_kernel_csk.cuh)
     int m64;                    // 1 or 2: 64×64 tiles, one CTA per tile, k-blocks per stage (gemm_kernel_m64.cuh)
     int kps;                    // two-SM kernel: k-blocks per tensor copy (1 or 2)
+    // two-SM kernel: the tile columns in one sub-grid per die (see GemmParams)
+    int die_split, sub_n[2], sub_rs, sub_a[2], sub_s[2], sub_b[2], sub_u[2], sub_tiles[2], sub_sk_tiles[2],
+        sub_sk_pieces[2];
 };
 
 // Split-K pays only when the k-blocks saved per CTA outweigh the partial-tile
@@ -375,6 +392,9 @@ constexpr int kMinKbPerPiece = 8;
 // the gain (measured on GB300 at 4096²: 224-wide whole tiles 8 % faster at
 // K = 1024, even at 1536, stream-K ahead from 2048).
 constexpr int kMinKbForSk = 32;
+constexpr int kMaxDieSplitCols = 16;   // automatic die split up to this many tile columns (two blocks)
+constexpr int kMinDieSplitPairs = 32;  // and only on a whole GPU's pairs
+constexpr int kMinDieSplitWaves = 3;   // and at least this many tiles per pair
 constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed when pieces are all a pair does
 
 // Stream-K split of the last (partial) wave of pair tiles: with `tiles` tiles
@@ -477,9 +497,10 @@ int deepest_stages(InKind ik, OutKind ok, int bn, int prod, int pair, int slots 
 // Chooses the tile shape, ring depth, one- or two-SM kernel and grid.
 // `sms` is the SM count; `pair_clusters(v)` returns how many two-CTA clusters
 // of pair variant v fit on the device at once.
+// die_pairs[d]: pairs of SMs on each die of the device (0, 0: not known).
 template <class PairClusters>
 int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cfg, int sms,
-              PairClusters pair_clusters, Plan* pl) {
+              PairClusters pair_clusters, const int* die_pairs, Plan* pl) {
     const int bk = 128 / in_bytes(ik);
     const int prod = cfg ? cfg->producer : PROD_TMA;
     if (prod != PROD_TMA && prod != PROD_SYNC && prod != PROD_CPASYNC) return TCL_ERR_CONFIG;
@@ -694,6 +715,7 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     // measured no faster on GB300 at 128×256 and 128×128 tiles.)
     const int want_kps = cfg ? cfg->kblocks_per_stage : 0;
     if (want_kps < 0 || want_kps > 2 || (cfg && (cfg->b_copy < 0 || cfg->b_copy > 1))) return TCL_ERR_CONFIG;
+    if (cfg && (cfg->die_split < 0 || cfg->die_split > 2 || (cfg->die_split == 2 && !pair))) return TCL_ERR_CONFIG;
     const bool kps2_ok = pair && !pl->s8_in_kernel && bn == 256 && prod == PROD_TMA && K % bk == 0 &&
                          N % (128 / in_bytes(ik)) == 0 && pl->stages >= 4 && pl->stages % 2 == 0;
     if (want_kps == 2 && !kps2_ok) return TCL_ERR_CONFIG;
@@ -729,6 +751,12 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
     pl->sk_pieces = 1;
     pl->sk_ws_rows = 0;
     pl->sk_balanced = pl->sk_first = pl->sk_region = 0;
+    pl->die_split = 0;
+    pl->sub_rs = 0;
+    for (int h = 0; h < 2; ++h)
+        pl->sub_n[h] = pl->sub_a[h] = pl->sub_s[h] = pl->sub_b[h] = pl->sub_u[h] = pl->sub_tiles[h] =
+            pl->sub_sk_tiles[h] = 0;
+    for (int h = 0; h < 2; ++h) pl->sub_sk_pieces[h] = 1;
     if (pair) {
         const int cl = 2;   // CTAs per cluster: one pair
         int clusters = cfg && cfg->max_ctas > 0 ? cfg->max_ctas / cl : pair_clusters(v);
@@ -778,6 +806,66 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
                 pl->sk_pieces = 1;
                 pl->sk_balanced = 0;
             }
+        }
+        // Die split: each die's pairs walk their own block of tile columns, row by row, with
+        // its own stream-K tail, so that each die's half of the L2 holds the operands of its
+        // own tiles: each die's L2 keeps what its SMs read, so a wave whose pairs span all
+        // of B holds B twice. The block is whole columns plus part of one (cut at a tile
+        // row), so that each die's tile count follows its pairs to the tile (the dies of a
+        // GB300 need not have equal pairs). Automatic where each die's block is at most about
+        // 8 tile columns wide (a wave then covers whole rows of it) and holds at least 3 waves
+        // of tiles. Measured on GB300 (CUDA graphs, on and off alternating in one process):
+        // dies of 36 and 40 pairs, bf16 4096³ 81.4 against 83.3 µs, bf16 C 83.1 against 84.5,
+        // int8 98.4 against 99.5, TF32 4096³ and 4096²×8192 within 0.5 and 0.9 % with 5–7 %
+        // less HBM traffic; dies of 38 and 38, 6144×4096×4096 124.5 against 130.4, 4096²×3072
+        // 66.1 against 68.0, 8192×4096×4096 164.2 against 166.8. Wider blocks (8192³ 3 %
+        // slower) and shorter grids (128–144 tiles: up to 4.5 % slower) keep the whole grid.
+        const int want_ds = cfg ? cfg->die_split : 0;
+        if (want_ds < 0 || want_ds > 2) return TCL_ERR_CONFIG;
+        const int pairs_all = pl->grid / cl;
+        const bool ds_ok = die_pairs && die_pairs[0] > 0 && die_pairs[1] > 0 &&
+                           die_pairs[0] + die_pairs[1] == pairs_all && pairs_all >= kMinDieSplitPairs &&
+                           !pl->sk_balanced && !pl->s8_in_kernel &&
+                           pl->tiles_n >= 2 && !(cfg && cfg->one_cta_per_tile);
+        if (want_ds == 2 && !ds_ok) return TCL_ERR_CONFIG;
+        // (a requested raster group keeps the whole grid unless the split is asked for too:
+        // the blocks are walked row by row)
+        const bool ds_auto = want_ds == 0 && pl->tiles_n <= kMaxDieSplitCols &&
+                             pl->num_tiles >= kMinDieSplitWaves * pairs_all && !(cfg && cfg->group_m > 0);
+        if (ds_ok && (want_ds == 2 || ds_auto)) {
+            const int n0 = die_pairs[0], n1 = die_pairs[1];
+            const long long all = static_cast<long long>(pl->tiles_m) * pl->tiles_n;
+            long long t0 = (all * n0 + (n0 + n1) / 2) / (n0 + n1);
+            t0 = std::max(1ll, std::min(t0, all - 1));
+            const int c0 = static_cast<int>(t0 / pl->tiles_m);   // whole columns of die 0
+            pl->die_split = 1;
+            pl->sub_n[0] = n0;
+            pl->sub_n[1] = n1;
+            pl->sub_rs = static_cast<int>(t0 % pl->tiles_m);        // rows of column c0 that are die 0's
+            pl->sub_a[0] = c0 + 1, pl->sub_s[0] = 0, pl->sub_b[0] = c0, pl->sub_u[0] = 0;
+            pl->sub_a[1] = pl->tiles_n - c0 - 1, pl->sub_s[1] = c0 + 1, pl->sub_b[1] = pl->tiles_n - c0,
+            pl->sub_u[1] = c0;
+            int total_sk = 0;
+            for (int h = 0; h < 2; ++h) {
+                const long long t = static_cast<long long>(pl->sub_rs) * pl->sub_a[h] +
+                                    static_cast<long long>(pl->tiles_m - pl->sub_rs) * pl->sub_b[h];
+                pl->sub_tiles[h] = static_cast<int>(t);
+                int skt = 0, skp = 1;
+                if (sk_capable && want_sk != 1 &&
+                    stream_k_split(t, static_cast<int>(std::min<long long>(pl->sub_n[h], t)), pl->num_kb,
+                                   want_sk, &skt, &skp))
+                    skt = 0, skp = 1;
+                pl->sub_sk_tiles[h] = skt;
+                pl->sub_sk_pieces[h] = skp;
+                total_sk += skt;
+            }
+            if (total_sk > kMaxSkTiles) {
+                for (int h = 0; h < 2; ++h) pl->sub_sk_tiles[h] = 0, pl->sub_sk_pieces[h] = 1;
+                total_sk = 0;
+            }
+            pl->sk_tiles = total_sk;
+            pl->sk_pieces = std::max(pl->sub_sk_pieces[0], pl->sub_sk_pieces[1]);
+            pl->group_m = 1;   // the sub-grids are walked row by row
         }
         // a bf16 C's fp32 workspace: one block per split tile (per range boundary when balanced)
         if (ok == OutKind::BF16 && (pl->sk_tiles || pl->sk_balanced))
@@ -833,9 +921,27 @@ int device_pair_clusters(DevState* ds, const VariantInfo* v) {
     return ds->pair_clusters[idx];
 }
 
+// Which die each pair of SMs is on (k_diemap.cu), measured at the first call that is
+// not being captured (the measurement allocates and synchronises); up to three tries.
+void ensure_die_map(DevState* ds, cudaStream_t stream) {
+    if (ds->die_state > 0 || ds->die_state <= -3) return;
+    int st = TCL_OK;
+    if (is_capturing(stream, &st) || st) return;
+    int n0 = 0, n1 = 0;
+    if (calibrate_die_map(ds->sms, ds->die_of_tpc, 128, &n0, &n1)) {
+        ds->die_pairs[0] = n0;
+        ds->die_pairs[1] = n1;
+        ds->die_state = 1;
+    } else {
+        ds->die_pairs[0] = ds->die_pairs[1] = 0;
+        --ds->die_state;
+    }
+}
+
 int plan_on_device(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cfg, DevState* ds, Plan* pl) {
+    const int pairs[2] = {ds->die_pairs[0], ds->die_pairs[1]};
     return make_plan(ik, ok, M, N, K, cfg, ds->sms,
-                     [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, pl);
+                     [ds](const VariantInfo* v) { return device_pair_clusters(ds, v); }, pairs, pl);
 }
 
 // Builds tensor maps and launches one GEMM over device operands (and, for a
@@ -960,6 +1066,19 @@ int run_gemm(const Plan& pl, InKind ik, OutKind ok, int M, int N, int K, const v
     p.k_serpentine = pl.k_serpentine;
     p.b_3d = b3d ? 1 : 0;
     p.kps2 = pl.kps == 2 ? 1 : 0;
+    p.die_split = pl.die_split;
+    p.sub_rs = pl.sub_rs;
+    for (int h = 0; h < 2; ++h) {
+        p.sub_n[h] = pl.sub_n[h];
+        p.sub_a[h] = pl.sub_a[h];
+        p.sub_s[h] = pl.sub_s[h];
+        p.sub_b[h] = pl.sub_b[h];
+        p.sub_u[h] = pl.sub_u[h];
+        p.sub_sk_tiles[h] = pl.sub_sk_tiles[h];
+        p.sub_sk_pieces[h] = pl.sub_sk_pieces[h];
+    }
+    p.sched_ctr = sr->sched_ctr;
+    std::memcpy(p.die_of_tpc, ds->die_of_tpc, sizeof p.die_of_tpc);
     if (pl.sk_ws_rows) {   // (16-byte accesses: the workspace starts on a 256-byte boundary)
         p.sk_ws = static_cast<float*>(workspace);
         p.sk_ws_rows = pl.sk_ws_rows;
@@ -1042,6 +1161,7 @@ int gemm_bf16_impl(int M, int N, int K, const void* A, int lda, const void* B, i
     StreamRes* sr;
     if ((st = stream_res(ds, stream, &sr))) return st;
     Plan pl;
+    ensure_die_map(ds, stream);
     if ((st = plan_on_device(InKind::BF16, ok, M, N, K2, cfg, ds, &pl))) return st;
     const size_t a_bytes = pack_a ? static_cast<size_t>(M) * lda2 * 2 : 0;
     const size_t b_bytes = pack_b ? static_cast<size_t>(K2) * ldb2 * 2 : 0;
@@ -1091,6 +1211,7 @@ int gemm_tf32_impl(int M, int N, int K, const float* A, int lda, const float* B,
     StreamRes* sr;
     if ((st = stream_res(ds, stream, &sr))) return st;
     Plan pl;
+    ensure_die_map(ds, stream);
     if ((st = plan_on_device(InKind::TF32, OutKind::F32, M, N, K4, cfg, ds, &pl))) return st;
     const size_t a_bytes = pack_a ? static_cast<size_t>(M) * K4 * 4 : 0;
     const size_t b_bytes = pack_b ? static_cast<size_t>(K4) * ldb2 * 4 : 0;
@@ -1135,6 +1256,7 @@ int gemm_s8_impl(int M, int N, int K, const int8_t* A, int lda, const int8_t* B,
     StreamRes* sr;
     if ((st = stream_res(ds, stream, &sr))) return st;
     Plan pl;
+    ensure_die_map(ds, stream);
     if ((st = plan_on_device(InKind::BF16, OutKind::S32, M, N, K, cfg, ds, &pl))) return st;
     // The in-kernel widening copies the int8 rows with tensor copies: 16-byte rows only.
     if (pl.s8_in_kernel && !(aligned16(A) && aligned16(B) && lda % 16 == 0 && ldb % 16 == 0)) return TCL_ERR_ALIGN;
@@ -1222,6 +1344,7 @@ int gemm_bf16_host_impl(int M, int N, int K, const void* A, int lda, const void*
     chunks = (M + rows - 1) / rows;
     const int last_rows = M - (chunks - 1) * rows;
     Plan pf, plast;
+    ensure_die_map(ds, ds->comp);
     if ((st = plan_on_device(InKind::BF16, ok, rows < M ? rows : M, N, K2, cfg, ds, &pf))) return st;
     if ((st = plan_on_device(InKind::BF16, ok, last_rows, N, K2, cfg, ds, &plast))) return st;
     const size_t ws_bytes = std::max(split_workspace(pf, rows < M ? rows : M, N).bytes,
@@ -1403,14 +1526,17 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
     Plan pl;
     int st;
     if (cfg && cfg->max_ctas > 0) {
-        // planning without a device: max_ctas stands for the SM count (pairs: max_ctas / 2)
-        st = make_plan(ik, ok, M, N, K, cfg, cfg->max_ctas, [](const VariantInfo*) { return 0; }, &pl);
+        // planning without a device: max_ctas stands for the SM count (pairs: max_ctas / 2,
+        // half of them on each die)
+        const int pairs[2] = {cfg->max_ctas / 4, cfg->max_ctas / 2 - cfg->max_ctas / 4};
+        st = make_plan(ik, ok, M, N, K, cfg, cfg->max_ctas, [](const VariantInfo*) { return 0; }, pairs, &pl);
     } else {
         std::lock_guard<std::mutex> lock(g_mu);
         int dev;
         DevState* ds;
         st = current_device(&dev, &ds);
         if (st) return st;
+        ensure_die_map(ds, cudaStreamLegacy);
         st = plan_on_device(ik, ok, M, N, K, cfg, ds, &pl);
     }
     if (st) return st;
@@ -1433,6 +1559,8 @@ int tcl_plan(int in_kind, int out, int M, int N, int K, const tcl_config_t* cfg,
         plan->cluster_k = pl.csk ? pl.csk : 1;
         plan->tile_m = pl.pair ? 256 : pl.m64 ? 64 : 128;
         plan->kblocks_per_stage = pl.m64 ? pl.m64 : pl.kps;
+        plan->die_split = pl.die_split;
+        plan->die_tiles0 = pl.die_split ? pl.sub_tiles[0] : 0;
     }
     return TCL_OK;
 }
@@ -1484,6 +1612,20 @@ int tcl_num_sms(void) {
     DevState* ds;
     if (current_device(&dev, &ds)) return 0;
     return ds->sms;
+}
+
+int tcl_die_pairs(int* n0, int* n1) {
+    if (n0) *n0 = 0;
+    if (n1) *n1 = 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    DevState* ds;
+    int st = current_device(&dev, &ds);
+    if (st) return st;
+    ensure_die_map(ds, cudaStreamLegacy);
+    if (n0) *n0 = ds->die_pairs[0];
+    if (n1) *n1 = ds->die_pairs[1];
+    return TCL_OK;
 }
 
 int tcl_stream_release(cudaStream_t stream) {

@@ -55,6 +55,7 @@ enum : unsigned int {
     DEV_TIMEOUT_MMA_ACC = 3,    // MMA warp waited too long for a free accumulator
     DEV_TIMEOUT_EPILOGUE = 4,   // epilogue waited too long for a finished accumulator
     DEV_TIMEOUT_SK_ORDER = 5,   // epilogue waited too long for the previous piece of a split tile
+    DEV_SCHED_RANK = 6,         // die split: a pair found no rank free (counters not zeroed)
 };
 
 template <InKind IK>
@@ -138,6 +139,26 @@ struct GemmParams {
     // the copies at an even ring slot fill that slot and the next, the odd slot loads nothing,
     // slots are released in pairs, and each tile's walk starts on an even slot
     int kps2;
+    // Die split (two-SM kernel): the tile columns are cut into two sub-grids, one per die
+    // of the GPU, each walked by the pairs of SMs on that die (so that each die's half of
+    // the L2 holds its own sub-grid's operands). A pair's leader takes a rank on its die
+    // (sched_ctr[die], one atomic; when that die's ranks are all taken, a rank on the other
+    // die), so every rank is taken exactly once whatever the placement; the last pair to
+    // finish zeroes the counters (sched_ctr[2] counts finished pairs). Each sub-grid has
+    // its own stream-K tail; its split tiles are numbered after those of the sub-grids
+    // before it.
+    int die_split;
+    int sub_n[2];            // pairs of each sub-grid (sub_n[0] + sub_n[1] = gridDim.x / 2)
+    // Sub-grid h holds, in tile rows below sub_rs, the sub_a[h] tile columns from sub_s[h],
+    // and in the other rows the sub_b[h] columns from sub_u[h]: a block of whole columns
+    // plus part of one column, so that each sub-grid's tile count follows its pairs to the
+    // tile. Walked row by row.
+    int sub_rs;
+    int sub_a[2], sub_s[2], sub_b[2], sub_u[2];
+    int sub_sk_tiles[2];     // stream-K split tiles of each sub-grid
+    int sub_sk_pieces[2];
+    unsigned long long* sched_ctr;
+    uint8_t die_of_tpc[128];   // die (0, 1; 255 unknown) of the pair of SMs (SM id / 2)
 };
 
 // K coordinate (in k-blocks) that the load at position kb of the range

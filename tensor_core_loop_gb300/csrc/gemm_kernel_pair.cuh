@@ -143,6 +143,61 @@ struct PairUnit {
     int tile, kb_lo, kb_hi, piece, sk_index;   // sk_index: split-tile number, -1 for a whole tile
 };
 
+// The tiles a pair walks: the whole grid (in groups of group_m tile rows), or under the
+// die split its die's sub-grid (row by row: rs rows of a columns from s, then rows of b
+// columns from u). cluster / clusters: the pair's index among the sub-grid's pairs and
+// their number; split tiles are numbered from sk_off.
+struct Sched {
+    int cluster, clusters, num_tiles, sk_tiles, sk_pieces, sk_off;
+    int split, rs, a, s, b, u;
+};
+
+__device__ __forceinline__ Sched make_sched(const GemmParams& p, int slot, int pairs) {
+    Sched S;
+    S.split = p.die_split;
+    if (!p.die_split) {
+        S.cluster = slot;
+        S.clusters = pairs;
+        S.num_tiles = p.num_tiles;
+        S.sk_tiles = p.sk_tiles;
+        S.sk_pieces = p.sk_pieces;
+        S.sk_off = 0;
+        S.rs = S.a = S.s = S.b = S.u = 0;
+        return S;
+    }
+    const int h = slot < p.sub_n[0] ? 0 : 1;
+    S.cluster = slot - (h ? p.sub_n[0] : 0);
+    S.clusters = p.sub_n[h];
+    S.rs = p.sub_rs;
+    S.a = p.sub_a[h];
+    S.s = p.sub_s[h];
+    S.b = p.sub_b[h];
+    S.u = p.sub_u[h];
+    S.num_tiles = S.rs * S.a + (p.tiles_m - S.rs) * S.b;
+    S.sk_tiles = p.sub_sk_tiles[h];
+    S.sk_pieces = p.sub_sk_pieces[h];
+    S.sk_off = h ? p.sub_sk_tiles[0] : 0;
+    return S;
+}
+
+// Tile t of the walk: the grouped raster order over the whole grid, or the sub-grid's
+// tiles row by row.
+__device__ __forceinline__ void sched_tile_coords(int t, const GemmParams& p, const Sched& S, int& mb, int& nb) {
+    if (!S.split) {
+        tile_coords(t, p, mb, nb);
+        return;
+    }
+    const int head = S.rs * S.a;   // tiles in the rows below rs
+    if (t < head) {
+        mb = t / S.a;
+        nb = S.s + t % S.a;
+    } else {
+        const int r = t - head;
+        mb = S.rs + r / S.b;
+        nb = S.u + r % S.b;
+    }
+}
+
 // Balanced stream-K: pair c's share of the region's k-blocks, [lo, hi) in the
 // tile-major order of the region, as (tile, k-block) positions.
 struct SkRange {
@@ -202,30 +257,34 @@ __device__ __forceinline__ PairUnit pair_unit_balanced(const GemmParams& p, int 
     return U;
 }
 
-__device__ __forceinline__ int pair_units(const GemmParams& p, int cluster, int clusters) {
-    if (p.sk_balanced) return pair_units_balanced(p, cluster, clusters);
-    const int whole = p.num_tiles - p.sk_tiles;
-    const int n = cluster < whole ? (whole - 1 - cluster) / clusters + 1 : 0;
-    return n + (cluster < p.sk_tiles * p.sk_pieces ? 1 : 0);
+__device__ __forceinline__ int pair_units(const GemmParams& p, const Sched& S) {
+    if (S.cluster < 0) return 0;   // die split without a rank (reported): no work
+    if (p.sk_balanced) return pair_units_balanced(p, S.cluster, S.clusters);
+    const int whole = S.num_tiles - S.sk_tiles;
+    const int n = S.cluster < whole ? (whole - 1 - S.cluster) / S.clusters + 1 : 0;
+    return n + (S.cluster < S.sk_tiles * S.sk_pieces ? 1 : 0);
 }
 
-__device__ __forceinline__ PairUnit pair_unit(const GemmParams& p, int cluster, int clusters, int u) {
-    if (p.sk_balanced) return pair_unit_balanced(p, cluster, clusters, u);
+// (tile numbers are the sub-grid's; sk_index is global)
+__device__ __forceinline__ PairUnit pair_unit(const GemmParams& p, const Sched& S, int u) {
+    if (p.sk_balanced) return pair_unit_balanced(p, S.cluster, S.clusters, u);
     PairUnit r;
-    const bool has_piece = cluster < p.sk_tiles * p.sk_pieces;
-    const int piece = has_piece ? cluster % p.sk_pieces : 0;
-    const bool piece_first = has_piece && piece + 1 < p.sk_pieces;
-    const int piece_at = piece_first ? 0 : pair_units(p, cluster, clusters) - 1;   // the piece's position
+    const int cluster = S.cluster;
+    const bool has_piece = cluster < S.sk_tiles * S.sk_pieces;
+    const int piece = has_piece ? cluster % S.sk_pieces : 0;
+    const bool piece_first = has_piece && piece + 1 < S.sk_pieces;
+    const int piece_at = piece_first ? 0 : pair_units(p, S) - 1;   // the piece's position
     if (has_piece && u == piece_at) {
-        r.sk_index = cluster / p.sk_pieces;
+        const int d = cluster / S.sk_pieces;
+        r.sk_index = S.sk_off + d;
         r.piece = piece;
-        r.tile = p.num_tiles - p.sk_tiles + r.sk_index;
-        r.kb_lo = r.piece * p.num_kb / p.sk_pieces;
-        r.kb_hi = (r.piece + 1) * p.num_kb / p.sk_pieces;
+        r.tile = S.num_tiles - S.sk_tiles + d;
+        r.kb_lo = r.piece * p.num_kb / S.sk_pieces;
+        r.kb_hi = (r.piece + 1) * p.num_kb / S.sk_pieces;
     } else {
         r.sk_index = -1;
         r.piece = 0;
-        r.tile = cluster + (u - (piece_first ? 1 : 0)) * clusters;
+        r.tile = cluster + (u - (piece_first ? 1 : 0)) * S.clusters;
         r.kb_lo = 0;
         r.kb_hi = p.num_kb;
     }
@@ -263,6 +322,24 @@ __device__ __forceinline__ bool wait_sk_flag(const uint32_t* flag, uint32_t want
     return ok != 0;
 }
 
+// Die split: this pair's rank (its slot among all pairs, sub-grid 0's first). One
+// atomic on the counter of the pair's own die; when all of that die's ranks are taken
+// (more pairs landed there than the map counted), one on the other die's. The counters
+// start each launch at zero and every pair takes one rank, so the ranks are a
+// permutation of the slots; -1 (reported) only if a counter was not zeroed.
+__device__ __forceinline__ int claim_rank(const GemmParams& p) {
+    const uint32_t tpc = ptx::smid() >> 1;
+    uint32_t d = tpc < 128u ? p.die_of_tpc[tpc] : 255u;
+    if (d > 1u) d = 0u;   // a pair the map does not place: either die (only locality depends on it)
+    unsigned long long r = atomicAdd(p.sched_ctr + d, 1ull);
+    if (r < static_cast<unsigned long long>(p.sub_n[d])) return (d ? p.sub_n[0] : 0) + static_cast<int>(r);
+    const uint32_t e = d ^ 1u;
+    r = atomicAdd(p.sched_ctr + e, 1ull);
+    if (r < static_cast<unsigned long long>(p.sub_n[e])) return (e ? p.sub_n[0] : 0) + static_cast<int>(r);
+    atomicCAS(p.status, 0u, DEV_SCHED_RANK);
+    return -1;
+}
+
 __device__ __forceinline__ void spin_ns(unsigned long long ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < ns) {
@@ -283,6 +360,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
     volatile uint32_t* abort_flag = tmem_holder + 1;
     volatile uint32_t* progress = tmem_holder + 2;   // k-blocks whose loads this CTA's producer has issued
+    volatile int* slot_word = reinterpret_cast<volatile int*>(tmem_holder + 3);   // die split: the pair's rank
 
     const uint32_t full0 = ptx::smem_u32(bars);
     const uint32_t empty0 = ptx::smem_u32(bars + STAGES);
@@ -336,8 +414,21 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
     const bool kps2 = p.kps2 != 0;
     const bool rel2 = C::REL == 2 || kps2;   // ring slots released in pairs (commits on odd slots)
     auto rel_slot = [rel2](uint32_t s) { return rel2 ? (s | 1u) : s; };
-    const int cluster = blockIdx.x / C::CL;
-    const int clusters = gridDim.x / C::CL;
+    const int pairs = gridDim.x / C::CL;
+    int slot = blockIdx.x / C::CL;
+    if (p.die_split) {
+        // the leader takes the pair's rank and writes it into both CTAs; the cluster
+        // barrier makes it visible to every thread of the pair
+        if (leader && threadIdx.x == 0) {
+            const int r = claim_rank(p);
+            *slot_word = r;
+            ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32(const_cast<int*>(slot_word)), 1u),
+                                static_cast<uint32_t>(r));
+        }
+        ptx::cluster_sync();
+        slot = *slot_word;
+    }
+    const Sched S = make_sched(p, slot, pairs);
     const bool tracing = (p.trace != nullptr) && (blockIdx.x == 0);
     if (tracing && threadIdx.x == 0) {   // SM clock and wall clock at the start of CTA 0's work
         p.trace[4 * p.trace_cap + 0] = ptx::clock64();
@@ -350,11 +441,11 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
         // elected lane.
         uint32_t it = 0;
         bool ok = true;
-        const int units = pair_units(p, cluster, clusters);
+        const int units = pair_units(p, S);
         for (int u = 0; ok && u < units; ++u) {
-            const PairUnit U = pair_unit(p, cluster, clusters, u);
+            const PairUnit U = pair_unit(p, S, u);
             int mb, nb;
-            tile_coords(U.tile, p, mb, nb);
+            sched_tile_coords(U.tile, p, S, mb, nb);
             const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
             const int col = nb * C::BN + static_cast<int>(rank) * (C::BN / 2);
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
@@ -445,9 +536,9 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             static_assert(C::KSUB == 4, "four MMAs per k-block");
             uint32_t it = 0, unit = 0, s = 0, ph = 0;
             bool ok = true;
-            const int units = pair_units(p, cluster, clusters);
+            const int units = pair_units(p, S);
             for (int u = 0; ok && u < units; ++u) {
-                const PairUnit U = pair_unit(p, cluster, clusters, u);
+                const PairUnit U = pair_unit(p, S, u);
                 const bool desc = p.k_serpentine && (u & 1);   // this tile's loads walk K downwards
                 // accumulation units of kb_per_unit k-blocks (exact-integer mode: 1024 K
                 // values, drained into int32 sums; otherwise the whole range)
@@ -536,7 +627,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             if (!wait_sk_flag(flag, (p.sk_gen << 3) | static_cast<uint32_t>(U.piece), abort_flag, peer_abort,
                               p.timeout_ns, p.status))
                 return false;
-            if (U.piece + 1 == p.sk_pieces) {
+            if (U.piece + 1 == S.sk_pieces) {
                 // the flag's last reader leaves it as this launch found it (0), so that a
                 // replay of the same launch (a CUDA graph: same generation) waits again
                 __syncwarp();   // every lane has made its acquire of the flag
@@ -557,12 +648,12 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
             }
             __syncwarp();
         };
-        const int units = pair_units(p, cluster, clusters);
+        const int units = pair_units(p, S);
         for (int u = 0; ok && u < units; ++u) {
-            const PairUnit U = pair_unit(p, cluster, clusters, u);
+            const PairUnit U = pair_unit(p, S, u);
             it_next += static_cast<uint32_t>(kps2 ? (U.kb_hi - U.kb_lo + 1) & ~1 : U.kb_hi - U.kb_lo);
             int mb, nb;
-            tile_coords(U.tile, p, mb, nb);
+            sched_tile_coords(U.tile, p, S, mb, nb);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
             // bf16 C, split tile: this warp's block of the fp32 workspace (32 rows × BN)
             [[maybe_unused]] float* blk = nullptr;
@@ -625,7 +716,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                                 &tmC, slab_pair, store_count, v, lane, nb * C::BN + h * CW + c * 32, row0, p,
                                 U.piece > 0);
                         }
-                        if (flag && U.piece + 1 < p.sk_pieces) hand_over(flag, U);
+                        if (flag && U.piece + 1 < S.sk_pieces) hand_over(flag, U);
                     }
                     continue;
                 }
@@ -645,7 +736,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                         // bf16 C, split tile: the pieces' fp32 sums meet in this warp's
                         // workspace block (stored by piece 0, added by the next ones in piece
                         // order); the last piece adds the block and rounds once into C
-                        if (U.piece + 1 < p.sk_pieces) {
+                        if (U.piece + 1 < S.sk_pieces) {
                             drain_to_workspace<C::BN / 32>(tbase, lane, blk, release, U.piece > 0);
                             hand_over(flag, U);
                         } else {
@@ -665,7 +756,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                         // CTA's last unit, and a stream-K piece (the next piece waits for
                         // it), store at once.
                         if (u + 1 >= units || c == 0 || U.sk_index >= 0) return;
-                        const PairUnit V = pair_unit(p, cluster, clusters, u + 1);
+                        const PairUnit V = pair_unit(p, S, u + 1);
                         const uint32_t n = static_cast<uint32_t>(V.kb_hi - V.kb_lo);
                         // (the producer issues all n k-blocks of the next unit, so the target is reached)
                         const uint32_t target = it_next + min(n, STAGES + c * n / C::EPI_CHUNKS);
@@ -676,7 +767,7 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                         }
                         __syncwarp();
                     });
-                if (flag && U.piece + 1 < p.sk_pieces) hand_over(flag, U);
+                if (flag && U.piece + 1 < S.sk_pieces) hand_over(flag, U);
             }
         }
         if (lane == 0) ptx::bulk_wait<0>();
@@ -691,6 +782,18 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
         p.trace[4 * p.trace_cap + 3] = ptx::globaltimer_ns();
     }
     ptx::cluster_sync();   // no CTA frees TMEM or exits while its peer may still signal it
+    if (p.die_split && leader && threadIdx.x == 0) {
+        // the last pair to finish zeroes the rank counters for the next launch (every
+        // pair took its rank before it got here)
+        __threadfence();
+        const unsigned long long done = atomicAdd(p.sched_ctr + 2, 1ull);
+        if (done + 1 == static_cast<unsigned long long>(pairs)) {
+            __threadfence();
+            atomicExch(p.sched_ctr + 0, 0ull);
+            atomicExch(p.sched_ctr + 1, 0ull);
+            atomicExch(p.sched_ctr + 2, 0ull);
+        }
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);

@@ -205,9 +205,8 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
     const uint32_t tokens_leader0 = ptx::mapa_shared(tokens0, 0u);
     const uint32_t acce_leader0 = ptx::mapa_shared(acce0, 0u);
     const AbortNet peer_abort{ptx::smem_u32(const_cast<uint32_t*>(abort_flag)), 2};
-    const int cluster = blockIdx.x / 2;
-    const int clusters = gridDim.x / 2;
-    const int units = pair_units(p, cluster, clusters);
+    const Sched S = make_sched(p, blockIdx.x / 2, gridDim.x / 2);   // the whole grid (no die split here)
+    const int units = pair_units(p, S);
     // per-k-block %clock64 stamps of CTA 0 (raw copy issued by the producer; raw slot
     // landed, stage converted and fenced, stage handed over — seen by the first
     // converter thread)
@@ -220,7 +219,7 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int u = 0; ok && u < units; ++u) {
-            const PairUnit U = pair_unit(p, cluster, clusters, u);
+            const PairUnit U = pair_unit(p, S, u);
             for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                 const uint32_t r = it % RAW, rph = (it / RAW) & 1u;
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -285,9 +284,9 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int u = 0; ok && u < units; ++u) {
-                const PairUnit U = pair_unit(p, cluster, clusters, u);
+                const PairUnit U = pair_unit(p, S, u);
                 int mb, nb;
-                tile_coords(U.tile, p, mb, nb);
+                sched_tile_coords(U.tile, p, S, mb, nb);
                 const int row = mb * C::BM + static_cast<int>(rank) * C::ROWS;
                 const int col = nb * C::BN + static_cast<int>(rank) * C::COLS;
                 for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
@@ -315,7 +314,7 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int u = 0; ok && u < units; ++u) {
-                const PairUnit U = pair_unit(p, cluster, clusters, u);
+                const PairUnit U = pair_unit(p, S, u);
                 for (int kb = U.kb_lo; kb < U.kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     if (!wait_warp_pair(cfull0 + 8 * s, ph, abort_flag, peer_abort, p.timeout_ns, p.status,
@@ -346,7 +345,7 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
             uint32_t unit = 0, s = 0, ph = 0, mit = 0;
             bool ok = true;
             for (int u = 0; ok && u < units; ++u) {
-                const PairUnit U = pair_unit(p, cluster, clusters, u);
+                const PairUnit U = pair_unit(p, S, u);
                 for (int kb0 = U.kb_lo; ok && kb0 < U.kb_hi; kb0 += p.kb_per_unit, ++unit) {
                     const int kb1 = min(kb0 + p.kb_per_unit, U.kb_hi);
                     const uint32_t buf = unit & 1u;
@@ -401,9 +400,9 @@ __global__ void __launch_bounds__(S8PairCfg<STAGES, RAW>::THREADS, 1)
         uint32_t unit = 0;
         bool ok = true;
         for (int u = 0; ok && u < units; ++u) {
-            const PairUnit U = pair_unit(p, cluster, clusters, u);
+            const PairUnit U = pair_unit(p, S, u);
             int mb, nb;
-            tile_coords(U.tile, p, mb, nb);
+            sched_tile_coords(U.tile, p, S, mb, nb);
             const int row0 = mb * C::BM + static_cast<int>(rank) * C::ROWS + q * 32;
             uint32_t* flag =
                 U.sk_index >= 0 ? p.sk_flags + (U.sk_index * 2 + rank) * C::EPI_WARPS + ew : nullptr;

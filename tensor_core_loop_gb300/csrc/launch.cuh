@@ -57,6 +57,9 @@ int csk_smem_bytes(int cl);
 int s8_pair_stages();
 int s8_pair_smem_bytes();
 int s8_pair_max_clusters();
+// Die of each pair of SMs (k_diemap.cu): fills die_of_tpc[SM id / 2] with 0 or 1 and the
+// pairs per die; false when the measurement shows no clear two groups.
+bool calibrate_die_map(int sms, uint8_t* die_of_tpc, int max_tpc, int* n0, int* n1);
 
 // int8 -> bf16 widening (exact) of two matrices in one launch: rows × cols of
 // src (leading dimension ld_src) into a packed row-major buffer dst with ld_dst

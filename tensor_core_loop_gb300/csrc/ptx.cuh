@@ -22,6 +22,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Index of the SM this thread runs on (two consecutive ids are the two SMs of a pair).
+__device__ __forceinline__ uint32_t smid() {
+    uint32_t s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
+
 __device__ __forceinline__ uint64_t clock64() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));

@@ -196,9 +196,11 @@ def test_plan_without_device(L):
     for in_kind, k in ((tcl.IN_BF16, 8192), (tcl.IN_TF32, 4096)):
         p = tcl.plan(in_kind, tcl.OUT_F32, 4096, 4096, k, cfg)
         assert (p["cta_pair"], p["group_m"], p["k_serpentine"]) == (2, 1, 1)
-    for k in (1024, 4096):
-        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, cfg)
+    for k in (2048, 4096):   # (the whole grid: automatically these run the die split, row by row)
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, tcl.Config(max_ctas=152, die_split=1))
         assert (p["group_m"], p["k_serpentine"]) == (8, 0)
+        p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, cfg)
+        assert (p["die_split"], p["group_m"], p["k_serpentine"]) == (1, 1, 0)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, group_m=4, k_order=1))
     assert (p["group_m"], p["k_serpentine"]) == (4, 0)
     # int8 on 256-wide pair tiles widens inside the kernel on request (s8_path 2) only
@@ -325,6 +327,42 @@ def test_planner_kblocks_per_copy(L):
     # one SM per tile: 64×64 tiles report their two k-blocks per 32 KB stage
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 256, cfg)["kblocks_per_stage"] == 2
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 512, 512, 520, cfg)["kblocks_per_stage"] == 1
+
+
+def test_planner_die_split(L):
+    # two-SM grids of at most 16 tile columns: the tiles in one block of columns per die,
+    # each with its own stream-K tail (offline, half of the max_ctas / 2 pairs on each die)
+    cfg = tcl.Config(max_ctas=152)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, cfg)
+    assert (p["cta_pair"], p["die_split"], p["die_tiles0"], p["group_m"]) == (2, 1, 128, 1)
+    # 16 × 8 tiles per die on 38 pairs: 3 waves and 14 tiles in 2 pieces, on each die
+    assert (p["sk_tiles"], p["sk_pieces"], p["grid"]) == (28, 2, 152)
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 4096, cfg)["die_split"] == 1   # 16 KB rows
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_BF16, 4096, 4096, 8192, cfg)["die_split"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)["die_split"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 8192, 8192, 8192, cfg)["die_split"] == 0   # 32 columns
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, group_m=4))["die_split"] == 0
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=8))["die_split"] == 0   # 4 pairs
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 3072, 3072, 4096, cfg)["die_split"] == 0   # 144 tiles: < 3 waves
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 6144, 4096, 4096, cfg)["die_split"] == 1
+    on = tcl.Config(max_ctas=152, die_split=2)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 8192, 8192, 8192, on)
+    assert (p["die_split"], p["die_tiles0"]) == (1, 512)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, tcl.Config(max_ctas=152, die_split=1))["die_split"] == 0
+    # uneven dies: the tiles in proportion to the pairs, to the tile (offline: 37 and 38
+    # pairs for max_ctas 150: 256 · 37 / 75 rounds to 126 tiles, 7 columns and 14 rows of
+    # the 8th; 192 · 37 / 75 to 95)
+    p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, tcl.Config(max_ctas=150))
+    assert p["die_split"] == 1 and p["die_tiles0"] == 126 and p["grid"] == 150
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 3072, 8192,
+                    tcl.Config(max_ctas=150, die_split=2))["die_tiles0"] == 95
+    for bad in (tcl.Config(max_ctas=152, die_split=3), tcl.Config(max_ctas=152, die_split=-1),
+                tcl.Config(max_ctas=152, die_split=2, cta_pair=1),
+                tcl.Config(max_ctas=152, die_split=2, stream_k=5)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, bad)
+    with pytest.raises(tcl.TclError):   # fewer tiles than pairs: not every pair would take a place
+        tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 1024, 1024, 8192, tcl.Config(max_ctas=152, die_split=2, cta_pair=2))
 
 
 def test_planner_producer_kinds(L):

@@ -556,6 +556,78 @@ def test_b_boxes_in_one_copy(oracle_mod, kind, M, N, K, cfg):
                        run(a, b, out_dtype=od, cfg=per_box, canary=False))
 
 
+def test_die_map_measured():
+    # the two dies of a GB300 each hold half of its pairs of SMs
+    n0, n1 = tcl.die_pairs()
+    assert n0 > 0 and n1 > 0 and n0 + n1 == tcl.num_sms() // 2, (n0, n1)
+
+
+@pytest.mark.parametrize("kind,M,N,K,extra", [
+    ("bf16", 2304, 4096, 2048, dict()),                 # 9 × 8 tiles per die on ~38 pairs, no tail
+    ("bf16", 4096, 4096, 2048, dict()),                 # a stream-K tail on each die
+    ("bf16", 4000, 3968, 2040, dict()),                 # ragged M, N and last k-block
+    ("bf16_out", 4096, 4096, 2048, dict()),             # bf16 C: tail pieces through the fp32 workspace
+    ("tf32", 4096, 3072, 1024, dict()),
+    ("s8", 4096, 4096, 2048, dict()),                   # exact integers
+    ("bf16", 4096, 4096, 2048, dict(k_order=2)),        # alternating K order
+])
+def test_die_split(oracle_mod, kind, M, N, K, extra):
+    """Each die's pairs walk their own block of tile columns: within the oracle's bound on
+    sampled rows (and exact for int8)."""
+    cfg = tcl.Config(cta_pair=2, die_split=2, **extra)
+    in_kind = {"bf16": tcl.IN_BF16, "bf16_out": tcl.IN_BF16, "tf32": tcl.IN_TF32, "s8": tcl.IN_S8}[kind]
+    out = tcl.OUT_BF16 if kind == "bf16_out" else tcl.OUT_F32
+    assert tcl.plan(in_kind, out, M, N, K, cfg)["die_split"] == 1
+    rows = sample_rows(M, n=12, seed=M + K)
+    if kind in ("bf16", "bf16_out"):
+        bf16_case(oracle_mod, M, N, K, seed=K + 7, out_dtype=torch.bfloat16 if kind == "bf16_out" else torch.float32,
+                  cfg=cfg, ldc=up(N, 8), rows=rows)
+    elif kind == "tf32":
+        a, b = inputs.tf32_pair(M, N, K, seed=K + 7)
+        got = run(a.to(DEV), b.to(DEV), cfg=cfg).double().numpy()
+        for r in rows:
+            ref, S = oracle_mod.gemm_tf32(a.numpy(), b.numpy(), rows=(r, r + 1))
+            assert_within("tf32", got[r:r + 1], ref, S, f"tf32 die split row {r}")
+    else:
+        a, b = inputs.s8_pair(M, N, K, seed=K + 7)
+        got = run(a.to(DEV), b.to(DEV), cfg=cfg).numpy()
+        for r in rows:
+            assert_exact(got[r:r + 1], oracle_mod.gemm_s8(a.numpy(), b.numpy(), rows=(r, r + 1)), f"s8 row {r}")
+    assert tcl.last_device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("N", [4096, 3840])
+def test_die_split_whole_tiles_bitwise_and_replays(N):
+    """Whole tiles in ascending K: the die split changes which pair computes a tile, not
+    how, so the bits are those of the plain walk (every tile computed once: with 15 tile
+    columns the dies' blocks meet inside a column whatever their pairs); and the rank
+    counters are zero again after every launch (CUDA graph replays and back-to-back calls
+    stay exact)."""
+    a, b = inputs.bf16_pair(4096, N, 1024, seed=31)
+    a, b = a.to(DEV), b.to(DEV)
+    base = dict(cta_pair=2, stream_k=1, k_order=1)
+    plain = run(a, b, cfg=tcl.Config(die_split=1, **base), canary=False)
+    split_cfg = tcl.Config(die_split=2, **base)
+    pl = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, N, 1024, split_cfg)
+    assert pl["die_split"] == 1 and 0 < pl["die_tiles0"] < pl["num_tiles"]
+    for _ in range(3):
+        assert torch.equal(run(a, b, cfg=split_cfg, canary=False), plain)
+    c = torch.empty((4096, N), dtype=torch.float32, device=DEV)
+    tcl.gemm_into(a, b, c, cfg=split_cfg)   # scratch in place before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(3):
+            tcl.gemm_into(a, b, c, cfg=split_cfg)
+    for _ in range(4):
+        c.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(c.cpu(), plain)
+    assert tcl.last_device_error() == (0, 0)
+
+
 def test_variants_bitwise_identical():
     """Pipelining only reorders loads: every ring depth, persistent or one CTA per
     tile, gives the same bits (the MMA order inside a tile does not change)."""

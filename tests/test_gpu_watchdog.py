@@ -63,6 +63,23 @@ def test_two_sm_kernel_bounded_wait_runs_out(kps, skip):
     assert tcl.last_device_error() == (0, 0)
 
 
+def test_die_split_bounded_wait_runs_out_and_counters_reset():
+    # under the die split CTA 0 skips a k-block: the wait runs out, every pair still reaches
+    # the end (the last one zeroes the rank counters), and the next calls are exact
+    a, b = inputs.bf16_pair(4096, 4096, 2048, seed=12)
+    a, b = a.to(DEV), b.to(DEV)
+    c = torch.zeros((4096, 4096), dtype=torch.float32, device=DEV)
+    base = dict(cta_pair=2, die_split=2, stream_k=1, k_order=1)
+    tcl.gemm_into(a, b, c, cfg=tcl.Config(timeout_ns=50_000_000, debug_skip_kblock=3, **base))
+    st, code = tcl.last_device_error()
+    assert st == 7 and code in (1, 2, 3, 4), (st, code)
+    x = tcl.gemm(a, b, cfg=tcl.Config(**base))
+    y = tcl.gemm(a, b, cfg=tcl.Config(cta_pair=2, die_split=1, stream_k=1, k_order=1))
+    torch.cuda.synchronize()
+    assert torch.equal(x, y)
+    assert tcl.last_device_error() == (0, 0)
+
+
 @pytest.mark.parametrize("sk,split", [(2, 1), (5, 3)])
 def test_stream_k_order_wait_runs_out(sk, split):
     # the first piece of split tile 0 (balanced: of the tile cut by the first range boundary)

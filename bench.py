@@ -558,9 +558,10 @@ COMPARE_GROUPS = {
                  [("automatic", dict()), ("one SM", dict(cta_pair=1)), ("two SMs, 256 wide", dict(cta_pair=2, bn=256)),
                   ("two SMs, 224 wide", dict(cta_pair=2, bn=224))]),
     # each die's pairs on their own block of tile columns, against all pairs on all tiles
-    "die_split": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096), ("bf16", 8192, 8192, 8192),
-                   ("bf16->bf16", 4096, 4096, 8192), ("s8", 4096, 4096, 8192), ("bf16", 4096, 4096, 4096),
-                   ("bf16", 8192, 8192, 4096)],
+    "die_split": ([("bf16", 4096, 4096, 4096), ("bf16->bf16", 4096, 4096, 4096), ("s8", 4096, 4096, 4096),
+                   ("tf32", 4096, 4096, 4096), ("bf16", 4096, 4096, 8192), ("bf16", 4096, 4096, 3072),
+                   ("bf16", 6144, 4096, 4096), ("bf16", 8192, 4096, 4096), ("bf16", 3072, 3072, 4096),
+                   ("bf16", 4096, 2048, 4096), ("bf16", 8192, 8192, 8192)],
                   [("automatic", dict()), ("die split off", dict(die_split=1)), ("die split on", dict(die_split=2))]),
     # tensor copies per k-block: two k-blocks per copy (two-SM 256-wide tiles), a CTA's B boxes
     # in one copy, or one copy per box and k-block

@@ -563,6 +563,10 @@ COMPARE_GROUPS = {
                    ("bf16", 6144, 4096, 4096), ("bf16", 8192, 4096, 4096), ("bf16", 3072, 3072, 4096),
                    ("bf16", 4096, 2048, 4096), ("bf16", 8192, 8192, 8192)],
                   [("automatic", dict()), ("die split off", dict(die_split=1)), ("die split on", dict(die_split=2))]),
+    # L2 eviction priorities on the two-SM kernel's loads (A evict-first, B evict-last)
+    "l2_hints": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096), ("bf16->bf16", 4096, 4096, 8192),
+                  ("s8", 4096, 4096, 8192), ("bf16", 4096, 4096, 4096)],
+                 [("automatic", dict()), ("hints off", dict(l2_hints=1)), ("hints on", dict(l2_hints=2))]),
     # tensor copies per k-block: two k-blocks per copy (two-SM 256-wide tiles), a CTA's B boxes
     # in one copy, or one copy per box and k-block
     "copies": ([("bf16", 4096, 4096, 4096), ("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096),
@@ -582,6 +586,8 @@ VARIANT_LAUNCHES = {
     "tf32": ([("tf32", 4096, 4096, 4096)], [("automatic", dict())]),
     "die_split": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096), ("bf16", 4096, 4096, 4096)],
                   [("die split off", dict(die_split=1)), ("die split on", dict(die_split=2))]),
+    "l2_hints": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096), ("bf16", 4096, 4096, 4096)],
+                 [("hints off", dict(l2_hints=1)), ("hints on", dict(l2_hints=2))]),
 }
 
 

@@ -234,6 +234,11 @@ typedef struct {
                                       as graph-captured calls on different streams do, must not
                                       run concurrently); whole tiles give the same result either
                                       way */
+    int l2_hints;                  /* two-SM kernel: 0 automatic (on with the die split for rows of
+                                      A of at least 16 KB), 1 off, 2 on. On: the loads of A carry
+                                      an L2 evict-first policy and those of B evict-last, so that
+                                      each die's L2 keeps the B columns its waves share. Same
+                                      result */
 } tcl_config_t;
 
 /* bf16 A, B (raw 16-bit patterns); fp32 accumulation; C fp32 (out = TCL_OUT_F32)
@@ -350,6 +355,7 @@ typedef struct {
     int kblocks_per_stage;          /* k-blocks that one tensor copy of each operand brings (1 or 2) */
     int die_split;                  /* 1: the tile columns in one block per die (tcl_config_t.die_split) */
     int die_tiles0;                 /* with die_split: tiles of the first die's block */
+    int l2_hints;                   /* 1: A's loads evict-first, B's evict-last (tcl_config_t.l2_hints) */
 } tcl_plan_t;
 
 /* Fills *plan (if not NULL) with the launch the library would make for this

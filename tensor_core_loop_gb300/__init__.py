@@ -74,6 +74,7 @@ class Config(ctypes.Structure):
         ("kblocks_per_stage", ctypes.c_int),
         ("b_copy", ctypes.c_int),
         ("die_split", ctypes.c_int),
+        ("l2_hints", ctypes.c_int),
     ]
 
 
@@ -100,6 +101,7 @@ class PlanInfo(ctypes.Structure):
         ("kblocks_per_stage", ctypes.c_int),
         ("die_split", ctypes.c_int),
         ("die_tiles0", ctypes.c_int),
+        ("l2_hints", ctypes.c_int),
     ]
 
 

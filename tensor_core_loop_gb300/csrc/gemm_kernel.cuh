@@ -147,6 +147,10 @@ struct GemmParams {
     // finish zeroes the counters (sched_ctr[2] counts finished pairs). Each sub-grid has
     // its own stream-K tail; its split tiles are numbered after those of the sub-grids
     // before it.
+    // 1 (two-SM kernel): A's loads carry an L2 evict-first policy and B's evict-last, so
+    // that each die's half of the L2 keeps the B columns its waves share while the rows
+    // of A stream through
+    int l2_hints;
     int die_split;
     int sub_n[2];            // pairs of each sub-grid (sub_n[0] + sub_n[1] = gridDim.x / 2)
     // Sub-grid h holds, in tile rows below sub_rs, the sub_a[h] tile columns from sub_s[h],

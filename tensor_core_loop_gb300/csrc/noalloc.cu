@@ -142,6 +142,7 @@ extern "C" TCL_API int gemm_s8_static(int M, int N, int K, const int8_t* A, int 
     p.b_3d = 0;
     p.kps2 = 0;
     p.die_split = 0;
+    p.l2_hints = 0;
 
     if (launch_s8_to_bf16({A, lda, reinterpret_cast<uint16_t*>(a2), lda2, M, K, 0},
                           {B, ldb, reinterpret_cast<uint16_t*>(b2), ldb2, K, N, 0}, sms, stream) != cudaSuccess) {

@@ -446,6 +446,50 @@ __device__ __forceinline__ void tma_load_3d_pair_elected(uint32_t dst, const CUt
         : "memory");
 }
 
+// L2 eviction-priority policies (for whole lines) that tensor loads can carry
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// The pair loads above with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                      int32_t c0, int32_t c1, uint64_t pol) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                      int32_t c0, int32_t c1, int32_t c2, uint64_t pol) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                      int32_t c0, int32_t c1, int32_t c2, int32_t c3, uint64_t pol) {
+    asm volatile(
+        "{\n\t.reg .pred el;\n\t.reg .b32 lane_sel;\n\t"
+        "elect.sync lane_sel|el, 0xffffffff;\n\t"
+        "@el cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+        : "memory");
+}
+
 // 4-D form of the same (coordinates innermost first).
 __device__ __forceinline__ void tma_load_4d_pair_elected(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
                                                          int32_t c0, int32_t c1, int32_t c2, int32_t c3) {

@@ -345,6 +345,16 @@ def test_planner_die_split(L):
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=8))["die_split"] == 0   # 4 pairs
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 3072, 3072, 4096, cfg)["die_split"] == 0   # 144 tiles: < 3 waves
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 6144, 4096, 4096, cfg)["die_split"] == 1
+    # L2 eviction hints (A evict-first, B evict-last) with the die split for deep tiles only
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, cfg)["l2_hints"] == 1
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 4096, cfg)["l2_hints"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, cfg)["l2_hints"] == 0
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 8192, 8192, 8192, cfg)["l2_hints"] == 0   # no die split
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, l2_hints=2))["l2_hints"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, tcl.Config(max_ctas=152, l2_hints=1))["l2_hints"] == 0
+    for bad in (tcl.Config(max_ctas=152, l2_hints=3), tcl.Config(max_ctas=152, l2_hints=2, cta_pair=1)):
+        with pytest.raises(tcl.TclError):
+            tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, bad)
     on = tcl.Config(max_ctas=152, die_split=2)
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 8192, 8192, 8192, on)
     assert (p["die_split"], p["die_tiles0"]) == (1, 512)

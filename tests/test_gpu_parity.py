@@ -570,6 +570,7 @@ def test_die_map_measured():
     ("tf32", 4096, 3072, 1024, dict()),
     ("s8", 4096, 4096, 2048, dict()),                   # exact integers
     ("bf16", 4096, 4096, 2048, dict(k_order=2)),        # alternating K order
+    ("bf16", 4096, 4096, 8192, dict()),                 # deep: L2 eviction hints on A and B too
 ])
 def test_die_split(oracle_mod, kind, M, N, K, extra):
     """Each die's pairs walk their own block of tile columns: within the oracle's bound on
@@ -593,6 +594,17 @@ def test_die_split(oracle_mod, kind, M, N, K, extra):
         got = run(a.to(DEV), b.to(DEV), cfg=cfg).numpy()
         for r in rows:
             assert_exact(got[r:r + 1], oracle_mod.gemm_s8(a.numpy(), b.numpy(), rows=(r, r + 1)), f"s8 row {r}")
+    assert tcl.last_device_error() == (0, 0)
+
+
+def test_l2_hints_change_nothing_in_the_result():
+    # the eviction priorities on A's and B's loads only steer the L2: the same bits
+    a, b = inputs.bf16_pair(4096, 4096, 8192, seed=41)
+    a, b = a.to(DEV), b.to(DEV)
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, None)["l2_hints"] == 1
+    x = run(a, b, cfg=tcl.Config(l2_hints=2), canary=False)
+    y = run(a, b, cfg=tcl.Config(l2_hints=1), canary=False)
+    assert torch.equal(x, y)
     assert tcl.last_device_error() == (0, 0)
 
 

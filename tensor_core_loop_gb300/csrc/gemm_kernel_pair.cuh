@@ -442,7 +442,6 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
         uint32_t it = 0;
         bool ok = true;
         const bool hints = p.l2_hints != 0;
-        const uint64_t pol_a = ptx::policy_evict_first(), pol_b = ptx::policy_evict_last();
         const int units = pair_units(p, S);
         for (int u = 0; ok && u < units; ++u) {
             const PairUnit U = pair_unit(p, S, u);
@@ -488,19 +487,20 @@ __global__ void __launch_bounds__(PairCfg<OK, BN, STAGES, SLOTS, IK>::THREADS, 1
                 if (kps2) {
                     const int k0 = two ? min(kc, load_kblock(p, u, kb + 1, U.kb_lo, U.kb_hi)) : kc;
                     if (hints) {
-                        ptx::tma_load_3d_pair_hint(sa, &tmA, fb, 0, row, k0, pol_a);
-                        ptx::tma_load_4d_pair_hint(sb, &tmB, fb, 0, 0, col / C::B_BOX_N, k0, pol_b);
+                        ptx::tma_load_3d_pair_hint(sa, &tmA, fb, 0, row, k0, ptx::policy_evict_first());
+                        ptx::tma_load_4d_pair_hint(sb, &tmB, fb, 0, 0, col / C::B_BOX_N, k0, ptx::policy_evict_last());
                     } else {
                         ptx::tma_load_3d_pair_elected(sa, &tmA, fb, 0, row, k0);
                         ptx::tma_load_4d_pair_elected(sb, &tmB, fb, 0, 0, col / C::B_BOX_N, k0);
                     }
                 } else {
                     if (hints)
-                        ptx::tma_load_2d_pair_hint(sa, &tmA, fb, kc * C::BK, row, pol_a);
+                        ptx::tma_load_2d_pair_hint(sa, &tmA, fb, kc * C::BK, row, ptx::policy_evict_first());
                     else
                         ptx::tma_load_2d_pair_elected(sa, &tmA, fb, kc * C::BK, row);
                     if (p.b_3d && hints) {
-                        ptx::tma_load_3d_pair_hint(sb, &tmB, fb, 0, kc * C::BK, col / C::B_BOX_N, pol_b);
+                        ptx::tma_load_3d_pair_hint(sb, &tmB, fb, 0, kc * C::BK, col / C::B_BOX_N,
+                                                   ptx::policy_evict_last());
                     } else if (p.b_3d) {   // this CTA's B_BOXES boxes in one copy (boxes B_BOX_BYTES apart, as below)
                         ptx::tma_load_3d_pair_elected(sb, &tmB, fb, 0, kc * C::BK, col / C::B_BOX_N);
                     } else {

@@ -109,7 +109,8 @@ def measured_peaks():
 # helpers and PTX wrappers, its launch): a recorded ncu traffic figure stays
 # valid while these are unchanged and the planner still picks the same launch.
 KERNEL_SOURCES = ("ptx.cuh", "gemm_kernel.cuh", "gemm_kernel_pair.cuh", "k_pair.cu")
-PLAN_KEYS = ("bn", "stages", "cta_pair", "splits", "sk_tiles", "sk_pieces", "kblocks_per_stage", "die_split")
+PLAN_KEYS = ("bn", "stages", "cta_pair", "splits", "sk_tiles", "sk_pieces", "kblocks_per_stage", "die_split",
+             "l2_hints")
 
 
 def _code_only(text):

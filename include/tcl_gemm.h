@@ -25,7 +25,11 @@
  *   work may still use it) and a small array of stream-K progress flags
  *   (8 KB, allocated and zeroed at the stream's first call). Calls on
  *   different streams therefore never share scratch or flags and may overlap
- *   on the GPU. The legacy and per-thread default streams share one set; a
+ *   on the GPU. (The pieces of a stream-K tile wait for one another, and the
+ *   persistent grid is sized so that all of its CTAs fit on the GPU at once;
+ *   a launch that another kernel keeps partly off the SMs for longer than
+ *   timeout_ns reports device code 5 instead of waiting on.) The legacy and
+ *   per-thread default streams share one set; a
  *   call captured into a graph on a stream that has not run a call outside
  *   capture before takes that default set too (and so do the graph's
  *   replays), so such a replay must not overlap work on the default streams.

@@ -396,6 +396,11 @@ constexpr int kMinKbForSk = 32;
 constexpr int kMaxDieSplitCols = 16;   // automatic die split up to this many tile columns (two blocks)
 constexpr int kMinDieSplitPairs = 32;  // and only on a whole GPU's pairs
 constexpr int kMinDieSplitWaves = 3;   // and at least this many tiles per pair
+// and at least this many k-blocks (128-byte rows of K) per tile: measured on GB300 (CUDA
+// graphs, round robin) at 4096² bf16 → fp32, the split against the whole grid is 3.3 %
+// slower at K = 1536 (42.02 against 40.69 µs), level at 2048, 0.6 % faster at 2560 and
+// 2.4 % at 3072; at K ≤ 1024 (two SMs per tile asked for) 6 % slower
+constexpr int kMinDieSplitKb = 32;
 constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed when pieces are all a pair does
 
 // Stream-K split of the last (partial) wave of pair tiles: with `tiles` tiles
@@ -834,7 +839,8 @@ int make_plan(InKind ik, OutKind ok, int M, int N, int K, const tcl_config_t* cf
         // (a requested raster group keeps the whole grid unless the split is asked for too:
         // the blocks are walked row by row)
         const bool ds_auto = want_ds == 0 && pl->tiles_n <= kMaxDieSplitCols &&
-                             pl->num_tiles >= kMinDieSplitWaves * pairs_all && !(cfg && cfg->group_m > 0);
+                             pl->num_tiles >= kMinDieSplitWaves * pairs_all && pl->num_kb >= kMinDieSplitKb &&
+                             !(cfg && cfg->group_m > 0);
         if (ds_ok && (want_ds == 2 || ds_auto)) {
             const int n0 = die_pairs[0], n1 = die_pairs[1];
             const long long all = static_cast<long long>(pl->tiles_m) * pl->tiles_n;

@@ -345,6 +345,11 @@ def test_planner_die_split(L):
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=8))["die_split"] == 0   # 4 pairs
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 3072, 3072, 4096, cfg)["die_split"] == 0   # 144 tiles: < 3 waves
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 6144, 4096, 4096, cfg)["die_split"] == 1
+    # and from 32 k-blocks (4 KB of K per operand row) on
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2048, cfg)["die_split"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1536, cfg)["die_split"] == 0
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 1024, cfg)["die_split"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1536, tcl.Config(max_ctas=152, die_split=2))["die_split"] == 1
     # L2 eviction hints (A evict-first, B evict-last) with the die split for deep tiles only
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, cfg)["l2_hints"] == 1
     assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 4096, cfg)["l2_hints"] == 1

@@ -564,6 +564,11 @@ COMPARE_GROUPS = {
                    ("bf16", 6144, 4096, 4096), ("bf16", 8192, 4096, 4096), ("bf16", 3072, 3072, 4096),
                    ("bf16", 4096, 2048, 4096), ("bf16", 8192, 8192, 8192)],
                   [("automatic", dict()), ("die split off", dict(die_split=1)), ("die split on", dict(die_split=2))]),
+    # the die split against K depth (two SMs per tile asked for, so that K ≤ 1024 is covered too)
+    "die_split_depth": ([("bf16", 4096, 4096, k) for k in (256, 512, 1536, 2048, 2560)] +
+                        [("bf16", 6144, 4096, 2048), ("bf16", 8192, 4096, 2048)],
+                        [("two SMs, die split off", dict(cta_pair=2, bn=256, die_split=1)),
+                         ("two SMs, die split on", dict(cta_pair=2, bn=256, die_split=2))]),
     # L2 eviction priorities on the two-SM kernel's loads (A evict-first, B evict-last)
     "l2_hints": ([("bf16", 4096, 4096, 8192), ("tf32", 4096, 4096, 4096), ("bf16->bf16", 4096, 4096, 8192),
                   ("s8", 4096, 4096, 8192), ("bf16", 4096, 4096, 4096)],

@@ -565,8 +565,9 @@ COMPARE_GROUPS = {
                    ("bf16", 4096, 2048, 4096), ("bf16", 8192, 8192, 8192)],
                   [("automatic", dict()), ("die split off", dict(die_split=1)), ("die split on", dict(die_split=2))]),
     # the die split against K depth (two SMs per tile asked for, so that K ≤ 1024 is covered too)
-    "die_split_depth": ([("bf16", 4096, 4096, k) for k in (256, 512, 1536, 2048, 2560)] +
-                        [("bf16", 6144, 4096, 2048), ("bf16", 8192, 4096, 2048)],
+    "die_split_depth": ([("bf16", 4096, 4096, k) for k in (256, 512, 1536, 2048, 2560, 3072)] +
+                        [("bf16", 6144, 4096, 2048), ("bf16", 8192, 4096, 2048)] +
+                        [("tf32", 4096, 4096, k) for k in (768, 1024, 2048)] + [("tf32", 6144, 4096, 1024)],
                         [("two SMs, die split off", dict(cta_pair=2, bn=256, die_split=1)),
                          ("two SMs, die split on", dict(cta_pair=2, bn=256, die_split=2))]),
     # L2 eviction priorities on the two-SM kernel's loads (A evict-first, B evict-last)

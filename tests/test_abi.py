@@ -196,11 +196,11 @@ def test_plan_without_device(L):
     for in_kind, k in ((tcl.IN_BF16, 8192), (tcl.IN_TF32, 4096)):
         p = tcl.plan(in_kind, tcl.OUT_F32, 4096, 4096, k, cfg)
         assert (p["cta_pair"], p["group_m"], p["k_serpentine"]) == (2, 1, 1)
-    for k in (2048, 4096):   # (the whole grid: automatically these run the die split, row by row)
+    for k in (2048, 3072, 4096):   # (the whole grid: automatically, from 48 k-blocks on, the die split, row by row)
         p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, tcl.Config(max_ctas=152, die_split=1))
         assert (p["group_m"], p["k_serpentine"]) == (8, 0)
         p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, k, cfg)
-        assert (p["die_split"], p["group_m"], p["k_serpentine"]) == (1, 1, 0)
+        assert (p["die_split"], p["group_m"], p["k_serpentine"]) == ((1, 1, 0) if k >= 3072 else (0, 8, 0))
     p = tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=152, group_m=4, k_order=1))
     assert (p["group_m"], p["k_serpentine"]) == (4, 0)
     # int8 on 256-wide pair tiles widens inside the kernel on request (s8_path 2) only
@@ -345,10 +345,12 @@ def test_planner_die_split(L):
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 4096, tcl.Config(max_ctas=8))["die_split"] == 0   # 4 pairs
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 3072, 3072, 4096, cfg)["die_split"] == 0   # 144 tiles: < 3 waves
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 6144, 4096, 4096, cfg)["die_split"] == 1
-    # and from 32 k-blocks (4 KB of K per operand row) on
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2048, cfg)["die_split"] == 1
-    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1536, cfg)["die_split"] == 0
-    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 1024, cfg)["die_split"] == 1
+    # and from 48 k-blocks (6 KB of K per operand row) on
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 3072, cfg)["die_split"] == 1
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2560, cfg)["die_split"] == 0
+    assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 2048, cfg)["die_split"] == 0
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 2048, cfg)["die_split"] == 1
+    assert tcl.plan(tcl.IN_TF32, tcl.OUT_F32, 4096, 4096, 1024, cfg)["die_split"] == 0
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 1536, tcl.Config(max_ctas=152, die_split=2))["die_split"] == 1
     # L2 eviction hints (A evict-first, B evict-last) with the die split for deep tiles only
     assert tcl.plan(tcl.IN_BF16, tcl.OUT_F32, 4096, 4096, 8192, cfg)["l2_hints"] == 1

@@ -397,9 +397,9 @@ constexpr int kMaxDieSplitCols = 16;   // automatic die split up to this many ti
 constexpr int kMinDieSplitPairs = 32;  // and only on a whole GPU's pairs
 constexpr int kMinDieSplitWaves = 3;   // and at least this many tiles per pair
 // and at least this many k-blocks (128-byte rows of K) per tile: measured on GB300 (CUDA
-// graphs, round robin), the split against the whole grid is 2–5 % slower below 4 KB of K
-// per operand row (bf16 K ≤ 1536, TF32 K = 768), 0.3 % slower on average over eight
-// shapes at 4 KB (bf16 K = 2048, TF32 K = 1024), 0.4 % faster at 5 KB and 1.4–2.4 % at
+// graphs, round robin), the split against the whole grid is 2.6–5.1 % slower below 4 KB
+// of K per operand row (bf16 K ≤ 1536, TF32 K = 768), about level at 4 KB (bf16 K = 2048,
+// TF32 K = 1024: −1.0 to +1.3 % over five shapes), 0.4 % faster at 5 KB and 1.7–2.3 % at
 // 6–8 KB (bf16 K = 3072, TF32 K = 2048)
 constexpr int kMinDieSplitKb = 48;
 constexpr long long kSkLinkCycles = 4096;   // one piece's epilogue, exposed when pieces are all a pair does

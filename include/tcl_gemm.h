@@ -223,8 +223,9 @@ typedef struct {
                                       several boxes: 128- and 256-wide one-SM tiles, 256-wide
                                       two-SM tiles); 1 one copy per box. Same result */
     int die_split;                 /* two-SM kernel: 0 automatic (on for grids of at most 16 tile
-                                      columns and at least 3 tiles per pair of SMs, when the die
-                                      of every pair of SMs is known),
+                                      columns, at least 3 tiles per pair of SMs and at least 48
+                                      k-blocks, 6 KB of K per operand row, when the die of every
+                                      pair of SMs is known and no raster group is asked for),
                                       1 off, 2 on where possible (TCL_ERR_CONFIG otherwise). On:
                                       the tiles are cut into one block of columns per die of the
                                       GPU (whole columns and part of one, in proportion to the

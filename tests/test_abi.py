@@ -31,6 +31,31 @@ def test_header_declares_expected_api():
     assert set(syms) == set(tcl.EXPORTED_SYMBOLS), syms
 
 
+@pytest.mark.parametrize("struct,mirror", [("tcl_config_t", tcl.Config), ("tcl_plan_t", tcl.PlanInfo)])
+def test_struct_mirrors_match_the_header(struct, mirror, tmp_path):
+    """The ctypes mirrors have the C structs' size and every field at the C offset (a C
+    program compiled against the header prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = next((d for d in ("/usr/local/cuda/include", os.path.join(os.environ.get("CUDA_HOME", ""), "include"))
+                     if os.path.exists(os.path.join(d, "cuda_runtime_api.h"))), None)
+    if not cc or not cuda_inc:
+        pytest.skip("no C compiler or CUDA headers")
+    names = [n for n, _ in mirror._fields_]
+    body = "".join(f'printf("%zu\\n", offsetof({struct}, {n}));' for n in names)
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "tcl_gemm.h"\n'
+                   f'int main(void) {{ printf("%zu\\n", sizeof({struct})); {body} return 0; }}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert len(got) == len(names) + 1
+    assert got[0] == ctypes.sizeof(mirror), (struct, got[0], ctypes.sizeof(mirror))
+    for n, off in zip(names, got[1:]):
+        assert getattr(mirror, n).offset == off, (struct, n, off, getattr(mirror, n).offset)
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in header_symbols():
         assert hasattr(L, name), name

@@ -1004,17 +1004,23 @@ def main():
                       torch.empty((M, N), dtype=out_dtype, device=dev)) for i in range(nset_)]
             fn = (lambda x, y, z: tcl.gemm_into(x, y, z))
             ms_rot = time_rotating(fn, sets_, 200, 20, stream, torch)
+            ms_graph = time_graph_rotating(fn, sets_, max(40, 2 * nset_), 5, torch)
             x, y, z = sets_[0]
             ms_one = time_flushed(lambda: fn(x, y, z), (), 20, stream, torch, flush)
-            return ms_rot, ms_one, sets_[0]
-        ms8, ms8_one, _ = whole_call(inputs.s8_pair, torch.int32)
+            return ms_rot, ms_graph, ms_one, sets_[0]
+        ms8, ms8_graph, ms8_one, _ = whole_call(inputs.s8_pair, torch.int32)
         extra["int8_tops_4096"] = round(FLOPS / (ms8 * 1e-3) / 1e12, 1)
+        extra["int8_tops_4096_graph"] = round(FLOPS / (ms8_graph * 1e-3) / 1e12, 1)
         extra["int8_tops_4096_single_flushed"] = round(FLOPS / (ms8_one * 1e-3) / 1e12, 1)
-        mst, mst_one, (at, bt, ct) = whole_call(inputs.tf32_pair, torch.float32)
+        mst, mst_graph, mst_one, (at, bt, ct) = whole_call(inputs.tf32_pair, torch.float32)
         extra["tf32_tflops_4096"] = round(FLOPS / (mst * 1e-3) / 1e12, 1)
+        extra["tf32_tflops_4096_graph"] = round(FLOPS / (mst_graph * 1e-3) / 1e12, 1)
         extra["tf32_tflops_4096_single_flushed"] = round(FLOPS / (mst_one * 1e-3) / 1e12, 1)
         extra["int8_tf32_timing"] = ("*_4096: back-to-back whole calls over rotating input sets (footprint "
-                                     "> 2x L2), as the headline; *_single_flushed: one call after an L2 flush")
+                                     "> 2x L2), issued one by one from Python, as the headline; *_graph: the "
+                                     "same calls captured in a CUDA graph (the host's per-call cost removed; "
+                                     "int8: widening pass and GEMM per call); *_single_flushed: one call "
+                                     "after an L2 flush")
         extra["sgemm_simt_4096"] = measure_simt(tcl, torch, dev, stream, at, bt, ct, flush)
         del at, bt, ct
         del flush
